@@ -1,0 +1,274 @@
+"""Benchmark of the Dory looped nGPT token forward on GB300.
+
+Default workload: the 2B-shaped bf16 model (hidden 2048, 16 q / 4 kv heads of 128, ffn
+5632, vocab 32000, 2/4/2 attention+MLP pairs, loops 4, sliding window 512, last_loop f32
+KV): a 4096-token seeded prompt in 64-row chunks, then batch-1 decode steps with
+teacher-forced seeded ids. One step = one decode token through the whole forward.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line. Under torchrun each rank runs its own replica (batch-1 decode does
+not shard), ranks meet at a barrier around the timed region, and the slowest rank's time
+counts. `--impl reference` times the CPU oracle on the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "decode tokens/s at batch 1/64 (loops=4) + fraction of HBM roofline; prefill tok/s"
+SEED = 1236  # seed = 1234 + config index (the 2B decode workload is the second config)
+PROMPT = 4096
+DECODE = 256
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        j = json.load(open(p))
+        return j["hbm_gbs"], j["bf16_tflops"], "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+class Clocks:
+    """nvidia-smi samples of the SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev: int):
+        self.dev = dev
+        self.p = None
+
+    def __enter__(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.p = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.p:
+            self.p.terminate()
+            try:
+                self.out, _ = self.p.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.p.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = max(mx, float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx or None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def workload_config():
+    return synth.dory2b(max_batch=1, max_seqs=1, max_context=PROMPT + DECODE + 64)
+
+
+def bench_ours(args, rank, world):
+    import torch
+
+    from looped_normalized_gpt_gb300 import Dory, build
+
+    dev = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(dev)
+    build()
+    cfg = workload_config()
+    t0 = time.time()
+    w = synth.weights(cfg, SEED)
+    t_gen = time.time() - t0
+    stream = torch.cuda.current_stream()
+    g = Dory(cfg, w, stream=stream.cuda_stream)
+    ids = synth.token_ids(SEED, 0, PROMPT + DECODE, cfg.vocab)
+    prompt, dec = ids[:PROMPT], ids[PROMPT:]
+    for a in range(0, PROMPT, 64):
+        g.prefill_chunk(0, prompt[a:a + 64], a, cfg.loops, "last" if a + 64 >= PROMPT else "none")
+    torch.cuda.synchronize()
+    dec_dev = torch.from_numpy(dec.astype(np.int32)).to(f"cuda:{dev}")
+    K, W = args.steps, args.warmup
+    assert W + K <= DECODE, "warmup + steps must fit the 256 decode tokens"
+    for i in range(W):
+        g.decode_step(dec_dev[i:i + 1], [0], cfg.loops)
+    st = g.stats()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with Clocks(dev) as clk:
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(W, W + K):
+            g.decode_step(dec_dev[i:i + 1], [0], cfg.loops)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms], device=f"cuda:{dev}")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        torch.distributed.barrier()
+        ms = float(t.item())
+    value = world * K / (ms / 1e3)
+
+    # end to end: host ids from pinned memory in, logits back to host, every step
+    g2_ids = torch.from_numpy(dec.astype(np.int32)).pin_memory()
+    host_logits = torch.empty(cfg.vocab, dtype=torch.float32).pin_memory()
+    g.reset(0)
+    for a in range(0, PROMPT, 64):
+        g.prefill_chunk(0, prompt[a:a + 64], a, cfg.loops, "last" if a + 64 >= PROMPT else "none")
+    for i in range(W):
+        g.decode_step(g2_ids[i:i + 1], [0], cfg.loops)
+        g.logits(0, out=host_logits)
+    torch.cuda.synchronize()
+    t_a = time.perf_counter()
+    for i in range(W, W + K):
+        g.decode_step(g2_ids[i:i + 1], [0], cfg.loops)
+        g.logits(0, out=host_logits)
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t_a
+    e2e = world * K / e2e_s
+
+    hbm, tf, src = peaks()
+    bytes_step = st["weight_bytes"] + st["kv_read_bytes"] + st["kv_write_bytes"]
+    achieved = bytes_step / (ms / 1e3 / K) / 1e9
+    clocks = clk.summary()
+    out = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": round(ms / K, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16 weights, f32 activations and KV",
+        "data": "synthetic: seeded unit-row random weights, seeded uniform token ids",
+        "config": {"workload": "Dory-2B-shape batch-1 decode after a 4096-token prompt, loops 4, "
+                               "sliding window 512, last_loop f32 KV",
+                   "batch": 1, "loops": 4, "prompt": PROMPT, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (2.1 GB of weights streamed per token)"},
+        "e2e": {"value": round(e2e, 2), "unit": "tokens/s", "h2d_bytes_per_step": 4 + 16,
+                "d2h_bytes_per_step": cfg.vocab * 4},
+        "gpu_launches": int(st["launches"]) * K,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "traffic": None,
+                     "note": f"whole step: algorithmic bytes per token {bytes_step} / step time; peak {src}"},
+        "clocks": clocks,
+        "weights_gen_s": round(t_gen, 1),
+    }
+    return out, g, cfg, w
+
+
+def cpu_baseline(cfg, w, steps: int = 6):
+    """The oracle as it stands, on this host's cores: a 64-token prompt, then `steps` timed
+    decode tokens of the same model."""
+    from oracle import dory_oracle as O
+
+    o = O.DoryOracle(cfg, w)
+    st = O.SeqState()
+    ids = synth.token_ids(SEED, 0, 64 + steps + 1, cfg.vocab)
+    o.forward_chunk(st, ids[:64], 0, cfg.loops, "last")
+    o.forward_chunk(st, ids[64:65], 64, cfg.loops, "last")
+    t = time.perf_counter()
+    for i in ids[65:65 + steps]:
+        o.forward_chunk(st, [int(i)], st.pos, cfg.loops, "last")
+    s = time.perf_counter() - t
+    return {"value": round(steps / s, 3), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{steps} batch-1 decode tokens after a 64-token prompt, same model, float64 NumPy"}
+
+
+def bench_reference(args, rank, world):
+    if rank != 0:
+        return None
+    cfg = workload_config()
+    w = synth.weights(cfg, SEED)
+    from oracle import dory_oracle as O
+
+    o = O.DoryOracle(cfg, w)
+    st = O.SeqState()
+    ids = synth.token_ids(SEED, 0, 64 + args.warmup + args.steps, cfg.vocab)
+    o.forward_chunk(st, ids[:64], 0, cfg.loops, "last")
+    for i in ids[64:64 + args.warmup]:
+        o.forward_chunk(st, [int(i)], st.pos, cfg.loops, "last")
+    t = time.perf_counter()
+    for i in ids[64 + args.warmup:]:
+        o.forward_chunk(st, [int(i)], st.pos, cfg.loops, "last")
+    s = time.perf_counter() - t
+    v = args.steps / s
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(v, 3), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * s / args.steps, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic: seeded unit-row random weights, seeded uniform token ids",
+        "config": {"workload": "Dory-2B-shape batch-1 decode after a 64-token prompt (bounded CPU sample), loops 4, "
+                               "sliding window 512, last_loop f32 KV", "batch": 1, "loops": 4},
+        "cpu_baseline": {"value": round(v, 3), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": f"{args.steps} decode tokens after a 64-token prompt"},
+        "e2e": {"value": round(v, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=64)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        out = bench_reference(args, rank, world)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return
+    if world > 1:
+        import torch
+
+        torch.distributed.init_process_group("nccl")
+    out, g, cfg, w = bench_ours(args, rank, world)
+    g.close()
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            out["cpu_baseline"] = cpu_baseline(cfg, w)
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch
+
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,737 @@
+// The C ABI of include/dory.h: the handle, weight residency, KV rings and the launch
+// sequence of one forward step (dory.rs fn forward_host / fn stack for one chunk, or
+// one decode row per sequence).
+#include <algorithm>
+#include <climits>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/dory.h"
+#include "kernels.h"
+
+using namespace dory;
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return code;
+}
+
+#define CK(call)                                                                          \
+  do {                                                                                    \
+    cudaError_t e_ = (call);                                                              \
+    if (e_ != cudaSuccess) return fail(DORY_ECUDA, "%s: %s", #call, cudaGetErrorString(e_)); \
+  } while (0)
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+constexpr int KEYS_PER_SPLIT = 128;
+constexpr int RING_EXTRA = 64 + 448;  // a chunk and the rewind slack (gpu_metal/dory.rs fn run)
+
+struct LayerDev {
+  bool attn = false, sliding = false, rec = false, out = false;
+  int ordinal = -1;
+  void *wqkvg = nullptr, *wo = nullptr, *wgu = nullptr, *wdown = nullptr;
+  float *sq = nullptr, *sg = nullptr, *alpha = nullptr, *msg = nullptr, *msu = nullptr;
+};
+
+struct OrdInfo {
+  bool sliding = true, rec = false;
+  int cap = 0, window = 0, slots = 1;
+  size_t off = 0;  // slot 0 within a sequence block
+  SlotLayout L;
+};
+
+}  // namespace
+
+struct dory_handle {
+  dory_config cfg{};
+  std::string pattern;
+  Dims dims{};
+  int wdtype = 0;
+  size_t esz = 4;
+  cudaStream_t stream = nullptr;
+  int Tmax = 64;
+
+  char *wmem = nullptr;
+  size_t wbytes = 0;
+  void *embed = nullptr, *head = nullptr;
+  float *logit_scale = nullptr;
+  std::vector<LayerDev> layers;
+  std::vector<OrdInfo> ords;
+
+  char *kvmem = nullptr;
+  size_t seq_stride = 0, kv_bytes = 0;
+  int max_splits = 1;
+
+  float *h = nullptr, *input = nullptr, *state = nullptr, *qkvg = nullptr, *z = nullptr, *out = nullptr,
+        *mlp = nullptr, *logits = nullptr, *rope = nullptr, *part = nullptr, *kst = nullptr, *vst = nullptr;
+  int32_t *d_ids = nullptr, *d_row_seq = nullptr, *d_row_off = nullptr, *d_seq_pos = nullptr,
+          *d_adv_seq = nullptr, *d_adv_cnt = nullptr, *d_zero = nullptr;
+  char *act = nullptr;
+
+  std::vector<int> seq_pos;     // host mirror of d_seq_pos
+  std::vector<int> appended;    // rows appended per (seq, ordinal, slot)
+  std::vector<int> slot_index;  // first flat slot index of each ordinal
+  int n_flat_slots = 0;
+  int logits_rows = 0, last_rows = 0;
+  dory_stats st{};
+
+  Ring ring(int ordinal, int slot) const {
+    const OrdInfo &o = ords[ordinal];
+    Ring r;
+    r.base = kvmem;
+    r.seq_stride = seq_stride;
+    r.off = o.off + (size_t)slot * o.L.bytes;
+    r.L = o.L;
+    r.cap = o.cap;
+    r.window = o.window;
+    r.q8 = cfg.kv_quant == DORY_KV_Q8_2F;
+    return r;
+  }
+  int &app(int seq, int ordinal, int slot) {
+    return appended[(size_t)seq * n_flat_slots + slot_index[ordinal] + slot];
+  }
+};
+
+namespace {
+
+int validate(const dory_config *c, std::string &pat) {
+  if (!c) return fail(DORY_EINVAL, "config is NULL");
+  if (c->hidden <= 0 || c->ffn <= 0 || c->vocab <= 0 || c->nh <= 0 || c->nk <= 0 || c->hd <= 0)
+    return fail(DORY_EINVAL, "dimensions must be positive");
+  if (c->nh % c->nk != 0) return fail(DORY_EINVAL, "nh (%d) must be a multiple of nk (%d)", c->nh, c->nk);
+  const int rep = c->nh / c->nk;
+  if (rep != 1 && rep != 2 && rep != 4 && rep != 8) return fail(DORY_EINVAL, "nh/nk must be 1, 2, 4 or 8");
+  if (c->hd != 32 && c->hd != 64 && c->hd != 128) return fail(DORY_EINVAL, "hd must be 32, 64 or 128");
+  if (c->hidden % 32 || c->ffn % 32) return fail(DORY_EINVAL, "hidden and ffn must be multiples of 32");
+  if (c->hidden > 8192) return fail(DORY_EINVAL, "hidden above 8192");
+  if (c->max_loops < 1 || c->max_loops > DORY_MAX_LOOPS)
+    return fail(DORY_EINVAL, "max_loops=%d: want 1..%d", c->max_loops, DORY_MAX_LOOPS);
+  if (c->window < 1) return fail(DORY_EINVAL, "window must be positive");
+  if (c->full_window < 0) return fail(DORY_EINVAL, "full_window must be >= 0");
+  if (c->kv_mode != DORY_KV_PER_LOOP && c->kv_mode != DORY_KV_LAST_LOOP) return fail(DORY_EINVAL, "kv_mode");
+  if (c->kv_quant != DORY_KV_F32 && c->kv_quant != DORY_KV_Q8_2F) return fail(DORY_EINVAL, "kv_quant");
+  if (c->weight_dtype != DORY_W_F32 && c->weight_dtype != DORY_W_BF16) return fail(DORY_EINVAL, "weight_dtype");
+  if (c->max_batch < 1 || c->max_batch > DORY_MAX_BATCH) return fail(DORY_EINVAL, "max_batch 1..%d", DORY_MAX_BATCH);
+  if (c->max_seqs < 1) return fail(DORY_EINVAL, "max_seqs must be positive");
+  if (c->prompt_loops < 0) return fail(DORY_EINVAL, "prompt_loops must be >= 0");
+  if (c->n_in < 0 || c->n_rec < 0 || c->n_out < 0) return fail(DORY_EINVAL, "block sizes must be >= 0");
+  if (!c->layer_pattern) return fail(DORY_EINVAL, "layer_pattern is NULL");
+  pat = c->layer_pattern;
+  if ((int)pat.size() != c->n_in + c->n_rec + c->n_out)
+    return fail(DORY_EINVAL, "layer_pattern has %zu layers, blocks give %d", pat.size(), c->n_in + c->n_rec + c->n_out);
+  for (char ch : pat)
+    if (ch != 'S' && ch != '*' && ch != '-') return fail(DORY_EINVAL, "layer_pattern char '%c'", ch);
+  bool has_full = false;
+  for (char ch : pat) has_full |= ch == '*';
+  if (has_full && c->full_window == 0 && c->max_context < 1) return fail(DORY_EINVAL, "max_context must be positive");
+  return DORY_OK;
+}
+
+int copy_in(void *dst, const void *src, size_t bytes, const char *what) {
+  if (!src) return fail(DORY_EINVAL, "weight %s is NULL", what);
+  CK(cudaMemcpy(dst, src, bytes, cudaMemcpyDefault));
+  return DORY_OK;
+}
+
+void free_all(dory_t *d) {
+  if (d->wmem) cudaFree(d->wmem);
+  if (d->kvmem) cudaFree(d->kvmem);
+  if (d->act) cudaFree(d->act);
+  d->wmem = d->kvmem = d->act = nullptr;
+}
+
+int reset_seq(dory_t *d, int seq) {
+  char *blk = d->kvmem + (size_t)seq * d->seq_stride;
+  CK(cudaMemsetAsync(blk, 0, d->seq_stride, d->stream));
+  for (size_t o = 0; o < d->ords.size(); o++)
+    for (int s = 0; s < d->ords[o].slots; s++) {
+      Ring r = d->ring((int)o, s);
+      CK(cudaMemsetAsync(blk + r.off + r.L.tags, 0xFF, (size_t)r.cap * 4, d->stream));
+    }
+  CK(cudaMemsetAsync(d->d_seq_pos + seq, 0, 4, d->stream));
+  d->seq_pos[seq] = 0;
+  for (int i = 0; i < d->n_flat_slots; i++) d->appended[(size_t)seq * d->n_flat_slots + i] = 0;
+  return DORY_OK;
+}
+
+Rows make_rows(dory_t *d, int n) {
+  Rows r;
+  r.seq = d->d_row_seq;
+  r.off = d->d_row_off;
+  r.seq_pos = d->d_seq_pos;
+  r.n = n;
+  return r;
+}
+
+// One forward over the step's rows (already uploaded): row r is sequence hseq[r] at
+// position seq_pos[hseq[r]] + hoff[r]. `loops` passes; `head_rows` rows of logits taken
+// from the last head_rows rows (0: none).
+int run_step(dory_t *d, int T, const std::vector<int> &hseq, const std::vector<int> &hoff, int loops,
+             int head_from, int head_rows) {
+  const dory_config &c = d->cfg;
+  const Dims dm = d->dims;
+  cudaStream_t s = d->stream;
+  Rows rows = make_rows(d, T);
+  d->st.weight_bytes = d->st.kv_read_bytes = d->st.kv_write_bytes = 0;
+  d->st.launches = d->st.gemm_launches = 0;
+  const int q_size = dm.nh * dm.hd, kv_size = dm.nk * dm.hd;
+  const int ldq = 2 * q_size + 2 * kv_size;
+  long pmax = 0;
+  for (int r = 0; r < T; r++) pmax = std::max(pmax, (long)d->seq_pos[hseq[r]] + hoff[r]);
+  const bool q8 = c.kv_quant == DORY_KV_Q8_2F;
+  const size_t kv_row_bytes = q8 ? (size_t)dm.hd * 2 + (dm.hd / 32) * 4 + 4 : (size_t)dm.hd * 8;
+
+  CK(launch_embed_rope(d->d_ids, d->embed, d->wdtype, dm, rows, c.rope_theta_sliding, c.rope_theta_full, d->h,
+                       d->rope, s));
+  d->st.launches++;
+
+  auto gemm = [&](const void *W, int N, int K, const float *X, int ldx, float *Y, int ldy, EpiArgs ep) -> int {
+    CK(launch_gemm(W, d->wdtype, N, K, X, ldx, T, Y, ldy, ep, s));
+    d->st.launches++;
+    d->st.gemm_launches++;
+    d->st.weight_bytes += (uint64_t)N * K * d->esz * (ep.mode == EPI_SILU ? 2 : 1);
+    return DORY_OK;
+  };
+
+  auto layer = [&](int li, int loop_i, int mix) -> int {
+    const LayerDev &L = d->layers[li];
+    int rc;
+    if (L.attn) {
+      const int sl = (c.kv_mode == DORY_KV_PER_LOOP && L.rec) ? loop_i : 0;
+      const bool rewrite = c.kv_mode == DORY_KV_LAST_LOOP && (L.rec || L.out) && loop_i > 0;
+      Ring ring = d->ring(L.ordinal, sl);
+      EpiArgs ep{EPI_STORE, nullptr, nullptr, 0};
+      if ((rc = gemm(L.wqkvg, ldq, dm.hidden, d->h, dm.hidden, d->qkvg, ldq, ep))) return rc;
+      CK(launch_prep(d->qkvg, ldq, dm, rows, d->rope, L.sliding ? 0 : 1, L.sq, ring, d->kst, d->vst, s));
+      d->st.launches++;
+      if (q8) {
+        CK(launch_q8_append(d->kst, d->vst, kv_size, dm, rows, ring, rewrite ? 1 : 0, s));
+        d->st.launches++;
+      }
+      long keys = ring.window == INT_MAX ? pmax + 1 : std::min<long>(ring.window, pmax + 1);
+      const int splits = (int)((keys + KEYS_PER_SPLIT - 1) / KEYS_PER_SPLIT);
+      if (splits > d->max_splits) return fail(DORY_ERANGE, "attention needs %d splits (max %d)", splits, d->max_splits);
+      CK(launch_attention(d->qkvg, ldq, dm, rows, ring, splits, KEYS_PER_SPLIT, d->part, L.sg, d->z, s));
+      d->st.launches += 2;
+      for (int r = 0; r < T; r++) {
+        const long p = (long)d->seq_pos[hseq[r]] + hoff[r];
+        const long kr = ring.window == INT_MAX ? p + 1 : std::min<long>(ring.window, p + 1);
+        d->st.kv_read_bytes += (uint64_t)kr * dm.nk * kv_row_bytes;
+      }
+      d->st.kv_write_bytes += (uint64_t)T * dm.nk * kv_row_bytes;
+      if (!rewrite)
+        for (int r = 0; r < T; r++) d->app(hseq[r], L.ordinal, sl)++;
+      CK(launch_rownorm(d->z, T, q_size, q_size, s));
+      d->st.launches++;
+      if ((rc = gemm(L.wo, dm.hidden, q_size, d->z, q_size, d->out, dm.hidden, ep))) return rc;
+    } else {
+      EpiArgs ep{EPI_SILU, L.msg, L.msu, (long)dm.ffn};
+      if ((rc = gemm(L.wgu, dm.ffn, dm.hidden, d->h, dm.hidden, d->mlp, dm.ffn, ep))) return rc;
+      CK(launch_rownorm(d->mlp, T, dm.ffn, dm.ffn, s));
+      d->st.launches++;
+      EpiArgs e2{EPI_STORE, nullptr, nullptr, 0};
+      if ((rc = gemm(L.wdown, dm.hidden, dm.ffn, d->mlp, dm.ffn, d->out, dm.hidden, e2))) return rc;
+    }
+    CK(launch_residual(d->h, d->out, L.alpha, T, dm.hidden, mix, d->input, d->state, 1, s));
+    d->st.launches++;
+    return DORY_OK;
+  };
+  auto mix_only = [&](int mix) -> int {
+    CK(launch_residual(d->h, d->out, nullptr, T, dm.hidden, mix, d->input, d->state, 0, s));
+    d->st.launches++;
+    return DORY_OK;
+  };
+
+  int rc;
+  const int n_in = c.n_in, n_rec = c.n_rec, n_all = (int)d->layers.size();
+  for (int li = 0; li < n_in; li++)
+    if ((rc = layer(li, 0, li == n_in - 1 ? MIX_BEGIN : MIX_NONE))) return rc;
+  if (n_in == 0 && (rc = mix_only(MIX_BEGIN))) return rc;
+  for (int i = 0; i < loops; i++) {
+    const int m = i == loops - 1 ? MIX_END : MIX_LOOP;
+    for (int li = n_in; li < n_in + n_rec; li++)
+      if ((rc = layer(li, i, li == n_in + n_rec - 1 ? m : MIX_NONE))) return rc;
+    if (n_rec == 0 && (rc = mix_only(m))) return rc;
+  }
+  for (int li = n_in + n_rec; li < n_all; li++)
+    if ((rc = layer(li, 0, MIX_NONE))) return rc;
+  if (head_rows > 0) {
+    EpiArgs ep{EPI_SCALE, d->logit_scale, nullptr, 0};
+    CK(launch_gemm(d->head, d->wdtype, dm.vocab, dm.hidden, d->h + (size_t)head_from * dm.hidden, dm.hidden,
+                   head_rows, d->logits, dm.vocab, ep, s));
+    d->st.launches++;
+    d->st.gemm_launches++;
+    d->st.weight_bytes += (uint64_t)dm.vocab * dm.hidden * d->esz;
+  }
+  d->last_rows = T;
+  return DORY_OK;
+}
+
+// Upload a step's row table and the per-sequence position advance.
+int upload_rows(dory_t *d, const std::vector<int> &hseq, const std::vector<int> &hoff, const std::vector<int> &aseq,
+                const std::vector<int> &acnt) {
+  const int T = (int)hseq.size();
+  CK(cudaMemcpyAsync(d->d_row_seq, hseq.data(), T * 4, cudaMemcpyHostToDevice, d->stream));
+  CK(cudaMemcpyAsync(d->d_row_off, hoff.data(), T * 4, cudaMemcpyHostToDevice, d->stream));
+  CK(cudaMemcpyAsync(d->d_adv_seq, aseq.data(), aseq.size() * 4, cudaMemcpyHostToDevice, d->stream));
+  CK(cudaMemcpyAsync(d->d_adv_cnt, acnt.data(), acnt.size() * 4, cudaMemcpyHostToDevice, d->stream));
+  // pageable sources: the copies above have staged the data before returning
+  return DORY_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *dory_last_error(void) { return g_err.c_str(); }
+
+int dory_create(const dory_config *cfg, const dory_weights *w, void *stream, dory_t **out) {
+  if (!out) return fail(DORY_EINVAL, "out is NULL");
+  *out = nullptr;
+  std::string pat;
+  int rc = validate(cfg, pat);
+  if (rc) return rc;
+  if (!w || !w->layers) return fail(DORY_EINVAL, "weights are NULL");
+  dory_t *d = new dory_t();
+  d->cfg = *cfg;
+  d->pattern = pat;
+  d->cfg.layer_pattern = nullptr;
+  d->dims = Dims{cfg->hidden, cfg->ffn, cfg->vocab, cfg->nh, cfg->nk, cfg->hd};
+  d->wdtype = cfg->weight_dtype == DORY_W_BF16 ? W_BF16 : W_F32;
+  d->esz = cfg->weight_dtype == DORY_W_BF16 ? 2 : 4;
+  d->stream = static_cast<cudaStream_t>(stream);
+  d->Tmax = std::max(DORY_CHUNK_ROWS, cfg->max_batch);
+  const Dims &dm = d->dims;
+  const size_t esz = d->esz;
+  const int q_size = dm.nh * dm.hd, kv_size = dm.nk * dm.hd;
+  auto cleanup = [&](int code) {
+    free_all(d);
+    delete d;
+    return code;
+  };
+
+  // ---- weights -----------------------------------------------------------------------
+  size_t wb = 0;
+  auto reserve = [&](size_t bytes) {
+    size_t at = wb;
+    wb = align256(wb + bytes);
+    return at;
+  };
+  const size_t o_embed = reserve((size_t)dm.vocab * dm.hidden * esz);
+  const size_t o_head = reserve((size_t)dm.vocab * dm.hidden * esz);
+  const size_t o_ls = reserve((size_t)dm.vocab * 4);
+  struct Offs {
+    size_t qkvg, o, sq, sg, gu, down, msg, msu, alpha;
+  };
+  std::vector<Offs> offs(pat.size());
+  for (size_t li = 0; li < pat.size(); li++) {
+    Offs &o = offs[li];
+    if (pat[li] == '-') {
+      o.gu = reserve((size_t)2 * dm.ffn * dm.hidden * esz);
+      o.down = reserve((size_t)dm.hidden * dm.ffn * esz);
+      o.msg = reserve((size_t)dm.ffn * 4);
+      o.msu = reserve((size_t)dm.ffn * 4);
+    } else {
+      o.qkvg = reserve((size_t)(2 * q_size + 2 * kv_size) * dm.hidden * esz);
+      o.o = reserve((size_t)dm.hidden * q_size * esz);
+      o.sq = reserve((size_t)q_size * 4);
+      o.sg = reserve((size_t)q_size * 4);
+    }
+    o.alpha = reserve((size_t)dm.hidden * 4);
+  }
+  if (cudaMalloc(&d->wmem, wb) != cudaSuccess) {
+    cudaGetLastError();
+    fail(DORY_ENOMEM, "cudaMalloc of %zu weight bytes", wb);
+    return cleanup(DORY_ENOMEM);
+  }
+  d->wbytes = wb;
+  char *W = d->wmem;
+  d->embed = W + o_embed;
+  d->head = W + o_head;
+  d->logit_scale = reinterpret_cast<float *>(W + o_ls);
+#define COPY(dst, src, bytes, what)                       \
+  if ((rc = copy_in((dst), (src), (bytes), (what))) != 0) \
+    return cleanup(rc);
+  COPY(d->embed, w->embed, (size_t)dm.vocab * dm.hidden * esz, "embed");
+  COPY(d->head, w->head, (size_t)dm.vocab * dm.hidden * esz, "head");
+  COPY(d->logit_scale, w->logit_scale, (size_t)dm.vocab * 4, "logit_scale");
+  d->layers.resize(pat.size());
+  int ordinal = 0;
+  for (size_t li = 0; li < pat.size(); li++) {
+    const dory_layer_weights &lw = w->layers[li];
+    const Offs &o = offs[li];
+    LayerDev &L = d->layers[li];
+    L.rec = (int)li >= cfg->n_in && (int)li < cfg->n_in + cfg->n_rec;
+    L.out = (int)li >= cfg->n_in + cfg->n_rec;
+    L.alpha = reinterpret_cast<float *>(W + o.alpha);
+    COPY(L.alpha, lw.alpha, (size_t)dm.hidden * 4, "alpha");
+    if (pat[li] == '-') {
+      L.attn = false;
+      L.wgu = W + o.gu;
+      L.wdown = W + o.down;
+      L.msg = reinterpret_cast<float *>(W + o.msg);
+      L.msu = reinterpret_cast<float *>(W + o.msu);
+      const size_t m = (size_t)dm.ffn * dm.hidden * esz;
+      COPY(L.wgu, lw.gate, m, "gate");
+      COPY(static_cast<char *>(L.wgu) + m, lw.up, m, "up");
+      COPY(L.wdown, lw.down, (size_t)dm.hidden * dm.ffn * esz, "down");
+      COPY(L.msg, lw.mlp_sg, (size_t)dm.ffn * 4, "mlp_sg");
+      COPY(L.msu, lw.mlp_su, (size_t)dm.ffn * 4, "mlp_su");
+    } else {
+      L.attn = true;
+      L.sliding = pat[li] == 'S';
+      L.ordinal = ordinal++;
+      L.wqkvg = W + o.qkvg;
+      L.wo = W + o.o;
+      L.sq = reinterpret_cast<float *>(W + o.sq);
+      L.sg = reinterpret_cast<float *>(W + o.sg);
+      char *qk = static_cast<char *>(L.wqkvg);
+      const size_t qb = (size_t)q_size * dm.hidden * esz, kb = (size_t)kv_size * dm.hidden * esz;
+      COPY(qk, lw.q, qb, "q");
+      COPY(qk + qb, lw.k, kb, "k");
+      COPY(qk + qb + kb, lw.v, kb, "v");
+      COPY(qk + qb + 2 * kb, lw.g, qb, "g");
+      COPY(L.wo, lw.o, (size_t)dm.hidden * q_size * esz, "o");
+      COPY(L.sq, lw.sq, (size_t)q_size * 4, "sq");
+      COPY(L.sg, lw.sg, (size_t)q_size * 4, "sg");
+    }
+  }
+#undef COPY
+
+  // ---- KV rings ------------------------------------------------------------------------
+  const bool q8 = cfg->kv_quant == DORY_KV_Q8_2F;
+  size_t sb = 0;
+  d->ords.resize(ordinal);
+  d->slot_index.resize(ordinal);
+  int flat = 0;
+  for (size_t li = 0; li < pat.size(); li++) {
+    const LayerDev &L = d->layers[li];
+    if (!L.attn) continue;
+    OrdInfo &o = d->ords[L.ordinal];
+    o.sliding = L.sliding;
+    o.rec = L.rec;
+    if (L.sliding) {
+      o.cap = cfg->window + RING_EXTRA;
+      o.window = cfg->window;
+    } else if (cfg->full_window > 0) {
+      o.cap = cfg->full_window + RING_EXTRA;
+      o.window = cfg->full_window;
+    } else {
+      o.cap = cfg->max_context;
+      o.window = INT_MAX;
+    }
+    o.slots = (cfg->kv_mode == DORY_KV_PER_LOOP && L.rec) ? cfg->max_loops : 1;
+    o.L = slot_layout(o.cap, dm.nk, dm.hd, q8);
+    o.off = sb;
+    sb = align256(sb + (size_t)o.slots * o.L.bytes);
+    d->slot_index[L.ordinal] = flat;
+    flat += o.slots;
+    const long keys = o.window == INT_MAX ? (long)o.cap : (long)o.window;
+    d->max_splits = std::max<int>(d->max_splits, (int)((keys + KEYS_PER_SPLIT - 1) / KEYS_PER_SPLIT));
+  }
+  d->n_flat_slots = flat;
+  d->seq_stride = std::max<size_t>(sb, 256);
+  d->kv_bytes = d->seq_stride * cfg->max_seqs;
+  if (cudaMalloc(&d->kvmem, d->kv_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    fail(DORY_ENOMEM, "cudaMalloc of %zu KV bytes", d->kv_bytes);
+    return cleanup(DORY_ENOMEM);
+  }
+
+  // ---- activations ---------------------------------------------------------------------
+  const int T = d->Tmax;
+  const int rep = dm.nh / dm.nk;
+  size_t ab = 0;
+  auto areserve = [&](size_t bytes) {
+    size_t at = ab;
+    ab = align256(ab + bytes);
+    return at;
+  };
+  const size_t a_h = areserve((size_t)T * dm.hidden * 4), a_in = areserve((size_t)T * dm.hidden * 4),
+               a_st = areserve((size_t)T * dm.hidden * 4),
+               a_qkvg = areserve((size_t)T * (2 * q_size + 2 * kv_size) * 4),
+               a_z = areserve((size_t)T * q_size * 4), a_out = areserve((size_t)T * dm.hidden * 4),
+               a_mlp = areserve((size_t)T * dm.ffn * 4), a_lg = areserve((size_t)T * dm.vocab * 4),
+               a_rope = areserve((size_t)T * 2 * dm.hd * 4),
+               a_part = areserve((size_t)T * dm.nk * d->max_splits * rep * (dm.hd + 2) * 4),
+               a_kst = areserve((size_t)T * kv_size * 4), a_vst = areserve((size_t)T * kv_size * 4),
+               a_ids = areserve((size_t)T * 4), a_rs = areserve((size_t)T * 4), a_ro = areserve((size_t)T * 4),
+               a_sp = areserve((size_t)cfg->max_seqs * 4), a_as = areserve((size_t)T * 4),
+               a_ac = areserve((size_t)T * 4), a_zero = areserve((size_t)cfg->max_seqs * 4);
+  if (cudaMalloc(&d->act, ab) != cudaSuccess) {
+    cudaGetLastError();
+    fail(DORY_ENOMEM, "cudaMalloc of %zu activation bytes", ab);
+    return cleanup(DORY_ENOMEM);
+  }
+  char *A = d->act;
+  d->h = reinterpret_cast<float *>(A + a_h);
+  d->input = reinterpret_cast<float *>(A + a_in);
+  d->state = reinterpret_cast<float *>(A + a_st);
+  d->qkvg = reinterpret_cast<float *>(A + a_qkvg);
+  d->z = reinterpret_cast<float *>(A + a_z);
+  d->out = reinterpret_cast<float *>(A + a_out);
+  d->mlp = reinterpret_cast<float *>(A + a_mlp);
+  d->logits = reinterpret_cast<float *>(A + a_lg);
+  d->rope = reinterpret_cast<float *>(A + a_rope);
+  d->part = reinterpret_cast<float *>(A + a_part);
+  d->kst = reinterpret_cast<float *>(A + a_kst);
+  d->vst = reinterpret_cast<float *>(A + a_vst);
+  d->d_ids = reinterpret_cast<int32_t *>(A + a_ids);
+  d->d_row_seq = reinterpret_cast<int32_t *>(A + a_rs);
+  d->d_row_off = reinterpret_cast<int32_t *>(A + a_ro);
+  d->d_seq_pos = reinterpret_cast<int32_t *>(A + a_sp);
+  d->d_adv_seq = reinterpret_cast<int32_t *>(A + a_as);
+  d->d_adv_cnt = reinterpret_cast<int32_t *>(A + a_ac);
+  d->d_zero = reinterpret_cast<int32_t *>(A + a_zero);
+  if (cudaMemsetAsync(d->act, 0, ab, d->stream) != cudaSuccess) return cleanup(fail(DORY_ECUDA, "memset"));
+
+  d->seq_pos.assign(cfg->max_seqs, 0);
+  d->appended.assign((size_t)cfg->max_seqs * d->n_flat_slots, 0);
+  for (int s = 0; s < cfg->max_seqs; s++)
+    if ((rc = reset_seq(d, s))) return cleanup(rc);
+  if (cudaStreamSynchronize(d->stream) != cudaSuccess) return cleanup(fail(DORY_ECUDA, "sync after create"));
+  d->st.weight_bytes_device = wb;
+  d->st.kv_bytes_device = d->kv_bytes;
+  *out = d;
+  g_err.clear();
+  return DORY_OK;
+}
+
+int dory_destroy(dory_t *d) {
+  if (!d) return DORY_OK;
+  cudaStreamSynchronize(d->stream);
+  free_all(d);
+  delete d;
+  return DORY_OK;
+}
+
+int dory_reset(dory_t *d, int32_t seq) {
+  if (!d) return fail(DORY_EINVAL, "handle is NULL");
+  if (seq < 0 || seq >= d->cfg.max_seqs) return fail(DORY_EINVAL, "seq %d out of range", seq);
+  return reset_seq(d, seq);
+}
+
+static int check_range(dory_t *d, int seq, long last_pos) {
+  for (const OrdInfo &o : d->ords)
+    if (o.window == INT_MAX && last_pos >= o.cap)
+      return fail(DORY_ERANGE, "position %ld of sequence %d is past max_context %d", last_pos, seq, o.cap);
+  return DORY_OK;
+}
+
+int dory_prefill_chunk(dory_t *d, int32_t seq, const int32_t *ids, int32_t n, int32_t pos0, int32_t loops,
+                       int32_t want) {
+  if (!d) return fail(DORY_EINVAL, "handle is NULL");
+  if (seq < 0 || seq >= d->cfg.max_seqs) return fail(DORY_EINVAL, "seq %d out of range", seq);
+  if (n < 1 || n > DORY_CHUNK_ROWS) return fail(DORY_EINVAL, "n=%d: want 1..%d", n, DORY_CHUNK_ROWS);
+  if (!ids) return fail(DORY_EINVAL, "ids is NULL");
+  if (loops < 1 || loops > d->cfg.max_loops) return fail(DORY_EINVAL, "loops=%d: want 1..%d", loops, d->cfg.max_loops);
+  if (want < DORY_WANT_NONE || want > DORY_WANT_ALL) return fail(DORY_EINVAL, "want=%d", want);
+  if (pos0 != d->seq_pos[seq])
+    return fail(DORY_ESTATE, "pos0=%d but sequence %d is at %d", pos0, seq, d->seq_pos[seq]);
+  int rc = check_range(d, seq, (long)pos0 + n - 1);
+  if (rc) return rc;
+  // dory.rs fn chunk_loops
+  int L = loops;
+  if (want == DORY_WANT_NONE && d->cfg.prompt_loops > 0 && d->cfg.kv_mode == DORY_KV_LAST_LOOP)
+    L = std::min(loops, d->cfg.prompt_loops);
+  std::vector<int> hseq(n, seq), hoff(n);
+  for (int i = 0; i < n; i++) hoff[i] = i;
+  std::vector<int> aseq(1, seq), acnt(1, n);
+  if ((rc = upload_rows(d, hseq, hoff, aseq, acnt))) return rc;
+  CK(cudaMemcpyAsync(d->d_ids, ids, (size_t)n * 4, cudaMemcpyDefault, d->stream));
+  const int head_rows = want == DORY_WANT_ALL ? n : (want == DORY_WANT_LAST ? 1 : 0);
+  const int head_from = want == DORY_WANT_ALL ? 0 : n - 1;
+  if ((rc = run_step(d, n, hseq, hoff, L, head_from, head_rows))) return rc;
+  CK(launch_advance(d->d_seq_pos, d->d_adv_seq, d->d_adv_cnt, 1, d->stream));
+  d->st.launches++;
+  d->seq_pos[seq] += n;
+  d->logits_rows = head_rows;
+  return DORY_OK;
+}
+
+int dory_decode_step(dory_t *d, const int32_t *ids, const int32_t *seqs, int32_t batch, int32_t loops) {
+  if (!d) return fail(DORY_EINVAL, "handle is NULL");
+  if (batch < 1 || batch > d->cfg.max_batch) return fail(DORY_EINVAL, "batch=%d: want 1..%d", batch, d->cfg.max_batch);
+  if (!ids || !seqs) return fail(DORY_EINVAL, "ids or seqs is NULL");
+  if (loops < 1 || loops > d->cfg.max_loops) return fail(DORY_EINVAL, "loops=%d: want 1..%d", loops, d->cfg.max_loops);
+  std::vector<int> hseq(batch), hoff(batch, 0), acnt(batch, 1);
+  std::vector<char> seen(d->cfg.max_seqs, 0);
+  int rc;
+  for (int b = 0; b < batch; b++) {
+    const int s = seqs[b];
+    if (s < 0 || s >= d->cfg.max_seqs) return fail(DORY_EINVAL, "seqs[%d]=%d out of range", b, s);
+    if (seen[s]) return fail(DORY_EINVAL, "sequence %d appears twice in one step", s);
+    seen[s] = 1;
+    hseq[b] = s;
+    if ((rc = check_range(d, s, d->seq_pos[s]))) return rc;
+  }
+  if ((rc = upload_rows(d, hseq, hoff, hseq, acnt))) return rc;
+  CK(cudaMemcpyAsync(d->d_ids, ids, (size_t)batch * 4, cudaMemcpyDefault, d->stream));
+  if ((rc = run_step(d, batch, hseq, hoff, loops, 0, batch))) return rc;
+  CK(launch_advance(d->d_seq_pos, d->d_adv_seq, d->d_adv_cnt, batch, d->stream));
+  d->st.launches++;
+  for (int b = 0; b < batch; b++) d->seq_pos[hseq[b]] += 1;
+  d->logits_rows = batch;
+  return DORY_OK;
+}
+
+int dory_logits(dory_t *d, int32_t row, float *dst, size_t cap) {
+  if (!d || !dst) return fail(DORY_EINVAL, "NULL argument");
+  if (d->logits_rows == 0) return fail(DORY_ESTATE, "the last call produced no logits");
+  if (row < 0 || row >= d->logits_rows) return fail(DORY_EINVAL, "row %d of %d", row, d->logits_rows);
+  if (cap < (size_t)d->dims.vocab) return fail(DORY_EINVAL, "cap %zu < vocab %d", cap, d->dims.vocab);
+  CK(cudaMemcpyAsync(dst, d->logits + (size_t)row * d->dims.vocab, (size_t)d->dims.vocab * 4, cudaMemcpyDefault,
+                     d->stream));
+  CK(cudaStreamSynchronize(d->stream));
+  return DORY_OK;
+}
+
+int dory_logits_device(dory_t *d, const float **out, int32_t *rows) {
+  if (!d || !out || !rows) return fail(DORY_EINVAL, "NULL argument");
+  *out = d->logits;
+  *rows = d->logits_rows;
+  return DORY_OK;
+}
+
+int dory_read_hidden(dory_t *d, float *dst, size_t cap) {
+  if (!d || !dst) return fail(DORY_EINVAL, "NULL argument");
+  const size_t n = (size_t)d->last_rows * d->dims.hidden;
+  if (cap < n) return fail(DORY_EINVAL, "cap %zu < %zu", cap, n);
+  CK(cudaMemcpyAsync(dst, d->h, n * 4, cudaMemcpyDefault, d->stream));
+  CK(cudaStreamSynchronize(d->stream));
+  return DORY_OK;
+}
+
+int dory_slot_info(dory_t *d, int32_t ordinal, int32_t *cap, int32_t *slots, int32_t *sliding) {
+  if (!d) return fail(DORY_EINVAL, "handle is NULL");
+  if (ordinal < 0 || ordinal >= (int)d->ords.size()) return fail(DORY_EINVAL, "ordinal %d", ordinal);
+  const OrdInfo &o = d->ords[ordinal];
+  if (cap) *cap = o.cap;
+  if (slots) *slots = o.slots;
+  if (sliding) *sliding = o.sliding ? 1 : 0;
+  return DORY_OK;
+}
+
+static int check_slot(dory_t *d, int seq, int ordinal, int slot) {
+  if (!d) return fail(DORY_EINVAL, "handle is NULL");
+  if (seq < 0 || seq >= d->cfg.max_seqs) return fail(DORY_EINVAL, "seq %d", seq);
+  if (ordinal < 0 || ordinal >= (int)d->ords.size()) return fail(DORY_EINVAL, "ordinal %d", ordinal);
+  if (slot < 0 || slot >= d->ords[ordinal].slots) return fail(DORY_EINVAL, "slot %d", slot);
+  return DORY_OK;
+}
+
+int dory_write_kv_rows(dory_t *d, int32_t seq, int32_t ordinal, int32_t loop_slot, int32_t pos0, int32_t n,
+                       const float *k, const float *v) {
+  int rc = check_slot(d, seq, ordinal, loop_slot);
+  if (rc) return rc;
+  if (n < 0 || !k || !v) return fail(DORY_EINVAL, "bad rows");
+  int &cnt = d->app(seq, ordinal, loop_slot);
+  if (pos0 != cnt) return fail(DORY_ESTATE, "pos0=%d but the slot holds %d rows", pos0, cnt);
+  const OrdInfo &o = d->ords[ordinal];
+  if (o.window == INT_MAX && (long)pos0 + n > o.cap) return fail(DORY_ERANGE, "rows past max_context");
+  const Dims dm = d->dims;
+  const size_t row = (size_t)dm.nk * dm.hd;
+  Ring ring = d->ring(ordinal, loop_slot);
+  const bool q8 = d->cfg.kv_quant == DORY_KV_Q8_2F;
+  cudaStream_t s = d->stream;
+  for (int a = 0; a < n;) {
+    int m = std::min(n - a, d->Tmax);
+    // q8: rows up to and including the freeze go one at a time in order
+    const int c = cnt + a;
+    int seq_rows = 0;
+    if (q8 && c <= 64) seq_rows = std::min(m, 65 - c);
+    if (seq_rows > 0) m = seq_rows;
+    CK(cudaMemcpyAsync(d->kst, k + (size_t)a * row, (size_t)m * row * 4, cudaMemcpyDefault, s));
+    CK(cudaMemcpyAsync(d->vst, v + (size_t)a * row, (size_t)m * row * 4, cudaMemcpyDefault, s));
+    if (!q8) {
+      CK(launch_ring_write_f32(d->kst, d->vst, m, pos0 + a, dm, ring, seq, s));
+    } else if (seq_rows > 0) {
+      std::vector<int> hseq(m, seq), hoff(m);
+      for (int i = 0; i < m; i++) hoff[i] = pos0 + a + i;
+      CK(cudaMemcpyAsync(d->d_row_seq, hseq.data(), m * 4, cudaMemcpyHostToDevice, s));
+      CK(cudaMemcpyAsync(d->d_row_off, hoff.data(), m * 4, cudaMemcpyHostToDevice, s));
+      Rows rows;
+      rows.seq = d->d_row_seq;
+      rows.off = d->d_row_off;
+      rows.seq_pos = d->d_zero;
+      rows.n = m;
+      CK(launch_q8_append(d->kst, d->vst, (int)row, dm, rows, ring, 0, s));
+    } else {
+      CK(launch_q8_append_frozen(d->kst, d->vst, m, dm, seq, (long)pos0 + a, ring, s));
+    }
+    // the staging rows are reused by the next chunk only after these kernels ran
+    CK(cudaStreamSynchronize(s));
+    a += m;
+  }
+  cnt += n;
+  return DORY_OK;
+}
+
+int dory_set_position(dory_t *d, int32_t seq, int32_t pos) {
+  if (!d) return fail(DORY_EINVAL, "handle is NULL");
+  if (seq < 0 || seq >= d->cfg.max_seqs || pos < 0) return fail(DORY_EINVAL, "seq %d pos %d", seq, pos);
+  d->seq_pos[seq] = pos;
+  CK(cudaMemcpyAsync(d->d_seq_pos + seq, &d->seq_pos[seq], 4, cudaMemcpyHostToDevice, d->stream));
+  CK(cudaStreamSynchronize(d->stream));
+  return DORY_OK;
+}
+
+int dory_read_kv_f32(dory_t *d, int32_t seq, int32_t ordinal, int32_t loop_slot, int32_t *tags, float *k, float *v) {
+  int rc = check_slot(d, seq, ordinal, loop_slot);
+  if (rc) return rc;
+  if (d->cfg.kv_quant != DORY_KV_F32) return fail(DORY_EINVAL, "the rings hold q8_2f rows");
+  Ring r = d->ring(ordinal, loop_slot);
+  const char *slot = d->kvmem + (size_t)seq * d->seq_stride + r.off;
+  const size_t n = (size_t)d->dims.nk * r.cap * d->dims.hd;
+  CK(cudaStreamSynchronize(d->stream));
+  if (tags) CK(cudaMemcpy(tags, slot + r.L.tags, (size_t)r.cap * 4, cudaMemcpyDefault));
+  if (k) CK(cudaMemcpy(k, slot + r.L.k, n * 4, cudaMemcpyDefault));
+  if (v) CK(cudaMemcpy(v, slot + r.L.v, n * 4, cudaMemcpyDefault));
+  return DORY_OK;
+}
+
+int dory_read_kv_q8(dory_t *d, int32_t seq, int32_t ordinal, int32_t loop_slot, int32_t *tags, int8_t *kq, float *ks,
+                    int8_t *vq, float *vs, float *kcol, float *vcol, int32_t *frozen) {
+  int rc = check_slot(d, seq, ordinal, loop_slot);
+  if (rc) return rc;
+  if (d->cfg.kv_quant != DORY_KV_Q8_2F) return fail(DORY_EINVAL, "the rings hold f32 rows");
+  Ring r = d->ring(ordinal, loop_slot);
+  const char *slot = d->kvmem + (size_t)seq * d->seq_stride + r.off;
+  const int nk = d->dims.nk, hd = d->dims.hd;
+  const size_t rows = (size_t)nk * r.cap;
+  CK(cudaStreamSynchronize(d->stream));
+  if (tags) CK(cudaMemcpy(tags, slot + r.L.tags, (size_t)r.cap * 4, cudaMemcpyDefault));
+  if (kq) CK(cudaMemcpy(kq, slot + r.L.kq, rows * hd, cudaMemcpyDefault));
+  if (ks) CK(cudaMemcpy(ks, slot + r.L.ks, rows * (hd / 32) * 4, cudaMemcpyDefault));
+  if (vq) CK(cudaMemcpy(vq, slot + r.L.vq, rows * hd, cudaMemcpyDefault));
+  if (vs) CK(cudaMemcpy(vs, slot + r.L.vs, rows * 4, cudaMemcpyDefault));
+  if (kcol) CK(cudaMemcpy(kcol, slot + r.L.kcol, (size_t)nk * hd * 4, cudaMemcpyDefault));
+  if (vcol) CK(cudaMemcpy(vcol, slot + r.L.vcol, (size_t)nk * hd * 4, cudaMemcpyDefault));
+  if (frozen) {
+    std::vector<int32_t> meta(nk * 4);
+    CK(cudaMemcpy(meta.data(), slot + r.L.meta, (size_t)nk * 16, cudaMemcpyDefault));
+    for (int h = 0; h < nk; h++) frozen[h] = meta[h * 4 + 1];
+  }
+  return DORY_OK;
+}
+
+int dory_get_stats(dory_t *d, dory_stats *out) {
+  if (!d || !out) return fail(DORY_EINVAL, "NULL argument");
+  *out = d->st;
+  return DORY_OK;
+}
+
+}  // extern "C"

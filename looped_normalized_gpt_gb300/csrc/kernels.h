@@ -1,0 +1,100 @@
+// Internal launch interface of the Dory kernels. Host code only passes plain pointers,
+// sizes and the small structs below; every launch goes on the given stream.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace dory {
+
+enum WDtype { W_F32 = 0, W_BF16 = 1 };
+
+// GEMM epilogues: Y = X W^T, then
+enum Epi {
+  EPI_STORE = 0,  // y
+  EPI_SCALE = 1,  // y * vec[n]                         (head: logit_scale)
+  EPI_SILU = 2,   // silu(g * sg[n]) * (u * su[n])       (SwiGLU; g = row n, u = row n + pair)
+};
+
+struct EpiArgs {
+  int mode;
+  const float *vec;  // EPI_SCALE: [N]; EPI_SILU: sg [N]
+  const float *vec2; // EPI_SILU: su [N]
+  long pair;         // EPI_SILU: row offset of the `up` rows within W
+};
+
+// Where a step's rows sit: row r is sequence seq[r] at position seq_pos[seq[r]] + off[r].
+struct Rows {
+  const int32_t *seq;
+  const int32_t *off;
+  const int32_t *seq_pos;
+  int n;
+};
+
+// Byte layout of one KV slot (one sequence, one attention layer, one loop slot).
+struct SlotLayout {
+  size_t bytes;
+  size_t tags, k, v;                  // f32: tags[cap] i32, K/V [nk][cap][hd] f32
+  size_t kq, ks, vq, vs;              // q8: codes [nk][cap][hd] i8, K scales [nk][cap][hd/32], V scales [nk][cap]
+  size_t kcol, vcol, meta;            // q8: fields [nk][hd] f32, meta [nk][4] i32 {appended, frozen}
+  size_t wpos, wkq, wks, wvq, wvs;    // q8: the first 64 appended rows, [nk][64]...
+};
+
+SlotLayout slot_layout(int cap, int nk, int hd, bool q8);
+
+// One attention layer's ring as the kernels see it.
+struct Ring {
+  char *base;         // device base of all KV memory
+  size_t seq_stride;  // bytes per sequence
+  size_t off;         // bytes from a sequence's block to this (layer, loop slot)
+  SlotLayout L;
+  int cap;
+  int window;         // keys [p - window + 1, p]; INT32_MAX: every stored row
+  int q8;
+};
+
+struct Dims {
+  int hidden, ffn, vocab, nh, nk, hd;
+};
+
+// --- launches -------------------------------------------------------------------------
+
+cudaError_t launch_embed_rope(const int32_t *ids, const void *E, int wdtype, Dims d, Rows rows,
+                              double theta_s, double theta_f, float *h, float *rope, cudaStream_t s);
+
+cudaError_t launch_gemm(const void *W, int wdtype, int N, int K, const float *X, int ldx, int T, float *Y,
+                        int ldy, EpiArgs ep, cudaStream_t s);
+
+// q, k rotation + per-head justnorm + q*sq; f32 rings get k, v and the tag, q8 rings get
+// k, v into the staging rows kst/vst [T][nk][hd].
+cudaError_t launch_prep(float *qkvg, int ldq, Dims d, Rows rows, const float *rope, int kind, const float *sq,
+                        Ring ring, float *kst, float *vst, cudaStream_t s);
+
+// q8_2f append of staged rows, with the 64-row freeze (one block per (sequence, kv head)).
+// Rows of one sequence are consecutive; `rewrite` marks a last_loop rewrite of those rows.
+cudaError_t launch_q8_append(const float *kst, const float *vst, int ld_rows, Dims d, Rows rows, Ring ring,
+                             int rewrite, cudaStream_t s);
+
+// Rows [n][nk][hd] of one sequence appended at pos0.. to a slot whose field is frozen.
+cudaError_t launch_q8_append_frozen(const float *kst, const float *vst, int n, Dims d, int seq, long pos0, Ring ring,
+                                    cudaStream_t s);
+
+// Split-KV attention: partials, then the combine with the output gate y * sigmoid(g*sg).
+cudaError_t launch_attention(const float *qkvg, int ldq, Dims d, Rows rows, Ring ring, int splits, int keys_per_split,
+                             float *part, const float *sg, float *z, cudaStream_t s);
+
+cudaError_t launch_rownorm(float *x, int T, int width, int ld, cudaStream_t s);
+
+enum Mix { MIX_NONE = 0, MIX_BEGIN = 1, MIX_LOOP = 2, MIX_END = 3 };
+
+// x = (x^ + alpha (out^ - x^))^ per row, then the loop mix (dory.rs fn stack).
+cudaError_t launch_residual(float *h, const float *out, const float *alpha, int T, int hidden, int mix,
+                            float *input, float *state, int do_residual, cudaStream_t s);
+
+cudaError_t launch_advance(int32_t *seq_pos, const int32_t *seq, const int32_t *count, int n, cudaStream_t s);
+
+cudaError_t launch_ring_write_f32(const float *k, const float *v, int n, int pos0, Dims d, Ring ring, int seq,
+                                  cudaStream_t s);
+
+}  // namespace dory
