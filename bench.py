@@ -96,6 +96,8 @@ def workload_config():
 
 
 def bench_ours(args, rank, world):
+    global PROMPT
+    PROMPT = args.prompt
     import torch
 
     from looped_normalized_gpt_gb300 import Dory, build
@@ -174,7 +176,7 @@ def bench_ours(args, rank, world):
         "vs_baseline": None,
         "dtype": "bf16 weights, f32 activations and KV",
         "data": "synthetic: seeded unit-row random weights, seeded uniform token ids",
-        "config": {"workload": "Dory-2B-shape batch-1 decode after a 4096-token prompt, loops 4, "
+        "config": {"workload": f"Dory-2B-shape batch-1 decode after a {PROMPT}-token prompt, loops 4, "
                                "sliding window 512, last_loop f32 KV",
                    "batch": 1, "loops": 4, "prompt": PROMPT, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (2.1 GB of weights streamed per token)"},
@@ -246,6 +248,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prompt", type=int, default=PROMPT, help="prompt tokens before the decode steps")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

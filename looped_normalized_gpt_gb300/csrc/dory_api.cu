@@ -7,6 +7,7 @@
 #include <cstdio>
 #include <cstring>
 #include <string>
+#include <unordered_map>
 #include <vector>
 
 #include "../../include/dory.h"
@@ -46,6 +47,13 @@ struct LayerDev {
   float *sq = nullptr, *sg = nullptr, *alpha = nullptr, *msg = nullptr, *msu = nullptr;
 };
 
+struct Plan {
+  cudaGraphExec_t exec = nullptr;
+  int32_t *rt = nullptr;  // the captured step's own row table
+  int launches = 0, gemm_launches = 0;
+  float *h_last = nullptr;
+};
+
 struct OrdInfo {
   bool sliding = true, rec = false;
   int cap = 0, window = 0, slots = 1;
@@ -75,11 +83,18 @@ struct dory_handle {
   size_t seq_stride = 0, kv_bytes = 0;
   int max_splits = 1;
 
+  float *h2 = nullptr, *h_last = nullptr;  // second hidden buffer (fused path), final rows
+  int32_t *hctr = nullptr, *actr = nullptr;  // arrival counters of the fused kernels
+  bool fused_ok = false;
   float *h = nullptr, *input = nullptr, *state = nullptr, *qkvg = nullptr, *z = nullptr, *out = nullptr,
         *mlp = nullptr, *logits = nullptr, *rope = nullptr, *part = nullptr, *kst = nullptr, *vst = nullptr;
-  int32_t *d_ids = nullptr, *d_row_seq = nullptr, *d_row_off = nullptr, *d_seq_pos = nullptr,
-          *d_adv_seq = nullptr, *d_adv_cnt = nullptr, *d_zero = nullptr;
+  int32_t *d_ids = nullptr, *d_seq_pos = nullptr, *d_zero = nullptr;
   char *act = nullptr;
+
+  cudaStream_t cap_stream = nullptr;  // graphs are captured here and replayed on `stream`
+  bool use_graphs = true;
+  std::unordered_map<std::string, Plan> plans;
+  int32_t *d_rows = nullptr;  // step table when graphs are off: seq, off, advance seq, count
 
   std::vector<int> seq_pos;     // host mirror of d_seq_pos
   std::vector<int> appended;    // rows appended per (seq, ordinal, slot)
@@ -147,6 +162,13 @@ int copy_in(void *dst, const void *src, size_t bytes, const char *what) {
 }
 
 void free_all(dory_t *d) {
+  for (auto &kv : d->plans) {
+    if (kv.second.exec) cudaGraphExecDestroy(kv.second.exec);
+    if (kv.second.rt) cudaFree(kv.second.rt);
+  }
+  d->plans.clear();
+  if (d->cap_stream) cudaStreamDestroy(d->cap_stream);
+  d->cap_stream = nullptr;
   if (d->wmem) cudaFree(d->wmem);
   if (d->kvmem) cudaFree(d->kvmem);
   if (d->act) cudaFree(d->act);
@@ -167,45 +189,86 @@ int reset_seq(dory_t *d, int seq) {
   return DORY_OK;
 }
 
-Rows make_rows(dory_t *d, int n) {
-  Rows r;
-  r.seq = d->d_row_seq;
-  r.off = d->d_row_off;
-  r.seq_pos = d->d_seq_pos;
-  r.n = n;
-  return r;
-}
+// The rows of one step: row r is sequence hseq[r] at position seq_pos[hseq[r]] + hoff[r];
+// aseq/acnt are the position advances at the step's end. `loops` recurrent passes; logits
+// for head_rows rows starting at row head_from.
+struct StepArgs {
+  int T = 0, loops = 1, head_from = 0, head_rows = 0;
+  std::vector<int> hseq, hoff, aseq, acnt;
+  std::string key() const {
+    std::string k = std::to_string(T) + ":" + std::to_string(loops) + ":" + std::to_string(head_from) + ":" +
+                    std::to_string(head_rows) + "|";
+    for (int i = 0; i < T; i++) k += std::to_string(hseq[i]) + "," + std::to_string(hoff[i]) + ";";
+    return k;
+  }
+};
 
-// One forward over the step's rows (already uploaded): row r is sequence hseq[r] at
-// position seq_pos[hseq[r]] + hoff[r]. `loops` passes; `head_rows` rows of logits taken
-// from the last head_rows rows (0: none).
-int run_step(dory_t *d, int T, const std::vector<int> &hseq, const std::vector<int> &hoff, int loops,
-             int head_from, int head_rows) {
+// Host-side accounting of a step: algorithmic bytes and the rows each slot appends.
+void account(dory_t *d, const StepArgs &a) {
   const dory_config &c = d->cfg;
   const Dims dm = d->dims;
-  cudaStream_t s = d->stream;
-  Rows rows = make_rows(d, T);
-  d->st.weight_bytes = d->st.kv_read_bytes = d->st.kv_write_bytes = 0;
-  d->st.launches = d->st.gemm_launches = 0;
+  const bool q8 = c.kv_quant == DORY_KV_Q8_2F;
+  const size_t kv_row_bytes = q8 ? (size_t)dm.hd * 2 + (dm.hd / 32) * 4 + 4 : (size_t)dm.hd * 8;
+  const int q_size = dm.nh * dm.hd, kv_size = dm.nk * dm.hd;
+  uint64_t wb = 0, kr = 0, kw = 0;
+  auto layer = [&](int li, int loop_i) {
+    const LayerDev &L = d->layers[li];
+    if (L.attn) {
+      wb += (uint64_t)(2 * q_size + 2 * kv_size) * dm.hidden * d->esz + (uint64_t)dm.hidden * q_size * d->esz;
+      const int sl = (c.kv_mode == DORY_KV_PER_LOOP && L.rec) ? loop_i : 0;
+      const bool rewrite = c.kv_mode == DORY_KV_LAST_LOOP && (L.rec || L.out) && loop_i > 0;
+      const OrdInfo &o = d->ords[L.ordinal];
+      for (int r = 0; r < a.T; r++) {
+        const long p = (long)d->seq_pos[a.hseq[r]] + a.hoff[r];
+        const long keys = o.window == INT_MAX ? p + 1 : std::min<long>(o.window, p + 1);
+        kr += (uint64_t)keys * dm.nk * kv_row_bytes;
+        if (!rewrite) d->app(a.hseq[r], L.ordinal, sl)++;
+      }
+      kw += (uint64_t)a.T * dm.nk * kv_row_bytes;
+    } else {
+      wb += (uint64_t)3 * dm.ffn * dm.hidden * d->esz;
+    }
+  };
+  const int n_in = c.n_in, n_rec = c.n_rec, n_all = (int)d->layers.size();
+  for (int li = 0; li < n_in; li++) layer(li, 0);
+  for (int i = 0; i < a.loops; i++)
+    for (int li = n_in; li < n_in + n_rec; li++) layer(li, i);
+  for (int li = n_in + n_rec; li < n_all; li++) layer(li, 0);
+  if (a.head_rows > 0) wb += (uint64_t)dm.vocab * dm.hidden * d->esz;
+  d->st.weight_bytes = wb;
+  d->st.kv_read_bytes = kr;
+  d->st.kv_write_bytes = kw;
+}
+
+// Issue every launch of one step on stream s. `rt` holds the device row table: seq[Tmax],
+// off[Tmax], advance seq[Tmax], advance count[Tmax]. With fixed_splits the attention grids
+// cover the whole window whatever the positions (for replayed graphs).
+int issue_step(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_splits, cudaStream_t s, int *launches,
+               int *gemm_launches) {
+  const dory_config &c = d->cfg;
+  const Dims dm = d->dims;
+  const int T = a.T;
+  Rows rows;
+  rows.seq = rt;
+  rows.off = rt + d->Tmax;
+  rows.seq_pos = d->d_seq_pos;
+  rows.n = T;
+  int nl = 0, ng = 0;
   const int q_size = dm.nh * dm.hd, kv_size = dm.nk * dm.hd;
   const int ldq = 2 * q_size + 2 * kv_size;
   long pmax = 0;
-  for (int r = 0; r < T; r++) pmax = std::max(pmax, (long)d->seq_pos[hseq[r]] + hoff[r]);
+  for (int r = 0; r < T; r++) pmax = std::max(pmax, (long)d->seq_pos[a.hseq[r]] + a.hoff[r]);
   const bool q8 = c.kv_quant == DORY_KV_Q8_2F;
-  const size_t kv_row_bytes = q8 ? (size_t)dm.hd * 2 + (dm.hd / 32) * 4 + 4 : (size_t)dm.hd * 8;
 
   CK(launch_embed_rope(d->d_ids, d->embed, d->wdtype, dm, rows, c.rope_theta_sliding, c.rope_theta_full, d->h,
                        d->rope, s));
-  d->st.launches++;
-
+  nl++;
   auto gemm = [&](const void *W, int N, int K, const float *X, int ldx, float *Y, int ldy, EpiArgs ep) -> int {
     CK(launch_gemm(W, d->wdtype, N, K, X, ldx, T, Y, ldy, ep, s));
-    d->st.launches++;
-    d->st.gemm_launches++;
-    d->st.weight_bytes += (uint64_t)N * K * d->esz * (ep.mode == EPI_SILU ? 2 : 1);
+    nl++;
+    ng++;
     return DORY_OK;
   };
-
   auto layer = [&](int li, int loop_i, int mix) -> int {
     const LayerDev &L = d->layers[li];
     int rc;
@@ -216,42 +279,35 @@ int run_step(dory_t *d, int T, const std::vector<int> &hseq, const std::vector<i
       EpiArgs ep{EPI_STORE, nullptr, nullptr, 0};
       if ((rc = gemm(L.wqkvg, ldq, dm.hidden, d->h, dm.hidden, d->qkvg, ldq, ep))) return rc;
       CK(launch_prep(d->qkvg, ldq, dm, rows, d->rope, L.sliding ? 0 : 1, L.sq, ring, d->kst, d->vst, s));
-      d->st.launches++;
+      nl++;
       if (q8) {
         CK(launch_q8_append(d->kst, d->vst, kv_size, dm, rows, ring, rewrite ? 1 : 0, s));
-        d->st.launches++;
+        nl++;
       }
-      long keys = ring.window == INT_MAX ? pmax + 1 : std::min<long>(ring.window, pmax + 1);
+      const long wmax = ring.window == INT_MAX ? (long)ring.cap : (long)ring.window;
+      const long keys = fixed_splits ? wmax : std::min<long>(wmax, pmax + 1);
       const int splits = (int)((keys + KEYS_PER_SPLIT - 1) / KEYS_PER_SPLIT);
       if (splits > d->max_splits) return fail(DORY_ERANGE, "attention needs %d splits (max %d)", splits, d->max_splits);
       CK(launch_attention(d->qkvg, ldq, dm, rows, ring, splits, KEYS_PER_SPLIT, d->part, L.sg, d->z, s));
-      d->st.launches += 2;
-      for (int r = 0; r < T; r++) {
-        const long p = (long)d->seq_pos[hseq[r]] + hoff[r];
-        const long kr = ring.window == INT_MAX ? p + 1 : std::min<long>(ring.window, p + 1);
-        d->st.kv_read_bytes += (uint64_t)kr * dm.nk * kv_row_bytes;
-      }
-      d->st.kv_write_bytes += (uint64_t)T * dm.nk * kv_row_bytes;
-      if (!rewrite)
-        for (int r = 0; r < T; r++) d->app(hseq[r], L.ordinal, sl)++;
+      nl += 2;
       CK(launch_rownorm(d->z, T, q_size, q_size, s));
-      d->st.launches++;
+      nl++;
       if ((rc = gemm(L.wo, dm.hidden, q_size, d->z, q_size, d->out, dm.hidden, ep))) return rc;
     } else {
       EpiArgs ep{EPI_SILU, L.msg, L.msu, (long)dm.ffn};
       if ((rc = gemm(L.wgu, dm.ffn, dm.hidden, d->h, dm.hidden, d->mlp, dm.ffn, ep))) return rc;
       CK(launch_rownorm(d->mlp, T, dm.ffn, dm.ffn, s));
-      d->st.launches++;
+      nl++;
       EpiArgs e2{EPI_STORE, nullptr, nullptr, 0};
       if ((rc = gemm(L.wdown, dm.hidden, dm.ffn, d->mlp, dm.ffn, d->out, dm.hidden, e2))) return rc;
     }
     CK(launch_residual(d->h, d->out, L.alpha, T, dm.hidden, mix, d->input, d->state, 1, s));
-    d->st.launches++;
+    nl++;
     return DORY_OK;
   };
   auto mix_only = [&](int mix) -> int {
     CK(launch_residual(d->h, d->out, nullptr, T, dm.hidden, mix, d->input, d->state, 0, s));
-    d->st.launches++;
+    nl++;
     return DORY_OK;
   };
 
@@ -260,35 +316,244 @@ int run_step(dory_t *d, int T, const std::vector<int> &hseq, const std::vector<i
   for (int li = 0; li < n_in; li++)
     if ((rc = layer(li, 0, li == n_in - 1 ? MIX_BEGIN : MIX_NONE))) return rc;
   if (n_in == 0 && (rc = mix_only(MIX_BEGIN))) return rc;
-  for (int i = 0; i < loops; i++) {
-    const int m = i == loops - 1 ? MIX_END : MIX_LOOP;
+  for (int i = 0; i < a.loops; i++) {
+    const int m = i == a.loops - 1 ? MIX_END : MIX_LOOP;
     for (int li = n_in; li < n_in + n_rec; li++)
       if ((rc = layer(li, i, li == n_in + n_rec - 1 ? m : MIX_NONE))) return rc;
     if (n_rec == 0 && (rc = mix_only(m))) return rc;
   }
   for (int li = n_in + n_rec; li < n_all; li++)
     if ((rc = layer(li, 0, MIX_NONE))) return rc;
-  if (head_rows > 0) {
+  if (a.head_rows > 0) {
     EpiArgs ep{EPI_SCALE, d->logit_scale, nullptr, 0};
-    CK(launch_gemm(d->head, d->wdtype, dm.vocab, dm.hidden, d->h + (size_t)head_from * dm.hidden, dm.hidden,
-                   head_rows, d->logits, dm.vocab, ep, s));
-    d->st.launches++;
-    d->st.gemm_launches++;
-    d->st.weight_bytes += (uint64_t)dm.vocab * dm.hidden * d->esz;
+    CK(launch_gemm(d->head, d->wdtype, dm.vocab, dm.hidden, d->h + (size_t)a.head_from * dm.hidden, dm.hidden,
+                   a.head_rows, d->logits, dm.vocab, ep, s));
+    nl++;
+    ng++;
   }
-  d->last_rows = T;
+  CK(launch_advance(d->d_seq_pos, rt + 2 * d->Tmax, rt + 3 * d->Tmax, (int)a.aseq.size(), s));
+  nl++;
+  *launches = nl;
+  *gemm_launches = ng;
   return DORY_OK;
 }
 
-// Upload a step's row table and the per-sequence position advance.
-int upload_rows(dory_t *d, const std::vector<int> &hseq, const std::vector<int> &hoff, const std::vector<int> &aseq,
-                const std::vector<int> &acnt) {
-  const int T = (int)hseq.size();
-  CK(cudaMemcpyAsync(d->d_row_seq, hseq.data(), T * 4, cudaMemcpyHostToDevice, d->stream));
-  CK(cudaMemcpyAsync(d->d_row_off, hoff.data(), T * 4, cudaMemcpyHostToDevice, d->stream));
-  CK(cudaMemcpyAsync(d->d_adv_seq, aseq.data(), aseq.size() * 4, cudaMemcpyHostToDevice, d->stream));
-  CK(cudaMemcpyAsync(d->d_adv_cnt, acnt.data(), acnt.size() * 4, cudaMemcpyHostToDevice, d->stream));
-  // pageable sources: the copies above have staged the data before returning
+// The fused launch sequence for steps of up to 4 rows: per attention sub-layer the q/k/v/g
+// GEMV (its prologue takes the previous residual and loop mix, its last block per head the
+// RoPE/norm/ring write), [the q8 append], attention with the merge and gate, the O GEMV
+// (row norm in its prologue); per MLP the gate/up GEMV with SwiGLU and the down GEMV.
+// Kernels after the first use programmatic dependent launch.
+int issue_step_fused(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_splits, cudaStream_t s, int *launches,
+                     int *gemm_launches) {
+  const dory_config &c = d->cfg;
+  const Dims dm = d->dims;
+  const int T = a.T;
+  Rows rows;
+  rows.seq = rt;
+  rows.off = rt + d->Tmax;
+  rows.seq_pos = d->d_seq_pos;
+  rows.n = T;
+  int nl = 0, ng = 0;
+  const int q_size = dm.nh * dm.hd, kv_size = dm.nk * dm.hd;
+  const int ldq = 2 * q_size + 2 * kv_size;
+  long pmax = 0;
+  for (int r = 0; r < T; r++) pmax = std::max(pmax, (long)d->seq_pos[a.hseq[r]] + a.hoff[r]);
+  const bool q8 = c.kv_quant == DORY_KV_Q8_2F;
+  CK(launch_embed_rope(d->d_ids, d->embed, d->wdtype, dm, rows, c.rope_theta_sliding, c.rope_theta_full, d->h,
+                       d->rope, s));
+  nl++;
+  float *cur = d->h, *other = d->h2;
+  struct {
+    bool on = false;
+    const float *alpha = nullptr;
+    int mix = MIX_NONE;
+  } pend;
+  auto first_in = [&]() {
+    GemvIn g{};
+    if (!pend.on) {
+      g.mode = IN_PLAIN;
+      g.src = cur;
+      g.ld = dm.hidden;
+      return g;
+    }
+    g.mode = IN_RESID;
+    g.src = cur;
+    g.ld = dm.hidden;
+    g.out = d->out;
+    g.alpha = pend.alpha;
+    g.mix = pend.mix;
+    g.h_dst = other;
+    g.input = d->input;
+    g.state = d->state;
+    std::swap(cur, other);
+    pend.on = false;
+    return g;
+  };
+  HeadEpi none{};
+  none.enabled = 0;
+  auto layer = [&](int li, int loop_i, int mix) -> int {
+    const LayerDev &L = d->layers[li];
+    if (L.attn) {
+      const int sl = (c.kv_mode == DORY_KV_PER_LOOP && L.rec) ? loop_i : 0;
+      const bool rewrite = c.kv_mode == DORY_KV_LAST_LOOP && (L.rec || L.out) && loop_i > 0;
+      Ring ring = d->ring(L.ordinal, sl);
+      HeadEpi he{};
+      he.enabled = 1;
+      he.counters = d->hctr;
+      he.d = dm;
+      he.rows = rows;
+      he.rope = d->rope;
+      he.kind = L.sliding ? 0 : 1;
+      he.sq = L.sq;
+      he.ring = ring;
+      he.kst = d->kst;
+      he.vst = d->vst;
+      EpiArgs ep{EPI_STORE, nullptr, nullptr, 0};
+      CK(launch_gemv_fused(L.wqkvg, d->wdtype, ldq, dm.hidden, T, first_in(), d->qkvg, ldq, ep, he, true, s));
+      nl++;
+      ng++;
+      if (q8) {
+        CK(launch_q8_append(d->kst, d->vst, kv_size, dm, rows, ring, rewrite ? 1 : 0, s));
+        nl++;
+      }
+      const long wmax = ring.window == INT_MAX ? (long)ring.cap : (long)ring.window;
+      const long keys = fixed_splits ? wmax : std::min<long>(wmax, pmax + 1);
+      const int splits = (int)((keys + KEYS_PER_SPLIT - 1) / KEYS_PER_SPLIT);
+      if (splits > d->max_splits) return fail(DORY_ERANGE, "attention needs %d splits (max %d)", splits, d->max_splits);
+      CK(launch_attention_fused(d->qkvg, ldq, dm, rows, ring, splits, KEYS_PER_SPLIT, d->part, L.sg, d->z, d->actr,
+                                true, s));
+      nl++;
+      GemvIn in{};
+      in.mode = IN_NORM;
+      in.src = d->z;
+      in.ld = q_size;
+      CK(launch_gemv_fused(L.wo, d->wdtype, dm.hidden, q_size, T, in, d->out, dm.hidden, ep, none, true, s));
+      nl++;
+      ng++;
+    } else {
+      EpiArgs ep{EPI_SILU, L.msg, L.msu, (long)dm.ffn};
+      CK(launch_gemv_fused(L.wgu, d->wdtype, dm.ffn, dm.hidden, T, first_in(), d->mlp, dm.ffn, ep, none, true, s));
+      GemvIn in{};
+      in.mode = IN_NORM;
+      in.src = d->mlp;
+      in.ld = dm.ffn;
+      EpiArgs e2{EPI_STORE, nullptr, nullptr, 0};
+      CK(launch_gemv_fused(L.wdown, d->wdtype, dm.hidden, dm.ffn, T, in, d->out, dm.hidden, e2, none, true, s));
+      nl += 2;
+      ng += 2;
+    }
+    pend.on = true;
+    pend.alpha = L.alpha;
+    pend.mix = mix;
+    return DORY_OK;
+  };
+  int rc;
+  const int n_in = c.n_in, n_rec = c.n_rec, n_all = (int)d->layers.size();
+  for (int li = 0; li < n_in; li++)
+    if ((rc = layer(li, 0, li == n_in - 1 ? MIX_BEGIN : MIX_NONE))) return rc;
+  for (int i = 0; i < a.loops; i++) {
+    const int m = i == a.loops - 1 ? MIX_END : MIX_LOOP;
+    for (int li = n_in; li < n_in + n_rec; li++)
+      if ((rc = layer(li, i, li == n_in + n_rec - 1 ? m : MIX_NONE))) return rc;
+  }
+  for (int li = n_in + n_rec; li < n_all; li++)
+    if ((rc = layer(li, 0, MIX_NONE))) return rc;
+  EpiArgs eh{EPI_SCALE, d->logit_scale, nullptr, 0};
+  if (a.head_rows == T && a.head_from == 0) {
+    CK(launch_gemv_fused(d->head, d->wdtype, dm.vocab, dm.hidden, T, first_in(), d->logits, dm.vocab, eh, none, true,
+                         s));
+    nl++;
+    ng++;
+  } else {
+    CK(launch_residual(cur, d->out, pend.alpha, T, dm.hidden, pend.mix, d->input, d->state, 1, s));
+    nl++;
+    pend.on = false;
+    if (a.head_rows > 0) {
+      CK(launch_gemm(d->head, d->wdtype, dm.vocab, dm.hidden, cur + (size_t)a.head_from * dm.hidden, dm.hidden,
+                     a.head_rows, d->logits, dm.vocab, eh, s));
+      nl++;
+      ng++;
+    }
+  }
+  d->h_last = cur;
+  CK(launch_advance(d->d_seq_pos, rt + 2 * d->Tmax, rt + 3 * d->Tmax, (int)a.aseq.size(), s));
+  nl++;
+  *launches = nl;
+  *gemm_launches = ng;
+  return DORY_OK;
+}
+
+int issue_any(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_splits, cudaStream_t s, int *nl, int *ng) {
+  if (d->fused_ok && a.T <= 4) return issue_step_fused(d, a, rt, fixed_splits, s, nl, ng);
+  d->h_last = d->h;
+  return issue_step(d, a, rt, fixed_splits, s, nl, ng);
+}
+
+int upload_table(dory_t *d, const StepArgs &a, int32_t *rt, cudaStream_t s) {
+  std::vector<int32_t> t((size_t)4 * d->Tmax, 0);
+  for (int i = 0; i < a.T; i++) {
+    t[i] = a.hseq[i];
+    t[d->Tmax + i] = a.hoff[i];
+  }
+  for (size_t i = 0; i < a.aseq.size(); i++) {
+    t[2 * d->Tmax + i] = a.aseq[i];
+    t[3 * d->Tmax + i] = a.acnt[i];
+  }
+  CK(cudaMemcpyAsync(rt, t.data(), t.size() * 4, cudaMemcpyHostToDevice, s));
+  CK(cudaStreamSynchronize(s));
+  return DORY_OK;
+}
+
+// Run one step: replay its captured graph (captured on first use), or issue the launches.
+int do_step(dory_t *d, const StepArgs &a, const int32_t *ids) {
+  int rc;
+  CK(cudaMemcpyAsync(d->d_ids, ids, (size_t)a.T * 4, cudaMemcpyDefault, d->stream));
+  if (!d->use_graphs) {
+    if ((rc = upload_table(d, a, d->d_rows, d->stream))) return rc;
+    int nl = 0, ng = 0;
+    if ((rc = issue_any(d, a, d->d_rows, false, d->stream, &nl, &ng))) return rc;
+    d->st.launches = nl;
+    d->st.gemm_launches = ng;
+  } else {
+    const std::string key = a.key();
+    auto it = d->plans.find(key);
+    if (it == d->plans.end()) {
+      Plan p;
+      if (cudaMalloc(&p.rt, (size_t)4 * d->Tmax * 4) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(DORY_ENOMEM, "cudaMalloc of a step table");
+      }
+      if ((rc = upload_table(d, a, p.rt, d->stream))) {
+        cudaFree(p.rt);
+        return rc;
+      }
+      cudaGraph_t g = nullptr;
+      CK(cudaStreamBeginCapture(d->cap_stream, cudaStreamCaptureModeThreadLocal));
+      rc = issue_any(d, a, p.rt, true, d->cap_stream, &p.launches, &p.gemm_launches);
+      p.h_last = d->h_last;
+      cudaError_t ec = cudaStreamEndCapture(d->cap_stream, &g);
+      if (rc || ec != cudaSuccess) {
+        if (g) cudaGraphDestroy(g);
+        cudaFree(p.rt);
+        cudaGetLastError();
+        return rc ? rc : fail(DORY_ECUDA, "graph capture: %s", cudaGetErrorString(ec));
+      }
+      ec = cudaGraphInstantiate(&p.exec, g, 0);
+      cudaGraphDestroy(g);
+      if (ec != cudaSuccess) {
+        cudaFree(p.rt);
+        return fail(DORY_ECUDA, "graph instantiate: %s", cudaGetErrorString(ec));
+      }
+      it = d->plans.emplace(key, p).first;
+    }
+    CK(cudaGraphLaunch(it->second.exec, d->stream));
+    d->h_last = it->second.h_last;
+    d->st.launches = it->second.launches;
+    d->st.gemm_launches = it->second.gemm_launches;
+  }
+  account(d, a);
+  for (size_t i = 0; i < a.aseq.size(); i++) d->seq_pos[a.aseq[i]] += a.acnt[i];
+  d->last_rows = a.T;
   return DORY_OK;
 }
 
@@ -460,6 +725,8 @@ int dory_create(const dory_config *cfg, const dory_weights *w, void *stream, dor
     ab = align256(ab + bytes);
     return at;
   };
+  const size_t a_h2 = areserve((size_t)T * dm.hidden * 4), a_hc = areserve((size_t)(2 * dm.nh + 2 * dm.nk) * 4),
+               a_ac2 = areserve((size_t)T * dm.nk * 4);
   const size_t a_h = areserve((size_t)T * dm.hidden * 4), a_in = areserve((size_t)T * dm.hidden * 4),
                a_st = areserve((size_t)T * dm.hidden * 4),
                a_qkvg = areserve((size_t)T * (2 * q_size + 2 * kv_size) * 4),
@@ -468,9 +735,9 @@ int dory_create(const dory_config *cfg, const dory_weights *w, void *stream, dor
                a_rope = areserve((size_t)T * 2 * dm.hd * 4),
                a_part = areserve((size_t)T * dm.nk * d->max_splits * rep * (dm.hd + 2) * 4),
                a_kst = areserve((size_t)T * kv_size * 4), a_vst = areserve((size_t)T * kv_size * 4),
-               a_ids = areserve((size_t)T * 4), a_rs = areserve((size_t)T * 4), a_ro = areserve((size_t)T * 4),
-               a_sp = areserve((size_t)cfg->max_seqs * 4), a_as = areserve((size_t)T * 4),
-               a_ac = areserve((size_t)T * 4), a_zero = areserve((size_t)cfg->max_seqs * 4);
+               a_ids = areserve((size_t)T * 4),
+               a_sp = areserve((size_t)cfg->max_seqs * 4), a_rows = areserve((size_t)4 * T * 4),
+               a_zero = areserve((size_t)cfg->max_seqs * 4);
   if (cudaMalloc(&d->act, ab) != cudaSuccess) {
     cudaGetLastError();
     fail(DORY_ENOMEM, "cudaMalloc of %zu activation bytes", ab);
@@ -478,6 +745,18 @@ int dory_create(const dory_config *cfg, const dory_weights *w, void *stream, dor
   }
   char *A = d->act;
   d->h = reinterpret_cast<float *>(A + a_h);
+  d->h2 = reinterpret_cast<float *>(A + a_h2);
+  d->h_last = d->h;
+  d->hctr = reinterpret_cast<int32_t *>(A + a_hc);
+  d->actr = reinterpret_cast<int32_t *>(A + a_ac2);
+  {
+    const int hdv = dm.hd;
+    const size_t kmax = std::max(std::max(dm.hidden, dm.ffn), dm.nh * dm.hd);
+    d->fused_ok = (hdv == 64 || hdv == 128) && cfg->n_in >= 1 && cfg->n_rec >= 1 && cfg->n_out >= 1 &&
+                  kmax % 8 == 0 && 4 * kmax * 4 <= 96 * 1024;
+    const char *e = getenv("DORY_FUSED");
+    if (e && e[0] == '0') d->fused_ok = false;
+  }
   d->input = reinterpret_cast<float *>(A + a_in);
   d->state = reinterpret_cast<float *>(A + a_st);
   d->qkvg = reinterpret_cast<float *>(A + a_qkvg);
@@ -490,14 +769,17 @@ int dory_create(const dory_config *cfg, const dory_weights *w, void *stream, dor
   d->kst = reinterpret_cast<float *>(A + a_kst);
   d->vst = reinterpret_cast<float *>(A + a_vst);
   d->d_ids = reinterpret_cast<int32_t *>(A + a_ids);
-  d->d_row_seq = reinterpret_cast<int32_t *>(A + a_rs);
-  d->d_row_off = reinterpret_cast<int32_t *>(A + a_ro);
   d->d_seq_pos = reinterpret_cast<int32_t *>(A + a_sp);
-  d->d_adv_seq = reinterpret_cast<int32_t *>(A + a_as);
-  d->d_adv_cnt = reinterpret_cast<int32_t *>(A + a_ac);
+  d->d_rows = reinterpret_cast<int32_t *>(A + a_rows);
   d->d_zero = reinterpret_cast<int32_t *>(A + a_zero);
   if (cudaMemsetAsync(d->act, 0, ab, d->stream) != cudaSuccess) return cleanup(fail(DORY_ECUDA, "memset"));
 
+  {
+    const char *e = getenv("DORY_GRAPHS");
+    d->use_graphs = !(e && e[0] == '0');
+  }
+  if (cudaStreamCreateWithFlags(&d->cap_stream, cudaStreamNonBlocking) != cudaSuccess)
+    return cleanup(fail(DORY_ECUDA, "stream create"));
   d->seq_pos.assign(cfg->max_seqs, 0);
   d->appended.assign((size_t)cfg->max_seqs * d->n_flat_slots, 0);
   for (int s = 0; s < cfg->max_seqs; s++)
@@ -547,17 +829,18 @@ int dory_prefill_chunk(dory_t *d, int32_t seq, const int32_t *ids, int32_t n, in
   int L = loops;
   if (want == DORY_WANT_NONE && d->cfg.prompt_loops > 0 && d->cfg.kv_mode == DORY_KV_LAST_LOOP)
     L = std::min(loops, d->cfg.prompt_loops);
-  std::vector<int> hseq(n, seq), hoff(n);
-  for (int i = 0; i < n; i++) hoff[i] = i;
-  std::vector<int> aseq(1, seq), acnt(1, n);
-  if ((rc = upload_rows(d, hseq, hoff, aseq, acnt))) return rc;
-  CK(cudaMemcpyAsync(d->d_ids, ids, (size_t)n * 4, cudaMemcpyDefault, d->stream));
+  StepArgs st;
+  st.T = n;
+  st.loops = L;
+  st.hseq.assign(n, seq);
+  st.hoff.resize(n);
+  for (int i = 0; i < n; i++) st.hoff[i] = i;
+  st.aseq.assign(1, seq);
+  st.acnt.assign(1, n);
   const int head_rows = want == DORY_WANT_ALL ? n : (want == DORY_WANT_LAST ? 1 : 0);
-  const int head_from = want == DORY_WANT_ALL ? 0 : n - 1;
-  if ((rc = run_step(d, n, hseq, hoff, L, head_from, head_rows))) return rc;
-  CK(launch_advance(d->d_seq_pos, d->d_adv_seq, d->d_adv_cnt, 1, d->stream));
-  d->st.launches++;
-  d->seq_pos[seq] += n;
+  st.head_rows = head_rows;
+  st.head_from = want == DORY_WANT_ALL ? 0 : n - 1;
+  if ((rc = do_step(d, st, ids))) return rc;
   d->logits_rows = head_rows;
   return DORY_OK;
 }
@@ -567,7 +850,12 @@ int dory_decode_step(dory_t *d, const int32_t *ids, const int32_t *seqs, int32_t
   if (batch < 1 || batch > d->cfg.max_batch) return fail(DORY_EINVAL, "batch=%d: want 1..%d", batch, d->cfg.max_batch);
   if (!ids || !seqs) return fail(DORY_EINVAL, "ids or seqs is NULL");
   if (loops < 1 || loops > d->cfg.max_loops) return fail(DORY_EINVAL, "loops=%d: want 1..%d", loops, d->cfg.max_loops);
-  std::vector<int> hseq(batch), hoff(batch, 0), acnt(batch, 1);
+  StepArgs st;
+  st.T = batch;
+  st.loops = loops;
+  st.hseq.resize(batch);
+  st.hoff.assign(batch, 0);
+  st.acnt.assign(batch, 1);
   std::vector<char> seen(d->cfg.max_seqs, 0);
   int rc;
   for (int b = 0; b < batch; b++) {
@@ -575,15 +863,13 @@ int dory_decode_step(dory_t *d, const int32_t *ids, const int32_t *seqs, int32_t
     if (s < 0 || s >= d->cfg.max_seqs) return fail(DORY_EINVAL, "seqs[%d]=%d out of range", b, s);
     if (seen[s]) return fail(DORY_EINVAL, "sequence %d appears twice in one step", s);
     seen[s] = 1;
-    hseq[b] = s;
+    st.hseq[b] = s;
     if ((rc = check_range(d, s, d->seq_pos[s]))) return rc;
   }
-  if ((rc = upload_rows(d, hseq, hoff, hseq, acnt))) return rc;
-  CK(cudaMemcpyAsync(d->d_ids, ids, (size_t)batch * 4, cudaMemcpyDefault, d->stream));
-  if ((rc = run_step(d, batch, hseq, hoff, loops, 0, batch))) return rc;
-  CK(launch_advance(d->d_seq_pos, d->d_adv_seq, d->d_adv_cnt, batch, d->stream));
-  d->st.launches++;
-  for (int b = 0; b < batch; b++) d->seq_pos[hseq[b]] += 1;
+  st.aseq = st.hseq;
+  st.head_rows = batch;
+  st.head_from = 0;
+  if ((rc = do_step(d, st, ids))) return rc;
   d->logits_rows = batch;
   return DORY_OK;
 }
@@ -610,7 +896,7 @@ int dory_read_hidden(dory_t *d, float *dst, size_t cap) {
   if (!d || !dst) return fail(DORY_EINVAL, "NULL argument");
   const size_t n = (size_t)d->last_rows * d->dims.hidden;
   if (cap < n) return fail(DORY_EINVAL, "cap %zu < %zu", cap, n);
-  CK(cudaMemcpyAsync(dst, d->h, n * 4, cudaMemcpyDefault, d->stream));
+  CK(cudaMemcpyAsync(dst, d->h_last, n * 4, cudaMemcpyDefault, d->stream));
   CK(cudaStreamSynchronize(d->stream));
   return DORY_OK;
 }
@@ -661,11 +947,11 @@ int dory_write_kv_rows(dory_t *d, int32_t seq, int32_t ordinal, int32_t loop_slo
     } else if (seq_rows > 0) {
       std::vector<int> hseq(m, seq), hoff(m);
       for (int i = 0; i < m; i++) hoff[i] = pos0 + a + i;
-      CK(cudaMemcpyAsync(d->d_row_seq, hseq.data(), m * 4, cudaMemcpyHostToDevice, s));
-      CK(cudaMemcpyAsync(d->d_row_off, hoff.data(), m * 4, cudaMemcpyHostToDevice, s));
+      CK(cudaMemcpyAsync(d->d_rows, hseq.data(), m * 4, cudaMemcpyHostToDevice, s));
+      CK(cudaMemcpyAsync(d->d_rows + d->Tmax, hoff.data(), m * 4, cudaMemcpyHostToDevice, s));
       Rows rows;
-      rows.seq = d->d_row_seq;
-      rows.off = d->d_row_off;
+      rows.seq = d->d_rows;
+      rows.off = d->d_rows + d->Tmax;
       rows.seq_pos = d->d_zero;
       rows.n = m;
       CK(launch_q8_append(d->kst, d->vst, (int)row, dm, rows, ring, 0, s));

@@ -1,0 +1,658 @@
+// Fused decode kernels for steps of up to 4 rows (batch-1..4 decode, tiny chunks).
+//
+// gemv_fused_kernel streams one weight row per warp with 16-byte loads, like gemv_kernel,
+// but
+//   * issues its first weight loads before griddepcontrol.wait, so under programmatic
+//     dependent launch they overlap the previous kernel's tail;
+//   * builds its input rows itself (prologue): the nGPT residual of the previous
+//     sub-layer with the loop mix after it (dory.rs fn slerp, fn stack), or the row norm
+//     of an attention or MLP output (fn attn_layer's justnorm over nh*hd, fn mlp_layer's
+//     over ffn); block 0 stores the new hidden rows for the layers after;
+//   * for the q/k/v/g projection, the last block to finish a head (an arrival counter per
+//     head) does that head's epilogue: RoPE + justnorm (+ s_q^2) for q and k, and the f32
+//     ring write (or staging for q8) of k and v (dory.rs fn attn_layer).
+// attn_fused_kernel is the split-KV attention of k_attn.cu whose last split block per
+// (row, kv head) merges the splits and applies the gate (no second launch).
+#include <climits>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace dory {
+
+namespace {
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+constexpr int FW = 8;     // warps per block
+// 8-element chunks of a row loaded before the dependency wait
+template <typename WT>
+struct Pre {
+  static constexpr int n = sizeof(WT) == 2 ? 8 : 2;
+};
+constexpr int MAXT = 4;   // rows
+
+template <typename WT>
+struct Chunk;
+template <>
+struct Chunk<__nv_bfloat16> {
+  uint4 u;
+  __device__ __forceinline__ void load(const __nv_bfloat16 *p) { u = __ldg(reinterpret_cast<const uint4 *>(p)); }
+  __device__ __forceinline__ void get(float *w) const { unpack8(u, w); }
+};
+template <>
+struct Chunk<float> {
+  float4 a, b;
+  __device__ __forceinline__ void load(const float *p) {
+    a = __ldg(reinterpret_cast<const float4 *>(p));
+    b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+  }
+  __device__ __forceinline__ void get(float *w) const {
+    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+    w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+  }
+};
+
+// Sum of v over the block for up to MAXT values at once (one per row).
+template <int NT>
+__device__ __forceinline__ void block_sum_n(float *v, float (*red)[FW]) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int t = 0; t < NT; t++) v[t] = warp_sum(v[t]);
+  __syncthreads();
+  if (lane == 0)
+#pragma unroll
+    for (int t = 0; t < NT; t++) red[t][warp] = v[t];
+  __syncthreads();
+#pragma unroll
+  for (int t = 0; t < NT; t++) {
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < FW; w++) s += red[t][w];
+    v[t] = s;
+  }
+  __syncthreads();
+}
+
+// Prologue: the block's input rows xs[t][K] from the previous kernels' outputs.
+template <int TT>
+__device__ void build_input(const GemvIn &in, int T, int K, float *xs) {
+  __shared__ float red[MAXT][FW];
+  const int tid = threadIdx.x, nt = blockDim.x;
+  if (in.mode == IN_PLAIN) {
+    for (int t = 0; t < T; t++)
+      for (int i = tid; i < K; i += nt) xs[t * K + i] = in.src[(size_t)t * in.ld + i];
+    __syncthreads();
+    return;
+  }
+  if (in.mode == IN_NORM) {
+    float ss[TT];
+#pragma unroll
+    for (int t = 0; t < TT; t++) ss[t] = 0.f;
+    for (int t = 0; t < T; t++)
+      for (int i = tid; i < K; i += nt) {
+        const float v = in.src[(size_t)t * in.ld + i];
+        xs[t * K + i] = v;
+        ss[t] += v * v;
+      }
+    block_sum_n<TT>(ss, red);
+    for (int t = 0; t < T; t++) {
+      const float inv = 1.f / sqrtf(ss[t] + DORY_EPS);
+      for (int i = tid; i < K; i += nt) xs[t * K + i] *= inv;
+    }
+    __syncthreads();
+    return;
+  }
+  // IN_RESID: x = (x^ + alpha (out^ - x^))^, then the loop mix
+  const bool lead = blockIdx.x == 0;
+  float a[TT], b[TT];
+  if (in.alpha) {
+#pragma unroll
+    for (int t = 0; t < TT; t++) a[t] = b[t] = 0.f;
+    for (int t = 0; t < T; t++)
+      for (int i = tid; i < K; i += nt) {
+        const float x = in.src[(size_t)t * in.ld + i], o = in.out[(size_t)t * K + i];
+        a[t] += x * x;
+        b[t] += o * o;
+      }
+    block_sum_n<TT>(a, red);
+    block_sum_n<TT>(b, red);
+#pragma unroll
+    for (int t = 0; t < TT; t++) {
+      a[t] = 1.f / sqrtf(a[t] + DORY_EPS);
+      b[t] = 1.f / sqrtf(b[t] + DORY_EPS);
+    }
+    float s[TT];
+#pragma unroll
+    for (int t = 0; t < TT; t++) s[t] = 0.f;
+    for (int t = 0; t < T; t++)
+      for (int i = tid; i < K; i += nt) {
+        const float xh = in.src[(size_t)t * in.ld + i] * a[t], oh = in.out[(size_t)t * K + i] * b[t];
+        const float v = xh + in.alpha[i] * (oh - xh);
+        xs[t * K + i] = v;
+        s[t] += v * v;
+      }
+    block_sum_n<TT>(s, red);
+    for (int t = 0; t < T; t++) {
+      const float inv = 1.f / sqrtf(s[t] + DORY_EPS);
+      for (int i = tid; i < K; i += nt) xs[t * K + i] *= inv;
+    }
+  } else {
+    for (int t = 0; t < T; t++)
+      for (int i = tid; i < K; i += nt) xs[t * K + i] = in.src[(size_t)t * in.ld + i];
+  }
+  __syncthreads();
+  if (in.mix == MIX_LOOP || in.mix == MIX_END) {  // state = h^
+    float s[TT];
+#pragma unroll
+    for (int t = 0; t < TT; t++) s[t] = 0.f;
+    for (int t = 0; t < T; t++)
+      for (int i = tid; i < K; i += nt) s[t] += xs[t * K + i] * xs[t * K + i];
+    block_sum_n<TT>(s, red);
+    for (int t = 0; t < T; t++) {
+      const float inv = 1.f / sqrtf(s[t] + DORY_EPS);
+      for (int i = tid; i < K; i += nt) {
+        const float v = xs[t * K + i] * inv;
+        xs[t * K + i] = v;
+        if (lead) in.state[(size_t)t * K + i] = v;
+      }
+    }
+    __syncthreads();
+  }
+  if (in.mix == MIX_BEGIN || in.mix == MIX_LOOP) {  // h = (state + input)^
+    float s[TT];
+#pragma unroll
+    for (int t = 0; t < TT; t++) s[t] = 0.f;
+    for (int t = 0; t < T; t++)
+      for (int i = tid; i < K; i += nt) {
+        const float st = xs[t * K + i];
+        float inp;
+        if (in.mix == MIX_BEGIN) {
+          inp = st;
+          if (lead) {
+            in.input[(size_t)t * K + i] = st;
+            in.state[(size_t)t * K + i] = st;
+          }
+        } else {
+          inp = in.input[(size_t)t * K + i];
+        }
+        const float v = st + inp;
+        xs[t * K + i] = v;
+        s[t] += v * v;
+      }
+    block_sum_n<TT>(s, red);
+    for (int t = 0; t < T; t++) {
+      const float inv = 1.f / sqrtf(s[t] + DORY_EPS);
+      for (int i = tid; i < K; i += nt) xs[t * K + i] *= inv;
+    }
+    __syncthreads();
+  }
+  if (lead && in.h_dst)
+    for (int t = 0; t < T; t++)
+      for (int i = tid; i < K; i += nt) in.h_dst[(size_t)t * K + i] = xs[t * K + i];
+}
+
+// The last block of a q/k/v/g head: RoPE + justnorm (+ s_q^2) and the ring write.
+__device__ void head_epilogue(const HeadEpi &he, int head, int T, float *Y, int ldy) {
+  __shared__ float red2[MAXT][FW];
+  const Dims &d = he.d;
+  const int hd = d.hd, half = hd / 2;
+  const int tid = threadIdx.x;
+  const int t = tid / half, j = tid % half;  // blockDim 256 >= T * half for hd <= 128
+  const bool act = t < T;
+  const bool is_q = head < d.nh, is_k = head >= d.nh && head < d.nh + d.nk;
+  const bool is_v = head >= d.nh + d.nk && head < d.nh + 2 * d.nk;
+  if (!(is_q || is_k || is_v)) return;  // gate heads need nothing (block-uniform)
+  float a = 0.f, b = 0.f;
+  float *row = Y + (size_t)(act ? t : 0) * ldy + head * hd;
+  if (act) {
+    a = __ldcg(row + j);
+    b = __ldcg(row + j + half);
+  }
+  if (is_q || is_k) {
+    if (act) {
+      const float *cs = he.rope + ((size_t)t * 2 + he.kind) * hd;
+      const float *sn = cs + half;
+      const float x = a, y = b;
+      a = x * cs[j] - y * sn[j];
+      b = y * cs[j] + x * sn[j];
+    }
+    // per-row sums over the row's half threads (two warps when hd = 128)
+    float ss[MAXT] = {0.f, 0.f, 0.f, 0.f};
+    float v = act ? a * a + b * b : 0.f;
+    v = warp_sum(v);
+    const int lane = tid & 31, warp = tid >> 5;
+    __syncthreads();
+    if (lane == 0) red2[0][warp] = v;
+    __syncthreads();
+    const int wpr = (half + 31) / 32;  // warps per row
+    if (act) {
+      float s = 0.f;
+      for (int w = 0; w < wpr; w++) s += red2[0][t * wpr + w];
+      ss[0] = s;
+      const float inv = 1.f / sqrtf(ss[0] + DORY_EPS);
+      a *= inv;
+      b *= inv;
+    }
+  }
+  if (!act) return;
+  if (is_q) {
+    row[j] = a * he.sq[head * hd + j];
+    row[j + half] = b * he.sq[head * hd + j + half];
+    return;
+  }
+  const int kh = is_k ? head - d.nh : head - d.nh - d.nk;
+  if (is_k) {  // rotated, normalised key back into the projection rows for reference
+    row[j] = a;
+    row[j + half] = b;
+  }
+  const Ring &ring = he.ring;
+  if (ring.q8) {
+    float *dst = (is_k ? he.kst : he.vst) + ((size_t)t * d.nk + kh) * hd;
+    dst[j] = a;
+    dst[j + half] = b;
+    return;
+  }
+  const int seq = he.rows.seq[t];
+  const long pos = (long)he.rows.seq_pos[seq] + he.rows.off[t];
+  const int rr = (int)(pos % ring.cap);
+  char *slot = ring.base + (size_t)seq * ring.seq_stride + ring.off;
+  float *dst = reinterpret_cast<float *>(slot + (is_k ? ring.L.k : ring.L.v)) + ((size_t)kh * ring.cap + rr) * hd;
+  dst[j] = a;
+  dst[j + half] = b;
+  if (is_k && kh == 0 && j == 0) reinterpret_cast<int32_t *>(slot + ring.L.tags)[rr] = (int32_t)pos;
+}
+
+template <typename WT, int TT, bool DUAL>
+__global__ void __launch_bounds__(FW * 32, 2) gemv_fused_kernel(const WT *__restrict__ W, int N, int K, int T,
+                                                                GemvIn in, float *__restrict__ Y, int ldy,
+                                                                EpiArgs ep, HeadEpi he) {
+  extern __shared__ float xs[];  // [T][K]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = blockIdx.x * FW + warp;
+  const bool has_row = n < N;
+  const WT *w0 = W + (size_t)(has_row ? n : 0) * K;
+  const WT *w1 = DUAL ? W + (size_t)((has_row ? n : 0) + ep.pair) * K : nullptr;
+  // weights do not depend on earlier kernels: start them before the wait
+  constexpr int PRE = Pre<WT>::n;
+  Chunk<WT> pa[PRE], pb[DUAL ? PRE : 1];
+  const int nchunks = K / 8;
+#pragma unroll
+  for (int c = 0; c < PRE; c++) {
+    const int ci = lane + 32 * c;
+    if (has_row && ci < nchunks) {
+      pa[c].load(w0 + ci * 8);
+      if (DUAL) pb[c].load(w1 + ci * 8);
+    }
+  }
+  pdl_wait();
+  pdl_trigger();
+  build_input<TT>(in, T, K, xs);
+
+  float acc0[TT], acc1[TT];
+#pragma unroll
+  for (int t = 0; t < TT; t++) acc0[t] = acc1[t] = 0.f;
+  auto fma_chunk = [&](const float *w, const float *u, int ci) {
+    const int k = ci * 8;
+#pragma unroll
+    for (int t = 0; t < TT; t++) {
+      if (t < T) {
+        const float4 xa = *reinterpret_cast<const float4 *>(&xs[t * K + k]);
+        const float4 xb = *reinterpret_cast<const float4 *>(&xs[t * K + k + 4]);
+        const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+          acc0[t] = fmaf(w[i], xv[i], acc0[t]);
+          if (DUAL) acc1[t] = fmaf(u[i], xv[i], acc1[t]);
+        }
+      }
+    }
+  };
+  if (has_row) {
+#pragma unroll
+    for (int c = 0; c < PRE; c++) {
+      const int ci = lane + 32 * c;
+      if (ci < nchunks) {
+        float w[8], u[8];
+        pa[c].get(w);
+        if (DUAL) pb[c].get(u);
+        fma_chunk(w, u, ci);
+      }
+    }
+#pragma unroll 4
+    for (int ci = lane + 32 * PRE; ci < nchunks; ci += 32) {
+      Chunk<WT> x, y;
+      x.load(w0 + ci * 8);
+      if (DUAL) y.load(w1 + ci * 8);
+      float w[8], u[8];
+      x.get(w);
+      if (DUAL) y.get(u);
+      fma_chunk(w, u, ci);
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < TT; t++) {
+    if (t >= T) break;
+    const float a = warp_sum(acc0[t]);
+    const float b = DUAL ? warp_sum(acc1[t]) : 0.f;
+    if (lane == 0 && has_row) {
+      float y;
+      if (ep.mode == EPI_SCALE) {
+        y = a * ep.vec[n];
+      } else if (ep.mode == EPI_SILU) {
+        const float g = a * ep.vec[n];
+        y = g * sigmoidf_(g) * (b * ep.vec2[n]);
+      } else {
+        y = a;
+      }
+      Y[(size_t)t * ldy + n] = y;
+    }
+  }
+  if (!he.enabled) return;
+  // arrival per head: the last block of a head runs its epilogue
+  __shared__ int last;
+  __threadfence();
+  __syncthreads();
+  const int head = (blockIdx.x * FW) / he.d.hd;
+  if (threadIdx.x == 0) {
+    const int per_head = he.d.hd / FW;
+    const int old = atomicAdd(&he.counters[head], 1);
+    last = old == per_head - 1;
+    if (last) he.counters[head] = 0;  // ready for the next launch
+  }
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  head_epilogue(he, head, T, Y, ldy);
+}
+
+// ---------------------------------------------------------------------------------------
+// attention with the combine in the last split block
+// ---------------------------------------------------------------------------------------
+
+constexpr int AW = 4;
+
+template <bool Q8, int REP, int NV>
+__global__ void __launch_bounds__(AW * 32) attn_fused_kernel(const float *__restrict__ qkvg, int ldq, Dims d,
+                                                             Rows rows, Ring ring, int splits, int ks_len,
+                                                             float *__restrict__ part, const float *__restrict__ sg,
+                                                             float *__restrict__ z, int *counters) {
+  constexpr int HD = NV * 32;
+  __shared__ float qs[REP][HD];
+  __shared__ float wm[AW][REP], wl[AW][REP];
+  __shared__ float wo[AW][REP][HD];
+  __shared__ int last;
+  pdl_wait();
+  pdl_trigger();
+  const int r = blockIdx.x / d.nk, kh = blockIdx.x % d.nk, sp = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int seq = rows.seq[r];
+  const long p = (long)rows.seq_pos[seq] + rows.off[r];
+  const long lo = ring.window == INT_MAX ? 0 : (p + 1 - ring.window > 0 ? p + 1 - ring.window : 0);
+  const long k0 = lo + (long)sp * ks_len;
+  const long k1 = (k0 + ks_len - 1 < p) ? k0 + ks_len - 1 : p;
+  const char *slot = ring.base + (size_t)seq * ring.seq_stride + ring.off;
+  const int32_t *tags = reinterpret_cast<const int32_t *>(slot + ring.L.tags);
+  const float *q = qkvg + (size_t)r * ldq + (size_t)kh * REP * HD;
+  const float *kcol = Q8 ? reinterpret_cast<const float *>(slot + ring.L.kcol) + (size_t)kh * HD : nullptr;
+  const int frozen = Q8 ? reinterpret_cast<const int32_t *>(slot + ring.L.meta)[kh * 4 + 1] : 0;
+  for (int i = threadIdx.x; i < REP * HD; i += blockDim.x) {
+    float v = q[i];
+    if (Q8 && frozen) v *= kcol[i % HD];
+    qs[i / HD][i % HD] = v;
+  }
+  __syncthreads();
+  const float scale = 1.f / sqrtf((float)HD);
+  float m[REP], l[REP], acc[REP][NV];
+#pragma unroll
+  for (int h = 0; h < REP; h++) {
+    m[h] = -INFINITY;
+    l[h] = 0.f;
+#pragma unroll
+    for (int i = 0; i < NV; i++) acc[h][i] = 0.f;
+  }
+  for (long kb = k0 + warp * 32; kb <= k1; kb += AW * 32) {
+    const long pe = kb + lane;
+    const int rr = (int)(pe % ring.cap);
+    const bool valid = pe <= k1 && tags[rr] == (int32_t)pe;
+    float s[REP];
+#pragma unroll
+    for (int h = 0; h < REP; h++) s[h] = 0.f;
+    if (valid) {
+      if (!Q8) {
+        const float4 *kr = reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(slot + ring.L.k) +
+                                                            ((size_t)kh * ring.cap + rr) * HD);
+#pragma unroll 4
+        for (int c = 0; c < HD / 4; c++) {
+          const float4 k4 = __ldg(kr + c);
+#pragma unroll
+          for (int h = 0; h < REP; h++) {
+            const float4 q4 = *reinterpret_cast<const float4 *>(&qs[h][c * 4]);
+            s[h] = fmaf(q4.x, k4.x, fmaf(q4.y, k4.y, fmaf(q4.z, k4.z, fmaf(q4.w, k4.w, s[h]))));
+          }
+        }
+      } else {
+        const int8_t *kq = reinterpret_cast<const int8_t *>(slot + ring.L.kq) + ((size_t)kh * ring.cap + rr) * HD;
+        const float *ksc = reinterpret_cast<const float *>(slot + ring.L.ks) + ((size_t)kh * ring.cap + rr) * (HD / 32);
+#pragma unroll
+        for (int g = 0; g < HD / 32; g++) {
+          float dg[REP];
+#pragma unroll
+          for (int h = 0; h < REP; h++) dg[h] = 0.f;
+#pragma unroll
+          for (int c = 0; c < 2; c++) {
+            const int4 w = __ldg(reinterpret_cast<const int4 *>(kq + g * 32 + c * 16));
+            const int8_t *bb = reinterpret_cast<const int8_t *>(&w);
+#pragma unroll
+            for (int e = 0; e < 16; e++) {
+              const float kv = (float)bb[e];
+#pragma unroll
+              for (int h = 0; h < REP; h++) dg[h] = fmaf(qs[h][g * 32 + c * 16 + e], kv, dg[h]);
+            }
+          }
+          const float sgk = __ldg(ksc + g);
+#pragma unroll
+          for (int h = 0; h < REP; h++) s[h] = fmaf(sgk, dg[h], s[h]);
+        }
+      }
+    }
+    float pw[REP];
+    bool any = false;
+#pragma unroll
+    for (int h = 0; h < REP; h++) {
+      const float sv = valid ? s[h] * scale : -INFINITY;
+      const float mb = warp_max(sv);
+      if (mb == -INFINITY) {
+        pw[h] = 0.f;
+        continue;
+      }
+      any = true;
+      const float mn = fmaxf(m[h], mb);
+      const float corr = expf(m[h] - mn);
+      pw[h] = valid ? expf(sv - mn) : 0.f;
+      l[h] = l[h] * corr + warp_sum(pw[h]);
+#pragma unroll
+      for (int i = 0; i < NV; i++) acc[h][i] *= corr;
+      m[h] = mn;
+    }
+    if (!any) continue;
+    const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+    for (int j = 0; j < 32; j++) {
+      if (!((vmask >> j) & 1u)) continue;
+      const long pj = kb + j;
+      const int rj = (int)(pj % ring.cap);
+      float pj_h[REP];
+#pragma unroll
+      for (int h = 0; h < REP; h++) pj_h[h] = __shfl_sync(0xffffffffu, pw[h], j);
+      if (!Q8) {
+        const float *vr = reinterpret_cast<const float *>(slot + ring.L.v) + ((size_t)kh * ring.cap + rj) * HD;
+#pragma unroll
+        for (int i = 0; i < NV; i++) {
+          const float vv = __ldg(vr + lane + 32 * i);
+#pragma unroll
+          for (int h = 0; h < REP; h++) acc[h][i] = fmaf(pj_h[h], vv, acc[h][i]);
+        }
+      } else {
+        const int8_t *vq = reinterpret_cast<const int8_t *>(slot + ring.L.vq) + ((size_t)kh * ring.cap + rj) * HD;
+        const float vs = __ldg(reinterpret_cast<const float *>(slot + ring.L.vs) + (size_t)kh * ring.cap + rj);
+#pragma unroll
+        for (int i = 0; i < NV; i++) {
+          const float vv = (float)vq[lane + 32 * i];
+#pragma unroll
+          for (int h = 0; h < REP; h++) acc[h][i] = fmaf(pj_h[h] * vs, vv, acc[h][i]);
+        }
+      }
+    }
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int h = 0; h < REP; h++) {
+      wm[warp][h] = m[h];
+      wl[warp][h] = l[h];
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < REP; h++)
+#pragma unroll
+    for (int i = 0; i < NV; i++) wo[warp][h][lane + 32 * i] = acc[h][i];
+  __syncthreads();
+  float *out = part + ((size_t)(r * d.nk + kh) * splits + sp) * REP * (HD + 2);
+  for (int i = threadIdx.x; i < REP * HD; i += blockDim.x) {
+    const int h = i / HD, c = i % HD;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < AW; w++) M = fmaxf(M, wm[w][h]);
+    float o = 0.f, L = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < AW; w++) {
+        const float f = expf(wm[w][h] - M);
+        o += wo[w][h][c] * f;
+        L += wl[w][h] * f;
+      }
+    }
+    out[h * (HD + 2) + c] = o;
+    if (c == 0) {
+      out[h * (HD + 2) + HD] = M;
+      out[h * (HD + 2) + HD + 1] = L;
+    }
+  }
+  // the last split block of (row, kv head) merges the splits and gates
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int *ctr = counters + r * d.nk + kh;
+    const int old = atomicAdd(ctr, 1);
+    last = old == splits - 1;
+    if (last) *ctr = 0;
+  }
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  const float *pr = part + (size_t)(r * d.nk + kh) * splits * REP * (HD + 2);
+  float vcol = 1.f;
+  const float *g = qkvg + (size_t)r * ldq + (size_t)(d.nh + 2 * d.nk) * HD;
+  for (int i = threadIdx.x; i < REP * HD; i += blockDim.x) {
+    const int h = i / HD, c = i % HD;
+    if (Q8 && frozen) vcol = reinterpret_cast<const float *>(slot + ring.L.vcol)[kh * HD + c];
+    float M = -INFINITY;
+    for (int s = 0; s < splits; s++) M = fmaxf(M, __ldcg(pr + (s * REP + h) * (HD + 2) + HD));
+    float o = 0.f, L = 0.f;
+    for (int s = 0; s < splits; s++) {
+      const float *ps = pr + (s * REP + h) * (HD + 2);
+      const float ms = __ldcg(ps + HD);
+      if (ms == -INFINITY) continue;
+      const float f = expf(ms - M);
+      o += __ldcg(ps + c) * f;
+      L += __ldcg(ps + HD + 1) * f;
+    }
+    const int col = (kh * REP + h) * HD + c;
+    const float y = (L > 0.f ? o / L : 0.f) * vcol;
+    z[(size_t)r * d.nh * HD + col] = y * sigmoidf_(g[col] * sg[col]);
+  }
+}
+
+template <typename K, typename... Args>
+cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, bool pdl, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+template <typename WT, int TT, bool DUAL>
+cudaError_t gemv_fused_t(const void *W, int N, int K, int T, GemvIn in, float *Y, int ldy, EpiArgs ep, HeadEpi he,
+                         bool pdl, cudaStream_t s) {
+  auto kern = gemv_fused_kernel<WT, TT, DUAL>;
+  const size_t smem = (size_t)T * K * sizeof(float);
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+    attr_done = true;
+  }
+  dim3 grid((N + FW - 1) / FW);
+  return launch_pdl(kern, grid, dim3(FW * 32), smem, pdl, s, static_cast<const WT *>(W), N, K, T, in, Y, ldy, ep, he);
+}
+
+template <typename WT, bool DUAL>
+cudaError_t gemv_fused_d(const void *W, int N, int K, int T, GemvIn in, float *Y, int ldy, EpiArgs ep, HeadEpi he,
+                         bool pdl, cudaStream_t s) {
+  switch (T) {
+    case 1: return gemv_fused_t<WT, 1, DUAL>(W, N, K, T, in, Y, ldy, ep, he, pdl, s);
+    case 2: return gemv_fused_t<WT, 2, DUAL>(W, N, K, T, in, Y, ldy, ep, he, pdl, s);
+    default: return gemv_fused_t<WT, 4, DUAL>(W, N, K, T, in, Y, ldy, ep, he, pdl, s);
+  }
+}
+
+template <bool Q8, int REP, int NV>
+cudaError_t attn_fused_t(const float *qkvg, int ldq, Dims d, Rows rows, Ring ring, int splits, int kps, float *part,
+                         const float *sg, float *z, int *counters, bool pdl, cudaStream_t s) {
+  dim3 grid(rows.n * d.nk, splits);
+  return launch_pdl(attn_fused_kernel<Q8, REP, NV>, grid, dim3(AW * 32), 0, pdl, s, qkvg, ldq, d, rows, ring, splits,
+                    kps, part, sg, z, counters);
+}
+
+template <bool Q8>
+cudaError_t attn_fused_q(const float *qkvg, int ldq, Dims d, Rows rows, Ring ring, int splits, int kps, float *part,
+                         const float *sg, float *z, int *counters, bool pdl, cudaStream_t s) {
+  const int rep = d.nh / d.nk, nv = d.hd / 32;
+#define DISPATCH(R, N)       \
+  if (rep == R && nv == N) \
+    return attn_fused_t<Q8, R, N>(qkvg, ldq, d, rows, ring, splits, kps, part, sg, z, counters, pdl, s);
+  DISPATCH(1, 1) DISPATCH(1, 2) DISPATCH(1, 4)
+  DISPATCH(2, 1) DISPATCH(2, 2) DISPATCH(2, 4)
+  DISPATCH(4, 1) DISPATCH(4, 2) DISPATCH(4, 4)
+  DISPATCH(8, 1) DISPATCH(8, 2) DISPATCH(8, 4)
+#undef DISPATCH
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_gemv_fused(const void *W, int wdtype, int N, int K, int T, GemvIn in, float *Y, int ldy,
+                              EpiArgs ep, HeadEpi he, bool pdl, cudaStream_t s) {
+  if (T < 1 || T > MAXT || K % 8 != 0 || (size_t)T * K * 4 > 96 * 1024) return cudaErrorInvalidValue;
+  if (he.enabled && ((he.d.hd / 2) % 32 != 0 || T * (he.d.hd / 2) > FW * 32)) return cudaErrorInvalidValue;
+  const bool dual = ep.mode == EPI_SILU;
+  if (wdtype == W_BF16)
+    return dual ? gemv_fused_d<__nv_bfloat16, true>(W, N, K, T, in, Y, ldy, ep, he, pdl, s)
+                : gemv_fused_d<__nv_bfloat16, false>(W, N, K, T, in, Y, ldy, ep, he, pdl, s);
+  return dual ? gemv_fused_d<float, true>(W, N, K, T, in, Y, ldy, ep, he, pdl, s)
+              : gemv_fused_d<float, false>(W, N, K, T, in, Y, ldy, ep, he, pdl, s);
+}
+
+cudaError_t launch_attention_fused(const float *qkvg, int ldq, Dims d, Rows rows, Ring ring, int splits, int kps,
+                                   float *part, const float *sg, float *z, int *counters, bool pdl, cudaStream_t s) {
+  return ring.q8 ? attn_fused_q<true>(qkvg, ldq, d, rows, ring, splits, kps, part, sg, z, counters, pdl, s)
+                 : attn_fused_q<false>(qkvg, ldq, d, rows, ring, splits, kps, part, sg, z, counters, pdl, s);
+}
+
+}  // namespace dory

@@ -92,6 +92,45 @@ enum Mix { MIX_NONE = 0, MIX_BEGIN = 1, MIX_LOOP = 2, MIX_END = 3 };
 cudaError_t launch_residual(float *h, const float *out, const float *alpha, int T, int hidden, int mix,
                             float *input, float *state, int do_residual, cudaStream_t s);
 
+// ---- fused decode path (up to 4 rows) -------------------------------------------------
+
+enum InMode { IN_PLAIN = 0, IN_NORM = 1, IN_RESID = 2 };
+
+// How a fused GEMV builds its input rows: the source rows as they are, their row norm,
+// or the nGPT residual of the previous sub-layer (src = its input h, out = its output)
+// followed by the loop mix. With IN_RESID block 0 stores the result to h_dst (and the
+// mix's input/state rows).
+struct GemvIn {
+  int mode;
+  const float *src;
+  int ld;
+  const float *out;
+  const float *alpha;  // nullptr: the mix alone
+  int mix;
+  float *h_dst;
+  float *input;
+  float *state;
+};
+
+// Per-head epilogue of the q/k/v/g projection (RoPE, justnorm, s_q^2, ring write).
+struct HeadEpi {
+  int enabled;
+  int *counters;  // one arrival counter per head, zero between launches
+  Dims d;
+  Rows rows;
+  const float *rope;
+  int kind;
+  const float *sq;
+  Ring ring;
+  float *kst, *vst;
+};
+
+cudaError_t launch_gemv_fused(const void *W, int wdtype, int N, int K, int T, GemvIn in, float *Y, int ldy,
+                              EpiArgs ep, HeadEpi he, bool pdl, cudaStream_t s);
+
+cudaError_t launch_attention_fused(const float *qkvg, int ldq, Dims d, Rows rows, Ring ring, int splits, int kps,
+                                   float *part, const float *sg, float *z, int *counters, bool pdl, cudaStream_t s);
+
 cudaError_t launch_advance(int32_t *seq_pos, const int32_t *seq, const int32_t *count, int n, cudaStream_t s);
 
 cudaError_t launch_ring_write_f32(const float *k, const float *v, int n, int pos0, Dims d, Ring ring, int seq,
