@@ -2,6 +2,7 @@
 // sequence of one forward step (dory.rs fn forward_host / fn stack for one chunk, or
 // one decode row per sequence).
 #include <algorithm>
+#include <array>
 #include <climits>
 #include <cstdarg>
 #include <cstdio>
@@ -47,6 +48,14 @@ struct LayerDev {
   float *sq = nullptr, *sg = nullptr, *alpha = nullptr, *msg = nullptr, *msu = nullptr;
 };
 
+struct TcW {
+  CUtensorMap map;
+  int N = 0, K = 0, splits = 1;
+  long pair = 0;
+};
+
+int bn_index(int bn) { return bn <= 16 ? 0 : bn <= 32 ? 1 : bn <= 64 ? 2 : bn <= 128 ? 3 : 4; }
+
 struct Plan {
   cudaGraphExec_t exec = nullptr;
   int32_t *rt = nullptr;  // the captured step's own row table
@@ -86,10 +95,22 @@ struct dory_handle {
   float *h2 = nullptr, *h_last = nullptr;  // second hidden buffer (fused path), final rows
   int32_t *hctr = nullptr, *actr = nullptr;  // arrival counters of the fused kernels
   bool fused_ok = false;
+  // tensor-core projections: weight maps per layer ([0] q/k/v/g or gate/up, [1] o or down)
+  bool tc_ok = false;
+  std::vector<std::array<TcW, 2>> tcw;
+  TcW tc_head;
+  CUtensorMap xmap[3][2][5];  // activation rows (h, z, y) x (hi, lo) x tile rows 16..256
+  Emit em_h{}, em_z{}, em_y{};
+  CUtensorMap kvmap;          // f32 KV memory as [rows][hd] for the attention's tile copies
+  bool kv_tma = false;
+  int32_t *dev_err = nullptr;  // set by a kernel whose bounded wait expired
+  float *tc_ws = nullptr;
+  int32_t *tc_ctr = nullptr, *tc_err = nullptr;
   float *h = nullptr, *input = nullptr, *state = nullptr, *qkvg = nullptr, *z = nullptr, *out = nullptr,
         *mlp = nullptr, *logits = nullptr, *rope = nullptr, *part = nullptr, *kst = nullptr, *vst = nullptr;
   int32_t *d_ids = nullptr, *d_seq_pos = nullptr, *d_zero = nullptr;
   char *act = nullptr;
+  char *tcmem = nullptr;
 
   cudaStream_t cap_stream = nullptr;  // graphs are captured here and replayed on `stream`
   bool use_graphs = true;
@@ -172,7 +193,8 @@ void free_all(dory_t *d) {
   if (d->wmem) cudaFree(d->wmem);
   if (d->kvmem) cudaFree(d->kvmem);
   if (d->act) cudaFree(d->act);
-  d->wmem = d->kvmem = d->act = nullptr;
+  if (d->tcmem) cudaFree(d->tcmem);
+  d->wmem = d->kvmem = d->act = d->tcmem = nullptr;
 }
 
 int reset_seq(dory_t *d, int seq) {
@@ -240,6 +262,17 @@ void account(dory_t *d, const StepArgs &a) {
   d->st.kv_write_bytes = kw;
 }
 
+// 64-position blocks the attention of the step's rows covers: the most over the rows.
+int tma_splits(dory_t *d, const StepArgs &a, const Ring &ring) {
+  int nb = 1;
+  for (int r = 0; r < a.T; r++) {
+    const long p = (long)d->seq_pos[a.hseq[r]] + a.hoff[r];
+    const long lo = ring.window == INT_MAX ? 0 : std::max<long>(p + 1 - ring.window, 0);
+    nb = std::max<int>(nb, (int)(p / 64 - lo / 64 + 1));
+  }
+  return nb;
+}
+
 // Issue every launch of one step on stream s. `rt` holds the device row table: seq[Tmax],
 // off[Tmax], advance seq[Tmax], advance count[Tmax]. With fixed_splits the attention grids
 // cover the whole window whatever the positions (for replayed graphs).
@@ -260,9 +293,28 @@ int issue_step(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_splits, cud
   for (int r = 0; r < T; r++) pmax = std::max(pmax, (long)d->seq_pos[a.hseq[r]] + a.hoff[r]);
   const bool q8 = c.kv_quant == DORY_KV_Q8_2F;
 
+  const bool tc = d->tc_ok && T >= 5;
   CK(launch_embed_rope(d->d_ids, d->embed, d->wdtype, dm, rows, c.rope_theta_sliding, c.rope_theta_full, d->h,
-                       d->rope, s));
+                       d->rope, tc ? d->em_h : Emit{nullptr, nullptr}, s));
   nl++;
+  auto tcg = [&](const TcW &w, int xbuf, int rowsT, int t_base, float *Y, int ldy, EpiArgs ep) -> int {
+    TcGemm g;
+    g.tmW = w.map;
+    const int bi = bn_index(tc_tile_rows(rowsT));
+    g.tmXh = d->xmap[xbuf][0][bi];
+    g.tmXl = d->xmap[xbuf][1][bi];
+    g.N = w.N;
+    g.K = w.K;
+    g.splits = (rowsT + tc_tile_rows(rowsT) - 1) / tc_tile_rows(rowsT) > 1 ? 1 : w.splits;
+    g.pair_rows = w.pair;
+    g.ws = d->tc_ws;
+    g.ctr = d->tc_ctr;
+    g.err = d->tc_err;
+    CK(launch_tc_gemm(g, rowsT, t_base, Y, ldy, ep, true, s));
+    nl++;
+    ng++;
+    return DORY_OK;
+  };
   auto gemm = [&](const void *W, int N, int K, const float *X, int ldx, float *Y, int ldy, EpiArgs ep) -> int {
     CK(launch_gemm(W, d->wdtype, N, K, X, ldx, T, Y, ldy, ep, s));
     nl++;
@@ -277,36 +329,65 @@ int issue_step(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_splits, cud
       const bool rewrite = c.kv_mode == DORY_KV_LAST_LOOP && (L.rec || L.out) && loop_i > 0;
       Ring ring = d->ring(L.ordinal, sl);
       EpiArgs ep{EPI_STORE, nullptr, nullptr, 0};
-      if ((rc = gemm(L.wqkvg, ldq, dm.hidden, d->h, dm.hidden, d->qkvg, ldq, ep))) return rc;
+      if (tc) {
+        if ((rc = tcg(d->tcw[li][0], 0, T, 0, d->qkvg, ldq, ep))) return rc;
+      } else if ((rc = gemm(L.wqkvg, ldq, dm.hidden, d->h, dm.hidden, d->qkvg, ldq, ep))) {
+        return rc;
+      }
       CK(launch_prep(d->qkvg, ldq, dm, rows, d->rope, L.sliding ? 0 : 1, L.sq, ring, d->kst, d->vst, s));
       nl++;
       if (q8) {
         CK(launch_q8_append(d->kst, d->vst, kv_size, dm, rows, ring, rewrite ? 1 : 0, s));
         nl++;
       }
-      const long wmax = ring.window == INT_MAX ? (long)ring.cap : (long)ring.window;
+      const long wmax = ring.window == INT_MAX ? (long)ring.cap : std::min<long>(ring.window, ring.cap);
       const long keys = fixed_splits ? wmax : std::min<long>(wmax, pmax + 1);
       const int splits = (int)((keys + KEYS_PER_SPLIT - 1) / KEYS_PER_SPLIT);
       if (splits > d->max_splits) return fail(DORY_ERANGE, "attention needs %d splits (max %d)", splits, d->max_splits);
-      CK(launch_attention(d->qkvg, ldq, dm, rows, ring, splits, KEYS_PER_SPLIT, d->part, L.sg, d->z, s));
-      nl += 2;
-      CK(launch_rownorm(d->z, T, q_size, q_size, s));
+      if (d->kv_tma) {
+        const int tsp = fixed_splits ? attn_tma_splits(wmax) : tma_splits(d, a, ring);
+        CK(launch_attention_tma(d->kvmap, d->qkvg, ldq, dm, rows, ring, tsp, d->part, L.sg, d->z, d->actr, d->dev_err,
+                                true, s));
+        nl += 1;
+      } else if (tc) {
+        CK(launch_attention_fused(d->qkvg, ldq, dm, rows, ring, splits, KEYS_PER_SPLIT, d->part, L.sg, d->z, d->actr,
+                                  true, s));
+        nl += 1;
+      } else {
+        CK(launch_attention(d->qkvg, ldq, dm, rows, ring, splits, KEYS_PER_SPLIT, d->part, L.sg, d->z, s));
+        nl += 2;
+      }
+      CK(launch_rownorm(d->z, T, q_size, q_size, tc ? d->em_z : Emit{nullptr, nullptr}, s));
       nl++;
-      if ((rc = gemm(L.wo, dm.hidden, q_size, d->z, q_size, d->out, dm.hidden, ep))) return rc;
+      if (tc) {
+        if ((rc = tcg(d->tcw[li][1], 1, T, 0, d->out, dm.hidden, ep))) return rc;
+      } else if ((rc = gemm(L.wo, dm.hidden, q_size, d->z, q_size, d->out, dm.hidden, ep))) {
+        return rc;
+      }
     } else {
       EpiArgs ep{EPI_SILU, L.msg, L.msu, (long)dm.ffn};
-      if ((rc = gemm(L.wgu, dm.ffn, dm.hidden, d->h, dm.hidden, d->mlp, dm.ffn, ep))) return rc;
-      CK(launch_rownorm(d->mlp, T, dm.ffn, dm.ffn, s));
+      if (tc) {
+        if ((rc = tcg(d->tcw[li][0], 0, T, 0, d->mlp, dm.ffn, ep))) return rc;
+      } else if ((rc = gemm(L.wgu, dm.ffn, dm.hidden, d->h, dm.hidden, d->mlp, dm.ffn, ep))) {
+        return rc;
+      }
+      CK(launch_rownorm(d->mlp, T, dm.ffn, dm.ffn, tc ? d->em_y : Emit{nullptr, nullptr}, s));
       nl++;
       EpiArgs e2{EPI_STORE, nullptr, nullptr, 0};
-      if ((rc = gemm(L.wdown, dm.hidden, dm.ffn, d->mlp, dm.ffn, d->out, dm.hidden, e2))) return rc;
+      if (tc) {
+        if ((rc = tcg(d->tcw[li][1], 2, T, 0, d->out, dm.hidden, e2))) return rc;
+      } else if ((rc = gemm(L.wdown, dm.hidden, dm.ffn, d->mlp, dm.ffn, d->out, dm.hidden, e2))) {
+        return rc;
+      }
     }
-    CK(launch_residual(d->h, d->out, L.alpha, T, dm.hidden, mix, d->input, d->state, 1, s));
+    CK(launch_residual(d->h, d->out, L.alpha, T, dm.hidden, mix, d->input, d->state, 1,
+                       tc ? d->em_h : Emit{nullptr, nullptr}, s));
     nl++;
     return DORY_OK;
   };
   auto mix_only = [&](int mix) -> int {
-    CK(launch_residual(d->h, d->out, nullptr, T, dm.hidden, mix, d->input, d->state, 0, s));
+    CK(launch_residual(d->h, d->out, nullptr, T, dm.hidden, mix, d->input, d->state, 0,
+                       tc ? d->em_h : Emit{nullptr, nullptr}, s));
     nl++;
     return DORY_OK;
   };
@@ -326,10 +407,14 @@ int issue_step(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_splits, cud
     if ((rc = layer(li, 0, MIX_NONE))) return rc;
   if (a.head_rows > 0) {
     EpiArgs ep{EPI_SCALE, d->logit_scale, nullptr, 0};
-    CK(launch_gemm(d->head, d->wdtype, dm.vocab, dm.hidden, d->h + (size_t)a.head_from * dm.hidden, dm.hidden,
-                   a.head_rows, d->logits, dm.vocab, ep, s));
-    nl++;
-    ng++;
+    if (tc && a.head_rows >= 5) {
+      if ((rc = tcg(d->tc_head, 0, a.head_rows, a.head_from, d->logits, dm.vocab, ep))) return rc;
+    } else {
+      CK(launch_gemm(d->head, d->wdtype, dm.vocab, dm.hidden, d->h + (size_t)a.head_from * dm.hidden, dm.hidden,
+                     a.head_rows, d->logits, dm.vocab, ep, s));
+      nl++;
+      ng++;
+    }
   }
   CK(launch_advance(d->d_seq_pos, rt + 2 * d->Tmax, rt + 3 * d->Tmax, (int)a.aseq.size(), s));
   nl++;
@@ -360,7 +445,7 @@ int issue_step_fused(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_split
   for (int r = 0; r < T; r++) pmax = std::max(pmax, (long)d->seq_pos[a.hseq[r]] + a.hoff[r]);
   const bool q8 = c.kv_quant == DORY_KV_Q8_2F;
   CK(launch_embed_rope(d->d_ids, d->embed, d->wdtype, dm, rows, c.rope_theta_sliding, c.rope_theta_full, d->h,
-                       d->rope, s));
+                       d->rope, Emit{nullptr, nullptr}, s));
   nl++;
   float *cur = d->h, *other = d->h2;
   struct {
@@ -416,12 +501,18 @@ int issue_step_fused(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_split
         CK(launch_q8_append(d->kst, d->vst, kv_size, dm, rows, ring, rewrite ? 1 : 0, s));
         nl++;
       }
-      const long wmax = ring.window == INT_MAX ? (long)ring.cap : (long)ring.window;
+      const long wmax = ring.window == INT_MAX ? (long)ring.cap : std::min<long>(ring.window, ring.cap);
       const long keys = fixed_splits ? wmax : std::min<long>(wmax, pmax + 1);
       const int splits = (int)((keys + KEYS_PER_SPLIT - 1) / KEYS_PER_SPLIT);
       if (splits > d->max_splits) return fail(DORY_ERANGE, "attention needs %d splits (max %d)", splits, d->max_splits);
-      CK(launch_attention_fused(d->qkvg, ldq, dm, rows, ring, splits, KEYS_PER_SPLIT, d->part, L.sg, d->z, d->actr,
+      if (d->kv_tma) {
+        const int tsp = fixed_splits ? attn_tma_splits(wmax) : tma_splits(d, a, ring);
+        CK(launch_attention_tma(d->kvmap, d->qkvg, ldq, dm, rows, ring, tsp, d->part, L.sg, d->z, d->actr, d->dev_err,
                                 true, s));
+      } else {
+        CK(launch_attention_fused(d->qkvg, ldq, dm, rows, ring, splits, KEYS_PER_SPLIT, d->part, L.sg, d->z, d->actr,
+                                  true, s));
+      }
       nl++;
       GemvIn in{};
       in.mode = IN_NORM;
@@ -465,7 +556,8 @@ int issue_step_fused(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_split
     nl++;
     ng++;
   } else {
-    CK(launch_residual(cur, d->out, pend.alpha, T, dm.hidden, pend.mix, d->input, d->state, 1, s));
+    CK(launch_residual(cur, d->out, pend.alpha, T, dm.hidden, pend.mix, d->input, d->state, 1,
+                       Emit{nullptr, nullptr}, s));
     nl++;
     pend.on = false;
     if (a.head_rows > 0) {
@@ -554,6 +646,94 @@ int do_step(dory_t *d, const StepArgs &a, const int32_t *ids) {
   account(d, a);
   for (size_t i = 0; i < a.aseq.size(); i++) d->seq_pos[a.aseq[i]] += a.acnt[i];
   d->last_rows = a.T;
+  return DORY_OK;
+}
+
+
+// Tensor maps, split counts and buffers of the tensor-core projections (bf16 weights).
+int setup_tc(dory_t *d) {
+  const Dims dm = d->dims;
+  const int q_size = dm.nh * dm.hd, kv_size = dm.nk * dm.hd, ldq = 2 * q_size + 2 * kv_size;
+  {
+    const char *e = getenv("DORY_TC");
+    if (e && e[0] == '0') return DORY_OK;
+  }
+  if (d->wdtype != W_BF16 || dm.hidden % 64 || dm.ffn % 64 || q_size % 64) return DORY_OK;
+  int dev = 0, sms = 148;
+  CK(cudaGetDevice(&dev));
+  CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  const int bn_max = tc_tile_rows(d->Tmax);
+  size_t ws_floats = 0;
+  int max_tiles = 1;
+  auto mk = [&](TcW &w, const void *base, long rows, int K, int N, long pair) -> int {
+    if (make_tmap_bf16(&w.map, base, rows, K, 128)) return fail(DORY_ECUDA, "tensor map of a weight matrix");
+    w.N = N;
+    w.K = K;
+    w.pair = pair;
+    const int mt = (N + 127) / 128, nkb = K / 64;
+    w.splits = std::max(1, std::min(std::min(2 * sms / mt, 8), nkb));
+    const int t_tiles = (d->Tmax + bn_max - 1) / bn_max;
+    ws_floats = std::max(ws_floats, (size_t)mt * t_tiles * w.splits * (pair ? 2 : 1) * bn_max * 128);
+    max_tiles = std::max(max_tiles, mt * t_tiles);
+    return DORY_OK;
+  };
+  d->tcw.assign(d->layers.size(), {});
+  int rc;
+  for (size_t li = 0; li < d->layers.size(); li++) {
+    const LayerDev &L = d->layers[li];
+    if (L.attn) {
+      if ((rc = mk(d->tcw[li][0], L.wqkvg, ldq, dm.hidden, ldq, 0))) return rc;
+      if ((rc = mk(d->tcw[li][1], L.wo, dm.hidden, q_size, dm.hidden, 0))) return rc;
+    } else {
+      if ((rc = mk(d->tcw[li][0], L.wgu, 2L * dm.ffn, dm.hidden, dm.ffn, dm.ffn))) return rc;
+      if ((rc = mk(d->tcw[li][1], L.wdown, dm.hidden, dm.ffn, dm.hidden, 0))) return rc;
+    }
+  }
+  if ((rc = mk(d->tc_head, d->head, dm.vocab, dm.hidden, dm.vocab, 0))) return rc;
+  const int XR = std::max(d->Tmax, 256);
+  const int widths[3] = {dm.hidden, q_size, dm.ffn};
+  size_t off = 0, offs[3][2];
+  for (int b = 0; b < 3; b++)
+    for (int h = 0; h < 2; h++) {
+      offs[b][h] = off;
+      off = align256(off + (size_t)XR * widths[b] * 2);
+    }
+  const size_t o_ws = off;
+  off = align256(off + ws_floats * 4);
+  const size_t o_ctr = off;
+  off = align256(off + (size_t)max_tiles * 4);
+  const size_t o_err = off;
+  off = align256(off + 4);
+  if (cudaMalloc(&d->tcmem, off) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(DORY_ENOMEM, "cudaMalloc of %zu tensor-core bytes", off);
+  }
+  CK(cudaMemset(d->tcmem, 0, off));
+  __nv_bfloat16 *buf[3][2];
+  for (int b = 0; b < 3; b++)
+    for (int h = 0; h < 2; h++) {
+      buf[b][h] = reinterpret_cast<__nv_bfloat16 *>(d->tcmem + offs[b][h]);
+      for (int bi = 0; bi < 5; bi++)
+        if (make_tmap_bf16(&d->xmap[b][h][bi], buf[b][h], XR, widths[b], 16 << bi))
+          return fail(DORY_ECUDA, "tensor map of an activation buffer");
+    }
+  d->em_h = Emit{buf[0][0], buf[0][1]};
+  d->em_z = Emit{buf[1][0], buf[1][1]};
+  d->em_y = Emit{buf[2][0], buf[2][1]};
+  d->tc_ws = reinterpret_cast<float *>(d->tcmem + o_ws);
+  d->tc_ctr = reinterpret_cast<int32_t *>(d->tcmem + o_ctr);
+  d->tc_err = d->dev_err;
+  (void)o_err;
+  d->tc_ok = true;
+  return DORY_OK;
+}
+
+// A bounded wait in a tensor-core GEMM expired during the last calls.
+int check_device_error(dory_t *d) {
+  if (!d->dev_err) return DORY_OK;
+  int32_t e = 0;
+  CK(cudaMemcpy(&e, d->dev_err, 4, cudaMemcpyDeviceToHost));
+  if (e) return fail(DORY_ECUDA, "a kernel gave up waiting for its copies or MMAs (code %d)", e);
   return DORY_OK;
 }
 
@@ -698,22 +878,29 @@ int dory_create(const dory_config *cfg, const dory_weights *w, void *stream, dor
       o.cap = cfg->max_context;
       o.window = INT_MAX;
     }
+    o.cap = (o.cap + 63) / 64 * 64;  // whole 64-row blocks: a block of positions is contiguous in the ring
     o.slots = (cfg->kv_mode == DORY_KV_PER_LOOP && L.rec) ? cfg->max_loops : 1;
     o.L = slot_layout(o.cap, dm.nk, dm.hd, q8);
     o.off = sb;
-    sb = align256(sb + (size_t)o.slots * o.L.bytes);
+    sb = (sb + (size_t)o.slots * o.L.bytes + 1023) & ~(size_t)1023;
     d->slot_index[L.ordinal] = flat;
     flat += o.slots;
-    const long keys = o.window == INT_MAX ? (long)o.cap : (long)o.window;
+    const long keys = o.window == INT_MAX ? (long)o.cap : std::min<long>(o.window, o.cap);
     d->max_splits = std::max<int>(d->max_splits, (int)((keys + KEYS_PER_SPLIT - 1) / KEYS_PER_SPLIT));
+    d->max_splits = std::max<int>(d->max_splits, attn_tma_splits(keys));
   }
   d->n_flat_slots = flat;
-  d->seq_stride = std::max<size_t>(sb, 256);
+  d->seq_stride = std::max<size_t>(sb, 1024);
   d->kv_bytes = d->seq_stride * cfg->max_seqs;
   if (cudaMalloc(&d->kvmem, d->kv_bytes) != cudaSuccess) {
     cudaGetLastError();
     fail(DORY_ENOMEM, "cudaMalloc of %zu KV bytes", d->kv_bytes);
     return cleanup(DORY_ENOMEM);
+  }
+
+  if (!q8) {
+    const char *e = getenv("DORY_KV_TMA");
+    d->kv_tma = !(e && e[0] == '0') && make_tmap_kv_f32(&d->kvmap, d->kvmem, d->kv_bytes, dm.hd) == 0;
   }
 
   // ---- activations ---------------------------------------------------------------------
@@ -737,7 +924,7 @@ int dory_create(const dory_config *cfg, const dory_weights *w, void *stream, dor
                a_kst = areserve((size_t)T * kv_size * 4), a_vst = areserve((size_t)T * kv_size * 4),
                a_ids = areserve((size_t)T * 4),
                a_sp = areserve((size_t)cfg->max_seqs * 4), a_rows = areserve((size_t)4 * T * 4),
-               a_zero = areserve((size_t)cfg->max_seqs * 4);
+               a_zero = areserve((size_t)cfg->max_seqs * 4), a_err = areserve(256);
   if (cudaMalloc(&d->act, ab) != cudaSuccess) {
     cudaGetLastError();
     fail(DORY_ENOMEM, "cudaMalloc of %zu activation bytes", ab);
@@ -772,6 +959,7 @@ int dory_create(const dory_config *cfg, const dory_weights *w, void *stream, dor
   d->d_seq_pos = reinterpret_cast<int32_t *>(A + a_sp);
   d->d_rows = reinterpret_cast<int32_t *>(A + a_rows);
   d->d_zero = reinterpret_cast<int32_t *>(A + a_zero);
+  d->dev_err = reinterpret_cast<int32_t *>(A + a_err);
   if (cudaMemsetAsync(d->act, 0, ab, d->stream) != cudaSuccess) return cleanup(fail(DORY_ECUDA, "memset"));
 
   {
@@ -780,6 +968,7 @@ int dory_create(const dory_config *cfg, const dory_weights *w, void *stream, dor
   }
   if (cudaStreamCreateWithFlags(&d->cap_stream, cudaStreamNonBlocking) != cudaSuccess)
     return cleanup(fail(DORY_ECUDA, "stream create"));
+  if ((rc = setup_tc(d))) return cleanup(rc);
   d->seq_pos.assign(cfg->max_seqs, 0);
   d->appended.assign((size_t)cfg->max_seqs * d->n_flat_slots, 0);
   for (int s = 0; s < cfg->max_seqs; s++)
@@ -882,7 +1071,7 @@ int dory_logits(dory_t *d, int32_t row, float *dst, size_t cap) {
   CK(cudaMemcpyAsync(dst, d->logits + (size_t)row * d->dims.vocab, (size_t)d->dims.vocab * 4, cudaMemcpyDefault,
                      d->stream));
   CK(cudaStreamSynchronize(d->stream));
-  return DORY_OK;
+  return check_device_error(d);
 }
 
 int dory_logits_device(dory_t *d, const float **out, int32_t *rows) {
@@ -898,7 +1087,7 @@ int dory_read_hidden(dory_t *d, float *dst, size_t cap) {
   if (cap < n) return fail(DORY_EINVAL, "cap %zu < %zu", cap, n);
   CK(cudaMemcpyAsync(dst, d->h_last, n * 4, cudaMemcpyDefault, d->stream));
   CK(cudaStreamSynchronize(d->stream));
-  return DORY_OK;
+  return check_device_error(d);
 }
 
 int dory_slot_info(dory_t *d, int32_t ordinal, int32_t *cap, int32_t *slots, int32_t *sliding) {

@@ -7,14 +7,16 @@
 
 namespace dory {
 
-static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+static size_t align1k(size_t x) { return (x + 1023) & ~(size_t)1023; }
 
+// Every sub-array starts on a 1024-byte boundary, so a ring row of hd f32 values sits at a
+// whole row index of the KV memory seen as [rows][hd] (the attention's tensor map).
 SlotLayout slot_layout(int cap, int nk, int hd, bool q8) {
   SlotLayout L = {};
   size_t o = 0;
   auto take = [&](size_t bytes) {
     size_t at = o;
-    o = align256(o + bytes);
+    o = align1k(o + bytes);
     return at;
   };
   const size_t rows = (size_t)nk * cap;
@@ -42,21 +44,38 @@ SlotLayout slot_layout(int cap, int nk, int hd, bool q8) {
 
 namespace {
 
+__device__ __forceinline__ void emit(const Emit &em, size_t i, float x) {
+  if (em.hi) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(x);
+    em.hi[i] = h;
+    em.lo[i] = __float2bfloat16_rn(x - __bfloat162float(h));
+  }
+}
+
+__device__ __forceinline__ void pdl_trigger_() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // h[r] = E[id] (zero for an id outside the vocabulary: dory.rs fn forward_host leaves the
 // row at zero), and the row's RoPE table for both layer kinds: angle pos*inv[j] in f64,
 // inv[j] = theta^(-2j/hd) rounded to f32, cos/sin stored as f32 (dory.rs fn stack).
 template <typename WT>
 __global__ void embed_rope_kernel(const int32_t *__restrict__ ids, const WT *__restrict__ E, Dims d, Rows rows,
                                   double theta_s, double theta_f, float *__restrict__ h,
-                                  float *__restrict__ rope) {
+                                  float *__restrict__ rope, Emit em) {
   const int r = blockIdx.x;
   const int id = ids[r];
   float *hr = h + (size_t)r * d.hidden;
   if (id >= 0 && id < d.vocab) {
     const WT *er = E + (size_t)id * d.hidden;
-    for (int i = threadIdx.x; i < d.hidden; i += blockDim.x) hr[i] = load_w(er, i);
+    for (int i = threadIdx.x; i < d.hidden; i += blockDim.x) {
+      const float x = load_w(er, i);
+      hr[i] = x;
+      emit(em, (size_t)r * d.hidden + i, x);
+    }
   } else {
-    for (int i = threadIdx.x; i < d.hidden; i += blockDim.x) hr[i] = 0.f;
+    for (int i = threadIdx.x; i < d.hidden; i += blockDim.x) {
+      hr[i] = 0.f;
+      emit(em, (size_t)r * d.hidden + i, 0.f);
+    }
   }
   const int half = d.hd / 2;
   const long pos = (long)rows.seq_pos[rows.seq[r]] + rows.off[r];
@@ -80,6 +99,7 @@ __global__ void prep_kernel(float *__restrict__ qkvg, int ldq, Dims d, Rows rows
                             int kind, const float *__restrict__ sq, Ring ring, float *__restrict__ kst,
                             float *__restrict__ vst) {
   __shared__ float red[32];
+  pdl_trigger_();
   const int r = blockIdx.x, head = blockIdx.y;
   const int half = d.hd / 2;
   const bool is_q = head < d.nh;
@@ -133,14 +153,19 @@ __global__ void prep_kernel(float *__restrict__ qkvg, int ldq, Dims d, Rows rows
 }
 
 // x / sqrt(sum x^2 + eps) per row, in place (dory.rs fn justnorm).
-__global__ void rownorm_kernel(float *__restrict__ x, int width, int ld) {
+__global__ void rownorm_kernel(float *__restrict__ x, int width, int ld, Emit em) {
   __shared__ float red[32];
+  pdl_trigger_();
   float *row = x + (size_t)blockIdx.x * ld;
   float s = 0.f;
   for (int i = threadIdx.x; i < width; i += blockDim.x) s += row[i] * row[i];
   s = block_sum(s, red);
   const float inv = 1.f / sqrtf(s + DORY_EPS);
-  for (int i = threadIdx.x; i < width; i += blockDim.x) row[i] *= inv;
+  for (int i = threadIdx.x; i < width; i += blockDim.x) {
+    const float v = row[i] * inv;
+    row[i] = v;
+    emit(em, (size_t)blockIdx.x * width + i, v);
+  }
 }
 
 // The nGPT residual (dory.rs fn slerp) and the loop mix that follows the input block
@@ -150,8 +175,9 @@ __global__ void rownorm_kernel(float *__restrict__ x, int width, int ld) {
 template <int MAXV>
 __global__ void residual_kernel(float *__restrict__ h, const float *__restrict__ out,
                                 const float *__restrict__ alpha, int hidden, int mix, float *__restrict__ input,
-                                float *__restrict__ state, int do_residual) {
+                                float *__restrict__ state, int do_residual, Emit em) {
   __shared__ float red[32];
+  pdl_trigger_();
   const int r = blockIdx.x;
   float *hr = h + (size_t)r * hidden;
   const float *orow = out + (size_t)r * hidden;
@@ -232,7 +258,10 @@ __global__ void residual_kernel(float *__restrict__ h, const float *__restrict__
 #pragma unroll
   for (int i = 0; i < MAXV; i++) {
     const int c = threadIdx.x + i * blockDim.x;
-    if (i < nper && c < hidden) hr[c] = x[i];
+    if (i < nper && c < hidden) {
+      hr[c] = x[i];
+      emit(em, (size_t)r * hidden + c, x[i]);
+    }
   }
 }
 
@@ -263,13 +292,13 @@ __global__ void ring_write_f32_kernel(const float *__restrict__ k, const float *
 }  // namespace
 
 cudaError_t launch_embed_rope(const int32_t *ids, const void *E, int wdtype, Dims d, Rows rows, double theta_s,
-                              double theta_f, float *h, float *rope, cudaStream_t s) {
+                              double theta_f, float *h, float *rope, Emit em, cudaStream_t s) {
   if (wdtype == W_BF16)
     embed_rope_kernel<__nv_bfloat16><<<rows.n, 256, 0, s>>>(ids, static_cast<const __nv_bfloat16 *>(E), d, rows,
-                                                             theta_s, theta_f, h, rope);
+                                                             theta_s, theta_f, h, rope, em);
   else
     embed_rope_kernel<float><<<rows.n, 256, 0, s>>>(ids, static_cast<const float *>(E), d, rows, theta_s, theta_f,
-                                                     h, rope);
+                                                     h, rope, em);
   return cudaGetLastError();
 }
 
@@ -281,19 +310,19 @@ cudaError_t launch_prep(float *qkvg, int ldq, Dims d, Rows rows, const float *ro
   return cudaGetLastError();
 }
 
-cudaError_t launch_rownorm(float *x, int T, int width, int ld, cudaStream_t s) {
-  rownorm_kernel<<<T, 512, 0, s>>>(x, width, ld);
+cudaError_t launch_rownorm(float *x, int T, int width, int ld, Emit em, cudaStream_t s) {
+  rownorm_kernel<<<T, 512, 0, s>>>(x, width, ld, em);
   return cudaGetLastError();
 }
 
 cudaError_t launch_residual(float *h, const float *out, const float *alpha, int T, int hidden, int mix, float *input,
-                            float *state, int do_residual, cudaStream_t s) {
+                            float *state, int do_residual, Emit em, cudaStream_t s) {
   const int threads = 512;
   const int nper = (hidden + threads - 1) / threads;
   if (nper <= 4)
-    residual_kernel<4><<<T, threads, 0, s>>>(h, out, alpha, hidden, mix, input, state, do_residual);
+    residual_kernel<4><<<T, threads, 0, s>>>(h, out, alpha, hidden, mix, input, state, do_residual, em);
   else if (nper <= 16)
-    residual_kernel<16><<<T, threads, 0, s>>>(h, out, alpha, hidden, mix, input, state, do_residual);
+    residual_kernel<16><<<T, threads, 0, s>>>(h, out, alpha, hidden, mix, input, state, do_residual, em);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();

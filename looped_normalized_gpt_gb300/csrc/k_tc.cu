@@ -1,0 +1,403 @@
+// Tensor-core projections for steps of 5 or more rows on sm_103a (tcgen05 + TMEM + TMA).
+//
+// Y[t][n] = sum_k W[n][k] X[t][k] with W bf16 [N][K] (weights stream from HBM) and X the
+// step's activation rows, held as two bf16 halves X = Xhi + Xlo (Xhi = bf16(X),
+// Xlo = bf16(X - Xhi)) so the product keeps about 16 mantissa bits of the activations.
+// Swap-AB: the MMA's M side is 128 weight rows, its N side the step's rows (a tile of BN
+// rows, 16 <= BN <= 256), K steps of 16.
+//
+// Block roles (192 threads): warp 0 lane 0 drives TMA (128B-swizzled tiles into a ring of
+// shared-memory stages, completion on mbarriers), warp 1 allocates TMEM and lane 0 issues
+// tcgen05.mma (two per K step: Xhi and Xlo; gate and up for SwiGLU) and tcgen05.commit,
+// warps 2..5 read the accumulator back with tcgen05.ld. K is split over blocks when the
+// weight tiles alone would not fill the GPU; each split writes its fp32 partial tile to a
+// workspace and the last split block of a tile (an arrival counter) adds them in split
+// order and applies the epilogue (plain, logit scale, or SwiGLU).
+//
+// Every mbarrier wait is bounded: on expiry the block records an error code, stops
+// issuing work, waits (bounded) for its own copies and MMAs, frees TMEM and returns.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace dory {
+
+namespace {
+
+constexpr int TC_THREADS = 192;
+constexpr int BM = 128;  // weight rows per tile (MMA M)
+constexpr int BK = 64;   // K elements per stage (one 128-byte swizzle row)
+constexpr uint32_t WAIT_LIMIT = 1u << 20;
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+// Wait for the phase with the given parity to complete; false after the bound.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  for (uint32_t i = 0; i < WAIT_LIMIT; i++) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (ok) return true;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+
+// tcgen05 shared-memory matrix descriptor: K-major operand in 128-byte swizzled rows,
+// 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr & 0x3FFFF) >> 4);
+  d |= (uint64_t)1 << 16;             // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;   // stride byte offset: 8 rows x 128 B
+  d |= (uint64_t)1 << 46;             // descriptor version
+  d |= (uint64_t)2 << 61;             // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor of kind::f16: bf16 x bf16 -> f32, both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
+          tmem_d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; i++) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+template <int BN, bool DUAL, int ST>
+struct TcSmem {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE = A_BYTES * (DUAL ? 2 : 1) + 2 * B_BYTES;  // A (gate, up), B hi and lo
+  static constexpr int TOTAL = ST * STAGE + 1024;                     // + alignment slack
+  static constexpr int TMEM_COLS = (DUAL ? 2 : 1) * BN <= 32    ? 32
+                                   : (DUAL ? 2 : 1) * BN <= 64  ? 64
+                                   : (DUAL ? 2 : 1) * BN <= 128 ? 128
+                                   : (DUAL ? 2 : 1) * BN <= 256 ? 256
+                                                                : 512;
+};
+
+template <int BN, bool DUAL, int ST>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmXh,
+                   const __grid_constant__ CUtensorMap tmXl, int N, int K, int T, int t_base, int splits,
+                   long pair_rows, float *__restrict__ ws, int *__restrict__ tile_ctr, float *__restrict__ Y, int ldy,
+                   EpiArgs ep, int *__restrict__ err) {
+  using S = TcSmem<BN, DUAL, ST>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bar_full[ST], bar_empty[ST], bar_acc;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int is_last, failed;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile = blockIdx.x / splits, split = blockIdx.x % splits;
+  const int n0 = tile * BM;
+  const int t0 = blockIdx.y * BN;
+  const int nkb = K / BK;
+  const int kb0 = (int)((long)nkb * split / splits), kb1 = (int)((long)nkb * (split + 1) / splits);
+  const int nk = kb1 - kb0;
+  const uint32_t base = (smem_u32(smem_raw) + 1023) & ~1023u;
+  auto a_addr = [&](int s, int half) { return base + s * S::STAGE + half * S::A_BYTES; };
+  auto b_addr = [&](int s, int lo) {
+    return base + s * S::STAGE + (DUAL ? 2 : 1) * S::A_BYTES + lo * S::B_BYTES;
+  };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < ST; s++) {
+      mbar_init(smem_u32(&bar_full[s]), 1);
+      mbar_init(smem_u32(&bar_empty[s]), 1);
+    }
+    mbar_init(smem_u32(&bar_acc), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    failed = 0;
+    is_last = 0;
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base_sh)),
+                 "r"(S::TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  const uint32_t tx = (uint32_t)(S::A_BYTES * (DUAL ? 2 : 1) + 2 * S::B_BYTES);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // weight tiles do not depend on earlier kernels: issue the first stages' before the wait
+      const int pre = nk < ST ? nk : ST;
+      for (int i = 0; i < pre; i++) {
+        const uint32_t fb = smem_u32(&bar_full[i]);
+        mbar_expect_tx(fb, tx);
+        const int kc = (kb0 + i) * BK;
+        tma_load_2d(a_addr(i, 0), &tmW, kc, n0, fb);
+        if (DUAL) tma_load_2d(a_addr(i, 1), &tmW, kc, (int)(n0 + pair_rows), fb);
+      }
+      pdl_wait();
+      for (int i = 0; i < pre; i++) {
+        const uint32_t fb = smem_u32(&bar_full[i]);
+        const int kc = (kb0 + i) * BK;
+        tma_load_2d(b_addr(i, 0), &tmXh, kc, t_base + t0, fb);
+        tma_load_2d(b_addr(i, 1), &tmXl, kc, t_base + t0, fb);
+      }
+      for (int i = pre; i < nk; i++) {
+        const int s = i % ST;
+        if (!mbar_wait(smem_u32(&bar_empty[s]), ((i / ST) - 1) & 1)) {
+          atomicExch(err, 1);
+          failed = 1;
+          break;
+        }
+        const uint32_t fb = smem_u32(&bar_full[s]);
+        mbar_expect_tx(fb, tx);
+        const int kc = (kb0 + i) * BK;
+        tma_load_2d(a_addr(s, 0), &tmW, kc, n0, fb);
+        if (DUAL) tma_load_2d(a_addr(s, 1), &tmW, kc, (int)(n0 + pair_rows), fb);
+        tma_load_2d(b_addr(s, 0), &tmXh, kc, t_base + t0, fb);
+        tma_load_2d(b_addr(s, 1), &tmXl, kc, t_base + t0, fb);
+      }
+    }
+  } else if (warp == 1) {
+    pdl_wait();
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(BM, BN);
+      for (int i = 0; i < nk; i++) {
+        const int s = i % ST;
+        if (!mbar_wait(smem_u32(&bar_full[s]), (i / ST) & 1)) {
+          atomicExch(err, 2);
+          failed = 1;
+          break;
+        }
+        fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; kk++) {
+          const uint64_t ad = sw128_desc(a_addr(s, 0) + kk * 32);
+          const uint64_t bh = sw128_desc(b_addr(s, 0) + kk * 32);
+          const uint64_t bl = sw128_desc(b_addr(s, 1) + kk * 32);
+          const uint32_t first = (i == 0 && kk == 0) ? 0u : 1u;
+          mma_bf16(tmem, ad, bh, idesc, first);
+          mma_bf16(tmem, ad, bl, idesc, 1u);
+          if (DUAL) {
+            const uint64_t au = sw128_desc(a_addr(s, 1) + kk * 32);
+            mma_bf16(tmem + BN, au, bh, idesc, first);
+            mma_bf16(tmem + BN, au, bl, idesc, 1u);
+          }
+        }
+        mma_commit(smem_u32(&bar_empty[s]));
+      }
+      mma_commit(smem_u32(&bar_acc));
+    }
+  } else {
+    pdl_wait();
+  }
+  pdl_trigger();
+
+  // epilogue: warps 2..5, warp w reads TMEM lanes 32*(w % 4) ..
+  if (warp >= 2) {
+    const int q = warp & 3;
+    const int m = q * 32 + lane;  // row within the tile
+    const int n = n0 + m;
+    bool ok = mbar_wait(smem_u32(&bar_acc), 0);
+    if (!ok) {
+      atomicExch(err, 3);
+      failed = 1;
+    }
+    fence_after();
+    const int tcount = (T - t0) < BN ? (T - t0) : BN;  // valid step rows in this tile
+    float *wsp = ws + ((size_t)(tile * gridDim.y + blockIdx.y) * splits + split) * (DUAL ? 2 : 1) * BN * BM;
+    if (ok && !failed) {
+      for (int c = 0; c < BN; c += 16) {
+        float v[16], u[16];
+        tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + c, v);
+        if (DUAL) tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + BN + c, u);
+        if (splits == 1) {
+#pragma unroll
+          for (int i = 0; i < 16; i++) {
+            const int t = c + i;
+            if (t < tcount && n < N) {
+              float y = v[i];
+              if (ep.mode == EPI_SCALE) {
+                y = v[i] * ep.vec[n];
+              } else if (ep.mode == EPI_SILU) {
+                const float g = v[i] * ep.vec[n];
+                y = g * sigmoidf_(g) * (u[i] * ep.vec2[n]);
+              }
+              Y[(size_t)(t0 + t) * ldy + n] = y;
+            }
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; i++) {
+            wsp[(size_t)(c + i) * BM + m] = v[i];
+            if (DUAL) wsp[(size_t)(BN + c + i) * BM + m] = u[i];
+          }
+        }
+      }
+    }
+    if (splits > 1) {
+      __threadfence();
+      epi_bar();
+      if (warp == 2 && lane == 0) {
+        int *ctr = tile_ctr + tile * gridDim.y + blockIdx.y;
+        const int old = atomicAdd(ctr, 1);
+        is_last = old == splits - 1;
+        if (is_last) *ctr = 0;
+      }
+      epi_bar();
+      if (is_last) {
+        __threadfence();
+        const float *w0 = ws + (size_t)(tile * gridDim.y + blockIdx.y) * splits * (DUAL ? 2 : 1) * BN * BM;
+        for (int t = 0; t < tcount; t++) {
+          float a = 0.f, b = 0.f;
+          for (int sp = 0; sp < splits; sp++) {
+            const float *p = w0 + (size_t)sp * (DUAL ? 2 : 1) * BN * BM;
+            a += __ldcg(p + (size_t)t * BM + m);
+            if (DUAL) b += __ldcg(p + (size_t)(BN + t) * BM + m);
+          }
+          if (n < N) {
+            float y = a;
+            if (ep.mode == EPI_SCALE) {
+              y = a * ep.vec[n];
+            } else if (ep.mode == EPI_SILU) {
+              const float g = a * ep.vec[n];
+              y = g * sigmoidf_(g) * (b * ep.vec2[n]);
+            }
+            Y[(size_t)(t0 + t) * ldy + n] = y;
+          }
+        }
+      }
+    }
+  }
+  fence_before();
+  __syncthreads();
+  if (failed && threadIdx.x == 64) {
+    // let copies and MMAs already issued land before TMEM is freed
+    mbar_wait(smem_u32(&bar_acc), 0);
+  }
+  __syncthreads();
+  fence_after();
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(S::TMEM_COLS) : "memory");
+}
+
+template <int BN, bool DUAL, int ST>
+cudaError_t tc_launch(const TcGemm &g, int T, int t_base, float *Y, int ldy, EpiArgs ep, bool pdl, cudaStream_t s) {
+  using S = TcSmem<BN, DUAL, ST>;
+  auto kern = tc_gemm_kernel<BN, DUAL, ST>;
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::TOTAL);
+    attr = true;
+  }
+  const int m_tiles = (g.N + BM - 1) / BM;
+  const int t_tiles = (T + BN - 1) / BN;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(m_tiles * g.splits, t_tiles);
+  cfg.blockDim = dim3(TC_THREADS);
+  cfg.dynamicSmemBytes = S::TOTAL;
+  cfg.stream = s;
+  cudaLaunchAttribute attr1[1];
+  attr1[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr1[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr1;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, g.tmW, g.tmXh, g.tmXl, g.N, g.K, T, t_base, g.splits, g.pair_rows, g.ws,
+                            g.ctr, Y, ldy, ep, g.err);
+}
+
+}  // namespace
+
+int tc_tile_rows(int T) {
+  if (T <= 16) return 16;
+  if (T <= 32) return 32;
+  if (T <= 64) return 64;
+  if (T <= 128) return 128;
+  return 256;
+}
+
+cudaError_t launch_tc_gemm(const TcGemm &g, int T, int t_base, float *Y, int ldy, EpiArgs ep, bool pdl,
+                           cudaStream_t s) {
+  const bool dual = ep.mode == EPI_SILU;
+  const int bn = tc_tile_rows(T);
+#define TCL(B, D, ST)                                                      \
+  if (bn == B && dual == D) return tc_launch<B, D, ST>(g, T, t_base, Y, ldy, ep, pdl, s);
+  TCL(16, false, 4) TCL(32, false, 4) TCL(64, false, 3) TCL(128, false, 3) TCL(256, false, 2)
+  TCL(16, true, 4) TCL(32, true, 3) TCL(64, true, 2) TCL(128, true, 2) TCL(256, true, 1)
+#undef TCL
+  return cudaErrorInvalidValue;
+}
+
+// Tensor map of a row-major bf16 matrix [rows][cols] read in boxes of box_rows x 64.
+int make_tmap_bf16(CUtensorMap *map, const void *base, long rows, long cols, int box_rows) {
+  typedef CUresult (*EncodeTiled)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  static EncodeTiled encode = nullptr;
+  if (!encode) {
+    cudaDriverEntryPointQueryResult q;
+    void *fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return -1;
+    encode = reinterpret_cast<EncodeTiled>(fn);
+  }
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : -2;
+}
+
+}  // namespace dory

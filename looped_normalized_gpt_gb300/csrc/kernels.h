@@ -2,6 +2,8 @@
 // sizes and the small structs below; every launch goes on the given stream.
 #pragma once
 
+#include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -60,8 +62,14 @@ struct Dims {
 
 // --- launches -------------------------------------------------------------------------
 
+// Rows kept as f32 and, for the tensor-core projections, as two bf16 halves
+// (hi = bf16(x), lo = bf16(x - hi)); hi/lo may be null.
+struct Emit {
+  __nv_bfloat16 *hi, *lo;
+};
+
 cudaError_t launch_embed_rope(const int32_t *ids, const void *E, int wdtype, Dims d, Rows rows,
-                              double theta_s, double theta_f, float *h, float *rope, cudaStream_t s);
+                              double theta_s, double theta_f, float *h, float *rope, Emit em, cudaStream_t s);
 
 cudaError_t launch_gemm(const void *W, int wdtype, int N, int K, const float *X, int ldx, int T, float *Y,
                         int ldy, EpiArgs ep, cudaStream_t s);
@@ -84,13 +92,13 @@ cudaError_t launch_q8_append_frozen(const float *kst, const float *vst, int n, D
 cudaError_t launch_attention(const float *qkvg, int ldq, Dims d, Rows rows, Ring ring, int splits, int keys_per_split,
                              float *part, const float *sg, float *z, cudaStream_t s);
 
-cudaError_t launch_rownorm(float *x, int T, int width, int ld, cudaStream_t s);
+cudaError_t launch_rownorm(float *x, int T, int width, int ld, Emit em, cudaStream_t s);
 
 enum Mix { MIX_NONE = 0, MIX_BEGIN = 1, MIX_LOOP = 2, MIX_END = 3 };
 
 // x = (x^ + alpha (out^ - x^))^ per row, then the loop mix (dory.rs fn stack).
 cudaError_t launch_residual(float *h, const float *out, const float *alpha, int T, int hidden, int mix,
-                            float *input, float *state, int do_residual, cudaStream_t s);
+                            float *input, float *state, int do_residual, Emit em, cudaStream_t s);
 
 // ---- fused decode path (up to 4 rows) -------------------------------------------------
 
@@ -130,6 +138,31 @@ cudaError_t launch_gemv_fused(const void *W, int wdtype, int N, int K, int T, Ge
 
 cudaError_t launch_attention_fused(const float *qkvg, int ldq, Dims d, Rows rows, Ring ring, int splits, int kps,
                                    float *part, const float *sg, float *z, int *counters, bool pdl, cudaStream_t s);
+
+// ---- tensor-core projections (tcgen05) for steps of 5+ rows ----------------------------
+
+struct TcGemm {
+  CUtensorMap tmW;          // W bf16 [rows][K], boxes of 128 x 64
+  CUtensorMap tmXh, tmXl;   // activation halves bf16 [rows][K], boxes of BN x 64
+  int N, K, splits;
+  long pair_rows;           // SwiGLU: offset of the up rows in W
+  float *ws;                // split-K partial tiles
+  int *ctr;                 // per-tile arrival counters (zero between launches)
+  int *err;                 // set when a bounded wait expires
+};
+
+int tc_tile_rows(int T);
+int make_tmap_bf16(CUtensorMap *map, const void *base, long rows, long cols, int box_rows);
+cudaError_t launch_tc_gemm(const TcGemm &g, int T, int t_base, float *Y, int ldy, EpiArgs ep, bool pdl,
+                           cudaStream_t s);
+
+// ---- attention over f32 rings with TMA-staged tiles ------------------------------------
+
+int attn_tma_splits(long window_keys);
+int make_tmap_kv_f32(CUtensorMap *map, const void *base, size_t bytes, int hd);
+cudaError_t launch_attention_tma(const CUtensorMap &map, const float *qkvg, int ldq, Dims d, Rows rows, Ring ring,
+                                 int splits, float *part, const float *sg, float *z, int *counters, int *err, bool pdl,
+                                 cudaStream_t s);
 
 cudaError_t launch_advance(int32_t *seq_pos, const int32_t *seq, const int32_t *count, int n, cudaStream_t s);
 
