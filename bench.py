@@ -101,6 +101,7 @@ def bench_ours(args, rank, world):
     import torch
 
     from looped_normalized_gpt_gb300 import Dory, build
+    from looped_normalized_gpt_gb300.shard import job_throughput, slowest
 
     dev = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(dev)
@@ -133,13 +134,10 @@ def bench_ours(args, rank, world):
             g.decode_step(dec_dev[i:i + 1], [0], cfg.loops)
         e1.record(stream)
         torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1)
+    ms = slowest(e0.elapsed_time(e1))  # the slowest rank's time (one replica per rank)
     if world > 1:
-        t = torch.tensor([ms], device=f"cuda:{dev}")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         torch.distributed.barrier()
-        ms = float(t.item())
-    value = world * K / (ms / 1e3)
+    value = job_throughput(K, ms, world)
 
     # end to end: host ids from pinned memory in, logits back to host, every step
     g2_ids = torch.from_numpy(dec.astype(np.int32)).pin_memory()
@@ -190,6 +188,81 @@ def bench_ours(args, rank, world):
         "weights_gen_s": round(t_gen, 1),
     }
     return out, g, cfg, w
+
+
+def bench_batch(g_cls, torch, w, dev, batch: int = 64, ctx: int = 1024, steps: int = 16, warmup: int = 3):
+    """Batch decode on the same model: `batch` sequences, each with `ctx` positions of
+    synthetic unit-norm K/V rows in every slot, then `steps` decode steps at loops 4."""
+    cfg = synth.dory2b(max_batch=batch, max_seqs=batch, max_context=ctx + steps + warmup + 64)
+    stream = torch.cuda.current_stream()
+    g = g_cls(cfg, w, stream=stream.cuda_stream)
+    try:
+        gen = torch.Generator(device=f"cuda:{dev}")
+        gen.manual_seed(SEED + 100)
+        n_attn = cfg.attn_layers
+        for s_ in range(batch):
+            for o in range(n_attn):
+                k = torch.randn(ctx, cfg.nk, cfg.hd, device=f"cuda:{dev}", generator=gen)
+                v = torch.randn(ctx, cfg.nk, cfg.hd, device=f"cuda:{dev}", generator=gen)
+                k /= k.norm(dim=2, keepdim=True)
+                v /= v.norm(dim=2, keepdim=True)
+                g.write_kv_rows(s_, o, 0, 0, k.contiguous(), v.contiguous())
+            g.set_position(s_, ctx)
+        ids = torch.from_numpy(synth.token_ids(SEED, 7, batch * (steps + warmup), cfg.vocab)).to(f"cuda:{dev}")
+        seqs = list(range(batch))
+        for i in range(warmup):
+            g.decode_step(ids[i * batch:(i + 1) * batch], seqs, cfg.loops)
+        st = g.stats()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(warmup, warmup + steps):
+            g.decode_step(ids[i * batch:(i + 1) * batch], seqs, cfg.loops)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        hbm, _, _ = peaks()
+        b = st["weight_bytes"] + st["kv_read_bytes"] + st["kv_write_bytes"]
+        return {"value": round(batch / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
+                "batch": batch, "context": ctx, "loops": cfg.loops,
+                "roofline": {"bound": "hbm", "achieved": round(b / (ms / 1e3) / 1e9, 1), "peak": hbm, "unit": "GB/s",
+                             "frac": round(b / (ms / 1e3) / 1e9 / hbm, 4), "bytes_per_step": b}}
+    finally:
+        g.close()
+
+
+def bench_prefill(g_cls, torch, w, n_tokens: int = 16384, prompt_loops: int = 2):
+    """Prefill of an n-token seeded prompt in 64-row chunks at loops 4 (prompt_loops for the
+    chunks whose logits are unread, the last chunk reads its last row)."""
+    cfg = synth.dory2b(max_batch=1, max_seqs=1, max_context=n_tokens + 64, prompt_loops=prompt_loops)
+    stream = torch.cuda.current_stream()
+    g = g_cls(cfg, w, stream=stream.cuda_stream)
+    try:
+        ids = synth.token_ids(SEED + 2, 0, n_tokens, cfg.vocab)
+        dids = torch.from_numpy(ids).to("cuda")
+
+        def run():
+            g.reset(0)
+            wb = 0
+            for a in range(0, n_tokens, 64):
+                g.prefill_chunk(0, dids[a:a + 64], a, cfg.loops, "last" if a + 64 >= n_tokens else "none")
+                wb += g.stats()["weight_bytes"]
+            return wb
+        run()  # warm-up: captures the chunk graphs
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        wb = run()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        hbm, _, _ = peaks()
+        return {"value": round(n_tokens / (ms / 1e3), 1), "unit": "tokens/s", "ms": round(ms, 2),
+                "tokens": n_tokens, "chunk": 64, "loops": cfg.loops, "prompt_loops": prompt_loops,
+                "roofline": {"bound": "hbm", "achieved": round(wb / (ms / 1e3) / 1e9, 1), "peak": hbm,
+                             "unit": "GB/s", "frac": round(wb / (ms / 1e3) / 1e9 / hbm, 4), "weight_bytes": wb}}
+    finally:
+        g.close()
 
 
 def cpu_baseline(cfg, w, steps: int = 6):
@@ -248,6 +321,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the batch-64 decode and prefill lines")
     ap.add_argument("--prompt", type=int, default=PROMPT, help="prompt tokens before the decode steps")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -263,6 +337,14 @@ def main():
         torch.distributed.init_process_group("nccl")
     out, g, cfg, w = bench_ours(args, rank, world)
     g.close()
+    if not args.no_extra:
+        import torch
+
+        from looped_normalized_gpt_gb300 import Dory
+
+        dev = int(os.environ.get("LOCAL_RANK", "0"))
+        out["extra"] = {"decode_batch64": bench_batch(Dory, torch, w, dev),
+                        "prefill_16k": bench_prefill(Dory, torch, w)}
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
             out["cpu_baseline"] = cpu_baseline(cfg, w)

@@ -103,6 +103,8 @@ struct dory_handle {
   Emit em_h{}, em_z{}, em_y{};
   CUtensorMap kvmap;          // f32 KV memory as [rows][hd] for the attention's tile copies
   bool kv_tma = false;
+  KvMaps kvq;                 // q8 KV memory (hd = 128) for the attention's tile copies
+  bool kv_tma_q8 = false;
   int32_t *dev_err = nullptr;  // set by a kernel whose bounded wait expired
   float *tc_ws = nullptr;
   int32_t *tc_ctr = nullptr, *tc_err = nullptr;
@@ -344,10 +346,14 @@ int issue_step(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_splits, cud
       const long keys = fixed_splits ? wmax : std::min<long>(wmax, pmax + 1);
       const int splits = (int)((keys + KEYS_PER_SPLIT - 1) / KEYS_PER_SPLIT);
       if (splits > d->max_splits) return fail(DORY_ERANGE, "attention needs %d splits (max %d)", splits, d->max_splits);
-      if (d->kv_tma) {
+      if (d->kv_tma || d->kv_tma_q8) {
         const int tsp = fixed_splits ? attn_tma_splits(wmax) : tma_splits(d, a, ring);
-        CK(launch_attention_tma(d->kvmap, d->qkvg, ldq, dm, rows, ring, tsp, d->part, L.sg, d->z, d->actr, d->dev_err,
-                                true, s));
+        if (d->kv_tma)
+          CK(launch_attention_tma(d->kvmap, d->qkvg, ldq, dm, rows, ring, tsp, d->part, L.sg, d->z, d->actr,
+                                  d->dev_err, true, s));
+        else
+          CK(launch_attention_tma_q8(d->kvq, d->qkvg, ldq, dm, rows, ring, tsp, d->part, L.sg, d->z, d->actr,
+                                     d->dev_err, true, s));
         nl += 1;
       } else if (tc) {
         CK(launch_attention_fused(d->qkvg, ldq, dm, rows, ring, splits, KEYS_PER_SPLIT, d->part, L.sg, d->z, d->actr,
@@ -494,7 +500,7 @@ int issue_step_fused(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_split
       he.kst = d->kst;
       he.vst = d->vst;
       EpiArgs ep{EPI_STORE, nullptr, nullptr, 0};
-      CK(launch_gemv_fused(L.wqkvg, d->wdtype, ldq, dm.hidden, T, first_in(), d->qkvg, ldq, ep, he, true, s));
+      CK(launch_gemv_fused(L.wqkvg, d->wdtype, ldq, dm.hidden, T, first_in(), d->qkvg, ldq, ep, he, d->dev_err, true, s));
       nl++;
       ng++;
       if (q8) {
@@ -505,10 +511,14 @@ int issue_step_fused(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_split
       const long keys = fixed_splits ? wmax : std::min<long>(wmax, pmax + 1);
       const int splits = (int)((keys + KEYS_PER_SPLIT - 1) / KEYS_PER_SPLIT);
       if (splits > d->max_splits) return fail(DORY_ERANGE, "attention needs %d splits (max %d)", splits, d->max_splits);
-      if (d->kv_tma) {
+      if (d->kv_tma || d->kv_tma_q8) {
         const int tsp = fixed_splits ? attn_tma_splits(wmax) : tma_splits(d, a, ring);
-        CK(launch_attention_tma(d->kvmap, d->qkvg, ldq, dm, rows, ring, tsp, d->part, L.sg, d->z, d->actr, d->dev_err,
-                                true, s));
+        if (d->kv_tma)
+          CK(launch_attention_tma(d->kvmap, d->qkvg, ldq, dm, rows, ring, tsp, d->part, L.sg, d->z, d->actr,
+                                  d->dev_err, true, s));
+        else
+          CK(launch_attention_tma_q8(d->kvq, d->qkvg, ldq, dm, rows, ring, tsp, d->part, L.sg, d->z, d->actr,
+                                     d->dev_err, true, s));
       } else {
         CK(launch_attention_fused(d->qkvg, ldq, dm, rows, ring, splits, KEYS_PER_SPLIT, d->part, L.sg, d->z, d->actr,
                                   true, s));
@@ -518,18 +528,18 @@ int issue_step_fused(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_split
       in.mode = IN_NORM;
       in.src = d->z;
       in.ld = q_size;
-      CK(launch_gemv_fused(L.wo, d->wdtype, dm.hidden, q_size, T, in, d->out, dm.hidden, ep, none, true, s));
+      CK(launch_gemv_fused(L.wo, d->wdtype, dm.hidden, q_size, T, in, d->out, dm.hidden, ep, none, d->dev_err, true, s));
       nl++;
       ng++;
     } else {
       EpiArgs ep{EPI_SILU, L.msg, L.msu, (long)dm.ffn};
-      CK(launch_gemv_fused(L.wgu, d->wdtype, dm.ffn, dm.hidden, T, first_in(), d->mlp, dm.ffn, ep, none, true, s));
+      CK(launch_gemv_fused(L.wgu, d->wdtype, dm.ffn, dm.hidden, T, first_in(), d->mlp, dm.ffn, ep, none, d->dev_err, true, s));
       GemvIn in{};
       in.mode = IN_NORM;
       in.src = d->mlp;
       in.ld = dm.ffn;
       EpiArgs e2{EPI_STORE, nullptr, nullptr, 0};
-      CK(launch_gemv_fused(L.wdown, d->wdtype, dm.hidden, dm.ffn, T, in, d->out, dm.hidden, e2, none, true, s));
+      CK(launch_gemv_fused(L.wdown, d->wdtype, dm.hidden, dm.ffn, T, in, d->out, dm.hidden, e2, none, d->dev_err, true, s));
       nl += 2;
       ng += 2;
     }
@@ -551,8 +561,8 @@ int issue_step_fused(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_split
     if ((rc = layer(li, 0, MIX_NONE))) return rc;
   EpiArgs eh{EPI_SCALE, d->logit_scale, nullptr, 0};
   if (a.head_rows == T && a.head_from == 0) {
-    CK(launch_gemv_fused(d->head, d->wdtype, dm.vocab, dm.hidden, T, first_in(), d->logits, dm.vocab, eh, none, true,
-                         s));
+    CK(launch_gemv_fused(d->head, d->wdtype, dm.vocab, dm.hidden, T, first_in(), d->logits, dm.vocab, eh, none, d->dev_err,
+                         true, s));
     nl++;
     ng++;
   } else {
@@ -898,9 +908,11 @@ int dory_create(const dory_config *cfg, const dory_weights *w, void *stream, dor
     return cleanup(DORY_ENOMEM);
   }
 
-  if (!q8) {
+  {
     const char *e = getenv("DORY_KV_TMA");
-    d->kv_tma = !(e && e[0] == '0') && make_tmap_kv_f32(&d->kvmap, d->kvmem, d->kv_bytes, dm.hd) == 0;
+    const bool on = !(e && e[0] == '0');
+    if (!q8) d->kv_tma = on && make_tmap_kv_f32(&d->kvmap, d->kvmem, d->kv_bytes, dm.hd) == 0;
+    else d->kv_tma_q8 = on && dm.hd == 128 && make_tmap_kv_q8(&d->kvq, d->kvmem, d->kv_bytes) == 0;
   }
 
   // ---- activations ---------------------------------------------------------------------

@@ -13,7 +13,9 @@
 //     ring write (or staging for q8) of k and v (dory.rs fn attn_layer).
 // attn_fused_kernel is the split-KV attention of k_attn.cu whose last split block per
 // (row, kv head) merges the splits and applies the gate (no second launch).
+#include <algorithm>
 #include <climits>
+#include <cstdlib>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -588,6 +590,199 @@ cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, bool pdl, c
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+// ---------------------------------------------------------------------------------------
+// bf16 GEMV with the weights streamed by bulk copies (TMA) into a shared-memory ring
+// ---------------------------------------------------------------------------------------
+//
+// One block per SM takes a contiguous range of output rows. Thread 0 copies chunks of CH
+// rows (and, for SwiGLU, the matching up rows) with cp.async.bulk into ST stages; the
+// first ST chunks are requested before griddepcontrol.wait, so the weights are in flight
+// while the previous kernel finishes and while the prologue builds the input rows. Each
+// warp reduces whole rows of a chunk from shared memory. With ~100 KB of shared memory and
+// few registers per thread the next kernel's block fits beside this one.
+
+constexpr uint32_t SWAIT = 1u << 20;
+
+__device__ __forceinline__ uint32_t s_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ bool s_wait(uint32_t bar, uint32_t parity) {
+  for (uint32_t i = 0; i < SWAIT; i++) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (ok) return true;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+template <int TT, bool DUAL>
+__global__ void __launch_bounds__(FW * 32) gemv_stream_kernel(const __nv_bfloat16 *__restrict__ W, int N, int K,
+                                                              int T, int CH, int ST, GemvIn in,
+                                                              float *__restrict__ Y, int ldy, EpiArgs ep, HeadEpi he,
+                                                              int *err) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full[8];
+  __shared__ int last_sh, fail_sh;
+  float *xs = reinterpret_cast<float *>(smem_raw);  // [T][K]
+  const uint32_t wbase = (s_u32(smem_raw) + (uint32_t)T * K * 4 + 127) & ~127u;
+  const int rb = (int)((long)N * blockIdx.x / gridDim.x), re = (int)((long)N * (blockIdx.x + 1) / gridDim.x);
+  const int nchunks = (re - rb + CH - 1) / CH;
+  const uint32_t row_bytes = (uint32_t)K * 2;
+  const uint32_t stage_bytes = (uint32_t)CH * row_bytes * (DUAL ? 2 : 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  auto issue = [&](int c) {
+    const int s = c % ST;
+    const int r0 = rb + c * CH, nr = min(CH, re - r0);
+    const uint32_t bar = s_u32(&full[s]);
+    const uint32_t bytes = (uint32_t)nr * row_bytes;
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes * (DUAL ? 2 : 1))
+                 : "memory");
+    bulk_copy(wbase + s * stage_bytes, W + (size_t)r0 * K, bytes, bar);
+    if (DUAL) bulk_copy(wbase + s * stage_bytes + CH * row_bytes, W + (size_t)(r0 + ep.pair) * K, bytes, bar);
+  };
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < ST; s++) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(s_u32(&full[s])) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    fail_sh = 0;
+    for (int c = 0; c < ST && c < nchunks; c++) issue(c);  // weights only: before the wait
+  }
+  pdl_wait();
+  pdl_trigger();
+  build_input<TT>(in, T, K, xs);  // ends with __syncthreads
+
+  for (int c = 0; c < nchunks; c++) {
+    const int s = c % ST;
+    if (!s_wait(s_u32(&full[s]), (c / ST) & 1)) {
+      if (lane == 0) atomicExch(err, 5);
+      fail_sh = 1;
+    }
+    __syncthreads();
+    if (fail_sh) break;
+    const int r0 = rb + c * CH, nr = min(CH, re - r0);
+    const __nv_bfloat16 *ws = reinterpret_cast<const __nv_bfloat16 *>(smem_raw + (wbase - s_u32(smem_raw)) +
+                                                                      (size_t)s * stage_bytes);
+    for (int rr = warp; rr < nr; rr += FW) {
+      const __nv_bfloat16 *w0 = ws + (size_t)rr * K;
+      const __nv_bfloat16 *w1 = DUAL ? ws + (size_t)(CH + rr) * K : nullptr;
+      float acc0[TT], acc1[TT];
+#pragma unroll
+      for (int t = 0; t < TT; t++) acc0[t] = acc1[t] = 0.f;
+#pragma unroll 4
+      for (int k = lane * 8; k < K; k += 256) {
+        float w[8], u[8];
+        unpack8(*reinterpret_cast<const uint4 *>(w0 + k), w);
+        if (DUAL) unpack8(*reinterpret_cast<const uint4 *>(w1 + k), u);
+#pragma unroll
+        for (int t = 0; t < TT; t++) {
+          if (t < T) {
+            const float4 xa = *reinterpret_cast<const float4 *>(&xs[t * K + k]);
+            const float4 xb = *reinterpret_cast<const float4 *>(&xs[t * K + k + 4]);
+            const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+              acc0[t] = fmaf(w[i], xv[i], acc0[t]);
+              if (DUAL) acc1[t] = fmaf(u[i], xv[i], acc1[t]);
+            }
+          }
+        }
+      }
+      const int n = r0 + rr;
+#pragma unroll
+      for (int t = 0; t < TT; t++) {
+        if (t >= T) break;
+        const float a = warp_sum(acc0[t]);
+        const float b = DUAL ? warp_sum(acc1[t]) : 0.f;
+        if (lane == 0) {
+          float y;
+          if (ep.mode == EPI_SCALE) {
+            y = a * ep.vec[n];
+          } else if (ep.mode == EPI_SILU) {
+            const float g = a * ep.vec[n];
+            y = g * sigmoidf_(g) * (b * ep.vec2[n]);
+          } else {
+            y = a;
+          }
+          Y[(size_t)t * ldy + n] = y;
+        }
+      }
+    }
+    __syncthreads();  // the stage is free again
+    if (threadIdx.x == 0 && c + ST < nchunks) issue(c + ST);
+  }
+  if (!he.enabled || fail_sh) return;
+  // heads this block finished rows of: the block that completes a head runs its epilogue
+  __threadfence();
+  __syncthreads();
+  const int hd = he.d.hd;
+  for (int h = rb / hd; h <= (re - 1) / hd && re > rb; h++) {
+    if (threadIdx.x == 0) {
+      const int cnt = min(re, (h + 1) * hd) - max(rb, h * hd);
+      const int old = atomicAdd(&he.counters[h], cnt);
+      last_sh = old + cnt == hd;
+      if (last_sh) he.counters[h] = 0;
+    }
+    __syncthreads();
+    if (last_sh) {
+      __threadfence();
+      head_epilogue(he, h, T, Y, ldy);
+    }
+    __syncthreads();
+  }
+}
+
+template <int TT, bool DUAL>
+cudaError_t gemv_stream_t(const void *W, int N, int K, int T, GemvIn in, float *Y, int ldy, EpiArgs ep, HeadEpi he,
+                          int *err, bool pdl, cudaStream_t s) {
+  static int sms = 0;
+  if (!sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 148;
+  }
+  const size_t row_bytes = (size_t)K * 2 * (DUAL ? 2 : 1);
+  const size_t xs_bytes = (size_t)T * K * 4;
+  const size_t budget = 110 * 1024;
+  if (xs_bytes + 128 + 2 * row_bytes > 200 * 1024) return cudaErrorInvalidValue;
+  const size_t wbudget = budget > xs_bytes + 128 + 2 * row_bytes ? budget - xs_bytes - 128 : 2 * row_bytes;
+  int CH = (int)std::min<size_t>(32, std::max<size_t>(1, (wbudget / 3) / row_bytes));
+  int ST = (int)std::min<size_t>(8, std::max<size_t>(2, wbudget / (CH * row_bytes)));
+  const int rows_per_block = (N + sms - 1) / sms;
+  if (CH > rows_per_block) CH = rows_per_block;
+  ST = (int)std::min<size_t>(ST, std::max<size_t>(2, wbudget / (CH * row_bytes)));
+  ST = std::min(ST, 8);
+  const size_t smem = xs_bytes + 128 + (size_t)ST * CH * row_bytes;
+  auto kern = gemv_stream_kernel<TT, DUAL>;
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    attr = true;
+  }
+  const int grid = std::min(sms, N);
+  return launch_pdl(kern, dim3(grid), dim3(FW * 32), smem, pdl, s, static_cast<const __nv_bfloat16 *>(W), N, K, T, CH,
+                    ST, in, Y, ldy, ep, he, err);
+}
+
+template <bool DUAL>
+cudaError_t gemv_stream_d(const void *W, int N, int K, int T, GemvIn in, float *Y, int ldy, EpiArgs ep, HeadEpi he,
+                          int *err, bool pdl, cudaStream_t s) {
+  switch (T) {
+    case 1: return gemv_stream_t<1, DUAL>(W, N, K, T, in, Y, ldy, ep, he, err, pdl, s);
+    case 2: return gemv_stream_t<2, DUAL>(W, N, K, T, in, Y, ldy, ep, he, err, pdl, s);
+    default: return gemv_stream_t<4, DUAL>(W, N, K, T, in, Y, ldy, ep, he, err, pdl, s);
+  }
+}
+
 template <typename WT, int TT, bool DUAL>
 cudaError_t gemv_fused_t(const void *W, int N, int K, int T, GemvIn in, float *Y, int ldy, EpiArgs ep, HeadEpi he,
                          bool pdl, cudaStream_t s) {
@@ -638,10 +833,17 @@ cudaError_t attn_fused_q(const float *qkvg, int ldq, Dims d, Rows rows, Ring rin
 }  // namespace
 
 cudaError_t launch_gemv_fused(const void *W, int wdtype, int N, int K, int T, GemvIn in, float *Y, int ldy,
-                              EpiArgs ep, HeadEpi he, bool pdl, cudaStream_t s) {
+                              EpiArgs ep, HeadEpi he, int *err, bool pdl, cudaStream_t s) {
   if (T < 1 || T > MAXT || K % 8 != 0 || (size_t)T * K * 4 > 96 * 1024) return cudaErrorInvalidValue;
   if (he.enabled && ((he.d.hd / 2) % 32 != 0 || T * (he.d.hd / 2) > FW * 32)) return cudaErrorInvalidValue;
   const bool dual = ep.mode == EPI_SILU;
+  static const bool stream_off = [] {
+    const char *e = getenv("DORY_GEMV_STREAM");
+    return e && e[0] == '0';
+  }();
+  if (wdtype == W_BF16 && !stream_off)
+    return dual ? gemv_stream_d<true>(W, N, K, T, in, Y, ldy, ep, he, err, pdl, s)
+                : gemv_stream_d<false>(W, N, K, T, in, Y, ldy, ep, he, err, pdl, s);
   if (wdtype == W_BF16)
     return dual ? gemv_fused_d<__nv_bfloat16, true>(W, N, K, T, in, Y, ldy, ep, he, pdl, s)
                 : gemv_fused_d<__nv_bfloat16, false>(W, N, K, T, in, Y, ldy, ep, he, pdl, s);

@@ -134,7 +134,7 @@ struct HeadEpi {
 };
 
 cudaError_t launch_gemv_fused(const void *W, int wdtype, int N, int K, int T, GemvIn in, float *Y, int ldy,
-                              EpiArgs ep, HeadEpi he, bool pdl, cudaStream_t s);
+                              EpiArgs ep, HeadEpi he, int *err, bool pdl, cudaStream_t s);
 
 cudaError_t launch_attention_fused(const float *qkvg, int ldq, Dims d, Rows rows, Ring ring, int splits, int kps,
                                    float *part, const float *sg, float *z, int *counters, bool pdl, cudaStream_t s);
@@ -163,6 +163,15 @@ int make_tmap_kv_f32(CUtensorMap *map, const void *base, size_t bytes, int hd);
 cudaError_t launch_attention_tma(const CUtensorMap &map, const float *qkvg, int ldq, Dims d, Rows rows, Ring ring,
                                  int splits, float *part, const float *sg, float *z, int *counters, int *err, bool pdl,
                                  cudaStream_t s);
+
+// q8_2f rings with hd = 128: the KV memory as code rows, K-scale rows and V-scale runs.
+struct KvMaps {
+  CUtensorMap codes, kscales, vscales;
+};
+int make_tmap_kv_q8(KvMaps *m, const void *base, size_t bytes);
+cudaError_t launch_attention_tma_q8(const KvMaps &m, const float *qkvg, int ldq, Dims d, Rows rows, Ring ring,
+                                    int splits, float *part, const float *sg, float *z, int *counters, int *err,
+                                    bool pdl, cudaStream_t s);
 
 cudaError_t launch_advance(int32_t *seq_pos, const int32_t *seq, const int32_t *count, int n, cudaStream_t s);
 

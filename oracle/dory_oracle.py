@@ -161,23 +161,47 @@ def freeze_field(codes: np.ndarray, scales: np.ndarray, group: int):
     return col, new_codes, new_scales
 
 
+class _Rows:
+    """Rows indexed by absolute position, grown on demand (storage only)."""
+
+    def __init__(self, shape, dtype):
+        self.shape, self.dtype = shape, dtype
+        self.a = np.zeros((0,) + shape, dtype)
+
+    def _fit(self, n):
+        if n > len(self.a):
+            b = np.zeros((max(n, 2 * len(self.a), 64),) + self.shape, self.dtype)
+            b[:len(self.a)] = self.a
+            self.a = b
+
+    def __getitem__(self, p):
+        return self.a[p]
+
+    def __setitem__(self, p, v):
+        self._fit(int(p) + 1)
+        self.a[p] = v
+
+
 class Slot:
     """One KV slot of one sequence: rows by absolute position.
 
     f32: k, v rows as f32 (dory.rs, struct KvSlot). q8_2f: per (row, kv head) int8 K codes
     with one f32 scale per 32 channels, int8 V codes with one f32 scale per row, and
-    per-channel fields kcol/vcol frozen after 64 rows (kv_cache.rs, struct LayerKvCache)."""
+    per-channel fields kcol/vcol frozen after 64 rows (kv_cache.rs, struct LayerKvCache).
+    Rows live in arrays indexed by position; `valid` marks the positions the slot holds."""
 
     def __init__(self, nk: int, hd: int, quant: bool):
         self.nk, self.hd, self.quant = nk, hd, quant
+        ng = hd // KV_K_GROUP
         self.positions: list[int] = []  # stored rows in append order
-        self.k: dict[int, np.ndarray] = {}
-        self.v: dict[int, np.ndarray] = {}
+        self.valid = _Rows((), bool)
+        self.k = _Rows((nk, hd), F32)
+        self.v = _Rows((nk, hd), F32)
         # q8 state
-        self.kq: dict[int, np.ndarray] = {}
-        self.ks: dict[int, np.ndarray] = {}
-        self.vq: dict[int, np.ndarray] = {}
-        self.vs: dict[int, np.ndarray] = {}
+        self.kq = _Rows((nk, hd), np.int8)
+        self.ks = _Rows((nk, ng), F32)
+        self.vq = _Rows((nk, hd), np.int8)
+        self.vs = _Rows((nk,), F32)
         self.kcol: np.ndarray | None = None  # [nk][hd] f32, None until frozen
         self.vcol: np.ndarray | None = None
 
@@ -187,24 +211,18 @@ class Slot:
 
     def _freeze(self) -> None:
         nk, hd = self.nk, self.hd
-        ng = hd // KV_K_GROUP
         kcol = np.zeros((nk, hd), dtype=F32)
         vcol = np.zeros((nk, hd), dtype=F32)
-        P = self.positions
+        P = np.asarray(self.positions)
         for h in range(nk):
-            kc = np.stack([self.kq[p][h] for p in P])
-            ksc = np.stack([self.ks[p][h] for p in P])
-            col, kc2, ks2 = freeze_field(kc, ksc, KV_K_GROUP)
+            col, kc2, ks2 = freeze_field(self.kq.a[P, h], self.ks.a[P, h], KV_K_GROUP)
             kcol[h] = col
-            vc = np.stack([self.vq[p][h] for p in P])
-            vsc = np.stack([self.vs[p][h : h + 1] for p in P])
-            colv, vc2, vs2 = freeze_field(vc, vsc, hd)
+            colv, vc2, vs2 = freeze_field(self.vq.a[P, h], self.vs.a[P, h][:, None], hd)
             vcol[h] = colv
-            for i, p in enumerate(P):
-                self.kq[p][h] = kc2[i]
-                self.ks[p][h] = ks2[i].reshape(ng)
-                self.vq[p][h] = vc2[i]
-                self.vs[p][h] = vs2[i][0]
+            self.kq.a[P, h] = kc2
+            self.ks.a[P, h] = ks2
+            self.vq.a[P, h] = vc2
+            self.vs.a[P, h] = vs2[:, 0]
         self.kcol, self.vcol = kcol, vcol
 
     def append(self, pos: int, k: np.ndarray, v: np.ndarray) -> None:
@@ -227,19 +245,18 @@ class Slot:
                 vq[h], vs[h] = c, s[0]
             self.kq[pos], self.ks[pos], self.vq[pos], self.vs[pos] = kq, ks, vq, vs
         else:
-            self.k[pos], self.v[pos] = k.copy(), v.copy()
+            self.k[pos], self.v[pos] = k, v
+        self.valid[pos] = True
         self.positions.append(pos)
 
     def truncate(self, n: int) -> None:
         """Drop the last n stored rows (dory.rs fn attn_layer's overwrite, kv_cache.rs
         fn truncate_last). A frozen field stays frozen."""
         for _ in range(min(n, self.stored)):
-            p = self.positions.pop()
-            for d in (self.k, self.v, self.kq, self.ks, self.vq, self.vs):
-                d.pop(p, None)
+            self.valid[self.positions.pop()] = False
 
     def has(self, pos: int) -> bool:
-        return pos in (self.kq if self.quant else self.k)
+        return 0 <= pos < len(self.valid.a) and bool(self.valid.a[pos])
 
     def attend(self, qg: np.ndarray, kh: int, p: int, window: int | None) -> np.ndarray:
         """Attention of the query heads of one KV group at position p.
@@ -251,27 +268,30 @@ class Slot:
         (kv_cache.rs fn attend_group_upto)."""
         hd = self.hd
         lo = 0 if window is None else max(p + 1 - window, 0)
-        keys = [j for j in range(lo, p + 1) if self.has(j)]
+        span = np.arange(lo, p + 1)
+        keys = span[self.valid.a[lo:p + 1]] if len(self.valid.a) > p else \
+            np.array([j for j in span if self.has(j)], dtype=np.int64)
         scale = 1.0 / math.sqrt(hd)
         out = np.zeros_like(qg)
+        if self.quant:
+            codes = self.kq.a[keys, kh].astype(np.float64).reshape(len(keys), -1, KV_K_GROUP)  # [n][g][32]
+            kscale = self.ks.a[keys, kh].astype(np.float64)  # [n][g]
+            vcodes = self.vq.a[keys, kh].astype(np.float64)
+            vscale = self.vs.a[keys, kh].astype(np.float64)
+        else:
+            K = self.k.a[keys, kh].astype(np.float64)
+            V = self.v.a[keys, kh].astype(np.float64)
         for h in range(qg.shape[0]):
             q = qg[h]
             if self.quant:
                 qc = q if self.kcol is None else q * self.kcol[kh].astype(np.float64)
-                s = np.empty(len(keys))
-                for i, j in enumerate(keys):
-                    codes = self.kq[j][kh].astype(np.float64)
-                    dots = (qc * codes).reshape(-1, KV_K_GROUP).sum(axis=1)
-                    s[i] = scale * np.dot(self.ks[j][kh].astype(np.float64), dots)
+                dots = np.einsum("ngc,gc->ng", codes, qc.reshape(-1, KV_K_GROUP))  # per group
+                s = scale * np.sum(kscale * dots, axis=1)
                 a = softmax(s)
-                y = np.zeros(hd)
-                for i, j in enumerate(keys):
-                    y += (a[i] * float(self.vs[j][kh])) * self.vq[j][kh].astype(np.float64)
+                y = (a * vscale) @ vcodes
                 if self.vcol is not None:
                     y = y * self.vcol[kh].astype(np.float64)
             else:
-                K = np.stack([self.k[j][kh] for j in keys]).astype(np.float64)
-                V = np.stack([self.v[j][kh] for j in keys]).astype(np.float64)
                 a = softmax(K @ q * scale)
                 y = a @ V
             out[h] = y

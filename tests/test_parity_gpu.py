@@ -218,10 +218,13 @@ def test_q8_decode_batch_over_a_synthetic_context():
 def test_state_and_range_errors():
     from looped_normalized_gpt_gb300 import DoryError
 
-    cfg = synth.small(rec_kinds="S*", full_window=0, max_context=80, max_batch=2, max_seqs=2)
+    # a full layer without full_window holds max_context positions (a whole number of
+    # 64-row blocks: 128 here)
+    cfg = synth.small(rec_kinds="S*", full_window=0, max_context=128, max_batch=2, max_seqs=2)
     P = Pair(cfg, 2009)
     try:
         g = P.gpu
+        assert g.slot_info(1)[0] == 128
         with pytest.raises(DoryError) as e:
             g.prefill_chunk(0, [1, 2], 5, 2, "last")
         assert e.value.code == -4
@@ -232,8 +235,12 @@ def test_state_and_range_errors():
             g.decode_step([1, 2], [0, 0], 2)
         assert e.value.code == -1
         g.prefill_chunk(0, list(range(64)), 0, 1, "none")
+        g.prefill_chunk(0, list(range(64)), 64, 1, "none")
         with pytest.raises(DoryError) as e:
-            g.prefill_chunk(0, list(range(20)), 64, 1, "none")
+            g.prefill_chunk(0, list(range(20)), 128, 1, "none")
+        assert e.value.code == -5
+        with pytest.raises(DoryError) as e:
+            g.decode_step([7], [0], 1)
         assert e.value.code == -5
         with pytest.raises(DoryError) as e:
             g.logits(0)
@@ -266,5 +273,28 @@ def test_2b_prefill_chunk_then_decode(w2b):
         assert P.max_hidden_err <= 2e-2, P.max_hidden_err
         assert P.max_hidden_err <= 1e-4, P.max_hidden_err
         assert all(P.top1)
+    finally:
+        P.close()
+
+
+@pytest.mark.parametrize("kv_quant", ["q8_2f", "f32"])
+def test_head_width_128_rings_with_tile_copies(kv_quant):
+    """hd = 128 takes the tile-copy attention for both row formats (q8_2f only there)."""
+    cfg = synth.small(kv_quant=kv_quant, kv_mode="last_loop", hd=128, nh=4, nk=2, rec_kinds="S*", full_window=150,
+                      max_batch=3, max_seqs=3, loops=3)
+    P = Pair(cfg, 2010)
+    try:
+        for s in range(2):
+            P.write_context(s, 200, 2010 + s)
+        ids = synth.token_ids(2010, 30, 100, cfg.vocab)
+        P.prefill(2, ids[:64], 3, "none")
+        P.prefill(2, ids[64:100], 3, "last")
+        for step in range(3):
+            P.decode([1, 2, 0], synth.token_ids(2010, 40 + step, 3, cfg.vocab), 3)
+        assert P.max_hidden_err <= (1e-4 if kv_quant == "f32" else tol_of(cfg)), P.max_hidden_err
+        assert np.mean(P.top1) >= 0.99
+        if kv_quant == "f32":
+            for s in range(3):
+                P.check_rings(s, 1e-5)
     finally:
         P.close()
