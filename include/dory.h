@@ -200,6 +200,32 @@ typedef struct dory_stats {
 /* Byte and launch accounting of the handle and of its last call. */
 int dory_get_stats(dory_t *d, dory_stats *out);
 
+/* ---- for callers that cannot allocate device memory ---------------------------------- */
+
+/* The pages have no counterpart of this entry point: it serves callers that may not call
+ * cudaMalloc (code running inside another runtime's allocator or memory pool, code that
+ * runs while a CUDA graph is being captured, plugins that must not grow the process's
+ * device memory). It quantises n K and V rows to q8_2f exactly as dory_write_kv_rows
+ * appends them to an empty slot: the same codes, scales and frozen fields, bit for bit,
+ * without a handle and without allocating anything.
+ *   k, v   [n][nk][hd] f32 rows, in memory the current device can read (device, managed or
+ *          mapped pinned memory);
+ *   kq, vq [nk][n][hd] int8 codes; ks [nk][n][hd/32] and vs [nk][n] f32 scales;
+ *   kcol, vcol [nk][hd] f32 fields (all zero when n <= 64: nothing froze) - all outputs in
+ *          device memory the caller owns;
+ *   stream a cudaStream_t (NULL: the legacy default stream); the call returns once the work
+ *          is queued on it.
+ * Limits: 1 <= nk <= 16, hd in {32, 64, 128}, n >= 1; anything else is DORY_EINVAL.
+ * Working memory: a static device array of about 290 KB inside the library (the row
+ * counters and the first 64 rows the freeze reads back), held by every GPU that loads the
+ * library until the process exits. The first call on a device looks up that array's device
+ * address (cudaGetSymbolAddress) and must come before any stream capture on that device.
+ * Every call clears the counters it needs at zero; calls share the array, so two calls
+ * whose work overlaps on the GPU race and must not be made. Errors: DORY_EINVAL,
+ * DORY_ECUDA; the message is dory_last_error(). */
+int dory_q8_quantize_noalloc(const float *k, const float *v, int32_t n, int32_t nk, int32_t hd, int8_t *kq,
+                             float *ks, int8_t *vq, float *vs, float *kcol, float *vcol, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -749,6 +749,10 @@ int check_device_error(dory_t *d) {
 
 }  // namespace
 
+namespace dory {
+void set_last_error(const char *msg) { g_err = msg; }
+}  // namespace dory
+
 extern "C" {
 
 const char *dory_last_error(void) { return g_err.c_str(); }

@@ -80,6 +80,7 @@ SIGNATURES = {
                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "dory_get_stats": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(StatsC)]),
+    "dory_q8_quantize_noalloc": (ctypes.c_int, [ctypes.c_void_p] * 2 + [ctypes.c_int32] * 3 + [ctypes.c_void_p] * 7),
 }
 
 _LIB = None
