@@ -902,6 +902,10 @@ int dory_create(const dory_config *cfg, const dory_weights *w, void *stream, dor
     const long keys = o.window == INT_MAX ? (long)o.cap : std::min<long>(o.window, o.cap);
     d->max_splits = std::max<int>(d->max_splits, (int)((keys + KEYS_PER_SPLIT - 1) / KEYS_PER_SPLIT));
     d->max_splits = std::max<int>(d->max_splits, attn_tma_splits(keys));
+    if ((keys + KEYS_PER_SPLIT - 1) / KEYS_PER_SPLIT > 2 * dm.hd) {
+      fail(DORY_EINVAL, "a window of %ld keys is more than the attention merge holds for hd %d", keys, dm.hd);
+      return cleanup(DORY_EINVAL);
+    }
   }
   d->n_flat_slots = flat;
   d->seq_stride = std::max<size_t>(sb, 1024);

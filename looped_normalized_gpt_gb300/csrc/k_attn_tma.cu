@@ -188,24 +188,9 @@ __global__ void __launch_bounds__(128) attn_tma_kernel(const __grid_constant__ C
   if (!last) return;
   __threadfence();
   const float *pr = part + (size_t)(r * d.nk + kh) * splits * REP * (HD + 2);
-  const float *g = qkvg + (size_t)r * ldq + (size_t)(d.nh + 2 * d.nk) * HD;
-  for (int i = threadIdx.x; i < REP * HD; i += blockDim.x) {
-    const int h = i / HD, c = i % HD;
-    float M = -INFINITY;
-    for (int s = 0; s < splits; s++) M = fmaxf(M, __ldcg(pr + (s * REP + h) * (HD + 2) + HD));
-    float o = 0.f, L = 0.f;
-    for (int s = 0; s < splits; s++) {
-      const float *pp = pr + (s * REP + h) * (HD + 2);
-      const float ms = __ldcg(pp + HD);
-      if (ms == -INFINITY) continue;
-      const float f = expf(ms - M);
-      o += __ldcg(pp + c) * f;
-      L += __ldcg(pp + HD + 1) * f;
-    }
-    const int col = (kh * REP + h) * HD + c;
-    const float y = L > 0.f ? o / L : 0.f;
-    z[(size_t)r * d.nh * HD + col] = y * sigmoidf_(g[col] * sg[col]);
-  }
+  const size_t col0 = (size_t)kh * REP * HD;
+  merge_splits<REP, HD>(pr, splits, Ks, qkvg + (size_t)r * ldq + (size_t)(d.nh + 2 * d.nk) * HD + col0, sg + col0,
+                        nullptr, z + (size_t)r * d.nh * HD + col0);
 }
 
 template <int REP, int NV>
@@ -397,25 +382,11 @@ __global__ void __launch_bounds__(128) attn_tma_q8_kernel(const __grid_constant_
   if (!last) return;
   __threadfence();
   const float *pr = part + (size_t)(r * d.nk + kh) * splits * REP * (HD + 2);
-  const float *g = qkvg + (size_t)r * ldq + (size_t)(d.nh + 2 * d.nk) * HD;
   const float *vcol = reinterpret_cast<const float *>(slot + ring.L.vcol) + (size_t)kh * HD;
-  for (int i = threadIdx.x; i < REP * HD; i += blockDim.x) {
-    const int h = i / HD, c = i % HD;
-    float M = -INFINITY;
-    for (int s2 = 0; s2 < splits; s2++) M = fmaxf(M, __ldcg(pr + (s2 * REP + h) * (HD + 2) + HD));
-    float o = 0.f, L = 0.f;
-    for (int s2 = 0; s2 < splits; s2++) {
-      const float *pp = pr + (s2 * REP + h) * (HD + 2);
-      const float ms = __ldcg(pp + HD);
-      if (ms == -INFINITY) continue;
-      const float f = expf(ms - M);
-      o += __ldcg(pp + c) * f;
-      L += __ldcg(pp + HD + 1) * f;
-    }
-    const int col = (kh * REP + h) * HD + c;
-    const float y = (L > 0.f ? o / L : 0.f) * (frozen ? vcol[c] : 1.f);
-    z[(size_t)r * d.nh * HD + col] = y * sigmoidf_(g[col] * sg[col]);
-  }
+  const size_t col0 = (size_t)kh * REP * HD;
+  merge_splits<REP, HD>(pr, splits, reinterpret_cast<float *>(Kq), qkvg + (size_t)r * ldq +
+                        (size_t)(d.nh + 2 * d.nk) * HD + col0, sg + col0, frozen ? vcol : nullptr,
+                        z + (size_t)r * d.nh * HD + col0);
 }
 
 template <int REP>

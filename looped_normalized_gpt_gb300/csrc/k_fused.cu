@@ -77,122 +77,135 @@ __device__ __forceinline__ void block_sum_n(float *v, float (*red)[FW]) {
   __syncthreads();
 }
 
-// Prologue: the block's input rows xs[t][K] from the previous kernels' outputs.
-template <int TT>
-__device__ void build_input(const GemvIn &in, int T, int K, float *xs) {
-  __shared__ float red[MAXT][FW];
-  const int tid = threadIdx.x, nt = blockDim.x;
-  if (in.mode == IN_PLAIN) {
-    for (int t = 0; t < T; t++)
-      for (int i = tid; i < K; i += nt) xs[t * K + i] = in.src[(size_t)t * in.ld + i];
-    __syncthreads();
-    return;
-  }
-  if (in.mode == IN_NORM) {
-    float ss[TT];
-#pragma unroll
-    for (int t = 0; t < TT; t++) ss[t] = 0.f;
-    for (int t = 0; t < T; t++)
-      for (int i = tid; i < K; i += nt) {
-        const float v = in.src[(size_t)t * in.ld + i];
-        xs[t * K + i] = v;
-        ss[t] += v * v;
-      }
-    block_sum_n<TT>(ss, red);
-    for (int t = 0; t < T; t++) {
-      const float inv = 1.f / sqrtf(ss[t] + DORY_EPS);
-      for (int i = tid; i < K; i += nt) xs[t * K + i] *= inv;
-    }
-    __syncthreads();
-    return;
-  }
-  // IN_RESID: x = (x^ + alpha (out^ - x^))^, then the loop mix
-  const bool lead = blockIdx.x == 0;
-  float a[TT], b[TT];
-  if (in.alpha) {
-#pragma unroll
-    for (int t = 0; t < TT; t++) a[t] = b[t] = 0.f;
-    for (int t = 0; t < T; t++)
-      for (int i = tid; i < K; i += nt) {
-        const float x = in.src[(size_t)t * in.ld + i], o = in.out[(size_t)t * K + i];
-        a[t] += x * x;
-        b[t] += o * o;
-      }
-    block_sum_n<TT>(a, red);
-    block_sum_n<TT>(b, red);
-#pragma unroll
-    for (int t = 0; t < TT; t++) {
-      a[t] = 1.f / sqrtf(a[t] + DORY_EPS);
-      b[t] = 1.f / sqrtf(b[t] + DORY_EPS);
-    }
-    float s[TT];
-#pragma unroll
-    for (int t = 0; t < TT; t++) s[t] = 0.f;
-    for (int t = 0; t < T; t++)
-      for (int i = tid; i < K; i += nt) {
-        const float xh = in.src[(size_t)t * in.ld + i] * a[t], oh = in.out[(size_t)t * K + i] * b[t];
-        const float v = xh + in.alpha[i] * (oh - xh);
-        xs[t * K + i] = v;
-        s[t] += v * v;
-      }
-    block_sum_n<TT>(s, red);
-    for (int t = 0; t < T; t++) {
-      const float inv = 1.f / sqrtf(s[t] + DORY_EPS);
-      for (int i = tid; i < K; i += nt) xs[t * K + i] *= inv;
-    }
-  } else {
-    for (int t = 0; t < T; t++)
-      for (int i = tid; i < K; i += nt) xs[t * K + i] = in.src[(size_t)t * in.ld + i];
+// Sums of two values over the block (every thread gets both).
+__device__ __forceinline__ void block_sum2(float &a, float &b, float (*red)[FW]) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  a = warp_sum(a);
+  b = warp_sum(b);
+  __syncthreads();
+  if (lane == 0) {
+    red[0][warp] = a;
+    red[1][warp] = b;
   }
   __syncthreads();
-  if (in.mix == MIX_LOOP || in.mix == MIX_END) {  // state = h^
-    float s[TT];
+  a = b = 0.f;
 #pragma unroll
-    for (int t = 0; t < TT; t++) s[t] = 0.f;
-    for (int t = 0; t < T; t++)
-      for (int i = tid; i < K; i += nt) s[t] += xs[t * K + i] * xs[t * K + i];
-    block_sum_n<TT>(s, red);
-    for (int t = 0; t < T; t++) {
-      const float inv = 1.f / sqrtf(s[t] + DORY_EPS);
-      for (int i = tid; i < K; i += nt) {
-        const float v = xs[t * K + i] * inv;
-        xs[t * K + i] = v;
-        if (lead) in.state[(size_t)t * K + i] = v;
-      }
-    }
-    __syncthreads();
+  for (int w = 0; w < FW; w++) {
+    a += red[0][w];
+    b += red[1][w];
   }
-  if (in.mix == MIX_BEGIN || in.mix == MIX_LOOP) {  // h = (state + input)^
-    float s[TT];
+}
+
+// Prologue: the block's input rows xs[t][K] from the previous kernels' outputs. Each
+// thread owns the float4 chunks tid + j * blockDim of a row (KC of them at most) and loads
+// all the vectors it needs for them at once, so a row costs one memory round trip; the
+// reductions pair up their sums.
+template <int TT, int KC>
+__device__ void build_input(const GemvIn &in, int T, int K, float *xs) {
+  __shared__ float red[2][FW];
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const int nch = K / 4;
+  const bool lead = blockIdx.x == 0;
+  for (int t = 0; t < T; t++) {
+    const float4 *src = reinterpret_cast<const float4 *>(in.src + (size_t)t * in.ld);
+    float4 x[KC], o[KC], al[KC], inp[KC];
 #pragma unroll
-    for (int t = 0; t < TT; t++) s[t] = 0.f;
-    for (int t = 0; t < T; t++)
-      for (int i = tid; i < K; i += nt) {
-        const float st = xs[t * K + i];
-        float inp;
-        if (in.mix == MIX_BEGIN) {
-          inp = st;
-          if (lead) {
-            in.input[(size_t)t * K + i] = st;
-            in.state[(size_t)t * K + i] = st;
-          }
-        } else {
-          inp = in.input[(size_t)t * K + i];
+    for (int j = 0; j < KC; j++) {
+      const int c = tid + j * nt;
+      x[j] = o[j] = al[j] = inp[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (c < nch) {
+        x[j] = src[c];
+        if (in.mode == IN_RESID && in.alpha) {
+          o[j] = reinterpret_cast<const float4 *>(in.out + (size_t)t * K)[c];
+          al[j] = reinterpret_cast<const float4 *>(in.alpha)[c];
         }
-        const float v = st + inp;
-        xs[t * K + i] = v;
-        s[t] += v * v;
+        if (in.mode == IN_RESID && in.mix == MIX_LOOP) inp[j] = reinterpret_cast<const float4 *>(in.input + (size_t)t * K)[c];
       }
-    block_sum_n<TT>(s, red);
-    for (int t = 0; t < T; t++) {
-      const float inv = 1.f / sqrtf(s[t] + DORY_EPS);
-      for (int i = tid; i < K; i += nt) xs[t * K + i] *= inv;
     }
-    __syncthreads();
+    auto sq4 = [](const float4 &v) { return v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w; };
+    auto scale4 = [](float4 &v, float f) {
+      v.x *= f;
+      v.y *= f;
+      v.z *= f;
+      v.w *= f;
+    };
+    if (in.mode == IN_NORM) {
+      float ss = 0.f, dummy = 0.f;
+#pragma unroll
+      for (int j = 0; j < KC; j++) ss += sq4(x[j]);
+      block_sum2(ss, dummy, red);
+      const float inv = 1.f / sqrtf(ss + DORY_EPS);
+#pragma unroll
+      for (int j = 0; j < KC; j++) scale4(x[j], inv);
+    } else if (in.mode == IN_RESID) {
+      if (in.alpha) {
+        float sx = 0.f, so = 0.f;
+#pragma unroll
+        for (int j = 0; j < KC; j++) {
+          sx += sq4(x[j]);
+          so += sq4(o[j]);
+        }
+        block_sum2(sx, so, red);
+        const float ix = 1.f / sqrtf(sx + DORY_EPS), io = 1.f / sqrtf(so + DORY_EPS);
+        float sr = 0.f, dummy = 0.f;
+#pragma unroll
+        for (int j = 0; j < KC; j++) {
+          float4 xh = x[j], oh = o[j];
+          scale4(xh, ix);
+          scale4(oh, io);
+          x[j] = make_float4(xh.x + al[j].x * (oh.x - xh.x), xh.y + al[j].y * (oh.y - xh.y),
+                             xh.z + al[j].z * (oh.z - xh.z), xh.w + al[j].w * (oh.w - xh.w));
+          sr += sq4(x[j]);
+        }
+        block_sum2(sr, dummy, red);
+        const float inv = 1.f / sqrtf(sr + DORY_EPS);
+#pragma unroll
+        for (int j = 0; j < KC; j++) scale4(x[j], inv);
+      }
+      if (in.mix == MIX_LOOP || in.mix == MIX_END) {  // state = h^
+        float ss = 0.f, dummy = 0.f;
+#pragma unroll
+        for (int j = 0; j < KC; j++) ss += sq4(x[j]);
+        block_sum2(ss, dummy, red);
+        const float inv = 1.f / sqrtf(ss + DORY_EPS);
+#pragma unroll
+        for (int j = 0; j < KC; j++) {
+          scale4(x[j], inv);
+          const int c = tid + j * nt;
+          if (lead && c < nch) reinterpret_cast<float4 *>(in.state + (size_t)t * K)[c] = x[j];
+        }
+      }
+      if (in.mix == MIX_BEGIN || in.mix == MIX_LOOP) {  // h = (state + input)^
+        float ss = 0.f, dummy = 0.f;
+#pragma unroll
+        for (int j = 0; j < KC; j++) {
+          const int c = tid + j * nt;
+          if (in.mix == MIX_BEGIN) {
+            inp[j] = x[j];
+            if (lead && c < nch) {
+              reinterpret_cast<float4 *>(in.input + (size_t)t * K)[c] = x[j];
+              reinterpret_cast<float4 *>(in.state + (size_t)t * K)[c] = x[j];
+            }
+          }
+          x[j] = make_float4(x[j].x + inp[j].x, x[j].y + inp[j].y, x[j].z + inp[j].z, x[j].w + inp[j].w);
+          ss += sq4(x[j]);
+        }
+        block_sum2(ss, dummy, red);
+        const float inv = 1.f / sqrtf(ss + DORY_EPS);
+#pragma unroll
+        for (int j = 0; j < KC; j++) scale4(x[j], inv);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < KC; j++) {
+      const int c = tid + j * nt;
+      if (c < nch) {
+        reinterpret_cast<float4 *>(xs + (size_t)t * K)[c] = x[j];
+        if (in.mode == IN_RESID && lead && in.h_dst) reinterpret_cast<float4 *>(in.h_dst + (size_t)t * K)[c] = x[j];
+      }
+    }
   }
-  if (lead && in.h_dst)
-    for (int t = 0; t < T; t++)
-      for (int i = tid; i < K; i += nt) in.h_dst[(size_t)t * K + i] = xs[t * K + i];
+  __syncthreads();
 }
 
 // The last block of a q/k/v/g head: RoPE + justnorm (+ s_q^2) and the ring write.
@@ -266,7 +279,7 @@ __device__ void head_epilogue(const HeadEpi &he, int head, int T, float *Y, int 
   if (is_k && kh == 0 && j == 0) reinterpret_cast<int32_t *>(slot + ring.L.tags)[rr] = (int32_t)pos;
 }
 
-template <typename WT, int TT, bool DUAL>
+template <typename WT, int TT, bool DUAL, int KC>
 __global__ void __launch_bounds__(FW * 32, 2) gemv_fused_kernel(const WT *__restrict__ W, int N, int K, int T,
                                                                 GemvIn in, float *__restrict__ Y, int ldy,
                                                                 EpiArgs ep, HeadEpi he) {
@@ -290,7 +303,7 @@ __global__ void __launch_bounds__(FW * 32, 2) gemv_fused_kernel(const WT *__rest
   }
   pdl_wait();
   pdl_trigger();
-  build_input<TT>(in, T, K, xs);
+  build_input<TT, KC>(in, T, K, xs);
 
   float acc0[TT], acc1[TT];
 #pragma unroll
@@ -553,26 +566,11 @@ __global__ void __launch_bounds__(AW * 32) attn_fused_kernel(const float *__rest
   if (!last) return;
   __threadfence();
   const float *pr = part + (size_t)(r * d.nk + kh) * splits * REP * (HD + 2);
-  float vcol = 1.f;
-  const float *g = qkvg + (size_t)r * ldq + (size_t)(d.nh + 2 * d.nk) * HD;
-  for (int i = threadIdx.x; i < REP * HD; i += blockDim.x) {
-    const int h = i / HD, c = i % HD;
-    if (Q8 && frozen) vcol = reinterpret_cast<const float *>(slot + ring.L.vcol)[kh * HD + c];
-    float M = -INFINITY;
-    for (int s = 0; s < splits; s++) M = fmaxf(M, __ldcg(pr + (s * REP + h) * (HD + 2) + HD));
-    float o = 0.f, L = 0.f;
-    for (int s = 0; s < splits; s++) {
-      const float *ps = pr + (s * REP + h) * (HD + 2);
-      const float ms = __ldcg(ps + HD);
-      if (ms == -INFINITY) continue;
-      const float f = expf(ms - M);
-      o += __ldcg(ps + c) * f;
-      L += __ldcg(ps + HD + 1) * f;
-    }
-    const int col = (kh * REP + h) * HD + c;
-    const float y = (L > 0.f ? o / L : 0.f) * vcol;
-    z[(size_t)r * d.nh * HD + col] = y * sigmoidf_(g[col] * sg[col]);
-  }
+  const size_t col0 = (size_t)kh * REP * HD;
+  const float *vcol = (Q8 && frozen) ? reinterpret_cast<const float *>(slot + ring.L.vcol) + (size_t)kh * HD : nullptr;
+  // the warps' partial outputs are no longer needed: their space holds the merge's factors
+  merge_splits<REP, HD>(pr, splits, &wo[0][0][0], qkvg + (size_t)r * ldq + (size_t)(d.nh + 2 * d.nk) * HD + col0,
+                        sg + col0, vcol, z + (size_t)r * d.nh * HD + col0);
 }
 
 template <typename K, typename... Args>
@@ -624,7 +622,7 @@ __device__ __forceinline__ void bulk_copy(uint32_t dst, const void *src, uint32_
                : "memory");
 }
 
-template <int TT, bool DUAL>
+template <int TT, bool DUAL, int KC>
 __global__ void __launch_bounds__(FW * 32) gemv_stream_kernel(const __nv_bfloat16 *__restrict__ W, int N, int K,
                                                               int T, int CH, int ST, GemvIn in,
                                                               float *__restrict__ Y, int ldy, EpiArgs ep, HeadEpi he,
@@ -658,7 +656,7 @@ __global__ void __launch_bounds__(FW * 32) gemv_stream_kernel(const __nv_bfloat1
   }
   pdl_wait();
   pdl_trigger();
-  build_input<TT>(in, T, K, xs);  // ends with __syncthreads
+  build_input<TT, KC>(in, T, K, xs);  // ends with __syncthreads
 
   for (int c = 0; c < nchunks; c++) {
     const int s = c % ST;
@@ -740,8 +738,8 @@ __global__ void __launch_bounds__(FW * 32) gemv_stream_kernel(const __nv_bfloat1
   }
 }
 
-template <int TT, bool DUAL>
-cudaError_t gemv_stream_t(const void *W, int N, int K, int T, GemvIn in, float *Y, int ldy, EpiArgs ep, HeadEpi he,
+template <int TT, bool DUAL, int KC>
+cudaError_t gemv_stream_k(const void *W, int N, int K, int T, GemvIn in, float *Y, int ldy, EpiArgs ep, HeadEpi he,
                           int *err, bool pdl, cudaStream_t s) {
   static int sms = 0;
   if (!sms) {
@@ -762,7 +760,7 @@ cudaError_t gemv_stream_t(const void *W, int N, int K, int T, GemvIn in, float *
   ST = (int)std::min<size_t>(ST, std::max<size_t>(2, wbudget / (CH * row_bytes)));
   ST = std::min(ST, 8);
   const size_t smem = xs_bytes + 128 + (size_t)ST * CH * row_bytes;
-  auto kern = gemv_stream_kernel<TT, DUAL>;
+  auto kern = gemv_stream_kernel<TT, DUAL, KC>;
   static bool attr = false;
   if (!attr) {
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
@@ -771,6 +769,16 @@ cudaError_t gemv_stream_t(const void *W, int N, int K, int T, GemvIn in, float *
   const int grid = std::min(sms, N);
   return launch_pdl(kern, dim3(grid), dim3(FW * 32), smem, pdl, s, static_cast<const __nv_bfloat16 *>(W), N, K, T, CH,
                     ST, in, Y, ldy, ep, he, err);
+}
+
+template <int TT, bool DUAL>
+cudaError_t gemv_stream_t(const void *W, int N, int K, int T, GemvIn in, float *Y, int ldy, EpiArgs ep, HeadEpi he,
+                          int *err, bool pdl, cudaStream_t s) {
+  const int kc = (K / 4 + FW * 32 - 1) / (FW * 32);
+  if (kc <= 2) return gemv_stream_k<TT, DUAL, 2>(W, N, K, T, in, Y, ldy, ep, he, err, pdl, s);
+  if (kc <= 4) return gemv_stream_k<TT, DUAL, 4>(W, N, K, T, in, Y, ldy, ep, he, err, pdl, s);
+  if (kc <= 6) return gemv_stream_k<TT, DUAL, 6>(W, N, K, T, in, Y, ldy, ep, he, err, pdl, s);
+  return gemv_stream_k<TT, DUAL, 8>(W, N, K, T, in, Y, ldy, ep, he, err, pdl, s);
 }
 
 template <bool DUAL>
@@ -783,10 +791,10 @@ cudaError_t gemv_stream_d(const void *W, int N, int K, int T, GemvIn in, float *
   }
 }
 
-template <typename WT, int TT, bool DUAL>
-cudaError_t gemv_fused_t(const void *W, int N, int K, int T, GemvIn in, float *Y, int ldy, EpiArgs ep, HeadEpi he,
+template <typename WT, int TT, bool DUAL, int KC>
+cudaError_t gemv_fused_k(const void *W, int N, int K, int T, GemvIn in, float *Y, int ldy, EpiArgs ep, HeadEpi he,
                          bool pdl, cudaStream_t s) {
-  auto kern = gemv_fused_kernel<WT, TT, DUAL>;
+  auto kern = gemv_fused_kernel<WT, TT, DUAL, KC>;
   const size_t smem = (size_t)T * K * sizeof(float);
   static bool attr_done = false;
   if (!attr_done) {
@@ -795,6 +803,16 @@ cudaError_t gemv_fused_t(const void *W, int N, int K, int T, GemvIn in, float *Y
   }
   dim3 grid((N + FW - 1) / FW);
   return launch_pdl(kern, grid, dim3(FW * 32), smem, pdl, s, static_cast<const WT *>(W), N, K, T, in, Y, ldy, ep, he);
+}
+
+template <typename WT, int TT, bool DUAL>
+cudaError_t gemv_fused_t(const void *W, int N, int K, int T, GemvIn in, float *Y, int ldy, EpiArgs ep, HeadEpi he,
+                         bool pdl, cudaStream_t s) {
+  const int kc = (K / 4 + FW * 32 - 1) / (FW * 32);
+  if (kc <= 2) return gemv_fused_k<WT, TT, DUAL, 2>(W, N, K, T, in, Y, ldy, ep, he, pdl, s);
+  if (kc <= 4) return gemv_fused_k<WT, TT, DUAL, 4>(W, N, K, T, in, Y, ldy, ep, he, pdl, s);
+  if (kc <= 6) return gemv_fused_k<WT, TT, DUAL, 6>(W, N, K, T, in, Y, ldy, ep, he, pdl, s);
+  return gemv_fused_k<WT, TT, DUAL, 8>(W, N, K, T, in, Y, ldy, ep, he, pdl, s);
 }
 
 template <typename WT, bool DUAL>
@@ -834,7 +852,7 @@ cudaError_t attn_fused_q(const float *qkvg, int ldq, Dims d, Rows rows, Ring rin
 
 cudaError_t launch_gemv_fused(const void *W, int wdtype, int N, int K, int T, GemvIn in, float *Y, int ldy,
                               EpiArgs ep, HeadEpi he, int *err, bool pdl, cudaStream_t s) {
-  if (T < 1 || T > MAXT || K % 8 != 0 || (size_t)T * K * 4 > 96 * 1024) return cudaErrorInvalidValue;
+  if (T < 1 || T > MAXT || K % 8 != 0 || K > 8192 || (size_t)T * K * 4 > 96 * 1024) return cudaErrorInvalidValue;
   if (he.enabled && ((he.d.hd / 2) % 32 != 0 || T * (he.d.hd / 2) > FW * 32)) return cudaErrorInvalidValue;
   const bool dual = ep.mode == EPI_SILU;
   static const bool stream_off = [] {

@@ -112,6 +112,30 @@ __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.lau
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
+__device__ __forceinline__ void cluster_sync() {
+  __syncwarp();  // the .aligned barrier wants the whole warp converged
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// float4 at a shared address of block `rank` of the cluster
+__device__ __forceinline__ float4 ld_cluster4(uint32_t local, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(remote)
+               : "memory");
+  return v;
+}
+
 template <int BN, bool DUAL, int ST>
 struct TcSmem {
   static constexpr int A_BYTES = BM * BK * 2;
@@ -241,6 +265,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   pdl_trigger();
 
   // epilogue: warps 2..5, warp w reads TMEM lanes 32*(w % 4) ..
+  // With split K the blocks of a tile form a cluster: each parks its fp32 partial tile
+  // in its own (drained) stage memory as P[m][BN + 4] (gate, then up), and after a cluster
+  // barrier block r adds the splits' partials for its slice of the tile's rows over DSMEM.
+  constexpr int PS = BN + 4;  // padded row: conflict-free float4 stores
+  float *P = reinterpret_cast<float *>(smem_raw + (base - smem_u32(smem_raw)));
+  const int tcount = (T - t0) < BN ? (T - t0) : BN;  // valid step rows in this tile
+  auto epi = [&](float a, float b, int n) {
+    if (ep.mode == EPI_SCALE) return a * ep.vec[n];
+    if (ep.mode == EPI_SILU) {
+      const float g = a * ep.vec[n];
+      return g * sigmoidf_(g) * (b * ep.vec2[n]);
+    }
+    return a;
+  };
   if (warp >= 2) {
     const int q = warp & 3;
     const int m = q * 32 + lane;  // row within the tile
@@ -251,8 +289,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       failed = 1;
     }
     fence_after();
-    const int tcount = (T - t0) < BN ? (T - t0) : BN;  // valid step rows in this tile
-    float *wsp = ws + ((size_t)(tile * gridDim.y + blockIdx.y) * splits + split) * (DUAL ? 2 : 1) * BN * BM;
     if (ok && !failed) {
       for (int c = 0; c < BN; c += 16) {
         float v[16], u[16];
@@ -262,59 +298,49 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 #pragma unroll
           for (int i = 0; i < 16; i++) {
             const int t = c + i;
-            if (t < tcount && n < N) {
-              float y = v[i];
-              if (ep.mode == EPI_SCALE) {
-                y = v[i] * ep.vec[n];
-              } else if (ep.mode == EPI_SILU) {
-                const float g = v[i] * ep.vec[n];
-                y = g * sigmoidf_(g) * (u[i] * ep.vec2[n]);
-              }
-              Y[(size_t)(t0 + t) * ldy + n] = y;
-            }
+            if (t < tcount && n < N) Y[(size_t)(t0 + t) * ldy + n] = epi(v[i], DUAL ? u[i] : 0.f, n);
           }
         } else {
 #pragma unroll
-          for (int i = 0; i < 16; i++) {
-            wsp[(size_t)(c + i) * BM + m] = v[i];
-            if (DUAL) wsp[(size_t)(BN + c + i) * BM + m] = u[i];
+          for (int i = 0; i < 16; i += 4) {
+            *reinterpret_cast<float4 *>(P + (size_t)m * PS + c + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+            if (DUAL)
+              *reinterpret_cast<float4 *>(P + (size_t)(BM + m) * PS + c + i) =
+                  make_float4(u[i], u[i + 1], u[i + 2], u[i + 3]);
           }
         }
       }
     }
-    if (splits > 1) {
-      __threadfence();
-      epi_bar();
-      if (warp == 2 && lane == 0) {
-        int *ctr = tile_ctr + tile * gridDim.y + blockIdx.y;
-        const int old = atomicAdd(ctr, 1);
-        is_last = old == splits - 1;
-        if (is_last) *ctr = 0;
-      }
-      epi_bar();
-      if (is_last) {
-        __threadfence();
-        const float *w0 = ws + (size_t)(tile * gridDim.y + blockIdx.y) * splits * (DUAL ? 2 : 1) * BN * BM;
-        for (int t = 0; t < tcount; t++) {
-          float a = 0.f, b = 0.f;
-          for (int sp = 0; sp < splits; sp++) {
-            const float *p = w0 + (size_t)sp * (DUAL ? 2 : 1) * BN * BM;
-            a += __ldcg(p + (size_t)t * BM + m);
-            if (DUAL) b += __ldcg(p + (size_t)(BN + t) * BM + m);
+  }
+  if (splits > 1) {
+    cluster_sync();  // every block's partial tile is in place
+    if (warp >= 2) {
+      const int q = warp & 3;
+      const int m = q * 32 + lane;
+      const int n = n0 + m;
+      const uint32_t rank = cluster_rank();
+      const int per = ((tcount + splits - 1) / splits + 3) & ~3;  // rows per block, whole float4s
+      const int ta = (int)rank * per, tb = min(tcount, ta + per);
+      const uint32_t pa = smem_u32(P + (size_t)m * PS), pu = smem_u32(P + (size_t)(BM + m) * PS);
+      for (int t = ta; t < tb; t += 4) {
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+        for (int sp = 0; sp < splits; sp++) {
+          const float4 x = ld_cluster4(pa + t * 4, (uint32_t)sp);
+          a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
+          if (DUAL) {
+            const float4 y = ld_cluster4(pu + t * 4, (uint32_t)sp);
+            b.x += y.x; b.y += y.y; b.z += y.z; b.w += y.w;
           }
-          if (n < N) {
-            float y = a;
-            if (ep.mode == EPI_SCALE) {
-              y = a * ep.vec[n];
-            } else if (ep.mode == EPI_SILU) {
-              const float g = a * ep.vec[n];
-              y = g * sigmoidf_(g) * (b * ep.vec2[n]);
-            }
-            Y[(size_t)(t0 + t) * ldy + n] = y;
-          }
+        }
+        if (n < N) {
+          const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+          for (int u = 0; u < 4; u++)
+            if (t + u < tb) Y[(size_t)(t0 + t + u) * ldy + n] = epi(av[u], bv[u], n);
         }
       }
     }
+    cluster_sync();  // no block leaves while another reads its shared memory
   }
   fence_before();
   __syncthreads();
@@ -339,17 +365,31 @@ cudaError_t tc_launch(const TcGemm &g, int T, int t_base, float *Y, int ldy, Epi
   }
   const int m_tiles = (g.N + BM - 1) / BM;
   const int t_tiles = (T + BN - 1) / BN;
+  int splits = g.splits;
+  // the partial tile of a split must fit the stage memory it reuses
+  if ((size_t)BM * (BN + 4) * 4 * (DUAL ? 2 : 1) > (size_t)ST * S::STAGE || t_tiles > 1) splits = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(m_tiles * g.splits, t_tiles);
+  cfg.gridDim = dim3(m_tiles * splits, t_tiles);
   cfg.blockDim = dim3(TC_THREADS);
   cfg.dynamicSmemBytes = S::TOTAL;
   cfg.stream = s;
-  cudaLaunchAttribute attr1[1];
-  attr1[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr1[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr1[2];
+  int na = 0;
+  if (pdl) {
+    attr1[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr1[na].val.programmaticStreamSerializationAllowed = 1;
+    na++;
+  }
+  if (splits > 1) {
+    attr1[na].id = cudaLaunchAttributeClusterDimension;
+    attr1[na].val.clusterDim.x = splits;
+    attr1[na].val.clusterDim.y = 1;
+    attr1[na].val.clusterDim.z = 1;
+    na++;
+  }
   cfg.attrs = attr1;
-  cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kern, g.tmW, g.tmXh, g.tmXl, g.N, g.K, T, t_base, g.splits, g.pair_rows, g.ws,
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, kern, g.tmW, g.tmXh, g.tmXl, g.N, g.K, T, t_base, splits, g.pair_rows, g.ws,
                             g.ctr, Y, ldy, ep, g.err);
 }
 

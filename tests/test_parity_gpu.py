@@ -224,7 +224,7 @@ def test_state_and_range_errors():
     P = Pair(cfg, 2009)
     try:
         g = P.gpu
-        assert g.slot_info(1)[0] == 128
+        assert g.slot_info(2)[0] == 128  # the recurrent full layer
         with pytest.raises(DoryError) as e:
             g.prefill_chunk(0, [1, 2], 5, 2, "last")
         assert e.value.code == -4
