@@ -61,59 +61,3 @@ __device__ __forceinline__ float load_w(const __nv_bfloat16 *p, size_t i) { retu
 __device__ __forceinline__ float sigmoidf_(float x) { return 1.f / (1.f + expf(-x)); }
 
 }  // namespace dory
-
-namespace dory {
-
-// Merge the split-KV partials of one (row, kv head) and apply the output gate.
-// Split s left, per query head h of the group, o[HD] (unnormalised) then m and l at
-// pr[(s * REP + h) * (HD + 2)]. y = sum_s o_s e^(m_s - M) / sum_s l_s e^(m_s - M), times
-// vcol (q8_2f, once frozen), then z = y * sigmoid(g * sg). The maxima and sums of all
-// splits go to shared memory first (`sm`, 2 * REP * splits floats), every partial output
-// is read with eight independent loads in flight per thread.
-template <int REP, int HD>
-__device__ void merge_splits(const float *pr, int splits, float *sm, const float *g, const float *sg,
-                             const float *vcol, float *zrow) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  float *fm = sm, *fl = sm + REP * splits;
-  for (int i = threadIdx.x; i < REP * splits; i += blockDim.x) {
-    const int sp = i / REP, h = i % REP;
-    fm[i] = __ldcg(pr + (size_t)(sp * REP + h) * (HD + 2) + HD);
-    fl[i] = __ldcg(pr + (size_t)(sp * REP + h) * (HD + 2) + HD + 1);
-  }
-  __syncthreads();
-  for (int h = warp; h < REP; h += nw) {
-    float M = -INFINITY;
-    for (int sp = lane; sp < splits; sp += 32) M = fmaxf(M, fm[sp * REP + h]);
-    M = warp_max(M);
-    float L = 0.f;
-    for (int sp = lane; sp < splits; sp += 32) {
-      const float m = fm[sp * REP + h];
-      if (m != -INFINITY) L += fl[sp * REP + h] * expf(m - M);
-    }
-    L = warp_sum(L);
-    __syncwarp();
-    for (int sp = lane; sp < splits; sp += 32) {
-      const float m = fm[sp * REP + h];
-      fm[sp * REP + h] = (m == -INFINITY || !(L > 0.f)) ? 0.f : expf(m - M) / L;
-    }
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < REP * HD; i += blockDim.x) {
-    const int h = i / HD, c = i % HD;
-    const float *base = pr + (size_t)h * (HD + 2) + c;
-    float o = 0.f;
-    int sp = 0;
-    for (; sp + 8 <= splits; sp += 8) {
-      float v[8];
-#pragma unroll
-      for (int u = 0; u < 8; u++) v[u] = __ldcg(base + (size_t)(sp + u) * REP * (HD + 2));
-#pragma unroll
-      for (int u = 0; u < 8; u++) o = fmaf(v[u], fm[(sp + u) * REP + h], o);
-    }
-    for (; sp < splits; sp++) o = fmaf(__ldcg(base + (size_t)sp * REP * (HD + 2)), fm[sp * REP + h], o);
-    const float y = o * (vcol ? vcol[c] : 1.f);
-    zrow[i] = y * sigmoidf_(g[i] * sg[i]);
-  }
-}
-
-}  // namespace dory

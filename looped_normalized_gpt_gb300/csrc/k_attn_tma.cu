@@ -13,6 +13,7 @@
 #include <climits>
 
 #include "common.cuh"
+#include "fused_body.cuh"
 #include "kernels.h"
 
 namespace dory {
@@ -189,7 +190,7 @@ __global__ void __launch_bounds__(128) attn_tma_kernel(const __grid_constant__ C
   __threadfence();
   const float *pr = part + (size_t)(r * d.nk + kh) * splits * REP * (HD + 2);
   const size_t col0 = (size_t)kh * REP * HD;
-  merge_splits<REP, HD>(pr, splits, Ks, qkvg + (size_t)r * ldq + (size_t)(d.nh + 2 * d.nk) * HD + col0, sg + col0,
+  merge_splits<REP, HD>(BlockTeam{}, pr, splits, Ks, qkvg + (size_t)r * ldq + (size_t)(d.nh + 2 * d.nk) * HD + col0, sg + col0,
                         nullptr, z + (size_t)r * d.nh * HD + col0);
 }
 
@@ -384,7 +385,7 @@ __global__ void __launch_bounds__(128) attn_tma_q8_kernel(const __grid_constant_
   const float *pr = part + (size_t)(r * d.nk + kh) * splits * REP * (HD + 2);
   const float *vcol = reinterpret_cast<const float *>(slot + ring.L.vcol) + (size_t)kh * HD;
   const size_t col0 = (size_t)kh * REP * HD;
-  merge_splits<REP, HD>(pr, splits, reinterpret_cast<float *>(Kq), qkvg + (size_t)r * ldq +
+  merge_splits<REP, HD>(BlockTeam{}, pr, splits, reinterpret_cast<float *>(Kq), qkvg + (size_t)r * ldq +
                         (size_t)(d.nh + 2 * d.nk) * HD + col0, sg + col0, frozen ? vcol : nullptr,
                         z + (size_t)r * d.nh * HD + col0);
 }

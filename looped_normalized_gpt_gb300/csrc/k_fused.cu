@@ -18,6 +18,7 @@
 #include <cstdlib>
 
 #include "common.cuh"
+#include "fused_body.cuh"
 #include "kernels.h"
 
 namespace dory {
@@ -56,229 +57,6 @@ struct Chunk<float> {
   }
 };
 
-// Sum of v over the block for up to MAXT values at once (one per row).
-template <int NT>
-__device__ __forceinline__ void block_sum_n(float *v, float (*red)[FW]) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int t = 0; t < NT; t++) v[t] = warp_sum(v[t]);
-  __syncthreads();
-  if (lane == 0)
-#pragma unroll
-    for (int t = 0; t < NT; t++) red[t][warp] = v[t];
-  __syncthreads();
-#pragma unroll
-  for (int t = 0; t < NT; t++) {
-    float s = 0.f;
-#pragma unroll
-    for (int w = 0; w < FW; w++) s += red[t][w];
-    v[t] = s;
-  }
-  __syncthreads();
-}
-
-// Sums of two values over the block (every thread gets both).
-__device__ __forceinline__ void block_sum2(float &a, float &b, float (*red)[FW]) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  a = warp_sum(a);
-  b = warp_sum(b);
-  __syncthreads();
-  if (lane == 0) {
-    red[0][warp] = a;
-    red[1][warp] = b;
-  }
-  __syncthreads();
-  a = b = 0.f;
-#pragma unroll
-  for (int w = 0; w < FW; w++) {
-    a += red[0][w];
-    b += red[1][w];
-  }
-}
-
-// Prologue: the block's input rows xs[t][K] from the previous kernels' outputs. Each
-// thread owns the float4 chunks tid + j * blockDim of a row (KC of them at most) and loads
-// all the vectors it needs for them at once, so a row costs one memory round trip; the
-// reductions pair up their sums.
-template <int TT, int KC>
-__device__ void build_input(const GemvIn &in, int T, int K, float *xs) {
-  __shared__ float red[2][FW];
-  const int tid = threadIdx.x, nt = blockDim.x;
-  const int nch = K / 4;
-  const bool lead = blockIdx.x == 0;
-  for (int t = 0; t < T; t++) {
-    const float4 *src = reinterpret_cast<const float4 *>(in.src + (size_t)t * in.ld);
-    float4 x[KC], o[KC], al[KC], inp[KC];
-#pragma unroll
-    for (int j = 0; j < KC; j++) {
-      const int c = tid + j * nt;
-      x[j] = o[j] = al[j] = inp[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (c < nch) {
-        x[j] = src[c];
-        if (in.mode == IN_RESID && in.alpha) {
-          o[j] = reinterpret_cast<const float4 *>(in.out + (size_t)t * K)[c];
-          al[j] = reinterpret_cast<const float4 *>(in.alpha)[c];
-        }
-        if (in.mode == IN_RESID && in.mix == MIX_LOOP) inp[j] = reinterpret_cast<const float4 *>(in.input + (size_t)t * K)[c];
-      }
-    }
-    auto sq4 = [](const float4 &v) { return v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w; };
-    auto scale4 = [](float4 &v, float f) {
-      v.x *= f;
-      v.y *= f;
-      v.z *= f;
-      v.w *= f;
-    };
-    if (in.mode == IN_NORM) {
-      float ss = 0.f, dummy = 0.f;
-#pragma unroll
-      for (int j = 0; j < KC; j++) ss += sq4(x[j]);
-      block_sum2(ss, dummy, red);
-      const float inv = 1.f / sqrtf(ss + DORY_EPS);
-#pragma unroll
-      for (int j = 0; j < KC; j++) scale4(x[j], inv);
-    } else if (in.mode == IN_RESID) {
-      if (in.alpha) {
-        float sx = 0.f, so = 0.f;
-#pragma unroll
-        for (int j = 0; j < KC; j++) {
-          sx += sq4(x[j]);
-          so += sq4(o[j]);
-        }
-        block_sum2(sx, so, red);
-        const float ix = 1.f / sqrtf(sx + DORY_EPS), io = 1.f / sqrtf(so + DORY_EPS);
-        float sr = 0.f, dummy = 0.f;
-#pragma unroll
-        for (int j = 0; j < KC; j++) {
-          float4 xh = x[j], oh = o[j];
-          scale4(xh, ix);
-          scale4(oh, io);
-          x[j] = make_float4(xh.x + al[j].x * (oh.x - xh.x), xh.y + al[j].y * (oh.y - xh.y),
-                             xh.z + al[j].z * (oh.z - xh.z), xh.w + al[j].w * (oh.w - xh.w));
-          sr += sq4(x[j]);
-        }
-        block_sum2(sr, dummy, red);
-        const float inv = 1.f / sqrtf(sr + DORY_EPS);
-#pragma unroll
-        for (int j = 0; j < KC; j++) scale4(x[j], inv);
-      }
-      if (in.mix == MIX_LOOP || in.mix == MIX_END) {  // state = h^
-        float ss = 0.f, dummy = 0.f;
-#pragma unroll
-        for (int j = 0; j < KC; j++) ss += sq4(x[j]);
-        block_sum2(ss, dummy, red);
-        const float inv = 1.f / sqrtf(ss + DORY_EPS);
-#pragma unroll
-        for (int j = 0; j < KC; j++) {
-          scale4(x[j], inv);
-          const int c = tid + j * nt;
-          if (lead && c < nch) reinterpret_cast<float4 *>(in.state + (size_t)t * K)[c] = x[j];
-        }
-      }
-      if (in.mix == MIX_BEGIN || in.mix == MIX_LOOP) {  // h = (state + input)^
-        float ss = 0.f, dummy = 0.f;
-#pragma unroll
-        for (int j = 0; j < KC; j++) {
-          const int c = tid + j * nt;
-          if (in.mix == MIX_BEGIN) {
-            inp[j] = x[j];
-            if (lead && c < nch) {
-              reinterpret_cast<float4 *>(in.input + (size_t)t * K)[c] = x[j];
-              reinterpret_cast<float4 *>(in.state + (size_t)t * K)[c] = x[j];
-            }
-          }
-          x[j] = make_float4(x[j].x + inp[j].x, x[j].y + inp[j].y, x[j].z + inp[j].z, x[j].w + inp[j].w);
-          ss += sq4(x[j]);
-        }
-        block_sum2(ss, dummy, red);
-        const float inv = 1.f / sqrtf(ss + DORY_EPS);
-#pragma unroll
-        for (int j = 0; j < KC; j++) scale4(x[j], inv);
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < KC; j++) {
-      const int c = tid + j * nt;
-      if (c < nch) {
-        reinterpret_cast<float4 *>(xs + (size_t)t * K)[c] = x[j];
-        if (in.mode == IN_RESID && lead && in.h_dst) reinterpret_cast<float4 *>(in.h_dst + (size_t)t * K)[c] = x[j];
-      }
-    }
-  }
-  __syncthreads();
-}
-
-// The last block of a q/k/v/g head: RoPE + justnorm (+ s_q^2) and the ring write.
-__device__ void head_epilogue(const HeadEpi &he, int head, int T, float *Y, int ldy) {
-  __shared__ float red2[MAXT][FW];
-  const Dims &d = he.d;
-  const int hd = d.hd, half = hd / 2;
-  const int tid = threadIdx.x;
-  const int t = tid / half, j = tid % half;  // blockDim 256 >= T * half for hd <= 128
-  const bool act = t < T;
-  const bool is_q = head < d.nh, is_k = head >= d.nh && head < d.nh + d.nk;
-  const bool is_v = head >= d.nh + d.nk && head < d.nh + 2 * d.nk;
-  if (!(is_q || is_k || is_v)) return;  // gate heads need nothing (block-uniform)
-  float a = 0.f, b = 0.f;
-  float *row = Y + (size_t)(act ? t : 0) * ldy + head * hd;
-  if (act) {
-    a = __ldcg(row + j);
-    b = __ldcg(row + j + half);
-  }
-  if (is_q || is_k) {
-    if (act) {
-      const float *cs = he.rope + ((size_t)t * 2 + he.kind) * hd;
-      const float *sn = cs + half;
-      const float x = a, y = b;
-      a = x * cs[j] - y * sn[j];
-      b = y * cs[j] + x * sn[j];
-    }
-    // per-row sums over the row's half threads (two warps when hd = 128)
-    float ss[MAXT] = {0.f, 0.f, 0.f, 0.f};
-    float v = act ? a * a + b * b : 0.f;
-    v = warp_sum(v);
-    const int lane = tid & 31, warp = tid >> 5;
-    __syncthreads();
-    if (lane == 0) red2[0][warp] = v;
-    __syncthreads();
-    const int wpr = (half + 31) / 32;  // warps per row
-    if (act) {
-      float s = 0.f;
-      for (int w = 0; w < wpr; w++) s += red2[0][t * wpr + w];
-      ss[0] = s;
-      const float inv = 1.f / sqrtf(ss[0] + DORY_EPS);
-      a *= inv;
-      b *= inv;
-    }
-  }
-  if (!act) return;
-  if (is_q) {
-    row[j] = a * he.sq[head * hd + j];
-    row[j + half] = b * he.sq[head * hd + j + half];
-    return;
-  }
-  const int kh = is_k ? head - d.nh : head - d.nh - d.nk;
-  if (is_k) {  // rotated, normalised key back into the projection rows for reference
-    row[j] = a;
-    row[j + half] = b;
-  }
-  const Ring &ring = he.ring;
-  if (ring.q8) {
-    float *dst = (is_k ? he.kst : he.vst) + ((size_t)t * d.nk + kh) * hd;
-    dst[j] = a;
-    dst[j + half] = b;
-    return;
-  }
-  const int seq = he.rows.seq[t];
-  const long pos = (long)he.rows.seq_pos[seq] + he.rows.off[t];
-  const int rr = (int)(pos % ring.cap);
-  char *slot = ring.base + (size_t)seq * ring.seq_stride + ring.off;
-  float *dst = reinterpret_cast<float *>(slot + (is_k ? ring.L.k : ring.L.v)) + ((size_t)kh * ring.cap + rr) * hd;
-  dst[j] = a;
-  dst[j + half] = b;
-  if (is_k && kh == 0 && j == 0) reinterpret_cast<int32_t *>(slot + ring.L.tags)[rr] = (int32_t)pos;
-}
-
 template <typename WT, int TT, bool DUAL, int KC>
 __global__ void __launch_bounds__(FW * 32, 2) gemv_fused_kernel(const WT *__restrict__ W, int N, int K, int T,
                                                                 GemvIn in, float *__restrict__ Y, int ldy,
@@ -303,7 +81,7 @@ __global__ void __launch_bounds__(FW * 32, 2) gemv_fused_kernel(const WT *__rest
   }
   pdl_wait();
   pdl_trigger();
-  build_input<TT, KC>(in, T, K, xs);
+  build_input<TT, KC>(BlockTeam{}, in, T, K, xs, blockIdx.x == 0);
 
   float acc0[TT], acc1[TT];
 #pragma unroll
@@ -379,7 +157,7 @@ __global__ void __launch_bounds__(FW * 32, 2) gemv_fused_kernel(const WT *__rest
   __syncthreads();
   if (!last) return;
   __threadfence();
-  head_epilogue(he, head, T, Y, ldy);
+  head_epilogue(BlockTeam{}, he, head, T, Y, ldy);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -569,7 +347,7 @@ __global__ void __launch_bounds__(AW * 32) attn_fused_kernel(const float *__rest
   const size_t col0 = (size_t)kh * REP * HD;
   const float *vcol = (Q8 && frozen) ? reinterpret_cast<const float *>(slot + ring.L.vcol) + (size_t)kh * HD : nullptr;
   // the warps' partial outputs are no longer needed: their space holds the merge's factors
-  merge_splits<REP, HD>(pr, splits, &wo[0][0][0], qkvg + (size_t)r * ldq + (size_t)(d.nh + 2 * d.nk) * HD + col0,
+  merge_splits<REP, HD>(BlockTeam{}, pr, splits, &wo[0][0][0], qkvg + (size_t)r * ldq + (size_t)(d.nh + 2 * d.nk) * HD + col0,
                         sg + col0, vcol, z + (size_t)r * d.nh * HD + col0);
 }
 
@@ -656,7 +434,7 @@ __global__ void __launch_bounds__(FW * 32) gemv_stream_kernel(const __nv_bfloat1
   }
   pdl_wait();
   pdl_trigger();
-  build_input<TT, KC>(in, T, K, xs);  // ends with __syncthreads
+  build_input<TT, KC>(BlockTeam{}, in, T, K, xs, blockIdx.x == 0);  // ends with __syncthreads
 
   for (int c = 0; c < nchunks; c++) {
     const int s = c % ST;
@@ -732,7 +510,7 @@ __global__ void __launch_bounds__(FW * 32) gemv_stream_kernel(const __nv_bfloat1
     __syncthreads();
     if (last_sh) {
       __threadfence();
-      head_epilogue(he, h, T, Y, ldy);
+      head_epilogue(BlockTeam{}, he, h, T, Y, ldy);
     }
     __syncthreads();
   }
