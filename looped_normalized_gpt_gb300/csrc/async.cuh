@@ -1,0 +1,76 @@
+// Asynchronous-copy helpers (sm_100+ PTX): shared-memory mbarriers with bounded waits,
+// the untiled bulk copy global -> shared, proxy fences and gpu-scope counters.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dory {
+
+// try_wait rounds before a wait gives up (each round suspends for a bounded time in the
+// hardware, so the limit is well above any legitimate wait)
+constexpr uint32_t MBAR_WAIT_LIMIT = 1u << 20;
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_fence_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase of parity `parity` to complete; false when the limit ran out or
+// `*stop` became nonzero (stop may be null).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int *stop = nullptr) {
+  for (uint32_t i = 0; i < MBAR_WAIT_LIMIT; i++) {
+    if (mbar_test(bar, parity)) return true;
+    if (stop && *stop) return false;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+// `bytes` (a multiple of 16, both addresses 16-byte aligned) from global to shared memory,
+// completion counted on `bar`
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+// Order this thread's generic-proxy global writes before later async-proxy (bulk copy)
+// reads of the same memory, and the reverse on the reading side.
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+// Order earlier generic-proxy accesses of shared memory (after a barrier, the whole team's)
+// before a bulk copy that overwrites it.
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ int ld_acquire_gpu(const int *p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void red_release_gpu_add(int *p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+}  // namespace dory

@@ -59,6 +59,7 @@ int bn_index(int bn) { return bn <= 16 ? 0 : bn <= 32 ? 1 : bn <= 64 ? 2 : bn <=
 struct Plan {
   cudaGraphExec_t exec = nullptr;
   int32_t *rt = nullptr;  // the captured step's own row table
+  MegaStage *stages = nullptr;  // the persistent decode kernel's stage list (device)
   int launches = 0, gemm_launches = 0;
   float *h_last = nullptr;
 };
@@ -95,6 +96,14 @@ struct dory_handle {
   float *h2 = nullptr, *h_last = nullptr;  // second hidden buffer (fused path), final rows
   int32_t *hctr = nullptr, *actr = nullptr;  // arrival counters of the fused kernels
   bool fused_ok = false;
+  // persistent batch-1 decode: one block per SM; counters zeroed before each launch:
+  // [0] grid barrier, [1] RoPE entries, [64..) per-head arrivals, then per-kv-head items
+  bool mega_ok = false;
+  int sms = 0;
+  int32_t *mega_sync = nullptr;
+  size_t mega_sync_bytes = 0;
+  MegaStage *mega_stages = nullptr;  // stage list of the launches issued without graphs
+  size_t mega_cap = 0;
   // tensor-core projections: weight maps per layer ([0] q/k/v/g or gate/up, [1] o or down)
   bool tc_ok = false;
   std::vector<std::array<TcW, 2>> tcw;
@@ -188,7 +197,11 @@ void free_all(dory_t *d) {
   for (auto &kv : d->plans) {
     if (kv.second.exec) cudaGraphExecDestroy(kv.second.exec);
     if (kv.second.rt) cudaFree(kv.second.rt);
+    if (kv.second.stages) cudaFree(kv.second.stages);
   }
+  if (d->mega_stages) cudaFree(d->mega_stages);
+  d->mega_stages = nullptr;
+  d->mega_cap = 0;
   d->plans.clear();
   if (d->cap_stream) cudaStreamDestroy(d->cap_stream);
   d->cap_stream = nullptr;
@@ -591,6 +604,163 @@ int issue_any(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_splits, cuda
   return issue_step(d, a, rt, fixed_splits, s, nl, ng);
 }
 
+// The persistent kernel runs steps of one row that end with that row's logits.
+bool use_mega(const dory_t *d, const StepArgs &a) {
+  return d->mega_ok && a.T == 1 && a.head_rows == 1 && a.head_from == 0 && a.aseq.size() == 1;
+}
+
+// The stage list of a one-row step, in the order of issue_step_fused's launches.
+int mega_build(dory_t *d, const StepArgs &a, int32_t *rt, std::vector<MegaStage> &out, float **h_last) {
+  const dory_config &c = d->cfg;
+  const Dims dm = d->dims;
+  const int q_size = dm.nh * dm.hd, kv_size = dm.nk * dm.hd;
+  const int ldq = 2 * q_size + 2 * kv_size;
+  Rows rows;
+  rows.seq = rt;
+  rows.off = rt + d->Tmax;
+  rows.seq_pos = d->d_seq_pos;
+  rows.n = 1;
+  out.clear();
+  float *cur = d->h, *other = d->h2;
+  bool first = true;
+  struct {
+    bool on = false;
+    const float *alpha = nullptr;
+    int mix = MIX_NONE;
+  } pend;
+  auto first_in = [&]() {
+    GemvIn g{};
+    g.ld = dm.hidden;
+    if (first) {  // the token's embedding row, stored as the hidden row
+      first = false;
+      g.mode = IN_EMBED;
+      g.ids = d->d_ids;
+      g.embed = static_cast<const __nv_bfloat16 *>(d->embed);
+      g.vocab = dm.vocab;
+      g.h_dst = cur;
+      return g;
+    }
+    if (!pend.on) {
+      g.mode = IN_PLAIN;
+      g.src = cur;
+      return g;
+    }
+    g.mode = IN_RESID;
+    g.src = cur;
+    g.out = d->out;
+    g.alpha = pend.alpha;
+    g.mix = pend.mix;
+    g.h_dst = other;
+    g.input = d->input;
+    g.state = d->state;
+    std::swap(cur, other);
+    pend.on = false;
+    return g;
+  };
+  auto gemv = [&](const void *W, int N, int K, long pair, const GemvIn &in, float *Y, EpiArgs ep,
+                  const HeadEpi *he) {
+    MegaStage st{};
+    st.kind = MK_GEMV;
+    st.W = static_cast<const __nv_bfloat16 *>(W);
+    st.N = N;
+    st.K = K;
+    st.pair = pair;
+    st.R = mega_chunk_rows(K, pair > 0);
+    st.in = in;
+    st.Y = Y;
+    st.ep = ep;
+    if (he) st.he = *he;
+    else st.he.enabled = 0;
+    out.push_back(st);
+  };
+  int32_t *heads = d->mega_sync + 64;
+  auto layer = [&](int li, int loop_i, int mix) {
+    const LayerDev &L = d->layers[li];
+    if (L.attn) {
+      const int sl = (c.kv_mode == DORY_KV_PER_LOOP && L.rec) ? loop_i : 0;
+      const Ring ring = d->ring(L.ordinal, sl);
+      HeadEpi he{};
+      he.enabled = 1;
+      he.counters = heads;
+      he.d = dm;
+      he.rows = rows;
+      he.rope = d->rope;
+      he.kind = L.sliding ? 0 : 1;
+      he.sq = L.sq;
+      he.ring = ring;
+      gemv(L.wqkvg, ldq, dm.hidden, 0, first_in(), d->qkvg, EpiArgs{EPI_STORE, nullptr, nullptr, 0}, &he);
+      MegaStage at{};
+      at.kind = MK_ATTN;
+      at.ring = ring;
+      at.qkvg = d->qkvg;
+      at.sg = L.sg;
+      at.z = d->z;
+      at.part = d->part;
+      const long keys = ring.window == INT_MAX ? (long)ring.cap : std::min<long>(ring.window, ring.cap);
+      at.maxblk = (int)(keys / MEGA_AK + 2);
+      out.push_back(at);
+      GemvIn in{};
+      in.mode = IN_NORM;
+      in.src = d->z;
+      in.ld = q_size;
+      gemv(L.wo, dm.hidden, q_size, 0, in, d->out, EpiArgs{EPI_STORE, nullptr, nullptr, 0}, nullptr);
+    } else {
+      gemv(L.wgu, dm.ffn, dm.hidden, dm.ffn, first_in(), d->mlp, EpiArgs{EPI_SILU, L.msg, L.msu, (long)dm.ffn},
+           nullptr);
+      GemvIn in{};
+      in.mode = IN_NORM;
+      in.src = d->mlp;
+      in.ld = dm.ffn;
+      gemv(L.wdown, dm.hidden, dm.ffn, 0, in, d->out, EpiArgs{EPI_STORE, nullptr, nullptr, 0}, nullptr);
+    }
+    pend.on = true;
+    pend.alpha = L.alpha;
+    pend.mix = mix;
+  };
+  const int n_in = c.n_in, n_rec = c.n_rec, n_all = (int)d->layers.size();
+  for (int li = 0; li < n_in; li++) layer(li, 0, li == n_in - 1 ? MIX_BEGIN : MIX_NONE);
+  for (int i = 0; i < a.loops; i++) {
+    const int m = i == a.loops - 1 ? MIX_END : MIX_LOOP;
+    for (int li = n_in; li < n_in + n_rec; li++) layer(li, i, li == n_in + n_rec - 1 ? m : MIX_NONE);
+  }
+  for (int li = n_in + n_rec; li < n_all; li++) layer(li, 0, MIX_NONE);
+  gemv(d->head, dm.vocab, dm.hidden, 0, first_in(), d->logits, EpiArgs{EPI_SCALE, d->logit_scale, nullptr, 0},
+       nullptr);
+  *h_last = cur;
+  return DORY_OK;
+}
+
+// Zero the kernel's counters and launch it over the uploaded stage list.
+int issue_mega(dory_t *d, const StepArgs &a, int32_t *rt, const MegaStage *stages, int nstages, cudaStream_t s) {
+  const dory_config &c = d->cfg;
+  CK(cudaMemsetAsync(d->mega_sync, 0, d->mega_sync_bytes, s));
+  MegaArgs m{};
+  m.stages = stages;
+  m.nstages = nstages;
+  m.d = d->dims;
+  m.rows.seq = rt;
+  m.rows.off = rt + d->Tmax;
+  m.rows.seq_pos = d->d_seq_pos;
+  m.rows.n = 1;
+  m.theta_s = c.rope_theta_sliding;
+  m.theta_f = c.rope_theta_full;
+  m.rope = d->rope;
+  m.sync = d->mega_sync;
+  m.actr = d->mega_sync + 64 + 2 * d->dims.nh + 2 * d->dims.nk;
+  m.err = d->dev_err;
+  m.seq_pos = d->d_seq_pos;
+  m.adv_seq = a.aseq[0];
+  m.adv_cnt = a.acnt[0];
+  CK(launch_mega_decode(m, d->sms, s));
+  return DORY_OK;
+}
+
+int count_gemv(const std::vector<MegaStage> &st) {
+  int n = 0;
+  for (const MegaStage &x : st) n += x.kind == MK_GEMV;
+  return n;
+}
+
 int upload_table(dory_t *d, const StepArgs &a, int32_t *rt, cudaStream_t s) {
   std::vector<int32_t> t((size_t)4 * d->Tmax, 0);
   for (int i = 0; i < a.T; i++) {
@@ -610,10 +780,32 @@ int upload_table(dory_t *d, const StepArgs &a, int32_t *rt, cudaStream_t s) {
 int do_step(dory_t *d, const StepArgs &a, const int32_t *ids) {
   int rc;
   CK(cudaMemcpyAsync(d->d_ids, ids, (size_t)a.T * 4, cudaMemcpyDefault, d->stream));
+  const bool mega = use_mega(d, a);
   if (!d->use_graphs) {
     if ((rc = upload_table(d, a, d->d_rows, d->stream))) return rc;
     int nl = 0, ng = 0;
-    if ((rc = issue_any(d, a, d->d_rows, false, d->stream, &nl, &ng))) return rc;
+    if (mega) {
+      std::vector<MegaStage> st;
+      if ((rc = mega_build(d, a, d->d_rows, st, &d->h_last))) return rc;
+      if (st.size() > d->mega_cap) {
+        if (d->mega_stages) cudaFree(d->mega_stages);
+        d->mega_stages = nullptr;
+        d->mega_cap = 0;
+        if (cudaMalloc(&d->mega_stages, st.size() * sizeof(MegaStage)) != cudaSuccess) {
+          cudaGetLastError();
+          return fail(DORY_ENOMEM, "cudaMalloc of a stage list");
+        }
+        d->mega_cap = st.size();
+      }
+      CK(cudaMemcpyAsync(d->mega_stages, st.data(), st.size() * sizeof(MegaStage), cudaMemcpyHostToDevice,
+                         d->stream));
+      if ((rc = issue_mega(d, a, d->d_rows, d->mega_stages, (int)st.size(), d->stream))) return rc;
+      CK(cudaStreamSynchronize(d->stream));  // the host stage list is freed on return
+      nl = 1;
+      ng = count_gemv(st);
+    } else if ((rc = issue_any(d, a, d->d_rows, false, d->stream, &nl, &ng))) {
+      return rc;
+    }
     d->st.launches = nl;
     d->st.gemm_launches = ng;
   } else {
@@ -629,14 +821,34 @@ int do_step(dory_t *d, const StepArgs &a, const int32_t *ids) {
         cudaFree(p.rt);
         return rc;
       }
+      std::vector<MegaStage> st;
+      if (mega) {
+        if ((rc = mega_build(d, a, p.rt, st, &p.h_last))) {
+          cudaFree(p.rt);
+          return rc;
+        }
+        if (cudaMalloc(&p.stages, st.size() * sizeof(MegaStage)) != cudaSuccess) {
+          cudaGetLastError();
+          cudaFree(p.rt);
+          return fail(DORY_ENOMEM, "cudaMalloc of a stage list");
+        }
+        CK(cudaMemcpy(p.stages, st.data(), st.size() * sizeof(MegaStage), cudaMemcpyHostToDevice));
+      }
       cudaGraph_t g = nullptr;
       CK(cudaStreamBeginCapture(d->cap_stream, cudaStreamCaptureModeThreadLocal));
-      rc = issue_any(d, a, p.rt, true, d->cap_stream, &p.launches, &p.gemm_launches);
-      p.h_last = d->h_last;
+      if (mega) {
+        rc = issue_mega(d, a, p.rt, p.stages, (int)st.size(), d->cap_stream);
+        p.launches = 1;
+        p.gemm_launches = count_gemv(st);
+      } else {
+        rc = issue_any(d, a, p.rt, true, d->cap_stream, &p.launches, &p.gemm_launches);
+        p.h_last = d->h_last;
+      }
       cudaError_t ec = cudaStreamEndCapture(d->cap_stream, &g);
       if (rc || ec != cudaSuccess) {
         if (g) cudaGraphDestroy(g);
         cudaFree(p.rt);
+        if (p.stages) cudaFree(p.stages);
         cudaGetLastError();
         return rc ? rc : fail(DORY_ECUDA, "graph capture: %s", cudaGetErrorString(ec));
       }
@@ -644,6 +856,7 @@ int do_step(dory_t *d, const StepArgs &a, const int32_t *ids) {
       cudaGraphDestroy(g);
       if (ec != cudaSuccess) {
         cudaFree(p.rt);
+        if (p.stages) cudaFree(p.stages);
         return fail(DORY_ECUDA, "graph instantiate: %s", cudaGetErrorString(ec));
       }
       it = d->plans.emplace(key, p).first;
@@ -945,6 +1158,7 @@ int dory_create(const dory_config *cfg, const dory_weights *w, void *stream, dor
                a_ids = areserve((size_t)T * 4),
                a_sp = areserve((size_t)cfg->max_seqs * 4), a_rows = areserve((size_t)4 * T * 4),
                a_zero = areserve((size_t)cfg->max_seqs * 4), a_err = areserve(256);
+  const size_t ms_bytes = (size_t)(64 + 2 * dm.nh + 2 * dm.nk + dm.nk) * 4, a_ms = areserve(ms_bytes);
   if (cudaMalloc(&d->act, ab) != cudaSuccess) {
     cudaGetLastError();
     fail(DORY_ENOMEM, "cudaMalloc of %zu activation bytes", ab);
@@ -963,6 +1177,32 @@ int dory_create(const dory_config *cfg, const dory_weights *w, void *stream, dor
                   kmax % 8 == 0 && 4 * kmax * 4 <= 96 * 1024;
     const char *e = getenv("DORY_FUSED");
     if (e && e[0] == '0') d->fused_ok = false;
+  }
+  d->mega_sync = reinterpret_cast<int32_t *>(A + a_ms);
+  d->mega_sync_bytes = ms_bytes;
+  {
+    // the persistent decode kernel: bf16 weights, f32 rings, rows that stream as whole
+    // 16-byte runs and fit a ring slot, a block's input row and attention scratch within
+    // its work area
+    int dev = 0;
+    CK(cudaGetDevice(&dev));
+    CK(cudaDeviceGetAttribute(&d->sms, cudaDevAttrMultiProcessorCount, dev));
+    const size_t kmax = std::max(std::max(dm.hidden, dm.ffn), q_size);
+    bool ok = d->wdtype == W_BF16 && !q8 && (dm.hd == 64 || dm.hd == 128) && dm.hidden % 8 == 0 &&
+              dm.ffn % 8 == 0 && q_size % 8 == 0 && kmax <= mega_work_floats() &&
+              (size_t)2 * MEGA_AK * dm.hd <= mega_work_floats() && mega_chunk_rows(dm.hidden, true) >= 1 &&
+              mega_chunk_rows((int)kmax, false) >= 1;
+    const int ldq = 2 * q_size + 2 * kv_size;
+    if (d->sms > 0 && ((ldq + d->sms - 1) / d->sms) / dm.hd + 2 > mega_max_heads_per_block()) ok = false;
+    for (const OrdInfo &o : d->ords) {
+      const long keys = o.window == INT_MAX ? (long)o.cap : std::min<long>(o.window, o.cap);
+      const long maxblk = keys / MEGA_AK + 2;
+      if ((size_t)2 * rep * maxblk > mega_work_floats()) ok = false;  // merge scratch
+      if (maxblk > (long)T * d->max_splits) ok = false;               // partials buffer
+    }
+    const char *e = getenv("DORY_MEGA");
+    if (e && e[0] == '0') ok = false;
+    d->mega_ok = ok && mega_supported(dm.hd, d->sms);
   }
   d->input = reinterpret_cast<float *>(A + a_in);
   d->state = reinterpret_cast<float *>(A + a_st);

@@ -20,6 +20,7 @@ __device__ void build_input(const Team &tm, const GemvIn &in, int T, int K, floa
   const int tid = tm.tid(), nt = tm.size();
   const int nch = K / 4;
   for (int t = 0; t < T; t++) {
+    // rows written earlier in the same launch (persistent kernel) are read from L2
     const float4 *src = reinterpret_cast<const float4 *>(in.src + (size_t)t * in.ld);
     float4 x[KC], o[KC], al[KC], inp[KC];
 #pragma unroll
@@ -27,12 +28,23 @@ __device__ void build_input(const Team &tm, const GemvIn &in, int T, int K, floa
       const int c = tid + j * nt;
       x[j] = o[j] = al[j] = inp[j] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (c < nch) {
-        x[j] = src[c];
-        if (in.mode == IN_RESID && in.alpha) {
-          o[j] = reinterpret_cast<const float4 *>(in.out + (size_t)t * K)[c];
-          al[j] = reinterpret_cast<const float4 *>(in.alpha)[c];
+        if (in.mode == IN_EMBED) {
+          const int id = in.ids[t];
+          if (id >= 0 && id < in.vocab) {
+            const uint2 u = __ldg(reinterpret_cast<const uint2 *>(in.embed + (size_t)id * K) + c);
+            const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
+            const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
+            x[j] = make_float4(a.x, a.y, b.x, b.y);
+          }
+        } else {
+          x[j] = __ldcg(src + c);
         }
-        if (in.mode == IN_RESID && in.mix == MIX_LOOP) inp[j] = reinterpret_cast<const float4 *>(in.input + (size_t)t * K)[c];
+        if (in.mode == IN_RESID && in.alpha) {
+          o[j] = __ldcg(reinterpret_cast<const float4 *>(in.out + (size_t)t * K) + c);
+          al[j] = __ldg(reinterpret_cast<const float4 *>(in.alpha) + c);
+        }
+        if (in.mode == IN_RESID && in.mix == MIX_LOOP)
+          inp[j] = __ldcg(reinterpret_cast<const float4 *>(in.input + (size_t)t * K) + c);
       }
     }
     auto sq4 = [](const float4 &v) { return v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w; };
@@ -114,7 +126,8 @@ __device__ void build_input(const Team &tm, const GemvIn &in, int T, int K, floa
       const int c = tid + j * nt;
       if (c < nch) {
         reinterpret_cast<float4 *>(xs + (size_t)t * K)[c] = x[j];
-        if (in.mode == IN_RESID && lead && in.h_dst) reinterpret_cast<float4 *>(in.h_dst + (size_t)t * K)[c] = x[j];
+        if ((in.mode == IN_RESID || in.mode == IN_EMBED) && lead && in.h_dst)
+          reinterpret_cast<float4 *>(in.h_dst + (size_t)t * K)[c] = x[j];
       }
     }
   }
@@ -143,10 +156,10 @@ __device__ void head_epilogue(const Team &tm, const HeadEpi &he, int head, int T
   if (is_q || is_k) {
     if (act) {
       const float *cs = he.rope + ((size_t)t * 2 + he.kind) * hd;
-      const float *sn = cs + half;
+      const float c = __ldcg(cs + j), sn = __ldcg(cs + half + j);
       const float x = a, y = b;
-      a = x * cs[j] - y * sn[j];
-      b = y * cs[j] + x * sn[j];
+      a = x * c - y * sn;
+      b = y * c + x * sn;
     }
     // per-row sums over the row's half threads (two warps when hd = 128)
     float v = act ? a * a + b * b : 0.f;
@@ -240,7 +253,7 @@ __device__ void merge_splits(const Team &tm, const float *pr, int splits, float 
     }
     for (; sp < splits; sp++) o = fmaf(__ldcg(base + (size_t)sp * REP * (HD + 2)), fm[sp * REP + h], o);
     const float y = o * (vcol ? vcol[c] : 1.f);
-    zrow[i] = y * sigmoidf_(g[i] * sg[i]);
+    zrow[i] = y * sigmoidf_(__ldcg(g + i) * sg[i]);
   }
 }
 

@@ -102,12 +102,13 @@ cudaError_t launch_residual(float *h, const float *out, const float *alpha, int 
 
 // ---- fused decode path (up to 4 rows) -------------------------------------------------
 
-enum InMode { IN_PLAIN = 0, IN_NORM = 1, IN_RESID = 2 };
+enum InMode { IN_PLAIN = 0, IN_NORM = 1, IN_RESID = 2, IN_EMBED = 3 };
 
 // How a fused GEMV builds its input rows: the source rows as they are, their row norm,
-// or the nGPT residual of the previous sub-layer (src = its input h, out = its output)
-// followed by the loop mix. With IN_RESID block 0 stores the result to h_dst (and the
-// mix's input/state rows).
+// the nGPT residual of the previous sub-layer (src = its input h, out = its output)
+// followed by the loop mix, or the embedding rows of the step's token ids (bf16 table).
+// With IN_RESID and IN_EMBED the leading block stores the result to h_dst (and the mix's
+// input/state rows).
 struct GemvIn {
   int mode;
   const float *src;
@@ -118,6 +119,9 @@ struct GemvIn {
   float *h_dst;
   float *input;
   float *state;
+  const int32_t *ids;            // IN_EMBED: token ids [T]; an id outside [0, vocab) gives a zero row
+  const __nv_bfloat16 *embed;    // IN_EMBED: table [vocab][K]
+  int vocab;
 };
 
 // Per-head epilogue of the q/k/v/g projection (RoPE, justnorm, s_q^2, ring write).
@@ -172,6 +176,56 @@ int make_tmap_kv_q8(KvMaps *m, const void *base, size_t bytes);
 cudaError_t launch_attention_tma_q8(const KvMaps &m, const float *qkvg, int ldq, Dims d, Rows rows, Ring ring,
                                     int splits, float *part, const float *sg, float *z, int *counters, int *err,
                                     bool pdl, cudaStream_t s);
+
+// ---- persistent batch-1 decode ---------------------------------------------------------
+
+enum MegaKind { MK_GEMV = 0, MK_ATTN = 1 };
+
+// One stage of the persistent decode kernel. Stages run in order; every block finishes a
+// stage before any block starts the next.
+struct MegaStage {
+  int kind;
+  // MK_GEMV: Y[n] = epilogue(W[n] . x) for n < N, x built from `in`; bf16 W [N(+pair)][K]
+  const __nv_bfloat16 *W;
+  int N, K;
+  int R;          // rows per streamed chunk
+  long pair;      // > 0: SwiGLU, up rows at n + pair
+  GemvIn in;
+  float *Y;
+  EpiArgs ep;
+  HeadEpi he;     // q/k/v/g projection: per-head RoPE, norm, ring write
+  // MK_ATTN: windowed attention of the one row over `ring`, gate, into z
+  Ring ring;
+  const float *qkvg;
+  const float *sg;
+  float *z;
+  float *part;    // [nk][maxblk][REP][hd + 2] item partials
+  int maxblk;     // items per kv head at most
+};
+
+struct MegaArgs {
+  const MegaStage *stages;
+  int nstages;
+  Dims d;
+  Rows rows;                // one row
+  double theta_s, theta_f;  // RoPE bases of sliding and full layers
+  float *rope;              // [2][hd] cos | sin of the row's position
+  int *sync;                // [0] blocks past each stage, [1] RoPE entries ready; zero at launch
+  int *actr;                // [nk] attention item arrivals; zero at launch
+  int *err;
+  int32_t *seq_pos;         // advanced by `adv` at the last stage
+  int adv_seq, adv_cnt;
+};
+
+// Bytes of dynamic shared memory and whether the device runs the kernel (one block per SM,
+// cooperative launch).
+size_t mega_smem_bytes(int hd);
+bool mega_supported(int hd, int sms);
+int mega_chunk_rows(int K, bool dual);  // rows (or gate/up row pairs) per streamed chunk; 0: too long
+int mega_max_heads_per_block();
+size_t mega_work_floats();              // shared scratch of a block: input row, tiles, merge
+constexpr int MEGA_AK = 32;             // positions per attention item
+cudaError_t launch_mega_decode(const MegaArgs &a, int grid, cudaStream_t s);
 
 cudaError_t launch_advance(int32_t *seq_pos, const int32_t *seq, const int32_t *count, int n, cudaStream_t s);
 

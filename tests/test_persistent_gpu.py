@@ -1,0 +1,89 @@
+"""The persistent batch-1 decode kernel (one launch per token) against the oracle and
+against the multi-kernel decode path, on the same seeded inputs."""
+import numpy as np
+import pytest
+
+import synth
+from parity import Pair
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(P, cfg, seed, steps):
+    """Context in every slot, a prompt chunk, then `steps` batch-1 decode tokens."""
+    P.write_context(0, 150, seed)
+    ids = synth.token_ids(seed, 1, 40 + steps, cfg.vocab)
+    P.prefill(0, ids[:40], cfg.loops, "last")
+    launches = []
+    for i in ids[40:]:
+        P.decode([0], [int(i)], cfg.loops)
+        launches.append(P.gpu.stats()["launches"])
+    return launches
+
+
+@pytest.mark.parametrize("kv_mode,hd,rec_kinds", [
+    ("last_loop", 64, "S*"),
+    ("per_loop", 64, "*S"),
+    ("last_loop", 128, "SS"),
+    ("per_loop", 128, "S*"),
+])
+def test_one_launch_per_token_matches_the_oracle(kv_mode, hd, rec_kinds):
+    nh, nk = (8, 2) if hd == 64 else (4, 1)
+    cfg = synth.small(kv_mode=kv_mode, hd=hd, nh=nh, nk=nk, rec_kinds=rec_kinds, full_window=0, loops=3,
+                      max_loops=3, max_context=1024)
+    P = Pair(cfg, 3001)
+    try:
+        launches = _run(P, cfg, 3001, 6)
+        assert launches == [1] * 6, launches  # the whole token in one kernel
+        assert P.max_hidden_err <= 1e-4, P.max_hidden_err
+        assert all(P.top1)
+        P.check_rings(0, 1e-5)
+    finally:
+        P.close()
+
+
+def test_same_logits_as_the_multi_kernel_path(monkeypatch):
+    cfg = synth.small(kv_mode="last_loop", rec_kinds="S*", full_window=0, loops=3, max_context=1024)
+    w = synth.weights(cfg, 3002)
+    out = {}
+    for mega in ("1", "0"):
+        monkeypatch.setenv("DORY_MEGA", mega)
+        P = Pair(cfg, 3002, weights=w)
+        try:
+            launches = _run(P, cfg, 3002, 4)
+            assert (launches[-1] == 1) == (mega == "1"), launches
+            out[mega] = (P.gpu.read_hidden(1).copy(), P.gpu.logits(0).copy())
+        finally:
+            P.close()
+    assert np.max(np.abs(out["1"][0] - out["0"][0])) <= 2e-5
+    assert np.max(np.abs(out["1"][1] - out["0"][1])) <= 2e-4
+
+
+def test_without_graphs_the_stage_list_is_uploaded_per_step(monkeypatch):
+    monkeypatch.setenv("DORY_GRAPHS", "0")
+    cfg = synth.small(kv_mode="per_loop", rec_kinds="S*", full_window=0, loops=2, max_loops=2, max_context=1024)
+    P = Pair(cfg, 3003)
+    try:
+        launches = _run(P, cfg, 3003, 3)
+        assert launches == [1] * 3, launches
+        assert P.max_hidden_err <= 1e-4, P.max_hidden_err
+        P.check_rings(0, 1e-5)
+    finally:
+        P.close()
+
+
+def test_loop_count_changes_between_tokens():
+    """Each loop count is its own stage list (and graph); per_loop holes are skipped."""
+    cfg = synth.small(kv_mode="per_loop", rec_kinds="SS", loops=3, max_loops=4, max_context=1024)
+    P = Pair(cfg, 3004)
+    try:
+        P.write_context(0, 90, 3004)
+        for step, loops in enumerate([1, 4, 2, 4, 3]):
+            i = synth.token_ids(3004, 10 + step, 1, cfg.vocab)
+            P.decode([0], [int(i[0])], loops)
+            assert P.gpu.stats()["launches"] == 1
+        assert P.max_hidden_err <= 1e-4, P.max_hidden_err
+        assert all(P.top1)
+        P.check_rings(0, 1e-5)
+    finally:
+        P.close()
