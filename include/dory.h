@@ -72,7 +72,7 @@ extern "C" {
 
 typedef struct dory_config {
   int32_t hidden, ffn, vocab; /* model width, MLP width, vocabulary rows */
-  int32_t nh, nk, hd;         /* query heads, KV heads (nh % nk == 0), head width (% 32 == 0, <= 256) */
+  int32_t nh, nk, hd;         /* query heads, KV heads (nh % nk == 0), head width: 32, 64 or 128; nh / nk in {1, 2, 4, 8} */
   int32_t window;             /* sliding attention window W: keys [p-W+1, p] */
   int32_t full_window;        /* full layers' window; 0: every earlier row up to max_context */
   int32_t max_context;        /* positions a full layer without full_window can hold */
@@ -113,7 +113,7 @@ typedef struct dory_weights {
 typedef struct dory_handle dory_t;
 
 /* Build a handle: checks the config (nh % nk == 0, 1 <= max_loops <= 16, the pattern's
- * length and chars, hd % 32 == 0 and hd <= 256, ...), copies every weight into device
+ * length and chars, hd in {32, 64, 128}, nh / nk in {1, 2, 4, 8}, ...), copies every weight into device
  * memory the handle owns (the caller may free its buffers on return), allocates the KV
  * rings of max_seqs sequences and resets them. `stream` is a cudaStream_t (NULL: the
  * legacy default stream) that orders all of the handle's work.

@@ -7,7 +7,9 @@
 // matrix (a contiguous range of rows) into a ring of shared-memory slots with cp.async.bulk,
 // completion on one mbarrier per slot. It never waits for activations, so the weights of
 // the next stages are already in flight while the consumers wait at a grid barrier or run
-// attention. Warps 1..8 are the consumers. Per stage they
+// attention. Warps 1..7 are the consumers, and consumer warp w owns slot w: it takes the
+// step's chunks w, w + 7, w + 14, ... (each wait on a slot's barrier is then for the phase
+// right after the one that warp saw last, never two ahead). Per stage they
 //   * wait until every block has finished the stage before (a counter in global memory);
 //   * GEMV: build the input row in shared memory (the embedding, a row norm, or the nGPT
 //     residual with the loop mix), then each warp takes whole chunks of rows from the ring,
@@ -35,10 +37,11 @@ namespace dory {
 
 namespace {
 
-constexpr int MW = 8;                       // consumer warps
+constexpr int MW = 7;                       // consumer warps
 constexpr int MTHREADS = 32 * (MW + 1);     // and the producer warp
-constexpr int NS = 7;                       // weight slots
-constexpr uint32_t SLOT = 24 * 1024;        // bytes per slot
+constexpr int NS = MW;                      // weight slots, one per consumer warp
+constexpr uint32_t SLOT = 26 * 1024;        // bytes per slot
+static_assert(NS == MW, "a slot's barrier phases are followed by one warp");
 constexpr uint32_t WORK = 32 * 1024;        // input row, or attention tiles and merge scratch
 constexpr int AK = MEGA_AK;                 // positions per attention item
 constexpr uint32_t SPIN_LIMIT = 1u << 22;   // polls of a global counter
@@ -127,7 +130,8 @@ __device__ void produce(const MegaArgs &a, uint8_t *ring, uint64_t *full, uint64
 
 // ---- GEMV stage ---------------------------------------------------------------------------
 
-// The consumer warps' share of a stage's chunks (chunk c goes to warp c mod MW). KI > 0:
+// The consumer warps' share of a stage's chunks (chunk c goes to warp c mod MW, in slot
+// c mod NS = the same warp's slot). KI > 0:
 // K = 256 KI and every lane keeps its 8 KI input values in registers; KI = 0: any K with
 // K % 8 == 0, the input read from shared memory.
 template <int KI>
@@ -237,7 +241,7 @@ __device__ bool gemv_stage(const WarpTeam &tm, const MegaArgs &a, const MegaStag
   const int G = gridDim.x, b = blockIdx.x;
   const int N = st.N, K = st.K;
   const int rb = (int)((long)N * b / G), re = (int)((long)N * (b + 1) / G);
-  const int kc = (K / 4 + 255) / 256;
+  const int kc = (K / 4 + tm.size() - 1) / tm.size();  // float4 chunks per thread
   if (kc <= 2) input_row<2>(tm, st.in, K, xs);
   else if (kc <= 4) input_row<4>(tm, st.in, K, xs);
   else if (kc <= 6) input_row<6>(tm, st.in, K, xs);
@@ -327,15 +331,15 @@ __device__ bool attn_stage(const WarpTeam &tm, const MegaArgs &a, const MegaStag
     const bool landed = mbar_wait(smem_addr(abar), (aph - 1) & 1, &ctl.abort);
     if (!landed && lane == 0) flag_error(ctl, a.err);
     if (!team_ok(tm, ctl)) return false;
-    if (cw < rep) {
-      // warp cw: query head kh * rep + cw; lane j: key P0 + j
+    for (int h = cw; h < rep; h += MW) {
+      // warp cw: query heads kh * rep + h; lane j: key P0 + j
       const int j = lane;
       const long pe = P0 + j;
       const bool valid = pe >= lo && pe <= p && __ldcg(tags + rr0 + j) == (int32_t)pe;
       float s0 = 0.f, s1 = 0.f;
       if (valid) {
         const float4 *kr = reinterpret_cast<const float4 *>(Ks + j * HD);
-        const float4 *q4 = reinterpret_cast<const float4 *>(qs[cw]);
+        const float4 *q4 = reinterpret_cast<const float4 *>(qs[h]);
 #pragma unroll 8
         for (int c = 0; c < NC; c++) {
           const int cc = (c + j) & (NC - 1);  // rotated: the 32 lanes spread over all banks
@@ -358,7 +362,7 @@ __device__ bool attn_stage(const WarpTeam &tm, const MegaArgs &a, const MegaStag
 #pragma unroll
         for (int i = 0; i < NV; i++) acc[i] = fmaf(wj, v[i], acc[i]);
       }
-      float *out = st.part + (((size_t)kh * st.maxblk + blk) * rep + cw) * (HD + 2);
+      float *out = st.part + (((size_t)kh * st.maxblk + blk) * rep + h) * (HD + 2);
 #pragma unroll
       for (int i = 0; i < NV; i++) out[lane * NV + i] = acc[i];
       if (lane == 0) {
