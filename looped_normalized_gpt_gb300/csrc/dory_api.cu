@@ -104,6 +104,11 @@ struct dory_handle {
   size_t mega_sync_bytes = 0;
   MegaStage *mega_stages = nullptr;  // stage list of the launches issued without graphs
   size_t mega_cap = 0;
+  // optional trace of the persistent kernel (DORY_MEGA_TRACE=<file>, written at destroy)
+  unsigned long long *mega_trace = nullptr;
+  size_t mega_trace_stages = 0;
+  std::string mega_trace_path;
+  std::vector<int32_t> mega_trace_desc;  // kind, N, K per stage of the last traced step
   // tensor-core projections: weight maps per layer ([0] q/k/v/g or gate/up, [1] o or down)
   bool tc_ok = false;
   std::vector<std::array<TcW, 2>> tcw;
@@ -201,6 +206,8 @@ void free_all(dory_t *d) {
   }
   if (d->mega_stages) cudaFree(d->mega_stages);
   d->mega_stages = nullptr;
+  if (d->mega_trace) cudaFree(d->mega_trace);
+  d->mega_trace = nullptr;
   d->mega_cap = 0;
   d->plans.clear();
   if (d->cap_stream) cudaStreamDestroy(d->cap_stream);
@@ -727,6 +734,14 @@ int mega_build(dory_t *d, const StepArgs &a, int32_t *rt, std::vector<MegaStage>
   gemv(d->head, dm.vocab, dm.hidden, 0, first_in(), d->logits, EpiArgs{EPI_SCALE, d->logit_scale, nullptr, 0},
        nullptr);
   *h_last = cur;
+  if (d->mega_trace) {
+    d->mega_trace_desc.clear();
+    for (const MegaStage &x : out) {
+      d->mega_trace_desc.push_back(x.kind);
+      d->mega_trace_desc.push_back(x.kind == MK_GEMV ? x.N : 0);
+      d->mega_trace_desc.push_back(x.kind == MK_GEMV ? x.K : 0);
+    }
+  }
   return DORY_OK;
 }
 
@@ -751,6 +766,7 @@ int issue_mega(dory_t *d, const StepArgs &a, int32_t *rt, const MegaStage *stage
   m.seq_pos = d->d_seq_pos;
   m.adv_seq = a.aseq[0];
   m.adv_cnt = a.acnt[0];
+  m.trace = (size_t)nstages <= d->mega_trace_stages ? d->mega_trace : nullptr;
   CK(launch_mega_decode(m, d->sms, s));
   return DORY_OK;
 }
@@ -1203,6 +1219,18 @@ int dory_create(const dory_config *cfg, const dory_weights *w, void *stream, dor
     const char *e = getenv("DORY_MEGA");
     if (e && e[0] == '0') ok = false;
     d->mega_ok = ok && mega_supported(dm.hd, d->sms);
+    const char *tp = getenv("DORY_MEGA_TRACE");
+    if (d->mega_ok && tp && tp[0]) {
+      const size_t stages = (size_t)3 * (cfg->n_in + cfg->max_loops * cfg->n_rec + cfg->n_out) + 2;
+      const size_t bytes = stages * d->sms * MEGA_TRACE_EVENTS * 8;
+      if (cudaMalloc(&d->mega_trace, bytes) == cudaSuccess && cudaMemset(d->mega_trace, 0, bytes) == cudaSuccess) {
+        d->mega_trace_stages = stages;
+        d->mega_trace_path = tp;
+      } else {
+        cudaGetLastError();
+        d->mega_trace = nullptr;
+      }
+    }
   }
   d->input = reinterpret_cast<float *>(A + a_in);
   d->state = reinterpret_cast<float *>(A + a_st);
@@ -1244,6 +1272,19 @@ int dory_create(const dory_config *cfg, const dory_weights *w, void *stream, dor
 int dory_destroy(dory_t *d) {
   if (!d) return DORY_OK;
   cudaStreamSynchronize(d->stream);
+  if (d->mega_trace && !d->mega_trace_desc.empty()) {
+    // file: int32 nstages, grid, events; int32 [nstages][3] (kind, N, K); u64 stamps
+    const int32_t hdr[3] = {(int32_t)(d->mega_trace_desc.size() / 3), d->sms, MEGA_TRACE_EVENTS};
+    std::vector<unsigned long long> t((size_t)hdr[0] * d->sms * MEGA_TRACE_EVENTS);
+    if (cudaMemcpy(t.data(), d->mega_trace, t.size() * 8, cudaMemcpyDeviceToHost) == cudaSuccess) {
+      if (FILE *f = fopen(d->mega_trace_path.c_str(), "wb")) {
+        fwrite(hdr, 4, 3, f);
+        fwrite(d->mega_trace_desc.data(), 4, d->mega_trace_desc.size(), f);
+        fwrite(t.data(), 8, t.size(), f);
+        fclose(f);
+      }
+    }
+  }
   free_all(d);
   delete d;
   return DORY_OK;

@@ -56,6 +56,17 @@ struct Ctl {
   int last;
 };
 
+// Optional per-stage timestamps (off when the trace pointer is null).
+struct Tracer {
+  unsigned long long *p;
+  __device__ __forceinline__ void mark(int stage, int event) const {
+    if (!p) return;
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    p[((size_t)stage * gridDim.x + blockIdx.x) * MEGA_TRACE_EVENTS + event] = t;
+  }
+};
+
 __device__ __forceinline__ void flag_error(Ctl &ctl, int *err) {
   if (!ctl.abort) {
     ctl.abort = 1;
@@ -100,11 +111,13 @@ __device__ __forceinline__ void grid_arrive(const WarpTeam &tm, int *ctr) {
 
 __device__ void produce(const MegaArgs &a, uint8_t *ring, uint64_t *full, uint64_t *empty, Ctl &ctl) {
   const int G = gridDim.x, b = blockIdx.x;
+  const Tracer tr{a.trace};
   int c = 0;  // chunks issued
   bool ok = true;
   for (int s = 0; s < a.nstages && ok; s++) {
     const MegaStage &st = a.stages[s];
     if (st.kind != MK_GEMV) continue;
+    const int c_first = c;
     const int N = st.N, K = st.K, R = st.R;
     const long pair = st.pair;
     const int rb = (int)((long)N * b / G), re = (int)((long)N * (b + 1) / G);
@@ -120,8 +133,10 @@ __device__ void produce(const MegaArgs &a, uint8_t *ring, uint64_t *full, uint64
       mbar_expect_tx(bar, pair > 0 ? 2 * bytes : bytes);
       bulk_g2s(dst, st.W + (size_t)r0 * K, bytes, bar);
       if (pair > 0) bulk_g2s(dst + bytes, st.W + (size_t)(r0 + pair) * K, bytes, bar);
+      if (c == c_first) tr.mark(s, 5);
       c++;
     }
+    tr.mark(s, 6);
   }
   if (!ok) flag_error(ctl, a.err);
   // the block may not exit while a copy into its shared memory is in flight
@@ -236,8 +251,9 @@ __device__ __forceinline__ void input_row(const WarpTeam &tm, const GemvIn &in, 
 }
 
 // Returns false (team-uniformly) when the block has stopped.
-__device__ bool gemv_stage(const WarpTeam &tm, const MegaArgs &a, const MegaStage &st, int &c, const uint8_t *ring,
-                           uint64_t *full, uint64_t *empty, float *xs, Ctl &ctl) {
+__device__ bool gemv_stage(const WarpTeam &tm, const MegaArgs &a, const MegaStage &st, int s, int &c,
+                           const uint8_t *ring, uint64_t *full, uint64_t *empty, float *xs, Ctl &ctl) {
+  const Tracer tr{tm.tid() == 0 ? a.trace : nullptr};
   const int G = gridDim.x, b = blockIdx.x;
   const int N = st.N, K = st.K;
   const int rb = (int)((long)N * b / G), re = (int)((long)N * (b + 1) / G);
@@ -246,6 +262,7 @@ __device__ bool gemv_stage(const WarpTeam &tm, const MegaArgs &a, const MegaStag
   else if (kc <= 4) input_row<4>(tm, st.in, K, xs);
   else if (kc <= 6) input_row<6>(tm, st.in, K, xs);
   else input_row<8>(tm, st.in, K, xs);
+  tr.mark(s, 2);
   switch (K) {
     case 256: gemv_chunks<1>(st, rb, re, c, ring, full, empty, xs, ctl, a.err); break;
     case 512: gemv_chunks<2>(st, rb, re, c, ring, full, empty, xs, ctl, a.err); break;
@@ -255,6 +272,7 @@ __device__ bool gemv_stage(const WarpTeam &tm, const MegaArgs &a, const MegaStag
   }
   c += re > rb ? (re - rb + st.R - 1) / st.R : 0;
   if (!team_ok(tm, ctl)) return false;
+  tr.mark(s, 3);
   if (!st.he.enabled) return true;
   // heads this block finished rows of: the block that completes a head runs its epilogue
   const Dims &d = a.d;
@@ -443,16 +461,20 @@ __global__ void __launch_bounds__(MTHREADS, 1) mega_decode_kernel(const __grid_c
   }
   int c = 0, aph = 0;
   bool ok = true;
+  const Tracer tr{tm.tid() == 0 ? a.trace : nullptr};
   for (int s = 0; s < a.nstages && ok; s++) {
     const MegaStage &st = a.stages[s];
+    tr.mark(s, 0);
     if (s > 0 && !team_wait_counter(tm, a.sync, s * G, ctl, a.err)) {
       ok = false;
       break;
     }
+    tr.mark(s, 1);
     // every reader of the position has passed: the last stage advances it
     if (s == a.nstages - 1 && b == 0 && tm.tid() == 0) a.seq_pos[a.adv_seq] += a.adv_cnt;
-    if (st.kind == MK_GEMV) ok = gemv_stage(tm, a, st, c, ring, full, empty, work, ctl);
+    if (st.kind == MK_GEMV) ok = gemv_stage(tm, a, st, s, c, ring, full, empty, work, ctl);
     else ok = attn_stage<HD>(tm, a, st, work, &abar, aph, qs, ctl);
+    tr.mark(s, 4);
     if (ok && s + 1 < a.nstages) grid_arrive(tm, a.sync);
   }
   // an attention copy may still be in flight after a stop

@@ -215,7 +215,13 @@ struct MegaArgs {
   int *err;
   int32_t *seq_pos;         // advanced by `adv` at the last stage
   int adv_seq, adv_cnt;
+  unsigned long long *trace;  // null, or [nstages][grid][MEGA_TRACE_EVENTS] %globaltimer stamps
 };
+
+// Stamps per (stage, block) of the persistent kernel's optional trace: 0 stage entered,
+// 1 grid barrier passed, 2 input row built, 3 chunks or attention items done, 4 stage done;
+// from the producer warp: 5 first chunk of the stage issued, 6 last chunk issued.
+constexpr int MEGA_TRACE_EVENTS = 8;
 
 // Bytes of dynamic shared memory and whether the device runs the kernel (one block per SM,
 // cooperative launch).
