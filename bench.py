@@ -95,6 +95,38 @@ def workload_config():
     return synth.dory2b(max_batch=1, max_seqs=1, max_context=PROMPT + DECODE + 64)
 
 
+def profile_case(args):
+    """A reduced case for ncu captures of the decode kernel: the 2B shape with one input,
+    one recurrent and one output pair and loops 1 (427 MB of weights per token, still
+    larger than L2, about 1 GB on the device). Prints one JSON line; not a bench line."""
+    import torch
+
+    from looped_normalized_gpt_gb300 import Dory, build
+
+    build()
+    pat, a, b, c = synth.pattern_of("S", "S", "S")
+    cfg = synth.dory2b(pattern=pat, n_in=a, n_rec=b, n_out=c, loops=1, max_batch=1, max_seqs=1,
+                       max_context=args.prompt + DECODE + 64)
+    w = synth.weights(cfg, SEED)
+    g = Dory(cfg, w)
+    ids = synth.token_ids(SEED, 0, args.prompt + DECODE, cfg.vocab)
+    for a0 in range(0, args.prompt, 64):
+        g.prefill_chunk(0, ids[a0:a0 + 64], a0, cfg.loops, "none")
+    dec = ids[args.prompt:]
+    for i in range(args.warmup):
+        g.decode_step([int(dec[i])], [0], cfg.loops)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(args.warmup, args.warmup + args.steps):
+        g.decode_step([int(dec[i])], [0], cfg.loops)
+    torch.cuda.synchronize()
+    ms = (time.perf_counter() - t0) * 1e3 / max(args.steps, 1)
+    st = g.stats()
+    g.close()
+    return {"case": "decode-2b-3pass", "ms_per_step_host": round(ms, 4), "launches_per_step": st["launches"],
+            "weight_bytes_per_step": st["weight_bytes"], "note": "profiling case, not a bench line"}
+
+
 def bench_ours(args, rank, world):
     global PROMPT
     PROMPT = args.prompt
@@ -323,7 +355,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the batch-64 decode and prefill lines")
     ap.add_argument("--prompt", type=int, default=PROMPT, help="prompt tokens before the decode steps")
+    ap.add_argument("--profile-case", action="store_true",
+                    help="run the reduced decode case used for ncu captures instead of the bench")
     args = ap.parse_args()
+    if args.profile_case:
+        print(json.dumps(profile_case(args)), flush=True)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
