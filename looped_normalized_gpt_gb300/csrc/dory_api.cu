@@ -97,7 +97,7 @@ struct dory_handle {
   int32_t *hctr = nullptr, *actr = nullptr;  // arrival counters of the fused kernels
   bool fused_ok = false;
   // persistent batch-1 decode: one block per SM; counters zeroed before each launch:
-  // [0] grid barrier, [1] RoPE entries, [64..) per-head arrivals, then per-kv-head items
+  // [0] grid barrier, [1] RoPE entries, [64..) per-kv-head attention item arrivals
   bool mega_ok = false;
   int sms = 0;
   int32_t *mega_sync = nullptr;
@@ -622,11 +622,7 @@ int mega_build(dory_t *d, const StepArgs &a, int32_t *rt, std::vector<MegaStage>
   const Dims dm = d->dims;
   const int q_size = dm.nh * dm.hd, kv_size = dm.nk * dm.hd;
   const int ldq = 2 * q_size + 2 * kv_size;
-  Rows rows;
-  rows.seq = rt;
-  rows.off = rt + d->Tmax;
-  rows.seq_pos = d->d_seq_pos;
-  rows.n = 1;
+  (void)rt;  // the row table reaches the kernel through its arguments
   out.clear();
   float *cur = d->h, *other = d->h2;
   bool first = true;
@@ -664,8 +660,7 @@ int mega_build(dory_t *d, const StepArgs &a, int32_t *rt, std::vector<MegaStage>
     pend.on = false;
     return g;
   };
-  auto gemv = [&](const void *W, int N, int K, long pair, const GemvIn &in, float *Y, EpiArgs ep,
-                  const HeadEpi *he) {
+  auto gemv = [&](const void *W, int N, int K, long pair, const GemvIn &in, float *Y, EpiArgs ep) {
     MegaStage st{};
     st.kind = MK_GEMV;
     st.W = static_cast<const __nv_bfloat16 *>(W);
@@ -676,30 +671,20 @@ int mega_build(dory_t *d, const StepArgs &a, int32_t *rt, std::vector<MegaStage>
     st.in = in;
     st.Y = Y;
     st.ep = ep;
-    if (he) st.he = *he;
-    else st.he.enabled = 0;
     out.push_back(st);
   };
-  int32_t *heads = d->mega_sync + 64;
   auto layer = [&](int li, int loop_i, int mix) {
     const LayerDev &L = d->layers[li];
     if (L.attn) {
       const int sl = (c.kv_mode == DORY_KV_PER_LOOP && L.rec) ? loop_i : 0;
       const Ring ring = d->ring(L.ordinal, sl);
-      HeadEpi he{};
-      he.enabled = 1;
-      he.counters = heads;
-      he.d = dm;
-      he.rows = rows;
-      he.rope = d->rope;
-      he.kind = L.sliding ? 0 : 1;
-      he.sq = L.sq;
-      he.ring = ring;
-      gemv(L.wqkvg, ldq, dm.hidden, 0, first_in(), d->qkvg, EpiArgs{EPI_STORE, nullptr, nullptr, 0}, &he);
+      gemv(L.wqkvg, ldq, dm.hidden, 0, first_in(), d->qkvg, EpiArgs{EPI_STORE, nullptr, nullptr, 0});
       MegaStage at{};
       at.kind = MK_ATTN;
       at.ring = ring;
       at.qkvg = d->qkvg;
+      at.sq = L.sq;
+      at.rope_kind = L.sliding ? 0 : 1;
       at.sg = L.sg;
       at.z = d->z;
       at.part = d->part;
@@ -710,15 +695,14 @@ int mega_build(dory_t *d, const StepArgs &a, int32_t *rt, std::vector<MegaStage>
       in.mode = IN_NORM;
       in.src = d->z;
       in.ld = q_size;
-      gemv(L.wo, dm.hidden, q_size, 0, in, d->out, EpiArgs{EPI_STORE, nullptr, nullptr, 0}, nullptr);
+      gemv(L.wo, dm.hidden, q_size, 0, in, d->out, EpiArgs{EPI_STORE, nullptr, nullptr, 0});
     } else {
-      gemv(L.wgu, dm.ffn, dm.hidden, dm.ffn, first_in(), d->mlp, EpiArgs{EPI_SILU, L.msg, L.msu, (long)dm.ffn},
-           nullptr);
+      gemv(L.wgu, dm.ffn, dm.hidden, dm.ffn, first_in(), d->mlp, EpiArgs{EPI_SILU, L.msg, L.msu, (long)dm.ffn});
       GemvIn in{};
       in.mode = IN_NORM;
       in.src = d->mlp;
       in.ld = dm.ffn;
-      gemv(L.wdown, dm.hidden, dm.ffn, 0, in, d->out, EpiArgs{EPI_STORE, nullptr, nullptr, 0}, nullptr);
+      gemv(L.wdown, dm.hidden, dm.ffn, 0, in, d->out, EpiArgs{EPI_STORE, nullptr, nullptr, 0});
     }
     pend.on = true;
     pend.alpha = L.alpha;
@@ -731,8 +715,7 @@ int mega_build(dory_t *d, const StepArgs &a, int32_t *rt, std::vector<MegaStage>
     for (int li = n_in; li < n_in + n_rec; li++) layer(li, i, li == n_in + n_rec - 1 ? m : MIX_NONE);
   }
   for (int li = n_in + n_rec; li < n_all; li++) layer(li, 0, MIX_NONE);
-  gemv(d->head, dm.vocab, dm.hidden, 0, first_in(), d->logits, EpiArgs{EPI_SCALE, d->logit_scale, nullptr, 0},
-       nullptr);
+  gemv(d->head, dm.vocab, dm.hidden, 0, first_in(), d->logits, EpiArgs{EPI_SCALE, d->logit_scale, nullptr, 0});
   *h_last = cur;
   if (d->mega_trace) {
     d->mega_trace_desc.clear();
@@ -761,7 +744,7 @@ int issue_mega(dory_t *d, const StepArgs &a, int32_t *rt, const MegaStage *stage
   m.theta_f = c.rope_theta_full;
   m.rope = d->rope;
   m.sync = d->mega_sync;
-  m.actr = d->mega_sync + 64 + 2 * d->dims.nh + 2 * d->dims.nk;
+  m.actr = d->mega_sync + 64;
   m.err = d->dev_err;
   m.seq_pos = d->d_seq_pos;
   m.adv_seq = a.aseq[0];
@@ -1174,7 +1157,7 @@ int dory_create(const dory_config *cfg, const dory_weights *w, void *stream, dor
                a_ids = areserve((size_t)T * 4),
                a_sp = areserve((size_t)cfg->max_seqs * 4), a_rows = areserve((size_t)4 * T * 4),
                a_zero = areserve((size_t)cfg->max_seqs * 4), a_err = areserve(256);
-  const size_t ms_bytes = (size_t)(64 + 2 * dm.nh + 2 * dm.nk + dm.nk) * 4, a_ms = areserve(ms_bytes);
+  const size_t ms_bytes = (size_t)(64 + dm.nk) * 4, a_ms = areserve(ms_bytes);
   if (cudaMalloc(&d->act, ab) != cudaSuccess) {
     cudaGetLastError();
     fail(DORY_ENOMEM, "cudaMalloc of %zu activation bytes", ab);
@@ -1208,13 +1191,10 @@ int dory_create(const dory_config *cfg, const dory_weights *w, void *stream, dor
               dm.ffn % 8 == 0 && q_size % 8 == 0 && kmax <= mega_work_floats() &&
               (size_t)2 * MEGA_AK * dm.hd <= mega_work_floats() && mega_chunk_rows(dm.hidden, true) >= 1 &&
               mega_chunk_rows((int)kmax, false) >= 1;
-    const int ldq = 2 * q_size + 2 * kv_size;
-    if (d->sms > 0 && ((ldq + d->sms - 1) / d->sms) / dm.hd + 2 > mega_max_heads_per_block()) ok = false;
     for (const OrdInfo &o : d->ords) {
       const long keys = o.window == INT_MAX ? (long)o.cap : std::min<long>(o.window, o.cap);
       const long maxblk = keys / MEGA_AK + 2;
-      if ((size_t)2 * rep * maxblk > mega_work_floats()) ok = false;  // merge scratch
-      if (maxblk > (long)T * d->max_splits) ok = false;               // partials buffer
+      if (maxblk > (long)T * d->max_splits) ok = false;  // partials buffer
     }
     const char *e = getenv("DORY_MEGA");
     if (e && e[0] == '0') ok = false;

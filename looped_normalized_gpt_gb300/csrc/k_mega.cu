@@ -3,24 +3,27 @@
 // block and the logits) as a list of stages.
 //
 // One block per SM, launched cooperatively so that every block is resident. Warp 0 is the
-// producer: it walks the stages in order and streams this block's share of every weight
-// matrix (a contiguous range of rows) into a ring of shared-memory slots with cp.async.bulk,
-// completion on one mbarrier per slot. It never waits for activations, so the weights of
-// the next stages are already in flight while the consumers wait at a grid barrier or run
-// attention. Warps 1..7 are the consumers, and consumer warp w owns slot w: it takes the
-// step's chunks w, w + 7, w + 14, ... (each wait on a slot's barrier is then for the phase
-// right after the one that warp saw last, never two ahead). Per stage they
-//   * wait until every block has finished the stage before (a counter in global memory);
+// producer: it walks this block's share of every weight matrix (a contiguous range of rows)
+// in stage order, asks L2 for the bytes about PREFETCH_AHEAD ahead (cp.async.bulk.prefetch),
+// and copies chunks into a ring of shared-memory slots with cp.async.bulk, completion on one
+// mbarrier per slot. It never waits for activations, so HBM keeps streaming the next stages'
+// weights while the consumers wait at a grid barrier or run attention. Warps 1..7 are the
+// consumers; consumer warp w owns slot w and takes the step's chunks w, w + 7, w + 14, ...
+// (so each wait on a slot's barrier is for the phase right after the one that warp saw
+// last). Per stage the consumers
+//   * copy the stage's descriptor into shared memory while their first thread waits until
+//     every block has finished the stage before (a counter in global memory);
 //   * GEMV: build the input row in shared memory (the embedding, a row norm, or the nGPT
-//     residual with the loop mix), then each warp takes whole chunks of rows from the ring,
-//     reduces them against the input (bf16 weights, f32 sums), applies the epilogue
-//     (SwiGLU, logit scale) and frees the slot; in the q/k/v/g projection the block that
-//     completes a head does its RoPE + justnorm (+ s_q^2) and the f32 ring write
-//     (dory.rs fn attn_layer);
-//   * attention: items of 32 positions of one kv head. The K and V rows of an item are
-//     contiguous in the ring and arrive with two bulk copies; warp h scores query head h
-//     (lane = key), takes the softmax of the item and its value sum; the last item of a kv
-//     head merges the items and applies the output gate (dory.rs fn attn_layer).
+//     residual with the loop mix), then each warp reduces its chunks against it (bf16
+//     weights, f32 sums), applies the epilogue (SwiGLU, logit scale) and frees the slot;
+//   * attention (dory.rs fn attn_layer), in items of 32 positions of one kv head: the K and
+//     V rows of an item are contiguous in the ring and arrive with two bulk copies; meanwhile
+//     warp h rotates and normalises query head h of the group from the raw projection row
+//     (q = s_q^2 q^), and in the item that holds the row's own position one warp rotates and
+//     normalises the new key, puts key and value into the tile and writes them (and the
+//     position tag) to the ring; warp h then scores (lane = key), takes the item's softmax and
+//     value sum; the last item of a kv head merges the items (all partials loaded at once)
+//     and applies the output gate.
 // Every wait is bounded. When one runs out the block records error 6, stops at the next
 // team-wide check, lets its copies in flight land and returns; the other blocks then stop
 // at their next grid barrier.
@@ -37,26 +40,27 @@ namespace dory {
 
 namespace {
 
-constexpr int MW = 7;                       // consumer warps
-constexpr int MTHREADS = 32 * (MW + 1);     // and the producer warp
-constexpr int NS = MW;                      // weight slots, one per consumer warp
-constexpr uint32_t SLOT = 26 * 1024;        // bytes per slot
+constexpr int MW = 7;                             // consumer warps
+constexpr int MTHREADS = 32 * (MW + 1);           // and the producer warp
+constexpr int NS = MW;                            // weight slots, one per consumer warp
+constexpr uint32_t SLOT = 26 * 1024;              // bytes per slot
+constexpr uint32_t WORK = 32 * 1024;              // input row, or attention tiles and merge scratch
+constexpr int AK = MEGA_AK;                       // positions per attention item
+constexpr uint32_t SPIN_LIMIT = 1u << 22;         // polls of a global counter
+constexpr int ERR_MEGA = 6;                       // dev_err: a wait of the persistent kernel ran out
+constexpr long PREFETCH_AHEAD = 448 * 1024;       // L2 lead of the producer, bytes per block
 static_assert(NS == MW, "a slot's barrier phases are followed by one warp");
-constexpr uint32_t WORK = 32 * 1024;        // input row, or attention tiles and merge scratch
-constexpr int AK = MEGA_AK;                 // positions per attention item
-constexpr uint32_t SPIN_LIMIT = 1u << 22;   // polls of a global counter
-constexpr int ERR_MEGA = 6;                 // dev_err: a wait of the persistent kernel ran out
-constexpr int MAX_HEADS_PER_BLOCK = 64;
+static_assert(sizeof(MegaStage) % 4 == 0 && sizeof(MegaStage) / 4 < 32 * MW, "stage copy by the team");
 
 struct Ctl {
   volatile int abort;  // a wait ran out somewhere in the block
   int decision;        // team-wide copy of `abort`, written by the team's first thread
-  int nheads;
-  int heads[MAX_HEADS_PER_BLOCK];
-  int last;
+  int last;            // this block merges the kv head's items
+  int seq;             // the row's sequence and position
+  long long p;
 };
 
-// Optional per-stage timestamps (off when the trace pointer is null).
+// Optional per-stage timestamps (off when the pointer is null).
 struct Tracer {
   unsigned long long *p;
   __device__ __forceinline__ void mark(int stage, int event) const {
@@ -99,44 +103,83 @@ __device__ bool team_wait_counter(const WarpTeam &tm, const int *ctr, int target
   return ctl.decision == 0;
 }
 
+// The block's writes of this stage, then one arrival (release orders them all: the
+// barrier before it makes every thread's writes precede the first thread's release).
 __device__ __forceinline__ void grid_arrive(const WarpTeam &tm, int *ctr) {
   tm.sync();
-  if (tm.tid() == 0) {
-    __threadfence();
-    red_release_gpu_add(ctr, 1);
-  }
+  if (tm.tid() == 0) red_release_gpu_add(ctr, 1);
 }
 
 // ---- producer -----------------------------------------------------------------------------
 
-__device__ void produce(const MegaArgs &a, uint8_t *ring, uint64_t *full, uint64_t *empty, Ctl &ctl) {
-  const int G = gridDim.x, b = blockIdx.x;
-  const Tracer tr{a.trace};
-  int c = 0;  // chunks issued
-  bool ok = true;
-  for (int s = 0; s < a.nstages && ok; s++) {
-    const MegaStage &st = a.stages[s];
-    if (st.kind != MK_GEMV) continue;
-    const int c_first = c;
-    const int N = st.N, K = st.K, R = st.R;
-    const long pair = st.pair;
-    const int rb = (int)((long)N * b / G), re = (int)((long)N * (b + 1) / G);
-    const uint32_t row_bytes = (uint32_t)K * 2;
-    for (int r0 = rb; r0 < re; r0 += R) {
-      const int nr = min(R, re - r0), sl = c % NS;
-      if (c >= NS && !mbar_wait(smem_addr(&empty[sl]), ((c / NS) - 1) & 1, &ctl.abort)) {
-        ok = false;
-        break;
+// A walk over this block's rows of the GEMV stages, chunk by chunk.
+struct ChunkWalk {
+  int s, r0, re, K, R;
+  long pair;
+  const __nv_bfloat16 *W;
+  bool ok;
+  __device__ void seek(const MegaArgs &a, int from) {
+    const int G = gridDim.x, b = blockIdx.x;
+    for (s = from; s < a.nstages; s++) {
+      const MegaStage &st = a.stages[s];
+      if (st.kind != MK_GEMV) continue;
+      const int rb = (int)((long)st.N * b / G);
+      re = (int)((long)st.N * (b + 1) / G);
+      if (rb < re) {
+        r0 = rb;
+        K = st.K;
+        R = st.R;
+        pair = st.pair;
+        W = st.W;
+        ok = true;
+        return;
       }
-      const uint32_t bytes = (uint32_t)nr * row_bytes, bar = smem_addr(&full[sl]);
-      const uint32_t dst = smem_addr(ring + (size_t)sl * SLOT);
-      mbar_expect_tx(bar, pair > 0 ? 2 * bytes : bytes);
-      bulk_g2s(dst, st.W + (size_t)r0 * K, bytes, bar);
-      if (pair > 0) bulk_g2s(dst + bytes, st.W + (size_t)(r0 + pair) * K, bytes, bar);
-      if (c == c_first) tr.mark(s, 5);
-      c++;
     }
-    tr.mark(s, 6);
+    ok = false;
+  }
+  __device__ int rows() const { return min(R, re - r0); }
+  __device__ void step(const MegaArgs &a) {
+    r0 += rows();
+    if (r0 >= re) seek(a, s + 1);
+  }
+};
+
+__device__ void produce(const MegaArgs &a, uint8_t *ring, uint64_t *full, uint64_t *empty, Ctl &ctl) {
+  const Tracer tr{a.trace};
+  ChunkWalk cp, pf;  // copies, and the L2 prefetch ahead of them
+  cp.seek(a, 0);
+  pf.seek(a, 0);
+  long ahead = 0;  // bytes asked of L2 and not yet copied
+  int c = 0;       // chunks issued
+  int marked = -1;
+  bool ok = true;
+  while (cp.ok) {
+    while (pf.ok && ahead < PREFETCH_AHEAD) {
+      const uint32_t pb = (uint32_t)pf.rows() * pf.K * 2;
+      prefetch_l2_bulk(pf.W + (size_t)pf.r0 * pf.K, pb);
+      if (pf.pair > 0) prefetch_l2_bulk(pf.W + (size_t)(pf.r0 + pf.pair) * pf.K, pb);
+      ahead += pf.pair > 0 ? 2 * pb : pb;
+      pf.step(a);
+    }
+    const int sl = c % NS;
+    if (c >= NS && !mbar_wait(smem_addr(&empty[sl]), ((c / NS) - 1) & 1, &ctl.abort)) {
+      ok = false;
+      break;
+    }
+    if (cp.s != marked) {
+      tr.mark(cp.s, 5);
+      marked = cp.s;
+    }
+    const uint32_t bytes = (uint32_t)cp.rows() * cp.K * 2, bar = smem_addr(&full[sl]);
+    const uint32_t dst = smem_addr(ring + (size_t)sl * SLOT);
+    mbar_expect_tx(bar, cp.pair > 0 ? 2 * bytes : bytes);
+    bulk_g2s(dst, cp.W + (size_t)cp.r0 * cp.K, bytes, bar);
+    if (cp.pair > 0) bulk_g2s(dst + bytes, cp.W + (size_t)(cp.r0 + cp.pair) * cp.K, bytes, bar);
+    ahead -= cp.pair > 0 ? 2 * bytes : bytes;
+    c++;
+    const int s_before = cp.s;
+    cp.step(a);
+    if (!cp.ok || cp.s != s_before) tr.mark(s_before, 6);
   }
   if (!ok) flag_error(ctl, a.err);
   // the block may not exit while a copy into its shared memory is in flight
@@ -146,16 +189,18 @@ __device__ void produce(const MegaArgs &a, uint8_t *ring, uint64_t *full, uint64
 // ---- GEMV stage ---------------------------------------------------------------------------
 
 // The consumer warps' share of a stage's chunks (chunk c goes to warp c mod MW, in slot
-// c mod NS = the same warp's slot). KI > 0:
-// K = 256 KI and every lane keeps its 8 KI input values in registers; KI = 0: any K with
-// K % 8 == 0, the input read from shared memory.
+// c mod NS = that warp's slot). KI > 0: K = 256 KI and every lane keeps its 8 KI input values
+// in registers; KI = 0: any K with K % 8 == 0, the input read from shared memory. `st` is
+// the stage's copy in shared memory.
 template <int KI>
 __device__ void gemv_chunks(const MegaStage &st, int rb, int re, int c0, const uint8_t *ring, uint64_t *full,
                             uint64_t *empty, const float *xs, Ctl &ctl, int *err) {
   const int lane = threadIdx.x & 31, cw = (threadIdx.x >> 5) - 1;
-  const int K = st.K, R = st.R;
+  const int K = st.K, R = st.R, mode = st.ep.mode;
   const bool dual = st.pair > 0;
-  const int mode = st.ep.mode;
+  float *__restrict__ Y = st.Y;
+  const float *__restrict__ v1 = st.ep.vec;
+  const float *__restrict__ v2 = st.ep.vec2;
   float xr[KI > 0 ? 8 * KI : 1];
   if (KI > 0) {
 #pragma unroll
@@ -167,9 +212,8 @@ __device__ void gemv_chunks(const MegaStage &st, int rb, int re, int c0, const u
     }
   }
   const int nch = re > rb ? (re - rb + R - 1) / R : 0;
-  for (int i = 0; i < nch; i++) {
+  for (int i = (cw - c0 % MW + MW) % MW; i < nch; i += MW) {
     const int c = c0 + i;  // chunk indices run over the whole step
-    if (c % MW != cw) continue;
     const int sl = c % NS;
     // decisions stay warp-uniform: the lanes shuffle below
     if (__shfl_sync(0xffffffffu, ctl.abort, 0)) break;
@@ -230,14 +274,14 @@ __device__ void gemv_chunks(const MegaStage &st, int rb, int re, int c0, const u
         const int n = r0 + rr;
         float y;
         if (mode == EPI_SCALE) {
-          y = g * __ldg(st.ep.vec + n);
+          y = g * __ldg(v1 + n);
         } else if (mode == EPI_SILU) {
-          const float gs = g * __ldg(st.ep.vec + n);
-          y = gs * sigmoidf_(gs) * (u * __ldg(st.ep.vec2 + n));
+          const float gs = g * __ldg(v1 + n);
+          y = gs * sigmoidf_(gs) * (u * __ldg(v2 + n));
         } else {
           y = g;
         }
-        st.Y[n] = y;
+        Y[n] = y;
       }
     }
     __syncwarp();
@@ -271,89 +315,210 @@ __device__ bool gemv_stage(const WarpTeam &tm, const MegaArgs &a, const MegaStag
     default: gemv_chunks<0>(st, rb, re, c, ring, full, empty, xs, ctl, a.err); break;
   }
   c += re > rb ? (re - rb + st.R - 1) / st.R : 0;
-  if (!team_ok(tm, ctl)) return false;
+  const bool ok = team_ok(tm, ctl);
   tr.mark(s, 3);
-  if (!st.he.enabled) return true;
-  // heads this block finished rows of: the block that completes a head runs its epilogue
-  const Dims &d = a.d;
-  const int hd = d.hd;
-  if (tm.tid() == 0) {
-    __threadfence();
-    int n = 0;
-    for (int h = rb / hd; re > rb && h <= (re - 1) / hd && n < MAX_HEADS_PER_BLOCK; h++) {
-      const int cnt = min(re, (h + 1) * hd) - max(rb, h * hd);
-      const int old = atomicAdd(&st.he.counters[h], cnt);
-      if (old + cnt == hd) {
-        st.he.counters[h] = 0;
-        ctl.heads[n++] = h;
-      }
-    }
-    ctl.nheads = n;
-  }
-  tm.sync();
-  const int nh = ctl.nheads;
-  if (nh > 0 && !team_wait_counter(tm, a.sync + 1, hd, ctl, a.err)) return false;  // RoPE table ready
-  for (int i = 0; i < nh; i++) {
-    __threadfence();
-    head_epilogue(tm, st.he, ctl.heads[i], 1, st.Y, 0);
-    fence_proxy_async_global();  // the ring rows are read by bulk copies after the barrier
-    tm.sync();
-  }
-  return true;
+  return ok;
 }
 
 // ---- attention stage ----------------------------------------------------------------------
 
+// Merge the items of kv head kh and gate: warp w loads the partials of items w, w + MW, ...
+// all at once (B per round) and folds them into a running (max, sum, output) per head; the
+// warps' results meet in shared memory (`scr`) and each thread finishes its outputs.
 template <int HD, int REP>
-__device__ __forceinline__ void merge_items(const WarpTeam &tm, const MegaStage &st, const Dims &d, int kh, int nblk,
-                                            float *scratch) {
+__device__ void merge_items(const WarpTeam &tm, const MegaStage &st, const Dims &d, int kh, int nblk, float *scr) {
+  constexpr int NV = HD / 32;
+  constexpr int B = REP <= 4 ? 3 : 1;
+  constexpr int OPT = (REP * HD + 32 * MW - 1) / (32 * MW);  // outputs per thread
+  const int cw = tm.warp(), lane = threadIdx.x & 31;
+  const float *pr = st.part + (size_t)kh * st.maxblk * REP * (HD + 2);
   const size_t col0 = (size_t)kh * REP * HD;
-  merge_splits<REP, HD>(tm, st.part + (size_t)kh * st.maxblk * REP * (HD + 2), nblk, scratch,
-                        st.qkvg + (size_t)(d.nh + 2 * d.nk) * HD + col0, st.sg + col0, nullptr, st.z + col0);
+  const float *graw = st.qkvg + (size_t)(d.nh + 2 * d.nk) * HD + col0;
+  float gv[OPT];
+#pragma unroll
+  for (int u = 0; u < OPT; u++) {
+    const int i = tm.tid() + u * tm.size();
+    gv[u] = i < REP * HD ? __ldcg(graw + i) : 0.f;
+  }
+  float M[REP], L[REP], acc[REP][NV];
+#pragma unroll
+  for (int h = 0; h < REP; h++) {
+    M[h] = -INFINITY;
+    L[h] = 0.f;
+#pragma unroll
+    for (int i = 0; i < NV; i++) acc[h][i] = 0.f;
+  }
+  for (int s0 = cw; s0 < nblk; s0 += B * MW) {
+    float m[B][REP], l[B][REP], o[B][REP][NV];
+#pragma unroll
+    for (int bb = 0; bb < B; bb++) {
+      const int sp = s0 + bb * MW;
+#pragma unroll
+      for (int h = 0; h < REP; h++) {
+        const float *base = pr + ((size_t)sp * REP + h) * (HD + 2);
+        const bool in = sp < nblk;
+        m[bb][h] = in ? __ldcg(base + HD) : -INFINITY;
+        l[bb][h] = in ? __ldcg(base + HD + 1) : 0.f;
+#pragma unroll
+        for (int i = 0; i < NV; i++) o[bb][h][i] = in ? __ldcg(base + lane * NV + i) : 0.f;
+      }
+    }
+#pragma unroll
+    for (int bb = 0; bb < B; bb++)
+#pragma unroll
+      for (int h = 0; h < REP; h++) {
+        const float mb = m[bb][h];
+        if (mb == -INFINITY) continue;
+        const float nm = fmaxf(M[h], mb);
+        const float sa = M[h] == -INFINITY ? 0.f : expf(M[h] - nm), sb = expf(mb - nm);
+        L[h] = L[h] * sa + l[bb][h] * sb;
+#pragma unroll
+        for (int i = 0; i < NV; i++) acc[h][i] = acc[h][i] * sa + o[bb][h][i] * sb;
+        M[h] = nm;
+      }
+  }
+  float *Ms = scr, *Ls = scr + MW * REP, *As = scr + 2 * MW * REP;  // [MW][REP], [MW][REP], [MW][REP][HD]
+#pragma unroll
+  for (int h = 0; h < REP; h++) {
+    if (lane == 0) {
+      Ms[cw * REP + h] = M[h];
+      Ls[cw * REP + h] = L[h];
+    }
+#pragma unroll
+    for (int i = 0; i < NV; i++) As[((size_t)cw * REP + h) * HD + lane * NV + i] = acc[h][i];
+  }
+  tm.sync();
+#pragma unroll
+  for (int u = 0; u < OPT; u++) {
+    const int i = tm.tid() + u * tm.size();
+    if (i >= REP * HD) break;
+    const int h = i / HD, cc = i % HD;
+    float Mx = -INFINITY;
+    for (int w = 0; w < MW; w++) Mx = fmaxf(Mx, Ms[w * REP + h]);
+    float Lx = 0.f, Ax = 0.f;
+    if (Mx != -INFINITY)
+      for (int w = 0; w < MW; w++) {
+        const float mw = Ms[w * REP + h];
+        if (mw == -INFINITY) continue;
+        const float e = expf(mw - Mx);
+        Lx += Ls[w * REP + h] * e;
+        Ax += As[((size_t)w * REP + h) * HD + cc] * e;
+      }
+    const float y = Lx > 0.f ? Ax / Lx : 0.f;
+    st.z[col0 + i] = y * sigmoidf_(gv[u] * __ldg(st.sg + col0 + i));
+  }
 }
 
 template <int HD>
 __device__ bool attn_stage(const WarpTeam &tm, const MegaArgs &a, const MegaStage &st, float *work, uint64_t *abar,
-                           int &aph, float (*qs)[HD], Ctl &ctl) {
-  constexpr int NV = HD / 32, NC = HD / 4;
+                           int &aph, float (*qs)[HD], float (*rope_s)[HD], Ctl &ctl) {
+  constexpr int NV = HD / 32, NC = HD / 4, HALF = HD / 2, PP = HALF / 32;  // pairs per lane
   const Dims &d = a.d;
   const int rep = d.nh / d.nk;
   const int cap = st.ring.cap, window = st.ring.window;
-  const int seq = a.rows.seq[0];
-  const long p = (long)a.rows.seq_pos[seq] + a.rows.off[0];
+  const int seq = ctl.seq;
+  const long p = (long)ctl.p;
   const long lo = window == INT_MAX ? 0 : (p + 1 - window > 0 ? p + 1 - window : 0);
   const long blk0 = lo / AK;
   const int nblk = (int)(p / AK - blk0 + 1);
   const int items = d.nk * nblk;
-  const char *slot = st.ring.base + (size_t)seq * st.ring.seq_stride + st.ring.off;
-  const int32_t *tags = reinterpret_cast<const int32_t *>(slot + st.ring.L.tags);
-  const size_t koff = st.ring.L.k, voff = st.ring.L.v;
+  char *slot = st.ring.base + (size_t)seq * st.ring.seq_stride + st.ring.off;
+  int32_t *tags = reinterpret_cast<int32_t *>(slot + st.ring.L.tags);
+  float *Kg = reinterpret_cast<float *>(slot + st.ring.L.k), *Vg = reinterpret_cast<float *>(slot + st.ring.L.v);
+  const float *qkvg = st.qkvg;
   float *Ks = work, *Vs = work + AK * HD;
   const int cw = tm.warp(), lane = threadIdx.x & 31;
+  const int kw = rep % MW;  // the warp that prepares the new key and value
+  const float *rc = rope_s[st.rope_kind], *rsn = rope_s[st.rope_kind] + HALF;
   const float scale = 1.f / sqrtf((float)HD);
   for (int it = blockIdx.x; it < items; it += gridDim.x) {
     const int kh = it / nblk, blk = it % nblk;
     const long P0 = (blk0 + blk) * AK;
     const int rr0 = (int)(P0 % cap);
-    tm.sync();  // the previous item's tiles and scratch are no longer read
+    const bool has_p = P0 + AK > p;  // the item that holds the row's own position
+    tm.sync();                       // the previous item's tiles and scratch are no longer read
     if (tm.tid() == 0) {
-      fence_proxy_async_global();  // ring rows written by this launch's head epilogues
+      fence_proxy_async_global();  // ring rows written earlier in this launch
       fence_proxy_async_smem();    // the input row, tiles and merge scratch written before
       const uint32_t bar = smem_addr(abar), bytes = AK * HD * 4;
       mbar_expect_tx(bar, 2 * bytes);
-      bulk_g2s(smem_addr(Ks), slot + koff + ((size_t)kh * cap + rr0) * HD * 4, bytes, bar);
-      bulk_g2s(smem_addr(Vs), slot + voff + ((size_t)kh * cap + rr0) * HD * 4, bytes, bar);
+      bulk_g2s(smem_addr(Ks), Kg + ((size_t)kh * cap + rr0) * HD, bytes, bar);
+      bulk_g2s(smem_addr(Vs), Vg + ((size_t)kh * cap + rr0) * HD, bytes, bar);
     }
     aph++;
-    for (int i = tm.tid(); i < rep * HD; i += tm.size()) qs[i / HD][i % HD] = __ldcg(st.qkvg + (size_t)kh * rep * HD + i);
+    const int tg = __ldcg(tags + rr0 + lane);
+    // the group's query heads: RoPE on the pairs (j, j + hd/2), justnorm, times s_q^2
+    for (int h = cw; h < rep; h += MW) {
+      const size_t off = (size_t)(kh * rep + h) * HD;
+      float x[PP], y[PP], ss = 0.f;
+#pragma unroll
+      for (int u = 0; u < PP; u++) {
+        const int j = lane + 32 * u;
+        const float a0 = __ldcg(qkvg + off + j), b0 = __ldcg(qkvg + off + j + HALF);
+        x[u] = a0 * rc[j] - b0 * rsn[j];
+        y[u] = b0 * rc[j] + a0 * rsn[j];
+        ss += x[u] * x[u] + y[u] * y[u];
+      }
+      ss = warp_sum(ss);
+      const float inv = 1.f / sqrtf(ss + DORY_EPS);
+#pragma unroll
+      for (int u = 0; u < PP; u++) {
+        const int j = lane + 32 * u;
+        qs[h][j] = x[u] * inv * __ldg(st.sq + off + j);
+        qs[h][j + HALF] = y[u] * inv * __ldg(st.sq + off + j + HALF);
+      }
+    }
+    // the new key (rotated, normalised) and value of kv head kh
+    float kx[PP], ky[PP], vx[PP], vy[PP];
+    if (has_p && cw == kw) {
+      const size_t ko = (size_t)(d.nh + kh) * HD, vo = (size_t)(d.nh + d.nk + kh) * HD;
+      float ss = 0.f;
+#pragma unroll
+      for (int u = 0; u < PP; u++) {
+        const int j = lane + 32 * u;
+        const float a0 = __ldcg(qkvg + ko + j), b0 = __ldcg(qkvg + ko + j + HALF);
+        kx[u] = a0 * rc[j] - b0 * rsn[j];
+        ky[u] = b0 * rc[j] + a0 * rsn[j];
+        ss += kx[u] * kx[u] + ky[u] * ky[u];
+        vx[u] = __ldcg(qkvg + vo + j);
+        vy[u] = __ldcg(qkvg + vo + j + HALF);
+      }
+      ss = warp_sum(ss);
+      const float inv = 1.f / sqrtf(ss + DORY_EPS);
+#pragma unroll
+      for (int u = 0; u < PP; u++) {
+        kx[u] *= inv;
+        ky[u] *= inv;
+      }
+    }
     const bool landed = mbar_wait(smem_addr(abar), (aph - 1) & 1, &ctl.abort);
     if (!landed && lane == 0) flag_error(ctl, a.err);
     if (!team_ok(tm, ctl)) return false;
+    if (has_p && cw == kw) {
+      // into the tile (it holds the ring's older row there), and into the ring
+      const int jp = (int)(p - P0), rr = (int)(p % cap);
+      float *kg = Kg + ((size_t)kh * cap + rr) * HD, *vg = Vg + ((size_t)kh * cap + rr) * HD;
+#pragma unroll
+      for (int u = 0; u < PP; u++) {
+        const int j = lane + 32 * u;
+        Ks[jp * HD + j] = kx[u];
+        Ks[jp * HD + j + HALF] = ky[u];
+        Vs[jp * HD + j] = vx[u];
+        Vs[jp * HD + j + HALF] = vy[u];
+        kg[j] = kx[u];
+        kg[j + HALF] = ky[u];
+        vg[j] = vx[u];
+        vg[j + HALF] = vy[u];
+      }
+      if (kh == 0 && lane == 0) tags[rr] = (int32_t)p;
+      fence_proxy_async_global();  // later passes read this row with bulk copies
+    }
+    tm.sync();
     for (int h = cw; h < rep; h += MW) {
-      // warp cw: query heads kh * rep + h; lane j: key P0 + j
+      // warp cw: query head kh * rep + h; lane j: key P0 + j
       const int j = lane;
       const long pe = P0 + j;
-      const bool valid = pe >= lo && pe <= p && __ldcg(tags + rr0 + j) == (int32_t)pe;
+      const bool valid = pe >= lo && pe <= p && (tg == (int32_t)pe || pe == p);
       float s0 = 0.f, s1 = 0.f;
       if (valid) {
         const float4 *kr = reinterpret_cast<const float4 *>(Ks + j * HD);
@@ -389,16 +554,14 @@ __device__ bool attn_stage(const WarpTeam &tm, const MegaArgs &a, const MegaStag
       }
     }
     // the last item of this kv head merges the items and gates
-    __threadfence();
     tm.sync();
     if (tm.tid() == 0) {
-      const int old = atomicAdd(a.actr + kh, 1);
+      const int old = atom_add_acq_rel_gpu(a.actr + kh, 1);
       ctl.last = old == nblk - 1;
       if (ctl.last) a.actr[kh] = 0;
     }
     tm.sync();
     if (ctl.last) {
-      __threadfence();
       switch (rep) {
         case 1: merge_items<HD, 1>(tm, st, d, kh, nblk, Ks); break;
         case 2: merge_items<HD, 2>(tm, st, d, kh, nblk, Ks); break;
@@ -410,6 +573,14 @@ __device__ bool attn_stage(const WarpTeam &tm, const MegaArgs &a, const MegaStag
   return true;
 }
 
+// Threads 1.. of the team copy a stage's descriptor into shared memory (thread 0 is waiting
+// at the grid barrier meanwhile; the barrier's team sync publishes the copy).
+__device__ __forceinline__ void copy_stage(const WarpTeam &tm, const MegaStage *src, MegaStage *dst) {
+  constexpr int n = sizeof(MegaStage) / 4;
+  const int i = tm.tid() - 1;
+  if (i >= 0 && i < n) reinterpret_cast<int *>(dst)[i] = __ldg(reinterpret_cast<const int *>(src) + i);
+}
+
 // ---- the kernel ---------------------------------------------------------------------------
 
 template <int HD>
@@ -419,6 +590,8 @@ __global__ void __launch_bounds__(MTHREADS, 1) mega_decode_kernel(const __grid_c
   float *work = reinterpret_cast<float *>(ring + (size_t)NS * SLOT);
   __shared__ __align__(8) uint64_t full[NS], empty[NS], abar;
   __shared__ __align__(16) float qs[8][HD];
+  __shared__ __align__(16) float rope_s[2][HD];
+  __shared__ __align__(16) MegaStage sst;
   __shared__ Ctl ctl;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -439,10 +612,13 @@ __global__ void __launch_bounds__(MTHREADS, 1) mega_decode_kernel(const __grid_c
   const WarpTeam tm{1, MW, 1};
   const int G = gridDim.x, b = blockIdx.x;
   const Dims &d = a.d;
-  // RoPE table of the row's position, one entry per block (f64 angle, f32 table; the
-  // heads' epilogues wait for all of it)
+  const Tracer tr{tm.tid() == 0 ? a.trace : nullptr};
+  // the row's position, and the RoPE table of it spread over the blocks (f64 angle, f32
+  // table; the first attention stage waits for all of it)
   if (tm.tid() == 0) {
-    const long pos = (long)a.rows.seq_pos[a.rows.seq[0]] + a.rows.off[0];
+    ctl.seq = a.rows.seq[0];
+    const long pos = (long)a.rows.seq_pos[ctl.seq] + a.rows.off[0];
+    ctl.p = pos;
     const int half = d.hd / 2;
     int n = 0;
     for (int i = b; i < d.hd; i += G, n++) {
@@ -454,26 +630,34 @@ __global__ void __launch_bounds__(MTHREADS, 1) mega_decode_kernel(const __grid_c
       a.rope[kind * d.hd + j] = (float)cs;
       a.rope[kind * d.hd + half + j] = (float)sn;
     }
-    if (n) {
-      __threadfence();
-      red_release_gpu_add(a.sync + 1, n);
-    }
+    if (n) red_release_gpu_add(a.sync + 1, n);
   }
   int c = 0, aph = 0;
-  bool ok = true;
-  const Tracer tr{tm.tid() == 0 ? a.trace : nullptr};
+  bool ok = true, rope_ready = false;
   for (int s = 0; s < a.nstages && ok; s++) {
-    const MegaStage &st = a.stages[s];
     tr.mark(s, 0);
-    if (s > 0 && !team_wait_counter(tm, a.sync, s * G, ctl, a.err)) {
+    copy_stage(tm, a.stages + s, &sst);
+    if (!team_wait_counter(tm, a.sync, s * G, ctl, a.err)) {
       ok = false;
       break;
     }
     tr.mark(s, 1);
     // every reader of the position has passed: the last stage advances it
     if (s == a.nstages - 1 && b == 0 && tm.tid() == 0) a.seq_pos[a.adv_seq] += a.adv_cnt;
-    if (st.kind == MK_GEMV) ok = gemv_stage(tm, a, st, s, c, ring, full, empty, work, ctl);
-    else ok = attn_stage<HD>(tm, a, st, work, &abar, aph, qs, ctl);
+    if (sst.kind == MK_GEMV) {
+      ok = gemv_stage(tm, a, sst, s, c, ring, full, empty, work, ctl);
+    } else {
+      if (!rope_ready) {
+        if (!team_wait_counter(tm, a.sync + 1, HD, ctl, a.err)) {
+          ok = false;
+          break;
+        }
+        for (int i = tm.tid(); i < 2 * HD; i += tm.size()) rope_s[i / HD][i % HD] = __ldcg(a.rope + i);
+        tm.sync();
+        rope_ready = true;
+      }
+      ok = attn_stage<HD>(tm, a, sst, work, &abar, aph, qs, rope_s, ctl);
+    }
     tr.mark(s, 4);
     if (ok && s + 1 < a.nstages) grid_arrive(tm, a.sync);
   }
@@ -489,8 +673,6 @@ int mega_chunk_rows(int K, bool dual) {  // 0: a row does not fit a slot
   const size_t rb = (size_t)K * 2 * (dual ? 2 : 1);
   return (int)std::min<size_t>(SLOT / rb, 64);
 }
-
-int mega_max_heads_per_block() { return MAX_HEADS_PER_BLOCK; }
 
 size_t mega_work_floats() { return WORK / 4; }
 

@@ -193,10 +193,12 @@ struct MegaStage {
   GemvIn in;
   float *Y;
   EpiArgs ep;
-  HeadEpi he;     // q/k/v/g projection: per-head RoPE, norm, ring write
-  // MK_ATTN: windowed attention of the one row over `ring`, gate, into z
+  // MK_ATTN: from the raw q/k/v/g row, RoPE + justnorm of q and k, q * s_q^2, the ring
+  // write of the new k and v, windowed attention over `ring`, the gate, into z
   Ring ring;
   const float *qkvg;
+  const float *sq;
+  int rope_kind;  // 0 sliding, 1 full (which RoPE base)
   const float *sg;
   float *z;
   float *part;    // [nk][maxblk][REP][hd + 2] item partials
@@ -228,7 +230,6 @@ constexpr int MEGA_TRACE_EVENTS = 8;
 size_t mega_smem_bytes(int hd);
 bool mega_supported(int hd, int sms);
 int mega_chunk_rows(int K, bool dual);  // rows (or gate/up row pairs) per streamed chunk; 0: too long
-int mega_max_heads_per_block();
 size_t mega_work_floats();              // shared scratch of a block: input row, tiles, merge
 constexpr int MEGA_AK = 32;             // positions per attention item
 cudaError_t launch_mega_decode(const MegaArgs &a, int grid, cudaStream_t s);
