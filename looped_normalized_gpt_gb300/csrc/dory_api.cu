@@ -1191,6 +1191,9 @@ int dory_create(const dory_config *cfg, const dory_weights *w, void *stream, dor
               dm.ffn % 8 == 0 && q_size % 8 == 0 && kmax <= mega_work_floats() &&
               (size_t)2 * MEGA_AK * dm.hd <= mega_work_floats() && mega_chunk_rows(dm.hidden, true) >= 1 &&
               mega_chunk_rows((int)kmax, false) >= 1;
+    // the merge's per-warp partials of a kv head's query heads
+    if ((size_t)mega_consumer_warps() * rep * (dm.hd + 2) > mega_work_floats()) ok = false;
+    if (dm.hidden > 8192 || dm.ffn > 8192 || q_size > 8192) ok = false;  // four 16-byte columns per thread
     for (const OrdInfo &o : d->ords) {
       const long keys = o.window == INT_MAX ? (long)o.cap : std::min<long>(o.window, o.cap);
       const long maxblk = keys / MEGA_AK + 2;

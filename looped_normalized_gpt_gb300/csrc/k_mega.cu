@@ -7,15 +7,15 @@
 // in stage order, asks L2 for the bytes about PREFETCH_AHEAD ahead (cp.async.bulk.prefetch),
 // and copies chunks into a ring of shared-memory slots with cp.async.bulk, completion on one
 // mbarrier per slot. It never waits for activations, so HBM keeps streaming the next stages'
-// weights while the consumers wait at a grid barrier or run attention. Warps 1..7 are the
-// consumers; consumer warp w owns slot w and takes the step's chunks w, w + 7, w + 14, ...
-// (so each wait on a slot's barrier is for the phase right after the one that warp saw
-// last). Per stage the consumers
+// weights while the consumers wait at a grid barrier or run attention. Warps 1..8 are the
+// consumers; they take the chunks in order, all of them on each chunk (so a slot's barrier
+// is always awaited for the phase right after the one last seen). Per stage the consumers
 //   * copy the stage's descriptor into shared memory while their first thread waits until
 //     every block has finished the stage before (a counter in global memory);
 //   * GEMV: build the input row in shared memory (the embedding, a row norm, or the nGPT
-//     residual with the loop mix), then each warp reduces its chunks against it (bf16
-//     weights, f32 sums), applies the epilogue (SwiGLU, logit scale) and frees the slot;
+//     residual with the loop mix), then reduce each chunk against it (bf16 weights, f32
+//     sums; a thread per 16-byte column, shuffles and shared memory across the columns),
+//     free the slot and apply the epilogue (SwiGLU, logit scale);
 //   * attention (dory.rs fn attn_layer), in items of 32 positions of one kv head: the K and
 //     V rows of an item are contiguous in the ring and arrive with two bulk copies; meanwhile
 //     warp h rotates and normalises query head h of the group from the raw projection row
@@ -40,16 +40,16 @@ namespace dory {
 
 namespace {
 
-constexpr int MW = 7;                             // consumer warps
+constexpr int MW = 8;                             // consumer warps
 constexpr int MTHREADS = 32 * (MW + 1);           // and the producer warp
-constexpr int NS = MW;                            // weight slots, one per consumer warp
+constexpr int NS = 7;                             // weight slots
 constexpr uint32_t SLOT = 26 * 1024;              // bytes per slot
+constexpr int RMAX = 8;                           // rows (or row pairs) per chunk at most
 constexpr uint32_t WORK = 32 * 1024;              // input row, or attention tiles and merge scratch
 constexpr int AK = MEGA_AK;                       // positions per attention item
 constexpr uint32_t SPIN_LIMIT = 1u << 22;         // polls of a global counter
 constexpr int ERR_MEGA = 6;                       // dev_err: a wait of the persistent kernel ran out
 constexpr long PREFETCH_AHEAD = 448 * 1024;       // L2 lead of the producer, bytes per block
-static_assert(NS == MW, "a slot's barrier phases are followed by one warp");
 static_assert(sizeof(MegaStage) % 4 == 0 && sizeof(MegaStage) / 4 < 32 * MW, "stage copy by the team");
 
 struct Ctl {
@@ -188,104 +188,101 @@ __device__ void produce(const MegaArgs &a, uint8_t *ring, uint64_t *full, uint64
 
 // ---- GEMV stage ---------------------------------------------------------------------------
 
-// The consumer warps' share of a stage's chunks (chunk c goes to warp c mod MW, in slot
-// c mod NS = that warp's slot). KI > 0: K = 256 KI and every lane keeps its 8 KI input values
-// in registers; KI = 0: any K with K % 8 == 0, the input read from shared memory. `st` is
-// the stage's copy in shared memory.
-template <int KI>
-__device__ void gemv_chunks(const MegaStage &st, int rb, int re, int c0, const uint8_t *ring, uint64_t *full,
-                            uint64_t *empty, const float *xs, Ctl &ctl, int *err) {
-  const int lane = threadIdx.x & 31, cw = (threadIdx.x >> 5) - 1;
-  const int K = st.K, R = st.R, mode = st.ep.mode;
-  const bool dual = st.pair > 0;
+// A stage's chunks, each reduced by the whole team in order: thread t owns the 16-byte
+// columns t, t + 256, ... (SEG of them) of every row, keeps its input values for them in
+// registers, sums its columns of the chunk's rows (and of the up rows, DUAL), the warps
+// reduce their rows with shuffles, and the warps' partial sums meet in shared memory `red`
+// (two buffers, alternating by chunk). The slot is freed as soon as the partials are out
+// of it. `st` is the stage's copy in shared memory.
+template <int SEG, bool DUAL>
+__device__ void gemv_chunks(const WarpTeam &tm, const MegaStage &st, int rb, int re, int c0, const uint8_t *ring,
+                            uint64_t *full, uint64_t *empty, const float *xs, float (*red)[MW][2 * RMAX], Ctl &ctl,
+                            int *err) {
+  const int t = tm.tid(), lane = threadIdx.x & 31, cw = tm.warp();
+  const int K = st.K, R = st.R, mode = st.ep.mode, nu = K / 8;  // 16-byte columns per row
   float *__restrict__ Y = st.Y;
   const float *__restrict__ v1 = st.ep.vec;
   const float *__restrict__ v2 = st.ep.vec2;
-  float xr[KI > 0 ? 8 * KI : 1];
-  if (KI > 0) {
+  float xr[8 * SEG];
 #pragma unroll
-    for (int i = 0; i < KI; i++) {
-      const float4 p = *reinterpret_cast<const float4 *>(xs + i * 256 + lane * 8);
-      const float4 q = *reinterpret_cast<const float4 *>(xs + i * 256 + lane * 8 + 4);
-      xr[8 * i + 0] = p.x; xr[8 * i + 1] = p.y; xr[8 * i + 2] = p.z; xr[8 * i + 3] = p.w;
-      xr[8 * i + 4] = q.x; xr[8 * i + 5] = q.y; xr[8 * i + 6] = q.z; xr[8 * i + 7] = q.w;
+  for (int g = 0; g < SEG; g++) {
+    const int u = t + g * 32 * MW;
+    float4 p = make_float4(0.f, 0.f, 0.f, 0.f), q = p;
+    if (u < nu) {
+      p = *reinterpret_cast<const float4 *>(xs + u * 8);
+      q = *reinterpret_cast<const float4 *>(xs + u * 8 + 4);
     }
+    xr[8 * g + 0] = p.x; xr[8 * g + 1] = p.y; xr[8 * g + 2] = p.z; xr[8 * g + 3] = p.w;
+    xr[8 * g + 4] = q.x; xr[8 * g + 5] = q.y; xr[8 * g + 6] = q.z; xr[8 * g + 7] = q.w;
   }
   const int nch = re > rb ? (re - rb + R - 1) / R : 0;
-  for (int i = (cw - c0 % MW + MW) % MW; i < nch; i += MW) {
-    const int c = c0 + i;  // chunk indices run over the whole step
-    const int sl = c % NS;
-    // decisions stay warp-uniform: the lanes shuffle below
-    if (__shfl_sync(0xffffffffu, ctl.abort, 0)) break;
-    if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&full[sl]), (c / NS) & 1, &ctl.abort))) {
-      if (lane == 0) flag_error(ctl, err);
-      break;
-    }
+  for (int i = 0; i < nch; i++) {
+    const int c = c0 + i, sl = c % NS;  // chunk indices run over the whole step
+    const bool landed = mbar_wait(smem_addr(&full[sl]), (c / NS) & 1, &ctl.abort);
+    if (!landed) flag_error(ctl, err);  // the block stops at the stage's end; the slot stays taken
     const int r0 = rb + i * R, nr = min(R, re - r0);
-    const __nv_bfloat16 *w = reinterpret_cast<const __nv_bfloat16 *>(ring + (size_t)sl * SLOT);
-    for (int rr = 0; rr < nr; rr++) {
-      const uint4 *w0 = reinterpret_cast<const uint4 *>(w + (size_t)rr * K);
-      const uint4 *w1 = reinterpret_cast<const uint4 *>(w + (size_t)(nr + rr) * K);
+    const uint4 *w = reinterpret_cast<const uint4 *>(ring + (size_t)sl * SLOT);
+    float acc[RMAX], acc2[RMAX];
+#pragma unroll
+    for (int r = 0; r < RMAX; r++) {
       float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
-      if (KI > 0) {
+      if (r < nr && landed) {
 #pragma unroll
-        for (int k = 0; k < KI; k++) {
-          float wv[8];
-          unpack8(w0[k * 32 + lane], wv);
-#pragma unroll
-          for (int e = 0; e < 8; e += 2) {
-            a0 = fmaf(wv[e], xr[8 * k + e], a0);
-            a1 = fmaf(wv[e + 1], xr[8 * k + e + 1], a1);
-          }
-          if (dual) {
-            unpack8(w1[k * 32 + lane], wv);
+        for (int g = 0; g < SEG; g++) {
+          const int u = t + g * 32 * MW;
+          if (u < nu) {
+            float wv[8];
+            unpack8(w[r * nu + u], wv);
 #pragma unroll
             for (int e = 0; e < 8; e += 2) {
-              b0 = fmaf(wv[e], xr[8 * k + e], b0);
-              b1 = fmaf(wv[e + 1], xr[8 * k + e + 1], b1);
+              a0 = fmaf(wv[e], xr[8 * g + e], a0);
+              a1 = fmaf(wv[e + 1], xr[8 * g + e + 1], a1);
             }
-          }
-        }
-      } else {
-        for (int k = lane * 8; k < K; k += 256) {
-          float wv[8];
-          const float4 p = *reinterpret_cast<const float4 *>(xs + k);
-          const float4 q = *reinterpret_cast<const float4 *>(xs + k + 4);
-          const float xv[8] = {p.x, p.y, p.z, p.w, q.x, q.y, q.z, q.w};
-          unpack8(w0[k / 8], wv);
+            if (DUAL) {
+              unpack8(w[(nr + r) * nu + u], wv);
 #pragma unroll
-          for (int e = 0; e < 8; e += 2) {
-            a0 = fmaf(wv[e], xv[e], a0);
-            a1 = fmaf(wv[e + 1], xv[e + 1], a1);
-          }
-          if (dual) {
-            unpack8(w1[k / 8], wv);
-#pragma unroll
-            for (int e = 0; e < 8; e += 2) {
-              b0 = fmaf(wv[e], xv[e], b0);
-              b1 = fmaf(wv[e + 1], xv[e + 1], b1);
+              for (int e = 0; e < 8; e += 2) {
+                b0 = fmaf(wv[e], xr[8 * g + e], b0);
+                b1 = fmaf(wv[e + 1], xr[8 * g + e + 1], b1);
+              }
             }
           }
         }
       }
-      const float g = warp_sum(a0 + a1);
-      const float u = dual ? warp_sum(b0 + b1) : 0.f;
+      acc[r] = a0 + a1;
+      acc2[r] = b0 + b1;
+    }
+    float(*rb_)[2 * RMAX] = red[i & 1];
+#pragma unroll
+    for (int r = 0; r < RMAX; r++) {
+      if (r >= nr) break;
+      const float g = warp_sum(acc[r]);
+      const float u = DUAL ? warp_sum(acc2[r]) : 0.f;
       if (lane == 0) {
-        const int n = r0 + rr;
-        float y;
-        if (mode == EPI_SCALE) {
-          y = g * __ldg(v1 + n);
-        } else if (mode == EPI_SILU) {
-          const float gs = g * __ldg(v1 + n);
-          y = gs * sigmoidf_(gs) * (u * __ldg(v2 + n));
-        } else {
-          y = g;
-        }
-        Y[n] = y;
+        rb_[cw][r] = g;
+        rb_[cw][RMAX + r] = u;
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_addr(&empty[sl]));
+    tm.sync();
+    if (t == 0 && !ctl.abort) mbar_arrive(smem_addr(&empty[sl]));  // the partials are out of the slot
+    if (t < nr) {
+      float g = 0.f, u = 0.f;
+      for (int ww = 0; ww < MW; ww++) {
+        g += rb_[ww][t];
+        if (DUAL) u += rb_[ww][RMAX + t];
+      }
+      const int n = r0 + t;
+      float y;
+      if (mode == EPI_SCALE) {
+        y = g * __ldg(v1 + n);
+      } else if (mode == EPI_SILU) {
+        const float gs = g * __ldg(v1 + n);
+        y = gs * sigmoidf_(gs) * (u * __ldg(v2 + n));
+      } else {
+        y = g;
+      }
+      Y[n] = y;
+    }
   }
 }
 
@@ -296,7 +293,8 @@ __device__ __forceinline__ void input_row(const WarpTeam &tm, const GemvIn &in, 
 
 // Returns false (team-uniformly) when the block has stopped.
 __device__ bool gemv_stage(const WarpTeam &tm, const MegaArgs &a, const MegaStage &st, int s, int &c,
-                           const uint8_t *ring, uint64_t *full, uint64_t *empty, float *xs, Ctl &ctl) {
+                           const uint8_t *ring, uint64_t *full, uint64_t *empty, float *xs,
+                           float (*red)[MW][2 * RMAX], Ctl &ctl) {
   const Tracer tr{tm.tid() == 0 ? a.trace : nullptr};
   const int G = gridDim.x, b = blockIdx.x;
   const int N = st.N, K = st.K;
@@ -307,13 +305,21 @@ __device__ bool gemv_stage(const WarpTeam &tm, const MegaArgs &a, const MegaStag
   else if (kc <= 6) input_row<6>(tm, st.in, K, xs);
   else input_row<8>(tm, st.in, K, xs);
   tr.mark(s, 2);
-  switch (K) {
-    case 256: gemv_chunks<1>(st, rb, re, c, ring, full, empty, xs, ctl, a.err); break;
-    case 512: gemv_chunks<2>(st, rb, re, c, ring, full, empty, xs, ctl, a.err); break;
-    case 1024: gemv_chunks<4>(st, rb, re, c, ring, full, empty, xs, ctl, a.err); break;
-    case 2048: gemv_chunks<8>(st, rb, re, c, ring, full, empty, xs, ctl, a.err); break;
-    default: gemv_chunks<0>(st, rb, re, c, ring, full, empty, xs, ctl, a.err); break;
+  const int seg = (K / 8 + 32 * MW - 1) / (32 * MW);
+  const bool dual = st.pair > 0;
+#define MEGA_CHUNKS(S)                                                                     \
+  if (dual) gemv_chunks<S, true>(tm, st, rb, re, c, ring, full, empty, xs, red, ctl, a.err); \
+  else gemv_chunks<S, false>(tm, st, rb, re, c, ring, full, empty, xs, red, ctl, a.err);
+  if (seg <= 1) {
+    MEGA_CHUNKS(1)
+  } else if (seg <= 2) {
+    MEGA_CHUNKS(2)
+  } else if (seg <= 3) {
+    MEGA_CHUNKS(3)
+  } else {
+    MEGA_CHUNKS(4)
   }
+#undef MEGA_CHUNKS
   c += re > rb ? (re - rb + st.R - 1) / st.R : 0;
   const bool ok = team_ok(tm, ctl);
   tr.mark(s, 3);
@@ -584,7 +590,9 @@ __device__ __forceinline__ void copy_stage(const WarpTeam &tm, const MegaStage *
 // ---- the kernel ---------------------------------------------------------------------------
 
 template <int HD>
-__global__ void __launch_bounds__(MTHREADS, 1) mega_decode_kernel(const __grid_constant__ MegaArgs a) {
+// 288 threads x 224 registers fit the SM; the cap keeps the compiler from spilling under a
+// lower default
+__global__ void __maxnreg__(224) mega_decode_kernel(const __grid_constant__ MegaArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   float *work = reinterpret_cast<float *>(ring + (size_t)NS * SLOT);
@@ -592,6 +600,7 @@ __global__ void __launch_bounds__(MTHREADS, 1) mega_decode_kernel(const __grid_c
   __shared__ __align__(16) float qs[8][HD];
   __shared__ __align__(16) float rope_s[2][HD];
   __shared__ __align__(16) MegaStage sst;
+  __shared__ float red[2][MW][2 * RMAX];
   __shared__ Ctl ctl;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -645,7 +654,7 @@ __global__ void __launch_bounds__(MTHREADS, 1) mega_decode_kernel(const __grid_c
     // every reader of the position has passed: the last stage advances it
     if (s == a.nstages - 1 && b == 0 && tm.tid() == 0) a.seq_pos[a.adv_seq] += a.adv_cnt;
     if (sst.kind == MK_GEMV) {
-      ok = gemv_stage(tm, a, sst, s, c, ring, full, empty, work, ctl);
+      ok = gemv_stage(tm, a, sst, s, c, ring, full, empty, work, red, ctl);
     } else {
       if (!rope_ready) {
         if (!team_wait_counter(tm, a.sync + 1, HD, ctl, a.err)) {
@@ -671,8 +680,10 @@ size_t mega_smem_bytes(int) { return 1024 + (size_t)NS * SLOT + WORK; }
 
 int mega_chunk_rows(int K, bool dual) {  // 0: a row does not fit a slot
   const size_t rb = (size_t)K * 2 * (dual ? 2 : 1);
-  return (int)std::min<size_t>(SLOT / rb, 64);
+  return (int)std::min<size_t>(SLOT / rb, RMAX);
 }
+
+int mega_consumer_warps() { return MW; }
 
 size_t mega_work_floats() { return WORK / 4; }
 

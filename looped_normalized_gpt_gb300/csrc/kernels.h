@@ -231,6 +231,7 @@ size_t mega_smem_bytes(int hd);
 bool mega_supported(int hd, int sms);
 int mega_chunk_rows(int K, bool dual);  // rows (or gate/up row pairs) per streamed chunk; 0: too long
 size_t mega_work_floats();              // shared scratch of a block: input row, tiles, merge
+int mega_consumer_warps();
 constexpr int MEGA_AK = 32;             // positions per attention item
 cudaError_t launch_mega_decode(const MegaArgs &a, int grid, cudaStream_t s);
 
