@@ -1193,7 +1193,7 @@ int dory_create(const dory_config *cfg, const dory_weights *w, void *stream, dor
               mega_chunk_rows((int)kmax, false) >= 1;
     // the merge's per-warp partials of a kv head's query heads
     if ((size_t)mega_consumer_warps() * rep * (dm.hd + 2) > mega_work_floats()) ok = false;
-    if (dm.hidden > 8192 || dm.ffn > 8192 || q_size > 8192) ok = false;  // four 16-byte columns per thread
+    if (dm.hidden > 6144 || dm.ffn > 6144 || q_size > 6144) ok = false;  // three 16-byte columns per thread
     for (const OrdInfo &o : d->ords) {
       const long keys = o.window == INT_MAX ? (long)o.cap : std::min<long>(o.window, o.cap);
       const long maxblk = keys / MEGA_AK + 2;

@@ -314,10 +314,8 @@ __device__ bool gemv_stage(const WarpTeam &tm, const MegaArgs &a, const MegaStag
     MEGA_CHUNKS(1)
   } else if (seg <= 2) {
     MEGA_CHUNKS(2)
-  } else if (seg <= 3) {
-    MEGA_CHUNKS(3)
   } else {
-    MEGA_CHUNKS(4)
+    MEGA_CHUNKS(3)
   }
 #undef MEGA_CHUNKS
   c += re > rb ? (re - rb + st.R - 1) / st.R : 0;
@@ -332,9 +330,9 @@ __device__ bool gemv_stage(const WarpTeam &tm, const MegaArgs &a, const MegaStag
 // all at once (B per round) and folds them into a running (max, sum, output) per head; the
 // warps' results meet in shared memory (`scr`) and each thread finishes its outputs.
 template <int HD, int REP>
-__device__ void merge_items(const WarpTeam &tm, const MegaStage &st, const Dims &d, int kh, int nblk, float *scr) {
+__device__ __noinline__ void merge_items(  // its own register allocation: keeps the main loop from spillingconst WarpTeam &tm, const MegaStage &st, const Dims &d, int kh, int nblk, float *scr) {
   constexpr int NV = HD / 32;
-  constexpr int B = REP <= 4 ? 3 : 1;
+  constexpr int B = REP <= 2 ? 2 : 1;  // partial sets a warp loads at once (registers)
   constexpr int OPT = (REP * HD + 32 * MW - 1) / (32 * MW);  // outputs per thread
   const int cw = tm.warp(), lane = threadIdx.x & 31;
   const float *pr = st.part + (size_t)kh * st.maxblk * REP * (HD + 2);
@@ -590,9 +588,8 @@ __device__ __forceinline__ void copy_stage(const WarpTeam &tm, const MegaStage *
 // ---- the kernel ---------------------------------------------------------------------------
 
 template <int HD>
-// 288 threads x 224 registers fit the SM; the cap keeps the compiler from spilling under a
-// lower default
-__global__ void __maxnreg__(224) mega_decode_kernel(const __grid_constant__ MegaArgs a) {
+// 9 warps: at most 3 on an SM sub-partition, so at most 168 registers a thread
+__global__ void __launch_bounds__(MTHREADS, 1) mega_decode_kernel(const __grid_constant__ MegaArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   float *work = reinterpret_cast<float *>(ring + (size_t)NS * SLOT);
