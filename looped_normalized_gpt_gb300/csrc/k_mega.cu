@@ -329,8 +329,9 @@ __device__ bool gemv_stage(const WarpTeam &tm, const MegaArgs &a, const MegaStag
 // Merge the items of kv head kh and gate: warp w loads the partials of items w, w + MW, ...
 // all at once (B per round) and folds them into a running (max, sum, output) per head; the
 // warps' results meet in shared memory (`scr`) and each thread finishes its outputs.
+// (not inlined: its own register allocation keeps the main loop from spilling)
 template <int HD, int REP>
-__device__ __noinline__ void merge_items(  // its own register allocation: keeps the main loop from spillingconst WarpTeam &tm, const MegaStage &st, const Dims &d, int kh, int nblk, float *scr) {
+__device__ __noinline__ void merge_items(const WarpTeam &tm, const MegaStage &st, const Dims &d, int kh, int nblk, float *scr) {
   constexpr int NV = HD / 32;
   constexpr int B = REP <= 2 ? 2 : 1;  // partial sets a warp loads at once (registers)
   constexpr int OPT = (REP * HD + 32 * MW - 1) / (32 * MW);  // outputs per thread
