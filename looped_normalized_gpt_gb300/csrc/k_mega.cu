@@ -4,7 +4,7 @@
 //
 // One block per SM, launched cooperatively so that every block is resident. Warp 0 is the
 // producer: it walks this block's share of every weight matrix (a contiguous range of rows)
-// in stage order, asks L2 for the bytes about PREFETCH_AHEAD ahead (cp.async.bulk.prefetch),
+// in stage order, optionally asks L2 for the bytes some distance ahead (cp.async.bulk.prefetch),
 // and copies chunks into a ring of shared-memory slots with cp.async.bulk, completion on one
 // mbarrier per slot. It never waits for activations, so HBM keeps streaming the next stages'
 // weights while the consumers wait at a grid barrier or run attention. Warps 1..8 are the
@@ -49,7 +49,6 @@ constexpr uint32_t WORK = 32 * 1024;              // input row, or attention til
 constexpr int AK = MEGA_AK;                       // positions per attention item
 constexpr uint32_t SPIN_LIMIT = 1u << 22;         // polls of a global counter
 constexpr int ERR_MEGA = 6;                       // dev_err: a wait of the persistent kernel ran out
-constexpr long PREFETCH_AHEAD = 448 * 1024;       // L2 lead of the producer, bytes per block
 static_assert(sizeof(MegaStage) % 4 == 0 && sizeof(MegaStage) / 4 < 32 * MW, "stage copy by the team");
 
 struct Ctl {
@@ -154,7 +153,7 @@ __device__ void produce(const MegaArgs &a, uint8_t *ring, uint64_t *full, uint64
   int marked = -1;
   bool ok = true;
   while (cp.ok) {
-    while (pf.ok && ahead < PREFETCH_AHEAD) {
+    while (pf.ok && ahead < a.prefetch_ahead) {
       const uint32_t pb = (uint32_t)pf.rows() * pf.K * 2;
       prefetch_l2_bulk(pf.W + (size_t)pf.r0 * pf.K, pb);
       if (pf.pair > 0) prefetch_l2_bulk(pf.W + (size_t)(pf.r0 + pf.pair) * pf.K, pb);
@@ -197,7 +196,7 @@ __device__ void produce(const MegaArgs &a, uint8_t *ring, uint64_t *full, uint64
 template <int SEG, bool DUAL>
 __device__ void gemv_chunks(const WarpTeam &tm, const MegaStage &st, int rb, int re, int c0, const uint8_t *ring,
                             uint64_t *full, uint64_t *empty, const float *xs, float (*red)[MW][2 * RMAX], Ctl &ctl,
-                            int *err) {
+                            int *err, const Tracer &tr, int s) {
   const int t = tm.tid(), lane = threadIdx.x & 31, cw = tm.warp();
   const int K = st.K, R = st.R, mode = st.ep.mode, nu = K / 8;  // 16-byte columns per row
   float *__restrict__ Y = st.Y;
@@ -220,6 +219,7 @@ __device__ void gemv_chunks(const WarpTeam &tm, const MegaStage &st, int rb, int
     const int c = c0 + i, sl = c % NS;  // chunk indices run over the whole step
     const bool landed = mbar_wait(smem_addr(&full[sl]), (c / NS) & 1, &ctl.abort);
     if (!landed) flag_error(ctl, err);  // the block stops at the stage's end; the slot stays taken
+    if (i == 0) tr.mark(s, 7);
     const int r0 = rb + i * R, nr = min(R, re - r0);
     const uint4 *w = reinterpret_cast<const uint4 *>(ring + (size_t)sl * SLOT);
     float acc[RMAX], acc2[RMAX];
@@ -308,8 +308,8 @@ __device__ bool gemv_stage(const WarpTeam &tm, const MegaArgs &a, const MegaStag
   const int seg = (K / 8 + 32 * MW - 1) / (32 * MW);
   const bool dual = st.pair > 0;
 #define MEGA_CHUNKS(S)                                                                     \
-  if (dual) gemv_chunks<S, true>(tm, st, rb, re, c, ring, full, empty, xs, red, ctl, a.err); \
-  else gemv_chunks<S, false>(tm, st, rb, re, c, ring, full, empty, xs, red, ctl, a.err);
+  if (dual) gemv_chunks<S, true>(tm, st, rb, re, c, ring, full, empty, xs, red, ctl, a.err, tr, s); \
+  else gemv_chunks<S, false>(tm, st, rb, re, c, ring, full, empty, xs, red, ctl, a.err, tr, s);
   if (seg <= 1) {
     MEGA_CHUNKS(1)
   } else if (seg <= 2) {

@@ -218,11 +218,13 @@ struct MegaArgs {
   int32_t *seq_pos;         // advanced by `adv` at the last stage
   int adv_seq, adv_cnt;
   unsigned long long *trace;  // null, or [nstages][grid][MEGA_TRACE_EVENTS] %globaltimer stamps
+  int prefetch_ahead;         // bytes per block the producer asks L2 for ahead of its copies
 };
 
 // Stamps per (stage, block) of the persistent kernel's optional trace: 0 stage entered,
 // 1 grid barrier passed, 2 input row built, 3 chunks or attention items done, 4 stage done;
-// from the producer warp: 5 first chunk of the stage issued, 6 last chunk issued.
+// from the producer warp: 5 first chunk of the stage issued, 6 last chunk issued; 7 the
+// stage's first chunk has landed (consumers).
 constexpr int MEGA_TRACE_EVENTS = 8;
 
 // Bytes of dynamic shared memory and whether the device runs the kernel (one block per SM,
