@@ -1196,6 +1196,8 @@ int dory_create(const dory_config *cfg, const dory_weights *w, void *stream, dor
     // the merge's per-warp partials of a kv head's query heads
     if ((size_t)mega_consumer_warps() * rep * (dm.hd + 2) > mega_work_floats()) ok = false;
     if (dm.hidden > 6144 || dm.ffn > 6144 || q_size > 6144) ok = false;  // three 16-byte columns per thread
+    const int nmax = std::max(std::max(dm.vocab, dm.ffn), 2 * q_size + 2 * kv_size);
+    if (d->sms > 0 && (nmax + d->sms - 1) / d->sms > mega_max_rows_per_block()) ok = false;
     for (const OrdInfo &o : d->ords) {
       const long keys = o.window == INT_MAX ? (long)o.cap : std::min<long>(o.window, o.cap);
       const long maxblk = keys / MEGA_AK + 2;

@@ -45,6 +45,7 @@ constexpr int MTHREADS = 32 * (MW + 1);           // and the producer warp
 constexpr int NS = 7;                             // weight slots
 constexpr uint32_t SLOT = 26 * 1024;              // bytes per slot
 constexpr int RMAX = 8;                           // rows (or row pairs) per chunk at most
+constexpr int EPI_ROWS = 256;                     // a block's rows of one GEMV at most
 constexpr uint32_t WORK = 32 * 1024;              // input row, or attention tiles and merge scratch
 constexpr int AK = MEGA_AK;                       // positions per attention item
 constexpr uint32_t SPIN_LIMIT = 1u << 22;         // polls of a global counter
@@ -195,13 +196,11 @@ __device__ void produce(const MegaArgs &a, uint8_t *ring, uint64_t *full, uint64
 // of it. `st` is the stage's copy in shared memory.
 template <int SEG, bool DUAL>
 __device__ void gemv_chunks(const WarpTeam &tm, const MegaStage &st, int rb, int re, int c0, const uint8_t *ring,
-                            uint64_t *full, uint64_t *empty, const float *xs, float (*red)[MW][2 * RMAX], Ctl &ctl,
-                            int *err, const Tracer &tr, int s) {
+                            uint64_t *full, uint64_t *empty, const float *xs, float (*red)[MW][2 * RMAX],
+                            const float (*epi)[EPI_ROWS], Ctl &ctl, int *err, const Tracer &tr, int s) {
   const int t = tm.tid(), lane = threadIdx.x & 31, cw = tm.warp();
   const int K = st.K, R = st.R, mode = st.ep.mode, nu = K / 8;  // 16-byte columns per row
   float *__restrict__ Y = st.Y;
-  const float *__restrict__ v1 = st.ep.vec;
-  const float *__restrict__ v2 = st.ep.vec2;
   float xr[8 * SEG];
 #pragma unroll
   for (int g = 0; g < SEG; g++) {
@@ -274,10 +273,10 @@ __device__ void gemv_chunks(const WarpTeam &tm, const MegaStage &st, int rb, int
       const int n = r0 + t;
       float y;
       if (mode == EPI_SCALE) {
-        y = g * __ldg(v1 + n);
+        y = g * epi[0][n - rb];
       } else if (mode == EPI_SILU) {
-        const float gs = g * __ldg(v1 + n);
-        y = gs * sigmoidf_(gs) * (u * __ldg(v2 + n));
+        const float gs = g * epi[0][n - rb];
+        y = gs * sigmoidf_(gs) * (u * epi[1][n - rb]);
       } else {
         y = g;
       }
@@ -292,13 +291,19 @@ __device__ __forceinline__ void input_row(const WarpTeam &tm, const GemvIn &in, 
 }
 
 // Returns false (team-uniformly) when the block has stopped.
-__device__ bool gemv_stage(const WarpTeam &tm, const MegaArgs &a, const MegaStage &st, int s, int &c,
+__device__ __noinline__ bool gemv_stage(const WarpTeam &tm, const MegaArgs &a, const MegaStage &st, int s, int &c,
                            const uint8_t *ring, uint64_t *full, uint64_t *empty, float *xs,
-                           float (*red)[MW][2 * RMAX], Ctl &ctl) {
+                           float (*red)[MW][2 * RMAX], float (*epi)[EPI_ROWS], Ctl &ctl) {
   const Tracer tr{tm.tid() == 0 ? a.trace : nullptr};
   const int G = gridDim.x, b = blockIdx.x;
   const int N = st.N, K = st.K;
   const int rb = (int)((long)N * b / G), re = (int)((long)N * (b + 1) / G);
+  // the epilogue's per-row scales of this block's rows, in flight with the input loads
+  if (st.ep.mode != EPI_STORE)
+    for (int i = tm.tid(); i < re - rb; i += tm.size()) {
+      epi[0][i] = __ldg(st.ep.vec + rb + i);
+      if (st.ep.mode == EPI_SILU) epi[1][i] = __ldg(st.ep.vec2 + rb + i);
+    }
   const int kc = (K / 4 + tm.size() - 1) / tm.size();  // float4 chunks per thread
   if (kc <= 2) input_row<2>(tm, st.in, K, xs);
   else if (kc <= 4) input_row<4>(tm, st.in, K, xs);
@@ -308,8 +313,8 @@ __device__ bool gemv_stage(const WarpTeam &tm, const MegaArgs &a, const MegaStag
   const int seg = (K / 8 + 32 * MW - 1) / (32 * MW);
   const bool dual = st.pair > 0;
 #define MEGA_CHUNKS(S)                                                                     \
-  if (dual) gemv_chunks<S, true>(tm, st, rb, re, c, ring, full, empty, xs, red, ctl, a.err, tr, s); \
-  else gemv_chunks<S, false>(tm, st, rb, re, c, ring, full, empty, xs, red, ctl, a.err, tr, s);
+  if (dual) gemv_chunks<S, true>(tm, st, rb, re, c, ring, full, empty, xs, red, epi, ctl, a.err, tr, s); \
+  else gemv_chunks<S, false>(tm, st, rb, re, c, ring, full, empty, xs, red, epi, ctl, a.err, tr, s);
   if (seg <= 1) {
     MEGA_CHUNKS(1)
   } else if (seg <= 2) {
@@ -414,8 +419,10 @@ __device__ __noinline__ void merge_items(const WarpTeam &tm, const MegaStage &st
   }
 }
 
+// (stages are not inlined: each gets its own register allocation, so the chunk loop does
+// not spill)
 template <int HD>
-__device__ bool attn_stage(const WarpTeam &tm, const MegaArgs &a, const MegaStage &st, float *work, uint64_t *abar,
+__device__ __noinline__ bool attn_stage(const WarpTeam &tm, const MegaArgs &a, const MegaStage &st, float *work, uint64_t *abar,
                            int &aph, float (*qs)[HD], float (*rope_s)[HD], Ctl &ctl) {
   constexpr int NV = HD / 32, NC = HD / 4, HALF = HD / 2, PP = HALF / 32;  // pairs per lane
   const Dims &d = a.d;
@@ -599,6 +606,7 @@ __global__ void __launch_bounds__(MTHREADS, 1) mega_decode_kernel(const __grid_c
   __shared__ __align__(16) float rope_s[2][HD];
   __shared__ __align__(16) MegaStage sst;
   __shared__ float red[2][MW][2 * RMAX];
+  __shared__ float epi[2][EPI_ROWS];
   __shared__ Ctl ctl;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -652,7 +660,7 @@ __global__ void __launch_bounds__(MTHREADS, 1) mega_decode_kernel(const __grid_c
     // every reader of the position has passed: the last stage advances it
     if (s == a.nstages - 1 && b == 0 && tm.tid() == 0) a.seq_pos[a.adv_seq] += a.adv_cnt;
     if (sst.kind == MK_GEMV) {
-      ok = gemv_stage(tm, a, sst, s, c, ring, full, empty, work, red, ctl);
+      ok = gemv_stage(tm, a, sst, s, c, ring, full, empty, work, red, epi, ctl);
     } else {
       if (!rope_ready) {
         if (!team_wait_counter(tm, a.sync + 1, HD, ctl, a.err)) {
@@ -682,6 +690,8 @@ int mega_chunk_rows(int K, bool dual) {  // 0: a row does not fit a slot
 }
 
 int mega_consumer_warps() { return MW; }
+
+int mega_max_rows_per_block() { return EPI_ROWS; }
 
 size_t mega_work_floats() { return WORK / 4; }
 
