@@ -69,6 +69,10 @@ struct Tracer {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     p[((size_t)stage * gridDim.x + blockIdx.x) * MEGA_TRACE_EVENTS + event] = t;
   }
+  __device__ __forceinline__ void put(int stage, int event, unsigned long long v) const {
+    if (p) p[((size_t)stage * gridDim.x + blockIdx.x) * MEGA_TRACE_EVENTS + event] = v;
+  }
+  __device__ __forceinline__ long long clk() const { return p ? clock64() : 0; }
 };
 
 __device__ __forceinline__ void flag_error(Ctl &ctl, int *err) {
@@ -188,6 +192,42 @@ __device__ void produce(const MegaArgs &a, uint8_t *ring, uint64_t *full, uint64
 
 // ---- GEMV stage ---------------------------------------------------------------------------
 
+// Sums of v[0..2N) over the warp, all at once: a butterfly that halves the vector at each of
+// the first log2(2N) steps (exchanging the half a lane does not keep), then sums over the
+// remaining lanes. Afterwards lane l holds the total of element slot_of(l), where slot_of
+// reads the lane bits 4, 3, ... from the most significant element bit down; the lanes of
+// one element agree. Depth 5 shuffles whatever N is, 2N - 1 + (5 - log2 2N) of them.
+template <int N2>
+__device__ __forceinline__ float warp_sum_many(float (&v)[N2], int lane) {
+  static_assert(N2 == 8 || N2 == 16, "8 or 16 sums");
+  constexpr int LOG = N2 == 8 ? 3 : 4;
+#pragma unroll
+  for (int step = 0; step < LOG; step++) {
+    const int half = N2 >> (step + 1);
+    const int bit = 16 >> step;  // lanes 16, 8, 4, 2 apart
+    const bool upper = lane & bit;
+#pragma unroll
+    for (int j = 0; j < half; j++) {
+      const float send = upper ? v[j] : v[j + half];
+      const float keep = upper ? v[j + half] : v[j];
+      v[j] = keep + __shfl_xor_sync(0xffffffffu, send, bit);
+    }
+  }
+#pragma unroll
+  for (int bit = 16 >> LOG; bit > 0; bit >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], bit);
+  return v[0];
+}
+
+// The element whose total lane l holds after warp_sum_many<N2>.
+template <int N2>
+__device__ __forceinline__ int sum_slot(int lane) {
+  constexpr int LOG = N2 == 8 ? 3 : 4;
+  int e = 0;
+#pragma unroll
+  for (int step = 0; step < LOG; step++) e |= ((lane >> (4 - step)) & 1) << (LOG - 1 - step);
+  return e;
+}
+
 // A stage's chunks, each reduced by the whole team in order: thread t owns the 16-byte
 // columns t, t + 256, ... (SEG of them) of every row, keeps its input values for them in
 // registers, sums its columns of the chunk's rows (and of the up rows, DUAL), the warps
@@ -214,14 +254,18 @@ __device__ void gemv_chunks(const WarpTeam &tm, const MegaStage &st, int rb, int
     xr[8 * g + 4] = q.x; xr[8 * g + 5] = q.y; xr[8 * g + 6] = q.z; xr[8 * g + 7] = q.w;
   }
   const int nch = re > rb ? (re - rb + R - 1) / R : 0;
+  long long cyc[4] = {0, 0, 0, 0};  // trace only: wait, reduce, barrier, epilogue
   for (int i = 0; i < nch; i++) {
     const int c = c0 + i, sl = c % NS;  // chunk indices run over the whole step
+    long long t0 = tr.clk();
     const bool landed = mbar_wait(smem_addr(&full[sl]), (c / NS) & 1, &ctl.abort);
+    long long t1 = tr.clk();
+    cyc[0] += t1 - t0;
     if (!landed) flag_error(ctl, err);  // the block stops at the stage's end; the slot stays taken
     if (i == 0) tr.mark(s, 7);
     const int r0 = rb + i * R, nr = min(R, re - r0);
     const uint4 *w = reinterpret_cast<const uint4 *>(ring + (size_t)sl * SLOT);
-    float acc[RMAX], acc2[RMAX];
+    float acc[2 * RMAX];  // [0, RMAX): rows; [RMAX, 2 RMAX): up rows (DUAL)
 #pragma unroll
     for (int r = 0; r < RMAX; r++) {
       float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
@@ -249,20 +293,22 @@ __device__ void gemv_chunks(const WarpTeam &tm, const MegaStage &st, int rb, int
         }
       }
       acc[r] = a0 + a1;
-      acc2[r] = b0 + b1;
+      acc[RMAX + r] = b0 + b1;
     }
     float(*rb_)[2 * RMAX] = red[i & 1];
-#pragma unroll
-    for (int r = 0; r < RMAX; r++) {
-      if (r >= nr) break;
-      const float g = warp_sum(acc[r]);
-      const float u = DUAL ? warp_sum(acc2[r]) : 0.f;
-      if (lane == 0) {
-        rb_[cw][r] = g;
-        rb_[cw][RMAX + r] = u;
-      }
+    if (DUAL) {
+      const float v = warp_sum_many<2 * RMAX>(acc, lane);
+      if ((lane & 1) == 0) rb_[cw][sum_slot<2 * RMAX>(lane)] = v;
+    } else {
+      float (&a8)[RMAX] = *reinterpret_cast<float(*)[RMAX]>(acc);
+      const float v = warp_sum_many<RMAX>(a8, lane);
+      if ((lane & 3) == 0) rb_[cw][sum_slot<RMAX>(lane)] = v;
     }
+    t0 = tr.clk();
+    cyc[1] += t0 - t1;
     tm.sync();
+    t1 = tr.clk();
+    cyc[2] += t1 - t0;
     if (t == 0 && !ctl.abort) mbar_arrive(smem_addr(&empty[sl]));  // the partials are out of the slot
     if (t < nr) {
       float g = 0.f, u = 0.f;
@@ -282,7 +328,9 @@ __device__ void gemv_chunks(const WarpTeam &tm, const MegaStage &st, int rb, int
       }
       Y[n] = y;
     }
+    cyc[3] += tr.clk() - t1;
   }
+  for (int k = 0; k < 4; k++) tr.put(s, 8 + k, (unsigned long long)cyc[k]);
 }
 
 template <int KC>

@@ -224,8 +224,10 @@ struct MegaArgs {
 // Stamps per (stage, block) of the persistent kernel's optional trace: 0 stage entered,
 // 1 grid barrier passed, 2 input row built, 3 chunks or attention items done, 4 stage done;
 // from the producer warp: 5 first chunk of the stage issued, 6 last chunk issued; 7 the
-// stage's first chunk has landed (consumers).
-constexpr int MEGA_TRACE_EVENTS = 8;
+// stage's first chunk has landed (consumers); 8..11 SM cycles the first consumer thread
+// spent over the stage's chunks waiting for a slot, reducing, at the team barrier, and in
+// the epilogue.
+constexpr int MEGA_TRACE_EVENTS = 12;
 
 // Bytes of dynamic shared memory and whether the device runs the kernel (one block per SM,
 // cooperative launch).
