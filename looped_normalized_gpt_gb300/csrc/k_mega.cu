@@ -69,8 +69,12 @@ struct Tracer {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     p[((size_t)stage * gridDim.x + blockIdx.x) * MEGA_TRACE_EVENTS + event] = t;
   }
-  __device__ __forceinline__ void put(int stage, int event, unsigned long long v) const {
-    if (p) p[((size_t)stage * gridDim.x + blockIdx.x) * MEGA_TRACE_EVENTS + event] = v;
+  __device__ __forceinline__ void add(int stage, int event, long long v) const {
+    if (p) p[((size_t)stage * gridDim.x + blockIdx.x) * MEGA_TRACE_EVENTS + event] += (unsigned long long)v;
+  }
+  __device__ __forceinline__ void zero(int stage) const {
+    if (p)
+      for (int e = 8; e < MEGA_TRACE_EVENTS; e++) p[((size_t)stage * gridDim.x + blockIdx.x) * MEGA_TRACE_EVENTS + e] = 0;
   }
   __device__ __forceinline__ long long clk() const { return p ? clock64() : 0; }
 };
@@ -254,13 +258,13 @@ __device__ void gemv_chunks(const WarpTeam &tm, const MegaStage &st, int rb, int
     xr[8 * g + 4] = q.x; xr[8 * g + 5] = q.y; xr[8 * g + 6] = q.z; xr[8 * g + 7] = q.w;
   }
   const int nch = re > rb ? (re - rb + R - 1) / R : 0;
-  long long cyc[4] = {0, 0, 0, 0};  // trace only: wait, reduce, barrier, epilogue
+  tr.zero(s);
   for (int i = 0; i < nch; i++) {
     const int c = c0 + i, sl = c % NS;  // chunk indices run over the whole step
     long long t0 = tr.clk();
     const bool landed = mbar_wait(smem_addr(&full[sl]), (c / NS) & 1, &ctl.abort);
     long long t1 = tr.clk();
-    cyc[0] += t1 - t0;
+    tr.add(s, 8, t1 - t0);
     if (!landed) flag_error(ctl, err);  // the block stops at the stage's end; the slot stays taken
     if (i == 0) tr.mark(s, 7);
     const int r0 = rb + i * R, nr = min(R, re - r0);
@@ -305,10 +309,10 @@ __device__ void gemv_chunks(const WarpTeam &tm, const MegaStage &st, int rb, int
       if ((lane & 3) == 0) rb_[cw][sum_slot<RMAX>(lane)] = v;
     }
     t0 = tr.clk();
-    cyc[1] += t0 - t1;
+    tr.add(s, 9, t0 - t1);
     tm.sync();
     t1 = tr.clk();
-    cyc[2] += t1 - t0;
+    tr.add(s, 10, t1 - t0);
     if (t == 0 && !ctl.abort) mbar_arrive(smem_addr(&empty[sl]));  // the partials are out of the slot
     if (t < nr) {
       float g = 0.f, u = 0.f;
@@ -328,9 +332,8 @@ __device__ void gemv_chunks(const WarpTeam &tm, const MegaStage &st, int rb, int
       }
       Y[n] = y;
     }
-    cyc[3] += tr.clk() - t1;
+    tr.add(s, 11, tr.clk() - t1);
   }
-  for (int k = 0; k < 4; k++) tr.put(s, 8 + k, (unsigned long long)cyc[k]);
 }
 
 template <int KC>
@@ -386,7 +389,7 @@ __device__ __noinline__ bool gemv_stage(const WarpTeam &tm, const MegaArgs &a, c
 template <int HD, int REP>
 __device__ __noinline__ void merge_items(const WarpTeam &tm, const MegaStage &st, const Dims &d, int kh, int nblk, float *scr) {
   constexpr int NV = HD / 32;
-  constexpr int B = REP <= 2 ? 2 : 1;  // partial sets a warp loads at once (registers)
+  constexpr int B = REP <= 4 ? 3 : 2;  // partial sets a warp loads at once (one round trip for 8 B sets)
   constexpr int OPT = (REP * HD + 32 * MW - 1) / (32 * MW);  // outputs per thread
   const int cw = tm.warp(), lane = threadIdx.x & 31;
   const float *pr = st.part + (size_t)kh * st.maxblk * REP * (HD + 2);
@@ -467,12 +470,63 @@ __device__ __noinline__ void merge_items(const WarpTeam &tm, const MegaStage &st
   }
 }
 
+// Warp-wide: query head h of kv head kh against the item's 32 keys (lane = key): scores,
+// the item's softmax statistics and its value sum, written as the item's partial.
+template <int HD>
+__device__ __noinline__ void attn_head(const MegaStage &st, const float *Ks, const float *Vs, const float *q, int tg,
+                                       long P0, long lo, long p, int kh, int blk, int rep, int h) {
+  constexpr int NV = HD / 32, NC = HD / 4;
+  const int lane = threadIdx.x & 31;
+  const float scale = 1.f / sqrtf((float)HD);
+  const int j = lane;
+  const long pe = P0 + j;
+  const bool valid = pe >= lo && pe <= p && (tg == (int32_t)pe || pe == p);
+  float s0 = 0.f, s1 = 0.f;
+  if (valid) {
+    const float4 *kr = reinterpret_cast<const float4 *>(Ks + j * HD);
+    const float4 *q4 = reinterpret_cast<const float4 *>(q);
+#pragma unroll 8
+    for (int c = 0; c < NC; c++) {
+      const int cc = (c + j) & (NC - 1);  // rotated: the 32 lanes spread over all banks
+      const float4 k = kr[cc], qq = q4[cc];
+      s0 = fmaf(qq.x, k.x, fmaf(qq.y, k.y, s0));
+      s1 = fmaf(qq.z, k.z, fmaf(qq.w, k.w, s1));
+    }
+  }
+  const float s = valid ? (s0 + s1) * scale : -INFINITY;
+  const float m = warp_max(s);
+  const float e = m == -INFINITY ? 0.f : expf(s - m);
+  const float l = warp_sum(e);
+  float acc[NV], acc_b[NV];  // two chains: even and odd keys
+#pragma unroll
+  for (int i = 0; i < NV; i++) acc[i] = acc_b[i] = 0.f;
+#pragma unroll 4
+  for (int jj = 0; jj < AK; jj += 2) {
+    const float w0 = __shfl_sync(0xffffffffu, e, jj), w1 = __shfl_sync(0xffffffffu, e, jj + 1);
+    const float *v0 = Vs + jj * HD + lane * NV, *v1 = v0 + HD;
+#pragma unroll
+    for (int i = 0; i < NV; i++) {
+      acc[i] = fmaf(w0, v0[i], acc[i]);
+      acc_b[i] = fmaf(w1, v1[i], acc_b[i]);
+    }
+  }
+  float *out = st.part + (((size_t)kh * st.maxblk + blk) * rep + h) * (HD + 2);
+#pragma unroll
+  for (int i = 0; i < NV; i++) out[lane * NV + i] = acc[i] + acc_b[i];
+  if (lane == 0) {
+    out[HD] = m;
+    out[HD + 1] = l;
+  }
+}
+
 // (stages are not inlined: each gets its own register allocation, so the chunk loop does
 // not spill)
 template <int HD>
-__device__ __noinline__ bool attn_stage(const WarpTeam &tm, const MegaArgs &a, const MegaStage &st, float *work, uint64_t *abar,
-                           int &aph, float (*qs)[HD], float (*rope_s)[HD], Ctl &ctl) {
-  constexpr int NV = HD / 32, NC = HD / 4, HALF = HD / 2, PP = HALF / 32;  // pairs per lane
+__device__ __noinline__ bool attn_stage(const WarpTeam &tm, const MegaArgs &a, const MegaStage &st, int s, float *work,
+                                        uint64_t *abar, int &aph, float (*qs)[HD], float (*rope_s)[HD], Ctl &ctl) {
+  const Tracer tr{tm.tid() == 0 ? a.trace : nullptr};
+  tr.zero(s);  // trace only: copy wait, compute, arrival, merge cycles
+  constexpr int HALF = HD / 2, PP = HALF / 32;  // pairs per lane
   const Dims &d = a.d;
   const int rep = d.nh / d.nk;
   const int cap = st.ring.cap, window = st.ring.window;
@@ -490,7 +544,6 @@ __device__ __noinline__ bool attn_stage(const WarpTeam &tm, const MegaArgs &a, c
   const int cw = tm.warp(), lane = threadIdx.x & 31;
   const int kw = rep % MW;  // the warp that prepares the new key and value
   const float *rc = rope_s[st.rope_kind], *rsn = rope_s[st.rope_kind] + HALF;
-  const float scale = 1.f / sqrtf((float)HD);
   for (int it = blockIdx.x; it < items; it += gridDim.x) {
     const int kh = it / nblk, blk = it % nblk;
     const long P0 = (blk0 + blk) * AK;
@@ -551,9 +604,12 @@ __device__ __noinline__ bool attn_stage(const WarpTeam &tm, const MegaArgs &a, c
         ky[u] *= inv;
       }
     }
+    long long t0 = tr.clk();
     const bool landed = mbar_wait(smem_addr(abar), (aph - 1) & 1, &ctl.abort);
     if (!landed && lane == 0) flag_error(ctl, a.err);
     if (!team_ok(tm, ctl)) return false;
+    long long t1 = tr.clk();
+    tr.add(s, 8, t1 - t0);
     if (has_p && cw == kw) {
       // into the tile (it holds the ring's older row there), and into the ring
       const int jp = (int)(p - P0), rr = (int)(p % cap);
@@ -574,53 +630,19 @@ __device__ __noinline__ bool attn_stage(const WarpTeam &tm, const MegaArgs &a, c
       fence_proxy_async_global();  // later passes read this row with bulk copies
     }
     tm.sync();
-    for (int h = cw; h < rep; h += MW) {
-      // warp cw: query head kh * rep + h; lane j: key P0 + j
-      const int j = lane;
-      const long pe = P0 + j;
-      const bool valid = pe >= lo && pe <= p && (tg == (int32_t)pe || pe == p);
-      float s0 = 0.f, s1 = 0.f;
-      if (valid) {
-        const float4 *kr = reinterpret_cast<const float4 *>(Ks + j * HD);
-        const float4 *q4 = reinterpret_cast<const float4 *>(qs[h]);
-#pragma unroll 8
-        for (int c = 0; c < NC; c++) {
-          const int cc = (c + j) & (NC - 1);  // rotated: the 32 lanes spread over all banks
-          const float4 k = kr[cc], q = q4[cc];
-          s0 = fmaf(q.x, k.x, fmaf(q.y, k.y, s0));
-          s1 = fmaf(q.z, k.z, fmaf(q.w, k.w, s1));
-        }
-      }
-      const float s = valid ? (s0 + s1) * scale : -INFINITY;
-      const float m = warp_max(s);
-      const float e = m == -INFINITY ? 0.f : expf(s - m);
-      const float l = warp_sum(e);
-      float acc[NV];
-#pragma unroll
-      for (int i = 0; i < NV; i++) acc[i] = 0.f;
-      for (int jj = 0; jj < AK; jj++) {
-        const float wj = __shfl_sync(0xffffffffu, e, jj);
-        if (wj == 0.f) continue;
-        const float *v = Vs + jj * HD + lane * NV;
-#pragma unroll
-        for (int i = 0; i < NV; i++) acc[i] = fmaf(wj, v[i], acc[i]);
-      }
-      float *out = st.part + (((size_t)kh * st.maxblk + blk) * rep + h) * (HD + 2);
-#pragma unroll
-      for (int i = 0; i < NV; i++) out[lane * NV + i] = acc[i];
-      if (lane == 0) {
-        out[HD] = m;
-        out[HD + 1] = l;
-      }
-    }
+    for (int h = cw; h < rep; h += MW) attn_head<HD>(st, Ks, Vs, qs[h], tg, P0, lo, p, kh, blk, rep, h);
     // the last item of this kv head merges the items and gates
     tm.sync();
+    t0 = tr.clk();
+    tr.add(s, 9, t0 - t1);
     if (tm.tid() == 0) {
       const int old = atom_add_acq_rel_gpu(a.actr + kh, 1);
       ctl.last = old == nblk - 1;
       if (ctl.last) a.actr[kh] = 0;
     }
     tm.sync();
+    t1 = tr.clk();
+    tr.add(s, 10, t1 - t0);
     if (ctl.last) {
       switch (rep) {
         case 1: merge_items<HD, 1>(tm, st, d, kh, nblk, Ks); break;
@@ -628,6 +650,7 @@ __device__ __noinline__ bool attn_stage(const WarpTeam &tm, const MegaArgs &a, c
         case 4: merge_items<HD, 4>(tm, st, d, kh, nblk, Ks); break;
         default: merge_items<HD, 8>(tm, st, d, kh, nblk, Ks); break;
       }
+      tr.add(s, 11, tr.clk() - t1);
     }
   }
   return true;
@@ -719,7 +742,7 @@ __global__ void __launch_bounds__(MTHREADS, 1) mega_decode_kernel(const __grid_c
         tm.sync();
         rope_ready = true;
       }
-      ok = attn_stage<HD>(tm, a, sst, work, &abar, aph, qs, rope_s, ctl);
+      ok = attn_stage<HD>(tm, a, sst, s, work, &abar, aph, qs, rope_s, ctl);
     }
     tr.mark(s, 4);
     if (ok && s + 1 < a.nstages) grid_arrive(tm, a.sync);
