@@ -60,6 +60,9 @@ struct Ctl {
   long long p;
 };
 
+// Cycle counts of the current stage's phases (trace only; the team's first thread).
+__shared__ unsigned long long trace_acc[4];
+
 // Optional per-stage timestamps (off when the pointer is null).
 struct Tracer {
   unsigned long long *p;
@@ -69,12 +72,16 @@ struct Tracer {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     p[((size_t)stage * gridDim.x + blockIdx.x) * MEGA_TRACE_EVENTS + event] = t;
   }
-  __device__ __forceinline__ void add(int stage, int event, long long v) const {
-    if (p) p[((size_t)stage * gridDim.x + blockIdx.x) * MEGA_TRACE_EVENTS + event] += (unsigned long long)v;
+  __device__ __forceinline__ void add(int, int event, long long v) const {
+    if (p) trace_acc[event - 8] += (unsigned long long)v;
   }
-  __device__ __forceinline__ void zero(int stage) const {
+  __device__ __forceinline__ void zero(int) const {
     if (p)
-      for (int e = 8; e < MEGA_TRACE_EVENTS; e++) p[((size_t)stage * gridDim.x + blockIdx.x) * MEGA_TRACE_EVENTS + e] = 0;
+      for (int e = 0; e < 4; e++) trace_acc[e] = 0;
+  }
+  __device__ __forceinline__ void flush(int stage) const {
+    if (p)
+      for (int e = 0; e < 4; e++) p[((size_t)stage * gridDim.x + blockIdx.x) * MEGA_TRACE_EVENTS + 8 + e] = trace_acc[e];
   }
   __device__ __forceinline__ long long clk() const { return p ? clock64() : 0; }
 };
@@ -334,6 +341,7 @@ __device__ void gemv_chunks(const WarpTeam &tm, const MegaStage &st, int rb, int
     }
     tr.add(s, 11, tr.clk() - t1);
   }
+  tr.flush(s);
 }
 
 template <int KC>
@@ -382,99 +390,99 @@ __device__ __noinline__ bool gemv_stage(const WarpTeam &tm, const MegaArgs &a, c
 
 // ---- attention stage ----------------------------------------------------------------------
 
-// Merge the items of kv head kh and gate: warp w loads the partials of items w, w + MW, ...
-// all at once (B per round) and folds them into a running (max, sum, output) per head; the
-// warps' results meet in shared memory (`scr`) and each thread finishes its outputs.
-// (not inlined: its own register allocation keeps the main loop from spilling)
-template <int HD, int REP>
-__device__ __noinline__ void merge_items(const WarpTeam &tm, const MegaStage &st, const Dims &d, int kh, int nblk, float *scr) {
-  constexpr int NV = HD / 32;
-  constexpr int B = REP <= 4 ? 3 : 2;  // partial sets a warp loads at once (one round trip for 8 B sets)
-  constexpr int OPT = (REP * HD + 32 * MW - 1) / (32 * MW);  // outputs per thread
-  const int cw = tm.warp(), lane = threadIdx.x & 31;
-  const float *pr = st.part + (size_t)kh * st.maxblk * REP * (HD + 2);
-  const size_t col0 = (size_t)kh * REP * HD;
-  const float *graw = st.qkvg + (size_t)(d.nh + 2 * d.nk) * HD + col0;
-  float gv[OPT];
+// Item partials of an attention stage: outputs o [nk][maxblk][rep][hd] (unnormalised),
+// then (max, sum) pairs [nk][maxblk][rep][2].
+__device__ __forceinline__ float *part_o(const MegaStage &st, int rep, int hd, int kh, int blk, int h) {
+  return st.part + (((size_t)kh * st.maxblk + blk) * rep + h) * hd;
+}
+__device__ __forceinline__ float *part_ml(const MegaStage &st, int nk, int rep, int hd, int kh, int blk, int h) {
+  return st.part + (size_t)nk * st.maxblk * rep * hd + (((size_t)kh * st.maxblk + blk) * rep + h) * 2;
+}
+
+// Merge the items of kv head kh and gate. Thread t takes the 4 outputs q = t mod nq of the
+// group's rep*hd and the items g, g + G, ... (g = t / nq, G = team size / nq groups), loads
+// all of their partials at once (IB per round), folds them with a running max; the groups
+// meet in shared memory `scr` and the first nq threads finish: y = sum o e^(m - M) / sum l
+// e^(m - M), z = y * sigmoid(g * s_g^2).
+template <int HD>
+__device__ __noinline__ void merge_items(const WarpTeam &tm, const MegaStage &st, const Dims &d, int kh, int nblk,
+                                         float *scr) {
+  constexpr int IB = 9;  // items a thread loads per round
+  const int rep = d.nh / d.nk, nq = rep * HD / 4;
+  const int groups = tm.size() / nq;
+  const size_t col0 = (size_t)kh * rep * HD;
+  float4 *Acc = reinterpret_cast<float4 *>(scr);  // [groups][nq]
+  float *Ms = scr + 4 * groups * nq, *Ls = Ms + groups * nq;
+  {  // nq = rep * hd / 4 <= 256 <= team size (rep <= 8, hd <= 128)
+    const int t = tm.tid();
+    const int q = t % nq, g = t / nq;
+    const bool act = g < groups;
+    const int h = act ? (q * 4) / HD : 0, dim = act ? (q * 4) % HD : 0;
+    float M = -INFINITY, L = 0.f;
+    float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i0 = g; act && i0 < nblk; i0 += IB * groups) {
+      float4 o[IB];
+      float2 ml[IB];
 #pragma unroll
-  for (int u = 0; u < OPT; u++) {
-    const int i = tm.tid() + u * tm.size();
-    gv[u] = i < REP * HD ? __ldcg(graw + i) : 0.f;
-  }
-  float M[REP], L[REP], acc[REP][NV];
+      for (int u = 0; u < IB; u++) {
+        const int it = i0 + u * groups;
+        const bool in = it < nblk;
+        o[u] = in ? __ldcg(reinterpret_cast<const float4 *>(part_o(st, rep, HD, kh, it, h) + dim))
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
+        ml[u] = in ? __ldcg(reinterpret_cast<const float2 *>(part_ml(st, d.nk, rep, HD, kh, it, h)))
+                   : make_float2(-INFINITY, 0.f);
+      }
 #pragma unroll
-  for (int h = 0; h < REP; h++) {
-    M[h] = -INFINITY;
-    L[h] = 0.f;
-#pragma unroll
-    for (int i = 0; i < NV; i++) acc[h][i] = 0.f;
-  }
-  for (int s0 = cw; s0 < nblk; s0 += B * MW) {
-    float m[B][REP], l[B][REP], o[B][REP][NV];
-#pragma unroll
-    for (int bb = 0; bb < B; bb++) {
-      const int sp = s0 + bb * MW;
-#pragma unroll
-      for (int h = 0; h < REP; h++) {
-        const float *base = pr + ((size_t)sp * REP + h) * (HD + 2);
-        const bool in = sp < nblk;
-        m[bb][h] = in ? __ldcg(base + HD) : -INFINITY;
-        l[bb][h] = in ? __ldcg(base + HD + 1) : 0.f;
-#pragma unroll
-        for (int i = 0; i < NV; i++) o[bb][h][i] = in ? __ldcg(base + lane * NV + i) : 0.f;
+      for (int u = 0; u < IB; u++) {
+        if (ml[u].x == -INFINITY) continue;
+        const float nm = fmaxf(M, ml[u].x);
+        const float sa = M == -INFINITY ? 0.f : expf(M - nm), sb = expf(ml[u].x - nm);
+        L = L * sa + ml[u].y * sb;
+        A = make_float4(A.x * sa + o[u].x * sb, A.y * sa + o[u].y * sb, A.z * sa + o[u].z * sb,
+                        A.w * sa + o[u].w * sb);
+        M = nm;
       }
     }
-#pragma unroll
-    for (int bb = 0; bb < B; bb++)
-#pragma unroll
-      for (int h = 0; h < REP; h++) {
-        const float mb = m[bb][h];
-        if (mb == -INFINITY) continue;
-        const float nm = fmaxf(M[h], mb);
-        const float sa = M[h] == -INFINITY ? 0.f : expf(M[h] - nm), sb = expf(mb - nm);
-        L[h] = L[h] * sa + l[bb][h] * sb;
-#pragma unroll
-        for (int i = 0; i < NV; i++) acc[h][i] = acc[h][i] * sa + o[bb][h][i] * sb;
-        M[h] = nm;
-      }
-  }
-  float *Ms = scr, *Ls = scr + MW * REP, *As = scr + 2 * MW * REP;  // [MW][REP], [MW][REP], [MW][REP][HD]
-#pragma unroll
-  for (int h = 0; h < REP; h++) {
-    if (lane == 0) {
-      Ms[cw * REP + h] = M[h];
-      Ls[cw * REP + h] = L[h];
+    if (act) {
+      Acc[g * nq + q] = A;
+      Ms[g * nq + q] = M;
+      Ls[g * nq + q] = L;
     }
-#pragma unroll
-    for (int i = 0; i < NV; i++) As[((size_t)cw * REP + h) * HD + lane * NV + i] = acc[h][i];
-  }
-  tm.sync();
-#pragma unroll
-  for (int u = 0; u < OPT; u++) {
-    const int i = tm.tid() + u * tm.size();
-    if (i >= REP * HD) break;
-    const int h = i / HD, cc = i % HD;
-    float Mx = -INFINITY;
-    for (int w = 0; w < MW; w++) Mx = fmaxf(Mx, Ms[w * REP + h]);
-    float Lx = 0.f, Ax = 0.f;
-    if (Mx != -INFINITY)
-      for (int w = 0; w < MW; w++) {
-        const float mw = Ms[w * REP + h];
-        if (mw == -INFINITY) continue;
-        const float e = expf(mw - Mx);
-        Lx += Ls[w * REP + h] * e;
-        Ax += As[((size_t)w * REP + h) * HD + cc] * e;
-      }
-    const float y = Lx > 0.f ? Ax / Lx : 0.f;
-    st.z[col0 + i] = y * sigmoidf_(gv[u] * __ldg(st.sg + col0 + i));
+    tm.sync();
+    if (g == 0 && act) {
+      float Mx = -INFINITY;
+      for (int k = 0; k < groups; k++) Mx = fmaxf(Mx, Ms[k * nq + q]);
+      float Lx = 0.f;
+      float4 Ax = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (Mx != -INFINITY)
+        for (int k = 0; k < groups; k++) {
+          const float mk = Ms[k * nq + q];
+          if (mk == -INFINITY) continue;
+          const float e = expf(mk - Mx);
+          const float4 ak = Acc[k * nq + q];
+          Lx += Ls[k * nq + q] * e;
+          Ax = make_float4(Ax.x + ak.x * e, Ax.y + ak.y * e, Ax.z + ak.z * e, Ax.w + ak.w * e);
+        }
+      const float inv = Lx > 0.f ? 1.f / Lx : 0.f;
+      const size_t c = col0 + (size_t)q * 4;
+      const float4 gr = __ldcg(reinterpret_cast<const float4 *>(st.qkvg + (size_t)(d.nh + 2 * d.nk) * HD + c));
+      const float4 sg = __ldg(reinterpret_cast<const float4 *>(st.sg + c));
+      float4 z;
+      z.x = Ax.x * inv * sigmoidf_(gr.x * sg.x);
+      z.y = Ax.y * inv * sigmoidf_(gr.y * sg.y);
+      z.z = Ax.z * inv * sigmoidf_(gr.z * sg.z);
+      z.w = Ax.w * inv * sigmoidf_(gr.w * sg.w);
+      *reinterpret_cast<float4 *>(st.z + c) = z;
+    }
+    tm.sync();
   }
 }
 
 // Warp-wide: query head h of kv head kh against the item's 32 keys (lane = key): scores,
 // the item's softmax statistics and its value sum, written as the item's partial.
 template <int HD>
-__device__ __noinline__ void attn_head(const MegaStage &st, const float *Ks, const float *Vs, const float *q, int tg,
-                                       long P0, long lo, long p, int kh, int blk, int rep, int h) {
+__device__ __forceinline__ void attn_head(const MegaStage &st, int nk, const float *Ks, const float *Vs, const float *q,
+                                          int tg, long P0, long lo, long p, int kh, int blk, int rep, int h) {
   constexpr int NV = HD / 32, NC = HD / 4;
   const int lane = threadIdx.x & 31;
   const float scale = 1.f / sqrtf((float)HD);
@@ -510,13 +518,10 @@ __device__ __noinline__ void attn_head(const MegaStage &st, const float *Ks, con
       acc_b[i] = fmaf(w1, v1[i], acc_b[i]);
     }
   }
-  float *out = st.part + (((size_t)kh * st.maxblk + blk) * rep + h) * (HD + 2);
+  float *out = part_o(st, rep, HD, kh, blk, h);
 #pragma unroll
   for (int i = 0; i < NV; i++) out[lane * NV + i] = acc[i] + acc_b[i];
-  if (lane == 0) {
-    out[HD] = m;
-    out[HD + 1] = l;
-  }
+  if (lane == 0) *reinterpret_cast<float2 *>(part_ml(st, nk, rep, HD, kh, blk, h)) = make_float2(m, l);
 }
 
 // (stages are not inlined: each gets its own register allocation, so the chunk loop does
@@ -630,7 +635,7 @@ __device__ __noinline__ bool attn_stage(const WarpTeam &tm, const MegaArgs &a, c
       fence_proxy_async_global();  // later passes read this row with bulk copies
     }
     tm.sync();
-    for (int h = cw; h < rep; h += MW) attn_head<HD>(st, Ks, Vs, qs[h], tg, P0, lo, p, kh, blk, rep, h);
+    for (int h = cw; h < rep; h += MW) attn_head<HD>(st, d.nk, Ks, Vs, qs[h], tg, P0, lo, p, kh, blk, rep, h);
     // the last item of this kv head merges the items and gates
     tm.sync();
     t0 = tr.clk();
@@ -644,15 +649,11 @@ __device__ __noinline__ bool attn_stage(const WarpTeam &tm, const MegaArgs &a, c
     t1 = tr.clk();
     tr.add(s, 10, t1 - t0);
     if (ctl.last) {
-      switch (rep) {
-        case 1: merge_items<HD, 1>(tm, st, d, kh, nblk, Ks); break;
-        case 2: merge_items<HD, 2>(tm, st, d, kh, nblk, Ks); break;
-        case 4: merge_items<HD, 4>(tm, st, d, kh, nblk, Ks); break;
-        default: merge_items<HD, 8>(tm, st, d, kh, nblk, Ks); break;
-      }
+      merge_items<HD>(tm, st, d, kh, nblk, Ks);
       tr.add(s, 11, tr.clk() - t1);
     }
   }
+  tr.flush(s);
   return true;
 }
 
