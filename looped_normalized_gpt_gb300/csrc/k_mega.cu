@@ -161,6 +161,9 @@ struct ChunkWalk {
 
 __device__ void produce(const MegaArgs &a, uint8_t *ring, uint64_t *full, uint64_t *empty, Ctl &ctl) {
   const Tracer tr{a.trace};
+  // weights are read once per step: they go through L2 evict-first, so that the step's
+  // activations, partials and counters stay there
+  const uint64_t pol = l2_evict_first_policy();
   ChunkWalk cp, pf;  // copies, and the L2 prefetch ahead of them
   cp.seek(a, 0);
   pf.seek(a, 0);
@@ -188,8 +191,8 @@ __device__ void produce(const MegaArgs &a, uint8_t *ring, uint64_t *full, uint64
     const uint32_t bytes = (uint32_t)cp.rows() * cp.K * 2, bar = smem_addr(&full[sl]);
     const uint32_t dst = smem_addr(ring + (size_t)sl * SLOT);
     mbar_expect_tx(bar, cp.pair > 0 ? 2 * bytes : bytes);
-    bulk_g2s(dst, cp.W + (size_t)cp.r0 * cp.K, bytes, bar);
-    if (cp.pair > 0) bulk_g2s(dst + bytes, cp.W + (size_t)(cp.r0 + cp.pair) * cp.K, bytes, bar);
+    bulk_g2s_hint(dst, cp.W + (size_t)cp.r0 * cp.K, bytes, bar, pol);
+    if (cp.pair > 0) bulk_g2s_hint(dst + bytes, cp.W + (size_t)(cp.r0 + cp.pair) * cp.K, bytes, bar, pol);
     ahead -= cp.pair > 0 ? 2 * bytes : bytes;
     c++;
     const int s_before = cp.s;
