@@ -324,7 +324,9 @@ __device__ void gemv_chunks(const WarpTeam &tm, const MegaStage &st, int rb, int
     t1 = tr.clk();
     tr.add(s, 10, t1 - t0);
     if (t == 0 && !ctl.abort) mbar_arrive(smem_addr(&empty[sl]));  // the partials are out of the slot
-    if (t < nr) {
+    // the chunk's epilogue goes to warp i mod MW, so its latency overlaps the next chunks
+    if (cw == i % MW && lane < nr) {
+      const int t = lane;
       float g = 0.f, u = 0.f;
       for (int ww = 0; ww < MW; ww++) {
         g += rb_[ww][t];
@@ -423,6 +425,13 @@ __device__ __noinline__ void merge_items(const WarpTeam &tm, const MegaStage &st
     const int h = act ? (q * 4) / HD : 0, dim = act ? (q * 4) % HD : 0;
     float M = -INFINITY, L = 0.f;
     float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+    // the gate inputs of the thread's outputs, in flight with the partials
+    const size_t c = col0 + (size_t)q * 4;
+    float4 gr = make_float4(0.f, 0.f, 0.f, 0.f), sg = gr;
+    if (g == 0 && act) {
+      gr = __ldcg(reinterpret_cast<const float4 *>(st.qkvg + (size_t)(d.nh + 2 * d.nk) * HD + c));
+      sg = __ldg(reinterpret_cast<const float4 *>(st.sg + c));
+    }
     for (int i0 = g; act && i0 < nblk; i0 += IB * groups) {
       float4 o[IB];
       float2 ml[IB];
@@ -467,9 +476,6 @@ __device__ __noinline__ void merge_items(const WarpTeam &tm, const MegaStage &st
           Ax = make_float4(Ax.x + ak.x * e, Ax.y + ak.y * e, Ax.z + ak.z * e, Ax.w + ak.w * e);
         }
       const float inv = Lx > 0.f ? 1.f / Lx : 0.f;
-      const size_t c = col0 + (size_t)q * 4;
-      const float4 gr = __ldcg(reinterpret_cast<const float4 *>(st.qkvg + (size_t)(d.nh + 2 * d.nk) * HD + c));
-      const float4 sg = __ldg(reinterpret_cast<const float4 *>(st.sg + c));
       float4 z;
       z.x = Ax.x * inv * sigmoidf_(gr.x * sg.x);
       z.y = Ax.y * inv * sigmoidf_(gr.y * sg.y);
