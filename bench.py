@@ -96,14 +96,33 @@ def workload_config():
 
 
 def profile_case(args):
-    """A reduced case for ncu captures of the decode kernel: the 2B shape with one input,
-    one recurrent and one output pair and loops 1 (427 MB of weights per token, still
-    larger than L2, about 1 GB on the device). Prints one JSON line; not a bench line."""
+    """Small cases for ncu captures (each prints one JSON line; none is a bench line):
+    decode-3pass: batch-1 decode of the 2B shape cut to one input, one recurrent and one
+    output pair at loops 1 (427 MB of weights per token, still larger than L2, about 1 GB on
+    the device); prefill: 64-row chunks of a prompt of --prompt tokens on the 2B model;
+    batch64: the batch-64 decode line with 4 timed steps."""
     import torch
 
     from looped_normalized_gpt_gb300 import Dory, build
 
     build()
+    if args.profile_case == "batch64":
+        w = synth.weights(synth.dory2b(), SEED)
+        out = bench_batch(Dory, torch, w, int(os.environ.get("LOCAL_RANK", "0")), steps=4)
+        return {"case": "batch64", **out, "note": "profiling case, not a bench line"}
+    if args.profile_case == "prefill":
+        cfg = synth.dory2b(max_batch=1, max_seqs=1, max_context=args.prompt + 64, prompt_loops=2)
+        g = Dory(cfg, synth.weights(cfg, SEED))
+        ids = synth.token_ids(SEED, 0, args.prompt, cfg.vocab)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for a0 in range(0, args.prompt, 64):
+            g.prefill_chunk(0, ids[a0:a0 + 64], a0, cfg.loops, "none")
+        torch.cuda.synchronize()
+        ms = (time.perf_counter() - t0) * 1e3
+        g.close()
+        return {"case": "prefill", "tokens": args.prompt, "ms_host": round(ms, 3),
+                "note": "profiling case, not a bench line"}
     pat, a, b, c = synth.pattern_of("S", "S", "S")
     cfg = synth.dory2b(pattern=pat, n_in=a, n_rec=b, n_out=c, loops=1, max_batch=1, max_seqs=1,
                        max_context=args.prompt + DECODE + 64)
@@ -355,8 +374,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the batch-64 decode and prefill lines")
     ap.add_argument("--prompt", type=int, default=PROMPT, help="prompt tokens before the decode steps")
-    ap.add_argument("--profile-case", action="store_true",
-                    help="run the reduced decode case used for ncu captures instead of the bench")
+    ap.add_argument("--profile-case", choices=["decode-3pass", "prefill", "batch64"],
+                    help="run a small case for ncu captures instead of the bench")
     args = ap.parse_args()
     if args.profile_case:
         print(json.dumps(profile_case(args)), flush=True)
