@@ -160,6 +160,12 @@ struct dory_handle {
 
 namespace {
 
+// An environment switch set to "0".
+bool getenv_off(const char *name) {
+  const char *e = getenv(name);
+  return e && e[0] == '0';
+}
+
 int validate(const dory_config *c, std::string &pat) {
   if (!c) return fail(DORY_EINVAL, "config is NULL");
   if (c->hidden <= 0 || c->ffn <= 0 || c->vocab <= 0 || c->nh <= 0 || c->nk <= 0 || c->hd <= 0)
@@ -304,6 +310,9 @@ int issue_step(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_splits, cud
   const dory_config &c = d->cfg;
   const Dims dm = d->dims;
   const int T = a.T;
+  // rows 0..T-1 are consecutive positions of one sequence (a prefill chunk)
+  bool chunk_rows = T > 1 && !getenv_off("DORY_CHUNK_ATTN");
+  for (int r = 1; r < T && chunk_rows; r++) chunk_rows = a.hseq[r] == a.hseq[0] && a.hoff[r] == a.hoff[0] + r;
   Rows rows;
   rows.seq = rt;
   rows.off = rt + d->Tmax;
@@ -367,7 +376,12 @@ int issue_step(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_splits, cud
       const long keys = fixed_splits ? wmax : std::min<long>(wmax, pmax + 1);
       const int splits = (int)((keys + KEYS_PER_SPLIT - 1) / KEYS_PER_SPLIT);
       if (splits > d->max_splits) return fail(DORY_ERANGE, "attention needs %d splits (max %d)", splits, d->max_splits);
-      if (d->kv_tma || d->kv_tma_q8) {
+      const int nkb = attn_chunk_blocks(wmax, T);
+      if (chunk_rows && !q8 && (dm.hd == 64 || dm.hd == 128) && nkb <= d->max_splits) {
+        // a prefill chunk: the rows share every key block
+        CK(launch_attention_chunk(d->qkvg, ldq, dm, rows, ring, nkb, d->part, L.sg, d->z, s));
+        nl += 2;
+      } else if (d->kv_tma || d->kv_tma_q8) {
         const int tsp = fixed_splits ? attn_tma_splits(wmax) : tma_splits(d, a, ring);
         if (d->kv_tma)
           CK(launch_attention_tma(d->kvmap, d->qkvg, ldq, dm, rows, ring, tsp, d->part, L.sg, d->z, d->actr,
@@ -1116,6 +1130,7 @@ int dory_create(const dory_config *cfg, const dory_weights *w, void *stream, dor
     const long keys = o.window == INT_MAX ? (long)o.cap : std::min<long>(o.window, o.cap);
     d->max_splits = std::max<int>(d->max_splits, (int)((keys + KEYS_PER_SPLIT - 1) / KEYS_PER_SPLIT));
     d->max_splits = std::max<int>(d->max_splits, attn_tma_splits(keys));
+    d->max_splits = std::max<int>(d->max_splits, attn_chunk_blocks(keys, d->Tmax));
     if ((keys + KEYS_PER_SPLIT - 1) / KEYS_PER_SPLIT > 2 * dm.hd) {
       fail(DORY_EINVAL, "a window of %ld keys is more than the attention merge holds for hd %d", keys, dm.hd);
       return cleanup(DORY_EINVAL);

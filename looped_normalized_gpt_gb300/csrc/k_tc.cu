@@ -29,6 +29,7 @@ constexpr int TC_THREADS = 192;
 constexpr int BM = 128;  // weight rows per tile (MMA M)
 constexpr int BK = 64;   // K elements per stage (one 128-byte swizzle row)
 constexpr uint32_t WAIT_LIMIT = 1u << 20;
+constexpr int MAX_SPLITS = 8;  // K splits of a tile at most: one portable cluster
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -323,13 +324,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const int ta = (int)rank * per, tb = min(tcount, ta + per);
       const uint32_t pa = smem_u32(P + (size_t)m * PS), pu = smem_u32(P + (size_t)(BM + m) * PS);
       for (int t = ta; t < tb; t += 4) {
+        // all splits' partials requested at once (one DSMEM round trip), added in split order
+        float4 xs[MAX_SPLITS], ys[MAX_SPLITS];
+#pragma unroll
+        for (int sp = 0; sp < MAX_SPLITS; sp++) {
+          if (sp < splits) {
+            xs[sp] = ld_cluster4(pa + t * 4, (uint32_t)sp);
+            if (DUAL) ys[sp] = ld_cluster4(pu + t * 4, (uint32_t)sp);
+          }
+        }
         float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
-        for (int sp = 0; sp < splits; sp++) {
-          const float4 x = ld_cluster4(pa + t * 4, (uint32_t)sp);
-          a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
-          if (DUAL) {
-            const float4 y = ld_cluster4(pu + t * 4, (uint32_t)sp);
-            b.x += y.x; b.y += y.y; b.z += y.z; b.w += y.w;
+#pragma unroll
+        for (int sp = 0; sp < MAX_SPLITS; sp++) {
+          if (sp < splits) {
+            a.x += xs[sp].x; a.y += xs[sp].y; a.z += xs[sp].z; a.w += xs[sp].w;
+            if (DUAL) {
+              b.x += ys[sp].x; b.y += ys[sp].y; b.z += ys[sp].z; b.w += ys[sp].w;
+            }
           }
         }
         if (n < N) {
