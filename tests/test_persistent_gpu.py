@@ -87,3 +87,24 @@ def test_loop_count_changes_between_tokens():
         P.check_rings(0, 1e-5)
     finally:
         P.close()
+
+
+@pytest.mark.parametrize("nh,nk,hd", [(8, 8, 64), (8, 4, 64), (8, 1, 64), (4, 2, 128), (4, 4, 128)])
+def test_group_sizes_prefill_chunks_and_decode(nh, nk, hd):
+    """Query heads per kv head 1, 2 and 8 (both head widths): prefill chunks take the chunk
+    attention, decode tokens the persistent kernel; both against the oracle."""
+    cfg = synth.small(kv_mode="last_loop", nh=nh, nk=nk, hd=hd, rec_kinds="S*", full_window=0, loops=2,
+                      max_loops=2, max_context=1024)
+    P = Pair(cfg, 3005)
+    try:
+        ids = synth.token_ids(3005, 1, 200, cfg.vocab)
+        for a in range(0, 192, 64):
+            P.prefill(0, ids[a:a + 64], cfg.loops, "last" if a + 64 >= 192 else "none")
+        for i in ids[192:]:
+            P.decode([0], [int(i)], cfg.loops)
+            assert P.gpu.stats()["launches"] == 1
+        assert P.max_hidden_err <= 1e-4, P.max_hidden_err
+        assert all(P.top1)
+        P.check_rings(0, 1e-5)
+    finally:
+        P.close()
