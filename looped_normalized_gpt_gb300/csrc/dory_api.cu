@@ -903,6 +903,8 @@ int setup_tc(dory_t *d) {
   const int bn_max = tc_tile_rows(d->Tmax);
   int max_split = 8;  // K splits per tile at most (a portable cluster); DORY_TC_SPLITS lowers it
   if (const char *e = getenv("DORY_TC_SPLITS")) max_split = std::max(1, std::min(8, atoi(e)));
+  int per_sm = 2;  // blocks per SM the splits aim at; DORY_TC_PER_SM changes it
+  if (const char *e = getenv("DORY_TC_PER_SM")) per_sm = std::max(1, std::min(4, atoi(e)));
   size_t ws_floats = 0;
   int max_tiles = 1;
   auto mk = [&](TcW &w, const void *base, long rows, int K, int N, long pair) -> int {
@@ -911,7 +913,7 @@ int setup_tc(dory_t *d) {
     w.K = K;
     w.pair = pair;
     const int mt = (N + 127) / 128, nkb = K / 64;
-    w.splits = std::max(1, std::min(std::min(2 * sms / mt, max_split), nkb));
+    w.splits = std::max(1, std::min(std::min(per_sm * sms / mt, max_split), nkb));
     const int t_tiles = (d->Tmax + bn_max - 1) / bn_max;
     ws_floats = std::max(ws_floats, (size_t)mt * t_tiles * w.splits * (pair ? 2 : 1) * bn_max * 128);
     max_tiles = std::max(max_tiles, mt * t_tiles);
