@@ -18,6 +18,8 @@
 // issuing work, waits (bounded) for its own copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
 
+#include <cstdlib>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -418,6 +420,14 @@ cudaError_t launch_tc_gemm(const TcGemm &g, int T, int t_base, float *Y, int ldy
                            cudaStream_t s) {
   const bool dual = ep.mode == EPI_SILU;
   const int bn = tc_tile_rows(T);
+  static const bool deep = [] {
+    const char *e = getenv("DORY_TC_DEEP");
+    return e && e[0] == '1';
+  }();
+  if (deep && bn == 64) {  // one block per SM with a deeper stage ring
+    if (dual) return tc_launch<64, true, 4>(g, T, t_base, Y, ldy, ep, pdl, s);
+    return tc_launch<64, false, 6>(g, T, t_base, Y, ldy, ep, pdl, s);
+  }
 #define TCL(B, D, ST)                                                      \
   if (bn == B && dual == D) return tc_launch<B, D, ST>(g, T, t_base, Y, ldy, ep, pdl, s);
   TCL(16, false, 4) TCL(32, false, 4) TCL(64, false, 3) TCL(128, false, 3) TCL(256, false, 2)
