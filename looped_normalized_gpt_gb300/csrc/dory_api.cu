@@ -903,7 +903,7 @@ int setup_tc(dory_t *d) {
   const int bn_max = tc_tile_rows(d->Tmax);
   int max_split = 4;  // K splits per tile at most (measured best for 64-row steps); DORY_TC_SPLITS changes it
   if (const char *e = getenv("DORY_TC_SPLITS")) max_split = std::max(1, std::min(8, atoi(e)));
-  int per_sm = 2;  // blocks per SM the splits aim at; DORY_TC_PER_SM changes it
+  int per_sm = 1;  // blocks per SM the splits aim at (one: the 64-row rings fill an SM); DORY_TC_PER_SM changes it
   if (const char *e = getenv("DORY_TC_PER_SM")) per_sm = std::max(1, std::min(4, atoi(e)));
   size_t ws_floats = 0;
   int max_tiles = 1;
