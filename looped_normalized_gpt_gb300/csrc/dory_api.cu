@@ -377,10 +377,13 @@ int issue_step(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_splits, cud
       const int splits = (int)((keys + KEYS_PER_SPLIT - 1) / KEYS_PER_SPLIT);
       if (splits > d->max_splits) return fail(DORY_ERANGE, "attention needs %d splits (max %d)", splits, d->max_splits);
       const int nkb = attn_chunk_blocks(wmax, T);
+      bool z_normed = false;
       if (chunk_rows && !q8 && (dm.hd == 64 || dm.hd == 128) && nkb <= d->max_splits) {
-        // a prefill chunk: the rows share every key block
-        CK(launch_attention_chunk(d->qkvg, ldq, dm, rows, ring, nkb, d->part, L.sg, d->z, s));
+        // a prefill chunk: the rows share every key block; the merge also row-normalises z
+        CK(launch_attention_chunk(d->qkvg, ldq, dm, rows, ring, nkb, d->part, L.sg, d->z,
+                                  tc ? d->em_z : Emit{nullptr, nullptr}, s));
         nl += 2;
+        z_normed = true;
       } else if (d->kv_tma || d->kv_tma_q8) {
         const int tsp = fixed_splits ? attn_tma_splits(wmax) : tma_splits(d, a, ring);
         if (d->kv_tma)
@@ -398,8 +401,10 @@ int issue_step(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_splits, cud
         CK(launch_attention(d->qkvg, ldq, dm, rows, ring, splits, KEYS_PER_SPLIT, d->part, L.sg, d->z, s));
         nl += 2;
       }
-      CK(launch_rownorm(d->z, T, q_size, q_size, tc ? d->em_z : Emit{nullptr, nullptr}, s));
-      nl++;
+      if (!z_normed) {
+        CK(launch_rownorm(d->z, T, q_size, q_size, tc ? d->em_z : Emit{nullptr, nullptr}, s));
+        nl++;
+      }
       if (tc) {
         if ((rc = tcg(d->tcw[li][1], 1, T, 0, d->out, dm.hidden, ep))) return rc;
       } else if ((rc = gemm(L.wo, dm.hidden, q_size, d->z, q_size, d->out, dm.hidden, ep))) {

@@ -247,23 +247,6 @@ cudaError_t attn_q8(const float *qkvg, int ldq, Dims d, Rows rows, Ring ring, in
 
 }  // namespace
 
-cudaError_t launch_attention_combine(const float *part, int splits, const float *qkvg, int ldq, Dims d, Rows rows,
-                                     Ring ring, const float *sg, float *z, cudaStream_t s) {
-  const int rep = d.nh / d.nk, nv = d.hd / 32;
-  const dim3 g2(rows.n, d.nk);
-#define COMBINE(R, N)                                                                                      \
-  if (rep == R && nv == N) {                                                                               \
-    attn_combine_kernel<false, R, N><<<g2, N * 32, 0, s>>>(part, splits, qkvg, ldq, d, rows, ring, sg, z); \
-    return cudaGetLastError();                                                                             \
-  }
-  COMBINE(1, 1) COMBINE(1, 2) COMBINE(1, 4)
-  COMBINE(2, 1) COMBINE(2, 2) COMBINE(2, 4)
-  COMBINE(4, 1) COMBINE(4, 2) COMBINE(4, 4)
-  COMBINE(8, 1) COMBINE(8, 2) COMBINE(8, 4)
-#undef COMBINE
-  return cudaErrorInvalidValue;
-}
-
 cudaError_t launch_attention(const float *qkvg, int ldq, Dims d, Rows rows, Ring ring, int splits, int kps, float *part,
                              const float *sg, float *z, cudaStream_t s) {
   return ring.q8 ? attn_q8<true>(qkvg, ldq, d, rows, ring, splits, kps, part, sg, z, s)

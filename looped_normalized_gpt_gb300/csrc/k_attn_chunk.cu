@@ -10,9 +10,11 @@
 // 4 x 4 register tile, and sums over the head width a float4 at a time. A key counts for
 // the row at p when it lies in [max(p - W + 1, 0), p] and its ring row's tag holds it. Then
 // the block's softmax statistics per query (four threads per query), and the value sum with
-// the same 4 x (hd/16) register tiling. Each block leaves (output, max, sum) per query in
-// the split-KV layout of k_attn.cu; the combine kernel there merges the key blocks and
-// applies the gate.
+// the same 4 x (hd/16) register tiling. Each block leaves per query its unnormalised output
+// o[hd] and (max, sum). A second kernel, one block per row, merges the key blocks of every
+// head (all partials requested at once), applies the output gate y * sigmoid(g * s_g^2),
+// justnorms the row over nh * hd and writes it with its two bf16 halves for the O
+// projection (dory.rs fn attn_layer).
 #include <climits>
 
 #include "common.cuh"
@@ -171,20 +173,76 @@ __global__ void __launch_bounds__(CK_THREADS) attn_chunk_kernel(const float *__r
   for (int a = 0; a < 4; a++) {
     const int qi = tq + 16 * a, r = r_first + qi / REP, h = qi % REP;
     if (r >= T) continue;
-    float *out = part + ((((size_t)r * d.nk + kh) * nkb + sb) * REP + h) * (HD + 2);
+    const size_t pi = (((size_t)r * d.nk + kh) * nkb + sb) * REP + h;  // partial index
+    float *out = part + pi * HD;
 #pragma unroll
     for (int g = 0; g < NG; g++)
-#pragma unroll
-      for (int i = 0; i < 4; i++) out[tk * 4 + 64 * g + i] = o[a][g][i];
-    if (tk == 0) {
-      out[HD] = S.m[qi];
-      out[HD + 1] = S.l[qi];
-    }
+      *reinterpret_cast<float4 *>(out + tk * 4 + 64 * g) = make_float4(o[a][g][0], o[a][g][1], o[a][g][2], o[a][g][3]);
+    if (tk == 0)
+      *reinterpret_cast<float2 *>(part + (size_t)T * d.nk * nkb * REP * HD + pi * 2) = make_float2(S.m[qi], S.l[qi]);
   }
 }
 
+__device__ __forceinline__ void emit4(const Emit &em, size_t i, float4 v) {
+  if (!em.hi) return;
+  const float x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int u = 0; u < 4; u++) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(x[u]);
+    em.hi[i + u] = h;
+    em.lo[i + u] = __float2bfloat16_rn(x[u] - __bfloat162float(h));
+  }
+}
+
+// One block per row, thread i owns z[4i .. 4i+4) (head (4i)/hd).
 template <int HD, int REP>
-cudaError_t chunk_t(const float *qkvg, int ldq, Dims d, Rows rows, Ring ring, int nkb, float *part, cudaStream_t s) {
+__global__ void attn_chunk_merge_kernel(const float *__restrict__ part, int nkb, const float *__restrict__ qkvg,
+                                        int ldq, Dims d, const float *__restrict__ sg, float *__restrict__ z,
+                                        Emit em) {
+  constexpr int MB = 12;  // key blocks requested at once
+  __shared__ float red[32];
+  const int r = blockIdx.x, T = gridDim.x, i = threadIdx.x;
+  const int hg = (4 * i) / HD, kh = hg / REP, h = hg % REP, dim = (4 * i) % HD;
+  const float4 graw = *reinterpret_cast<const float4 *>(qkvg + (size_t)r * ldq + (size_t)(d.nh + 2 * d.nk) * HD + 4 * i);
+  const float4 sgv = __ldg(reinterpret_cast<const float4 *>(sg + 4 * i));
+  const size_t p0 = ((size_t)r * d.nk + kh) * nkb * REP + h;  // partial index of key block 0
+  const float2 *ml = reinterpret_cast<const float2 *>(part + (size_t)T * d.nk * nkb * REP * HD);
+  float M = -INFINITY, L = 0.f;
+  float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int b0 = 0; b0 < nkb; b0 += MB) {
+    float4 o[MB];
+    float2 m[MB];
+#pragma unroll
+    for (int u = 0; u < MB; u++) {
+      const bool in = b0 + u < nkb;
+      const size_t pi = p0 + (size_t)(b0 + u) * REP;
+      o[u] = in ? *reinterpret_cast<const float4 *>(part + pi * HD + dim) : make_float4(0.f, 0.f, 0.f, 0.f);
+      m[u] = in ? ml[pi] : make_float2(-INFINITY, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < MB; u++) {
+      if (m[u].x == -INFINITY) continue;
+      const float nm = fmaxf(M, m[u].x);
+      const float sa = M == -INFINITY ? 0.f : expf(M - nm), sb = expf(m[u].x - nm);
+      L = L * sa + m[u].y * sb;
+      A = make_float4(A.x * sa + o[u].x * sb, A.y * sa + o[u].y * sb, A.z * sa + o[u].z * sb, A.w * sa + o[u].w * sb);
+      M = nm;
+    }
+  }
+  const float inv_l = L > 0.f ? 1.f / L : 0.f;
+  float4 y = make_float4(A.x * inv_l * sigmoidf_(graw.x * sgv.x), A.y * inv_l * sigmoidf_(graw.y * sgv.y),
+                         A.z * inv_l * sigmoidf_(graw.z * sgv.z), A.w * inv_l * sigmoidf_(graw.w * sgv.w));
+  const float ss = block_sum(y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w, red);
+  const float inv = 1.f / sqrtf(ss + DORY_EPS);
+  y = make_float4(y.x * inv, y.y * inv, y.z * inv, y.w * inv);
+  const size_t zi = (size_t)r * d.nh * HD + 4 * i;
+  *reinterpret_cast<float4 *>(z + zi) = y;
+  emit4(em, zi, y);
+}
+
+template <int HD, int REP>
+cudaError_t chunk_t(const float *qkvg, int ldq, Dims d, Rows rows, Ring ring, int nkb, float *part, const float *sg,
+                    float *z, Emit em, cudaStream_t s) {
   const size_t smem = sizeof(ChunkSmem<HD>);
   static bool attr = false;
   if (!attr) {
@@ -194,6 +252,7 @@ cudaError_t chunk_t(const float *qkvg, int ldq, Dims d, Rows rows, Ring ring, in
   constexpr int RG = CK_QUERIES / REP;
   const int nrg = (rows.n + RG - 1) / RG;
   attn_chunk_kernel<HD, REP><<<dim3(d.nk * nrg, nkb), CK_THREADS, smem, s>>>(qkvg, ldq, d, rows, ring, nkb, part);
+  attn_chunk_merge_kernel<HD, REP><<<rows.n, d.nh * HD / 4, 0, s>>>(part, nkb, qkvg, ldq, d, sg, z, em);
   return cudaGetLastError();
 }
 
@@ -204,16 +263,15 @@ int attn_chunk_blocks(long window_keys, int rows) {
 }
 
 cudaError_t launch_attention_chunk(const float *qkvg, int ldq, Dims d, Rows rows, Ring ring, int nkb, float *part,
-                                   const float *sg, float *z, cudaStream_t s) {
+                                   const float *sg, float *z, Emit em, cudaStream_t s) {
   const int rep = d.nh / d.nk;
-  cudaError_t e = cudaErrorInvalidValue;
+  if (d.nh * d.hd / 4 > 1024) return cudaErrorInvalidValue;  // one thread per 4 outputs of a row
 #define CHUNK(H, R) \
-  if (d.hd == H && rep == R) e = chunk_t<H, R>(qkvg, ldq, d, rows, ring, nkb, part, s);
+  if (d.hd == H && rep == R) return chunk_t<H, R>(qkvg, ldq, d, rows, ring, nkb, part, sg, z, em, s);
   CHUNK(64, 1) CHUNK(64, 2) CHUNK(64, 4) CHUNK(64, 8)
   CHUNK(128, 1) CHUNK(128, 2) CHUNK(128, 4) CHUNK(128, 8)
 #undef CHUNK
-  if (e != cudaSuccess) return e;
-  return launch_attention_combine(part, nkb, qkvg, ldq, d, rows, ring, sg, z, s);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace dory

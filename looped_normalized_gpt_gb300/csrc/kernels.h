@@ -92,16 +92,12 @@ cudaError_t launch_q8_append_frozen(const float *kst, const float *vst, int n, D
 cudaError_t launch_attention(const float *qkvg, int ldq, Dims d, Rows rows, Ring ring, int splits, int keys_per_split,
                              float *part, const float *sg, float *z, cudaStream_t s);
 
-// The combine step alone (f32 rings): merge `splits` partials per (row, kv head) laid out as
-// part[((row * nk + kh) * splits + s) * REP + h][hd + 2] and gate into z.
-cudaError_t launch_attention_combine(const float *part, int splits, const float *qkvg, int ldq, Dims d, Rows rows,
-                                     Ring ring, const float *sg, float *z, cudaStream_t s);
-
 // A prefill chunk's attention: rows 0..T-1 are consecutive positions of one sequence
-// (f32 ring, hd 64 or 128); `nkb` = attn_chunk_blocks(window keys, T) key blocks.
+// (f32 ring, hd 64 or 128); `nkb` = attn_chunk_blocks(window keys, T) key blocks. Writes z
+// gated and row-normalised (with its bf16 halves when em.hi is set).
 int attn_chunk_blocks(long window_keys, int rows);
 cudaError_t launch_attention_chunk(const float *qkvg, int ldq, Dims d, Rows rows, Ring ring, int nkb, float *part,
-                                   const float *sg, float *z, cudaStream_t s);
+                                   const float *sg, float *z, Emit em, cudaStream_t s);
 
 cudaError_t launch_rownorm(float *x, int T, int width, int ld, Emit em, cudaStream_t s);
 
