@@ -113,7 +113,8 @@ typedef struct dory_weights {
 typedef struct dory_handle dory_t;
 
 /* Build a handle: checks the config (nh % nk == 0, 1 <= max_loops <= 16, the pattern's
- * length and chars, hd in {32, 64, 128}, nh / nk in {1, 2, 4, 8}, ...), copies every weight into device
+ * length and chars, hd in {32, 64, 128}, nh / nk in {1, 2, 4, 8}, hidden and ffn multiples
+ * of 32, hidden <= 8192, ffn and nh * hd <= 32768, ...), copies every weight into device
  * memory the handle owns (the caller may free its buffers on return), allocates the KV
  * rings of max_seqs sequences and resets them. `stream` is a cudaStream_t (NULL: the
  * legacy default stream) that orders all of the handle's work.

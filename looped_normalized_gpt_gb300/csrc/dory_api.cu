@@ -176,6 +176,7 @@ int validate(const dory_config *c, std::string &pat) {
   if (c->hd != 32 && c->hd != 64 && c->hd != 128) return fail(DORY_EINVAL, "hd must be 32, 64 or 128");
   if (c->hidden % 32 || c->ffn % 32) return fail(DORY_EINVAL, "hidden and ffn must be multiples of 32");
   if (c->hidden > 8192) return fail(DORY_EINVAL, "hidden above 8192");
+  if (c->ffn > 32768 || c->nh * c->hd > 32768) return fail(DORY_EINVAL, "ffn or nh*hd above 32768");
   if (c->max_loops < 1 || c->max_loops > DORY_MAX_LOOPS)
     return fail(DORY_EINVAL, "max_loops=%d: want 1..%d", c->max_loops, DORY_MAX_LOOPS);
   if (c->window < 1) return fail(DORY_EINVAL, "window must be positive");

@@ -153,18 +153,30 @@ __global__ void prep_kernel(float *__restrict__ qkvg, int ldq, Dims d, Rows rows
 }
 
 // x / sqrt(sum x^2 + eps) per row, in place (dory.rs fn justnorm).
+// The row stays in registers between the sum of squares and the scaling (one read of x).
+template <int MAXV>
 __global__ void rownorm_kernel(float *__restrict__ x, int width, int ld, Emit em) {
   __shared__ float red[32];
   pdl_trigger_();
   float *row = x + (size_t)blockIdx.x * ld;
+  float v[MAXV];
   float s = 0.f;
-  for (int i = threadIdx.x; i < width; i += blockDim.x) s += row[i] * row[i];
+#pragma unroll
+  for (int j = 0; j < MAXV; j++) {
+    const int i = threadIdx.x + j * blockDim.x;
+    v[j] = i < width ? row[i] : 0.f;
+    s += v[j] * v[j];
+  }
   s = block_sum(s, red);
   const float inv = 1.f / sqrtf(s + DORY_EPS);
-  for (int i = threadIdx.x; i < width; i += blockDim.x) {
-    const float v = row[i] * inv;
-    row[i] = v;
-    emit(em, (size_t)blockIdx.x * width + i, v);
+#pragma unroll
+  for (int j = 0; j < MAXV; j++) {
+    const int i = threadIdx.x + j * blockDim.x;
+    if (i < width) {
+      const float y = v[j] * inv;
+      row[i] = y;
+      emit(em, (size_t)blockIdx.x * width + i, y);
+    }
   }
 }
 
@@ -311,7 +323,11 @@ cudaError_t launch_prep(float *qkvg, int ldq, Dims d, Rows rows, const float *ro
 }
 
 cudaError_t launch_rownorm(float *x, int T, int width, int ld, Emit em, cudaStream_t s) {
-  rownorm_kernel<<<T, 512, 0, s>>>(x, width, ld, em);
+  const int per = (width + 511) / 512;
+  if (per <= 4) rownorm_kernel<4><<<T, 512, 0, s>>>(x, width, ld, em);
+  else if (per <= 16) rownorm_kernel<16><<<T, 512, 0, s>>>(x, width, ld, em);
+  else if (per <= 64) rownorm_kernel<64><<<T, 512, 0, s>>>(x, width, ld, em);
+  else return cudaErrorInvalidValue;
   return cudaGetLastError();
 }
 
