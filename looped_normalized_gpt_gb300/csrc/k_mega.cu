@@ -410,7 +410,7 @@ __device__ __forceinline__ float *part_ml(const MegaStage &st, int nk, int rep, 
 // meet in shared memory `scr` and the first nq threads finish: y = sum o e^(m - M) / sum l
 // e^(m - M), z = y * sigmoid(g * s_g^2).
 template <int HD>
-__device__ __noinline__ void merge_items(const WarpTeam &tm, const MegaStage &st, const Dims &d, int kh, int nblk,
+__device__ __forceinline__ void merge_items(const WarpTeam &tm, const MegaStage &st, const Dims &d, int kh, int nblk,
                                          float *scr) {
   constexpr int IB = 9;  // items a thread loads per round
   const int rep = d.nh / d.nk, nq = rep * HD / 4;
