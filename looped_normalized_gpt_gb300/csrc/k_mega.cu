@@ -61,7 +61,7 @@ struct Ctl {
 };
 
 // Cycle counts of the current stage's phases (trace only; the team's first thread).
-__shared__ unsigned long long trace_acc[4];
+__shared__ unsigned long long trace_acc[6];
 
 // Optional per-stage timestamps (off when the pointer is null).
 struct Tracer {
@@ -77,11 +77,11 @@ struct Tracer {
   }
   __device__ __forceinline__ void zero(int) const {
     if (p)
-      for (int e = 0; e < 4; e++) trace_acc[e] = 0;
+      for (int e = 0; e < 6; e++) trace_acc[e] = 0;
   }
   __device__ __forceinline__ void flush(int stage) const {
     if (p)
-      for (int e = 0; e < 4; e++) p[((size_t)stage * gridDim.x + blockIdx.x) * MEGA_TRACE_EVENTS + 8 + e] = trace_acc[e];
+      for (int e = 0; e < 6; e++) p[((size_t)stage * gridDim.x + blockIdx.x) * MEGA_TRACE_EVENTS + 8 + e] = trace_acc[e];
   }
   __device__ __forceinline__ long long clk() const { return p ? clock64() : 0; }
 };
@@ -411,7 +411,8 @@ __device__ __forceinline__ float *part_ml(const MegaStage &st, int nk, int rep, 
 // e^(m - M), z = y * sigmoid(g * s_g^2).
 template <int HD>
 __device__ __forceinline__ void merge_items(const WarpTeam &tm, const MegaStage &st, const Dims &d, int kh, int nblk,
-                                         float *scr) {
+                                         float *scr, const Tracer &tr) {
+  const long long t_in = tr.clk();
   constexpr int IB = 9;  // items a thread loads per round
   const int rep = d.nh / d.nk, nq = rep * HD / 4;
   const int groups = tm.size() / nq;
@@ -460,7 +461,9 @@ __device__ __forceinline__ void merge_items(const WarpTeam &tm, const MegaStage 
       Ms[g * nq + q] = M;
       Ls[g * nq + q] = L;
     }
+    tr.add(0, 12, tr.clk() - t_in);
     tm.sync();
+    tr.add(0, 13, tr.clk() - t_in);
     if (g == 0 && act) {
       float Mx = -INFINITY;
       for (int k = 0; k < groups; k++) Mx = fmaxf(Mx, Ms[k * nq + q]);
@@ -658,7 +661,7 @@ __device__ __noinline__ bool attn_stage(const WarpTeam &tm, const MegaArgs &a, c
     t1 = tr.clk();
     tr.add(s, 10, t1 - t0);
     if (ctl.last) {
-      merge_items<HD>(tm, st, d, kh, nblk, Ks);
+      merge_items<HD>(tm, st, d, kh, nblk, Ks, tr);
       tr.add(s, 11, tr.clk() - t1);
     }
   }

@@ -233,8 +233,9 @@ struct MegaArgs {
 // from the producer warp: 5 first chunk of the stage issued, 6 last chunk issued; 7 the
 // stage's first chunk has landed (consumers); 8..11 SM cycles the first consumer thread
 // spent over the stage's chunks waiting for a slot, reducing, at the team barrier, and in
-// the epilogue.
-constexpr int MEGA_TRACE_EVENTS = 12;
+// the epilogue (attention stages: copy wait, compute, arrival, merge); 12, 13 cycles of
+// the attention merge until its partials are folded, and until its team sync.
+constexpr int MEGA_TRACE_EVENTS = 14;
 
 // Bytes of dynamic shared memory and whether the device runs the kernel (one block per SM,
 // cooperative launch).
