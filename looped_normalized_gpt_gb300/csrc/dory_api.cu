@@ -385,6 +385,10 @@ int issue_step(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_splits, cud
                                   tc ? d->em_z : Emit{nullptr, nullptr}, s));
         nl += 2;
         z_normed = true;
+      } else if (!q8 && (dm.hd == 64 || dm.hd == 128) && !getenv_off("DORY_STREAM_ATTN")) {
+        // rows of separate sequences: each (row, kv head) streams its own window
+        CK(launch_attention_stream(d->qkvg, ldq, dm, rows, ring, L.sg, d->z, d->dev_err, s));
+        nl += 1;
       } else if (d->kv_tma || d->kv_tma_q8) {
         const int tsp = fixed_splits ? attn_tma_splits(wmax) : tma_splits(d, a, ring);
         if (d->kv_tma)

@@ -99,6 +99,11 @@ int attn_chunk_blocks(long window_keys, int rows);
 cudaError_t launch_attention_chunk(const float *qkvg, int ldq, Dims d, Rows rows, Ring ring, int nkb, float *part,
                                    const float *sg, float *z, Emit em, cudaStream_t s);
 
+// Rows of any sequences (a batched decode step) over f32 rings, hd 64 or 128: one block per
+// (row, kv head) streams the window in 32-position tiles; writes z gated (not row-normalised).
+cudaError_t launch_attention_stream(const float *qkvg, int ldq, Dims d, Rows rows, Ring ring, const float *sg,
+                                    float *z, int *err, cudaStream_t s);
+
 cudaError_t launch_rownorm(float *x, int T, int width, int ld, Emit em, cudaStream_t s);
 
 enum Mix { MIX_NONE = 0, MIX_BEGIN = 1, MIX_LOOP = 2, MIX_END = 3 };
