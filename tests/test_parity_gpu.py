@@ -298,3 +298,23 @@ def test_head_width_128_rings_with_tile_copies(kv_quant):
                 P.check_rings(s, 1e-5)
     finally:
         P.close()
+
+
+@pytest.mark.parametrize("hd,nh,nk", [(64, 8, 2), (128, 4, 2)])
+def test_batched_decode_streams_each_window(hd, nh, nk):
+    """Six sequences with different context lengths (per_loop holes from changing loop
+    counts): a step of 6 rows takes the streaming attention (one block per row and kv head)."""
+    cfg = synth.small(kv_mode="per_loop", hd=hd, nh=nh, nk=nk, rec_kinds="S*", full_window=120, max_batch=6,
+                      max_seqs=6, max_loops=3, loops=3)
+    P = Pair(cfg, 2011)
+    try:
+        for s in range(6):
+            P.write_context(s, 20 + 37 * s, 2011 + s)
+        for step, loops in enumerate([3, 1, 2, 3]):
+            P.decode(list(range(6)), synth.token_ids(2011, 50 + step, 6, cfg.vocab), loops)
+        assert P.max_hidden_err <= 1e-4, P.max_hidden_err
+        assert np.mean(P.top1) >= 0.99
+        for s in range(6):
+            P.check_rings(s, 1e-5)
+    finally:
+        P.close()
