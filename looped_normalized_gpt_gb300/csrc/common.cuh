@@ -55,6 +55,17 @@ __device__ __forceinline__ void unpack8(const uint4 &u, float *w) {
   }
 }
 
+// Two fused multiply-adds in one instruction (packed f32x2, sm_100+): (a.x*b.x + c.x,
+// a.y*b.y + c.y), each rounded as fmaf rounds it.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n mov.b64 rc, {%6, %7};\n"
+      " fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}\n"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
 __device__ __forceinline__ float load_w(const float *p, size_t i) { return p[i]; }
 __device__ __forceinline__ float load_w(const __nv_bfloat16 *p, size_t i) { return __bfloat162float(p[i]); }
 

@@ -110,7 +110,7 @@ __global__ void __launch_bounds__(AS_WARPS * 32) attn_stream_kernel(const float 
     for (int u = 0; u < (REP + AS_WARPS - 1) / AS_WARPS; u++) {
       const int h = warp + u * AS_WARPS;
       if (h >= REP) break;
-      float s0 = 0.f, s1 = 0.f;
+      float2 s2 = make_float2(0.f, 0.f);
       if (valid) {
         const float4 *kr = reinterpret_cast<const float4 *>(Kt + lane * HD);
         const float4 *q4 = reinterpret_cast<const float4 *>(qs[h]);
@@ -118,11 +118,11 @@ __global__ void __launch_bounds__(AS_WARPS * 32) attn_stream_kernel(const float 
         for (int c = 0; c < NC; c++) {
           const int cc = (c + lane) & (NC - 1);
           const float4 k = kr[cc], q = q4[cc];
-          s0 = fmaf(q.x, k.x, fmaf(q.y, k.y, s0));
-          s1 = fmaf(q.z, k.z, fmaf(q.w, k.w, s1));
+          s2 = ffma2(make_float2(q.y, q.w), make_float2(k.y, k.w), s2);
+          s2 = ffma2(make_float2(q.x, q.z), make_float2(k.x, k.z), s2);
         }
       }
-      const float sc = valid ? (s0 + s1) * scale : -INFINITY;
+      const float sc = valid ? (s2.x + s2.y) * scale : -INFINITY;
       const float mt = warp_max(sc);
       const float mn = fmaxf(m[u], mt);
       if (mn == -INFINITY) continue;  // nothing valid yet (warp-uniform)
@@ -141,9 +141,13 @@ __global__ void __launch_bounds__(AS_WARPS * 32) attn_stream_kernel(const float 
         const float w0 = __shfl_sync(0xffffffffu, e, j), w1 = __shfl_sync(0xffffffffu, e, j + 1);
         const float *v0 = Vt + j * HD + lane * NV, *v1 = v0 + HD;
 #pragma unroll
-        for (int i = 0; i < NV; i++) {
-          a0[i] = fmaf(w0, v0[i], a0[i]);
-          a1[i] = fmaf(w1, v1[i], a1[i]);
+        for (int i = 0; i < NV; i += 2) {
+          const float2 r0 = ffma2(make_float2(w0, w0), make_float2(v0[i], v0[i + 1]), make_float2(a0[i], a0[i + 1]));
+          const float2 r1 = ffma2(make_float2(w1, w1), make_float2(v1[i], v1[i + 1]), make_float2(a1[i], a1[i + 1]));
+          a0[i] = r0.x;
+          a0[i + 1] = r0.y;
+          a1[i] = r1.x;
+          a1[i + 1] = r1.y;
         }
       }
 #pragma unroll

@@ -282,7 +282,7 @@ __device__ void gemv_chunks(const WarpTeam &tm, const MegaStage &st, int rb, int
     float acc[2 * RMAX];  // [0, RMAX): rows; [RMAX, 2 RMAX): up rows (DUAL)
 #pragma unroll
     for (int r = 0; r < RMAX; r++) {
-      float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+      float2 a = make_float2(0.f, 0.f), bb = a;  // even and odd columns
       if (r < nr && landed) {
 #pragma unroll
         for (int g = 0; g < SEG; g++) {
@@ -291,23 +291,19 @@ __device__ void gemv_chunks(const WarpTeam &tm, const MegaStage &st, int rb, int
             float wv[8];
             unpack8(w[r * nu + u], wv);
 #pragma unroll
-            for (int e = 0; e < 8; e += 2) {
-              a0 = fmaf(wv[e], xr[8 * g + e], a0);
-              a1 = fmaf(wv[e + 1], xr[8 * g + e + 1], a1);
-            }
+            for (int e = 0; e < 8; e += 2)
+              a = ffma2(make_float2(wv[e], wv[e + 1]), make_float2(xr[8 * g + e], xr[8 * g + e + 1]), a);
             if (DUAL) {
               unpack8(w[(nr + r) * nu + u], wv);
 #pragma unroll
-              for (int e = 0; e < 8; e += 2) {
-                b0 = fmaf(wv[e], xr[8 * g + e], b0);
-                b1 = fmaf(wv[e + 1], xr[8 * g + e + 1], b1);
-              }
+              for (int e = 0; e < 8; e += 2)
+                bb = ffma2(make_float2(wv[e], wv[e + 1]), make_float2(xr[8 * g + e], xr[8 * g + e + 1]), bb);
             }
           }
         }
       }
-      acc[r] = a0 + a1;
-      acc[RMAX + r] = b0 + b1;
+      acc[r] = a.x + a.y;
+      acc[RMAX + r] = bb.x + bb.y;
     }
     float(*rb_)[2 * RMAX] = red[i & 1];
     if (DUAL) {
