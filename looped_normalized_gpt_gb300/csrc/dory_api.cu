@@ -52,7 +52,10 @@ struct TcW {
   CUtensorMap map;
   int N = 0, K = 0, splits = 1;
   long pair = 0;
+  unsigned long long *trace = nullptr;  // DORY_TC_TRACE: the last launch's block timeline
+  int trace_grid = 0;                   // blocks of that launch
 };
+constexpr int TC_TRACE_BLOCKS = 1024;
 
 int bn_index(int bn) { return bn <= 16 ? 0 : bn <= 32 ? 1 : bn <= 64 ? 2 : bn <= 128 ? 3 : 4; }
 
@@ -216,6 +219,10 @@ void free_all(dory_t *d) {
   d->mega_stages = nullptr;
   if (d->mega_trace) cudaFree(d->mega_trace);
   d->mega_trace = nullptr;
+  for (auto &pr : d->tcw)
+    for (TcW &w : pr)
+      if (w.trace) cudaFree(w.trace), w.trace = nullptr;
+  if (d->tc_head.trace) cudaFree(d->tc_head.trace), d->tc_head.trace = nullptr;
   d->mega_cap = 0;
   d->plans.clear();
   if (d->cap_stream) cudaStreamDestroy(d->cap_stream);
@@ -343,6 +350,11 @@ int issue_step(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_splits, cud
     g.ws = d->tc_ws;
     g.ctr = d->tc_ctr;
     g.err = d->tc_err;
+    g.trace = w.trace;
+    if (w.trace) {
+      const int bn = tc_tile_rows(rowsT);
+      const_cast<TcW &>(w).trace_grid = ((w.N + 127) / 128) * g.splits * ((rowsT + bn - 1) / bn);
+    }
     CK(launch_tc_gemm(g, rowsT, t_base, Y, ldy, ep, true, s));
     nl++;
     ng++;
@@ -923,6 +935,12 @@ int setup_tc(dory_t *d) {
     w.K = K;
     w.pair = pair;
     const int mt = (N + 127) / 128, nkb = K / 64;
+    if (getenv("DORY_TC_TRACE") && !w.trace) {
+      if (cudaMalloc(&w.trace, (size_t)TC_TRACE_BLOCKS * 8 * 8) != cudaSuccess) {
+        cudaGetLastError();
+        w.trace = nullptr;
+      }
+    }
     w.splits = std::max(1, std::min(std::min(per_sm * sms / mt, max_split), nkb));
     const int t_tiles = (d->Tmax + bn_max - 1) / bn_max;
     ws_floats = std::max(ws_floats, (size_t)mt * t_tiles * w.splits * (pair ? 2 : 1) * bn_max * 128);
@@ -1289,6 +1307,24 @@ int dory_create(const dory_config *cfg, const dory_weights *w, void *stream, dor
 int dory_destroy(dory_t *d) {
   if (!d) return DORY_OK;
   cudaStreamSynchronize(d->stream);
+  if (const char *tp = getenv("DORY_TC_TRACE")) {
+    // file: records of int32 (layer, which, N, K, splits, blocks) then u64 [blocks][8]
+    if (FILE *f = fopen(tp, "wb")) {
+      auto dump = [&](const TcW &w, int li, int which) {
+        if (!w.trace || w.trace_grid <= 0) return;
+        const int nb = std::min(w.trace_grid, TC_TRACE_BLOCKS);
+        std::vector<unsigned long long> t((size_t)nb * 8);
+        if (cudaMemcpy(t.data(), w.trace, t.size() * 8, cudaMemcpyDeviceToHost) != cudaSuccess) return;
+        const int32_t hdr[6] = {li, which, w.N, w.K, w.splits, nb};
+        fwrite(hdr, 4, 6, f);
+        fwrite(t.data(), 8, t.size(), f);
+      };
+      for (size_t li = 0; li < d->tcw.size(); li++)
+        for (int which = 0; which < 2; which++) dump(d->tcw[li][which], (int)li, which);
+      dump(d->tc_head, -1, 0);
+      fclose(f);
+    }
+  }
   if (d->mega_trace && !d->mega_trace_desc.empty()) {
     // file: int32 nstages, grid, events; int32 [nstages][3] (kind, N, K); u64 stamps
     const int32_t hdr[3] = {(int32_t)(d->mega_trace_desc.size() / 3), d->sms, MEGA_TRACE_EVENTS};

@@ -157,13 +157,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmXh,
                    const __grid_constant__ CUtensorMap tmXl, int N, int K, int T, int t_base, int splits,
                    long pair_rows, float *__restrict__ ws, int *__restrict__ tile_ctr, float *__restrict__ Y, int ldy,
-                   EpiArgs ep, int *__restrict__ err) {
+                   EpiArgs ep, int *__restrict__ err, unsigned long long *__restrict__ trace) {
   using S = TcSmem<BN, DUAL, ST>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_full[ST], bar_empty[ST], bar_acc;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int is_last, failed;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // optional timeline: 0 start, 1 set up, 2 past the dependency wait, 3 first stage landed,
+  // 4 last MMA issued, 5 accumulator ready, 6 tile read out, 7 done
+  auto mark = [&](int e) {
+    if (!trace) return;
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    trace[((size_t)blockIdx.y * gridDim.x + blockIdx.x) * 8 + e] = t;
+  };
+  if (threadIdx.x == 0) mark(0);
   const int tile = blockIdx.x / splits, split = blockIdx.x % splits;
   const int n0 = tile * BM;
   const int t0 = blockIdx.y * BN;
@@ -195,6 +204,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   fence_before();
   __syncthreads();
   fence_after();
+  if (threadIdx.x == 0) mark(1);
   const uint32_t tmem = tmem_base_sh;
   const uint32_t tx = (uint32_t)(S::A_BYTES * (DUAL ? 2 : 1) + 2 * S::B_BYTES);
 
@@ -210,6 +220,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (DUAL) tma_load_2d(a_addr(i, 1), &tmW, kc, (int)(n0 + pair_rows), fb);
       }
       pdl_wait();
+      mark(2);
       for (int i = 0; i < pre; i++) {
         const uint32_t fb = smem_u32(&bar_full[i]);
         const int kc = (kb0 + i) * BK;
@@ -243,6 +254,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           failed = 1;
           break;
         }
+        if (i == 0) mark(3);
         fence_after();
 #pragma unroll
         for (int kk = 0; kk < BK / 16; kk++) {
@@ -260,6 +272,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         mma_commit(smem_u32(&bar_empty[s]));
       }
+      mark(4);
       mma_commit(smem_u32(&bar_acc));
     }
   } else {
@@ -291,6 +304,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       atomicExch(err, 3);
       failed = 1;
     }
+    if (threadIdx.x == 64) mark(5);
     fence_after();
     if (ok && !failed) {
       for (int c = 0; c < BN; c += 16) {
@@ -315,6 +329,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       }
     }
   }
+  if (threadIdx.x == 64) mark(6);
   if (splits > 1) {
     cluster_sync();  // every block's partial tile is in place
     if (warp >= 2) {
@@ -365,6 +380,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   fence_after();
   if (warp == 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(S::TMEM_COLS) : "memory");
+  if (threadIdx.x == 64) mark(7);
 }
 
 template <int BN, bool DUAL, int ST>
@@ -403,7 +419,7 @@ cudaError_t tc_launch(const TcGemm &g, int T, int t_base, float *Y, int ldy, Epi
   cfg.attrs = attr1;
   cfg.numAttrs = na;
   return cudaLaunchKernelEx(&cfg, kern, g.tmW, g.tmXh, g.tmXl, g.N, g.K, T, t_base, splits, g.pair_rows, g.ws,
-                            g.ctr, Y, ldy, ep, g.err);
+                            g.ctr, Y, ldy, ep, g.err, g.trace);
 }
 
 }  // namespace

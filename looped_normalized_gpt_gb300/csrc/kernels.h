@@ -165,6 +165,7 @@ struct TcGemm {
   float *ws;                // split-K partial tiles
   int *ctr;                 // per-tile arrival counters (zero between launches)
   int *err;                 // set when a bounded wait expires
+  unsigned long long *trace;  // null, or [grid.y][grid.x][8] %globaltimer stamps per block
 };
 
 int tc_tile_rows(int T);
