@@ -9,11 +9,11 @@
 // Block roles (192 threads): warp 0 lane 0 drives TMA (128B-swizzled tiles into a ring of
 // shared-memory stages, completion on mbarriers), warp 1 allocates TMEM and lane 0 issues
 // tcgen05.mma (two per K step: Xhi and Xlo; gate and up for SwiGLU) and tcgen05.commit,
-// warps 2..5 read the accumulator back with tcgen05.ld. K is split over blocks when the
-// weight tiles alone would not fill the GPU; each split writes its fp32 partial tile to a
-// workspace and the last split block of a tile (an arrival counter) adds them in split
-// order and applies the epilogue (plain, logit scale, or SwiGLU).
-//
+// warps 2..5 read the accumulator back with tcgen05.ld. K is split over the blocks of a
+// cluster when the weight tiles alone would not fill the GPU: once every block's MMAs are
+// done, each block pushes its partial sums of the step rows a rank owns into that rank's
+// shared memory (remote stores), and each rank adds the splits in split order and applies
+// the epilogue (plain, logit scale, or SwiGLU).
 // Every mbarrier wait is bounded: on expiry the block records an error code, stops
 // issuing work, waits (bounded) for its own copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -31,7 +31,6 @@ constexpr int TC_THREADS = 192;
 constexpr int BM = 128;  // weight rows per tile (MMA M)
 constexpr int BK = 64;   // K elements per stage (one 128-byte swizzle row)
 constexpr uint32_t WAIT_LIMIT = 1u << 20;
-constexpr int MAX_SPLITS = 8;  // K splits of a tile at most: one portable cluster
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -127,16 +126,13 @@ __device__ __forceinline__ uint32_t cluster_rank() {
   return r;
 }
 
-// float4 at a shared address of block `rank` of the cluster
-__device__ __forceinline__ float4 ld_cluster4(uint32_t local, uint32_t rank) {
+// float4 into shared memory at a local address of block `rank` of the cluster
+__device__ __forceinline__ void st_cluster4(uint32_t local, uint32_t rank, float4 v) {
   uint32_t remote;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(remote)
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(remote), "f"(v.x), "f"(v.y), "f"(v.z),
+               "f"(v.w)
                : "memory");
-  return v;
 }
 
 template <int BN, bool DUAL, int ST>
@@ -281,10 +277,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   pdl_trigger();
 
   // epilogue: warps 2..5, warp w reads TMEM lanes 32*(w % 4) ..
-  // With split K the blocks of a tile form a cluster: each parks its fp32 partial tile
-  // in its own (drained) stage memory as P[m][BN + 4] (gate, then up), and after a cluster
-  // barrier block r adds the splits' partials for its slice of the tile's rows over DSMEM.
-  constexpr int PS = BN + 4;  // padded row: conflict-free float4 stores
+  // With split K the blocks of a tile form a cluster; their stage memory (drained once every
+  // block's MMAs are done) receives the partial sums, see below.
   float *P = reinterpret_cast<float *>(smem_raw + (base - smem_u32(smem_raw)));
   const int tcount = (T - t0) < BN ? (T - t0) : BN;  // valid step rows in this tile
   auto epi = [&](float a, float b, int n) {
@@ -295,6 +289,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
     return a;
   };
+  bool good = false;  // this warp's accumulator is complete
   if (warp >= 2) {
     const int q = warp & 3;
     const int m = q * 32 + lane;  // row within the tile
@@ -306,58 +301,60 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
     if (threadIdx.x == 64) mark(5);
     fence_after();
-    if (ok && !failed) {
+    good = ok && !failed;
+    if (good && splits == 1) {
       for (int c = 0; c < BN; c += 16) {
         float v[16], u[16];
         tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + c, v);
         if (DUAL) tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + BN + c, u);
-        if (splits == 1) {
 #pragma unroll
-          for (int i = 0; i < 16; i++) {
-            const int t = c + i;
-            if (t < tcount && n < N) Y[(size_t)(t0 + t) * ldy + n] = epi(v[i], DUAL ? u[i] : 0.f, n);
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; i += 4) {
-            *reinterpret_cast<float4 *>(P + (size_t)m * PS + c + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-            if (DUAL)
-              *reinterpret_cast<float4 *>(P + (size_t)(BM + m) * PS + c + i) =
-                  make_float4(u[i], u[i + 1], u[i + 2], u[i + 3]);
-          }
+        for (int i = 0; i < 16; i++) {
+          const int t = c + i;
+          if (t < tcount && n < N) Y[(size_t)(t0 + t) * ldy + n] = epi(v[i], DUAL ? u[i] : 0.f, n);
         }
       }
     }
   }
   if (threadIdx.x == 64) mark(6);
   if (splits > 1) {
-    cluster_sync();  // every block's partial tile is in place
-    if (warp >= 2) {
-      const int q = warp & 3;
-      const int m = q * 32 + lane;
-      const int n = n0 + m;
-      const uint32_t rank = cluster_rank();
-      const int per = ((tcount + splits - 1) / splits + 3) & ~3;  // rows per block, whole float4s
-      const int ta = (int)rank * per, tb = min(tcount, ta + per);
-      const uint32_t pa = smem_u32(P + (size_t)m * PS), pu = smem_u32(P + (size_t)(BM + m) * PS);
-      for (int t = ta; t < tb; t += 4) {
-        // all splits' partials requested at once (one DSMEM round trip), added in split order
-        float4 xs[MAX_SPLITS], ys[MAX_SPLITS];
+    // Rank r of the cluster owns step rows [r * per, (r + 1) * per) of the tile. Every block
+    // pushes its partial sums of each rank's rows into that rank's receive buffer
+    // R[split][row m (gate, then up)][PL] with remote stores; the rank then adds the splits
+    // in split order from its own shared memory.
+    const int per = ((tcount + splits - 1) / splits + 3) & ~3;  // rows per rank, whole float4s
+    const int PL = per + 4;                                      // padded: conflict-free float4s
+    const uint32_t rank = cluster_rank();                        // = this block's split
+    cluster_sync();  // every block's MMAs are done: all stage memory may be overwritten
+    if (warp >= 2 && good) {
+      const int q = warp & 3, m = q * 32 + lane;
+      const uint32_t rg = smem_u32(P + ((size_t)rank * (DUAL ? 2 : 1) * BM + m) * PL);
+      const uint32_t ru = smem_u32(P + ((size_t)rank * 2 * BM + BM + m) * PL);
+      for (int c = 0; c < BN; c += 16) {
+        float v[16], u[16];
+        tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + c, v);
+        if (DUAL) tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + BN + c, u);
 #pragma unroll
-        for (int sp = 0; sp < MAX_SPLITS; sp++) {
-          if (sp < splits) {
-            xs[sp] = ld_cluster4(pa + t * 4, (uint32_t)sp);
-            if (DUAL) ys[sp] = ld_cluster4(pu + t * 4, (uint32_t)sp);
-          }
+        for (int g4 = 0; g4 < 16; g4 += 4) {
+          const int t = c + g4;
+          if (t >= tcount) break;
+          const uint32_t r = (uint32_t)(t / per), tt = (uint32_t)(t - (int)r * per);
+          st_cluster4(rg + tt * 4, r, make_float4(v[g4], v[g4 + 1], v[g4 + 2], v[g4 + 3]));
+          if (DUAL) st_cluster4(ru + tt * 4, r, make_float4(u[g4], u[g4 + 1], u[g4 + 2], u[g4 + 3]));
         }
+      }
+    }
+    cluster_sync();  // this rank's rows from every split are in place (nothing remote after)
+    if (warp >= 2) {
+      const int q = warp & 3, m = q * 32 + lane, n = n0 + m;
+      const int ta = (int)rank * per, tb = min(tcount, ta + per);
+      for (int t = ta; t < tb; t += 4) {
         float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
-#pragma unroll
-        for (int sp = 0; sp < MAX_SPLITS; sp++) {
-          if (sp < splits) {
-            a.x += xs[sp].x; a.y += xs[sp].y; a.z += xs[sp].z; a.w += xs[sp].w;
-            if (DUAL) {
-              b.x += ys[sp].x; b.y += ys[sp].y; b.z += ys[sp].z; b.w += ys[sp].w;
-            }
+        for (int sp = 0; sp < splits; sp++) {
+          const float4 x = *reinterpret_cast<const float4 *>(P + ((size_t)sp * (DUAL ? 2 : 1) * BM + m) * PL + (t - ta));
+          a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
+          if (DUAL) {
+            const float4 y = *reinterpret_cast<const float4 *>(P + ((size_t)sp * 2 * BM + BM + m) * PL + (t - ta));
+            b.x += y.x; b.y += y.y; b.z += y.z; b.w += y.w;
           }
         }
         if (n < N) {
@@ -368,7 +365,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
       }
     }
-    cluster_sync();  // no block leaves while another reads its shared memory
   }
   fence_before();
   __syncthreads();
@@ -396,7 +392,8 @@ cudaError_t tc_launch(const TcGemm &g, int T, int t_base, float *Y, int ldy, Epi
   const int t_tiles = (T + BN - 1) / BN;
   int splits = g.splits;
   // the partial tile of a split must fit the stage memory it reuses
-  if ((size_t)BM * (BN + 4) * 4 * (DUAL ? 2 : 1) > (size_t)ST * S::STAGE || t_tiles > 1) splits = 1;
+  const int per = ((BN + splits - 1) / splits + 3) & ~3;  // step rows a rank receives at most
+  if ((size_t)splits * (DUAL ? 2 : 1) * BM * (per + 4) * 4 > (size_t)ST * S::STAGE || t_tiles > 1) splits = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(m_tiles * splits, t_tiles);
   cfg.blockDim = dim3(TC_THREADS);
