@@ -95,17 +95,16 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
-  uint32_t r[16];
+// 16 columns of this warp's 32 TMEM lanes, without waiting (tmem_wait completes them)
+__device__ __forceinline__ void tmem_ld16_async(uint32_t taddr, uint32_t *r) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
         "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 16; i++) v[i] = __uint_as_float(r[i]);
 }
+
+__device__ __forceinline__ void tmem_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -289,6 +288,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
     return a;
   };
+  // accumulator columns read per round: all of a 64-column row (one wait for every load)
+  constexpr int RB = BN < 64 ? BN : 64;
+  auto read_row = [&](uint32_t lane_base, int c0, uint32_t *v, uint32_t *u) {
+#pragma unroll
+    for (int c = 0; c < RB; c += 16) {
+      tmem_ld16_async(lane_base + c0 + c, v + c);
+      if (DUAL) tmem_ld16_async(lane_base + BN + c0 + c, u + c);
+    }
+    tmem_wait();
+  };
   bool good = false;  // this warp's accumulator is complete
   if (warp >= 2) {
     const int q = warp & 3;
@@ -303,14 +312,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     fence_after();
     good = ok && !failed;
     if (good && splits == 1) {
-      for (int c = 0; c < BN; c += 16) {
-        float v[16], u[16];
-        tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + c, v);
-        if (DUAL) tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + BN + c, u);
+      for (int c0 = 0; c0 < BN; c0 += RB) {
+        uint32_t v[RB], u[DUAL ? RB : 1];
+        read_row(tmem + ((uint32_t)(q * 32) << 16), c0, v, u);
 #pragma unroll
-        for (int i = 0; i < 16; i++) {
-          const int t = c + i;
-          if (t < tcount && n < N) Y[(size_t)(t0 + t) * ldy + n] = epi(v[i], DUAL ? u[i] : 0.f, n);
+        for (int i = 0; i < RB; i++) {
+          const int t = c0 + i;
+          if (t < tcount && n < N)
+            Y[(size_t)(t0 + t) * ldy + n] = epi(__uint_as_float(v[i]), DUAL ? __uint_as_float(u[i]) : 0.f, n);
         }
       }
     }
@@ -329,17 +338,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const int q = warp & 3, m = q * 32 + lane;
       const uint32_t rg = smem_u32(P + ((size_t)rank * (DUAL ? 2 : 1) * BM + m) * PL);
       const uint32_t ru = smem_u32(P + ((size_t)rank * 2 * BM + BM + m) * PL);
-      for (int c = 0; c < BN; c += 16) {
-        float v[16], u[16];
-        tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + c, v);
-        if (DUAL) tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + BN + c, u);
+      for (int c0 = 0; c0 < BN; c0 += RB) {
+        uint32_t v[RB], u[DUAL ? RB : 1];
+        read_row(tmem + ((uint32_t)(q * 32) << 16), c0, v, u);
 #pragma unroll
-        for (int g4 = 0; g4 < 16; g4 += 4) {
-          const int t = c + g4;
+        for (int g4 = 0; g4 < RB; g4 += 4) {
+          const int t = c0 + g4;
           if (t >= tcount) break;
           const uint32_t r = (uint32_t)(t / per), tt = (uint32_t)(t - (int)r * per);
-          st_cluster4(rg + tt * 4, r, make_float4(v[g4], v[g4 + 1], v[g4 + 2], v[g4 + 3]));
-          if (DUAL) st_cluster4(ru + tt * 4, r, make_float4(u[g4], u[g4 + 1], u[g4 + 2], u[g4 + 3]));
+          st_cluster4(rg + tt * 4, r,
+                      make_float4(__uint_as_float(v[g4]), __uint_as_float(v[g4 + 1]), __uint_as_float(v[g4 + 2]),
+                                  __uint_as_float(v[g4 + 3])));
+          if (DUAL)
+            st_cluster4(ru + tt * 4, r,
+                        make_float4(__uint_as_float(u[g4]), __uint_as_float(u[g4 + 1]), __uint_as_float(u[g4 + 2]),
+                                    __uint_as_float(u[g4 + 3])));
         }
       }
     }
