@@ -936,7 +936,7 @@ int setup_tc(dory_t *d) {
     w.pair = pair;
     const int mt = (N + 127) / 128, nkb = K / 64;
     if (getenv("DORY_TC_TRACE") && !w.trace) {
-      if (cudaMalloc(&w.trace, (size_t)TC_TRACE_BLOCKS * 8 * 8) != cudaSuccess) {
+      if (cudaMalloc(&w.trace, (size_t)TC_TRACE_BLOCKS * TC_TRACE_EVENTS * 8) != cudaSuccess) {
         cudaGetLastError();
         w.trace = nullptr;
       }
@@ -1308,12 +1308,12 @@ int dory_destroy(dory_t *d) {
   if (!d) return DORY_OK;
   cudaStreamSynchronize(d->stream);
   if (const char *tp = getenv("DORY_TC_TRACE")) {
-    // file: records of int32 (layer, which, N, K, splits, blocks) then u64 [blocks][8]
+    // file: records of int32 (layer, which, N, K, splits, blocks) then u64 [blocks][TC_TRACE_EVENTS]
     if (FILE *f = fopen(tp, "wb")) {
       auto dump = [&](const TcW &w, int li, int which) {
         if (!w.trace || w.trace_grid <= 0) return;
         const int nb = std::min(w.trace_grid, TC_TRACE_BLOCKS);
-        std::vector<unsigned long long> t((size_t)nb * 8);
+        std::vector<unsigned long long> t((size_t)nb * TC_TRACE_EVENTS);
         if (cudaMemcpy(t.data(), w.trace, t.size() * 8, cudaMemcpyDeviceToHost) != cudaSuccess) return;
         const int32_t hdr[6] = {li, which, w.N, w.K, w.splits, nb};
         fwrite(hdr, 4, 6, f);

@@ -160,12 +160,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   __shared__ int is_last, failed;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // optional timeline: 0 start, 1 set up, 2 past the dependency wait, 3 first stage landed,
-  // 4 last MMA issued, 5 accumulator ready, 6 tile read out, 7 done
+  // 4 last MMA issued, 5 accumulator ready, 6 epilogue entered, 7 done; split K: 8 first
+  // cluster barrier passed, 9 partials pushed, 10 second barrier passed, 11 rows stored
   auto mark = [&](int e) {
     if (!trace) return;
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    trace[((size_t)blockIdx.y * gridDim.x + blockIdx.x) * 8 + e] = t;
+    trace[((size_t)blockIdx.y * gridDim.x + blockIdx.x) * TC_TRACE_EVENTS + e] = t;
   };
   if (threadIdx.x == 0) mark(0);
   const int tile = blockIdx.x / splits, split = blockIdx.x % splits;
@@ -334,6 +335,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int PL = per + 4;                                      // padded: conflict-free float4s
     const uint32_t rank = cluster_rank();                        // = this block's split
     cluster_sync();  // every block's MMAs are done: all stage memory may be overwritten
+    if (threadIdx.x == 64) mark(8);
     if (warp >= 2 && good) {
       const int q = warp & 3, m = q * 32 + lane;
       const uint32_t rg = smem_u32(P + ((size_t)rank * (DUAL ? 2 : 1) * BM + m) * PL);
@@ -356,7 +358,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
       }
     }
+    if (threadIdx.x == 64) mark(9);
     cluster_sync();  // this rank's rows from every split are in place (nothing remote after)
+    if (threadIdx.x == 64) mark(10);
     if (warp >= 2) {
       const int q = warp & 3, m = q * 32 + lane, n = n0 + m;
       const int ta = (int)rank * per, tb = min(tcount, ta + per);
@@ -378,6 +382,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
       }
     }
+    if (threadIdx.x == 64) mark(11);
   }
   fence_before();
   __syncthreads();

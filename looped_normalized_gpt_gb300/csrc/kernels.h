@@ -165,8 +165,9 @@ struct TcGemm {
   float *ws;                // split-K partial tiles
   int *ctr;                 // per-tile arrival counters (zero between launches)
   int *err;                 // set when a bounded wait expires
-  unsigned long long *trace;  // null, or [grid.y][grid.x][8] %globaltimer stamps per block
+  unsigned long long *trace;  // null, or [grid.y][grid.x][TC_TRACE_EVENTS] %globaltimer stamps
 };
+constexpr int TC_TRACE_EVENTS = 12;
 
 int tc_tile_rows(int T);
 int make_tmap_bf16(CUtensorMap *map, const void *base, long rows, long cols, int box_rows);
