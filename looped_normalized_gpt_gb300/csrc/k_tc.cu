@@ -152,7 +152,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmXh,
                    const __grid_constant__ CUtensorMap tmXl, int N, int K, int T, int t_base, int splits,
                    long pair_rows, float *__restrict__ ws, int *__restrict__ tile_ctr, float *__restrict__ Y, int ldy,
-                   EpiArgs ep, int *__restrict__ err, unsigned long long *__restrict__ trace) {
+                   EpiArgs ep, int *__restrict__ err, unsigned long long *__restrict__ trace, int late_trigger) {
   using S = TcSmem<BN, DUAL, ST>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_full[ST], bar_empty[ST], bar_acc;
@@ -274,7 +274,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   } else {
     pdl_wait();
   }
-  pdl_trigger();
+  if (!late_trigger) pdl_trigger();
 
   // epilogue: warps 2..5, warp w reads TMEM lanes 32*(w % 4) ..
   // With split K the blocks of a tile form a cluster; their stage memory (drained once every
@@ -394,7 +394,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   fence_after();
   if (warp == 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(S::TMEM_COLS) : "memory");
+  if (late_trigger) pdl_trigger();
   if (threadIdx.x == 64) mark(7);
+}
+
+// DORY_TC_TRIGGER=late: let the next kernel launch only once this one's epilogue is done
+int late_trigger() {
+  static const int v = [] {
+    const char *e = getenv("DORY_TC_TRIGGER");
+    return e && e[0] == 'l' ? 1 : 0;
+  }();
+  return v;
 }
 
 template <int BN, bool DUAL, int ST>
@@ -434,7 +444,7 @@ cudaError_t tc_launch(const TcGemm &g, int T, int t_base, float *Y, int ldy, Epi
   cfg.attrs = attr1;
   cfg.numAttrs = na;
   return cudaLaunchKernelEx(&cfg, kern, g.tmW, g.tmXh, g.tmXl, g.N, g.K, T, t_base, splits, g.pair_rows, g.ws,
-                            g.ctr, Y, ldy, ep, g.err, g.trace);
+                            g.ctr, Y, ldy, ep, g.err, g.trace, late_trigger());
 }
 
 }  // namespace
