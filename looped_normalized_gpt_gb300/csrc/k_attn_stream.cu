@@ -4,14 +4,17 @@
 // The window [max(p - W + 1, 0), p] is walked in tiles of 32 positions; a tile's K rows, V
 // rows and position tags are contiguous in the ring (capacities are whole multiples of 64)
 // and arrive with three bulk copies into one of three stages, completion on the stage's
-// mbarrier. Warp h takes query head h of the group (more heads than warps: h, h + 4, ...):
-// lane j scores key j (rotated chunk order, so the 32 lanes spread over the banks), then an
-// online softmax keeps the running max and sum, and the value sum runs with lane l owning
-// hd/32 dims and the weights broadcast by shuffles. A stage is refilled once every warp has
-// left it (an arrival per warp on the stage's second mbarrier). The output y / l is gated,
-// y * sigmoid(g * s_g^2), into z; the row norm follows in its own kernel. With two blocks
-// per SM about 190 KB of K/V are in flight per SM. Waits are bounded; on expiry the block
-// sets error 7, lets its copies land and returns.
+// mbarrier. Warp w takes positions 8w .. 8w + 7 of every tile for all REP query heads of the
+// group, lane l holding dims [l * HD/32, (l + 1) * HD/32) of q (in registers) and of the
+// value sums. A position's K row and V row are each read from shared memory once, as one
+// vector load per lane: the lane's partial dot products (8 positions x REP heads) are summed
+// across the warp by a transpose reduction (recursive halving: at each step a lane keeps half
+// of its values and adds its partner's copy of them), after which each lane holds one
+// (head, position) score. Each warp keeps its own online softmax per head (running max, sum
+// and value sums); the four warps' states are merged at the end. The last warp to leave a
+// stage refills it with the tile three ahead, so no warp waits to issue copies. The output
+// y / l is gated, y * sigmoid(g * s_g^2), into z; the row norm follows in its own kernel.
+// Waits are bounded; on expiry the block sets error 7, lets its copies land and returns.
 #include <climits>
 
 #include "async.cuh"
@@ -23,7 +26,8 @@ namespace dory {
 namespace {
 
 constexpr int AS_WARPS = 4;
-constexpr int AS_KEYS = 32;   // positions per tile
+constexpr int AS_KEYS = 32;                   // positions per tile
+constexpr int AS_KW = AS_KEYS / AS_WARPS;     // positions per warp per tile
 constexpr int AS_STAGES = 3;
 constexpr int ERR_STREAM = 7;
 
@@ -34,16 +38,53 @@ struct StreamSmem {
   static constexpr int TOTAL = AS_STAGES * STAGE + 128;      // + alignment slack
 };
 
+template <int DPL>
+__device__ __forceinline__ void ld_vec(const float *p, float (&v)[DPL]) {
+  if constexpr (DPL == 4) {
+    const float4 t = *reinterpret_cast<const float4 *>(p);
+    v[0] = t.x, v[1] = t.y, v[2] = t.z, v[3] = t.w;
+  } else {
+    const float2 t = *reinterpret_cast<const float2 *>(p);
+    v[0] = t.x, v[1] = t.y;
+  }
+}
+
+// Sum NV per-lane values (NV a power of two, at most 32) over the warp. Afterwards every lane
+// holds the total of value index lane / (32 / NV); the 32 / NV lanes sharing an index hold
+// the same total.
+template <int NV>
+__device__ __forceinline__ float transpose_sum(float (&v)[NV], int lane) {
+#pragma unroll
+  for (int cnt = NV, o = 16; cnt > 1; cnt >>= 1, o >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < cnt / 2; i++) {
+      const float send = up ? v[i] : v[i + cnt / 2];
+      const float keep = up ? v[i + cnt / 2] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+  float s = v[0];
+#pragma unroll
+  for (int o = 16 / NV; o >= 1; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  return s;
+}
+
 template <int HD, int REP>
 __global__ void __launch_bounds__(AS_WARPS * 32) attn_stream_kernel(const float *__restrict__ qkvg, int ldq, Dims d,
                                                                     Rows rows, Ring ring, const float *__restrict__ sg,
                                                                     float *__restrict__ z, int *err) {
-  constexpr int NV = HD / 32, NC = HD / 4;
+  constexpr int DPL = HD / 32;                                // dims per lane
+  constexpr int NV = REP * AS_KW < 32 ? REP * AS_KW : 32;     // partial scores reduced together
+  constexpr int NCH = REP * AS_KW / NV;                       // chunks of heads
+  constexpr int HC = NV / AS_KW;                              // heads per chunk
+  constexpr int LPI = 32 / NV;                                // lanes holding one reduced score
+  constexpr int GRP = AS_KW * LPI;                            // lanes holding one head's scores
   using S = StreamSmem<HD>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~(uintptr_t)127);
-  __shared__ __align__(8) uint64_t full[AS_STAGES], empty[AS_STAGES];
-  __shared__ __align__(16) float qs[REP][HD];
+  __shared__ __align__(8) uint64_t full[AS_STAGES];
+  __shared__ int done[AS_STAGES], hi;
   __shared__ volatile int stop;
   const int r = blockIdx.x / d.nk, kh = blockIdx.x % d.nk;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -69,28 +110,34 @@ __global__ void __launch_bounds__(AS_WARPS * 32) attn_stream_kernel(const float 
   if (threadIdx.x == 0) {
     for (int s = 0; s < AS_STAGES; s++) {
       mbar_init(smem_addr(&full[s]), 1);
-      mbar_init(smem_addr(&empty[s]), AS_WARPS);
+      done[s] = 0;
     }
     mbar_fence_init();
     stop = 0;
-    for (int t = 0; t < AS_STAGES && t < ntiles; t++) issue(t);
+    hi = ntiles < AS_STAGES ? ntiles : AS_STAGES;
+    for (int t = 0; t < hi; t++) issue(t);
   }
-  for (int i = threadIdx.x; i < REP * HD; i += blockDim.x)
-    qs[i / HD][i % HD] = qkvg[(size_t)r * ldq + (size_t)kh * REP * HD + i];
+  // this kv head's query heads, pre-scaled by 1/sqrt(hd); lane l holds dims l*DPL ..
+  const float scale = 1.f / sqrtf((float)HD);
+  float q[REP][DPL];
+#pragma unroll
+  for (int h = 0; h < REP; h++) {
+    float t[DPL];
+    ld_vec<DPL>(qkvg + (size_t)r * ldq + (size_t)(kh * REP + h) * HD + lane * DPL, t);
+#pragma unroll
+    for (int i = 0; i < DPL; i++) q[h][i] = t[i] * scale;
+  }
   __syncthreads();
 
-  const float scale = 1.f / sqrtf((float)HD);
-  float m[(REP + AS_WARPS - 1) / AS_WARPS], l[(REP + AS_WARPS - 1) / AS_WARPS];
-  float acc[(REP + AS_WARPS - 1) / AS_WARPS][NV];
+  float m[REP], l[REP], acc[REP][DPL];
 #pragma unroll
-  for (int u = 0; u < (REP + AS_WARPS - 1) / AS_WARPS; u++) {
-    m[u] = -INFINITY;
-    l[u] = 0.f;
+  for (int h = 0; h < REP; h++) {
+    m[h] = -INFINITY;
+    l[h] = 0.f;
 #pragma unroll
-    for (int i = 0; i < NV; i++) acc[u][i] = 0.f;
+    for (int i = 0; i < DPL; i++) acc[h][i] = 0.f;
   }
-  int issued = ntiles < AS_STAGES ? ntiles : AS_STAGES;
-  bool ok = true;
+  const int own_k = (lane / LPI) % AS_KW, own_hc = lane / GRP;  // the (position, head) a lane scores
   for (int t = 0; t < ntiles; t++) {
     const int s = t % AS_STAGES;
     if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&full[s]), (t / AS_STAGES) & 1, &stop))) {
@@ -98,90 +145,126 @@ __global__ void __launch_bounds__(AS_WARPS * 32) attn_stream_kernel(const float 
         stop = 1;
         atomicExch(err, ERR_STREAM);
       }
-      ok = false;
       break;
     }
-    const float *Kt = reinterpret_cast<const float *>(base + (size_t)s * S::STAGE);
+    const float *Kt = reinterpret_cast<const float *>(base + (size_t)s * S::STAGE) + warp * AS_KW * HD;
     const float *Vt = Kt + AS_KEYS * HD;
-    const int32_t *tags = reinterpret_cast<const int32_t *>(Vt + AS_KEYS * HD);
-    const long pe = (t0 + t) * AS_KEYS + lane;
-    const bool valid = pe >= lo && pe <= p && tags[lane] == (int32_t)pe;
+    const int32_t *tags = reinterpret_cast<const int32_t *>(base + (size_t)s * S::STAGE + 2 * S::TILE);
+    const int j = warp * AS_KW + own_k;
+    const long pe = (t0 + t) * AS_KEYS + j;
+    const bool valid = pe >= lo && pe <= p && tags[j] == (int32_t)pe;
+    float e[NCH], fold[REP];
 #pragma unroll
-    for (int u = 0; u < (REP + AS_WARPS - 1) / AS_WARPS; u++) {
-      const int h = warp + u * AS_WARPS;
-      if (h >= REP) break;
-      float2 s2 = make_float2(0.f, 0.f);
-      if (valid) {
-        const float4 *kr = reinterpret_cast<const float4 *>(Kt + lane * HD);
-        const float4 *q4 = reinterpret_cast<const float4 *>(qs[h]);
-#pragma unroll 8
-        for (int c = 0; c < NC; c++) {
-          const int cc = (c + lane) & (NC - 1);
-          const float4 k = kr[cc], q = q4[cc];
-          s2 = ffma2(make_float2(q.y, q.w), make_float2(k.y, k.w), s2);
-          s2 = ffma2(make_float2(q.x, q.z), make_float2(k.x, k.z), s2);
+    for (int c = 0; c < NCH; c++) {
+      float part[NV];
+#pragma unroll
+      for (int k = 0; k < AS_KW; k++) {
+        float kv[DPL];
+        ld_vec<DPL>(Kt + k * HD + lane * DPL, kv);
+#pragma unroll
+        for (int hc = 0; hc < HC; hc++) {
+          float2 s2 = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int i = 0; i < DPL; i += 2)
+            s2 = ffma2(make_float2(q[c * HC + hc][i], q[c * HC + hc][i + 1]), make_float2(kv[i], kv[i + 1]), s2);
+          part[hc * AS_KW + k] = s2.x + s2.y;
         }
       }
-      const float sc = valid ? (s2.x + s2.y) * scale : -INFINITY;
-      const float mt = warp_max(sc);
-      const float mn = fmaxf(m[u], mt);
-      if (mn == -INFINITY) continue;  // nothing valid yet (warp-uniform)
-      const float fold = m[u] == -INFINITY ? 0.f : expf(m[u] - mn);
-      const float e = sc == -INFINITY ? 0.f : expf(sc - mn);
-      l[u] = l[u] * fold + warp_sum(e);
-      m[u] = mn;
-      float a0[NV], a1[NV];
+      float sc = transpose_sum<NV>(part, lane);
+      sc = valid ? sc : -INFINITY;
+      float tm = sc;  // this head's maximum over the warp's positions
 #pragma unroll
-      for (int i = 0; i < NV; i++) {
-        a0[i] = acc[u][i] * fold;
-        a1[i] = 0.f;
+      for (int o = LPI; o < GRP; o <<= 1) tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, o));
+      float mown = -INFINITY;
+#pragma unroll
+      for (int hc = 0; hc < HC; hc++) {
+        const int h = c * HC + hc;
+        const float mn = fmaxf(m[h], __shfl_sync(0xffffffffu, tm, hc * GRP));
+        fold[h] = m[h] == -INFINITY ? 0.f : expf(m[h] - mn);
+        m[h] = mn;
+        if (hc == own_hc) mown = mn;
       }
-#pragma unroll 4
-      for (int j = 0; j < AS_KEYS; j += 2) {
-        const float w0 = __shfl_sync(0xffffffffu, e, j), w1 = __shfl_sync(0xffffffffu, e, j + 1);
-        const float *v0 = Vt + j * HD + lane * NV, *v1 = v0 + HD;
+      e[c] = sc == -INFINITY ? 0.f : expf(sc - mown);
+      float gs = e[c];
 #pragma unroll
-        for (int i = 0; i < NV; i += 2) {
-          const float2 r0 = ffma2(make_float2(w0, w0), make_float2(v0[i], v0[i + 1]), make_float2(a0[i], a0[i + 1]));
-          const float2 r1 = ffma2(make_float2(w1, w1), make_float2(v1[i], v1[i + 1]), make_float2(a1[i], a1[i + 1]));
-          a0[i] = r0.x;
-          a0[i + 1] = r0.y;
-          a1[i] = r1.x;
-          a1[i + 1] = r1.y;
-        }
+      for (int o = LPI; o < GRP; o <<= 1) gs += __shfl_xor_sync(0xffffffffu, gs, o);
+#pragma unroll
+      for (int hc = 0; hc < HC; hc++) {
+        const int h = c * HC + hc;
+        l[h] = l[h] * fold[h] + __shfl_sync(0xffffffffu, gs, hc * GRP);
       }
-#pragma unroll
-      for (int i = 0; i < NV; i++) acc[u][i] = a0[i] + a1[i];
     }
+#pragma unroll
+    for (int h = 0; h < REP; h++)
+#pragma unroll
+      for (int i = 0; i < DPL; i++) acc[h][i] *= fold[h];
+#pragma unroll
+    for (int k = 0; k < AS_KW; k++) {
+      float vv[DPL];
+      ld_vec<DPL>(Vt + k * HD + lane * DPL, vv);
+#pragma unroll
+      for (int c = 0; c < NCH; c++)
+#pragma unroll
+        for (int hc = 0; hc < HC; hc++) {
+          const int h = c * HC + hc;
+          const float w = __shfl_sync(0xffffffffu, e[c], (hc * AS_KW + k) * LPI);
+#pragma unroll
+          for (int i = 0; i < DPL; i += 2) {
+            const float2 a = ffma2(make_float2(w, w), make_float2(vv[i], vv[i + 1]), make_float2(acc[h][i], acc[h][i + 1]));
+            acc[h][i] = a.x;
+            acc[h][i + 1] = a.y;
+          }
+        }
+    }
+    // the last warp to leave the stage refills it with the tile three ahead
     __syncwarp();
-    if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
-    // thread 0 refills the stage once every warp has left it
-    if (threadIdx.x == 0 && issued < ntiles) {
-      if (!mbar_wait(smem_addr(&empty[s]), (t / AS_STAGES) & 1, &stop)) {
-        stop = 1;
-        atomicExch(err, ERR_STREAM);
-      } else {
-        issue(issued);
-        issued++;
+    if (lane == 0) {
+      __threadfence_block();
+      if (atomicAdd(&done[s], 1) == AS_WARPS * (t / AS_STAGES + 1) - 1 && t + AS_STAGES < ntiles && !stop) {
+        __threadfence_block();
+        atomicMax(&hi, t + AS_STAGES + 1);
+        issue(t + AS_STAGES);
       }
     }
   }
-  // copies in flight land before the block may exit
+  __syncthreads();
+  // copies in flight land before the stage memory is reused or the block exits
   if (threadIdx.x == 0)
-    for (int t = issued - AS_STAGES < 0 ? 0 : issued - AS_STAGES; t < issued; t++)
+    for (int t = hi - AS_STAGES < 0 ? 0 : hi - AS_STAGES; t < hi; t++)
       mbar_wait(smem_addr(&full[t % AS_STAGES]), (t / AS_STAGES) & 1);
-  if (!ok || stop) return;
-  const float *g = qkvg + (size_t)r * ldq + (size_t)(d.nh + 2 * d.nk) * HD;
+  __syncthreads();
+  if (stop) return;
+
+  // merge the warps' softmax states: m, l per (warp, head), then the value sums
+  float *ms = reinterpret_cast<float *>(base), *ls = ms + AS_WARPS * REP, *as = ls + AS_WARPS * REP;
+  if (lane == 0)
 #pragma unroll
-  for (int u = 0; u < (REP + AS_WARPS - 1) / AS_WARPS; u++) {
-    const int h = warp + u * AS_WARPS;
-    if (h >= REP) break;
-    const float inv = l[u] > 0.f ? 1.f / l[u] : 0.f;
-#pragma unroll
-    for (int i = 0; i < NV; i++) {
-      const int col = (kh * REP + h) * HD + lane * NV + i;
-      z[(size_t)r * d.nh * HD + col] = acc[u][i] * inv * sigmoidf_(g[col] * sg[col]);
+    for (int h = 0; h < REP; h++) {
+      ms[warp * REP + h] = m[h];
+      ls[warp * REP + h] = l[h];
     }
+#pragma unroll
+  for (int h = 0; h < REP; h++)
+#pragma unroll
+    for (int i = 0; i < DPL; i++) as[(warp * REP + h) * HD + lane * DPL + i] = acc[h][i];
+  __syncthreads();
+  const float *g = qkvg + (size_t)r * ldq + (size_t)(d.nh + 2 * d.nk) * HD;
+  for (int o = threadIdx.x; o < REP * HD; o += blockDim.x) {
+    const int h = o / HD, dd = o % HD;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < AS_WARPS; w++) M = fmaxf(M, ms[w * REP + h]);
+    float num = 0.f, den = 0.f;
+#pragma unroll
+    for (int w = 0; w < AS_WARPS; w++) {
+      const float mw = ms[w * REP + h];
+      if (mw == -INFINITY) continue;
+      const float f = expf(mw - M);
+      num += f * as[(w * REP + h) * HD + dd];
+      den += f * ls[w * REP + h];
+    }
+    const int col = (kh * REP + h) * HD + dd;
+    z[(size_t)r * d.nh * HD + col] = (den > 0.f ? num / den : 0.f) * sigmoidf_(g[col] * sg[col]);
   }
 }
 

@@ -281,11 +281,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   // block's MMAs are done) receives the partial sums, see below.
   float *P = reinterpret_cast<float *>(smem_raw + (base - smem_u32(smem_raw)));
   const int tcount = (T - t0) < BN ? (T - t0) : BN;  // valid step rows in this tile
-  auto epi = [&](float a, float b, int n) {
-    if (ep.mode == EPI_SCALE) return a * ep.vec[n];
-    if (ep.mode == EPI_SILU) {
-      const float g = a * ep.vec[n];
-      return g * sigmoidf_(g) * (b * ep.vec2[n]);
+  // A thread's output column n is fixed, so its scales are read once, before any Y store (which
+  // the compiler would otherwise have to assume may overwrite them).
+  float sv1 = 1.f, sv2 = 1.f;
+  if (warp >= 2 && n0 + (warp & 3) * 32 + lane < N) {
+    const int n = n0 + (warp & 3) * 32 + lane;
+    if (ep.mode != EPI_STORE) sv1 = __ldg(ep.vec + n);
+    if (ep.mode == EPI_SILU) sv2 = __ldg(ep.vec2 + n);
+  }
+  const int mode = ep.mode;
+  auto epi = [&](float a, float b, int) {
+    if (mode == EPI_SCALE) return a * sv1;
+    if (mode == EPI_SILU) {
+      const float g = a * sv1;
+      return g * sigmoidf_(g) * (b * sv2);
     }
     return a;
   };

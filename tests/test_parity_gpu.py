@@ -300,7 +300,7 @@ def test_head_width_128_rings_with_tile_copies(kv_quant):
         P.close()
 
 
-@pytest.mark.parametrize("hd,nh,nk", [(64, 8, 2), (128, 4, 2)])
+@pytest.mark.parametrize("hd,nh,nk", [(64, 8, 2), (128, 4, 2), (64, 8, 8), (128, 8, 1), (64, 8, 1), (128, 4, 4)])
 def test_batched_decode_streams_each_window(hd, nh, nk):
     """Six sequences with different context lengths (per_loop holes from changing loop
     counts): a step of 6 rows takes the streaming attention (one block per row and kv head)."""
