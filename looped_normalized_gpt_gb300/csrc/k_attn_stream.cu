@@ -82,7 +82,7 @@ __global__ void __launch_bounds__(AS_WARPS * 32) attn_stream_kernel(const float 
   constexpr int GRP = AS_KW * LPI;                            // lanes holding one head's scores
   using S = StreamSmem<HD>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~(uintptr_t)127);
+  uint8_t *base = smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u);  // stays a shared-space pointer
   __shared__ __align__(8) uint64_t full[AS_STAGES];
   __shared__ int done[AS_STAGES], hi;
   __shared__ volatile int stop;

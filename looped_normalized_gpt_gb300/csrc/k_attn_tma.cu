@@ -52,7 +52,7 @@ __global__ void __launch_bounds__(128) attn_tma_kernel(const __grid_constant__ C
   constexpr int HD = NV * 32;
   constexpr int NB = HD / 32;  // column boxes per tile
   extern __shared__ uint8_t smem_raw[];
-  float *Ks = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  float *Ks = reinterpret_cast<float *>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
   float *Vs = Ks + NB * AB * 32;
   __shared__ float qs[REP][HD];
   __shared__ float ps[REP][AB];
@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(128) attn_tma_q8_kernel(const __grid_constant_
                                                           int *counters, int *err) {
   constexpr int HD = 128;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t *Kq = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint8_t *Kq = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t *Vq = Kq + AB * HD;
   float *Ksc = reinterpret_cast<float *>(Vq + AB * HD);  // [64][4]
   float *Vsc = Ksc + AB * 4;                             // [64]

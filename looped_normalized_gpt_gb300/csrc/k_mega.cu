@@ -679,7 +679,7 @@ template <int HD>
 // 9 warps: at most 3 on an SM sub-partition, so at most 168 registers a thread
 __global__ void __launch_bounds__(MTHREADS, 1) mega_decode_kernel(const __grid_constant__ MegaArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint8_t *ring = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);  // stays a shared-space pointer
   float *work = reinterpret_cast<float *>(ring + (size_t)NS * SLOT);
   __shared__ __align__(8) uint64_t full[NS], empty[NS], abar;
   __shared__ __align__(16) float qs[8][HD];
