@@ -13,6 +13,15 @@ constexpr uint32_t MBAR_WAIT_LIMIT = 1u << 20;
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
+// The same shared-memory address as a pointer the compiler can see is in shared memory. A
+// pointer handed across a call that is not inlined arrives generic, and loads and stores
+// through it take the generic path; rebuilt from the shared window's base it is shared again.
+template <typename T>
+__device__ __forceinline__ T *in_shared(T *p) {
+  extern __shared__ uint8_t dyn_smem_base[];
+  return reinterpret_cast<T *>(dyn_smem_base + ((int)smem_addr(p) - (int)smem_addr(dyn_smem_base)));
+}
+
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }

@@ -113,6 +113,7 @@ struct dory_handle {
   std::string mega_trace_path;
   std::vector<int32_t> mega_trace_desc;  // kind, N, K per stage of the last traced step
   int mega_prefetch = 0;  // L2 lead of the kernel's weight stream, bytes per block (DORY_MEGA_PREFETCH)
+  int mega_inflight = 0;  // cap on a block's weight copies in flight (DORY_MEGA_INFLIGHT)
   // tensor-core projections: weight maps per layer ([0] q/k/v/g or gate/up, [1] o or down)
   bool tc_ok = false;
   std::vector<std::array<TcW, 2>> tcw;
@@ -788,6 +789,7 @@ int issue_mega(dory_t *d, const StepArgs &a, int32_t *rt, const MegaStage *stage
   m.adv_cnt = a.acnt[0];
   m.trace = (size_t)nstages <= d->mega_trace_stages ? d->mega_trace : nullptr;
   m.prefetch_ahead = d->mega_prefetch;
+  m.max_inflight = d->mega_inflight;
   CK(launch_mega_decode(m, d->sms, s));
   return DORY_OK;
 }
@@ -1254,6 +1256,7 @@ int dory_create(const dory_config *cfg, const dory_weights *w, void *stream, dor
     if (e && e[0] == '0') ok = false;
     d->mega_ok = ok && mega_supported(dm.hd, d->sms);
     if (const char *pe = getenv("DORY_MEGA_PREFETCH")) d->mega_prefetch = std::max(0, atoi(pe));
+    if (const char *pe = getenv("DORY_MEGA_INFLIGHT")) d->mega_inflight = std::max(0, atoi(pe));
     const char *tp = getenv("DORY_MEGA_TRACE");
     if (d->mega_ok && tp && tp[0]) {
       const size_t stages = (size_t)3 * (cfg->n_in + cfg->max_loops * cfg->n_rec + cfg->n_out) + 2;

@@ -8,14 +8,15 @@
 // and copies chunks into a ring of shared-memory slots with cp.async.bulk, completion on one
 // mbarrier per slot. It never waits for activations, so HBM keeps streaming the next stages'
 // weights while the consumers wait at a grid barrier or run attention. Warps 1..8 are the
-// consumers; they take the chunks in order, all of them on each chunk (so a slot's barrier
-// is always awaited for the phase right after the one last seen). Per stage the consumers
+// consumers; each of them awaits every chunk in order and frees it with its own arrival (so
+// a slot's barrier is always awaited for the phase right after the one last seen). Per
+// stage the consumers
 //   * copy the stage's descriptor into shared memory while their first thread waits until
 //     every block has finished the stage before (a counter in global memory);
 //   * GEMV: build the input row in shared memory (the embedding, a row norm, or the nGPT
-//     residual with the loop mix), then reduce each chunk against it (bf16 weights, f32
-//     sums; a thread per 16-byte column, shuffles and shared memory across the columns),
-//     free the slot and apply the epilogue (SwiGLU, logit scale);
+//     residual with the loop mix), then take the rows a warp each (bf16 weights, f32 sums;
+//     lanes split the row into 16-byte columns, one transpose reduction per 8 rows of a
+//     warp) and apply the epilogue (SwiGLU, logit scale) as the sums come out;
 //   * attention (dory.rs fn attn_layer), in items of 32 positions of one kv head: the K and
 //     V rows of an item are contiguous in the ring and arrive with two bulk copies; meanwhile
 //     warp h rotates and normalises query head h of the group from the raw projection row
@@ -45,6 +46,7 @@ constexpr int MTHREADS = 32 * (MW + 1);           // and the producer warp
 constexpr int NS = 7;                             // weight slots
 constexpr uint32_t SLOT = 26 * 1024;              // bytes per slot
 constexpr int RMAX = 8;                           // rows (or row pairs) per chunk at most
+static_assert(RMAX <= MW, "a chunk holds at most one row of each consumer warp");
 constexpr int EPI_ROWS = 256;                     // a block's rows of one GEMV at most
 constexpr uint32_t WORK = 32 * 1024;              // input row, or attention tiles and merge scratch
 constexpr int AK = MEGA_AK;                       // positions per attention item
@@ -184,6 +186,14 @@ __device__ void produce(const MegaArgs &a, uint8_t *ring, uint64_t *full, uint64
       ok = false;
       break;
     }
+    // with a cap on copies in flight, the copy max_inflight back lands first: bytes queued
+    // beyond what keeps HBM busy only delay the step's latency-bound loads
+    const int back = c - a.max_inflight;
+    if (a.max_inflight > 0 && a.max_inflight < NS && back >= 0 &&
+        !mbar_wait(smem_addr(&full[back % NS]), (back / NS) & 1, &ctl.abort)) {
+      ok = false;
+      break;
+    }
     if (cp.s != marked) {
       tr.mark(cp.s, 5);
       marked = cp.s;
@@ -242,23 +252,27 @@ __device__ __forceinline__ int sum_slot(int lane) {
   return e;
 }
 
-// A stage's chunks, each reduced by the whole team in order: thread t owns the 16-byte
-// columns t, t + 256, ... (SEG of them) of every row, keeps its input values for them in
-// registers, sums its columns of the chunk's rows (and of the up rows, DUAL), the warps
-// reduce their rows with shuffles, and the warps' partial sums meet in shared memory `red`
-// (two buffers, alternating by chunk). The slot is freed as soon as the partials are out
-// of it. `st` is the stage's copy in shared memory.
-template <int SEG, bool DUAL>
-__device__ void gemv_chunks(const WarpTeam &tm, const MegaStage &st, int rb, int re, int c0, const uint8_t *ring,
-                            uint64_t *full, uint64_t *empty, const float *xs, float (*red)[MW][2 * RMAX],
-                            const float (*epi)[EPI_ROWS], Ctl &ctl, int *err, const Tracer &tr, int s) {
-  const int t = tm.tid(), lane = threadIdx.x & 31, cw = tm.warp();
+// A stage's rows, a warp per row: warp w of the team takes the block's rows w, w + MW, ...
+// (pairs of gate and up rows, DUAL). Its lanes split a row into 16-byte columns (lane l:
+// columns l, l + 32, ...) and multiply them with the input row, which a lane keeps in
+// registers when it has at most 8 columns (XR of them) and otherwise reads from shared
+// memory (XR = 0). Every 8 rows of a warp one transpose reduction gives their sums, which
+// lanes 0, 4, .., 28 scale and store. A chunk holds at most one row of each warp (R <= MW).
+// Every warp awaits every chunk of the stage and frees it with its own arrival (MW per
+// slot), so no team barrier runs inside the loop; since a warp frees a chunk only after it
+// has landed, its arrivals always fall in the slot's current phase.
+template <int XR, bool DUAL>
+__device__ void gemv_rows(const WarpTeam &tm, const MegaStage &st, int rb, int re, int c0, const uint8_t *ring,
+                          uint64_t *full, uint64_t *empty, const float *xs, const float (*epi)[EPI_ROWS], Ctl &ctl,
+                          int *err, const Tracer &tr, int s) {
+  const int lane = threadIdx.x & 31, cw = tm.warp();
   const int K = st.K, R = st.R, mode = st.ep.mode, nu = K / 8;  // 16-byte columns per row
   float *__restrict__ Y = st.Y;
-  float xr[8 * SEG];
+  constexpr int XN = XR > 0 ? 8 * XR : 1;
+  float xr[XN];
 #pragma unroll
-  for (int g = 0; g < SEG; g++) {
-    const int u = t + g * 32 * MW;
+  for (int g = 0; g < XR; g++) {
+    const int u = lane + 32 * g;
     float4 p = make_float4(0.f, 0.f, 0.f, 0.f), q = p;
     if (u < nu) {
       p = *reinterpret_cast<const float4 *>(xs + u * 8);
@@ -267,80 +281,99 @@ __device__ void gemv_chunks(const WarpTeam &tm, const MegaStage &st, int rb, int
     xr[8 * g + 0] = p.x; xr[8 * g + 1] = p.y; xr[8 * g + 2] = p.z; xr[8 * g + 3] = p.w;
     xr[8 * g + 4] = q.x; xr[8 * g + 5] = q.y; xr[8 * g + 6] = q.z; xr[8 * g + 7] = q.w;
   }
-  const int nch = re > rb ? (re - rb + R - 1) / R : 0;
+  // a 16-byte column of weights against the input row: two chains of paired FMAs
+  auto dot8 = [&](const uint4 &wq, int g, int u, float2 &a0, float2 &a1) {
+    float wv[8];
+    unpack8(wq, wv);
+    float x[8];
+    if (XR > 0) {
+#pragma unroll
+      for (int e = 0; e < 8; e++) x[e] = xr[(8 * g + e) % XN];
+    } else {
+      const float4 p = *reinterpret_cast<const float4 *>(xs + u * 8), q = *reinterpret_cast<const float4 *>(xs + u * 8 + 4);
+      x[0] = p.x; x[1] = p.y; x[2] = p.z; x[3] = p.w; x[4] = q.x; x[5] = q.y; x[6] = q.z; x[7] = q.w;
+    }
+    a0 = ffma2(make_float2(wv[0], wv[1]), make_float2(x[0], x[1]), a0);
+    a1 = ffma2(make_float2(wv[2], wv[3]), make_float2(x[2], x[3]), a1);
+    a0 = ffma2(make_float2(wv[4], wv[5]), make_float2(x[4], x[5]), a0);
+    a1 = ffma2(make_float2(wv[6], wv[7]), make_float2(x[6], x[7]), a1);
+  };
+  const int n = re - rb;  // rows (pairs) of this block
+  const int nch = n > 0 ? (n + R - 1) / R : 0;
+  float pg[8], pu[8];
+#pragma unroll
+  for (int k = 0; k < 8; k++) pg[k] = pu[k] = 0.f;
+  int nb = 0, jb = cw;  // rows in the current batch, and its first row
   tr.zero(s);
-  for (int i = 0; i < nch; i++) {
-    const int c = c0 + i, sl = c % NS;  // chunk indices run over the whole step
+  for (int x = 0; x < nch; x++) {
+    const int c = c0 + x, sl = c % NS;
     long long t0 = tr.clk();
     const bool landed = mbar_wait(smem_addr(&full[sl]), (c / NS) & 1, &ctl.abort);
     long long t1 = tr.clk();
     tr.add(s, 8, t1 - t0);
-    if (!landed) flag_error(ctl, err);  // the block stops at the stage's end; the slot stays taken
-    if (i == 0) tr.mark(s, 7);
-    const int r0 = rb + i * R, nr = min(R, re - r0);
-    const uint4 *w = reinterpret_cast<const uint4 *>(ring + (size_t)sl * SLOT);
-    float acc[2 * RMAX];  // [0, RMAX): rows; [RMAX, 2 RMAX): up rows (DUAL)
+    if (!landed && lane == 0) flag_error(ctl, err);  // the block stops at the stage's end
+    if (x == 0) tr.mark(s, 7);
+    const int r0 = x * R, nr = min(R, n - r0);
+    const int jr = r0 + (((cw - r0) % MW) + MW) % MW;  // this warp's row in the chunk, if any
+    const bool mine = jr < r0 + nr;
+    if (mine) {
+      float2 a0 = make_float2(0.f, 0.f), a1 = a0, b0 = a0, b1 = a0;
+      if (landed) {
+        const uint4 *wg = reinterpret_cast<const uint4 *>(ring + (size_t)sl * SLOT) + (size_t)(jr - r0) * nu;
+        const uint4 *wu = wg + (size_t)nr * nu;
+        if (XR > 0) {
 #pragma unroll
-    for (int r = 0; r < RMAX; r++) {
-      float2 a = make_float2(0.f, 0.f), bb = a;  // even and odd columns
-      if (r < nr && landed) {
-#pragma unroll
-        for (int g = 0; g < SEG; g++) {
-          const int u = t + g * 32 * MW;
-          if (u < nu) {
-            float wv[8];
-            unpack8(w[r * nu + u], wv);
-#pragma unroll
-            for (int e = 0; e < 8; e += 2)
-              a = ffma2(make_float2(wv[e], wv[e + 1]), make_float2(xr[8 * g + e], xr[8 * g + e + 1]), a);
-            if (DUAL) {
-              unpack8(w[(nr + r) * nu + u], wv);
-#pragma unroll
-              for (int e = 0; e < 8; e += 2)
-                bb = ffma2(make_float2(wv[e], wv[e + 1]), make_float2(xr[8 * g + e], xr[8 * g + e + 1]), bb);
+          for (int g = 0; g < XR; g++) {
+            const int u = lane + 32 * g;
+            if (u < nu) {
+              dot8(wg[u], g, u, a0, a1);
+              if (DUAL) dot8(wu[u], g, u, b0, b1);
             }
+          }
+        } else {
+          for (int u = lane; u < nu; u += 32) {
+            dot8(wg[u], 0, u, a0, a1);
+            if (DUAL) dot8(wu[u], 0, u, b0, b1);
           }
         }
       }
-      acc[r] = a.x + a.y;
-      acc[RMAX + r] = bb.x + bb.y;
+      const float vg = (a0.x + a0.y) + (a1.x + a1.y), vu = (b0.x + b0.y) + (b1.x + b1.y);
+#pragma unroll
+      for (int k = 0; k < 8; k++)
+        if (k == nb) {
+          pg[k] = vg;
+          pu[k] = vu;
+        }
+      nb++;
     }
-    float(*rb_)[2 * RMAX] = red[i & 1];
-    if (DUAL) {
-      const float v = warp_sum_many<2 * RMAX>(acc, lane);
-      if ((lane & 1) == 0) rb_[cw][sum_slot<2 * RMAX>(lane)] = v;
-    } else {
-      float (&a8)[RMAX] = *reinterpret_cast<float(*)[RMAX]>(acc);
-      const float v = warp_sum_many<RMAX>(a8, lane);
-      if ((lane & 3) == 0) rb_[cw][sum_slot<RMAX>(lane)] = v;
-    }
+    __syncwarp();
+    if (lane == 0 && !ctl.abort) mbar_arrive(smem_addr(&empty[sl]));  // this warp is out of the slot
     t0 = tr.clk();
     tr.add(s, 9, t0 - t1);
-    tm.sync();
-    t1 = tr.clk();
-    tr.add(s, 10, t1 - t0);
-    if (t == 0 && !ctl.abort) mbar_arrive(smem_addr(&empty[sl]));  // the partials are out of the slot
-    // the chunk's epilogue goes to warp i mod MW, so its latency overlaps the next chunks
-    if (cw == i % MW && lane < nr) {
-      const int t = lane;
-      float g = 0.f, u = 0.f;
-      for (int ww = 0; ww < MW; ww++) {
-        g += rb_[ww][t];
-        if (DUAL) u += rb_[ww][RMAX + t];
+    if (nb > 0 && (nb == 8 || (mine && jr + MW >= n))) {
+      // the batch's sums: lane 4e holds row jb + e * MW
+      const float g = warp_sum_many<8>(pg, lane);
+      const float u = DUAL ? warp_sum_many<8>(pu, lane) : 0.f;
+      const int e = sum_slot<8>(lane);
+      if ((lane & 3) == 0 && e < nb) {
+        const int row = rb + jb + e * MW;
+        float y;
+        if (mode == EPI_SCALE) {
+          y = g * epi[0][row - rb];
+        } else if (mode == EPI_SILU) {
+          const float gs = g * epi[0][row - rb];
+          y = gs * sigmoidf_(gs) * (u * epi[1][row - rb]);
+        } else {
+          y = g;
+        }
+        Y[row] = y;
       }
-      const int n = r0 + t;
-      float y;
-      if (mode == EPI_SCALE) {
-        y = g * epi[0][n - rb];
-      } else if (mode == EPI_SILU) {
-        const float gs = g * epi[0][n - rb];
-        y = gs * sigmoidf_(gs) * (u * epi[1][n - rb]);
-      } else {
-        y = g;
-      }
-      Y[n] = y;
+#pragma unroll
+      for (int k = 0; k < 8; k++) pg[k] = pu[k] = 0.f;
+      jb += nb * MW;
+      nb = 0;
+      tr.add(s, 10, tr.clk() - t0);
     }
-    tr.add(s, 11, tr.clk() - t1);
   }
   tr.flush(s);
 }
@@ -353,7 +386,10 @@ __device__ __forceinline__ void input_row(const WarpTeam &tm, const GemvIn &in, 
 // Returns false (team-uniformly) when the block has stopped.
 __device__ __noinline__ bool gemv_stage(const WarpTeam &tm, const MegaArgs &a, const MegaStage &st, int s, int &c,
                            const uint8_t *ring, uint64_t *full, uint64_t *empty, float *xs,
-                           float (*red)[MW][2 * RMAX], float (*epi)[EPI_ROWS], Ctl &ctl) {
+                           float (*epi)[EPI_ROWS], Ctl &ctl) {
+  ring = in_shared(ring);  // shared-space loads and stores (this function is not inlined)
+  xs = in_shared(xs);
+  epi = in_shared(epi);
   const Tracer tr{tm.tid() == 0 ? a.trace : nullptr};
   const int G = gridDim.x, b = blockIdx.x;
   const int N = st.N, K = st.K;
@@ -370,19 +406,23 @@ __device__ __noinline__ bool gemv_stage(const WarpTeam &tm, const MegaArgs &a, c
   else if (kc <= 6) input_row<6>(tm, st.in, K, xs);
   else input_row<8>(tm, st.in, K, xs);
   tr.mark(s, 2);
-  const int seg = (K / 8 + 32 * MW - 1) / (32 * MW);
+  const int cpl = (K / 8 + 31) / 32;  // 16-byte columns per lane
   const bool dual = st.pair > 0;
-#define MEGA_CHUNKS(S)                                                                     \
-  if (dual) gemv_chunks<S, true>(tm, st, rb, re, c, ring, full, empty, xs, red, epi, ctl, a.err, tr, s); \
-  else gemv_chunks<S, false>(tm, st, rb, re, c, ring, full, empty, xs, red, epi, ctl, a.err, tr, s);
-  if (seg <= 1) {
-    MEGA_CHUNKS(1)
-  } else if (seg <= 2) {
-    MEGA_CHUNKS(2)
+#define MEGA_ROWS(X)                                                                        \
+  if (dual) gemv_rows<X, true>(tm, st, rb, re, c, ring, full, empty, xs, epi, ctl, a.err, tr, s); \
+  else gemv_rows<X, false>(tm, st, rb, re, c, ring, full, empty, xs, epi, ctl, a.err, tr, s);
+  if (cpl <= 1) {
+    MEGA_ROWS(1)
+  } else if (cpl <= 2) {
+    MEGA_ROWS(2)
+  } else if (cpl <= 4) {
+    MEGA_ROWS(4)
+  } else if (cpl <= 8) {
+    MEGA_ROWS(8)
   } else {
-    MEGA_CHUNKS(3)
+    MEGA_ROWS(0)
   }
-#undef MEGA_CHUNKS
+#undef MEGA_ROWS
   c += re > rb ? (re - rb + st.R - 1) / st.R : 0;
   const bool ok = team_ok(tm, ctl);
   tr.mark(s, 3);
@@ -537,6 +577,9 @@ __device__ __forceinline__ void attn_head(const MegaStage &st, int nk, const flo
 template <int HD>
 __device__ __noinline__ bool attn_stage(const WarpTeam &tm, const MegaArgs &a, const MegaStage &st, int s, float *work,
                                         uint64_t *abar, int &aph, float (*qs)[HD], float (*rope_s)[HD], Ctl &ctl) {
+  work = in_shared(work);  // shared-space loads and stores (this function is not inlined)
+  qs = in_shared(qs);
+  rope_s = in_shared(rope_s);
   const Tracer tr{tm.tid() == 0 ? a.trace : nullptr};
   tr.zero(s);  // trace only: copy wait, compute, arrival, merge cycles
   constexpr int HALF = HD / 2, PP = HALF / 32;  // pairs per lane
@@ -685,14 +728,13 @@ __global__ void __launch_bounds__(MTHREADS, 1) mega_decode_kernel(const __grid_c
   __shared__ __align__(16) float qs[8][HD];
   __shared__ __align__(16) float rope_s[2][HD];
   __shared__ __align__(16) MegaStage sst;
-  __shared__ float red[2][MW][2 * RMAX];
   __shared__ float epi[2][EPI_ROWS];
   __shared__ Ctl ctl;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; s++) {
       mbar_init(smem_addr(&full[s]), 1);
-      mbar_init(smem_addr(&empty[s]), 1);
+      mbar_init(smem_addr(&empty[s]), MW);  // every consumer warp frees every chunk
     }
     mbar_init(smem_addr(&abar), 1);
     mbar_fence_init();
@@ -740,7 +782,7 @@ __global__ void __launch_bounds__(MTHREADS, 1) mega_decode_kernel(const __grid_c
     // every reader of the position has passed: the last stage advances it
     if (s == a.nstages - 1 && b == 0 && tm.tid() == 0) a.seq_pos[a.adv_seq] += a.adv_cnt;
     if (sst.kind == MK_GEMV) {
-      ok = gemv_stage(tm, a, sst, s, c, ring, full, empty, work, red, epi, ctl);
+      ok = gemv_stage(tm, a, sst, s, c, ring, full, empty, work, epi, ctl);
     } else {
       if (!rope_ready) {
         if (!team_wait_counter(tm, a.sync + 1, HD, ctl, a.err)) {

@@ -233,6 +233,7 @@ struct MegaArgs {
   int adv_seq, adv_cnt;
   unsigned long long *trace;  // null, or [nstages][grid][MEGA_TRACE_EVENTS] %globaltimer stamps
   int prefetch_ahead;         // bytes per block the producer asks L2 for ahead of its copies
+  int max_inflight;           // weight copies a block keeps in flight at most (0: one per free slot)
 };
 
 // Stamps per (stage, block) of the persistent kernel's optional trace: 0 stage entered,
