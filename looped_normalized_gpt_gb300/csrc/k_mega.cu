@@ -15,8 +15,8 @@
 //     every block has finished the stage before (a counter in global memory);
 //   * GEMV: build the input row in shared memory (the embedding, a row norm, or the nGPT
 //     residual with the loop mix), then take the rows a warp each (bf16 weights, f32 sums;
-//     lanes split the row into 16-byte columns, one transpose reduction per 8 rows of a
-//     warp) and apply the epilogue (SwiGLU, logit scale) as the sums come out;
+//     lanes split the row into 16-byte columns, a butterfly sums them) and apply the
+//     epilogue (SwiGLU, logit scale) as each sum comes out;
 //   * attention (dory.rs fn attn_layer), in items of 32 positions of one kv head: the K and
 //     V rows of an item are contiguous in the ring and arrive with two bulk copies; meanwhile
 //     warp h rotates and normalises query head h of the group from the raw projection row
@@ -216,48 +216,13 @@ __device__ void produce(const MegaArgs &a, uint8_t *ring, uint64_t *full, uint64
 
 // ---- GEMV stage ---------------------------------------------------------------------------
 
-// Sums of v[0..2N) over the warp, all at once: a butterfly that halves the vector at each of
-// the first log2(2N) steps (exchanging the half a lane does not keep), then sums over the
-// remaining lanes. Afterwards lane l holds the total of element slot_of(l), where slot_of
-// reads the lane bits 4, 3, ... from the most significant element bit down; the lanes of
-// one element agree. Depth 5 shuffles whatever N is, 2N - 1 + (5 - log2 2N) of them.
-template <int N2>
-__device__ __forceinline__ float warp_sum_many(float (&v)[N2], int lane) {
-  static_assert(N2 == 8 || N2 == 16, "8 or 16 sums");
-  constexpr int LOG = N2 == 8 ? 3 : 4;
-#pragma unroll
-  for (int step = 0; step < LOG; step++) {
-    const int half = N2 >> (step + 1);
-    const int bit = 16 >> step;  // lanes 16, 8, 4, 2 apart
-    const bool upper = lane & bit;
-#pragma unroll
-    for (int j = 0; j < half; j++) {
-      const float send = upper ? v[j] : v[j + half];
-      const float keep = upper ? v[j + half] : v[j];
-      v[j] = keep + __shfl_xor_sync(0xffffffffu, send, bit);
-    }
-  }
-#pragma unroll
-  for (int bit = 16 >> LOG; bit > 0; bit >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], bit);
-  return v[0];
-}
-
-// The element whose total lane l holds after warp_sum_many<N2>.
-template <int N2>
-__device__ __forceinline__ int sum_slot(int lane) {
-  constexpr int LOG = N2 == 8 ? 3 : 4;
-  int e = 0;
-#pragma unroll
-  for (int step = 0; step < LOG; step++) e |= ((lane >> (4 - step)) & 1) << (LOG - 1 - step);
-  return e;
-}
-
 // A stage's rows, a warp per row: warp w of the team takes the block's rows w, w + MW, ...
 // (pairs of gate and up rows, DUAL). Its lanes split a row into 16-byte columns (lane l:
 // columns l, l + 32, ...) and multiply them with the input row, which a lane keeps in
 // registers when it has at most 8 columns (XR of them) and otherwise reads from shared
-// memory (XR = 0). Every 8 rows of a warp one transpose reduction gives their sums, which
-// lanes 0, 4, .., 28 scale and store. A chunk holds at most one row of each warp (R <= MW).
+// memory (XR = 0); a butterfly gives the row's sum, which lane 0 scales and stores (summing
+// 8 rows of a warp at once in one transpose reduction measured slower: the partials held
+// meanwhile crowd the registers). A chunk holds at most one row of each warp (R <= MW).
 // Every warp awaits every chunk of the stage and frees it with its own arrival (MW per
 // slot), so no team barrier runs inside the loop; since a warp frees a chunk only after it
 // has landed, its arrivals always fall in the slot's current phase.
@@ -300,10 +265,6 @@ __device__ void gemv_rows(const WarpTeam &tm, const MegaStage &st, int rb, int r
   };
   const int n = re - rb;  // rows (pairs) of this block
   const int nch = n > 0 ? (n + R - 1) / R : 0;
-  float pg[8], pu[8];
-#pragma unroll
-  for (int k = 0; k < 8; k++) pg[k] = pu[k] = 0.f;
-  int nb = 0, jb = cw;  // rows in the current batch, and its first row
   tr.zero(s);
   for (int x = 0; x < nch; x++) {
     const int c = c0 + x, sl = c % NS;
@@ -338,42 +299,24 @@ __device__ void gemv_rows(const WarpTeam &tm, const MegaStage &st, int rb, int r
         }
       }
       const float vg = (a0.x + a0.y) + (a1.x + a1.y), vu = (b0.x + b0.y) + (b1.x + b1.y);
-#pragma unroll
-      for (int k = 0; k < 8; k++)
-        if (k == nb) {
-          pg[k] = vg;
-          pu[k] = vu;
-        }
-      nb++;
-    }
-    __syncwarp();
-    if (lane == 0 && !ctl.abort) mbar_arrive(smem_addr(&empty[sl]));  // this warp is out of the slot
-    t0 = tr.clk();
-    tr.add(s, 9, t0 - t1);
-    if (nb > 0 && (nb == 8 || (mine && jr + MW >= n))) {
-      // the batch's sums: lane 4e holds row jb + e * MW
-      const float g = warp_sum_many<8>(pg, lane);
-      const float u = DUAL ? warp_sum_many<8>(pu, lane) : 0.f;
-      const int e = sum_slot<8>(lane);
-      if ((lane & 3) == 0 && e < nb) {
-        const int row = rb + jb + e * MW;
+      const float g = warp_sum(vg), u = DUAL ? warp_sum(vu) : 0.f;
+      if (lane == 0) {
+        const int row = rb + jr;
         float y;
         if (mode == EPI_SCALE) {
-          y = g * epi[0][row - rb];
+          y = g * epi[0][jr];
         } else if (mode == EPI_SILU) {
-          const float gs = g * epi[0][row - rb];
-          y = gs * sigmoidf_(gs) * (u * epi[1][row - rb]);
+          const float gs = g * epi[0][jr];
+          y = gs * sigmoidf_(gs) * (u * epi[1][jr]);
         } else {
           y = g;
         }
         Y[row] = y;
       }
-#pragma unroll
-      for (int k = 0; k < 8; k++) pg[k] = pu[k] = 0.f;
-      jb += nb * MW;
-      nb = 0;
-      tr.add(s, 10, tr.clk() - t0);
     }
+    __syncwarp();
+    if (lane == 0 && !ctl.abort) mbar_arrive(smem_addr(&empty[sl]));  // this warp is out of the slot
+    tr.add(s, 9, tr.clk() - t1);
   }
   tr.flush(s);
 }
