@@ -218,50 +218,30 @@ __device__ void produce(const MegaArgs &a, uint8_t *ring, uint64_t *full, uint64
 
 // A stage's rows, a warp per row: warp w of the team takes the block's rows w, w + MW, ...
 // (pairs of gate and up rows, DUAL). Its lanes split a row into 16-byte columns (lane l:
-// columns l, l + 32, ...) and multiply them with the input row, which a lane keeps in
-// registers when it has at most 8 columns (XR of them) and otherwise reads from shared
-// memory (XR = 0); a butterfly gives the row's sum, which lane 0 scales and stores (summing
-// 8 rows of a warp at once in one transpose reduction measured slower: the partials held
-// meanwhile crowd the registers). A chunk holds at most one row of each warp (R <= MW).
+// columns l, l + 32, ...) and multiply them with the input row, read from shared memory
+// (keeping a lane's part of the row in registers measured 2.5% slower: 64 registers held
+// across the stage), and a butterfly gives the row's sum, which lane 0 scales and stores
+// (summing 8 rows of a warp at once in one transpose reduction measured slower too). A
+// chunk holds at most one row of each warp (R <= MW).
 // Every warp awaits every chunk of the stage and frees it with its own arrival (MW per
 // slot), so no team barrier runs inside the loop; since a warp frees a chunk only after it
 // has landed, its arrivals always fall in the slot's current phase.
-template <int XR, bool DUAL>
+template <bool DUAL>
 __device__ void gemv_rows(const WarpTeam &tm, const MegaStage &st, int rb, int re, int c0, const uint8_t *ring,
                           uint64_t *full, uint64_t *empty, const float *xs, const float (*epi)[EPI_ROWS], Ctl &ctl,
                           int *err, const Tracer &tr, int s) {
   const int lane = threadIdx.x & 31, cw = tm.warp();
   const int K = st.K, R = st.R, mode = st.ep.mode, nu = K / 8;  // 16-byte columns per row
   float *__restrict__ Y = st.Y;
-  constexpr int XN = XR > 0 ? 8 * XR : 1;
-  float xr[XN];
-#pragma unroll
-  for (int g = 0; g < XR; g++) {
-    const int u = lane + 32 * g;
-    float4 p = make_float4(0.f, 0.f, 0.f, 0.f), q = p;
-    if (u < nu) {
-      p = *reinterpret_cast<const float4 *>(xs + u * 8);
-      q = *reinterpret_cast<const float4 *>(xs + u * 8 + 4);
-    }
-    xr[8 * g + 0] = p.x; xr[8 * g + 1] = p.y; xr[8 * g + 2] = p.z; xr[8 * g + 3] = p.w;
-    xr[8 * g + 4] = q.x; xr[8 * g + 5] = q.y; xr[8 * g + 6] = q.z; xr[8 * g + 7] = q.w;
-  }
   // a 16-byte column of weights against the input row: two chains of paired FMAs
-  auto dot8 = [&](const uint4 &wq, int g, int u, float2 &a0, float2 &a1) {
+  auto dot8 = [&](const uint4 &wq, int u, float2 &a0, float2 &a1) {
     float wv[8];
     unpack8(wq, wv);
-    float x[8];
-    if (XR > 0) {
-#pragma unroll
-      for (int e = 0; e < 8; e++) x[e] = xr[(8 * g + e) % XN];
-    } else {
-      const float4 p = *reinterpret_cast<const float4 *>(xs + u * 8), q = *reinterpret_cast<const float4 *>(xs + u * 8 + 4);
-      x[0] = p.x; x[1] = p.y; x[2] = p.z; x[3] = p.w; x[4] = q.x; x[5] = q.y; x[6] = q.z; x[7] = q.w;
-    }
-    a0 = ffma2(make_float2(wv[0], wv[1]), make_float2(x[0], x[1]), a0);
-    a1 = ffma2(make_float2(wv[2], wv[3]), make_float2(x[2], x[3]), a1);
-    a0 = ffma2(make_float2(wv[4], wv[5]), make_float2(x[4], x[5]), a0);
-    a1 = ffma2(make_float2(wv[6], wv[7]), make_float2(x[6], x[7]), a1);
+    const float4 p = *reinterpret_cast<const float4 *>(xs + u * 8), q = *reinterpret_cast<const float4 *>(xs + u * 8 + 4);
+    a0 = ffma2(make_float2(wv[0], wv[1]), make_float2(p.x, p.y), a0);
+    a1 = ffma2(make_float2(wv[2], wv[3]), make_float2(p.z, p.w), a1);
+    a0 = ffma2(make_float2(wv[4], wv[5]), make_float2(q.x, q.y), a0);
+    a1 = ffma2(make_float2(wv[6], wv[7]), make_float2(q.z, q.w), a1);
   };
   const int n = re - rb;  // rows (pairs) of this block
   const int nch = n > 0 ? (n + R - 1) / R : 0;
@@ -282,20 +262,10 @@ __device__ void gemv_rows(const WarpTeam &tm, const MegaStage &st, int rb, int r
       if (landed) {
         const uint4 *wg = reinterpret_cast<const uint4 *>(ring + (size_t)sl * SLOT) + (size_t)(jr - r0) * nu;
         const uint4 *wu = wg + (size_t)nr * nu;
-        if (XR > 0) {
-#pragma unroll
-          for (int g = 0; g < XR; g++) {
-            const int u = lane + 32 * g;
-            if (u < nu) {
-              dot8(wg[u], g, u, a0, a1);
-              if (DUAL) dot8(wu[u], g, u, b0, b1);
-            }
-          }
-        } else {
-          for (int u = lane; u < nu; u += 32) {
-            dot8(wg[u], 0, u, a0, a1);
-            if (DUAL) dot8(wu[u], 0, u, b0, b1);
-          }
+#pragma unroll 4
+        for (int u = lane; u < nu; u += 32) {
+          dot8(wg[u], u, a0, a1);
+          if (DUAL) dot8(wu[u], u, b0, b1);
         }
       }
       const float vg = (a0.x + a0.y) + (a1.x + a1.y), vu = (b0.x + b0.y) + (b1.x + b1.y);
@@ -349,23 +319,8 @@ __device__ __noinline__ bool gemv_stage(const WarpTeam &tm, const MegaArgs &a, c
   else if (kc <= 6) input_row<6>(tm, st.in, K, xs);
   else input_row<8>(tm, st.in, K, xs);
   tr.mark(s, 2);
-  const int cpl = (K / 8 + 31) / 32;  // 16-byte columns per lane
-  const bool dual = st.pair > 0;
-#define MEGA_ROWS(X)                                                                        \
-  if (dual) gemv_rows<X, true>(tm, st, rb, re, c, ring, full, empty, xs, epi, ctl, a.err, tr, s); \
-  else gemv_rows<X, false>(tm, st, rb, re, c, ring, full, empty, xs, epi, ctl, a.err, tr, s);
-  if (cpl <= 1) {
-    MEGA_ROWS(1)
-  } else if (cpl <= 2) {
-    MEGA_ROWS(2)
-  } else if (cpl <= 4) {
-    MEGA_ROWS(4)
-  } else if (cpl <= 8) {
-    MEGA_ROWS(8)
-  } else {
-    MEGA_ROWS(0)
-  }
-#undef MEGA_ROWS
+  if (st.pair > 0) gemv_rows<true>(tm, st, rb, re, c, ring, full, empty, xs, epi, ctl, a.err, tr, s);
+  else gemv_rows<false>(tm, st, rb, re, c, ring, full, empty, xs, epi, ctl, a.err, tr, s);
   c += re > rb ? (re - rb + st.R - 1) / st.R : 0;
   const bool ok = team_ok(tm, ctl);
   tr.mark(s, 3);
