@@ -262,7 +262,7 @@ __device__ void gemv_rows(const WarpTeam &tm, const MegaStage &st, int rb, int r
       if (landed) {
         const uint4 *wg = reinterpret_cast<const uint4 *>(ring + (size_t)sl * SLOT) + (size_t)(jr - r0) * nu;
         const uint4 *wu = wg + (size_t)nr * nu;
-#pragma unroll 4
+#pragma unroll 8
         for (int u = lane; u < nu; u += 32) {
           dot8(wg[u], u, a0, a1);
           if (DUAL) dot8(wu[u], u, b0, b1);
