@@ -92,9 +92,9 @@ class Clocks:
 
 
 # DRAM bytes (read + write) per algorithmic byte of the persistent decode kernel, from the
-# ncu capture of the reduced 3-pass case (431.1 + 5.3 MB for 427.3 MB of weights and KV);
+# ncu capture of the reduced 3-pass case (429.5 + 4.5 MB for 427.3 MB of weights and KV);
 # the kernel streams every weight once per token, so the ratio carries to the full model.
-MEGA_TRAFFIC_PER_BYTE = (431.1 + 5.3) / 427.3
+MEGA_TRAFFIC_PER_BYTE = (429.5 + 4.5) / 427.3
 
 
 def roofline_decode(st, bytes_step, achieved, hbm, src):
