@@ -129,6 +129,11 @@ def profile_case(args):
         w = synth.weights(synth.dory2b(), SEED)
         out = bench_batch(Dory, torch, w, int(os.environ.get("LOCAL_RANK", "0")), steps=4)
         return {"case": "batch64", **out, "note": "profiling case, not a bench line"}
+    if args.profile_case == "context":  # the two long-context batch lines alone
+        w = synth.weights(synth.dory2b(), SEED)
+        dev = int(os.environ.get("LOCAL_RANK", "0"))
+        return {"case": "context", "per_loop_batch16": bench_per_loop16(Dory, torch, w, dev),
+                "q8_batch64": bench_q8_batch64(Dory, torch, w, dev), "note": "profiling case, not a bench line"}
     if args.profile_case == "prefill":
         cfg = synth.dory2b(max_batch=1, max_seqs=1, max_context=args.prompt + 64, prompt_loops=2)
         g = Dory(cfg, synth.weights(cfg, SEED))
@@ -256,6 +261,71 @@ def bench_ours(args, rank, world):
         "weights_gen_s": round(t_gen, 1),
     }
     return out, g, cfg, w
+
+
+def bench_context_decode(g_cls, torch, w, dev, cfg, nseq: int, ctx: int, sched, warmup: int, seed: int):
+    """Batch decode at a long synthetic context: `nseq` sequences with `ctx` unit-norm K/V rows
+    in every slot (drawn on the GPU, written through the append path, so q8 rings quantise
+    and freeze as in a forward), then len(sched) timed steps, step i at sched[i] loops. The
+    algorithmic bytes are the weights once per step plus the K/V rows read and written,
+    summed over the timed steps. The weights are the main line's 2B set (the values do not
+    change the bytes moved)."""
+    stream = torch.cuda.current_stream()
+    g = g_cls(cfg, w, stream=stream.cuda_stream)
+    try:
+        gen = torch.Generator(device=f"cuda:{dev}")
+        gen.manual_seed(seed)
+        for s_ in range(nseq):
+            for o in range(cfg.attn_layers):
+                _, slots, _ = g.slot_info(o)
+                for sl in range(slots):
+                    k = torch.randn(ctx, cfg.nk, cfg.hd, device=f"cuda:{dev}", generator=gen)
+                    v = torch.randn(ctx, cfg.nk, cfg.hd, device=f"cuda:{dev}", generator=gen)
+                    k /= k.norm(dim=2, keepdim=True)
+                    v /= v.norm(dim=2, keepdim=True)
+                    g.write_kv_rows(s_, o, sl, 0, k.contiguous(), v.contiguous())
+            g.set_position(s_, ctx)
+        steps = len(sched)
+        ids = torch.from_numpy(synth.token_ids(seed, 7, nseq * (steps + warmup), cfg.vocab)).to(f"cuda:{dev}")
+        seqs = list(range(nseq))
+        for i in range(warmup):
+            g.decode_step(ids[i * nseq:(i + 1) * nseq], seqs, int(sched[i % steps]))
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        b = 0
+        e0.record(stream)
+        for i in range(steps):
+            j = warmup + i
+            g.decode_step(ids[j * nseq:(j + 1) * nseq], seqs, int(sched[i]))
+            st = g.stats()
+            b += st["weight_bytes"] + st["kv_read_bytes"] + st["kv_write_bytes"]
+        e1.record(stream)
+        torch.cuda.synchronize()
+        s_total = e0.elapsed_time(e1) / 1e3
+        hbm, _, _ = peaks()
+        return {"value": round(nseq * steps / s_total, 1), "unit": "tokens/s", "ms_per_step": round(s_total * 1e3 / steps, 4),
+                "batch": nseq, "context": ctx, "loops": sorted({int(x) for x in sched}), "kv": cfg.kv_quant,
+                "kv_mode": cfg.kv_mode,
+                "roofline": {"bound": "hbm", "achieved": round(b / s_total / 1e9, 1), "peak": hbm, "unit": "GB/s",
+                             "frac": round(b / s_total / 1e9 / hbm, 4), "bytes_per_step": round(b / steps)}}
+    finally:
+        g.close()
+
+
+def bench_per_loop16(g_cls, torch, w, dev, steps: int = 16, warmup: int = 3):
+    """per_loop KV, batch 16 at context 8192, every second recurrent attention layer full
+    (full_window 8192), loops drawn per step from {2, 4, 8}."""
+    cfg = synth.dory2b(rec_kinds="S*S*", kv_mode="per_loop", max_loops=8, loops=8, full_window=8192,
+                       max_batch=16, max_seqs=16, max_context=8192 + steps + warmup + 64)
+    return bench_context_decode(g_cls, torch, w, dev, cfg, 16, 8192, synth.loop_schedule(SEED + 1, steps), warmup,
+                                SEED + 1)
+
+
+def bench_q8_batch64(g_cls, torch, w, dev, steps: int = 8, warmup: int = 3):
+    """q8_2f KV (last_loop), batch 64 at context 8192, loops 16, full layers capped at 8192."""
+    cfg = synth.dory2b(rec_kinds="S*S*", kv_mode="last_loop", kv_quant="q8_2f", loops=16, max_loops=16,
+                       full_window=8192, max_batch=64, max_seqs=64, max_context=8192 + steps + warmup + 64)
+    return bench_context_decode(g_cls, torch, w, dev, cfg, 64, 8192, [16] * steps, warmup, SEED + 3)
 
 
 def bench_batch(g_cls, torch, w, dev, batch: int = 64, ctx: int = 1024, steps: int = 16, warmup: int = 3):
@@ -391,7 +461,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the batch-64 decode and prefill lines")
     ap.add_argument("--prompt", type=int, default=PROMPT, help="prompt tokens before the decode steps")
-    ap.add_argument("--profile-case", choices=["decode-3pass", "prefill", "batch64"],
+    ap.add_argument("--profile-case", choices=["decode-3pass", "prefill", "batch64", "context"],
                     help="run a small case for ncu captures instead of the bench")
     args = ap.parse_args()
     if args.profile_case:
@@ -417,7 +487,9 @@ def main():
 
         dev = int(os.environ.get("LOCAL_RANK", "0"))
         out["extra"] = {"decode_batch64": bench_batch(Dory, torch, w, dev),
-                        "prefill_16k": bench_prefill(Dory, torch, w)}
+                        "prefill_16k": bench_prefill(Dory, torch, w),
+                        "decode_per_loop_batch16_ctx8192": bench_per_loop16(Dory, torch, w, dev),
+                        "decode_q8_batch64_ctx8192": bench_q8_batch64(Dory, torch, w, dev)}
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
             out["cpu_baseline"] = cpu_baseline(cfg, w)
