@@ -17,7 +17,7 @@ the Rust crate cortiq-engine computes (docs.rs source pages
   * no blocking, fusion or reordering: one chunk at a time, one row and one KV
     head at a time for attention, library matmuls for the projections.
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent:
   * rope_inv_freq's body is not on the pages: inv[j] = theta^(-2j/hd) in f64,
     rounded to f32.
   * per_loop with a loop count that changes between steps leaves holes in the
