@@ -4,7 +4,7 @@
 //
 // One block per SM, launched cooperatively so that every block is resident. Warp 0 is the
 // producer: it walks this block's share of every weight matrix (a contiguous range of rows)
-// in stage order, optionally asks L2 for the bytes some distance ahead (cp.async.bulk.prefetch),
+// in stage order, asks L2 for the bytes about two chunks ahead (cp.async.bulk.prefetch),
 // and copies chunks into a ring of shared-memory slots with cp.async.bulk, completion on one
 // mbarrier per slot. It never waits for activations, so HBM keeps streaming the next stages'
 // weights while the consumers wait at a grid barrier or run attention. Warps 1..8 are the
