@@ -215,3 +215,46 @@ def test_prefill_16k_prompt_loops(torch):
         assert np.array_equal(tags.astype(np.int64), want)
     finally:
         g.close()
+
+
+def test_batch1_decode_at_prompt_4096_replays_exactly():
+    """The batch-1 decode line at its full size, in the benchmark's configuration (a
+    4096-token prompt in 64-row chunks, then decode steps through the persistent kernel),
+    by properties that hold at any size: every step is one launch, the hidden row stays on
+    the unit sphere, each ring row holds the latest position congruent to it modulo the
+    ring's capacity, and a replay of the same ids gives bit-identical logits. (The oracle
+    follows this workload on the reduced span of the test above.)"""
+    from looped_normalized_gpt_gb300 import Dory, build
+
+    build()
+    n_dec = 16
+    cfg = synth.dory2b(max_batch=1, max_seqs=1, max_context=4096 + n_dec + 64)
+    w = synth.weights(cfg, 1236)
+    g = Dory(cfg, w)
+    try:
+        ids = synth.token_ids(1236, 0, 4096 + n_dec, cfg.vocab)
+
+        def run():
+            for a in range(0, 4096, 64):
+                g.prefill_chunk(0, ids[a:a + 64], a, cfg.loops, "none")
+            out = []
+            for i in ids[4096:]:
+                g.decode_step([int(i)], [0], cfg.loops)
+                assert g.stats()["launches"] == 1
+                assert abs(float(np.linalg.norm(g.read_hidden(1)[0])) - 1.0) <= 1e-5
+                out.append(g.logits(0).copy())
+            return np.stack(out)
+
+        first = run()
+        last = 4096 + n_dec - 1
+        for ordn in range(cfg.attn_layers):
+            cap, _, _ = g.slot_info(ordn)
+            tags, _, _ = g.read_kv_f32(0, ordn, 0)
+            want = np.array([last - ((last - r) % cap) for r in range(cap)], np.int64)
+            assert np.array_equal(tags.astype(np.int64), want), ordn
+        g.reset(0)
+        second = run()
+        assert np.isfinite(first).all()
+        assert np.array_equal(first.view(np.uint32), second.view(np.uint32))
+    finally:
+        g.close()
