@@ -17,6 +17,8 @@
 // at zero (the counters), so a call does not depend on the one before; calls whose work
 // overlaps on the GPU (different streams, or different host threads without ordering)
 // race on the array and must not be made.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "../../include/dory.h"
@@ -43,10 +45,38 @@ struct NaScratch {
 static __device__ __align__(256) unsigned char g_q8_scratch[sizeof(NaScratch)];
 
 // In host code `g_q8_scratch` names a host-side stand-in, not device memory: the device
-// address comes from cudaGetSymbolAddress, once per device, with that device current.
+// address comes from cudaGetSymbolAddress, once per device (per primary context: a
+// cudaDeviceReset ends the context and the module with it, so a new context, told apart by
+// its process-unique id, looks the address up again), with that device current.
 constexpr int NA_MAX_DEVICES = 64;
 std::mutex g_na_mu;
 NaScratch *g_na_ptr[NA_MAX_DEVICES] = {};
+unsigned long long g_na_ctx[NA_MAX_DEVICES] = {};
+
+// The process-unique id of the calling thread's current context, or 0 if none is current
+// (driver calls reached through the runtime, so the library loads without libcuda).
+unsigned long long na_context_id() {
+  using GetCurrent = CUresult (*)(CUcontext *);
+  using GetId = CUresult (*)(CUcontext, unsigned long long *);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  if (!get_current || !get_id) {
+    void *f1 = nullptr, *f2 = nullptr;
+    cudaDriverEntryPointQueryResult q1, q2;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault, &q1) != cudaSuccess ||
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) != cudaSuccess ||
+        q1 != cudaDriverEntryPointSuccess || q2 != cudaDriverEntryPointSuccess || !f1 || !f2) {
+      cudaGetLastError();
+      return 0;
+    }
+    get_current = reinterpret_cast<GetCurrent>(f1);
+    get_id = reinterpret_cast<GetId>(f2);
+  }
+  CUcontext c = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&c) != CUDA_SUCCESS || !c || get_id(c, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
 
 int na_fail(int code, const char *msg) {
   dory::set_last_error(msg);
@@ -181,13 +211,15 @@ extern "C" int dory_q8_quantize_noalloc(const float *k, const float *v, int32_t 
   NaScratch *sc;
   {
     std::lock_guard<std::mutex> lock(g_na_mu);
-    if (!g_na_ptr[dev]) {
+    const unsigned long long ctx = na_context_id();
+    if (!g_na_ptr[dev] || ctx == 0 || ctx != g_na_ctx[dev]) {
       void *p = nullptr;
       if (cudaGetSymbolAddress(&p, g_q8_scratch) != cudaSuccess || !p) {
         cudaGetLastError();
         return na_fail(DORY_ECUDA, "cudaGetSymbolAddress of the static scratch failed");
       }
       g_na_ptr[dev] = static_cast<NaScratch *>(p);
+      g_na_ctx[dev] = na_context_id();  // the lookup made the primary context current
     }
     sc = g_na_ptr[dev];
   }

@@ -113,6 +113,10 @@ class DoryConfig:
     mlp_suv: float = 1.0  # raw suv; the effective MLP scale is suv*sqrt(hidden)
     logit_scale: float = 1.0
     alpha: tuple = (0.05, 0.05)  # |alpha| drawn uniformly in [lo, hi] per element
+    # per-element spread of the folded scale vectors (s_q^2, the gate's s_g^2, the MLP's
+    # s_g and s_u, logit_scale): each element is its base value above times a uniform draw
+    # in [1 - spread, 1 + spread]; 0 gives every element the base value
+    scale_spread: float = 0.0
 
     @property
     def n_layers(self) -> int:
@@ -152,7 +156,7 @@ def dory2b(rec_kinds: str = "SSSS", **kw) -> DoryConfig:
         name="dory-2b", hidden=2048, ffn=5632, vocab=32000, nh=16, nk=4, hd=128, window=512,
         pattern=pat, n_in=a, n_rec=b, n_out=c, loops=4, max_loops=16, kv_mode="last_loop",
         kv_quant="f32", weight_dtype="bf16", sq=128.0, attn_sg=1.0, mlp_suv=1.0,
-        logit_scale=1.0, alpha=(0.02, 0.1), max_context=16384 + 64,
+        logit_scale=1.0, alpha=(0.02, 0.1), max_context=16384 + 64, scale_spread=0.25,
     )
     base.update(kw)
     return DoryConfig(**base)
@@ -165,8 +169,8 @@ def small(rec_kinds: str = "S*", **kw) -> DoryConfig:
     base = dict(
         name="small", hidden=512, ffn=1024, vocab=1000, nh=8, nk=2, hd=64, window=48,
         pattern=pat, n_in=a, n_rec=b, n_out=c, loops=3, max_loops=16, kv_mode="last_loop",
-        kv_quant="f32", weight_dtype="bf16", sq=64.0, attn_sg=1.0, mlp_suv=1.0,
-        logit_scale=1.0, alpha=(0.02, 0.1), max_context=2048,
+        kv_quant="f32", weight_dtype="bf16", sq=64.0, attn_sg=6.0, mlp_suv=1.0,
+        logit_scale=1.5, alpha=(0.02, 0.1), max_context=2048, scale_spread=0.5,
     )
     base.update(kw)
     return DoryConfig(**base)
@@ -211,6 +215,12 @@ def _uniform_range(seed: int, stream: int, n: int, lo: float, hi: float) -> np.n
     return (lo + (hi - lo) * uniform(seed, stream, n)).astype(np.float32)
 
 
+def _scales(cfg: DoryConfig, seed: int, stream: int, n: int, base: float) -> np.ndarray:
+    """n folded scale values: `base` times a uniform draw in [1 - spread, 1 + spread] each."""
+    sp = cfg.scale_spread
+    return (np.float64(base) * _uniform_range(seed, stream, n, 1.0 - sp, 1.0 + sp)).astype(np.float32)
+
+
 def weights(cfg: DoryConfig, seed: int) -> dict:
     """Random-init weights of the given architecture, with the effective (folded) scales."""
     dt = cfg.weight_dtype
@@ -221,14 +231,14 @@ def weights(cfg: DoryConfig, seed: int) -> dict:
         s = 1000 + 32 * li
         alpha = _uniform_range(seed, s + 31, cfg.hidden, *cfg.alpha)
         if kind == "-":
-            eff = np.float32(cfg.mlp_suv * math.sqrt(cfg.hidden))
+            eff = cfg.mlp_suv * math.sqrt(cfg.hidden)
             layers.append(dict(
                 kind="mlp",
                 gate=unit_rows(seed, s + 0, cfg.ffn, cfg.hidden, dt),
                 up=unit_rows(seed, s + 1, cfg.ffn, cfg.hidden, dt),
                 down=unit_rows(seed, s + 2, cfg.hidden, cfg.ffn, dt),
-                sg=np.full(cfg.ffn, eff, dtype=np.float32),
-                su=np.full(cfg.ffn, eff, dtype=np.float32),
+                sg=_scales(cfg, seed, s + 5, cfg.ffn, eff),
+                su=_scales(cfg, seed, s + 6, cfg.ffn, eff),
                 alpha=alpha,
             ))
         else:
@@ -240,14 +250,14 @@ def weights(cfg: DoryConfig, seed: int) -> dict:
                 v=unit_rows(seed, s + 2, kv_row, cfg.hidden, dt),
                 g=unit_rows(seed, s + 3, q_size, cfg.hidden, dt),
                 o=unit_rows(seed, s + 4, cfg.hidden, q_size, dt),
-                sq=np.full(q_size, cfg.sq, dtype=np.float32),
-                sg=np.full(q_size, cfg.attn_sg, dtype=np.float32),
+                sq=_scales(cfg, seed, s + 5, q_size, cfg.sq),
+                sg=_scales(cfg, seed, s + 6, q_size, cfg.attn_sg),
                 alpha=alpha,
             ))
     return dict(
         embed=unit_rows(seed, 1, cfg.vocab, cfg.hidden, dt),
         head=unit_rows(seed, 2, cfg.vocab, cfg.hidden, dt),
-        logit_scale=np.full(cfg.vocab, cfg.logit_scale, dtype=np.float32),
+        logit_scale=_scales(cfg, seed, 3, cfg.vocab, cfg.logit_scale),
         layers=layers,
     )
 

@@ -17,6 +17,27 @@ def tol_of(cfg) -> float:
     return TOL_F32 if cfg.weight_dtype == "f32" else TOL_BF16
 
 
+# The head step alone (dory.rs fn head: logits = (H h) * logit_scale) on the GPU's own final
+# hidden rows: H's rows and h have unit norm, so |H_i . h| <= 1, and an f32 dot product over
+# bf16 weights (or over the tensor-core path's two bf16 halves of h, which keep about 16
+# mantissa bits) errs by far less than 1e-4 of it. A dropped or misindexed logit scale moves
+# a logit by |ls_i - ls_j| * |H_i . h|, orders of magnitude more.
+HEAD_TOL = 1e-4
+
+
+def head_err(orc, h_rows, lg_rows) -> float:
+    """Largest |GPU logit - (H h_gpu)_i * ls_i| / max|ls| over the given rows."""
+    want = (np.asarray(h_rows, np.float64) @ orc.head.T) * orc.logit_scale
+    return float(np.max(np.abs(np.asarray(lg_rows, np.float64) - want)) / np.max(np.abs(orc.logit_scale)))
+
+
+def logit_bound(orc, cfg, h_err_rows) -> float:
+    """Bound on |GPU logit - oracle logit| implied by the rows' hidden max-abs errors: with unit
+    rows of H, |H_i . dh| <= |dh|_2 <= sqrt(hidden) * max|dh|; plus the head's own HEAD_TOL."""
+    ls = float(np.max(np.abs(orc.logit_scale)))
+    return ls * (np.sqrt(cfg.hidden) * float(np.max(h_err_rows)) + HEAD_TOL)
+
+
 class Pair:
     """The GPU handle and the oracle for one config and seed."""
 
@@ -31,15 +52,26 @@ class Pair:
         self.states = [O.SeqState() for _ in range(cfg.max_seqs)]
         self.max_hidden_err = 0.0
         self.max_logit_err = 0.0
+        self.max_head_err = 0.0
         self.top1 = []
 
     def close(self):
         self.gpu.close()
 
     def _note(self, h_gpu, h_orc, lg_gpu=None, lg_orc=None):
-        self.max_hidden_err = max(self.max_hidden_err, float(np.max(np.abs(h_gpu - h_orc))))
+        """Record the hidden error of the rows; for a row with logits, assert the head step on
+        the GPU's own hidden row (HEAD_TOL) and the logits against the oracle's (the bound the
+        row's hidden error implies), and record top-1 agreement."""
+        err = float(np.max(np.abs(h_gpu - h_orc)))
+        self.max_hidden_err = max(self.max_hidden_err, err)
         if lg_gpu is not None:
-            self.max_logit_err = max(self.max_logit_err, float(np.max(np.abs(lg_gpu - lg_orc))))
+            he = head_err(self.orc, h_gpu, lg_gpu)
+            self.max_head_err = max(self.max_head_err, he)
+            assert he <= HEAD_TOL, f"head step: {he:.3e} of max|logit_scale|"
+            le = float(np.max(np.abs(lg_gpu - lg_orc)))
+            self.max_logit_err = max(self.max_logit_err, le)
+            bound = logit_bound(self.orc, self.cfg, np.abs(h_gpu - h_orc))
+            assert le <= bound, f"logits differ by {le:.3e}, above the bound {bound:.3e} of the hidden error"
             self.top1.append(int(np.argmax(lg_gpu)) == int(np.argmax(lg_orc)))
 
     def prefill(self, seq: int, ids, loops: int, want: str = "last"):
@@ -53,8 +85,10 @@ class Pair:
             return h_g, h_o, None, None
         rows = 1 if want == "last" else len(ids)
         lg_g = np.stack([self.gpu.logits(r) for r in range(rows)])
+        first = len(ids) - rows  # want last: the chunk's last row; want all: every row
+        self._note(h_g, h_o)
         for r in range(rows):
-            self._note(h_g, h_o, lg_g[r], lg_o[r])
+            self._note(h_g[first + r], h_o[first + r], lg_g[r], lg_o[r])
         return h_g, h_o, lg_g, lg_o
 
     def decode(self, seqs, ids, loops: int):

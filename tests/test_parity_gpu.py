@@ -318,3 +318,89 @@ def test_batched_decode_streams_each_window(hd, nh, nk):
             P.check_rings(s, 1e-5)
     finally:
         P.close()
+
+
+# ------------------------------------------------------------------------------------------
+# folded scales on every launch path
+# ------------------------------------------------------------------------------------------
+
+
+def scales_case():
+    """The model of the folded-scale test: every folded scale a per-element vector (spread 0.5
+    around s_q^2 = 64, gate s_g^2 = 6, MLP s = sqrt(512), logit_scale 1.5)."""
+    return synth.small(max_batch=6, max_seqs=6, rec_kinds="S*", full_window=0, max_context=1024, loops=3)
+
+
+SCALES_SEED = 2012
+
+
+@pytest.mark.parametrize("mega", ["1", "0"])
+def test_folded_scales_reach_every_launch_path(mega, monkeypatch):
+    """Prefill chunks and batch-6 steps run the tensor-core path, batch-3 steps the fused path,
+    batch-1 steps the persistent kernel (or the fused path without it). Each gate (hidden
+    1e-4, the head step on the GPU's own hidden row, logits within the bound the hidden error
+    implies) fails if any kernel drops or misreads one of the vectors: the CPU test
+    tests/test_scale_slips.py plants each such slip in the oracle on these inputs."""
+    monkeypatch.setenv("DORY_MEGA", mega)
+    cfg = scales_case()
+    P = Pair(cfg, SCALES_SEED)
+    try:
+        ids = synth.token_ids(SCALES_SEED, 0, 6 * 40, cfg.vocab)
+        for s in range(6):
+            P.prefill(s, ids[40 * s:40 * s + 33 + s], cfg.loops, "last")
+        launches = []
+        for step in range(3):
+            P.decode([0], synth.token_ids(SCALES_SEED, 10 + step, 1, cfg.vocab), cfg.loops)
+            launches.append(P.gpu.stats()["launches"])
+        assert (launches == [1] * 3) == (mega == "1"), launches
+        for step in range(2):
+            P.decode([3, 1, 2], synth.token_ids(SCALES_SEED, 20 + step, 3, cfg.vocab), cfg.loops)
+        for step in range(2):
+            P.decode([5, 0, 4, 2, 1, 3], synth.token_ids(SCALES_SEED, 30 + step, 6, cfg.vocab), cfg.loops)
+        P.prefill(5, synth.token_ids(SCALES_SEED, 40, 8, cfg.vocab), cfg.loops, "all")
+        assert P.max_hidden_err <= 1e-4, P.max_hidden_err
+        assert P.max_head_err <= 1e-4, P.max_head_err
+        assert all(P.top1)
+        for s in range(6):
+            P.check_rings(s, 1e-5)
+    finally:
+        P.close()
+
+
+def test_q8_per_loop_freeze_reads_rows_the_ring_no_longer_holds():
+    """q8_2f under per_loop with the loop count changing between chunks: loop slot 3 of the
+    sliding recurrent layer (ring of 576 rows) gets positions 0-31, then nothing until 576,
+    so its first 64 rows span 608 positions and, when the freeze comes (at the 65th row,
+    position 608), positions 0-31 are no longer in the ring. The freeze reads them from the
+    slot's copy of its first 64 rows; codes, scales and fields must then agree with the
+    oracle, which keeps every row."""
+    cfg = synth.small(kv_quant="q8_2f", kv_mode="per_loop", rec_kinds="S*", full_window=0, max_context=1024,
+                      max_loops=4, loops=4)
+    P = Pair(cfg, 2013)
+    try:
+        ids = synth.token_ids(2013, 0, 700, cfg.vocab)
+        plan = [(0, 32, 4)] + [(a, min(a + 64, 576), 2) for a in range(32, 576, 64)] + [(576, 640, 4), (640, 700, 3)]
+        for a, b, L in plan:
+            P.prefill(0, ids[a:b], L, "last")
+        for step, L in enumerate([4, 1, 4, 2]):
+            P.decode([0], synth.token_ids(2013, 10 + step, 1, cfg.vocab), L)
+        assert P.max_hidden_err <= tol_of(cfg), P.max_hidden_err
+        assert np.mean(P.top1) >= 0.99
+        ordn = 1  # the sliding recurrent attention layer
+        cap, slots, sliding = P.gpu.slot_info(ordn)
+        assert sliding and slots == 4 and cap < 608
+        slot = P.states[0].slots[(ordn, 3)]
+        assert slot.positions[:33] == list(range(32)) + [576] and slot.kcol is not None
+        for (o_, sl), s_ in P.states[0].slots.items():
+            got = P.gpu.read_kv_q8(0, o_, sl)
+            tags, kq, ks, vq, vs = _oracle_q8_ring(s_, P.gpu.slot_info(o_)[0], cfg.nk, cfg.hd)
+            assert np.array_equal(got["tags"].astype(np.int64), tags), (o_, sl)
+            assert got["frozen"].tolist() == [int(s_.kcol is not None)] * cfg.nk, (o_, sl)
+            held = tags >= 0
+            dk = np.abs(got["kq"][:, held].astype(int) - kq[:, held])
+            assert np.max(dk) <= 2 and np.mean(dk == 0) >= 0.97, (o_, sl)
+            if s_.kcol is not None:
+                assert np.allclose(got["kcol"], s_.kcol, rtol=2e-2, atol=1e-5), (o_, sl)
+                assert np.allclose(got["vcol"], s_.vcol, rtol=2e-2, atol=1e-5), (o_, sl)
+    finally:
+        P.close()
