@@ -121,11 +121,29 @@ typedef struct dory_handle dory_t;
  * Errors: DORY_EINVAL, DORY_ENOMEM, DORY_ECUDA; *out is NULL then. */
 int dory_create(const dory_config *cfg, const dory_weights *w, void *stream, dory_t **out);
 
-/* Free everything the handle owns (after synchronising its stream). NULL is a no-op. */
+/* Free everything the handle owns (after synchronising its stream). NULL is a no-op.
+ * The handle plays the part of the Metal path's per-model Device (page
+ * "src/gpu_metal/dory.rs", fn forward: built on a model's first forward and kept in the
+ * DEVICES map); the pages never remove one, so this entry point has no counterpart there
+ * beyond dropping that state. */
 int dory_destroy(dory_t *d);
 
 /* Empty one sequence's rings and set its position to 0 (gpu_metal/dory.rs fn reset). */
 int dory_reset(dory_t *d, int32_t seq);
+
+/* Forget the rows of sequence `seq` from position n on (dory.rs DoryState::rollback, which
+ * serves a rejected speculation or a new turn that rewrites the end of the last one): every
+ * slot keeps its rows at positions < n and the sequence's position becomes min(pos, n). On
+ * q8_2f rings the dropped rows leave the store as kv_cache.rs fn truncate_last drops them: a
+ * field that froze stays frozen, and a slot that has not frozen yet counts only the rows it
+ * keeps toward the 64 the freeze waits for. A ring keeps window + 64 + 448 rows (page
+ * "src/gpu_metal/dory.rs", fn run: the chunk and the REWIND rows), so a rollback may go back
+ * as long as every window that reads a row before n still finds its rows: at most
+ * rows - window + 1 positions on a sliding ring (513 with the pages' sizes); a full layer
+ * without full_window holds every position. n >= the position changes nothing.
+ * Errors: DORY_EINVAL (seq, n < 0), DORY_ERANGE (further back than a ring keeps; nothing
+ * changed), DORY_ECUDA. */
+int dory_rollback(dory_t *d, int32_t seq, int32_t n);
 
 /* One prefill chunk of `n` (1..64) rows of sequence `seq` at positions pos0..pos0+n-1
  * (dory.rs fn forward_host for one chunk): pos0 must equal the sequence's position
@@ -139,15 +157,57 @@ int dory_reset(dory_t *d, int32_t seq);
 int dory_prefill_chunk(dory_t *d, int32_t seq, const int32_t *ids, int32_t n, int32_t pos0,
                        int32_t loops, int32_t want);
 
+/* Prefill chunks of several sequences in one step (the chunk of dory.rs fn forward_host for
+ * each, at that sequence's position): sequence seqs[j] takes counts[j] (1..64) rows, ids
+ * [sum of counts] holding each sequence's rows in turn. Every projection runs once over all
+ * the rows; each sequence's rows attend causally to their own rings. `loops`, `want` and
+ * prompt_loops as in dory_prefill_chunk, for every sequence. Logits: want last gives one row
+ * per sequence (row j = sequence seqs[j]'s last row), want all every row in the order of
+ * `ids`. `seqs` and `counts` must be host pointers; at most max(64, max_batch) rows in all.
+ * Errors: DORY_EINVAL (nseq, counts, a duplicate sequence, too many rows, loops, want),
+ * DORY_ERANGE, DORY_ECUDA. */
+int dory_prefill_batch(dory_t *d, int32_t nseq, const int32_t *seqs, const int32_t *counts, const int32_t *ids,
+                       int32_t loops, int32_t want);
+
 /* One decode token for each of `batch` distinct sequences: row b is token ids[b] of
- * sequence seqs[b] at that sequence's position, a one-row chunk whose logits are read.
- * `seqs` must be a host pointer. One loop count for the whole step.
+ * sequence seqs[b] at that sequence's position, a one-row chunk whose logits are read
+ * (dory.rs fn forward_host with a chunk of t = 1 and Want::Last, once per sequence; the
+ * rows of the step share every weight pass). `seqs` must be a host pointer. One loop
+ * count for the whole step.
  * Errors: DORY_EINVAL (batch, duplicate or bad seq, loops), DORY_ERANGE, DORY_ECUDA. */
 int dory_decode_step(dory_t *d, const int32_t *ids, const int32_t *seqs, int32_t batch, int32_t loops);
 
+/* dory_decode_step with one loop count per sequence: row b runs loops[b] (1..max_loops)
+ * passes of the recurrent block, as sequence seqs[b]'s own forward would (dory.rs
+ * fn forward_host takes the loop count per call, so each row is that call for its sequence).
+ * The step runs the passes of the longest row; pass i computes only the rows with more than
+ * i loops, so a row's later passes neither cost weight-streaming rows nor write KV rows.
+ * `loops` must be a host pointer [batch]. Logits and hidden rows come back in the caller's
+ * order (row b = seqs[b]). Equal counts take dory_decode_step.
+ * Errors: as dory_decode_step. */
+int dory_decode_ragged(dory_t *d, const int32_t *ids, const int32_t *seqs, int32_t batch, const int32_t *loops);
+
+/* One decode token of one sequence under the Conf(th) early-exit gate (dory.rs enum Gate,
+ * fn stack's early-exit block, struct ExitRate, fn top_prob; the Metal path's token gate in
+ * page "src/gpu_metal/dory.rs", fn forward's run stages). The sequence's exit rate decides
+ * whether the token reads out after its first pass: while the rate of early exits is at least
+ * 0.35, and for one token in eight below it. A read-out runs the first pass, the output block
+ * and the head, and takes top_prob of the logits (the largest softmax probability, from the
+ * entries within 20 of the top); top_prob >= th ends the token there, with those logits. A
+ * token that stays (or does not read out) runs a second recurrent pass from the first pass's
+ * state and input, then the output block and head again; the second output block rewrites
+ * the rows the read-out appended in both KV modes. So a token makes 1 or 2 passes whatever
+ * the handle's loop count. `id`: one int32 token id (host or device). *passes gets 1 or 2,
+ * *top_prob the read-out's top probability or NaN without a read-out (either may be NULL).
+ * The decision needs the probability on the host: a read-out synchronises the stream.
+ * dory_reset restores the sequence's exit rate to its start (1.0, no tokens).
+ * Errors: DORY_EINVAL (seq, th NaN, max_loops < 2), DORY_ERANGE, DORY_ECUDA. */
+int dory_decode_conf(dory_t *d, const int32_t *id, int32_t seq, float th, int32_t *passes, float *top_prob);
+
 /* Copy the logits of row `row` of the last call that produced logits ([vocab] f32,
- * logit_scale applied) to dst, which has room for `cap` floats. Decode: row = batch index.
- * Prefill: want last gives row 0 only, want all rows 0..n-1.
+ * logits = (H h) * logit_scale per vocabulary row, dory.rs fn head) to dst, which has room
+ * for `cap` floats. Decode: row = batch index. Prefill: want last gives row 0 only (the
+ * chunk's last row, Want::Last), want all rows 0..n-1 (Want::All).
  * Errors: DORY_EINVAL (row, cap < vocab), DORY_ESTATE (no logits yet). */
 int dory_logits(dory_t *d, int32_t row, float *dst, size_t cap);
 
@@ -220,7 +280,9 @@ int dory_get_stats(dory_t *d, dory_stats *out);
  * Working memory: a static device array of about 290 KB inside the library (the row
  * counters and the first 64 rows the freeze reads back), held by every GPU that loads the
  * library until the process exits. The first call on a device looks up that array's device
- * address (cudaGetSymbolAddress) and must come before any stream capture on that device.
+ * address (cudaGetSymbolAddress) and must come before any stream capture on that device; so
+ * must the first call after a cudaDeviceReset of that device, which ends the context the
+ * address belonged to (the library notices the new context and looks the address up again).
  * Every call clears the counters it needs at zero; calls share the array, so two calls
  * whose work overlaps on the GPU race and must not be made. Errors: DORY_EINVAL,
  * DORY_ECUDA; the message is dory_last_error(). */

@@ -4,6 +4,7 @@
 #include <algorithm>
 #include <array>
 #include <climits>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -39,6 +40,8 @@ int fail(int code, const char *fmt, ...) {
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 constexpr int KEYS_PER_SPLIT = 128;
+// arrays of a step's row table: seq, off, advance seq, advance count, order, head rows
+constexpr int ROW_TABLE = 6;
 constexpr int RING_EXTRA = 64 + 448;  // a chunk and the rewind slack (gpu_metal/dory.rs fn run)
 
 struct LayerDev {
@@ -61,10 +64,28 @@ int bn_index(int bn) { return bn <= 16 ? 0 : bn <= 32 ? 1 : bn <= 64 ? 2 : bn <=
 
 struct Plan {
   cudaGraphExec_t exec = nullptr;
+  uint64_t used = 0;  // the handle's step counter at its last replay (least recently used goes first)
   int32_t *rt = nullptr;  // the captured step's own row table
   MegaStage *stages = nullptr;  // the persistent decode kernel's stage list (device)
   int launches = 0, gemm_launches = 0;
   float *h_last = nullptr;
+};
+
+// dory.rs struct ExitRate: the rate of tokens whose first read-out ended them; below 0.35 a
+// token goes straight to its second pass, except one token in eight, which still reads out.
+// f32 steps as the page writes them (the host code is built without contracted multiply-adds).
+struct ExitRate {
+  float rate = 1.0f;
+  uint32_t tokens = 0;
+  bool probe() {
+    tokens += 1;  // wraps like the page's u32
+    return rate >= 0.35f || tokens % 8 == 0;
+  }
+  void note(bool exited) {
+    const float diff = (exited ? 1.0f : 0.0f) - rate;
+    const float step = 0.1f * diff;
+    rate = rate + step;
+  }
 };
 
 struct OrdInfo {
@@ -131,15 +152,22 @@ struct dory_handle {
   int32_t *tc_ctr = nullptr, *tc_err = nullptr;
   float *h = nullptr, *input = nullptr, *state = nullptr, *qkvg = nullptr, *z = nullptr, *out = nullptr,
         *mlp = nullptr, *logits = nullptr, *rope = nullptr, *part = nullptr, *kst = nullptr, *vst = nullptr;
-  int32_t *d_ids = nullptr, *d_seq_pos = nullptr, *d_zero = nullptr;
+  float *logits2 = nullptr;  // logits of a reordered step, before they go back to the caller's order
+  int32_t *d_ids = nullptr, *d_ids2 = nullptr, *d_seq_pos = nullptr, *d_zero = nullptr;
   char *act = nullptr;
   char *tcmem = nullptr;
 
   cudaStream_t cap_stream = nullptr;  // graphs are captured here and replayed on `stream`
   bool use_graphs = true;
   std::unordered_map<std::string, Plan> plans;
-  int32_t *d_rows = nullptr;  // step table when graphs are off: seq, off, advance seq, count
+  size_t max_plans = 256;  // captured steps kept at most (DORY_MAX_PLANS); the least recently used goes
+  uint64_t steps = 0;
+  int32_t *d_rows = nullptr;  // step table when graphs are off: seq, off, advance seq, count, order
 
+  std::vector<ExitRate> exits;      // per sequence: the Conf gate's exit rate
+  float *d_top = nullptr;           // the gate's top probability of the last read-out
+  long long *slot_table = nullptr;  // per flat slot: tags offset, meta offset, ring rows (rollback)
+  int32_t *dropped = nullptr;       // per flat slot: rows the last rollback dropped
   std::vector<int> seq_pos;     // host mirror of d_seq_pos
   std::vector<int> appended;    // rows appended per (seq, ordinal, slot)
   std::vector<int> slot_index;  // first flat slot index of each ordinal
@@ -247,6 +275,7 @@ int reset_seq(dory_t *d, int seq) {
     }
   CK(cudaMemsetAsync(d->d_seq_pos + seq, 0, 4, d->stream));
   d->seq_pos[seq] = 0;
+  if ((size_t)seq < d->exits.size()) d->exits[seq] = ExitRate{};
   for (int i = 0; i < d->n_flat_slots; i++) d->appended[(size_t)seq * d->n_flat_slots + i] = 0;
   return DORY_OK;
 }
@@ -254,13 +283,39 @@ int reset_seq(dory_t *d, int seq) {
 // The rows of one step: row r is sequence hseq[r] at position seq_pos[hseq[r]] + hoff[r];
 // aseq/acnt are the position advances at the step's end. `loops` recurrent passes; logits
 // for head_rows rows starting at row head_from.
+// `resume`: the second pass of an early-exit gate that stayed (dory.rs fn stack): no
+// embedding or input block; h = (state + input)^ from the saved rows, recurrent passes
+// first_loop..loops-1, and the output block rewrites the rows its read-out appended.
+// `rl`: per-row loop counts (empty: every row runs `loops`), sorted from the most loops down
+// so that the rows a pass runs are a prefix; `perm[r]` is the caller's index of row r (ids
+// are gathered into this order, logits and hidden rows scattered back).
 struct StepArgs {
-  int T = 0, loops = 1, head_from = 0, head_rows = 0;
-  std::vector<int> hseq, hoff, aseq, acnt;
+  int T = 0, loops = 1, head_from = 0, head_rows = 0, first_loop = 0;
+  bool resume = false;
+  std::vector<int> hseq, hoff, aseq, acnt, rl, perm;
+  // rows whose logits are read when they are not one run (the last row of each sequence of a
+  // batched prefill): the head covers rows [0, T) and these rows are gathered, in order
+  std::vector<int> head_pick;
+  // rows that run pass i
+  int active(int i) const {
+    if (i >= loops) return 0;
+    if (rl.empty()) return T;
+    int n = 0;
+    while (n < T && rl[n] > i) n++;
+    return n;
+  }
   std::string key() const {
     std::string k = std::to_string(T) + ":" + std::to_string(loops) + ":" + std::to_string(head_from) + ":" +
-                    std::to_string(head_rows) + "|";
+                    std::to_string(head_rows) + ":" + std::to_string(first_loop) + (resume ? "r" : "") + "|";
     for (int i = 0; i < T; i++) k += std::to_string(hseq[i]) + "," + std::to_string(hoff[i]) + ";";
+    if (!rl.empty()) {
+      k += "L";
+      for (int i = 0; i < T; i++) k += std::to_string(rl[i]) + "," + std::to_string(perm[i]) + ";";
+    }
+    if (!head_pick.empty()) {
+      k += "H";
+      for (int x : head_pick) k += std::to_string(x) + ";";
+    }
     return k;
   }
 };
@@ -275,27 +330,29 @@ void account(dory_t *d, const StepArgs &a) {
   uint64_t wb = 0, kr = 0, kw = 0;
   auto layer = [&](int li, int loop_i) {
     const LayerDev &L = d->layers[li];
+    const int rows = L.rec ? a.active(loop_i) : a.T;
     if (L.attn) {
       wb += (uint64_t)(2 * q_size + 2 * kv_size) * dm.hidden * d->esz + (uint64_t)dm.hidden * q_size * d->esz;
       const int sl = (c.kv_mode == DORY_KV_PER_LOOP && L.rec) ? loop_i : 0;
-      const bool rewrite = c.kv_mode == DORY_KV_LAST_LOOP && (L.rec || L.out) && loop_i > 0;
+      const bool rewrite = (c.kv_mode == DORY_KV_LAST_LOOP && (L.rec || L.out) && loop_i > 0) || (a.resume && L.out);
       const OrdInfo &o = d->ords[L.ordinal];
-      for (int r = 0; r < a.T; r++) {
+      for (int r = 0; r < rows; r++) {
         const long p = (long)d->seq_pos[a.hseq[r]] + a.hoff[r];
         const long keys = o.window == INT_MAX ? p + 1 : std::min<long>(o.window, p + 1);
         kr += (uint64_t)keys * dm.nk * kv_row_bytes;
         if (!rewrite) d->app(a.hseq[r], L.ordinal, sl)++;
       }
-      kw += (uint64_t)a.T * dm.nk * kv_row_bytes;
+      kw += (uint64_t)rows * dm.nk * kv_row_bytes;
     } else {
       wb += (uint64_t)3 * dm.ffn * dm.hidden * d->esz;
     }
   };
   const int n_in = c.n_in, n_rec = c.n_rec, n_all = (int)d->layers.size();
-  for (int li = 0; li < n_in; li++) layer(li, 0);
-  for (int i = 0; i < a.loops; i++)
+  if (!a.resume)
+    for (int li = 0; li < n_in; li++) layer(li, 0);
+  for (int i = a.first_loop; i < a.loops; i++)
     for (int li = n_in; li < n_in + n_rec; li++) layer(li, i);
-  for (int li = n_in + n_rec; li < n_all; li++) layer(li, 0);
+  for (int li = n_in + n_rec; li < n_all; li++) layer(li, a.resume ? 1 : 0);
   if (a.head_rows > 0) wb += (uint64_t)dm.vocab * dm.hidden * d->esz;
   d->st.weight_bytes = wb;
   d->st.kv_read_bytes = kr;
@@ -321,9 +378,14 @@ int issue_step(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_splits, cud
   const dory_config &c = d->cfg;
   const Dims dm = d->dims;
   const int T = a.T;
-  // rows 0..T-1 are consecutive positions of one sequence (a prefill chunk)
-  bool chunk_rows = T > 1 && !getenv_off("DORY_CHUNK_ATTN");
-  for (int r = 1; r < T && chunk_rows; r++) chunk_rows = a.hseq[r] == a.hseq[0] && a.hoff[r] == a.hoff[0] + r;
+  // runs of rows that are consecutive positions of one sequence (prefill chunks); when some
+  // run has two rows or more, each run's attention takes the chunk kernel
+  std::vector<std::pair<int, int>> segs;  // (first row, rows)
+  for (int r = 0; r < T; r++) {
+    if (r > 0 && a.hseq[r] == a.hseq[r - 1] && a.hoff[r] == a.hoff[r - 1] + 1) segs.back().second++;
+    else segs.push_back({r, 1});
+  }
+  const bool chunk_rows = (int)segs.size() < T && !getenv_off("DORY_CHUNK_ATTN");
   Rows rows;
   rows.seq = rt;
   rows.off = rt + d->Tmax;
@@ -337,7 +399,15 @@ int issue_step(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_splits, cud
   const bool q8 = c.kv_quant == DORY_KV_Q8_2F;
 
   const bool tc = d->tc_ok && T >= 5;
-  CK(launch_embed_rope(d->d_ids, d->embed, d->wdtype, dm, rows, c.rope_theta_sliding, c.rope_theta_full, d->h,
+  const bool ragged = !a.rl.empty();
+  const int32_t *perm = rt + 4 * d->Tmax;
+  const int32_t *ids = d->d_ids;
+  if (ragged) {  // the caller's ids in the step's row order
+    CK(launch_gather_ids(d->d_ids, perm, T, d->d_ids2, s));
+    nl++;
+    ids = d->d_ids2;
+  }
+  CK(launch_embed_rope(ids, d->embed, d->wdtype, dm, rows, c.rope_theta_sliding, c.rope_theta_full, d->h,
                        d->rope, tc ? d->em_h : Emit{nullptr, nullptr}, s));
   nl++;
   auto tcg = [&](const TcW &w, int xbuf, int rowsT, int t_base, float *Y, int ldy, EpiArgs ep) -> int {
@@ -363,124 +433,169 @@ int issue_step(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_splits, cud
     ng++;
     return DORY_OK;
   };
-  auto gemm = [&](const void *W, int N, int K, const float *X, int ldx, float *Y, int ldy, EpiArgs ep) -> int {
-    CK(launch_gemm(W, d->wdtype, N, K, X, ldx, T, Y, ldy, ep, s));
+  auto gemm = [&](const void *W, int N, int K, const float *X, int ldx, int Tr, float *Y, int ldy,
+                  EpiArgs ep) -> int {
+    CK(launch_gemm(W, d->wdtype, N, K, X, ldx, Tr, Y, ldy, ep, s));
     nl++;
     ng++;
     return DORY_OK;
   };
-  auto layer = [&](int li, int loop_i, int mix) -> int {
+  // The residual of rows [0, Tr) with the loop mix `mix` for rows [0, Tsplit) and MIX_END for
+  // rows [Tsplit, Tr) (rows whose last pass this is, when loop counts differ per row).
+  auto resid = [&](const float *alpha, int mix, int Tr, int Tsplit, int do_res) -> int {
+    const Emit em = tc ? d->em_h : Emit{nullptr, nullptr};
+    if (Tsplit > 0) {
+      CK(launch_residual(d->h, d->out, alpha, Tsplit, dm.hidden, mix, d->input, d->state, do_res, em, s));
+      nl++;
+    }
+    if (Tr > Tsplit) {
+      const size_t o = (size_t)Tsplit * dm.hidden;
+      const Emit e2 = em.hi ? Emit{em.hi + o, em.lo + o} : em;
+      CK(launch_residual(d->h + o, d->out + o, alpha, Tr - Tsplit, dm.hidden, MIX_END, d->input + o, d->state + o,
+                         do_res, e2, s));
+      nl++;
+    }
+    return DORY_OK;
+  };
+  auto layer = [&](int li, int loop_i, int mix, int Tr, int Tsplit) -> int {
     const LayerDev &L = d->layers[li];
     int rc;
+    Rows rows_l = rows;
+    rows_l.n = Tr;
     if (L.attn) {
       const int sl = (c.kv_mode == DORY_KV_PER_LOOP && L.rec) ? loop_i : 0;
-      const bool rewrite = c.kv_mode == DORY_KV_LAST_LOOP && (L.rec || L.out) && loop_i > 0;
+      const bool rewrite = (c.kv_mode == DORY_KV_LAST_LOOP && (L.rec || L.out) && loop_i > 0) || (a.resume && L.out);
       Ring ring = d->ring(L.ordinal, sl);
       EpiArgs ep{EPI_STORE, nullptr, nullptr, 0};
       if (tc) {
-        if ((rc = tcg(d->tcw[li][0], 0, T, 0, d->qkvg, ldq, ep))) return rc;
-      } else if ((rc = gemm(L.wqkvg, ldq, dm.hidden, d->h, dm.hidden, d->qkvg, ldq, ep))) {
+        if ((rc = tcg(d->tcw[li][0], 0, Tr, 0, d->qkvg, ldq, ep))) return rc;
+      } else if ((rc = gemm(L.wqkvg, ldq, dm.hidden, d->h, dm.hidden, Tr, d->qkvg, ldq, ep))) {
         return rc;
       }
-      CK(launch_prep(d->qkvg, ldq, dm, rows, d->rope, L.sliding ? 0 : 1, L.sq, ring, d->kst, d->vst, s));
+      CK(launch_prep(d->qkvg, ldq, dm, rows_l, d->rope, L.sliding ? 0 : 1, L.sq, ring, d->kst, d->vst, s));
       nl++;
       if (q8) {
-        CK(launch_q8_append(d->kst, d->vst, kv_size, dm, rows, ring, rewrite ? 1 : 0, s));
+        CK(launch_q8_append(d->kst, d->vst, kv_size, dm, rows_l, ring, rewrite ? 1 : 0, s));
         nl++;
       }
       const long wmax = ring.window == INT_MAX ? (long)ring.cap : std::min<long>(ring.window, ring.cap);
       const long keys = fixed_splits ? wmax : std::min<long>(wmax, pmax + 1);
       const int splits = (int)((keys + KEYS_PER_SPLIT - 1) / KEYS_PER_SPLIT);
       if (splits > d->max_splits) return fail(DORY_ERANGE, "attention needs %d splits (max %d)", splits, d->max_splits);
-      const int nkb = attn_chunk_blocks(wmax, T);
       bool z_normed = false;
-      if (chunk_rows && !q8 && (dm.hd == 64 || dm.hd == 128) && nkb <= d->max_splits) {
-        // a prefill chunk: the rows share every key block; the merge also row-normalises z
-        CK(launch_attention_chunk(d->qkvg, ldq, dm, rows, ring, nkb, d->part, L.sg, d->z,
-                                  tc ? d->em_z : Emit{nullptr, nullptr}, s));
-        nl += 2;
+      if (chunk_rows && Tr == T && !q8 && (dm.hd == 64 || dm.hd == 128)) {
+        // prefill chunks: a chunk's rows share every key block; the merge also row-normalises z
+        for (const auto &sg_ : segs) {
+          const int r0 = sg_.first, n = sg_.second;
+          const int nkb = attn_chunk_blocks(wmax, n);
+          if (nkb > d->max_splits) return fail(DORY_ERANGE, "chunk attention needs %d key blocks", nkb);
+          Rows rs = rows_l;
+          rs.seq = rows_l.seq + r0;
+          rs.off = rows_l.off + r0;
+          rs.n = n;
+          const size_t zo = (size_t)r0 * q_size;
+          const Emit ez = tc ? Emit{d->em_z.hi + zo, d->em_z.lo + zo} : Emit{nullptr, nullptr};
+          CK(launch_attention_chunk(d->qkvg + (size_t)r0 * ldq, ldq, dm, rs, ring, nkb, d->part, L.sg, d->z + zo, ez,
+                                    s));
+          nl += 2;
+        }
         z_normed = true;
       } else if (!q8 && (dm.hd == 64 || dm.hd == 128) && !getenv_off("DORY_STREAM_ATTN")) {
         // rows of separate sequences: each (row, kv head) streams its own window
-        CK(launch_attention_stream(d->qkvg, ldq, dm, rows, ring, L.sg, d->z, d->dev_err, s));
+        CK(launch_attention_stream(d->qkvg, ldq, dm, rows_l, ring, L.sg, d->z, d->dev_err, s));
         nl += 1;
       } else if (d->kv_tma || d->kv_tma_q8) {
         const int tsp = fixed_splits ? attn_tma_splits(wmax) : tma_splits(d, a, ring);
         if (d->kv_tma)
-          CK(launch_attention_tma(d->kvmap, d->qkvg, ldq, dm, rows, ring, tsp, d->part, L.sg, d->z, d->actr,
+          CK(launch_attention_tma(d->kvmap, d->qkvg, ldq, dm, rows_l, ring, tsp, d->part, L.sg, d->z, d->actr,
                                   d->dev_err, true, s));
         else
-          CK(launch_attention_tma_q8(d->kvq, d->qkvg, ldq, dm, rows, ring, tsp, d->part, L.sg, d->z, d->actr,
+          CK(launch_attention_tma_q8(d->kvq, d->qkvg, ldq, dm, rows_l, ring, tsp, d->part, L.sg, d->z, d->actr,
                                      d->dev_err, true, s));
         nl += 1;
       } else if (tc) {
-        CK(launch_attention_fused(d->qkvg, ldq, dm, rows, ring, splits, KEYS_PER_SPLIT, d->part, L.sg, d->z, d->actr,
-                                  true, s));
+        CK(launch_attention_fused(d->qkvg, ldq, dm, rows_l, ring, splits, KEYS_PER_SPLIT, d->part, L.sg, d->z,
+                                  d->actr, true, s));
         nl += 1;
       } else {
-        CK(launch_attention(d->qkvg, ldq, dm, rows, ring, splits, KEYS_PER_SPLIT, d->part, L.sg, d->z, s));
+        CK(launch_attention(d->qkvg, ldq, dm, rows_l, ring, splits, KEYS_PER_SPLIT, d->part, L.sg, d->z, s));
         nl += 2;
       }
       if (!z_normed) {
-        CK(launch_rownorm(d->z, T, q_size, q_size, tc ? d->em_z : Emit{nullptr, nullptr}, s));
+        CK(launch_rownorm(d->z, Tr, q_size, q_size, tc ? d->em_z : Emit{nullptr, nullptr}, s));
         nl++;
       }
       if (tc) {
-        if ((rc = tcg(d->tcw[li][1], 1, T, 0, d->out, dm.hidden, ep))) return rc;
-      } else if ((rc = gemm(L.wo, dm.hidden, q_size, d->z, q_size, d->out, dm.hidden, ep))) {
+        if ((rc = tcg(d->tcw[li][1], 1, Tr, 0, d->out, dm.hidden, ep))) return rc;
+      } else if ((rc = gemm(L.wo, dm.hidden, q_size, d->z, q_size, Tr, d->out, dm.hidden, ep))) {
         return rc;
       }
     } else {
       EpiArgs ep{EPI_SILU, L.msg, L.msu, (long)dm.ffn};
       if (tc) {
-        if ((rc = tcg(d->tcw[li][0], 0, T, 0, d->mlp, dm.ffn, ep))) return rc;
-      } else if ((rc = gemm(L.wgu, dm.ffn, dm.hidden, d->h, dm.hidden, d->mlp, dm.ffn, ep))) {
+        if ((rc = tcg(d->tcw[li][0], 0, Tr, 0, d->mlp, dm.ffn, ep))) return rc;
+      } else if ((rc = gemm(L.wgu, dm.ffn, dm.hidden, d->h, dm.hidden, Tr, d->mlp, dm.ffn, ep))) {
         return rc;
       }
-      CK(launch_rownorm(d->mlp, T, dm.ffn, dm.ffn, tc ? d->em_y : Emit{nullptr, nullptr}, s));
+      CK(launch_rownorm(d->mlp, Tr, dm.ffn, dm.ffn, tc ? d->em_y : Emit{nullptr, nullptr}, s));
       nl++;
       EpiArgs e2{EPI_STORE, nullptr, nullptr, 0};
       if (tc) {
-        if ((rc = tcg(d->tcw[li][1], 2, T, 0, d->out, dm.hidden, e2))) return rc;
-      } else if ((rc = gemm(L.wdown, dm.hidden, dm.ffn, d->mlp, dm.ffn, d->out, dm.hidden, e2))) {
+        if ((rc = tcg(d->tcw[li][1], 2, Tr, 0, d->out, dm.hidden, e2))) return rc;
+      } else if ((rc = gemm(L.wdown, dm.hidden, dm.ffn, d->mlp, dm.ffn, Tr, d->out, dm.hidden, e2))) {
         return rc;
       }
     }
-    CK(launch_residual(d->h, d->out, L.alpha, T, dm.hidden, mix, d->input, d->state, 1,
-                       tc ? d->em_h : Emit{nullptr, nullptr}, s));
-    nl++;
-    return DORY_OK;
+    return resid(L.alpha, mix, Tr, Tsplit, 1);
   };
-  auto mix_only = [&](int mix) -> int {
-    CK(launch_residual(d->h, d->out, nullptr, T, dm.hidden, mix, d->input, d->state, 0,
-                       tc ? d->em_h : Emit{nullptr, nullptr}, s));
-    nl++;
-    return DORY_OK;
-  };
+  auto mix_only = [&](int mix, int Tr, int Tsplit) -> int { return resid(nullptr, mix, Tr, Tsplit, 0); };
 
   int rc;
   const int n_in = c.n_in, n_rec = c.n_rec, n_all = (int)d->layers.size();
-  for (int li = 0; li < n_in; li++)
-    if ((rc = layer(li, 0, li == n_in - 1 ? MIX_BEGIN : MIX_NONE))) return rc;
-  if (n_in == 0 && (rc = mix_only(MIX_BEGIN))) return rc;
-  for (int i = 0; i < a.loops; i++) {
-    const int m = i == a.loops - 1 ? MIX_END : MIX_LOOP;
-    for (int li = n_in; li < n_in + n_rec; li++)
-      if ((rc = layer(li, i, li == n_in + n_rec - 1 ? m : MIX_NONE))) return rc;
-    if (n_rec == 0 && (rc = mix_only(m))) return rc;
+  if (a.resume) {
+    if ((rc = mix_only(MIX_RESUME, T, T))) return rc;
+  } else {
+    for (int li = 0; li < n_in; li++)
+      if ((rc = layer(li, 0, li == n_in - 1 ? MIX_BEGIN : MIX_NONE, T, T))) return rc;
+    if (n_in == 0 && (rc = mix_only(MIX_BEGIN, T, T))) return rc;
+  }
+  // pass i runs the rows that still loop (a prefix); at its end those with more passes to go
+  // mix for the next pass and the others end (state = h^, h = state)
+  for (int i = a.first_loop; i < a.loops; i++) {
+    const int Ti = a.active(i), Tn = a.active(i + 1);
+    for (int li = n_in; li < n_in + n_rec; li++) {
+      const bool last = li == n_in + n_rec - 1;
+      if ((rc = layer(li, i, last ? MIX_LOOP : MIX_NONE, Ti, last ? Tn : Ti))) return rc;
+    }
+    if (n_rec == 0 && (rc = mix_only(MIX_LOOP, Ti, Tn))) return rc;
   }
   for (int li = n_in + n_rec; li < n_all; li++)
-    if ((rc = layer(li, 0, MIX_NONE))) return rc;
+    if ((rc = layer(li, a.resume ? 1 : 0, MIX_NONE, T, T))) return rc;
   if (a.head_rows > 0) {
     EpiArgs ep{EPI_SCALE, d->logit_scale, nullptr, 0};
+    const bool pick = !a.head_pick.empty();
+    float *lg = ragged || pick ? d->logits2 : d->logits;
     if (tc && a.head_rows >= 5) {
-      if ((rc = tcg(d->tc_head, 0, a.head_rows, a.head_from, d->logits, dm.vocab, ep))) return rc;
+      if ((rc = tcg(d->tc_head, 0, a.head_rows, a.head_from, lg, dm.vocab, ep))) return rc;
     } else {
       CK(launch_gemm(d->head, d->wdtype, dm.vocab, dm.hidden, d->h + (size_t)a.head_from * dm.hidden, dm.hidden,
-                     a.head_rows, d->logits, dm.vocab, ep, s));
+                     a.head_rows, lg, dm.vocab, ep, s));
       nl++;
       ng++;
     }
+    if (ragged) {  // logits rows back in the caller's order
+      CK(launch_scatter_rows(lg, d->logits, perm, T, dm.vocab, s));
+      nl++;
+    }
+    if (pick) {  // the wanted rows, in order
+      CK(launch_gather_rows(lg, d->logits, rt + 5 * d->Tmax, (int)a.head_pick.size(), dm.vocab, s));
+      nl++;
+    }
+  }
+  if (ragged) {  // and the final hidden rows
+    CK(launch_scatter_rows(d->h, d->h2, perm, T, dm.hidden, s));
+    nl++;
+    d->h_last = d->h2;
   }
   CK(launch_advance(d->d_seq_pos, rt + 2 * d->Tmax, rt + 3 * d->Tmax, (int)a.aseq.size(), s));
   nl++;
@@ -518,9 +633,23 @@ int issue_step_fused(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_split
     bool on = false;
     const float *alpha = nullptr;
     int mix = MIX_NONE;
+    bool resume = false;
   } pend;
+  pend.resume = a.resume;
   auto first_in = [&]() {
     GemvIn g{};
+    if (pend.resume) {  // h = (state + input)^ from the saved rows
+      g.mode = IN_RESID;
+      g.src = d->state;
+      g.ld = dm.hidden;
+      g.mix = MIX_RESUME;
+      g.h_dst = other;
+      g.input = d->input;
+      g.state = d->state;
+      std::swap(cur, other);
+      pend.resume = false;
+      return g;
+    }
     if (!pend.on) {
       g.mode = IN_PLAIN;
       g.src = cur;
@@ -546,7 +675,7 @@ int issue_step_fused(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_split
     const LayerDev &L = d->layers[li];
     if (L.attn) {
       const int sl = (c.kv_mode == DORY_KV_PER_LOOP && L.rec) ? loop_i : 0;
-      const bool rewrite = c.kv_mode == DORY_KV_LAST_LOOP && (L.rec || L.out) && loop_i > 0;
+      const bool rewrite = (c.kv_mode == DORY_KV_LAST_LOOP && (L.rec || L.out) && loop_i > 0) || (a.resume && L.out);
       Ring ring = d->ring(L.ordinal, sl);
       HeadEpi he{};
       he.enabled = 1;
@@ -610,15 +739,16 @@ int issue_step_fused(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_split
   };
   int rc;
   const int n_in = c.n_in, n_rec = c.n_rec, n_all = (int)d->layers.size();
-  for (int li = 0; li < n_in; li++)
-    if ((rc = layer(li, 0, li == n_in - 1 ? MIX_BEGIN : MIX_NONE))) return rc;
-  for (int i = 0; i < a.loops; i++) {
+  if (!a.resume)
+    for (int li = 0; li < n_in; li++)
+      if ((rc = layer(li, 0, li == n_in - 1 ? MIX_BEGIN : MIX_NONE))) return rc;
+  for (int i = a.first_loop; i < a.loops; i++) {
     const int m = i == a.loops - 1 ? MIX_END : MIX_LOOP;
     for (int li = n_in; li < n_in + n_rec; li++)
       if ((rc = layer(li, i, li == n_in + n_rec - 1 ? m : MIX_NONE))) return rc;
   }
   for (int li = n_in + n_rec; li < n_all; li++)
-    if ((rc = layer(li, 0, MIX_NONE))) return rc;
+    if ((rc = layer(li, a.resume ? 1 : 0, MIX_NONE))) return rc;
   EpiArgs eh{EPI_SCALE, d->logit_scale, nullptr, 0};
   if (a.head_rows == T && a.head_from == 0) {
     CK(launch_gemv_fused(d->head, d->wdtype, dm.vocab, dm.hidden, T, first_in(), d->logits, dm.vocab, eh, none, d->dev_err,
@@ -646,7 +776,8 @@ int issue_step_fused(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_split
 }
 
 int issue_any(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_splits, cudaStream_t s, int *nl, int *ng) {
-  if (d->fused_ok && a.T <= 4) return issue_step_fused(d, a, rt, fixed_splits, s, nl, ng);
+  if (d->fused_ok && a.T <= 4 && a.rl.empty() && a.head_pick.empty())
+    return issue_step_fused(d, a, rt, fixed_splits, s, nl, ng);
   d->h_last = d->h;
   return issue_step(d, a, rt, fixed_splits, s, nl, ng);
 }
@@ -674,6 +805,17 @@ int mega_build(dory_t *d, const StepArgs &a, int32_t *rt, std::vector<MegaStage>
   auto first_in = [&]() {
     GemvIn g{};
     g.ld = dm.hidden;
+    if (first && a.resume) {  // h = (state + input)^ from the saved rows
+      first = false;
+      g.mode = IN_RESID;
+      g.src = d->state;
+      g.mix = MIX_RESUME;
+      g.h_dst = other;
+      g.input = d->input;
+      g.state = d->state;
+      std::swap(cur, other);
+      return g;
+    }
     if (first) {  // the token's embedding row, stored as the hidden row
       first = false;
       g.mode = IN_EMBED;
@@ -749,12 +891,13 @@ int mega_build(dory_t *d, const StepArgs &a, int32_t *rt, std::vector<MegaStage>
     pend.mix = mix;
   };
   const int n_in = c.n_in, n_rec = c.n_rec, n_all = (int)d->layers.size();
-  for (int li = 0; li < n_in; li++) layer(li, 0, li == n_in - 1 ? MIX_BEGIN : MIX_NONE);
-  for (int i = 0; i < a.loops; i++) {
+  if (!a.resume)
+    for (int li = 0; li < n_in; li++) layer(li, 0, li == n_in - 1 ? MIX_BEGIN : MIX_NONE);
+  for (int i = a.first_loop; i < a.loops; i++) {
     const int m = i == a.loops - 1 ? MIX_END : MIX_LOOP;
     for (int li = n_in; li < n_in + n_rec; li++) layer(li, i, li == n_in + n_rec - 1 ? m : MIX_NONE);
   }
-  for (int li = n_in + n_rec; li < n_all; li++) layer(li, 0, MIX_NONE);
+  for (int li = n_in + n_rec; li < n_all; li++) layer(li, 0, MIX_NONE);  // f32 rings: the same row is rewritten
   gemv(d->head, dm.vocab, dm.hidden, 0, first_in(), d->logits, EpiArgs{EPI_SCALE, d->logit_scale, nullptr, 0});
   *h_last = cur;
   if (d->mega_trace) {
@@ -803,11 +946,13 @@ int count_gemv(const std::vector<MegaStage> &st) {
 }
 
 int upload_table(dory_t *d, const StepArgs &a, int32_t *rt, cudaStream_t s) {
-  std::vector<int32_t> t((size_t)4 * d->Tmax, 0);
+  std::vector<int32_t> t((size_t)ROW_TABLE * d->Tmax, 0);
   for (int i = 0; i < a.T; i++) {
     t[i] = a.hseq[i];
     t[d->Tmax + i] = a.hoff[i];
+    t[4 * d->Tmax + i] = a.perm.empty() ? i : a.perm[i];
   }
+  for (size_t j = 0; j < a.head_pick.size(); j++) t[5 * d->Tmax + j] = a.head_pick[j];
   for (size_t i = 0; i < a.aseq.size(); i++) {
     t[2 * d->Tmax + i] = a.aseq[i];
     t[3 * d->Tmax + i] = a.acnt[i];
@@ -852,9 +997,22 @@ int do_step(dory_t *d, const StepArgs &a, const int32_t *ids) {
   } else {
     const std::string key = a.key();
     auto it = d->plans.find(key);
-    if (it == d->plans.end()) {
+    const bool found = it != d->plans.end();
+    if (!found && d->plans.size() >= d->max_plans) {
+      // a server whose batches keep changing would grow without bound: drop the plan replayed
+      // longest ago (after the work queued so far, which may still replay it)
+      auto old = d->plans.begin();
+      for (auto j = d->plans.begin(); j != d->plans.end(); ++j)
+        if (j->second.used < old->second.used) old = j;
+      CK(cudaStreamSynchronize(d->stream));
+      cudaGraphExecDestroy(old->second.exec);
+      if (old->second.rt) cudaFree(old->second.rt);
+      if (old->second.stages) cudaFree(old->second.stages);
+      d->plans.erase(old);
+    }
+    if (!found) {
       Plan p;
-      if (cudaMalloc(&p.rt, (size_t)4 * d->Tmax * 4) != cudaSuccess) {
+      if (cudaMalloc(&p.rt, (size_t)ROW_TABLE * d->Tmax * 4) != cudaSuccess) {
         cudaGetLastError();
         return fail(DORY_ENOMEM, "cudaMalloc of a step table");
       }
@@ -902,6 +1060,7 @@ int do_step(dory_t *d, const StepArgs &a, const int32_t *ids) {
       }
       it = d->plans.emplace(key, p).first;
     }
+    it->second.used = ++d->steps;
     CK(cudaGraphLaunch(it->second.exec, d->stream));
     d->h_last = it->second.h_last;
     d->st.launches = it->second.launches;
@@ -1207,10 +1366,13 @@ int dory_create(const dory_config *cfg, const dory_weights *w, void *stream, dor
                a_rope = areserve((size_t)T * 2 * dm.hd * 4),
                a_part = areserve((size_t)T * dm.nk * d->max_splits * rep * (dm.hd + 2) * 4),
                a_kst = areserve((size_t)T * kv_size * 4), a_vst = areserve((size_t)T * kv_size * 4),
-               a_ids = areserve((size_t)T * 4),
-               a_sp = areserve((size_t)cfg->max_seqs * 4), a_rows = areserve((size_t)4 * T * 4),
+               a_ids = areserve((size_t)T * 4), a_ids2 = areserve((size_t)T * 4),
+               a_lg2 = areserve((size_t)T * dm.vocab * 4),
+               a_sp = areserve((size_t)cfg->max_seqs * 4), a_rows = areserve((size_t)ROW_TABLE * T * 4),
                a_zero = areserve((size_t)cfg->max_seqs * 4), a_err = areserve(256);
   const size_t ms_bytes = (size_t)(64 + dm.nk) * 4, a_ms = areserve(ms_bytes);
+  const size_t a_stab = areserve((size_t)d->n_flat_slots * 3 * 8), a_drop = areserve((size_t)d->n_flat_slots * 4),
+               a_top = areserve(4);
   if (cudaMalloc(&d->act, ab) != cudaSuccess) {
     cudaGetLastError();
     fail(DORY_ENOMEM, "cudaMalloc of %zu activation bytes", ab);
@@ -1284,20 +1446,41 @@ int dory_create(const dory_config *cfg, const dory_weights *w, void *stream, dor
   d->kst = reinterpret_cast<float *>(A + a_kst);
   d->vst = reinterpret_cast<float *>(A + a_vst);
   d->d_ids = reinterpret_cast<int32_t *>(A + a_ids);
+  d->d_ids2 = reinterpret_cast<int32_t *>(A + a_ids2);
+  d->logits2 = reinterpret_cast<float *>(A + a_lg2);
   d->d_seq_pos = reinterpret_cast<int32_t *>(A + a_sp);
   d->d_rows = reinterpret_cast<int32_t *>(A + a_rows);
   d->d_zero = reinterpret_cast<int32_t *>(A + a_zero);
   d->dev_err = reinterpret_cast<int32_t *>(A + a_err);
+  d->slot_table = reinterpret_cast<long long *>(A + a_stab);
+  d->dropped = reinterpret_cast<int32_t *>(A + a_drop);
+  d->d_top = reinterpret_cast<float *>(A + a_top);
   if (cudaMemsetAsync(d->act, 0, ab, d->stream) != cudaSuccess) return cleanup(fail(DORY_ECUDA, "memset"));
+  {
+    std::vector<long long> t((size_t)d->n_flat_slots * 3);
+    for (size_t o = 0; o < d->ords.size(); o++)
+      for (int sl = 0; sl < d->ords[o].slots; sl++) {
+        const Ring r = d->ring((int)o, sl);
+        long long *e = &t[(size_t)(d->slot_index[o] + sl) * 3];
+        e[0] = (long long)(r.off + r.L.tags);
+        e[1] = (long long)(r.off + r.L.meta);
+        e[2] = r.cap;
+      }
+    if (cudaMemcpyAsync(d->slot_table, t.data(), t.size() * 8, cudaMemcpyHostToDevice, d->stream) != cudaSuccess ||
+        cudaStreamSynchronize(d->stream) != cudaSuccess)
+      return cleanup(fail(DORY_ECUDA, "slot table upload"));
+  }
 
   {
     const char *e = getenv("DORY_GRAPHS");
     d->use_graphs = !(e && e[0] == '0');
+    if (const char *m = getenv("DORY_MAX_PLANS")) d->max_plans = (size_t)std::max(1, atoi(m));
   }
   if (cudaStreamCreateWithFlags(&d->cap_stream, cudaStreamNonBlocking) != cudaSuccess)
     return cleanup(fail(DORY_ECUDA, "stream create"));
   if ((rc = setup_tc(d))) return cleanup(rc);
   d->seq_pos.assign(cfg->max_seqs, 0);
+  d->exits.assign(cfg->max_seqs, ExitRate{});
   d->appended.assign((size_t)cfg->max_seqs * d->n_flat_slots, 0);
   for (int s = 0; s < cfg->max_seqs; s++)
     if ((rc = reset_seq(d, s))) return cleanup(rc);
@@ -1354,6 +1537,31 @@ int dory_reset(dory_t *d, int32_t seq) {
   return reset_seq(d, seq);
 }
 
+int dory_rollback(dory_t *d, int32_t seq, int32_t n) {
+  if (!d) return fail(DORY_EINVAL, "handle is NULL");
+  if (seq < 0 || seq >= d->cfg.max_seqs) return fail(DORY_EINVAL, "seq %d out of range", seq);
+  if (n < 0) return fail(DORY_EINVAL, "n=%d must be >= 0", n);
+  const int pos = d->seq_pos[seq];
+  if (n >= pos) return DORY_OK;  // nothing is stored at or past n: the position stays (min(pos, n))
+  // every window that reads a row before n must still find its rows in the ring
+  for (const OrdInfo &o : d->ords) {
+    if (o.window == INT_MAX) continue;  // such a ring holds every position from 0
+    const long need = std::max<long>(0, (long)n - o.window + 1), held = std::max<long>(0, (long)pos - o.cap);
+    if (need < held)
+      return fail(DORY_ERANGE, "rollback of sequence %d from %d to %d: a ring of %d rows with window %d keeps %d "
+                               "positions back at most", seq, pos, n, o.cap, o.window, o.cap - o.window + 1);
+  }
+  CK(launch_rollback(d->kvmem + (size_t)seq * d->seq_stride, d->slot_table, d->n_flat_slots, n, d->dims.nk,
+                     d->cfg.kv_quant == DORY_KV_Q8_2F ? 1 : 0, d->dropped, d->stream));
+  std::vector<int32_t> dropped(d->n_flat_slots);
+  CK(cudaMemcpyAsync(dropped.data(), d->dropped, dropped.size() * 4, cudaMemcpyDeviceToHost, d->stream));
+  d->seq_pos[seq] = n;
+  CK(cudaMemcpyAsync(d->d_seq_pos + seq, &d->seq_pos[seq], 4, cudaMemcpyHostToDevice, d->stream));
+  CK(cudaStreamSynchronize(d->stream));
+  for (int i = 0; i < d->n_flat_slots; i++) d->appended[(size_t)seq * d->n_flat_slots + i] -= dropped[i];
+  return DORY_OK;
+}
+
 static int check_range(dory_t *d, int seq, long last_pos) {
   for (const OrdInfo &o : d->ords)
     if (o.window == INT_MAX && last_pos >= o.cap)
@@ -1393,6 +1601,58 @@ int dory_prefill_chunk(dory_t *d, int32_t seq, const int32_t *ids, int32_t n, in
   return DORY_OK;
 }
 
+int dory_prefill_batch(dory_t *d, int32_t nseq, const int32_t *seqs, const int32_t *counts, const int32_t *ids,
+                       int32_t loops, int32_t want) {
+  if (!d) return fail(DORY_EINVAL, "handle is NULL");
+  if (!seqs || !counts || !ids) return fail(DORY_EINVAL, "seqs, counts or ids is NULL");
+  if (nseq < 1 || nseq > d->Tmax) return fail(DORY_EINVAL, "nseq=%d: want 1..%d", nseq, d->Tmax);
+  if (loops < 1 || loops > d->cfg.max_loops) return fail(DORY_EINVAL, "loops=%d: want 1..%d", loops, d->cfg.max_loops);
+  if (want < DORY_WANT_NONE || want > DORY_WANT_ALL) return fail(DORY_EINVAL, "want=%d", want);
+  std::vector<char> seen(d->cfg.max_seqs, 0);
+  int T = 0, rc;
+  for (int j = 0; j < nseq; j++) {
+    const int sq = seqs[j], n = counts[j];
+    if (sq < 0 || sq >= d->cfg.max_seqs) return fail(DORY_EINVAL, "seqs[%d]=%d out of range", j, sq);
+    if (seen[sq]) return fail(DORY_EINVAL, "sequence %d appears twice in one step", sq);
+    seen[sq] = 1;
+    if (n < 1 || n > DORY_CHUNK_ROWS) return fail(DORY_EINVAL, "counts[%d]=%d: want 1..%d", j, n, DORY_CHUNK_ROWS);
+    if ((rc = check_range(d, sq, (long)d->seq_pos[sq] + n - 1))) return rc;
+    T += n;
+  }
+  if (T > d->Tmax) return fail(DORY_EINVAL, "%d rows in one step: at most %d (max(64, max_batch))", T, d->Tmax);
+  // dory.rs fn chunk_loops
+  int L = loops;
+  if (want == DORY_WANT_NONE && d->cfg.prompt_loops > 0 && d->cfg.kv_mode == DORY_KV_LAST_LOOP)
+    L = std::min(loops, d->cfg.prompt_loops);
+  StepArgs st;
+  st.T = T;
+  st.loops = L;
+  for (int j = 0; j < nseq; j++)
+    for (int i = 0; i < counts[j]; i++) {
+      st.hseq.push_back(seqs[j]);
+      st.hoff.push_back(i);
+    }
+  st.aseq.assign(seqs, seqs + nseq);
+  st.acnt.assign(counts, counts + nseq);
+  if (want == DORY_WANT_ALL) {
+    st.head_from = 0;
+    st.head_rows = T;
+  } else if (want == DORY_WANT_LAST && nseq == 1) {
+    st.head_from = T - 1;
+    st.head_rows = 1;
+  } else if (want == DORY_WANT_LAST) {
+    st.head_from = 0;
+    st.head_rows = T;
+    for (int j = 0, r = 0; j < nseq; j++) {
+      r += counts[j];
+      st.head_pick.push_back(r - 1);
+    }
+  }
+  if ((rc = do_step(d, st, ids))) return rc;
+  d->logits_rows = want == DORY_WANT_ALL ? T : (want == DORY_WANT_LAST ? nseq : 0);
+  return DORY_OK;
+}
+
 int dory_decode_step(dory_t *d, const int32_t *ids, const int32_t *seqs, int32_t batch, int32_t loops) {
   if (!d) return fail(DORY_EINVAL, "handle is NULL");
   if (batch < 1 || batch > d->cfg.max_batch) return fail(DORY_EINVAL, "batch=%d: want 1..%d", batch, d->cfg.max_batch);
@@ -1419,6 +1679,99 @@ int dory_decode_step(dory_t *d, const int32_t *ids, const int32_t *seqs, int32_t
   st.head_from = 0;
   if ((rc = do_step(d, st, ids))) return rc;
   d->logits_rows = batch;
+  return DORY_OK;
+}
+
+int dory_decode_ragged(dory_t *d, const int32_t *ids, const int32_t *seqs, int32_t batch, const int32_t *loops) {
+  if (!d) return fail(DORY_EINVAL, "handle is NULL");
+  if (!loops) return fail(DORY_EINVAL, "loops is NULL");
+  if (batch < 1 || batch > d->cfg.max_batch) return fail(DORY_EINVAL, "batch=%d: want 1..%d", batch, d->cfg.max_batch);
+  if (!ids || !seqs) return fail(DORY_EINVAL, "ids or seqs is NULL");
+  int lmax = 0;
+  bool same = true;
+  for (int b = 0; b < batch; b++) {
+    if (loops[b] < 1 || loops[b] > d->cfg.max_loops)
+      return fail(DORY_EINVAL, "loops[%d]=%d: want 1..%d", b, loops[b], d->cfg.max_loops);
+    lmax = std::max(lmax, (int)loops[b]);
+    same &= loops[b] == loops[0];
+  }
+  if (same) return dory_decode_step(d, ids, seqs, batch, loops[0]);
+  StepArgs st;
+  st.T = batch;
+  st.loops = lmax;
+  std::vector<char> seen(d->cfg.max_seqs, 0);
+  int rc;
+  for (int b = 0; b < batch; b++) {
+    const int s = seqs[b];
+    if (s < 0 || s >= d->cfg.max_seqs) return fail(DORY_EINVAL, "seqs[%d]=%d out of range", b, s);
+    if (seen[s]) return fail(DORY_EINVAL, "sequence %d appears twice in one step", s);
+    seen[s] = 1;
+    if ((rc = check_range(d, s, d->seq_pos[s]))) return rc;
+  }
+  // rows by loop count, most first (stable): the rows of each pass are a prefix
+  st.perm.resize(batch);
+  for (int b = 0; b < batch; b++) st.perm[b] = b;
+  std::stable_sort(st.perm.begin(), st.perm.end(), [&](int x, int y) { return loops[x] > loops[y]; });
+  st.rl.resize(batch);
+  st.hseq.resize(batch);
+  for (int r = 0; r < batch; r++) {
+    st.rl[r] = loops[st.perm[r]];
+    st.hseq[r] = seqs[st.perm[r]];
+  }
+  st.hoff.assign(batch, 0);
+  st.aseq = st.hseq;
+  st.acnt.assign(batch, 1);
+  st.head_rows = batch;
+  st.head_from = 0;
+  if ((rc = do_step(d, st, ids))) return rc;
+  d->logits_rows = batch;
+  return DORY_OK;
+}
+
+int dory_decode_conf(dory_t *d, const int32_t *id, int32_t seq, float th, int32_t *passes, float *top_prob) {
+  if (!d) return fail(DORY_EINVAL, "handle is NULL");
+  if (!id) return fail(DORY_EINVAL, "id is NULL");
+  if (seq < 0 || seq >= d->cfg.max_seqs) return fail(DORY_EINVAL, "seq %d out of range", seq);
+  if (d->cfg.max_loops < 2) return fail(DORY_EINVAL, "the gate's second pass needs max_loops >= 2");
+  if (!(th == th)) return fail(DORY_EINVAL, "th is NaN");
+  int rc = check_range(d, seq, d->seq_pos[seq]);
+  if (rc) return rc;
+  StepArgs st;
+  st.T = 1;
+  st.hseq.assign(1, seq);
+  st.hoff.assign(1, 0);
+  st.aseq.assign(1, seq);
+  st.acnt.assign(1, 1);
+  st.head_rows = 1;
+  ExitRate &ex = d->exits[seq];
+  float tp = NAN;
+  int np = 2;
+  if (!ex.probe()) {  // no read-out: both passes at once
+    st.loops = 2;
+    if ((rc = do_step(d, st, id))) return rc;
+  } else {
+    st.loops = 1;  // the first pass, the output block and the head (the read-out)
+    if ((rc = do_step(d, st, id))) return rc;
+    CK(launch_top_prob(d->logits, d->dims.vocab, d->d_top, d->stream));
+    CK(cudaMemcpyAsync(&tp, d->d_top, 4, cudaMemcpyDeviceToHost, d->stream));
+    CK(cudaStreamSynchronize(d->stream));
+    const bool stay = tp < th;
+    ex.note(!stay);
+    if (stay) {  // the second pass from the saved rows; the output block rewrites its rows
+      StepArgs r = st;
+      r.resume = true;
+      r.loops = 2;
+      r.first_loop = 1;
+      r.hoff.assign(1, -1);  // the first step moved the position past the token
+      r.acnt.assign(1, 0);
+      if ((rc = do_step(d, r, id))) return rc;
+    } else {
+      np = 1;
+    }
+  }
+  d->logits_rows = 1;
+  if (passes) *passes = np;
+  if (top_prob) *top_prob = tp;
   return DORY_OK;
 }
 

@@ -43,7 +43,7 @@ __device__ void build_input(const Team &tm, const GemvIn &in, int T, int K, floa
           o[j] = __ldcg(reinterpret_cast<const float4 *>(in.out + (size_t)t * K) + c);
           al[j] = __ldg(reinterpret_cast<const float4 *>(in.alpha) + c);
         }
-        if (in.mode == IN_RESID && in.mix == MIX_LOOP)
+        if (in.mode == IN_RESID && (in.mix == MIX_LOOP || in.mix == MIX_RESUME))
           inp[j] = __ldcg(reinterpret_cast<const float4 *>(in.input + (size_t)t * K) + c);
       }
     }
@@ -100,7 +100,8 @@ __device__ void build_input(const Team &tm, const GemvIn &in, int T, int K, floa
           if (lead && c < nch) reinterpret_cast<float4 *>(in.state + (size_t)t * K)[c] = x[j];
         }
       }
-      if (in.mix == MIX_BEGIN || in.mix == MIX_LOOP) {  // h = (state + input)^
+      if (in.mix == MIX_BEGIN || in.mix == MIX_LOOP || in.mix == MIX_RESUME) {  // h = (state + input)^
+        // (MIX_RESUME: src is the saved state row, taken as it is)
         float ss = 0.f, dummy = 0.f;
 #pragma unroll
         for (int j = 0; j < KC; j++) {

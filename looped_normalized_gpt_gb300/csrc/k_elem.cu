@@ -1,5 +1,6 @@
 // Row kernels of the Dory forward: embedding + RoPE table, the fused norm/RoPE/s_q^2
 // prep with the f32 ring writer, row norms, the nGPT residual with the loop mix.
+#include <algorithm>
 #include <climits>
 
 #include "common.cuh"
@@ -201,7 +202,7 @@ __global__ void residual_kernel(float *__restrict__ h, const float *__restrict__
     const int c = threadIdx.x + i * blockDim.x;
     x[i] = 0.f;
     if (i < nper && c < hidden) {
-      x[i] = hr[c];
+      x[i] = mix == MIX_RESUME ? state[(size_t)r * hidden + c] : hr[c];
       if (do_residual) {
         const float o = orow[c];
         sx += x[i] * x[i];
@@ -238,7 +239,7 @@ __global__ void residual_kernel(float *__restrict__ h, const float *__restrict__
     for (int i = 0; i < MAXV; i++) x[i] *= inv;
   }
   float *in_r = input + (size_t)r * hidden, *st_r = state + (size_t)r * hidden;
-  if (mix == MIX_BEGIN || mix == MIX_LOOP) {
+  if (mix == MIX_BEGIN || mix == MIX_LOOP || mix == MIX_RESUME) {
     float s = 0.f;
 #pragma unroll
     for (int i = 0; i < MAXV; i++) {
@@ -251,7 +252,7 @@ __global__ void residual_kernel(float *__restrict__ h, const float *__restrict__
         } else {
           inp = in_r[c];
         }
-        st_r[c] = x[i];
+        if (mix != MIX_RESUME) st_r[c] = x[i];
         x[i] = x[i] + inp;
         s += x[i] * x[i];
       }
@@ -301,7 +302,123 @@ __global__ void ring_write_f32_kernel(const float *__restrict__ k, const float *
   if (kh == 0 && threadIdx.x == 0) reinterpret_cast<int32_t *>(slot + ring.L.tags)[rr] = (int32_t)pos;
 }
 
+// Rollback of one sequence to position n (dory.rs DoryState::rollback; kv_cache.rs
+// fn truncate_last on q8 rings): one block per slot of the sequence. Every ring row whose tag
+// is a position >= n becomes empty (-1); the count of such rows is what the slot drops, and a
+// q8 slot's stored-row counters (one per kv head) go down by it. The frozen flag and fields
+// stay as they are. Rows still to be dropped are all in the ring: a rollback never reaches
+// further back than a ring holds (the host checks it).
+__global__ void rollback_kernel(char *seq_block, const long long *table, int n, int nk, int q8, int32_t *dropped) {
+  __shared__ int red[32];
+  const long long *t = table + 3 * blockIdx.x;  // tags offset, meta offset, rows
+  int32_t *tags = reinterpret_cast<int32_t *>(seq_block + t[0]);
+  const int cap = (int)t[2];
+  int cnt = 0;
+  for (int r = threadIdx.x; r < cap; r += blockDim.x)
+    if (tags[r] >= n) {
+      tags[r] = -1;
+      cnt++;
+    }
+  cnt = __reduce_add_sync(0xffffffffu, cnt);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) red[warp] = cnt;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int total = 0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); w++) total += red[w];
+    dropped[blockIdx.x] = total;
+    if (q8) {
+      int32_t *meta = reinterpret_cast<int32_t *>(seq_block + t[1]);
+      for (int kh = 0; kh < nk; kh++) meta[kh * 4 + 0] -= total;
+    }
+  }
+}
+
+// dory.rs fn top_prob on one row of logits: the largest softmax probability, from the
+// entries within 20 of the top only. top = max (f32); den = sum of exp(x - top) over the x
+// with x - top > -20, the difference taken in f32, exp and sum in f64; 1 / den as f32.
+__global__ void top_prob_kernel(const float *__restrict__ lg, int n, float *out) {
+  __shared__ float red[32];
+  __shared__ double dred[32];
+  float m = -INFINITY;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) m = fmaxf(m, lg[i]);
+  m = block_max(m, red);
+  double den = 0.0;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const float t = __fsub_rn(lg[i], m);
+    if (t > -20.f) den += exp((double)t);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+  if (lane == 0) dred[warp] = den;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double t = 0.0;
+    for (int w = 0; w < nw; w++) t += dred[w];
+    *out = (float)(1.0 / t);
+  }
+}
+
+// Rows of a step in another order: ids_out[r] = ids[perm[r]] (the token ids in the step's
+// row order), and dst[perm[r]] = src[r] for rows of `width` floats (results back in the
+// caller's order).
+__global__ void gather_ids_kernel(const int32_t *__restrict__ ids, const int32_t *__restrict__ perm, int n,
+                                  int32_t *__restrict__ out) {
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r < n) out[r] = ids[perm[r]];
+}
+
+__global__ void scatter_rows_kernel(const float *__restrict__ src, float *__restrict__ dst,
+                                    const int32_t *__restrict__ perm, int width) {
+  const int r = blockIdx.y;
+  const float4 *s4 = reinterpret_cast<const float4 *>(src + (size_t)r * width);
+  float4 *d4 = reinterpret_cast<float4 *>(dst + (size_t)perm[r] * width);
+  for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < width / 4; c += gridDim.x * blockDim.x) d4[c] = s4[c];
+}
+
+// dst[j][.] = src[idx[j]][.] for `rows` rows of `width` floats.
+__global__ void gather_rows_kernel(const float *__restrict__ src, float *__restrict__ dst,
+                                   const int32_t *__restrict__ idx, int width) {
+  const int j = blockIdx.y;
+  const float4 *s4 = reinterpret_cast<const float4 *>(src + (size_t)idx[j] * width);
+  float4 *d4 = reinterpret_cast<float4 *>(dst + (size_t)j * width);
+  for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < width / 4; c += gridDim.x * blockDim.x) d4[c] = s4[c];
+}
+
 }  // namespace
+
+cudaError_t launch_gather_rows(const float *src, float *dst, const int32_t *idx, int rows, int width,
+                               cudaStream_t s) {
+  if (width % 4) return cudaErrorInvalidValue;
+  const int per_row = std::min(64, (width / 4 + 255) / 256);
+  gather_rows_kernel<<<dim3(per_row, rows), 256, 0, s>>>(src, dst, idx, width);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_ids(const int32_t *ids, const int32_t *perm, int n, int32_t *out, cudaStream_t s) {
+  gather_ids_kernel<<<(n + 127) / 128, 128, 0, s>>>(ids, perm, n, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scatter_rows(const float *src, float *dst, const int32_t *perm, int rows, int width,
+                                cudaStream_t s) {
+  if (width % 4) return cudaErrorInvalidValue;
+  const int per_row = std::min(64, (width / 4 + 255) / 256);
+  scatter_rows_kernel<<<dim3(per_row, rows), 256, 0, s>>>(src, dst, perm, width);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_top_prob(const float *logits, int n, float *out, cudaStream_t s) {
+  top_prob_kernel<<<1, 1024, 0, s>>>(logits, n, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rollback(char *seq_block, const long long *table, int nslots, int n, int nk, int q8,
+                            int32_t *dropped, cudaStream_t s) {
+  rollback_kernel<<<nslots, 256, 0, s>>>(seq_block, table, n, nk, q8, dropped);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_embed_rope(const int32_t *ids, const void *E, int wdtype, Dims d, Rows rows, double theta_s,
                               double theta_f, float *h, float *rope, Emit em, cudaStream_t s) {

@@ -106,7 +106,12 @@ cudaError_t launch_attention_stream(const float *qkvg, int ldq, Dims d, Rows row
 
 cudaError_t launch_rownorm(float *x, int T, int width, int ld, Emit em, cudaStream_t s);
 
-enum Mix { MIX_NONE = 0, MIX_BEGIN = 1, MIX_LOOP = 2, MIX_END = 3 };
+// The loop mix of dory.rs fn stack after a sub-layer: MIX_BEGIN (the input block's end:
+// input = state = h, h = (state + input)^), MIX_LOOP (a pass's end: state = h^, then
+// h = (state + input)^), MIX_END (the last pass's end: state = h^, h = state), and
+// MIX_RESUME, which replaces the sub-layer's output: h = (state + input)^ from the saved
+// input and state rows (the second pass of an early-exit gate that decided to stay).
+enum Mix { MIX_NONE = 0, MIX_BEGIN = 1, MIX_LOOP = 2, MIX_END = 3, MIX_RESUME = 4 };
 
 // x = (x^ + alpha (out^ - x^))^ per row, then the loop mix (dory.rs fn stack).
 cudaError_t launch_residual(float *h, const float *out, const float *alpha, int T, int hidden, int mix,
@@ -257,6 +262,25 @@ constexpr int MEGA_AK = 32;             // positions per attention item
 cudaError_t launch_mega_decode(const MegaArgs &a, int grid, cudaStream_t s);
 
 cudaError_t launch_advance(int32_t *seq_pos, const int32_t *seq, const int32_t *count, int n, cudaStream_t s);
+
+// A step whose rows run in another order than the caller's: ids_out[r] = ids[perm[r]], and
+// dst[perm[r]][.] = src[r][.] for `rows` rows of `width` floats (width a multiple of 4).
+cudaError_t launch_gather_ids(const int32_t *ids, const int32_t *perm, int n, int32_t *out, cudaStream_t s);
+cudaError_t launch_scatter_rows(const float *src, float *dst, const int32_t *perm, int rows, int width,
+                                cudaStream_t s);
+
+// dst[j][.] = src[idx[j]][.] for `rows` rows of `width` floats (width a multiple of 4).
+cudaError_t launch_gather_rows(const float *src, float *dst, const int32_t *idx, int rows, int width,
+                               cudaStream_t s);
+
+// dory.rs fn top_prob of one row of n logits into *out (one block).
+cudaError_t launch_top_prob(const float *logits, int n, float *out, cudaStream_t s);
+
+// Forget the rows at positions >= n in every slot of one sequence: `table` holds per slot
+// (tags offset, meta offset, ring rows) as int64 from the sequence's block; dropped[slot]
+// gets the rows each slot lost; q8 slots' stored-row counters go down by it.
+cudaError_t launch_rollback(char *seq_block, const long long *table, int nslots, int n, int nk, int q8,
+                            int32_t *dropped, cudaStream_t s);
 
 cudaError_t launch_ring_write_f32(const float *k, const float *v, int n, int pos0, Dims d, Ring ring, int seq,
                                   cudaStream_t s);

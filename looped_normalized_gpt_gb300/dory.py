@@ -62,10 +62,17 @@ SIGNATURES = {
                                    ctypes.POINTER(ctypes.c_void_p)]),
     "dory_destroy": (ctypes.c_int, [ctypes.c_void_p]),
     "dory_reset": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32]),
+    "dory_rollback": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32]),
     "dory_prefill_chunk": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32,
                                           ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]),
+    "dory_prefill_batch": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
+                                          ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32]),
     "dory_decode_step": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
                                         ctypes.c_int32]),
+    "dory_decode_ragged": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                                          ctypes.c_void_p]),
+    "dory_decode_conf": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_float,
+                                        c_int32_p, ctypes.POINTER(ctypes.c_float)]),
     "dory_logits": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t]),
     "dory_logits_device": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p), c_int32_p]),
     "dory_last_error": (ctypes.c_char_p, []),
@@ -181,10 +188,38 @@ class Dory:
         n = int(ids_a.numel() if hasattr(ids_a, "numel") else ids_a.size)
         self._check(self.lib.dory_prefill_chunk(self.h, seq, _ptr(ids_a), n, pos0, loops, WANT[want]))
 
+    def prefill_batch(self, seqs, chunks, loops: int, want: str = "last") -> None:
+        """One prefill chunk for each sequence in seqs (chunks[j]: its ids), in one step."""
+        seqs_a = np.ascontiguousarray(seqs, dtype=np.int32)
+        counts = np.ascontiguousarray([len(c) for c in chunks], dtype=np.int32)
+        if len(chunks) and all(hasattr(c, "data_ptr") for c in chunks):
+            import torch
+
+            ids_a = torch.cat(list(chunks)).to(torch.int32)
+        else:
+            ids_a = np.ascontiguousarray(np.concatenate([np.asarray(c) for c in chunks]), dtype=np.int32)
+        self._check(self.lib.dory_prefill_batch(self.h, len(seqs_a), _ptr(seqs_a), _ptr(counts), _ptr(ids_a), loops,
+                                                WANT[want]))
+
     def decode_step(self, ids, seqs, loops: int) -> None:
         ids_a = ids if hasattr(ids, "data_ptr") else np.ascontiguousarray(ids, dtype=np.int32)
         seqs_a = np.ascontiguousarray(seqs, dtype=np.int32)
         self._check(self.lib.dory_decode_step(self.h, _ptr(ids_a), _ptr(seqs_a), len(seqs_a), loops))
+
+    def decode_ragged(self, ids, seqs, loops) -> None:
+        """One decode token per sequence, each sequence with its own loop count."""
+        ids_a = ids if hasattr(ids, "data_ptr") else np.ascontiguousarray(ids, dtype=np.int32)
+        seqs_a = np.ascontiguousarray(seqs, dtype=np.int32)
+        loops_a = np.ascontiguousarray(loops, dtype=np.int32)
+        assert loops_a.size == seqs_a.size, "one loop count per sequence"
+        self._check(self.lib.dory_decode_ragged(self.h, _ptr(ids_a), _ptr(seqs_a), len(seqs_a), _ptr(loops_a)))
+
+    def decode_conf(self, token, seq: int, th: float) -> tuple[int, float]:
+        """One token under the Conf(th) early-exit gate: (passes, top probability or NaN)."""
+        ids_a = token if hasattr(token, "data_ptr") else np.ascontiguousarray([token], dtype=np.int32)
+        passes, tp = ctypes.c_int32(), ctypes.c_float()
+        self._check(self.lib.dory_decode_conf(self.h, _ptr(ids_a), seq, th, ctypes.byref(passes), ctypes.byref(tp)))
+        return passes.value, tp.value
 
     def logits(self, row: int = 0, out=None) -> np.ndarray:
         dst = out if out is not None else np.empty(self.cfg.vocab, dtype=np.float32)
@@ -207,6 +242,9 @@ class Dory:
 
     def reset(self, seq: int) -> None:
         self._check(self.lib.dory_reset(self.h, seq))
+
+    def rollback(self, seq: int, n: int) -> None:
+        self._check(self.lib.dory_rollback(self.h, seq, n))
 
     def set_position(self, seq: int, pos: int) -> None:
         self._check(self.lib.dory_set_position(self.h, seq, pos))

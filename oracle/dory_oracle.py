@@ -312,12 +312,49 @@ class Slot:
 # ----------------------------------------------------------------------------------------
 
 
+def top_prob(lg) -> np.float32:
+    """dory.rs fn top_prob: the largest softmax probability of a row of logits, counting only
+    the entries within 20 of the top. top = the row's max (f32); den = the sum, in vocabulary
+    order, of exp(x - top) over the x with x - top > -20, the difference in f32 and the exp
+    and sum in f64; the result 1/den rounded to f32."""
+    lg = np.asarray(lg, dtype=F32)
+    top = F32(np.max(lg))
+    den = 0.0
+    for x in lg:
+        t = F32(x - top)
+        if t > F32(-20.0):
+            den += math.exp(float(t))
+    return F32(1.0 / den)
+
+
+class ExitRate:
+    """dory.rs struct ExitRate: the rate of tokens whose first read-out ended them (f32, from
+    1.0) and a token counter (u32). probe(): is this token worth a read-out (rate >= 0.35, or
+    one token in eight); note(exited): rate += 0.1 (exited - rate), each step rounded to f32."""
+
+    def __init__(self):
+        self.rate = F32(1.0)
+        self.tokens = 0
+
+    def probe(self) -> bool:
+        self.tokens = (self.tokens + 1) % (1 << 32)
+        return bool(self.rate >= F32(0.35) or self.tokens % 8 == 0)
+
+    def note(self, exited: bool) -> None:
+        diff = F32(F32(1.0 if exited else 0.0) - self.rate)
+        self.rate = F32(self.rate + F32(F32(0.1) * diff))
+
+
 class SeqState:
-    """One sequence: slots[(attention ordinal, loop slot)] and the next position."""
+    """One sequence: slots[(attention ordinal, loop slot)], the next position, and the
+    early-exit gate's rate and counts (dory.rs struct DoryState)."""
 
     def __init__(self):
         self.slots: dict[tuple[int, int], Slot] = {}
         self.pos = 0
+        self.exits = ExitRate()
+        self.gate_tokens = 0
+        self.gate_one = 0
 
 
 class DoryOracle:
@@ -421,14 +458,17 @@ class DoryOracle:
         y = justnorm(silu_mul(g, u, L["sg"], L["su"]))
         return y @ L["down"].T
 
-    def run_layer(self, st: SeqState, li: int, loop_i: int, h: np.ndarray, pos0: int) -> np.ndarray:
-        """dory.rs fn stack, closure `run`: the sub-layer, then the residual per row."""
+    def run_layer(self, st: SeqState, li: int, loop_i: int, h: np.ndarray, pos0: int,
+                  rewrite_out: bool = False) -> np.ndarray:
+        """dory.rs fn stack, closure `run`: the sub-layer, then the residual per row.
+        `rewrite_out`: an output layer replaces this chunk's rows (the gate's second read-out)."""
         c = self.cfg
         L = self.layers[li]
         if L["kind"] == "attn":
             sl = self.slot_loop(li, loop_i)
             recurrent = self.is_rec(li)
             overwrite = c.kv_mode == "last_loop" and (recurrent or li >= c.n_in + c.n_rec) and loop_i > 0
+            overwrite = overwrite or (rewrite_out and li >= c.n_in + c.n_rec)
             out = self.attn_layer(L, self.slot(st, L["ordinal"], sl), h, pos0, overwrite)
         else:
             out = self.mlp_layer(L, h)
@@ -436,10 +476,24 @@ class DoryOracle:
 
     # -- a chunk ------------------------------------------------------------------------
 
-    def forward_chunk(self, st: SeqState, ids, pos0: int, loops: int, want: str = "last"):
+    def head_rows(self, h: np.ndarray) -> np.ndarray:
+        """dory.rs fn head: (H h) * logit_scale per row."""
+        return (h @ self.head.T) * self.logit_scale
+
+    def forward_chunk(self, st: SeqState, ids, pos0: int, loops: int, want: str = "last", gate=None):
         """One chunk of rows at positions pos0..: embed, input block, `loops` recurrent
         passes with the loop mix, output block, head (dory.rs fn stack, fn forward_host,
-        fn head). Returns (logits [rows][vocab] or None, final hidden [t][hidden])."""
+        fn head). Returns (logits [rows][vocab] or None, final hidden [t][hidden]).
+
+        gate: None, or th of the Conf(th) early-exit gate, which applies to a chunk of one
+        row (dory.rs fn stack's early-exit block): one pass; if the sequence's exit rate
+        asks for a read-out, the output block and the head on the pass's state, and
+        top_prob >= th ends the token with those logits; otherwise a second pass from the
+        state and the input, the output block again (rewriting the rows the read-out
+        appended) and the head. The rate notes every read-out. `loops` is not used then.
+        Reading: the second read-out replaces the first one's output-layer rows in both KV
+        modes (the page's comment states that intent; its per_loop branch would append the
+        position a second time)."""
         c = self.cfg
         if loops < 1 or loops > c.max_loops:
             raise ValueError("loops out of range")
@@ -452,24 +506,52 @@ class DoryOracle:
             if 0 <= i < c.vocab:  # an id past the vocabulary leaves a zero row
                 h[r] = self.embed[i]
         L = self.chunk_loops(loops, want)
+        early = t == 1 and gate is not None
         for li in range(c.n_in):
             h = self.run_layer(st, li, 0, h, pos0)
         inp = h.copy()
         state = inp.copy()
-        for i in range(L):
+        for i in range(1 if early else L):
             h = justnorm(state + inp)
             for li in range(c.n_in, c.n_in + c.n_rec):
                 h = self.run_layer(st, li, i, h, pos0)
             state = justnorm(h)
-        h = state
-        for li in range(c.n_in + c.n_rec, c.n_layers):
-            h = self.run_layer(st, li, 0, h, pos0)
+        exit_logits = None
+        if early:
+            stay, readout = False, False
+            h = state
+            if st.exits.probe():
+                readout = True
+                for li in range(c.n_in + c.n_rec, c.n_layers):
+                    h = self.run_layer(st, li, 0, h, pos0)
+                lg = self.head_rows(h)
+                stay = bool(top_prob(lg[0]) < F32(gate))
+                st.exits.note(not stay)
+                if not stay:
+                    exit_logits = lg
+            else:
+                stay = True
+            if stay:
+                h = justnorm(state + inp)
+                for li in range(c.n_in, c.n_in + c.n_rec):
+                    h = self.run_layer(st, li, 1, h, pos0)
+                h = justnorm(h)
+                for li in range(c.n_in + c.n_rec, c.n_layers):
+                    h = self.run_layer(st, li, int(readout), h, pos0, rewrite_out=readout)
+            st.gate_tokens += 1
+            st.gate_one += int(not stay)
+        else:
+            h = state
+            for li in range(c.n_in + c.n_rec, c.n_layers):
+                h = self.run_layer(st, li, 0, h, pos0)
         st.pos = pos0 + t
         logits = None
-        if want == "last":
-            logits = (h[-1:] @ self.head.T) * self.logit_scale
+        if exit_logits is not None:
+            logits = exit_logits if want != "none" else None
+        elif want == "last":
+            logits = self.head_rows(h[-1:])
         elif want == "all":
-            logits = (h @ self.head.T) * self.logit_scale
+            logits = self.head_rows(h)
         return logits, h
 
     def prefill(self, st: SeqState, ids, loops: int, chunk: int = CHUNK_ROWS):
@@ -482,14 +564,25 @@ class DoryOracle:
             out = self.forward_chunk(st, ids[a:b], st.pos, loops, want)
         return out
 
-    def decode_step(self, states: list, ids, loops: int):
-        """One token for each sequence (a one-row chunk each, logits read)."""
+    def decode_step(self, states: list, ids, loops):
+        """One token for each sequence (a one-row chunk each, logits read). `loops`: one
+        count for every sequence, or one per sequence (each row is its own sequence's
+        forward, dory.rs fn forward_host with that sequence's loop count)."""
+        per_seq = np.broadcast_to(np.asarray(loops, dtype=np.int64), (len(states),))
         logits, hidden = [], []
-        for st, i in zip(states, ids):
-            lg, h = self.forward_chunk(st, [int(i)], st.pos, loops, "last")
+        for st, i, L in zip(states, ids, per_seq):
+            lg, h = self.forward_chunk(st, [int(i)], st.pos, int(L), "last")
             logits.append(lg[0])
             hidden.append(h[0])
         return np.stack(logits), np.stack(hidden)
+
+    def rollback(self, st: SeqState, n: int) -> None:
+        """dory.rs DoryState::rollback: forget the rows from position n on. Every slot keeps
+        its stored rows at positions < n (a q8_2f field that froze stays frozen, kv_cache.rs
+        fn truncate_last drops rows only); the sequence's position becomes min(pos, n)."""
+        for slot in st.slots.values():
+            slot.truncate(sum(1 for p in slot.positions if p >= n))
+        st.pos = min(st.pos, n)
 
     def write_kv_rows(self, st: SeqState, ordinal: int, sl: int, pos0: int, k, v) -> None:
         """Append synthetic rows [n][nk][hd] to one slot through the normal append path."""

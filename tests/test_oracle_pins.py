@@ -26,7 +26,7 @@ def micro(kv_mode="per_loop", loops=2, window=5, **kw):
     base = dict(name="micro", hidden=16, ffn=16, vocab=11, nh=4, nk=2, hd=8, window=window,
                 pattern="S-*-S-*-S-*-", n_in=4, n_rec=4, n_out=4, loops=loops, max_loops=16,
                 kv_mode=kv_mode, kv_quant="f32", weight_dtype="f32", sq=4.0, attn_sg=2.0,
-                mlp_suv=1.5 / 4.0, logit_scale=3.0, alpha=(0.2, 0.3), max_context=4096)
+                mlp_suv=1.5 / 4.0, logit_scale=3.0, alpha=(0.2, 0.3), max_context=4096, scale_spread=0.5)
     base.update(kw)
     return synth.DoryConfig(**base)
 
@@ -289,6 +289,24 @@ def test_freeze_comes_at_the_65th_append_and_col_is_the_rms():
     assert np.array_equal(kcol, s.kcol)
 
 
+def test_freeze_sums_the_squares_in_f32_in_row_order():
+    """kv_cache.rs fn freeze_cols sums x^2 over the stored rows in f32, one row after another.
+    With one row of 4096 (x^2 = 2^24) and 63 rows of 1: in that order every 2^24 + 1 rounds
+    back to 2^24 (the tie goes to the even neighbour), so the sum stays 2^24 and the field is
+    sqrt(2^24 / 64) = 512 exactly; in the reverse order the ones first add up to 63 and
+    63 + 2^24 rounds to 2^24 + 64, so the field is sqrt(2^18 + 1), whose nearest f32 is
+    512 + 2^-10. A sum in f64, or pairwise, or in another order, gives other values."""
+    hd = 32
+    big = (np.full((1, hd), 64, np.int8), np.full((1, 1), 64.0, np.float32))  # x = 64 * 64 = 4096
+    one = (np.full((63, hd), 1, np.int8), np.full((63, 1), 1.0, np.float32))  # x = 1
+    for rows, want in (((big, one), 512.0), ((one, big), 512.0 + 2.0 ** -10)):
+        codes = np.concatenate([r[0] for r in rows])
+        scales = np.concatenate([r[1] for r in rows])
+        col, _, _ = O.freeze_field(codes, scales, hd)
+        assert col.dtype == np.float32
+        assert np.all(col == np.float32(want)), (col[0], want)
+
+
 def test_q8_attend_matches_f32_within_grid():
     nk, hd, rows = 2, 32, 100
     f = O.Slot(nk, hd, False)
@@ -530,6 +548,170 @@ def test_loops_above_the_maximum_are_refused():
 
 
 # ------------------------------------------------------------------------------------------
+# rollback (dory.rs DoryState::rollback, kv_cache.rs fn truncate_last)
+# ------------------------------------------------------------------------------------------
+
+
+def test_rollback_keeps_the_prefix_a_new_turn_extends():
+    """The pages' own test of rollback (dory.rs tests, rollback_keeps_the_prefix_a_new_turn_
+    extends): per_loop, 9 tokens, roll back to 5, then tokens 5.. again: the logits are those
+    of one run over the whole sequence (per_loop logits do not depend on the chunking)."""
+    cfg = micro(window=50)
+    w = synth.weights(cfg, 21)
+    ids = [(i * 3) % 11 for i in range(12)]
+    want = _run(cfg, w, ids, 1, 2)[3][-1]
+    o = O.DoryOracle(cfg, w)
+    st = O.SeqState()
+    o.forward_chunk(st, ids[:9], 0, 2, "last")
+    o.rollback(st, 5)
+    assert st.pos == 5
+    lg, _ = o.forward_chunk(st, ids[5:], 5, 2, "last")
+    assert np.max(np.abs(lg - want)) < 1e-9
+
+
+def test_rollback_under_last_loop_equals_the_shorter_chunk():
+    """Within a chunk a row sees only rows up to itself, at every loop, so rolling a chunk of
+    9 back to 5 leaves exactly what a chunk of 5 leaves, under last_loop too; then a new
+    turn gives the same logits."""
+    cfg = micro(kv_mode="last_loop", window=6)
+    w = synth.weights(cfg, 22)
+    ids = [(i * 5 + 2) % 11 for i in range(14)]
+    o = O.DoryOracle(cfg, w)
+    a, b = O.SeqState(), O.SeqState()
+    o.forward_chunk(a, ids[:9], 0, 3, "last")
+    o.rollback(a, 5)
+    o.forward_chunk(b, ids[:5], 0, 3, "last")
+    assert a.slots.keys() == b.slots.keys()
+    for key in a.slots:
+        assert a.slots[key].positions == b.slots[key].positions == list(range(5))
+        for p in range(5):
+            assert np.allclose(a.slots[key].k[p], b.slots[key].k[p], atol=1e-12)
+            assert np.allclose(a.slots[key].v[p], b.slots[key].v[p], atol=1e-12)
+    la, _ = o.forward_chunk(a, ids[5:], 5, 3, "last")
+    lb, _ = o.forward_chunk(b, ids[5:], 5, 3, "last")
+    assert np.max(np.abs(la - lb)) < 1e-9
+
+
+def test_rollback_past_the_position_changes_nothing_and_to_zero_is_a_reset():
+    cfg = micro()
+    w = synth.weights(cfg, 23)
+    o = O.DoryOracle(cfg, w)
+    st = O.SeqState()
+    o.forward_chunk(st, [1, 2, 3, 4], 0, 2, "last")
+    before = {k: list(s.positions) for k, s in st.slots.items()}
+    o.rollback(st, 9)
+    assert st.pos == 4 and {k: list(s.positions) for k, s in st.slots.items()} == before
+    o.rollback(st, 0)
+    assert st.pos == 0 and all(s.stored == 0 for s in st.slots.values())
+    l1, _ = o.forward_chunk(st, [5, 6], 0, 2, "last")
+    l2, _ = o.forward_chunk(O.SeqState(), [5, 6], 0, 2, "last")
+    assert np.max(np.abs(l1 - l2)) < 1e-12
+
+
+def test_q8_rollback_keeps_a_frozen_field_and_an_open_one_waits_for_64_kept_rows():
+    """kv_cache.rs fn truncate_last drops rows and keeps the fields: after the freeze a
+    rollback leaves kcol/vcol as they were; before it, only the rows kept count toward the 64
+    the freeze waits for, so 50 rows rolled back to 20 and then 45 more rows store exactly
+    what 20 + 45 rows store (the freeze at the 65th row reads the same 64 rows)."""
+    nk, hd = 2, 64
+    r = synth.kv_rows(5, 0, 120, nk, hd) * np.float32(2.0)
+    s_ = synth.kv_rows(5, 1, 120, nk, hd) * np.linspace(0.3, 3, hd).astype(np.float32)
+    frozen = O.Slot(nk, hd, True)
+    for p in range(70):
+        frozen.append(p, r[p], s_[p])
+    kcol, vcol = frozen.kcol.copy(), frozen.vcol.copy()
+    st = O.SeqState()
+    st.slots[(0, 0)] = frozen
+    st.pos = 70
+    O.DoryOracle.rollback(None, st, 30)
+    assert frozen.stored == 30 and np.array_equal(frozen.kcol, kcol) and np.array_equal(frozen.vcol, vcol)
+    a, b = O.Slot(nk, hd, True), O.Slot(nk, hd, True)
+    for p in range(50):
+        a.append(p, r[p], s_[p])
+    sa = O.SeqState()
+    sa.slots[(0, 0)] = a
+    sa.pos = 50
+    O.DoryOracle.rollback(None, sa, 20)
+    assert a.stored == 20 and a.kcol is None
+    for p in range(20):
+        b.append(p, r[p], s_[p])
+    for p in range(20, 65):
+        a.append(p, r[100 - p], s_[100 - p])
+        b.append(p, r[100 - p], s_[100 - p])
+    assert a.kcol is not None and np.array_equal(a.kcol, b.kcol) and np.array_equal(a.vcol, b.vcol)
+    for p in range(65):
+        assert np.array_equal(a.kq[p], b.kq[p]) and np.array_equal(a.ks[p], b.ks[p])
+        assert np.array_equal(a.vq[p], b.vq[p]) and np.array_equal(a.vs[p], b.vs[p])
+
+
+# ------------------------------------------------------------------------------------------
+# the Conf(th) early-exit gate (dory.rs fn stack's early-exit block, fn top_prob, ExitRate)
+# ------------------------------------------------------------------------------------------
+
+
+def test_top_prob_of_a_sure_row_and_of_ties():
+    """The pages' test (top_prob_of_a_sure_row) and closed forms: n equal entries give 1/n;
+    entries more than 20 below the top do not count, entries just within do."""
+    lg = np.full(100, -30.0, np.float32)
+    lg[7] = 30.0
+    assert O.top_prob(lg) > 0.999
+    assert abs(O.top_prob(np.array([1.0, 1.0], np.float32)) - 0.5) < 1e-5
+    assert O.top_prob(np.zeros(8, np.float32)) == np.float32(0.125)
+    assert O.top_prob(np.array([0.0, -25.0], np.float32)) == np.float32(1.0)
+    # 100000 entries at -20.5 hold 1.25e-4 of a full softmax's mass; top_prob skips them all
+    assert O.top_prob(np.concatenate([[0.0], np.full(100_000, -20.5)]).astype(np.float32)) == np.float32(1.0)
+    assert O.top_prob(np.array([0.0, -19.0], np.float32)) == np.float32(1.0 / (1.0 + math.exp(-19.0)))
+    assert O.top_prob(np.array([3.0, 3.0 - math.log(3.0)], np.float32)) == pytest.approx(0.75, rel=1e-6)
+
+
+def test_exit_rate_reads_out_while_exits_are_common_and_one_in_eight_after():
+    """ExitRate starts at 1.0; each read-out that stays multiplies the rate by 0.9, so the
+    first 10 tokens read out (0.9^9 >= 0.35 > 0.9^10), then only tokens 16, 24, ... do; exits
+    raise the rate by a tenth of its gap to 1."""
+    e = O.ExitRate()
+    pattern = []
+    for _ in range(24):
+        p = e.probe()
+        pattern.append(p)
+        if p:
+            e.note(False)
+    assert pattern == [True] * 10 + [False] * 5 + [True] + [False] * 7 + [True]
+    assert abs(e.rate - 0.9 ** 12) < 1e-6
+    r = e.rate
+    e.note(True)
+    assert abs(e.rate - (r + 0.1 * (1 - r))) < 1e-7
+
+
+@pytest.mark.parametrize("kv_mode", ["last_loop", "per_loop"])
+def test_a_gated_token_makes_one_pass_when_it_exits_and_two_when_it_stays(kv_mode):
+    """th = 0 ends every read-out token after one pass: logits, hidden rows and KV rows are a
+    loops=1 token's. th = 2 (above any probability) sends every token to a second pass: they
+    are a loops=2 token's, read-out or not (the second read-out replaces the first one's
+    output-layer rows)."""
+    cfg = micro(kv_mode=kv_mode)
+    w = synth.weights(cfg, 24)
+    ids = [(i * 7 + 3) % 11 for i in range(30)]
+    for th, loops in ((0.0, 1), (2.0, 2)):
+        o = O.DoryOracle(cfg, w)
+        a, b = O.SeqState(), O.SeqState()
+        o.forward_chunk(a, ids[:6], 0, 2, "last")
+        o.forward_chunk(b, ids[:6], 0, 2, "last")
+        probes = 0
+        for i in ids[6:]:
+            tokens_before = a.exits.tokens
+            la, ha = o.forward_chunk(a, [i], a.pos, 2, "last", gate=th)
+            lb, hb = o.forward_chunk(b, [i], b.pos, loops, "last")
+            probes += a.exits.tokens - tokens_before
+            assert np.max(np.abs(la - lb)) < 1e-12 and np.max(np.abs(ha - hb)) < 1e-12
+        assert a.gate_tokens == 24 and a.gate_one == (24 if th == 0.0 else 0)
+        assert a.slots.keys() == b.slots.keys()
+        for key in a.slots:
+            assert a.slots[key].positions == b.slots[key].positions
+            for p in a.slots[key].positions:
+                assert np.allclose(a.slots[key].k[p], b.slots[key].k[p], atol=1e-12)
+
+
+# ------------------------------------------------------------------------------------------
 # planted mistakes: each pin above must catch a plausible slip in the oracle
 # ------------------------------------------------------------------------------------------
 
@@ -574,3 +756,40 @@ def test_a_freeze_at_the_64th_row_is_caught(monkeypatch):
     monkeypatch.setattr(O, "KV_COL_WARMUP", 63)
     with pytest.raises(AssertionError):
         test_freeze_comes_at_the_65th_append_and_col_is_the_rms()
+
+
+def test_a_freeze_sum_in_f64_is_caught(monkeypatch):
+    def f64_freeze(codes, scales, group):
+        n, hd = codes.shape
+        rows = codes.astype(np.float64) * np.repeat(scales, group, axis=1)[:, :hd]
+        col = np.maximum(np.sqrt(np.sum(rows * rows, axis=0) / n), 1e-6).astype(np.float32)
+        return col, codes, scales
+
+    monkeypatch.setattr(O, "freeze_field", f64_freeze)
+    with pytest.raises(AssertionError):
+        test_freeze_sums_the_squares_in_f32_in_row_order()
+
+
+def test_a_rollback_that_keeps_the_dropped_rows_is_caught(monkeypatch):
+    def bad(self, st, n):
+        st.pos = min(st.pos, n)
+
+    monkeypatch.setattr(O.DoryOracle, "rollback", bad)
+    with pytest.raises(AssertionError):
+        test_rollback_keeps_the_prefix_a_new_turn_extends()
+
+
+def test_a_top_prob_that_counts_every_entry_is_caught(monkeypatch):
+    def full_softmax(lg):
+        lg = np.asarray(lg, np.float64)
+        return np.float32(1.0 / np.sum(np.exp(lg - lg.max())))
+
+    monkeypatch.setattr(O, "top_prob", full_softmax)
+    with pytest.raises(AssertionError):
+        test_top_prob_of_a_sure_row_and_of_ties()
+
+
+def test_an_exit_rate_that_never_stops_reading_out_is_caught(monkeypatch):
+    monkeypatch.setattr(O.ExitRate, "probe", lambda self: True)
+    with pytest.raises(AssertionError):
+        test_exit_rate_reads_out_while_exits_are_common_and_one_in_eight_after()
