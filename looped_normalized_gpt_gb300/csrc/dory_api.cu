@@ -60,6 +60,10 @@ struct TcW {
 };
 constexpr int TC_TRACE_BLOCKS = 1024;
 
+// Steps with at least this many rows take the tensor-core kernel with the step rows as the
+// MMA's M side and bf16 activations (below it the weights stream once for a thin row block).
+constexpr int TC_BIG_ROWS = 256;
+
 int bn_index(int bn) { return bn <= 16 ? 0 : bn <= 32 ? 1 : bn <= 64 ? 2 : bn <= 128 ? 3 : 4; }
 
 struct Plan {
@@ -139,6 +143,7 @@ struct dory_handle {
   int mega_inflight = 0;  // cap on a block's weight copies in flight (DORY_MEGA_INFLIGHT)
   // tensor-core projections: weight maps per layer ([0] q/k/v/g or gate/up, [1] o or down)
   bool tc_ok = false;
+  bool tc_big = true;  // steps of TC_BIG_ROWS rows and more take launch_tc_gemm_big (DORY_TC_BIG=0: never)
   std::vector<std::array<TcW, 2>> tcw;
   TcW tc_head;
   CUtensorMap xmap[3][2][5];  // activation rows (h, z, y) x (hi, lo) x tile rows 16..256
@@ -413,6 +418,17 @@ int issue_step(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_splits, cud
   auto tcg = [&](const TcW &w, int xbuf, int rowsT, int t_base, float *Y, int ldy, EpiArgs ep) -> int {
     TcGemm g;
     g.tmW = w.map;
+    if (rowsT >= TC_BIG_ROWS && d->tc_big) {  // a dense contraction: step rows as the MMA's M side
+      g.tmXh = d->xmap[xbuf][0][bn_index(128)];
+      g.N = w.N;
+      g.K = w.K;
+      g.pair_rows = w.pair;
+      g.err = d->tc_err;
+      CK(launch_tc_gemm_big(g, rowsT, t_base, Y, ldy, ep, true, s));
+      nl++;
+      ng++;
+      return DORY_OK;
+    }
     const int bi = bn_index(tc_tile_rows(rowsT));
     g.tmXh = d->xmap[xbuf][0][bi];
     g.tmXl = d->xmap[xbuf][1][bi];
@@ -1082,6 +1098,7 @@ int setup_tc(dory_t *d) {
     if (e && e[0] == '0') return DORY_OK;
   }
   if (d->wdtype != W_BF16 || dm.hidden % 64 || dm.ffn % 64 || q_size % 64) return DORY_OK;
+  d->tc_big = !getenv_off("DORY_TC_BIG") && dm.ffn % 128 == 0;
   int dev = 0, sms = 148;
   CK(cudaGetDevice(&dev));
   CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));

@@ -407,6 +407,191 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   if (threadIdx.x == 64) mark(7);
 }
 
+// ---- many step rows: tokens as the MMA's M side ---------------------------------------
+//
+// When a step has hundreds of rows (prefill rows of several chunks or sequences at once)
+// the projections are dense contractions bound by the tensor pipe, not weight streams. Then
+// the MMA's M side is 128 step rows and its N side 256 weight rows (SwiGLU: 128 gate rows and
+// the matching 128 up rows), K steps of 16; the activations enter as one bf16 operand (the
+// rows rounded to bf16: one MMA per K step). A 4-stage ring of 48 KB stages (activation tile
+// 128 x 64, weight tile 256 x 64, both 128B-swizzled, loaded by TMA) feeds one issuing thread;
+// the accumulator is 256 TMEM columns; warps 2..5 read a token row per lane and store it with
+// the epilogue. One tile per block, grid = weight tiles x token tiles.
+constexpr int BT = 128;   // step rows per tile (MMA M)
+constexpr int BW = 256;   // weight rows per tile (MMA N)
+constexpr int BIG_ST = 4;
+constexpr int BIG_A = BT * BK * 2;               // 16 KB
+constexpr int BIG_B = BW * BK * 2;               // 32 KB
+constexpr int BIG_STAGE = BIG_A + BIG_B;         // 48 KB
+constexpr int BIG_SMEM = BIG_ST * BIG_STAGE + 1024;
+
+template <bool DUAL>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    tcb_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, int N, int K,
+                    int T, int t_base, long pair_rows, float *__restrict__ Y, int ldy, EpiArgs ep,
+                    int *__restrict__ err) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bar_full[BIG_ST], bar_empty[BIG_ST], bar_acc;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int failed;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int OUT = DUAL ? BW / 2 : BW;  // output columns of a tile
+  const int n0 = blockIdx.x * OUT;         // first output column (SwiGLU: gate row)
+  const int t0 = blockIdx.y * BT;
+  const int nk = K / BK;
+  const uint32_t base = (smem_u32(smem_raw) + 1023) & ~1023u;
+  auto a_addr = [&](int st) { return base + st * BIG_STAGE; };
+  auto b_addr = [&](int st) { return base + st * BIG_STAGE + BIG_A; };
+  // the two 128-row halves of the weight tile
+  const int w_lo = n0, w_hi = DUAL ? (int)(n0 + pair_rows) : n0 + BW / 2;
+
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < BIG_ST; st++) {
+      mbar_init(smem_u32(&bar_full[st]), 1);
+      mbar_init(smem_u32(&bar_empty[st]), 1);
+    }
+    mbar_init(smem_u32(&bar_acc), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    failed = 0;
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base_sh)),
+                 "r"(BW)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // weight tiles do not depend on earlier kernels: the first stages' go before the wait
+      const int pre = nk < BIG_ST ? nk : BIG_ST;
+      for (int i = 0; i < pre; i++) {
+        const uint32_t fb = smem_u32(&bar_full[i]);
+        mbar_expect_tx(fb, BIG_STAGE);
+        tma_load_2d(b_addr(i), &tmW, i * BK, w_lo, fb);
+        tma_load_2d(b_addr(i) + BIG_B / 2, &tmW, i * BK, w_hi, fb);
+      }
+      pdl_wait();
+      for (int i = 0; i < pre; i++) tma_load_2d(a_addr(i), &tmX, i * BK, t_base + t0, smem_u32(&bar_full[i]));
+      for (int i = pre; i < nk; i++) {
+        const int st = i % BIG_ST;
+        if (!mbar_wait(smem_u32(&bar_empty[st]), ((i / BIG_ST) - 1) & 1)) {
+          atomicExch(err, 11);
+          failed = 1;
+          break;
+        }
+        const uint32_t fb = smem_u32(&bar_full[st]);
+        mbar_expect_tx(fb, BIG_STAGE);
+        tma_load_2d(b_addr(st), &tmW, i * BK, w_lo, fb);
+        tma_load_2d(b_addr(st) + BIG_B / 2, &tmW, i * BK, w_hi, fb);
+        tma_load_2d(a_addr(st), &tmX, i * BK, t_base + t0, fb);
+      }
+    }
+  } else if (warp == 1) {
+    pdl_wait();
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(BT, BW);
+      for (int i = 0; i < nk; i++) {
+        const int st = i % BIG_ST;
+        if (!mbar_wait(smem_u32(&bar_full[st]), (i / BIG_ST) & 1)) {
+          atomicExch(err, 12);
+          failed = 1;
+          break;
+        }
+        fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; kk++)
+          mma_bf16(tmem, sw128_desc(a_addr(st) + kk * 32), sw128_desc(b_addr(st) + kk * 32), idesc,
+                   (i == 0 && kk == 0) ? 0u : 1u);
+        mma_commit(smem_u32(&bar_empty[st]));
+      }
+      mma_commit(smem_u32(&bar_acc));
+    }
+  } else {
+    pdl_wait();
+  }
+  pdl_trigger();
+
+  if (warp >= 2) {
+    const int q = warp & 3;
+    const int t = t0 + q * 32 + lane;  // this lane's step row
+    bool ok = mbar_wait(smem_u32(&bar_acc), 0);
+    if (!ok) {
+      atomicExch(err, 13);
+      failed = 1;
+    }
+    fence_after();
+    if (ok && !failed) {
+      const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+      const int mode = ep.mode;
+      for (int c0 = 0; c0 < OUT; c0 += 16) {
+        uint32_t v[16], u[16];
+        tmem_ld16_async(lane_base + c0, v);
+        if (DUAL) tmem_ld16_async(lane_base + BW / 2 + c0, u);
+        tmem_wait();
+        if (t >= T) continue;
+        float o[16];
+#pragma unroll
+        for (int j = 0; j < 16; j++) {
+          const int n = n0 + c0 + j;
+          const float a = __uint_as_float(v[j]);
+          if (mode == EPI_SCALE) {
+            o[j] = n < N ? a * __ldg(ep.vec + n) : 0.f;
+          } else if (mode == EPI_SILU) {
+            const float g = a * (n < N ? __ldg(ep.vec + n) : 0.f);
+            o[j] = g * sigmoidf_(g) * (__uint_as_float(u[j]) * (n < N ? __ldg(ep.vec2 + n) : 0.f));
+          } else {
+            o[j] = a;
+          }
+        }
+        float *yrow = Y + (size_t)t * ldy + n0 + c0;
+        if (n0 + c0 + 16 <= N) {
+#pragma unroll
+          for (int j = 0; j < 16; j += 4)
+            *reinterpret_cast<float4 *>(yrow + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; j++)
+            if (n0 + c0 + j < N) yrow[j] = o[j];
+        }
+      }
+    }
+  }
+  fence_before();
+  __syncthreads();
+  if (failed && threadIdx.x == 64) mbar_wait(smem_u32(&bar_acc), 0);  // let issued copies and MMAs land
+  __syncthreads();
+  fence_after();
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(BW) : "memory");
+}
+
+template <bool DUAL>
+cudaError_t tcb_launch(const TcGemm &g, int T, int t_base, float *Y, int ldy, EpiArgs ep, bool pdl, cudaStream_t s) {
+  auto kern = tcb_gemm_kernel<DUAL>;
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BIG_SMEM);
+    attr = true;
+  }
+  constexpr int OUT = DUAL ? BW / 2 : BW;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((g.N + OUT - 1) / OUT, (T + BT - 1) / BT);
+  cfg.blockDim = dim3(TC_THREADS);
+  cfg.dynamicSmemBytes = BIG_SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, g.tmW, g.tmXh, g.N, g.K, T, t_base, g.pair_rows, Y, ldy, ep, g.err);
+}
+
 // DORY_TC_TRIGGER=late: let the next kernel launch only once this one's epilogue is done
 int late_trigger() {
   static const int v = [] {
@@ -464,6 +649,13 @@ int tc_tile_rows(int T) {
   if (T <= 64) return 64;
   if (T <= 128) return 128;
   return 256;
+}
+
+cudaError_t launch_tc_gemm_big(const TcGemm &g, int T, int t_base, float *Y, int ldy, EpiArgs ep, bool pdl,
+                               cudaStream_t s) {
+  if (g.K % BK || (ep.mode == EPI_SILU ? g.N % (BW / 2) : 0) || ldy % 4) return cudaErrorInvalidValue;
+  if (ep.mode == EPI_SILU) return tcb_launch<true>(g, T, t_base, Y, ldy, ep, pdl, s);
+  return tcb_launch<false>(g, T, t_base, Y, ldy, ep, pdl, s);
 }
 
 cudaError_t launch_tc_gemm(const TcGemm &g, int T, int t_base, float *Y, int ldy, EpiArgs ep, bool pdl,

@@ -179,6 +179,13 @@ int make_tmap_bf16(CUtensorMap *map, const void *base, long rows, long cols, int
 cudaError_t launch_tc_gemm(const TcGemm &g, int T, int t_base, float *Y, int ldy, EpiArgs ep, bool pdl,
                            cudaStream_t s);
 
+// Steps of many rows (a few hundred and up): step rows as the MMA's M side (128 per tile),
+// 256 weight rows as N (SwiGLU: 128 gate + 128 up rows), activations as one bf16 operand
+// (g.tmXh, boxes of 128 rows x 64), one tile per block. g.tmW: boxes of 128 weight rows.
+// K a multiple of 64; SwiGLU: N a multiple of 128.
+cudaError_t launch_tc_gemm_big(const TcGemm &g, int T, int t_base, float *Y, int ldy, EpiArgs ep, bool pdl,
+                               cudaStream_t s);
+
 // ---- attention over f32 rings with TMA-staged tiles ------------------------------------
 
 int attn_tma_splits(long window_keys);

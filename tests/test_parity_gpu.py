@@ -404,3 +404,22 @@ def test_q8_per_loop_freeze_reads_rows_the_ring_no_longer_holds():
                 assert np.allclose(got["vcol"], s_.vcol, rtol=2e-2, atol=1e-5), (o_, sl)
     finally:
         P.close()
+
+
+def test_a_bounded_step_cache_evicts_and_recaptures(monkeypatch):
+    """With room for two captured steps, four step shapes in turn evict one another on every
+    call; each step is captured again when it comes back and still matches the oracle."""
+    monkeypatch.setenv("DORY_MAX_PLANS", "2")
+    cfg = synth.small(max_batch=6, max_seqs=6, rec_kinds="S*", full_window=0, max_context=1024, loops=2)
+    P = Pair(cfg, 2014)
+    try:
+        for s in range(6):
+            P.write_context(s, 50, 2014 + s)
+        shapes = [[0], [1, 2], [3, 4, 5, 0, 1], [2, 3]]
+        for step in range(8):
+            seqs = shapes[step % 4]
+            P.decode(seqs, synth.token_ids(2014, 10 + step, len(seqs), cfg.vocab), 2)
+        assert P.max_hidden_err <= 1e-4, P.max_hidden_err
+        assert all(P.top1)
+    finally:
+        P.close()
