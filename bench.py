@@ -119,6 +119,7 @@ def profile_case(args):
     decode-3pass: batch-1 decode of the 2B shape cut to one input, one recurrent and one
     output pair at loops 1 (427 MB of weights per token, still larger than L2, about 1 GB on
     the device); prefill: 64-row chunks of a prompt of --prompt tokens on the 2B model;
+    prefill-whole: the same prompt in one dory_prefill call;
     batch64: the batch-64 decode line with 4 timed steps."""
     import torch
 
@@ -134,14 +135,17 @@ def profile_case(args):
         dev = int(os.environ.get("LOCAL_RANK", "0"))
         return {"case": "context", "per_loop_batch16": bench_per_loop16(Dory, torch, w, dev),
                 "q8_batch64": bench_q8_batch64(Dory, torch, w, dev), "note": "profiling case, not a bench line"}
-    if args.profile_case == "prefill":
+    if args.profile_case in ("prefill", "prefill-whole"):
         cfg = synth.dory2b(max_batch=1, max_seqs=1, max_context=args.prompt + 64, prompt_loops=2)
         g = Dory(cfg, synth.weights(cfg, SEED))
         ids = synth.token_ids(SEED, 0, args.prompt, cfg.vocab)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        for a0 in range(0, args.prompt, 64):
-            g.prefill_chunk(0, ids[a0:a0 + 64], a0, cfg.loops, "none")
+        if args.profile_case == "prefill-whole":
+            g.prefill(0, ids, 0, cfg.loops, "none")
+        else:
+            for a0 in range(0, args.prompt, 64):
+                g.prefill_chunk(0, ids[a0:a0 + 64], a0, cfg.loops, "none")
         torch.cuda.synchronize()
         ms = (time.perf_counter() - t0) * 1e3
         g.close()
@@ -369,9 +373,12 @@ def bench_batch(g_cls, torch, w, dev, batch: int = 64, ctx: int = 1024, steps: i
         g.close()
 
 
-def bench_prefill(g_cls, torch, w, n_tokens: int = 16384, prompt_loops: int = 2):
-    """Prefill of an n-token seeded prompt in 64-row chunks at loops 4 (prompt_loops for the
-    chunks whose logits are unread, the last chunk reads its last row)."""
+def bench_prefill(g_cls, torch, w, n_tokens: int = 16384, prompt_loops: int = 2, whole: bool = True):
+    """Prefill of an n-token seeded prompt at loops 4 (prompt_loops for the chunks whose logits
+    are unread, the last chunk reads its last row). whole: one dory_prefill call (input and
+    output blocks over 512 rows at once, the recurrent block in 64-row chunks); else one
+    dory_prefill_chunk call per 64 rows. Reports the HBM roofline (weights streamed per step)
+    and the bf16 tensor roofline (algorithmic projection FLOPs, 2 x weights x rows)."""
     cfg = synth.dory2b(max_batch=1, max_seqs=1, max_context=n_tokens + 64, prompt_loops=prompt_loops)
     stream = torch.cuda.current_stream()
     g = g_cls(cfg, w, stream=stream.cuda_stream)
@@ -381,24 +388,35 @@ def bench_prefill(g_cls, torch, w, n_tokens: int = 16384, prompt_loops: int = 2)
 
         def run():
             g.reset(0)
-            wb = 0
+            if whole:
+                g.prefill(0, dids, 0, cfg.loops, "last")
+                st = g.stats()
+                return st["weight_bytes"], st["flops"]
+            wb = fl = 0
             for a in range(0, n_tokens, 64):
                 g.prefill_chunk(0, dids[a:a + 64], a, cfg.loops, "last" if a + 64 >= n_tokens else "none")
-                wb += g.stats()["weight_bytes"]
-            return wb
-        run()  # warm-up: captures the chunk graphs
+                st = g.stats()
+                wb += st["weight_bytes"]
+                fl += st["flops"]
+            return wb, fl
+        run()  # warm-up: captures the step graphs
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        wb = run()
+        wb, fl = run()
         e1.record(stream)
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1)
-        hbm, _, _ = peaks()
+        hbm, tf, src = peaks()
         return {"value": round(n_tokens / (ms / 1e3), 1), "unit": "tokens/s", "ms": round(ms, 2),
-                "tokens": n_tokens, "chunk": 64, "loops": cfg.loops, "prompt_loops": prompt_loops,
+                "tokens": n_tokens, "call": "dory_prefill" if whole else "dory_prefill_chunk x 64 rows",
+                "loops": cfg.loops, "prompt_loops": prompt_loops,
                 "roofline": {"bound": "hbm", "achieved": round(wb / (ms / 1e3) / 1e9, 1), "peak": hbm,
-                             "unit": "GB/s", "frac": round(wb / (ms / 1e3) / 1e9 / hbm, 4), "weight_bytes": wb}}
+                             "unit": "GB/s", "frac": round(wb / (ms / 1e3) / 1e9 / hbm, 4), "weight_bytes": wb},
+                "tensor": {"achieved": round(fl / (ms / 1e3) / 1e12, 1), "peak": tf, "unit": "TFLOP/s",
+                           "frac": round(fl / (ms / 1e3) / 1e12 / tf, 4), "flops": fl,
+                           "note": f"algorithmic projection and head FLOPs (2 x weights x rows) over the call; "
+                                   f"peak: bf16 dense, {src}"}}
     finally:
         g.close()
 
@@ -461,7 +479,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the batch-64 decode and prefill lines")
     ap.add_argument("--prompt", type=int, default=PROMPT, help="prompt tokens before the decode steps")
-    ap.add_argument("--profile-case", choices=["decode-3pass", "prefill", "batch64", "context"],
+    ap.add_argument("--profile-case", choices=["decode-3pass", "prefill", "prefill-whole", "batch64", "context"],
                     help="run a small case for ncu captures instead of the bench")
     args = ap.parse_args()
     if args.profile_case:
@@ -488,6 +506,7 @@ def main():
         dev = int(os.environ.get("LOCAL_RANK", "0"))
         out["extra"] = {"decode_batch64": bench_batch(Dory, torch, w, dev),
                         "prefill_16k": bench_prefill(Dory, torch, w),
+                        "prefill_16k_chunks": bench_prefill(Dory, torch, w, whole=False),
                         "decode_per_loop_batch16_ctx8192": bench_per_loop16(Dory, torch, w, dev),
                         "decode_q8_batch64_ctx8192": bench_q8_batch64(Dory, torch, w, dev)}
     if rank == 0:

@@ -157,6 +157,19 @@ int dory_rollback(dory_t *d, int32_t seq, int32_t n);
 int dory_prefill_chunk(dory_t *d, int32_t seq, const int32_t *ids, int32_t n, int32_t pos0,
                        int32_t loops, int32_t want);
 
+/* A whole prompt of `n` rows of sequence `seq` from position pos0: the same result as
+ * dory_prefill_chunk over consecutive chunks of 64 rows from pos0 with `want` on the last
+ * chunk and DORY_WANT_NONE on the others (dory.rs fn forward_host; prompt_loops as there).
+ * The input and output blocks run once per row, at loop 0, and attend causally to their own
+ * rows, so they run over up to 512 rows of several chunks at once (dense contractions on the
+ * tensor cores, activations rounded to bf16 from 256 rows up), while the recurrent block
+ * runs chunk by chunk (under last_loop a chunk's rows see earlier chunks at their last
+ * pass). The row count per block step is what the input/output rings hold beyond their
+ * window (512 with the pages' sizes); without room for 128 rows, or with f32 weights, the
+ * prompt goes chunk by chunk. `want`: DORY_WANT_NONE or DORY_WANT_LAST (one logits row).
+ * Errors: as dory_prefill_chunk (n >= 1, want none or last). */
+int dory_prefill(dory_t *d, int32_t seq, const int32_t *ids, int32_t n, int32_t pos0, int32_t loops, int32_t want);
+
 /* Prefill chunks of several sequences in one step (the chunk of dory.rs fn forward_host for
  * each, at that sequence's position): sequence seqs[j] takes counts[j] (1..64) rows, ids
  * [sum of counts] holding each sequence's rows in turn. Every projection runs once over all
@@ -256,9 +269,11 @@ typedef struct dory_stats {
   uint64_t kv_write_bytes;      /* KV bytes the last call wrote */
   uint64_t launches;            /* kernels the last call launched */
   uint64_t gemm_launches;       /* of which weight-streaming GEMV/GEMM launches */
+  uint64_t flops;               /* algorithmic FLOPs of the last call's projections and head (2 x weights x rows) */
 } dory_stats;
 
-/* Byte and launch accounting of the handle and of its last call. */
+/* Byte and launch accounting of the handle and of its last call (dory_prefill: the totals
+ * over its steps). */
 int dory_get_stats(dory_t *d, dory_stats *out);
 
 /* ---- for callers that cannot allocate device memory ---------------------------------- */

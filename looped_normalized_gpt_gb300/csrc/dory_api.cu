@@ -109,6 +109,7 @@ struct dory_handle {
   size_t esz = 4;
   cudaStream_t stream = nullptr;
   int Tmax = 64;
+  int prefill_rows = 0;  // rows of a whole prompt's input/output-block steps (dory_prefill); 0: chunk by chunk
 
   char *wmem = nullptr;
   size_t wbytes = 0;
@@ -294,9 +295,12 @@ int reset_seq(dory_t *d, int seq) {
 // `rl`: per-row loop counts (empty: every row runs `loops`), sorted from the most loops down
 // so that the rows a pass runs are a prefix; `perm[r]` is the caller's index of row r (ids
 // are gathered into this order, logits and hidden rows scattered back).
+// `do_in` / `do_out`: run the input block (with the embedding) / the output block; a whole
+// prompt runs its input and output blocks over many chunks' rows at once and its recurrent
+// block chunk by chunk, each chunk's rows at row offset `h0` of the hidden buffers.
 struct StepArgs {
-  int T = 0, loops = 1, head_from = 0, head_rows = 0, first_loop = 0;
-  bool resume = false;
+  int T = 0, loops = 1, head_from = 0, head_rows = 0, first_loop = 0, h0 = 0;
+  bool resume = false, do_in = true, do_out = true;
   std::vector<int> hseq, hoff, aseq, acnt, rl, perm;
   // rows whose logits are read when they are not one run (the last row of each sequence of a
   // batched prefill): the head covers rows [0, T) and these rows are gathered, in order
@@ -311,7 +315,8 @@ struct StepArgs {
   }
   std::string key() const {
     std::string k = std::to_string(T) + ":" + std::to_string(loops) + ":" + std::to_string(head_from) + ":" +
-                    std::to_string(head_rows) + ":" + std::to_string(first_loop) + (resume ? "r" : "") + "|";
+                    std::to_string(head_rows) + ":" + std::to_string(first_loop) + (resume ? "r" : "") +
+                    (do_in ? "i" : "") + (do_out ? "o" : "") + std::to_string(h0) + "|";
     for (int i = 0; i < T; i++) k += std::to_string(hseq[i]) + "," + std::to_string(hoff[i]) + ";";
     if (!rl.empty()) {
       k += "L";
@@ -332,12 +337,14 @@ void account(dory_t *d, const StepArgs &a) {
   const bool q8 = c.kv_quant == DORY_KV_Q8_2F;
   const size_t kv_row_bytes = q8 ? (size_t)dm.hd * 2 + (dm.hd / 32) * 4 + 4 : (size_t)dm.hd * 8;
   const int q_size = dm.nh * dm.hd, kv_size = dm.nk * dm.hd;
-  uint64_t wb = 0, kr = 0, kw = 0;
+  uint64_t wb = 0, kr = 0, kw = 0, fl = 0;
   auto layer = [&](int li, int loop_i) {
     const LayerDev &L = d->layers[li];
     const int rows = L.rec ? a.active(loop_i) : a.T;
     if (L.attn) {
-      wb += (uint64_t)(2 * q_size + 2 * kv_size) * dm.hidden * d->esz + (uint64_t)dm.hidden * q_size * d->esz;
+      const uint64_t params = (uint64_t)(2 * q_size + 2 * kv_size) * dm.hidden + (uint64_t)dm.hidden * q_size;
+      wb += params * d->esz;
+      fl += 2 * params * rows;
       const int sl = (c.kv_mode == DORY_KV_PER_LOOP && L.rec) ? loop_i : 0;
       const bool rewrite = (c.kv_mode == DORY_KV_LAST_LOOP && (L.rec || L.out) && loop_i > 0) || (a.resume && L.out);
       const OrdInfo &o = d->ords[L.ordinal];
@@ -350,16 +357,22 @@ void account(dory_t *d, const StepArgs &a) {
       kw += (uint64_t)rows * dm.nk * kv_row_bytes;
     } else {
       wb += (uint64_t)3 * dm.ffn * dm.hidden * d->esz;
+      fl += (uint64_t)6 * dm.ffn * dm.hidden * rows;
     }
   };
   const int n_in = c.n_in, n_rec = c.n_rec, n_all = (int)d->layers.size();
-  if (!a.resume)
+  if (!a.resume && a.do_in)
     for (int li = 0; li < n_in; li++) layer(li, 0);
   for (int i = a.first_loop; i < a.loops; i++)
     for (int li = n_in; li < n_in + n_rec; li++) layer(li, i);
-  for (int li = n_in + n_rec; li < n_all; li++) layer(li, a.resume ? 1 : 0);
-  if (a.head_rows > 0) wb += (uint64_t)dm.vocab * dm.hidden * d->esz;
+  if (a.do_out)
+    for (int li = n_in + n_rec; li < n_all; li++) layer(li, a.resume ? 1 : 0);
+  if (a.head_rows > 0) {
+    wb += (uint64_t)dm.vocab * dm.hidden * d->esz;
+    fl += (uint64_t)2 * dm.vocab * dm.hidden * a.head_rows;
+  }
   d->st.weight_bytes = wb;
+  d->st.flops = fl;
   d->st.kv_read_bytes = kr;
   d->st.kv_write_bytes = kw;
 }
@@ -412,8 +425,14 @@ int issue_step(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_splits, cud
     nl++;
     ids = d->d_ids2;
   }
-  CK(launch_embed_rope(ids, d->embed, d->wdtype, dm, rows, c.rope_theta_sliding, c.rope_theta_full, d->h,
-                       d->rope, tc ? d->em_h : Emit{nullptr, nullptr}, s));
+  // the step's hidden rows: rows h0.. of the hidden, input and state buffers (and of the
+  // activations' bf16 halves)
+  const size_t ho = (size_t)a.h0 * dm.hidden;
+  float *const H = d->h + ho, *const IN = d->input + ho, *const ST = d->state + ho;
+  const Emit EH = tc ? Emit{d->em_h.hi + ho, d->em_h.lo + ho} : Emit{nullptr, nullptr};
+  const bool embed = a.do_in && !a.resume;
+  CK(launch_embed_rope(ids, d->embed, d->wdtype, dm, rows, c.rope_theta_sliding, c.rope_theta_full,
+                       embed ? H : nullptr, d->rope, EH, s));
   nl++;
   auto tcg = [&](const TcW &w, int xbuf, int rowsT, int t_base, float *Y, int ldy, EpiArgs ep) -> int {
     TcGemm g;
@@ -459,15 +478,15 @@ int issue_step(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_splits, cud
   // The residual of rows [0, Tr) with the loop mix `mix` for rows [0, Tsplit) and MIX_END for
   // rows [Tsplit, Tr) (rows whose last pass this is, when loop counts differ per row).
   auto resid = [&](const float *alpha, int mix, int Tr, int Tsplit, int do_res) -> int {
-    const Emit em = tc ? d->em_h : Emit{nullptr, nullptr};
+    const Emit em = EH;
     if (Tsplit > 0) {
-      CK(launch_residual(d->h, d->out, alpha, Tsplit, dm.hidden, mix, d->input, d->state, do_res, em, s));
+      CK(launch_residual(H, d->out, alpha, Tsplit, dm.hidden, mix, IN, ST, do_res, em, s));
       nl++;
     }
     if (Tr > Tsplit) {
       const size_t o = (size_t)Tsplit * dm.hidden;
       const Emit e2 = em.hi ? Emit{em.hi + o, em.lo + o} : em;
-      CK(launch_residual(d->h + o, d->out + o, alpha, Tr - Tsplit, dm.hidden, MIX_END, d->input + o, d->state + o,
+      CK(launch_residual(H + o, d->out + o, alpha, Tr - Tsplit, dm.hidden, MIX_END, IN + o, ST + o,
                          do_res, e2, s));
       nl++;
     }
@@ -484,8 +503,8 @@ int issue_step(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_splits, cud
       Ring ring = d->ring(L.ordinal, sl);
       EpiArgs ep{EPI_STORE, nullptr, nullptr, 0};
       if (tc) {
-        if ((rc = tcg(d->tcw[li][0], 0, Tr, 0, d->qkvg, ldq, ep))) return rc;
-      } else if ((rc = gemm(L.wqkvg, ldq, dm.hidden, d->h, dm.hidden, Tr, d->qkvg, ldq, ep))) {
+        if ((rc = tcg(d->tcw[li][0], 0, Tr, a.h0, d->qkvg, ldq, ep))) return rc;
+      } else if ((rc = gemm(L.wqkvg, ldq, dm.hidden, H, dm.hidden, Tr, d->qkvg, ldq, ep))) {
         return rc;
       }
       CK(launch_prep(d->qkvg, ldq, dm, rows_l, d->rope, L.sliding ? 0 : 1, L.sq, ring, d->kst, d->vst, s));
@@ -512,7 +531,7 @@ int issue_step(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_splits, cud
           const size_t zo = (size_t)r0 * q_size;
           const Emit ez = tc ? Emit{d->em_z.hi + zo, d->em_z.lo + zo} : Emit{nullptr, nullptr};
           CK(launch_attention_chunk(d->qkvg + (size_t)r0 * ldq, ldq, dm, rs, ring, nkb, d->part, L.sg, d->z + zo, ez,
-                                    s));
+                                    d->dev_err, s));
           nl += 2;
         }
         z_normed = true;
@@ -549,8 +568,8 @@ int issue_step(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_splits, cud
     } else {
       EpiArgs ep{EPI_SILU, L.msg, L.msu, (long)dm.ffn};
       if (tc) {
-        if ((rc = tcg(d->tcw[li][0], 0, Tr, 0, d->mlp, dm.ffn, ep))) return rc;
-      } else if ((rc = gemm(L.wgu, dm.ffn, dm.hidden, d->h, dm.hidden, Tr, d->mlp, dm.ffn, ep))) {
+        if ((rc = tcg(d->tcw[li][0], 0, Tr, a.h0, d->mlp, dm.ffn, ep))) return rc;
+      } else if ((rc = gemm(L.wgu, dm.ffn, dm.hidden, H, dm.hidden, Tr, d->mlp, dm.ffn, ep))) {
         return rc;
       }
       CK(launch_rownorm(d->mlp, Tr, dm.ffn, dm.ffn, tc ? d->em_y : Emit{nullptr, nullptr}, s));
@@ -570,7 +589,7 @@ int issue_step(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_splits, cud
   const int n_in = c.n_in, n_rec = c.n_rec, n_all = (int)d->layers.size();
   if (a.resume) {
     if ((rc = mix_only(MIX_RESUME, T, T))) return rc;
-  } else {
+  } else if (a.do_in) {
     for (int li = 0; li < n_in; li++)
       if ((rc = layer(li, 0, li == n_in - 1 ? MIX_BEGIN : MIX_NONE, T, T))) return rc;
     if (n_in == 0 && (rc = mix_only(MIX_BEGIN, T, T))) return rc;
@@ -585,16 +604,17 @@ int issue_step(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_splits, cud
     }
     if (n_rec == 0 && (rc = mix_only(MIX_LOOP, Ti, Tn))) return rc;
   }
-  for (int li = n_in + n_rec; li < n_all; li++)
-    if ((rc = layer(li, a.resume ? 1 : 0, MIX_NONE, T, T))) return rc;
+  if (a.do_out)
+    for (int li = n_in + n_rec; li < n_all; li++)
+      if ((rc = layer(li, a.resume ? 1 : 0, MIX_NONE, T, T))) return rc;
   if (a.head_rows > 0) {
     EpiArgs ep{EPI_SCALE, d->logit_scale, nullptr, 0};
     const bool pick = !a.head_pick.empty();
     float *lg = ragged || pick ? d->logits2 : d->logits;
     if (tc && a.head_rows >= 5) {
-      if ((rc = tcg(d->tc_head, 0, a.head_rows, a.head_from, lg, dm.vocab, ep))) return rc;
+      if ((rc = tcg(d->tc_head, 0, a.head_rows, a.h0 + a.head_from, lg, dm.vocab, ep))) return rc;
     } else {
-      CK(launch_gemm(d->head, d->wdtype, dm.vocab, dm.hidden, d->h + (size_t)a.head_from * dm.hidden, dm.hidden,
+      CK(launch_gemm(d->head, d->wdtype, dm.vocab, dm.hidden, H + (size_t)a.head_from * dm.hidden, dm.hidden,
                      a.head_rows, lg, dm.vocab, ep, s));
       nl++;
       ng++;
@@ -609,7 +629,7 @@ int issue_step(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_splits, cud
     }
   }
   if (ragged) {  // and the final hidden rows
-    CK(launch_scatter_rows(d->h, d->h2, perm, T, dm.hidden, s));
+    CK(launch_scatter_rows(H, d->h2, perm, T, dm.hidden, s));
     nl++;
     d->h_last = d->h2;
   }
@@ -792,7 +812,7 @@ int issue_step_fused(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_split
 }
 
 int issue_any(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_splits, cudaStream_t s, int *nl, int *ng) {
-  if (d->fused_ok && a.T <= 4 && a.rl.empty() && a.head_pick.empty())
+  if (d->fused_ok && a.T <= 4 && a.rl.empty() && a.head_pick.empty() && a.do_in && a.do_out && a.h0 == 0)
     return issue_step_fused(d, a, rt, fixed_splits, s, nl, ng);
   d->h_last = d->h;
   return issue_step(d, a, rt, fixed_splits, s, nl, ng);
@@ -800,7 +820,8 @@ int issue_any(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_splits, cuda
 
 // The persistent kernel runs steps of one row that end with that row's logits.
 bool use_mega(const dory_t *d, const StepArgs &a) {
-  return d->mega_ok && a.T == 1 && a.head_rows == 1 && a.head_from == 0 && a.aseq.size() == 1;
+  return d->mega_ok && a.T == 1 && a.head_rows == 1 && a.head_from == 0 && a.aseq.size() == 1 && a.do_in &&
+         a.do_out && a.h0 == 0;
 }
 
 // The stage list of a one-row step, in the order of issue_step_fused's launches.
@@ -1213,6 +1234,26 @@ int dory_create(const dory_config *cfg, const dory_weights *w, void *stream, dor
   d->esz = cfg->weight_dtype == DORY_W_BF16 ? 2 : 4;
   d->stream = static_cast<cudaStream_t>(stream);
   d->Tmax = std::max(DORY_CHUNK_ROWS, cfg->max_batch);
+  {
+    // dory_prefill runs the input and output blocks over up to 512 rows at once: all of them
+    // join a ring before any attends, so a sliding (or capped full) ring must hold the rows
+    // plus the window behind the first: rows + window - 1 <= ring rows
+    long lim = 512;
+    for (size_t li = 0; li < pat.size(); li++) {
+      const bool io = (int)li < cfg->n_in || (int)li >= cfg->n_in + cfg->n_rec;
+      if (!io || pat[li] == '-') continue;
+      long cap, win;
+      if (pat[li] == 'S') win = cfg->window;
+      else if (cfg->full_window > 0) win = cfg->full_window;
+      else continue;  // every position from 0 stays in such a ring
+      cap = (win + RING_EXTRA + 63) / 64 * 64;
+      lim = std::min(lim, cap - win + 1);
+    }
+    if (const char *e = getenv("DORY_PREFILL_ROWS")) lim = std::min<long>(lim, std::max(0, atoi(e)));
+    lim = lim / 64 * 64;
+    d->prefill_rows = (lim >= 128 && cfg->weight_dtype == DORY_W_BF16) ? (int)lim : 0;
+    d->Tmax = std::max(d->Tmax, d->prefill_rows);
+  }
   const Dims &dm = d->dims;
   const size_t esz = d->esz;
   const int q_size = dm.nh * dm.hd, kv_size = dm.nk * dm.hd;
@@ -1615,6 +1656,83 @@ int dory_prefill_chunk(dory_t *d, int32_t seq, const int32_t *ids, int32_t n, in
   st.head_from = want == DORY_WANT_ALL ? 0 : n - 1;
   if ((rc = do_step(d, st, ids))) return rc;
   d->logits_rows = head_rows;
+  return DORY_OK;
+}
+
+int dory_prefill(dory_t *d, int32_t seq, const int32_t *ids, int32_t n, int32_t pos0, int32_t loops, int32_t want) {
+  if (!d) return fail(DORY_EINVAL, "handle is NULL");
+  if (seq < 0 || seq >= d->cfg.max_seqs) return fail(DORY_EINVAL, "seq %d out of range", seq);
+  if (n < 1) return fail(DORY_EINVAL, "n=%d must be positive", n);
+  if (!ids) return fail(DORY_EINVAL, "ids is NULL");
+  if (loops < 1 || loops > d->cfg.max_loops) return fail(DORY_EINVAL, "loops=%d: want 1..%d", loops, d->cfg.max_loops);
+  if (want != DORY_WANT_NONE && want != DORY_WANT_LAST) return fail(DORY_EINVAL, "want=%d: none or last", want);
+  if (pos0 != d->seq_pos[seq])
+    return fail(DORY_ESTATE, "pos0=%d but sequence %d is at %d", pos0, seq, d->seq_pos[seq]);
+  int rc = check_range(d, seq, (long)pos0 + n - 1);
+  if (rc) return rc;
+  const int S = d->prefill_rows;
+  if (S < 128) {  // chunk by chunk
+    for (int a0 = 0; a0 < n; a0 += DORY_CHUNK_ROWS) {
+      const int m = std::min(DORY_CHUNK_ROWS, n - a0);
+      if ((rc = dory_prefill_chunk(d, seq, ids + a0, m, pos0 + a0, loops, a0 + m == n ? want : DORY_WANT_NONE)))
+        return rc;
+    }
+    return DORY_OK;
+  }
+  auto rows = [&](StepArgs &st, int T, int off0) {
+    st.T = T;
+    st.hseq.assign(T, seq);
+    st.hoff.resize(T);
+    for (int i = 0; i < T; i++) st.hoff[i] = off0 + i;
+    st.aseq.assign(1, seq);
+    st.acnt.assign(1, 0);
+  };
+  dory_stats sum{};
+  auto add = [&]() {
+    sum.weight_bytes += d->st.weight_bytes;
+    sum.kv_read_bytes += d->st.kv_read_bytes;
+    sum.kv_write_bytes += d->st.kv_write_bytes;
+    sum.launches += d->st.launches;
+    sum.gemm_launches += d->st.gemm_launches;
+    sum.flops += d->st.flops;
+  };
+  for (int a0 = 0; a0 < n; a0 += S) {
+    const int Sa = std::min(S, n - a0);
+    StepArgs in;  // embedding and input block over the rows (loop slot 0, run once)
+    rows(in, Sa, 0);
+    in.loops = 0;
+    in.do_out = false;
+    if ((rc = do_step(d, in, ids + a0))) return rc;
+    add();
+    for (int c = 0; c < Sa; c += DORY_CHUNK_ROWS) {  // the recurrent block, chunk by chunk
+      const int nc = std::min(DORY_CHUNK_ROWS, Sa - c);
+      const bool last = a0 + c + nc == n;
+      StepArgs r;
+      rows(r, nc, c);
+      r.h0 = c;
+      r.do_in = r.do_out = false;
+      r.loops = loops;  // dory.rs fn chunk_loops: a chunk whose logits are unread takes prompt_loops
+      if (!(last && want == DORY_WANT_LAST) && d->cfg.prompt_loops > 0 && d->cfg.kv_mode == DORY_KV_LAST_LOOP)
+        r.loops = std::min(loops, d->cfg.prompt_loops);
+      if ((rc = do_step(d, r, ids + a0 + c))) return rc;
+      add();
+    }
+    StepArgs out;  // output block over the rows' final states, the head of the prompt's last row
+    rows(out, Sa, 0);
+    out.loops = 0;
+    out.do_in = false;
+    out.acnt.assign(1, Sa);
+    if (a0 + Sa == n && want == DORY_WANT_LAST) {
+      out.head_from = Sa - 1;
+      out.head_rows = 1;
+    }
+    if ((rc = do_step(d, out, ids + a0))) return rc;
+    add();
+  }
+  sum.weight_bytes_device = d->st.weight_bytes_device;
+  sum.kv_bytes_device = d->st.kv_bytes_device;
+  d->st = sum;  // the call's totals over its steps
+  d->logits_rows = want == DORY_WANT_LAST ? 1 : 0;
   return DORY_OK;
 }
 

@@ -63,9 +63,11 @@ __global__ void embed_rope_kernel(const int32_t *__restrict__ ids, const WT *__r
                                   double theta_s, double theta_f, float *__restrict__ h,
                                   float *__restrict__ rope, Emit em) {
   const int r = blockIdx.x;
-  const int id = ids[r];
-  float *hr = h + (size_t)r * d.hidden;
-  if (id >= 0 && id < d.vocab) {
+  const int id = h ? ids[r] : -1;
+  float *hr = h ? h + (size_t)r * d.hidden : nullptr;
+  if (!h) {
+    // the RoPE table alone (rows that continue from saved hidden rows)
+  } else if (id >= 0 && id < d.vocab) {
     const WT *er = E + (size_t)id * d.hidden;
     for (int i = threadIdx.x; i < d.hidden; i += blockDim.x) {
       const float x = load_w(er, i);

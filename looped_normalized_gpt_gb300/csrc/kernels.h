@@ -68,6 +68,7 @@ struct Emit {
   __nv_bfloat16 *hi, *lo;
 };
 
+// h null: only the RoPE table of the rows (their hidden rows are not touched, ids unused).
 cudaError_t launch_embed_rope(const int32_t *ids, const void *E, int wdtype, Dims d, Rows rows,
                               double theta_s, double theta_f, float *h, float *rope, Emit em, cudaStream_t s);
 
@@ -97,7 +98,7 @@ cudaError_t launch_attention(const float *qkvg, int ldq, Dims d, Rows rows, Ring
 // gated and row-normalised (with its bf16 halves when em.hi is set).
 int attn_chunk_blocks(long window_keys, int rows);
 cudaError_t launch_attention_chunk(const float *qkvg, int ldq, Dims d, Rows rows, Ring ring, int nkb, float *part,
-                                   const float *sg, float *z, Emit em, cudaStream_t s);
+                                   const float *sg, float *z, Emit em, int *err, cudaStream_t s);
 
 // Rows of any sequences (a batched decode step) over f32 rings, hd 64 or 128: one block per
 // (row, kv head) streams the window in 32-position tiles; writes z gated (not row-normalised).

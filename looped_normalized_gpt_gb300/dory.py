@@ -53,7 +53,8 @@ class WeightsC(ctypes.Structure):
 
 class StatsC(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in ("weight_bytes_device", "kv_bytes_device", "weight_bytes",
-                                                "kv_read_bytes", "kv_write_bytes", "launches", "gemm_launches")]
+                                                "kv_read_bytes", "kv_write_bytes", "launches", "gemm_launches",
+                                                "flops")]
 
 
 # Every entry point of include/dory.h with its argument types.
@@ -65,6 +66,8 @@ SIGNATURES = {
     "dory_rollback": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32]),
     "dory_prefill_chunk": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32,
                                           ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]),
+    "dory_prefill": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32,
+                                    ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]),
     "dory_prefill_batch": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
                                           ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32]),
     "dory_decode_step": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
@@ -187,6 +190,12 @@ class Dory:
         ids_a = ids if hasattr(ids, "data_ptr") else np.ascontiguousarray(ids, dtype=np.int32)
         n = int(ids_a.numel() if hasattr(ids_a, "numel") else ids_a.size)
         self._check(self.lib.dory_prefill_chunk(self.h, seq, _ptr(ids_a), n, pos0, loops, WANT[want]))
+
+    def prefill(self, seq: int, ids, pos0: int, loops: int, want: str = "last") -> None:
+        """A whole prompt (any length) from pos0, as consecutive 64-row chunks."""
+        ids_a = ids if hasattr(ids, "data_ptr") else np.ascontiguousarray(ids, dtype=np.int32)
+        n = int(ids_a.numel() if hasattr(ids_a, "numel") else ids_a.size)
+        self._check(self.lib.dory_prefill(self.h, seq, _ptr(ids_a), n, pos0, loops, WANT[want]))
 
     def prefill_batch(self, seqs, chunks, loops: int, want: str = "last") -> None:
         """One prefill chunk for each sequence in seqs (chunks[j]: its ids), in one step."""

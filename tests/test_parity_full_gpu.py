@@ -290,3 +290,34 @@ def test_batch1_decode_at_prompt_4096_replays_exactly():
         assert np.array_equal(first.view(np.uint32), second.view(np.uint32))
     finally:
         g.close()
+
+
+def test_prefill_2048_in_block_steps_of_512_rows():
+    """The prefill workload's shape through dory_prefill: 2048 tokens, the input and output
+    blocks over 512 rows at once (tensor-core kernel with the step rows as the MMA's M side),
+    the recurrent block in 64-row chunks, prompt_loops 2, the last row's logits read; against
+    the oracle's chunked forward."""
+    from looped_normalized_gpt_gb300 import Dory, build
+
+    build()
+    cfg = synth.dory2b(prompt_loops=2, max_context=2048 + 64)
+    w = synth.weights(cfg, SEED_4)
+    g = Dory(cfg, w)
+    o = O.DoryOracle(cfg, w)
+    st = O.SeqState()
+    try:
+        ids = synth.token_ids(SEED_4, 0, 2048, cfg.vocab)
+        g.prefill(0, ids, 0, 4, "last")
+        for a in range(0, 2048, 64):
+            lo, ho = o.forward_chunk(st, ids[a:a + 64], a, 4, "last" if a + 64 >= 2048 else "none")
+        hg = g.read_hidden(512)
+        herr = float(np.max(np.abs(hg[-64:] - ho)))
+        assert herr <= 2e-2, herr
+        e, t1 = _check_row(o, cfg, hg[-1], ho[-1], g.logits(0), lo[0])
+        assert t1
+        for (ordn, sl), slot in st.slots.items():
+            cap, _, _ = g.slot_info(ordn)
+            tags, _, _ = g.read_kv_f32(0, ordn, sl)
+            assert np.array_equal(tags.astype(np.int64), slot.ring_image(cap))
+    finally:
+        g.close()
