@@ -63,6 +63,7 @@ constexpr int TC_TRACE_BLOCKS = 1024;
 // Steps with at least this many rows take the tensor-core kernel with the step rows as the
 // MMA's M side and bf16 activations (below it the weights stream once for a thin row block).
 constexpr int TC_BIG_ROWS = 256;
+constexpr int TC_BIG_CTRS = 4096;  // tile counters of launch_tc_gemm_big's split K
 
 int bn_index(int bn) { return bn <= 16 ? 0 : bn <= 32 ? 1 : bn <= 64 ? 2 : bn <= 128 ? 3 : 4; }
 
@@ -141,6 +142,9 @@ struct dory_handle {
   // L2 lead of the kernel's weight stream, bytes per block (DORY_MEGA_PREFETCH): about two
   // chunks measured best (1 chunk -0.5%, 5 chunks -1%, none -5%)
   int mega_prefetch = 32768;
+  // the L2 lead the producer builds while its slots are all taken, bytes per block
+  // (DORY_MEGA_LEAD; 0: no more than mega_prefetch)
+  int mega_lead = 0;
   int mega_inflight = 0;  // cap on a block's weight copies in flight (DORY_MEGA_INFLIGHT)
   // tensor-core projections: weight maps per layer ([0] q/k/v/g or gate/up, [1] o or down)
   bool tc_ok = false;
@@ -154,8 +158,8 @@ struct dory_handle {
   KvMaps kvq;                 // q8 KV memory (hd = 128) for the attention's tile copies
   bool kv_tma_q8 = false;
   int32_t *dev_err = nullptr;  // set by a kernel whose bounded wait expired
-  float *tc_ws = nullptr;
-  int32_t *tc_ctr = nullptr, *tc_err = nullptr;
+  float *tc_ws = nullptr, *tc_ws_big = nullptr;
+  int32_t *tc_ctr = nullptr, *tc_err = nullptr, *tc_ctr_big = nullptr;
   float *h = nullptr, *input = nullptr, *state = nullptr, *qkvg = nullptr, *z = nullptr, *out = nullptr,
         *mlp = nullptr, *logits = nullptr, *rope = nullptr, *part = nullptr, *kst = nullptr, *vst = nullptr;
   float *logits2 = nullptr;  // logits of a reordered step, before they go back to the caller's order
@@ -443,6 +447,10 @@ int issue_step(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_splits, cud
       g.K = w.K;
       g.pair_rows = w.pair;
       g.err = d->tc_err;
+      g.ws_big = d->tc_ws_big;
+      g.ctr_big = d->tc_ctr_big;
+      g.ctr_slots = TC_BIG_CTRS;
+      g.sms = d->sms;
       CK(launch_tc_gemm_big(g, rowsT, t_base, Y, ldy, ep, true, s));
       nl++;
       ng++;
@@ -971,6 +979,7 @@ int issue_mega(dory_t *d, const StepArgs &a, int32_t *rt, const MegaStage *stage
   m.adv_cnt = a.acnt[0];
   m.trace = (size_t)nstages <= d->mega_trace_stages ? d->mega_trace : nullptr;
   m.prefetch_ahead = d->mega_prefetch;
+  m.stall_lead = std::max(d->mega_prefetch, d->mega_lead);
   m.max_inflight = d->mega_inflight;
   CK(launch_mega_decode(m, d->sms, s));
   return DORY_OK;
@@ -1175,6 +1184,10 @@ int setup_tc(dory_t *d) {
   off = align256(off + (size_t)max_tiles * 4);
   const size_t o_err = off;
   off = align256(off + 4);
+  const size_t o_wsb = off;
+  if (d->tc_big) off = align256(off + (size_t)2 * sms * 128 * 256 * 4);
+  const size_t o_ctrb = off;
+  if (d->tc_big) off = align256(off + (size_t)TC_BIG_CTRS * 4);
   if (cudaMalloc(&d->tcmem, off) != cudaSuccess) {
     cudaGetLastError();
     return fail(DORY_ENOMEM, "cudaMalloc of %zu tensor-core bytes", off);
@@ -1192,6 +1205,10 @@ int setup_tc(dory_t *d) {
   d->em_z = Emit{buf[1][0], buf[1][1]};
   d->em_y = Emit{buf[2][0], buf[2][1]};
   d->tc_ws = reinterpret_cast<float *>(d->tcmem + o_ws);
+  if (d->tc_big) {
+    d->tc_ws_big = reinterpret_cast<float *>(d->tcmem + o_wsb);
+    d->tc_ctr_big = reinterpret_cast<int32_t *>(d->tcmem + o_ctrb);
+  }
   d->tc_ctr = reinterpret_cast<int32_t *>(d->tcmem + o_ctr);
   d->tc_err = d->dev_err;
   (void)o_err;
@@ -1478,6 +1495,7 @@ int dory_create(const dory_config *cfg, const dory_weights *w, void *stream, dor
     if (e && e[0] == '0') ok = false;
     d->mega_ok = ok && mega_supported(dm.hd, d->sms);
     if (const char *pe = getenv("DORY_MEGA_PREFETCH")) d->mega_prefetch = std::max(0, atoi(pe));
+    if (const char *pe = getenv("DORY_MEGA_LEAD")) d->mega_lead = std::max(0, atoi(pe));
     if (const char *pe = getenv("DORY_MEGA_INFLIGHT")) d->mega_inflight = std::max(0, atoi(pe));
     const char *tp = getenv("DORY_MEGA_TRACE");
     if (d->mega_ok && tp && tp[0]) {

@@ -317,36 +317,49 @@ __global__ void __launch_bounds__(CT_THREADS, 1)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  // operands into shared memory, split into bf16 halves
-  constexpr int NC = HD / 4;
-  for (int i = tid; i < CT_Q * NC; i += CT_THREADS) {
-    const int q = i / NC, c = i % NC, rq = r_first + q / REP, hq = q % REP;
-    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (rq < T) x = *reinterpret_cast<const float4 *>(qkvg + (size_t)rq * ldq + (size_t)(kh * REP + hq) * HD + c * 4);
+  // operands into shared memory, split into bf16 halves; loads go out UL at a time per thread
+  // (one L2 round trip for UL float4s instead of one each)
+  constexpr int NC = HD / 4, UL = 8;
+  auto put = [&](uint32_t hoff, uint32_t loff, uint32_t o, const float4 &x) {
     __nv_bfloat16 hv[4], lv[4];
     ct_split(x.x, hv[0], lv[0]);
     ct_split(x.y, hv[1], lv[1]);
     ct_split(x.z, hv[2], lv[2]);
     ct_split(x.w, hv[3], lv[3]);
-    const uint32_t o = ct_off(q, c * 4, CT_Q);
-    *reinterpret_cast<uint2 *>(sm + L::QH + o) = *reinterpret_cast<const uint2 *>(hv);
-    *reinterpret_cast<uint2 *>(sm + L::QL + o) = *reinterpret_cast<const uint2 *>(lv);
+    *reinterpret_cast<uint2 *>(sm + hoff + o) = *reinterpret_cast<const uint2 *>(hv);
+    *reinterpret_cast<uint2 *>(sm + loff + o) = *reinterpret_cast<const uint2 *>(lv);
+  };
+  static_assert((CT_Q * NC) % (CT_THREADS * UL) == 0 && (CK_KEYS * NC) % (CT_THREADS * UL) == 0, "whole rounds");
+  for (int i0 = tid; i0 < CT_Q * NC; i0 += CT_THREADS * UL) {
+    float4 x[UL];
+#pragma unroll
+    for (int u = 0; u < UL; u++) {
+      const int i = i0 + u * CT_THREADS, q = i / NC, c = i % NC, rq = r_first + q / REP, hq = q % REP;
+      x[u] = rq < T ? *reinterpret_cast<const float4 *>(qkvg + (size_t)rq * ldq + (size_t)(kh * REP + hq) * HD + c * 4)
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < UL; u++) {
+      const int i = i0 + u * CT_THREADS, q = i / NC, c = i % NC;
+      put(L::QH, L::QL, ct_off(q, c * 4, CT_Q), x[u]);
+    }
   }
   const float4 *kg = reinterpret_cast<const float4 *>(slot + ring.L.k) + ((size_t)kh * ring.cap + rr0) * NC;
   const float4 *vg = reinterpret_cast<const float4 *>(slot + ring.L.v) + ((size_t)kh * ring.cap + rr0) * NC;
   float *vf = reinterpret_cast<float *>(sm + L::VF);
-  for (int i = tid; i < CK_KEYS * NC; i += CT_THREADS) {
-    const int j = i / NC, c = i % NC;
-    const float4 x = kg[i];
-    __nv_bfloat16 hv[4], lv[4];
-    ct_split(x.x, hv[0], lv[0]);
-    ct_split(x.y, hv[1], lv[1]);
-    ct_split(x.z, hv[2], lv[2]);
-    ct_split(x.w, hv[3], lv[3]);
-    const uint32_t o = ct_off(j, c * 4, CK_KEYS);
-    *reinterpret_cast<uint2 *>(sm + L::KH + o) = *reinterpret_cast<const uint2 *>(hv);
-    *reinterpret_cast<uint2 *>(sm + L::KL + o) = *reinterpret_cast<const uint2 *>(lv);
-    *reinterpret_cast<float4 *>(vf + (size_t)j * HD + c * 4) = vg[i];
+  for (int i0 = tid; i0 < CK_KEYS * NC; i0 += CT_THREADS * UL) {
+    float4 x[UL], y[UL];
+#pragma unroll
+    for (int u = 0; u < UL; u++) {
+      x[u] = kg[i0 + u * CT_THREADS];
+      y[u] = vg[i0 + u * CT_THREADS];
+    }
+#pragma unroll
+    for (int u = 0; u < UL; u++) {
+      const int i = i0 + u * CT_THREADS, j = i / NC, c = i % NC;
+      put(L::KH, L::KL, ct_off(j, c * 4, CK_KEYS), x[u]);
+      *reinterpret_cast<float4 *>(vf + (size_t)j * HD + c * 4) = y[u];
+    }
   }
   if (tid < CK_KEYS) tag[tid] = reinterpret_cast<const int32_t *>(slot + ring.L.tags)[rr0 + tid];
   __syncthreads();

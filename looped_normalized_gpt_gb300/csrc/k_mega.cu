@@ -182,9 +182,26 @@ __device__ void produce(const MegaArgs &a, uint8_t *ring, uint64_t *full, uint64
       pf.step(a);
     }
     const int sl = c % NS;
-    if (c >= NS && !mbar_wait(smem_addr(&empty[sl]), ((c / NS) - 1) & 1, &ctl.abort)) {
-      ok = false;
-      break;
+    if (c >= NS) {
+      // wait for the slot; while it is taken (the consumers are at attention or a barrier),
+      // keep HBM busy by asking L2 for the next weights, up to a longer lead
+      const uint32_t eb = smem_addr(&empty[sl]), par = ((c / NS) - 1) & 1;
+      uint32_t polls = 0;
+      bool free_ = false;
+      while (!(free_ = mbar_test(eb, par))) {
+        if (ctl.abort || ++polls > MBAR_WAIT_LIMIT) break;
+        if (pf.ok && ahead < a.stall_lead) {
+          const uint32_t pb = (uint32_t)pf.rows() * pf.K * 2;
+          prefetch_l2_bulk(pf.W + (size_t)pf.r0 * pf.K, pb);
+          if (pf.pair > 0) prefetch_l2_bulk(pf.W + (size_t)(pf.r0 + pf.pair) * pf.K, pb);
+          ahead += pf.pair > 0 ? 2 * pb : pb;
+          pf.step(a);
+        }
+      }
+      if (!free_) {
+        ok = false;
+        break;
+      }
     }
     // with a cap on copies in flight, the copy max_inflight back lands first: bytes queued
     // beyond what keeps HBM busy only delay the step's latency-bound loads

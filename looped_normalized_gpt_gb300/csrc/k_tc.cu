@@ -425,20 +425,25 @@ constexpr int BIG_B = BW * BK * 2;               // 32 KB
 constexpr int BIG_STAGE = BIG_A + BIG_B;         // 48 KB
 constexpr int BIG_SMEM = BIG_ST * BIG_STAGE + 1024;
 
+// With `splits` > 1 (blockIdx.z) the blocks of a tile take consecutive K ranges, store their
+// partial tiles to `ws` and count in on the tile's counter; the last one adds the partials
+// in split order (the same order whichever block finishes last), applies the epilogue,
+// and resets the counter.
 template <bool DUAL>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tcb_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, int N, int K,
                     int T, int t_base, long pair_rows, float *__restrict__ Y, int ldy, EpiArgs ep,
-                    int *__restrict__ err) {
+                    int *__restrict__ err, int splits, float *__restrict__ ws, int *__restrict__ ctr) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_full[BIG_ST], bar_empty[BIG_ST], bar_acc;
   __shared__ uint32_t tmem_base_sh;
-  __shared__ int failed;
+  __shared__ int failed, is_last;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int OUT = DUAL ? BW / 2 : BW;  // output columns of a tile
   const int n0 = blockIdx.x * OUT;         // first output column (SwiGLU: gate row)
   const int t0 = blockIdx.y * BT;
-  const int nk = K / BK;
+  const int kb_all = K / BK, split = blockIdx.z;
+  const int kb0 = (int)((long)kb_all * split / splits), nk = (int)((long)kb_all * (split + 1) / splits) - kb0;
   const uint32_t base = (smem_u32(smem_raw) + 1023) & ~1023u;
   auto a_addr = [&](int st) { return base + st * BIG_STAGE; };
   auto b_addr = [&](int st) { return base + st * BIG_STAGE + BIG_A; };
@@ -472,11 +477,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       for (int i = 0; i < pre; i++) {
         const uint32_t fb = smem_u32(&bar_full[i]);
         mbar_expect_tx(fb, BIG_STAGE);
-        tma_load_2d(b_addr(i), &tmW, i * BK, w_lo, fb);
-        tma_load_2d(b_addr(i) + BIG_B / 2, &tmW, i * BK, w_hi, fb);
+        tma_load_2d(b_addr(i), &tmW, (kb0 + i) * BK, w_lo, fb);
+        tma_load_2d(b_addr(i) + BIG_B / 2, &tmW, (kb0 + i) * BK, w_hi, fb);
       }
       pdl_wait();
-      for (int i = 0; i < pre; i++) tma_load_2d(a_addr(i), &tmX, i * BK, t_base + t0, smem_u32(&bar_full[i]));
+      for (int i = 0; i < pre; i++)
+        tma_load_2d(a_addr(i), &tmX, (kb0 + i) * BK, t_base + t0, smem_u32(&bar_full[i]));
       for (int i = pre; i < nk; i++) {
         const int st = i % BIG_ST;
         if (!mbar_wait(smem_u32(&bar_empty[st]), ((i / BIG_ST) - 1) & 1)) {
@@ -486,9 +492,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         const uint32_t fb = smem_u32(&bar_full[st]);
         mbar_expect_tx(fb, BIG_STAGE);
-        tma_load_2d(b_addr(st), &tmW, i * BK, w_lo, fb);
-        tma_load_2d(b_addr(st) + BIG_B / 2, &tmW, i * BK, w_hi, fb);
-        tma_load_2d(a_addr(st), &tmX, i * BK, t_base + t0, fb);
+        tma_load_2d(b_addr(st), &tmW, (kb0 + i) * BK, w_lo, fb);
+        tma_load_2d(b_addr(st) + BIG_B / 2, &tmW, (kb0 + i) * BK, w_hi, fb);
+        tma_load_2d(a_addr(st), &tmX, (kb0 + i) * BK, t_base + t0, fb);
       }
     }
   } else if (warp == 1) {
@@ -516,9 +522,38 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   }
   pdl_trigger();
 
+  const int q = warp & 3, m = q * 32 + lane;  // epilogue warps: this lane's row of the tile
+  const int t = t0 + m;                        // and its step row
+  const int mode = ep.mode;
+  // the epilogue of 16 columns of this lane's row: v (and the up half u) to Y
+  auto emit16 = [&](int c0, const float *v, const float *u) {
+    if (t >= T) return;
+    float o[16];
+#pragma unroll
+    for (int j = 0; j < 16; j++) {
+      const int n = n0 + c0 + j;
+      const float a = v[j];
+      if (mode == EPI_SCALE) {
+        o[j] = n < N ? a * __ldg(ep.vec + n) : 0.f;
+      } else if (mode == EPI_SILU) {
+        const float g = a * (n < N ? __ldg(ep.vec + n) : 0.f);
+        o[j] = g * sigmoidf_(g) * (u[j] * (n < N ? __ldg(ep.vec2 + n) : 0.f));
+      } else {
+        o[j] = a;
+      }
+    }
+    float *yrow = Y + (size_t)t * ldy + n0 + c0;
+    if (n0 + c0 + 16 <= N) {
+#pragma unroll
+      for (int j = 0; j < 16; j += 4) *reinterpret_cast<float4 *>(yrow + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; j++)
+        if (n0 + c0 + j < N) yrow[j] = o[j];
+    }
+  };
+  const size_t tile = (size_t)blockIdx.y * gridDim.x + blockIdx.x;
   if (warp >= 2) {
-    const int q = warp & 3;
-    const int t = t0 + q * 32 + lane;  // this lane's step row
     bool ok = mbar_wait(smem_u32(&bar_acc), 0);
     if (!ok) {
       atomicExch(err, 13);
@@ -527,38 +562,56 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     fence_after();
     if (ok && !failed) {
       const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
-      const int mode = ep.mode;
       for (int c0 = 0; c0 < OUT; c0 += 16) {
         uint32_t v[16], u[16];
         tmem_ld16_async(lane_base + c0, v);
         if (DUAL) tmem_ld16_async(lane_base + BW / 2 + c0, u);
         tmem_wait();
-        if (t >= T) continue;
-        float o[16];
+        if (splits == 1) {
+          emit16(c0, reinterpret_cast<const float *>(v), reinterpret_cast<const float *>(u));
+        } else {  // this split's partial sums of the row to the workspace
+          float *w = ws + ((tile * splits + split) * BT + m) * BW;
 #pragma unroll
-        for (int j = 0; j < 16; j++) {
-          const int n = n0 + c0 + j;
-          const float a = __uint_as_float(v[j]);
-          if (mode == EPI_SCALE) {
-            o[j] = n < N ? a * __ldg(ep.vec + n) : 0.f;
-          } else if (mode == EPI_SILU) {
-            const float g = a * (n < N ? __ldg(ep.vec + n) : 0.f);
-            o[j] = g * sigmoidf_(g) * (__uint_as_float(u[j]) * (n < N ? __ldg(ep.vec2 + n) : 0.f));
-          } else {
-            o[j] = a;
+          for (int j = 0; j < 16; j += 4) {
+            *reinterpret_cast<float4 *>(w + c0 + j) = make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                                                                  __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
+            if (DUAL)
+              *reinterpret_cast<float4 *>(w + BW / 2 + c0 + j) =
+                  make_float4(__uint_as_float(u[j]), __uint_as_float(u[j + 1]), __uint_as_float(u[j + 2]),
+                              __uint_as_float(u[j + 3]));
           }
         }
-        float *yrow = Y + (size_t)t * ldy + n0 + c0;
-        if (n0 + c0 + 16 <= N) {
+      }
+    }
+  }
+  if (splits > 1) {
+    __threadfence();  // this block's partials before its count
+    __syncthreads();
+    if (threadIdx.x == 64) is_last = atomicAdd(ctr + tile, 1) == splits - 1;
+    __syncthreads();
+    if (is_last) {
+      __threadfence();
+      if (warp >= 2 && !failed) {
+        for (int c0 = 0; c0 < OUT; c0 += 16) {
+          float v[16], u[16];
 #pragma unroll
-          for (int j = 0; j < 16; j += 4)
-            *reinterpret_cast<float4 *>(yrow + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
-        } else {
+          for (int j = 0; j < 16; j++) v[j] = u[j] = 0.f;
+          for (int sp = 0; sp < splits; sp++) {
+            const float *w = ws + ((tile * splits + sp) * BT + m) * BW;
 #pragma unroll
-          for (int j = 0; j < 16; j++)
-            if (n0 + c0 + j < N) yrow[j] = o[j];
+            for (int j = 0; j < 16; j += 4) {
+              const float4 a = __ldcg(reinterpret_cast<const float4 *>(w + c0 + j));
+              v[j] += a.x, v[j + 1] += a.y, v[j + 2] += a.z, v[j + 3] += a.w;
+              if (DUAL) {
+                const float4 b = __ldcg(reinterpret_cast<const float4 *>(w + BW / 2 + c0 + j));
+                u[j] += b.x, u[j + 1] += b.y, u[j + 2] += b.z, u[j + 3] += b.w;
+              }
+            }
+          }
+          emit16(c0, v, u);
         }
       }
+      if (threadIdx.x == 64) ctr[tile] = 0;  // ready for the next launch
     }
   }
   fence_before();
@@ -579,8 +632,15 @@ cudaError_t tcb_launch(const TcGemm &g, int T, int t_base, float *Y, int ldy, Ep
     attr = true;
   }
   constexpr int OUT = DUAL ? BW / 2 : BW;
+  const int gx = (g.N + OUT - 1) / OUT, gy = (T + BT - 1) / BT, tiles = gx * gy;
+  // K splits until the tiles fill the SMs: at most 4, at least 8 K blocks each, and no more
+  // partial tiles than the workspace holds (2 per SM)
+  int splits = 1;
+  while (splits < 4 && tiles * splits < g.sms && (g.K / BK) / (2 * splits) >= 8 &&
+         tiles * 2 * splits <= 2 * g.sms && tiles <= g.ctr_slots && g.ws_big)
+    splits *= 2;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((g.N + OUT - 1) / OUT, (T + BT - 1) / BT);
+  cfg.gridDim = dim3(gx, gy, splits);
   cfg.blockDim = dim3(TC_THREADS);
   cfg.dynamicSmemBytes = BIG_SMEM;
   cfg.stream = s;
@@ -589,7 +649,8 @@ cudaError_t tcb_launch(const TcGemm &g, int T, int t_base, float *Y, int ldy, Ep
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kern, g.tmW, g.tmXh, g.N, g.K, T, t_base, g.pair_rows, Y, ldy, ep, g.err);
+  return cudaLaunchKernelEx(&cfg, kern, g.tmW, g.tmXh, g.N, g.K, T, t_base, g.pair_rows, Y, ldy, ep, g.err, splits,
+                            g.ws_big, g.ctr_big);
 }
 
 // DORY_TC_TRIGGER=late: let the next kernel launch only once this one's epilogue is done

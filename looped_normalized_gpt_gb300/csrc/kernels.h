@@ -172,6 +172,11 @@ struct TcGemm {
   int *ctr;                 // per-tile arrival counters (zero between launches)
   int *err;                 // set when a bounded wait expires
   unsigned long long *trace;  // null, or [grid.y][grid.x][TC_TRACE_EVENTS] %globaltimer stamps
+  // launch_tc_gemm_big's split K: 2 * sms partial tiles of 128 x 256 floats, and ctr_slots
+  // per-tile counters (zero between launches)
+  float *ws_big = nullptr;
+  int *ctr_big = nullptr;
+  int ctr_slots = 0, sms = 0;
 };
 constexpr int TC_TRACE_EVENTS = 12;
 
@@ -246,6 +251,7 @@ struct MegaArgs {
   int adv_seq, adv_cnt;
   unsigned long long *trace;  // null, or [nstages][grid][MEGA_TRACE_EVENTS] %globaltimer stamps
   int prefetch_ahead;         // bytes per block the producer asks L2 for ahead of its copies
+  int stall_lead;             // ... and up to this many while its slots are all taken
   int max_inflight;           // weight copies a block keeps in flight at most (0: one per free slot)
 };
 

@@ -87,9 +87,12 @@ def test_batched_prefill_equals_one_sequence_at_a_time():
         b.close()
 
 
-def test_batched_prefill_argument_errors():
+def test_batched_prefill_argument_errors(monkeypatch):
+    """A repeated sequence, more rows than a step holds (64 here: whole-prompt block steps are
+    off, max_batch 64), a sequence past max_seqs, a chunk of 65 rows: all DORY_EINVAL."""
     from looped_normalized_gpt_gb300 import DoryError
 
+    monkeypatch.setenv("DORY_PREFILL_ROWS", "0")
     cfg = synth.small(max_batch=64, max_seqs=3)
     P = Pair(cfg, 2403)
     try:
