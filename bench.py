@@ -130,11 +130,32 @@ def profile_case(args):
         w = synth.weights(synth.dory2b(), SEED)
         out = bench_batch(Dory, torch, w, int(os.environ.get("LOCAL_RANK", "0")), steps=4)
         return {"case": "batch64", **out, "note": "profiling case, not a bench line"}
-    if args.profile_case == "context":  # the two long-context batch lines alone
+    if args.profile_case == "context-small":
+        # the long-context lines on fewer sequences (a few GB on the device), the timed decode
+        # steps inside an NVTX range "decode" (ncu --nvtx --nvtx-include decode/)
         w = synth.weights(synth.dory2b(), SEED)
         dev = int(os.environ.get("LOCAL_RANK", "0"))
-        return {"case": "context", "per_loop_batch16": bench_per_loop16(Dory, torch, w, dev),
-                "q8_batch64": bench_q8_batch64(Dory, torch, w, dev), "note": "profiling case, not a bench line"}
+        # (6 and 8 rows: the steps of 5+ rows of the bench lines, tensor-core projections)
+        pl = synth.dory2b(rec_kinds="S*S*", kv_mode="per_loop", max_loops=8, loops=8, full_window=8192,
+                          max_batch=6, max_seqs=6, max_context=8192 + 64)
+        q8 = synth.dory2b(rec_kinds="S*S*", kv_mode="last_loop", kv_quant="q8_2f", loops=16, max_loops=16,
+                          full_window=8192, max_batch=8, max_seqs=8, max_context=8192 + 64)
+        return {"case": "context-small",
+                "per_loop_batch6": bench_context_decode(Dory, torch, w, dev, pl, 6, 8192, [2, 4, 8, 4], 1, SEED + 1,
+                                                        nvtx=True),
+                "q8_batch8": bench_context_decode(Dory, torch, w, dev, q8, 8, 8192, [16, 16], 1, SEED + 3, nvtx=True),
+                "note": "profiling case, not a bench line"}
+    if args.profile_case in ("context-per-loop", "context-q8"):  # one long-context batch line alone
+        w = synth.weights(synth.dory2b(), SEED)
+        dev = int(os.environ.get("LOCAL_RANK", "0"))
+        fn = bench_per_loop16 if args.profile_case == "context-per-loop" else bench_q8_batch64
+        return {"case": args.profile_case, "line": fn(Dory, torch, w, dev, nvtx=True),
+                "note": "profiling case, not a bench line"}
+    if args.profile_case == "context":  # the two long-context batch lines alone (timed steps in NVTX "decode")
+        w = synth.weights(synth.dory2b(), SEED)
+        dev = int(os.environ.get("LOCAL_RANK", "0"))
+        return {"case": "context", "per_loop_batch16": bench_per_loop16(Dory, torch, w, dev, nvtx=True),
+                "q8_batch64": bench_q8_batch64(Dory, torch, w, dev, nvtx=True), "note": "profiling case, not a bench line"}
     if args.profile_case in ("prefill", "prefill-whole"):
         cfg = synth.dory2b(max_batch=1, max_seqs=1, max_context=args.prompt + 64, prompt_loops=2)
         g = Dory(cfg, synth.weights(cfg, SEED))
@@ -267,7 +288,8 @@ def bench_ours(args, rank, world):
     return out, g, cfg, w
 
 
-def bench_context_decode(g_cls, torch, w, dev, cfg, nseq: int, ctx: int, sched, warmup: int, seed: int):
+def bench_context_decode(g_cls, torch, w, dev, cfg, nseq: int, ctx: int, sched, warmup: int, seed: int,
+                         nvtx: bool = False):
     """Batch decode at a long synthetic context: `nseq` sequences with `ctx` unit-norm K/V rows
     in every slot (drawn on the GPU, written through the append path, so q8 rings quantise
     and freeze as in a forward), then len(sched) timed steps, step i at sched[i] loops. The
@@ -297,6 +319,8 @@ def bench_context_decode(g_cls, torch, w, dev, cfg, nseq: int, ctx: int, sched, 
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         b = 0
+        if nvtx:
+            torch.cuda.nvtx.range_push("decode")
         e0.record(stream)
         for i in range(steps):
             j = warmup + i
@@ -304,6 +328,9 @@ def bench_context_decode(g_cls, torch, w, dev, cfg, nseq: int, ctx: int, sched, 
             st = g.stats()
             b += st["weight_bytes"] + st["kv_read_bytes"] + st["kv_write_bytes"]
         e1.record(stream)
+        if nvtx:
+            torch.cuda.synchronize()
+            torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize()
         s_total = e0.elapsed_time(e1) / 1e3
         hbm, _, _ = peaks()
@@ -316,20 +343,20 @@ def bench_context_decode(g_cls, torch, w, dev, cfg, nseq: int, ctx: int, sched, 
         g.close()
 
 
-def bench_per_loop16(g_cls, torch, w, dev, steps: int = 16, warmup: int = 3):
+def bench_per_loop16(g_cls, torch, w, dev, steps: int = 16, warmup: int = 3, nvtx: bool = False):
     """per_loop KV, batch 16 at context 8192, every second recurrent attention layer full
     (full_window 8192), loops drawn per step from {2, 4, 8}."""
     cfg = synth.dory2b(rec_kinds="S*S*", kv_mode="per_loop", max_loops=8, loops=8, full_window=8192,
                        max_batch=16, max_seqs=16, max_context=8192 + steps + warmup + 64)
     return bench_context_decode(g_cls, torch, w, dev, cfg, 16, 8192, synth.loop_schedule(SEED + 1, steps), warmup,
-                                SEED + 1)
+                                SEED + 1, nvtx=nvtx)
 
 
-def bench_q8_batch64(g_cls, torch, w, dev, steps: int = 8, warmup: int = 3):
+def bench_q8_batch64(g_cls, torch, w, dev, steps: int = 8, warmup: int = 3, nvtx: bool = False):
     """q8_2f KV (last_loop), batch 64 at context 8192, loops 16, full layers capped at 8192."""
     cfg = synth.dory2b(rec_kinds="S*S*", kv_mode="last_loop", kv_quant="q8_2f", loops=16, max_loops=16,
                        full_window=8192, max_batch=64, max_seqs=64, max_context=8192 + steps + warmup + 64)
-    return bench_context_decode(g_cls, torch, w, dev, cfg, 64, 8192, [16] * steps, warmup, SEED + 3)
+    return bench_context_decode(g_cls, torch, w, dev, cfg, 64, 8192, [16] * steps, warmup, SEED + 3, nvtx=nvtx)
 
 
 def bench_batch(g_cls, torch, w, dev, batch: int = 64, ctx: int = 1024, steps: int = 16, warmup: int = 3):
@@ -479,7 +506,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the batch-64 decode and prefill lines")
     ap.add_argument("--prompt", type=int, default=PROMPT, help="prompt tokens before the decode steps")
-    ap.add_argument("--profile-case", choices=["decode-3pass", "prefill", "prefill-whole", "batch64", "context"],
+    ap.add_argument("--profile-case", choices=["decode-3pass", "prefill", "prefill-whole", "batch64", "context",
+                                               "context-small", "context-per-loop", "context-q8"],
                     help="run a small case for ncu captures instead of the bench")
     args = ap.parse_args()
     if args.profile_case:

@@ -44,6 +44,10 @@ extern "C" {
 #define DORY_ECUDA (-3)  /* a CUDA call failed; the handle should be destroyed */
 #define DORY_ESTATE (-4) /* the call does not fit the sequence's state (e.g. pos0) */
 #define DORY_ERANGE (-5) /* a position past what the rings can hold */
+#define DORY_EWAIT (-6)  /* a kernel gave up a bounded wait (the message has its code): the rows
+                          * of the steps since the last reported status are undefined; reset
+                          * those sequences, the handle itself stays usable. Reported once, by
+                          * the next call that synchronises (dory_logits, the read hooks). */
 
 /* KV modes (dory.rs, enum KvMode): per_loop keeps one slot per loop for the
  * recurrent attention layers; last_loop keeps one slot per attention layer and
@@ -221,7 +225,8 @@ int dory_decode_conf(dory_t *d, const int32_t *id, int32_t seq, float th, int32_
  * logits = (H h) * logit_scale per vocabulary row, dory.rs fn head) to dst, which has room
  * for `cap` floats. Decode: row = batch index. Prefill: want last gives row 0 only (the
  * chunk's last row, Want::Last), want all rows 0..n-1 (Want::All).
- * Errors: DORY_EINVAL (row, cap < vocab), DORY_ESTATE (no logits yet). */
+ * Errors: DORY_EINVAL (row, cap < vocab), DORY_ESTATE (no logits yet), DORY_EWAIT (a kernel
+ * of the steps since the last check gave up a bounded wait), DORY_ECUDA. */
 int dory_logits(dory_t *d, int32_t row, float *dst, size_t cap);
 
 /* Device address of the logits buffer [rows][vocab] of the last call (no copy). */
@@ -232,7 +237,8 @@ const char *dory_last_error(void);
 
 /* ---- inspection and test hooks (same library, same rules) ---------------------------- */
 
-/* Final hidden states of the last forward call, [rows][hidden] f32, before the head. */
+/* Final hidden states of the last forward call, [rows][hidden] f32, before the head.
+ * Errors: DORY_EINVAL, DORY_EWAIT (as dory_logits), DORY_ECUDA. */
 int dory_read_hidden(dory_t *d, float *dst, size_t cap);
 
 /* Geometry of attention layer `ordinal`'s rings: rows per ring, loop slots, and whether

@@ -545,7 +545,11 @@ int issue_step(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_splits, cud
         z_normed = true;
       } else if (!q8 && (dm.hd == 64 || dm.hd == 128) && !getenv_off("DORY_STREAM_ATTN")) {
         // rows of separate sequences: each (row, kv head) streams its own window
-        CK(launch_attention_stream(d->qkvg, ldq, dm, rows_l, ring, L.sg, d->z, d->dev_err, s));
+        int ssp = attn_stream_splits(wmax, Tr, dm.nk, d->sms);
+        if (getenv_off("DORY_STREAM_SPLIT")) ssp = 1;
+        ssp = std::min(ssp, d->max_splits);
+        CK(launch_attention_stream(d->qkvg, ldq, dm, rows_l, ring, L.sg, d->z, d->dev_err, ssp, d->part, d->actr,
+                                   s));
         nl += 1;
       } else if (d->kv_tma || d->kv_tma_q8) {
         const int tsp = fixed_splits ? attn_tma_splits(wmax) : tma_splits(d, a, ring);
@@ -980,6 +984,10 @@ int issue_mega(dory_t *d, const StepArgs &a, int32_t *rt, const MegaStage *stage
   m.trace = (size_t)nstages <= d->mega_trace_stages ? d->mega_trace : nullptr;
   m.prefetch_ahead = d->mega_prefetch;
   m.stall_lead = std::max(d->mega_prefetch, d->mega_lead);
+  // DORY_MEGA_SPIN: polls of a grid counter before a block gives up (read at every launch
+  // that is not a graph replay, so that a test can make one wait run out)
+  m.spin_limit = 1u << 22;
+  if (const char *e = getenv("DORY_MEGA_SPIN")) m.spin_limit = (uint32_t)std::max(1, atoi(e));
   m.max_inflight = d->mega_inflight;
   CK(launch_mega_decode(m, d->sms, s));
   return DORY_OK;
@@ -1216,12 +1224,17 @@ int setup_tc(dory_t *d) {
   return DORY_OK;
 }
 
-// A bounded wait in a tensor-core GEMM expired during the last calls.
+// A bounded wait of a kernel ran out during the calls since the last check: reported once
+// (the flag is cleared), the handle stays usable.
 int check_device_error(dory_t *d) {
   if (!d->dev_err) return DORY_OK;
   int32_t e = 0;
   CK(cudaMemcpy(&e, d->dev_err, 4, cudaMemcpyDeviceToHost));
-  if (e) return fail(DORY_ECUDA, "a kernel gave up waiting for its copies or MMAs (code %d)", e);
+  if (e) {
+    CK(cudaMemset(d->dev_err, 0, 4));
+    return fail(DORY_EWAIT, "a kernel gave up a bounded wait (code %d): the rows of the steps since the last "
+                            "check are undefined; reset their sequences", e);
+  }
   return DORY_OK;
 }
 

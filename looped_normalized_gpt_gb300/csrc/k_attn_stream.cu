@@ -15,6 +15,12 @@
 // stage refills it with the tile three ahead, so no warp waits to issue copies. The output
 // y / l is gated, y * sigmoid(g * s_g^2), into z; the row norm follows in its own kernel.
 // Waits are bounded; on expiry the block sets error 7, lets its copies land and returns.
+// A long window is split over `splits` blocks of consecutive tiles (flash-decoding style)
+// when the (row, kv head) blocks alone would leave SMs idle: each block leaves its merged
+// softmax state (max, sum, value sums per head) in `part`, and the last block of a (row, kv
+// head) to finish (a counter in `ctr`, reset by that block) merges the splits in split order
+// and applies the gate.
+#include <algorithm>
 #include <climits>
 
 #include "async.cuh"
@@ -74,7 +80,8 @@ __device__ __forceinline__ float transpose_sum(float (&v)[NV], int lane) {
 template <int HD, int REP, int AS_WARPS>
 __global__ void __launch_bounds__(AS_WARPS * 32) attn_stream_kernel(const float *__restrict__ qkvg, int ldq, Dims d,
                                                                     Rows rows, Ring ring, const float *__restrict__ sg,
-                                                                    float *__restrict__ z, int *err) {
+                                                                    float *__restrict__ z, int *err, int splits,
+                                                                    float *__restrict__ part, int *__restrict__ ctr) {
   constexpr int AS_KW = AS_KEYS / AS_WARPS;                   // positions per warp per tile
   constexpr int DPL = HD / 32;                                // dims per lane
   constexpr int NV = REP * AS_KW < 32 ? REP * AS_KW : 32;     // partial scores reduced together
@@ -86,15 +93,18 @@ __global__ void __launch_bounds__(AS_WARPS * 32) attn_stream_kernel(const float 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u);  // stays a shared-space pointer
   __shared__ __align__(8) uint64_t full[AS_STAGES];
-  __shared__ int done[AS_STAGES], hi;
+  __shared__ int done[AS_STAGES], hi, last;
   __shared__ volatile int stop;
-  const int r = blockIdx.x / d.nk, kh = blockIdx.x % d.nk;
+  const int rk = blockIdx.x / splits, sp = blockIdx.x % splits;  // (row, kv head), split
+  const int r = rk / d.nk, kh = rk % d.nk;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int seq = rows.seq[r];
   const long p = (long)rows.seq_pos[seq] + rows.off[r];
   const long lo = ring.window == INT_MAX ? 0 : (p + 1 - ring.window > 0 ? p + 1 - ring.window : 0);
-  const long t0 = lo / AS_KEYS;
-  const int ntiles = (int)(p / AS_KEYS - t0 + 1);
+  const int nt_all = (int)(p / AS_KEYS - lo / AS_KEYS + 1);
+  const int tb = (int)((long)nt_all * sp / splits);               // this split's first tile
+  const long t0 = lo / AS_KEYS + tb;
+  const int ntiles = (int)((long)nt_all * (sp + 1) / splits) - tb;  // and its tile count (maybe 0)
   const char *slot = ring.base + (size_t)seq * ring.seq_stride + ring.off;
   const char *kbase = slot + ring.L.k + (size_t)kh * ring.cap * HD * 4;
   const char *vbase = slot + ring.L.v + (size_t)kh * ring.cap * HD * 4;
@@ -251,6 +261,9 @@ __global__ void __launch_bounds__(AS_WARPS * 32) attn_stream_kernel(const float 
     for (int i = 0; i < DPL; i++) as[(warp * REP + h) * HD + lane * DPL + i] = acc[h][i];
   __syncthreads();
   const float *g = qkvg + (size_t)r * ldq + (size_t)(d.nh + 2 * d.nk) * HD;
+  // a split's state: [REP] max, [REP] sum, [REP][HD] value sums
+  constexpr int PS = REP * (HD + 2);
+  float *mine = part + ((size_t)rk * splits + sp) * PS;
   for (int o = threadIdx.x; o < REP * HD; o += blockDim.x) {
     const int h = o / HD, dd = o % HD;
     float M = -INFINITY;
@@ -266,36 +279,81 @@ __global__ void __launch_bounds__(AS_WARPS * 32) attn_stream_kernel(const float 
       den += f * ls[w * REP + h];
     }
     const int col = (kh * REP + h) * HD + dd;
+    if (splits == 1) {
+      z[(size_t)r * d.nh * HD + col] = (den > 0.f ? num / den : 0.f) * sigmoidf_(g[col] * sg[col]);
+    } else {
+      mine[2 * REP + h * HD + dd] = num;
+      if (dd == 0) {
+        mine[h] = M;
+        mine[REP + h] = den;
+      }
+    }
+  }
+  if (splits == 1) return;
+  __threadfence();  // this split's state before its count
+  __syncthreads();
+  if (threadIdx.x == 0) last = atomicAdd(ctr + rk, 1) == splits - 1;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  const float *all = part + (size_t)rk * splits * PS;
+  for (int o = threadIdx.x; o < REP * HD; o += blockDim.x) {
+    const int h = o / HD, dd = o % HD;
+    float M = -INFINITY;
+    for (int k = 0; k < splits; k++) M = fmaxf(M, __ldcg(all + (size_t)k * PS + h));
+    float num = 0.f, den = 0.f;
+    for (int k = 0; k < splits; k++) {  // in split order
+      const float mk = __ldcg(all + (size_t)k * PS + h);
+      if (mk == -INFINITY) continue;
+      const float f = expf(mk - M);
+      num += f * __ldcg(all + (size_t)k * PS + 2 * REP + h * HD + dd);
+      den += f * __ldcg(all + (size_t)k * PS + REP + h);
+    }
+    const int col = (kh * REP + h) * HD + dd;
     z[(size_t)r * d.nh * HD + col] = (den > 0.f ? num / den : 0.f) * sigmoidf_(g[col] * sg[col]);
   }
+  if (threadIdx.x == 0) ctr[rk] = 0;  // ready for the next launch
 }
 
 template <int HD, int REP, int W>
 cudaError_t stream_w(const float *qkvg, int ldq, Dims d, Rows rows, Ring ring, const float *sg, float *z, int *err,
-                     cudaStream_t s) {
+                     int splits, float *part, int *ctr, cudaStream_t s) {
   using S = StreamSmem<HD>;
   static bool attr = false;
   if (!attr) {
     cudaFuncSetAttribute(attn_stream_kernel<HD, REP, W>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::TOTAL);
     attr = true;
   }
-  attn_stream_kernel<HD, REP, W><<<rows.n * d.nk, W * 32, S::TOTAL, s>>>(qkvg, ldq, d, rows, ring, sg, z, err);
+  attn_stream_kernel<HD, REP, W><<<rows.n * d.nk * splits, W * 32, S::TOTAL, s>>>(qkvg, ldq, d, rows, ring, sg, z,
+                                                                                 err, splits, part, ctr);
   return cudaGetLastError();
 }
 
 template <int HD, int REP>
 cudaError_t stream_t(const float *qkvg, int ldq, Dims d, Rows rows, Ring ring, const float *sg, float *z, int *err,
-                     cudaStream_t s) {
-  return stream_w<HD, REP, AS_WARPS_USED>(qkvg, ldq, d, rows, ring, sg, z, err, s);
+                     int splits, float *part, int *ctr, cudaStream_t s) {
+  return stream_w<HD, REP, AS_WARPS_USED>(qkvg, ldq, d, rows, ring, sg, z, err, splits, part, ctr, s);
 }
 
 }  // namespace
 
+int attn_stream_splits(long window_keys, int rows, int nk, int sms) {
+  // only when the (row, kv head) blocks leave SMs idle (at batch 64 x 4 kv heads a split
+  // measured slower: 2.22 -> 2.46 ms a step); then blocks for two per SM (the kernel's stages
+  // take under half an SM's shared memory), at least 4 tiles (128 positions) a split
+  if ((long)rows * nk >= sms) return 1;
+  const long tiles = (window_keys + AS_KEYS - 1) / AS_KEYS + 1;
+  const long want = (2L * sms + (long)rows * nk - 1) / ((long)rows * nk);
+  const long most = tiles / 4;
+  return (int)std::max(1L, std::min(want, std::min(most, 64L)));
+}
+
 cudaError_t launch_attention_stream(const float *qkvg, int ldq, Dims d, Rows rows, Ring ring, const float *sg,
-                                    float *z, int *err, cudaStream_t s) {
+                                    float *z, int *err, int splits, float *part, int *ctr, cudaStream_t s) {
   const int rep = d.nh / d.nk;
+  if (splits < 1 || (splits > 1 && (!part || !ctr))) return cudaErrorInvalidValue;
 #define STREAM(H, R) \
-  if (d.hd == H && rep == R) return stream_t<H, R>(qkvg, ldq, d, rows, ring, sg, z, err, s);
+  if (d.hd == H && rep == R) return stream_t<H, R>(qkvg, ldq, d, rows, ring, sg, z, err, splits, part, ctr, s);
   STREAM(64, 1) STREAM(64, 2) STREAM(64, 4) STREAM(64, 8)
   STREAM(128, 1) STREAM(128, 2) STREAM(128, 4) STREAM(128, 8)
 #undef STREAM

@@ -50,7 +50,6 @@ static_assert(RMAX <= MW, "a chunk holds at most one row of each consumer warp")
 constexpr int EPI_ROWS = 256;                     // a block's rows of one GEMV at most
 constexpr uint32_t WORK = 32 * 1024;              // input row, or attention tiles and merge scratch
 constexpr int AK = MEGA_AK;                       // positions per attention item
-constexpr uint32_t SPIN_LIMIT = 1u << 22;         // polls of a global counter
 constexpr int ERR_MEGA = 6;                       // dev_err: a wait of the persistent kernel ran out
 static_assert(sizeof(MegaStage) % 4 == 0 && sizeof(MegaStage) / 4 < 32 * MW, "stage copy by the team");
 
@@ -104,12 +103,13 @@ __device__ __forceinline__ bool team_ok(const WarpTeam &tm, Ctl &ctl) {
 }
 
 // Wait until `*ctr >= target` (blocks past a stage, or RoPE entries written).
-__device__ bool team_wait_counter(const WarpTeam &tm, const int *ctr, int target, Ctl &ctl, int *err) {
+__device__ bool team_wait_counter(const WarpTeam &tm, const int *ctr, int target, Ctl &ctl, int *err,
+                                  uint32_t limit) {
   if (tm.tid() == 0) {
     uint32_t i = 0;
     while (ld_acquire_gpu(ctr) < target) {
       if (ctl.abort) break;
-      if (++i > SPIN_LIMIT) {
+      if (++i > limit) {
         flag_error(ctl, err);
         break;
       }
@@ -689,7 +689,7 @@ __global__ void __launch_bounds__(MTHREADS, 1) mega_decode_kernel(const __grid_c
   for (int s = 0; s < a.nstages && ok; s++) {
     tr.mark(s, 0);
     copy_stage(tm, a.stages + s, &sst);
-    if (!team_wait_counter(tm, a.sync, s * G, ctl, a.err)) {
+    if (!team_wait_counter(tm, a.sync, s * G, ctl, a.err, a.spin_limit)) {
       ok = false;
       break;
     }
@@ -700,7 +700,7 @@ __global__ void __launch_bounds__(MTHREADS, 1) mega_decode_kernel(const __grid_c
       ok = gemv_stage(tm, a, sst, s, c, ring, full, empty, work, epi, ctl);
     } else {
       if (!rope_ready) {
-        if (!team_wait_counter(tm, a.sync + 1, HD, ctl, a.err)) {
+        if (!team_wait_counter(tm, a.sync + 1, HD, ctl, a.err, a.spin_limit)) {
           ok = false;
           break;
         }

@@ -633,11 +633,11 @@ cudaError_t tcb_launch(const TcGemm &g, int T, int t_base, float *Y, int ldy, Ep
   }
   constexpr int OUT = DUAL ? BW / 2 : BW;
   const int gx = (g.N + OUT - 1) / OUT, gy = (T + BT - 1) / BT, tiles = gx * gy;
-  // K splits until the tiles fill the SMs: at most 4, at least 8 K blocks each, and no more
-  // partial tiles than the workspace holds (2 per SM)
+  // K splits while the blocks still fit one wave (one block per SM: a second wave of a few
+  // blocks would double the time): at most 4, at least 8 K blocks each
   int splits = 1;
-  while (splits < 4 && tiles * splits < g.sms && (g.K / BK) / (2 * splits) >= 8 &&
-         tiles * 2 * splits <= 2 * g.sms && tiles <= g.ctr_slots && g.ws_big)
+  while (splits < 4 && tiles * 2 * splits <= g.sms && (g.K / BK) / (2 * splits) >= 8 && tiles <= g.ctr_slots &&
+         g.ws_big)
     splits *= 2;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(gx, gy, splits);

@@ -100,10 +100,13 @@ int attn_chunk_blocks(long window_keys, int rows);
 cudaError_t launch_attention_chunk(const float *qkvg, int ldq, Dims d, Rows rows, Ring ring, int nkb, float *part,
                                    const float *sg, float *z, Emit em, int *err, cudaStream_t s);
 
-// Rows of any sequences (a batched decode step) over f32 rings, hd 64 or 128: one block per
-// (row, kv head) streams the window in 32-position tiles; writes z gated (not row-normalised).
+// Rows of any sequences (a batched decode step) over f32 rings, hd 64 or 128: `splits` blocks
+// per (row, kv head) stream consecutive parts of the window in 32-position tiles; writes z
+// gated (not row-normalised). splits > 1: part holds rows * nk * splits * REP * (hd + 2)
+// floats, ctr rows * nk counters (zero between launches). attn_stream_splits picks splits.
+int attn_stream_splits(long window_keys, int rows, int nk, int sms);
 cudaError_t launch_attention_stream(const float *qkvg, int ldq, Dims d, Rows rows, Ring ring, const float *sg,
-                                    float *z, int *err, cudaStream_t s);
+                                    float *z, int *err, int splits, float *part, int *ctr, cudaStream_t s);
 
 cudaError_t launch_rownorm(float *x, int T, int width, int ld, Emit em, cudaStream_t s);
 
@@ -252,6 +255,7 @@ struct MegaArgs {
   unsigned long long *trace;  // null, or [nstages][grid][MEGA_TRACE_EVENTS] %globaltimer stamps
   int prefetch_ahead;         // bytes per block the producer asks L2 for ahead of its copies
   int stall_lead;             // ... and up to this many while its slots are all taken
+  uint32_t spin_limit;        // polls of a grid counter before a block gives up (error 6)
   int max_inflight;           // weight copies a block keeps in flight at most (0: one per free slot)
 };
 

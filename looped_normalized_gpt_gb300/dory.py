@@ -14,7 +14,7 @@ from . import build as _build
 
 c_int32_p = ctypes.POINTER(ctypes.c_int32)
 
-OK, EINVAL, ENOMEM, ECUDA, ESTATE, ERANGE = 0, -1, -2, -3, -4, -5
+OK, EINVAL, ENOMEM, ECUDA, ESTATE, ERANGE, EWAIT = 0, -1, -2, -3, -4, -5, -6
 KV_PER_LOOP, KV_LAST_LOOP = 0, 1
 KV_F32, KV_Q8_2F = 0, 1
 W_F32, W_BF16 = 0, 1

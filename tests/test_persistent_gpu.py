@@ -108,3 +108,39 @@ def test_group_sizes_prefill_chunks_and_decode(nh, nk, hd):
         P.check_rings(0, 1e-5)
     finally:
         P.close()
+
+
+def test_a_wait_that_runs_out_is_reported_and_the_handle_recovers(monkeypatch):
+    """The persistent kernel's grid-barrier wait bounded to one poll (DORY_MEGA_SPIN, read at
+    each launch when steps are not graph replays): a block gives up at its first barrier, the
+    kernel stops and returns, and the next synchronising call reports DORY_EWAIT with code 6
+    once. With the limit back, the sequence reset and its prompt run again, the same handle
+    matches the oracle."""
+    from looped_normalized_gpt_gb300 import DoryError
+    from oracle import dory_oracle as O
+
+    monkeypatch.setenv("DORY_GRAPHS", "0")
+    cfg = synth.small(kv_mode="last_loop", rec_kinds="S*", full_window=0, loops=2, max_loops=2, max_context=1024)
+    P = Pair(cfg, 3006)
+    try:
+        ids = synth.token_ids(3006, 0, 48, cfg.vocab)
+        P.prefill(0, ids[:40], 2, "last")
+        P.decode([0], [int(ids[40])], 2)
+        monkeypatch.setenv("DORY_MEGA_SPIN", "1")
+        P.gpu.decode_step([int(ids[41])], [0], 2)
+        assert P.gpu.stats()["launches"] == 1
+        with pytest.raises(DoryError) as e:
+            P.gpu.logits(0)
+        assert e.value.code == -6 and "code 6" in str(e.value)
+        monkeypatch.delenv("DORY_MEGA_SPIN")
+        P.gpu.reset(0)
+        P.states[0] = O.SeqState()
+        P.max_hidden_err = 0.0
+        P.prefill(0, ids[:40], 2, "last")
+        for i in ids[40:44]:
+            P.decode([0], [int(i)], 2)
+            assert P.gpu.stats()["launches"] == 1
+        assert P.max_hidden_err <= 1e-4, P.max_hidden_err
+        assert all(P.top1[-5:])
+    finally:
+        P.close()
