@@ -543,7 +543,8 @@ int issue_step(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_splits, cud
           nl += 2;
         }
         z_normed = true;
-      } else if (!q8 && (dm.hd == 64 || dm.hd == 128) && !getenv_off("DORY_STREAM_ATTN")) {
+      } else if ((q8 ? dm.hd == 128 && !getenv_off("DORY_STREAM_Q8") : (dm.hd == 64 || dm.hd == 128)) &&
+                 !getenv_off("DORY_STREAM_ATTN")) {
         // rows of separate sequences: each (row, kv head) streams its own window
         int ssp = attn_stream_splits(wmax, Tr, dm.nk, d->sms);
         if (getenv_off("DORY_STREAM_SPLIT")) ssp = 1;

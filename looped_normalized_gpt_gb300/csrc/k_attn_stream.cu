@@ -35,14 +35,22 @@ constexpr int AS_KEYS = 32;                   // positions per tile
 // warps per block: 8 (4 positions a warp per tile) measured 2.8% faster per batch-64 step
 // than 4 (8 positions a warp): twice the warps in flight at the same shared memory
 constexpr int AS_WARPS_USED = 8;
-constexpr int AS_STAGES = 3;
+constexpr int AS_STAGES_F32 = 3;
+// q8 tiles are a quarter of the bytes: 8 stages keep about as much in flight per block
+constexpr int AS_STAGES_Q8 = 8;
 constexpr int ERR_STREAM = 7;
 
-template <int HD>
+// A stage: K and V rows of a tile (f32, or q8_2f int8 codes), for q8 the K group scales
+// [AS_KEYS][HD/32] and V scales [AS_KEYS], then the position tags.
+template <int HD, bool Q8 = false>
 struct StreamSmem {
-  static constexpr int TILE = AS_KEYS * HD * 4;              // bytes of K (or V) per tile
-  static constexpr int STAGE = 2 * TILE + AS_KEYS * 4;       // K, V, tags
-  static constexpr int TOTAL = AS_STAGES * STAGE + 128;      // + alignment slack
+  static constexpr int ST = Q8 ? AS_STAGES_Q8 : AS_STAGES_F32;  // stages
+  static constexpr int TILE = AS_KEYS * HD * (Q8 ? 1 : 4);   // bytes of K (or V) per tile
+  static constexpr int KS = Q8 ? AS_KEYS * (HD / 32) * 4 : 0;
+  static constexpr int VS = Q8 ? AS_KEYS * 4 : 0;
+  static constexpr int TAGS = 2 * TILE + KS + VS;             // offset of the tags
+  static constexpr int STAGE = TAGS + AS_KEYS * 4;
+  static constexpr int TOTAL = ST * STAGE + 128;             // + alignment slack
 };
 
 template <int DPL>
@@ -77,7 +85,9 @@ __device__ __forceinline__ float transpose_sum(float (&v)[NV], int lane) {
   return s;
 }
 
-template <int HD, int REP, int AS_WARPS>
+// Q8: q8_2f rings (kv_cache.rs fn attend_group_upto): scores scale * sum_g ks[g] <q * kcol,
+// kq>_g, values (sum_j p_j vs_j vq_j) * vcol, the fields applied once the slot has frozen.
+template <int HD, int REP, int AS_WARPS, bool Q8 = false>
 __global__ void __launch_bounds__(AS_WARPS * 32) attn_stream_kernel(const float *__restrict__ qkvg, int ldq, Dims d,
                                                                     Rows rows, Ring ring, const float *__restrict__ sg,
                                                                     float *__restrict__ z, int *err, int splits,
@@ -89,7 +99,9 @@ __global__ void __launch_bounds__(AS_WARPS * 32) attn_stream_kernel(const float 
   constexpr int HC = NV / AS_KW;                              // heads per chunk
   constexpr int LPI = 32 / NV;                                // lanes holding one reduced score
   constexpr int GRP = AS_KW * LPI;                            // lanes holding one head's scores
-  using S = StreamSmem<HD>;
+  using S = StreamSmem<HD, Q8>;
+  constexpr int AS_STAGES = S::ST;
+  static_assert(!Q8 || HD == 128, "q8 rows: one 32-bit word of codes per lane");
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u);  // stays a shared-space pointer
   __shared__ __align__(8) uint64_t full[AS_STAGES];
@@ -106,18 +118,26 @@ __global__ void __launch_bounds__(AS_WARPS * 32) attn_stream_kernel(const float 
   const long t0 = lo / AS_KEYS + tb;
   const int ntiles = (int)((long)nt_all * (sp + 1) / splits) - tb;  // and its tile count (maybe 0)
   const char *slot = ring.base + (size_t)seq * ring.seq_stride + ring.off;
-  const char *kbase = slot + ring.L.k + (size_t)kh * ring.cap * HD * 4;
-  const char *vbase = slot + ring.L.v + (size_t)kh * ring.cap * HD * 4;
+  constexpr int EB = Q8 ? 1 : 4;  // bytes per stored element
+  const char *kbase = slot + (Q8 ? ring.L.kq : ring.L.k) + (size_t)kh * ring.cap * HD * EB;
+  const char *vbase = slot + (Q8 ? ring.L.vq : ring.L.v) + (size_t)kh * ring.cap * HD * EB;
+  const char *ksbase = slot + ring.L.ks + (size_t)kh * ring.cap * (HD / 32) * 4;
+  const char *vsbase = slot + ring.L.vs + (size_t)kh * ring.cap * 4;
   const char *tbase = slot + ring.L.tags;
+  const bool frozen = Q8 && reinterpret_cast<const int32_t *>(slot + ring.L.meta)[kh * 4 + 1] != 0;
 
   auto issue = [&](int t) {  // tile t into stage t % AS_STAGES
     const int s = t % AS_STAGES;
     const int rr = (int)(((t0 + t) * AS_KEYS) % ring.cap);
     const uint32_t bar = smem_addr(&full[s]), dst = smem_addr(base + (size_t)s * S::STAGE);
     mbar_expect_tx(bar, S::STAGE);
-    bulk_g2s(dst, kbase + (size_t)rr * HD * 4, S::TILE, bar);
-    bulk_g2s(dst + S::TILE, vbase + (size_t)rr * HD * 4, S::TILE, bar);
-    bulk_g2s(dst + 2 * S::TILE, tbase + (size_t)rr * 4, AS_KEYS * 4, bar);
+    bulk_g2s(dst, kbase + (size_t)rr * HD * EB, S::TILE, bar);
+    bulk_g2s(dst + S::TILE, vbase + (size_t)rr * HD * EB, S::TILE, bar);
+    if constexpr (Q8) {
+      bulk_g2s(dst + 2 * S::TILE, ksbase + (size_t)rr * (HD / 32) * 4, S::KS, bar);
+      bulk_g2s(dst + 2 * S::TILE + S::KS, vsbase + (size_t)rr * 4, S::VS, bar);
+    }
+    bulk_g2s(dst + S::TAGS, tbase + (size_t)rr * 4, AS_KEYS * 4, bar);
   };
   if (threadIdx.x == 0) {
     for (int s = 0; s < AS_STAGES; s++) {
@@ -129,15 +149,23 @@ __global__ void __launch_bounds__(AS_WARPS * 32) attn_stream_kernel(const float 
     hi = ntiles < AS_STAGES ? ntiles : AS_STAGES;
     for (int t = 0; t < hi; t++) issue(t);
   }
-  // this kv head's query heads, pre-scaled by 1/sqrt(hd); lane l holds dims l*DPL ..
+  // this kv head's query heads, pre-scaled by 1/sqrt(hd) (q8: and by the frozen K field);
+  // lane l holds dims l*DPL ..
   const float scale = 1.f / sqrtf((float)HD);
+  float kc[DPL], vc[DPL];
+#pragma unroll
+  for (int i = 0; i < DPL; i++) kc[i] = vc[i] = 1.f;
+  if (frozen) {
+    ld_vec<DPL>(reinterpret_cast<const float *>(slot + ring.L.kcol) + (size_t)kh * HD + lane * DPL, kc);
+    ld_vec<DPL>(reinterpret_cast<const float *>(slot + ring.L.vcol) + (size_t)kh * HD + lane * DPL, vc);
+  }
   float q[REP][DPL];
 #pragma unroll
   for (int h = 0; h < REP; h++) {
     float t[DPL];
     ld_vec<DPL>(qkvg + (size_t)r * ldq + (size_t)(kh * REP + h) * HD + lane * DPL, t);
 #pragma unroll
-    for (int i = 0; i < DPL; i++) q[h][i] = t[i] * scale;
+    for (int i = 0; i < DPL; i++) q[h][i] = t[i] * kc[i] * scale;
   }
   __syncthreads();
 
@@ -159,9 +187,14 @@ __global__ void __launch_bounds__(AS_WARPS * 32) attn_stream_kernel(const float 
       }
       break;
     }
-    const float *Kt = reinterpret_cast<const float *>(base + (size_t)s * S::STAGE) + warp * AS_KW * HD;
+    const uint8_t *st_base = base + (size_t)s * S::STAGE;
+    const float *Kt = reinterpret_cast<const float *>(st_base) + warp * AS_KW * HD;
     const float *Vt = Kt + AS_KEYS * HD;
-    const int32_t *tags = reinterpret_cast<const int32_t *>(base + (size_t)s * S::STAGE + 2 * S::TILE);
+    const int8_t *Kq = reinterpret_cast<const int8_t *>(st_base) + warp * AS_KW * HD;
+    const int8_t *Vq = reinterpret_cast<const int8_t *>(st_base + S::TILE) + warp * AS_KW * HD;
+    const float *Ks = reinterpret_cast<const float *>(st_base + 2 * S::TILE) + warp * AS_KW * (HD / 32);
+    const float *Vs = reinterpret_cast<const float *>(st_base + 2 * S::TILE + S::KS) + warp * AS_KW;
+    const int32_t *tags = reinterpret_cast<const int32_t *>(st_base + S::TAGS);
     const int j = warp * AS_KW + own_k;
     const long pe = (t0 + t) * AS_KEYS + j;
     const bool valid = pe >= lo && pe <= p && tags[j] == (int32_t)pe;
@@ -172,14 +205,22 @@ __global__ void __launch_bounds__(AS_WARPS * 32) attn_stream_kernel(const float 
 #pragma unroll
       for (int k = 0; k < AS_KW; k++) {
         float kv[DPL];
-        ld_vec<DPL>(Kt + k * HD + lane * DPL, kv);
+        float gsc = 1.f;  // q8: the K scale of this lane's 32-channel group
+        if constexpr (Q8) {
+          const int w4 = *reinterpret_cast<const int *>(Kq + k * HD + lane * 4);
+#pragma unroll
+          for (int i = 0; i < 4; i++) kv[i] = (float)(int8_t)(w4 >> (8 * i));
+          gsc = Ks[k * (HD / 32) + lane / 8];
+        } else {
+          ld_vec<DPL>(Kt + k * HD + lane * DPL, kv);
+        }
 #pragma unroll
         for (int hc = 0; hc < HC; hc++) {
           float2 s2 = make_float2(0.f, 0.f);
 #pragma unroll
           for (int i = 0; i < DPL; i += 2)
             s2 = ffma2(make_float2(q[c * HC + hc][i], q[c * HC + hc][i + 1]), make_float2(kv[i], kv[i + 1]), s2);
-          part[hc * AS_KW + k] = s2.x + s2.y;
+          part[hc * AS_KW + k] = (s2.x + s2.y) * gsc;
         }
       }
       float sc = transpose_sum<NV>(part, lane);
@@ -213,7 +254,14 @@ __global__ void __launch_bounds__(AS_WARPS * 32) attn_stream_kernel(const float 
 #pragma unroll
     for (int k = 0; k < AS_KW; k++) {
       float vv[DPL];
-      ld_vec<DPL>(Vt + k * HD + lane * DPL, vv);
+      if constexpr (Q8) {  // codes times the row's V scale
+        const int w4 = *reinterpret_cast<const int *>(Vq + k * HD + lane * 4);
+        const float vsk = Vs[k];
+#pragma unroll
+        for (int i = 0; i < 4; i++) vv[i] = (float)(int8_t)(w4 >> (8 * i)) * vsk;
+      } else {
+        ld_vec<DPL>(Vt + k * HD + lane * DPL, vv);
+      }
 #pragma unroll
       for (int c = 0; c < NCH; c++)
 #pragma unroll
@@ -247,6 +295,12 @@ __global__ void __launch_bounds__(AS_WARPS * 32) attn_stream_kernel(const float 
   __syncthreads();
   if (stop) return;
 
+  // q8: the frozen V field scales every value sum
+  if (frozen)
+#pragma unroll
+    for (int h = 0; h < REP; h++)
+#pragma unroll
+      for (int i = 0; i < DPL; i++) acc[h][i] *= vc[i];
   // merge the warps' softmax states: m, l per (warp, head), then the value sums
   float *ms = reinterpret_cast<float *>(base), *ls = ms + AS_WARPS * REP, *as = ls + AS_WARPS * REP;
   if (lane == 0)
@@ -315,16 +369,19 @@ __global__ void __launch_bounds__(AS_WARPS * 32) attn_stream_kernel(const float 
   if (threadIdx.x == 0) ctr[rk] = 0;  // ready for the next launch
 }
 
-template <int HD, int REP, int W>
+template <int HD, int REP, int W, bool Q8>
 cudaError_t stream_w(const float *qkvg, int ldq, Dims d, Rows rows, Ring ring, const float *sg, float *z, int *err,
                      int splits, float *part, int *ctr, cudaStream_t s) {
-  using S = StreamSmem<HD>;
+  using S = StreamSmem<HD, Q8>;
+  // the stages, or the warps' merge scratch after them (m, l and value sums per warp and head)
+  constexpr int MERGE = (2 * W * REP + W * REP * HD) * 4 + 128;
+  constexpr int SMEM = S::TOTAL > MERGE ? S::TOTAL : MERGE;
   static bool attr = false;
   if (!attr) {
-    cudaFuncSetAttribute(attn_stream_kernel<HD, REP, W>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::TOTAL);
+    cudaFuncSetAttribute(attn_stream_kernel<HD, REP, W, Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     attr = true;
   }
-  attn_stream_kernel<HD, REP, W><<<rows.n * d.nk * splits, W * 32, S::TOTAL, s>>>(qkvg, ldq, d, rows, ring, sg, z,
+  attn_stream_kernel<HD, REP, W, Q8><<<rows.n * d.nk * splits, W * 32, SMEM, s>>>(qkvg, ldq, d, rows, ring, sg, z,
                                                                                  err, splits, part, ctr);
   return cudaGetLastError();
 }
@@ -332,7 +389,10 @@ cudaError_t stream_w(const float *qkvg, int ldq, Dims d, Rows rows, Ring ring, c
 template <int HD, int REP>
 cudaError_t stream_t(const float *qkvg, int ldq, Dims d, Rows rows, Ring ring, const float *sg, float *z, int *err,
                      int splits, float *part, int *ctr, cudaStream_t s) {
-  return stream_w<HD, REP, AS_WARPS_USED>(qkvg, ldq, d, rows, ring, sg, z, err, splits, part, ctr, s);
+  if constexpr (HD == 128)
+    if (ring.q8) return stream_w<HD, REP, AS_WARPS_USED, true>(qkvg, ldq, d, rows, ring, sg, z, err, splits, part, ctr, s);
+  if (ring.q8) return cudaErrorInvalidValue;
+  return stream_w<HD, REP, AS_WARPS_USED, false>(qkvg, ldq, d, rows, ring, sg, z, err, splits, part, ctr, s);
 }
 
 }  // namespace

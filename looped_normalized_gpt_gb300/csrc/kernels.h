@@ -100,7 +100,8 @@ int attn_chunk_blocks(long window_keys, int rows);
 cudaError_t launch_attention_chunk(const float *qkvg, int ldq, Dims d, Rows rows, Ring ring, int nkb, float *part,
                                    const float *sg, float *z, Emit em, int *err, cudaStream_t s);
 
-// Rows of any sequences (a batched decode step) over f32 rings, hd 64 or 128: `splits` blocks
+// Rows of any sequences (a batched decode step) over f32 rings (hd 64 or 128) or q8_2f rings
+// (hd 128): `splits` blocks
 // per (row, kv head) stream consecutive parts of the window in 32-position tiles; writes z
 // gated (not row-normalised). splits > 1: part holds rows * nk * splits * REP * (hd + 2)
 // floats, ctr rows * nk counters (zero between launches). attn_stream_splits picks splits.

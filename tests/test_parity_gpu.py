@@ -423,3 +423,28 @@ def test_a_bounded_step_cache_evicts_and_recaptures(monkeypatch):
         assert all(P.top1)
     finally:
         P.close()
+
+
+@pytest.mark.parametrize("kv_mode,nk", [("last_loop", 2), ("per_loop", 1)])
+def test_q8_batched_decode_streams_each_window(kv_mode, nk):
+    """q8_2f rings at hd 128 in a step of 6 rows: the streaming attention reads the codes, the
+    group and row scales, and (once a slot has frozen) the per-channel fields; contexts of 20
+    to 320 rows leave some slots open and freeze others, per_loop holes come from changing
+    loop counts; 4 and 8 query heads per kv head."""
+    cfg = synth.small(kv_quant="q8_2f", kv_mode=kv_mode, hd=128, nh=8, nk=nk, rec_kinds="S*", full_window=300,
+                      max_batch=6, max_seqs=6, max_loops=3, loops=3)
+    P = Pair(cfg, 2015)
+    try:
+        for s in range(6):
+            P.write_context(s, 20 + 60 * s, 2015 + s)
+        for step, loops in enumerate([3, 1, 2, 3]):
+            P.decode([4, 0, 5, 2, 1, 3], synth.token_ids(2015, 60 + step, 6, cfg.vocab), loops)
+        assert P.max_hidden_err <= tol_of(cfg), P.max_hidden_err
+        assert np.mean(P.top1) >= 0.99
+        for s in range(6):
+            for (ordn, sl), slot in P.states[s].slots.items():
+                got = P.gpu.read_kv_q8(s, ordn, sl)
+                assert np.array_equal(got["tags"].astype(np.int64), slot.ring_image(P.gpu.slot_info(ordn)[0]))
+                assert got["frozen"].tolist() == [int(slot.kcol is not None)] * cfg.nk
+    finally:
+        P.close()
