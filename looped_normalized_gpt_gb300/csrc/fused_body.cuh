@@ -13,8 +13,11 @@ namespace dory {
 // thread owns the float4 chunks tid + j * (team size) of a row (KC of them at most) and loads
 // all the vectors it needs for them at once, so a row costs one memory round trip; the
 // reductions pair up their sums. `lead`: this team stores the new hidden rows (and the
-// mix's input/state rows).
-template <int TT, int KC, typename Team>
+// mix's input/state rows). HALVES: each row goes to shared memory as two halves, float4
+// chunk c at (c & 1) * K / 8 + c / 2, so that a lane reading the 8 inputs of a 16-byte
+// weight column reads float4 u of each half: consecutive lanes, consecutive addresses
+// (the plain layout puts a lane's two float4 loads 32 bytes apart, two-way bank conflicts).
+template <int TT, int KC, typename Team, bool HALVES = false>
 __device__ void build_input(const Team &tm, const GemvIn &in, int T, int K, float *xs, bool lead) {
   __shared__ float red[2][TEAM_MAX_WARPS];
   const int tid = tm.tid(), nt = tm.size();
@@ -126,7 +129,7 @@ __device__ void build_input(const Team &tm, const GemvIn &in, int T, int K, floa
     for (int j = 0; j < KC; j++) {
       const int c = tid + j * nt;
       if (c < nch) {
-        reinterpret_cast<float4 *>(xs + (size_t)t * K)[c] = x[j];
+        reinterpret_cast<float4 *>(xs + (size_t)t * K)[HALVES ? (c & 1) * (nch / 2) + (c >> 1) : c] = x[j];
         if ((in.mode == IN_RESID || in.mode == IN_EMBED) && lead && in.h_dst)
           reinterpret_cast<float4 *>(in.h_dst + (size_t)t * K)[c] = x[j];
       }

@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(FW * 32, 2) gemv_fused_kernel(const WT *__rest
   }
   pdl_wait();
   pdl_trigger();
-  build_input<TT, KC>(BlockTeam{}, in, T, K, xs, blockIdx.x == 0);
+  build_input<TT, KC, BlockTeam, true>(BlockTeam{}, in, T, K, xs, blockIdx.x == 0);
 
   float acc0[TT], acc1[TT];
 #pragma unroll
@@ -91,8 +91,8 @@ __global__ void __launch_bounds__(FW * 32, 2) gemv_fused_kernel(const WT *__rest
 #pragma unroll
     for (int t = 0; t < TT; t++) {
       if (t < T) {
-        const float4 xa = *reinterpret_cast<const float4 *>(&xs[t * K + k]);
-        const float4 xb = *reinterpret_cast<const float4 *>(&xs[t * K + k + 4]);
+        const float4 xa = reinterpret_cast<const float4 *>(xs + t * K)[ci];  // halves layout
+        const float4 xb = reinterpret_cast<const float4 *>(xs + t * K)[K / 8 + ci];
         const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
 #pragma unroll
         for (int i = 0; i < 8; i++) {
@@ -434,7 +434,7 @@ __global__ void __launch_bounds__(FW * 32) gemv_stream_kernel(const __nv_bfloat1
   }
   pdl_wait();
   pdl_trigger();
-  build_input<TT, KC>(BlockTeam{}, in, T, K, xs, blockIdx.x == 0);  // ends with __syncthreads
+  build_input<TT, KC, BlockTeam, true>(BlockTeam{}, in, T, K, xs, blockIdx.x == 0);  // ends with __syncthreads
 
   for (int c = 0; c < nchunks; c++) {
     const int s = c % ST;
@@ -461,8 +461,8 @@ __global__ void __launch_bounds__(FW * 32) gemv_stream_kernel(const __nv_bfloat1
 #pragma unroll
         for (int t = 0; t < TT; t++) {
           if (t < T) {
-            const float4 xa = *reinterpret_cast<const float4 *>(&xs[t * K + k]);
-            const float4 xb = *reinterpret_cast<const float4 *>(&xs[t * K + k + 4]);
+            const float4 xa = reinterpret_cast<const float4 *>(xs + t * K)[k / 8];  // halves layout
+            const float4 xb = reinterpret_cast<const float4 *>(xs + t * K)[K / 8 + k / 8];
             const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
 #pragma unroll
             for (int i = 0; i < 8; i++) {

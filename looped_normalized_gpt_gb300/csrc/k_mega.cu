@@ -51,6 +51,7 @@ constexpr int EPI_ROWS = 256;                     // a block's rows of one GEMV 
 constexpr uint32_t WORK = 32 * 1024;              // input row, or attention tiles and merge scratch
 constexpr int AK = MEGA_AK;                       // positions per attention item
 constexpr int ERR_MEGA = 6;                       // dev_err: a wait of the persistent kernel ran out
+static_assert(EPI_ROWS == 32 * MW, "a consumer thread holds one row's epilogue scales");
 static_assert(sizeof(MegaStage) % 4 == 0 && sizeof(MegaStage) / 4 < 32 * MW, "stage copy by the team");
 
 struct Ctl {
@@ -238,8 +239,10 @@ __device__ void produce(const MegaArgs &a, uint8_t *ring, uint64_t *full, uint64
 // columns l, l + 32, ...) and multiply them with the input row, read from shared memory
 // (keeping a lane's part of the row in registers measured 2.5% slower: 64 registers held
 // across the stage), and a butterfly gives the row's sum, which lane 0 scales and stores
-// (summing 8 rows of a warp at once in one transpose reduction measured slower too). A
-// chunk holds at most one row of each warp (R <= MW).
+// (summing 8 rows of a warp at once in one transpose reduction measured slower too). The
+// input row is held as two halves (inputs 8u..8u+3 at float4 u of the first, 8u+4..8u+7 of
+// the second), so a warp's loads of it are conflict-free. A chunk holds at most one row of
+// each warp (R <= MW).
 // Every warp awaits every chunk of the stage and frees it with its own arrival (MW per
 // slot), so no team barrier runs inside the loop; since a warp frees a chunk only after it
 // has landed, its arrivals always fall in the slot's current phase.
@@ -254,7 +257,7 @@ __device__ void gemv_rows(const WarpTeam &tm, const MegaStage &st, int rb, int r
   auto dot8 = [&](const uint4 &wq, int u, float2 &a0, float2 &a1) {
     float wv[8];
     unpack8(wq, wv);
-    const float4 p = *reinterpret_cast<const float4 *>(xs + u * 8), q = *reinterpret_cast<const float4 *>(xs + u * 8 + 4);
+    const float4 p = reinterpret_cast<const float4 *>(xs)[u], q = reinterpret_cast<const float4 *>(xs)[nu + u];
     a0 = ffma2(make_float2(wv[0], wv[1]), make_float2(p.x, p.y), a0);
     a1 = ffma2(make_float2(wv[2], wv[3]), make_float2(p.z, p.w), a1);
     a0 = ffma2(make_float2(wv[4], wv[5]), make_float2(q.x, q.y), a0);
@@ -310,7 +313,7 @@ __device__ void gemv_rows(const WarpTeam &tm, const MegaStage &st, int rb, int r
 
 template <int KC>
 __device__ __forceinline__ void input_row(const WarpTeam &tm, const GemvIn &in, int K, float *xs) {
-  build_input<1, KC>(tm, in, 1, K, xs, blockIdx.x == 0);
+  build_input<1, KC, WarpTeam, true>(tm, in, 1, K, xs, blockIdx.x == 0);
 }
 
 // Returns false (team-uniformly) when the block has stopped.
@@ -324,17 +327,27 @@ __device__ __noinline__ bool gemv_stage(const WarpTeam &tm, const MegaArgs &a, c
   const int G = gridDim.x, b = blockIdx.x;
   const int N = st.N, K = st.K;
   const int rb = (int)((long)N * b / G), re = (int)((long)N * (b + 1) / G);
-  // the epilogue's per-row scales of this block's rows, in flight with the input loads
-  if (st.ep.mode != EPI_STORE)
-    for (int i = tm.tid(); i < re - rb; i += tm.size()) {
-      epi[0][i] = __ldg(st.ep.vec + rb + i);
-      if (st.ep.mode == EPI_SILU) epi[1][i] = __ldg(st.ep.vec2 + rb + i);
-    }
+  // the epilogue's per-row scales of this block's rows (re - rb <= EPI_ROWS = team size),
+  // held in registers while the input row's loads are in flight, stored to shared memory after
+  const int ei = tm.tid();
+  const bool has_e = st.ep.mode != EPI_STORE && ei < re - rb;
+  float e0 = 0.f, e1 = 0.f;
+  if (has_e) {
+    e0 = __ldg(st.ep.vec + rb + ei);
+    if (st.ep.mode == EPI_SILU) e1 = __ldg(st.ep.vec2 + rb + ei);
+  }
   const int kc = (K / 4 + tm.size() - 1) / tm.size();  // float4 chunks per thread
   if (kc <= 2) input_row<2>(tm, st.in, K, xs);
   else if (kc <= 4) input_row<4>(tm, st.in, K, xs);
   else if (kc <= 6) input_row<6>(tm, st.in, K, xs);
   else input_row<8>(tm, st.in, K, xs);
+  if (st.ep.mode != EPI_STORE) {
+    if (has_e) {
+      epi[0][ei] = e0;
+      epi[1][ei] = e1;
+    }
+    tm.sync();
+  }
   tr.mark(s, 2);
   if (st.pair > 0) gemv_rows<true>(tm, st, rb, re, c, ring, full, empty, xs, epi, ctl, a.err, tr, s);
   else gemv_rows<false>(tm, st, rb, re, c, ring, full, empty, xs, epi, ctl, a.err, tr, s);
