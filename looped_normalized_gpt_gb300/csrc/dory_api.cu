@@ -978,6 +978,7 @@ int issue_mega(dory_t *d, const StepArgs &a, int32_t *rt, const MegaStage *stage
   m.rope = d->rope;
   m.sync = d->mega_sync;
   m.actr = d->mega_sync + 64;
+  m.aflag = d->mega_sync + 64 + d->dims.nk;
   m.err = d->dev_err;
   m.seq_pos = d->d_seq_pos;
   m.adv_seq = a.aseq[0];
@@ -1459,7 +1460,7 @@ int dory_create(const dory_config *cfg, const dory_weights *w, void *stream, dor
                a_lg2 = areserve((size_t)T * dm.vocab * 4),
                a_sp = areserve((size_t)cfg->max_seqs * 4), a_rows = areserve((size_t)ROW_TABLE * T * 4),
                a_zero = areserve((size_t)cfg->max_seqs * 4), a_err = areserve(256);
-  const size_t ms_bytes = (size_t)(64 + dm.nk) * 4, a_ms = areserve(ms_bytes);
+  const size_t ms_bytes = (size_t)(64 + dm.nk + dm.nk * MEGA_FLAGS) * 4, a_ms = areserve(ms_bytes);
   const size_t a_stab = areserve((size_t)d->n_flat_slots * 3 * 8), a_drop = areserve((size_t)d->n_flat_slots * 4),
                a_top = areserve(4);
   if (cudaMalloc(&d->act, ab) != cudaSuccess) {

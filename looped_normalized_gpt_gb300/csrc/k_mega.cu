@@ -454,6 +454,93 @@ __device__ __forceinline__ void merge_items(const WarpTeam &tm, const MegaStage 
   }
 }
 
+// Merge the items of query head h (of kv head kh = h / rep) once every item of kh has
+// published its flag for this stage, and gate: warp 0 polls the flags (relaxed loads, then an
+// acquire fence; the team sync passes the order on), then thread t takes the 4 outputs
+// q = t mod HD/4 and the items g, g + G, ... (g = t / (HD/4), G = team size / (HD/4)), loads
+// them at once and folds them in item order with a running max; the groups meet in shared
+// memory and warp 0 finishes in group order: y = sum o e^(m - M) / sum l e^(m - M),
+// z = y * sigmoid(g * s_g^2). Returns false (team-uniformly) when the block has stopped.
+template <int HD>
+__device__ __noinline__ bool merge_head(const WarpTeam &tm, const MegaArgs &a, const MegaStage &st, const Dims &d,
+                                        int h, int nblk, int s, float *scr, Ctl &ctl) {
+  scr = in_shared(scr);
+  constexpr int NQ = HD / 4, IB = MEGA_FLAGS / (32 * MW / NQ);  // items a thread holds at most
+  const int rep = d.nh / d.nk, kh = h / rep, hh = h % rep;
+  const int groups = tm.size() / NQ;
+  const int t = tm.tid(), q = t % NQ, g = t / NQ, lane = threadIdx.x & 31;
+  const size_t c = (size_t)h * HD + (size_t)q * 4;
+  float4 gr = make_float4(0.f, 0.f, 0.f, 0.f), sg = gr;
+  if (g == 0) {  // the gate inputs, in flight while the items finish
+    gr = __ldcg(reinterpret_cast<const float4 *>(st.qkvg + (size_t)(d.nh + 2 * d.nk) * HD + c));
+    sg = __ldg(reinterpret_cast<const float4 *>(st.sg + c));
+  }
+  if (tm.warp() == 0) {
+    const int *fl = a.aflag + kh * MEGA_FLAGS;
+    uint32_t polls = 0;
+    while (!__all_sync(0xffffffffu, lane >= nblk || ld_relaxed_gpu(fl + lane) == s + 1)) {
+      if (ctl.abort) break;
+      if (++polls > a.spin_limit) {
+        if (lane == 0) flag_error(ctl, a.err);
+        break;
+      }
+    }
+    fence_acq_rel_gpu();
+  }
+  if (!team_ok(tm, ctl)) return false;
+  float4 o[IB];
+  float2 ml[IB];
+#pragma unroll
+  for (int u = 0; u < IB; u++) {
+    const int it = g + u * groups;
+    const bool in = it < nblk;
+    o[u] = in ? __ldcg(reinterpret_cast<const float4 *>(part_o(st, rep, HD, kh, it, hh) + q * 4))
+              : make_float4(0.f, 0.f, 0.f, 0.f);
+    ml[u] = in ? __ldcg(reinterpret_cast<const float2 *>(part_ml(st, d.nk, rep, HD, kh, it, hh)))
+               : make_float2(-INFINITY, 0.f);
+  }
+  float M = -INFINITY, L = 0.f;
+  float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int u = 0; u < IB; u++) {
+    if (ml[u].x == -INFINITY) continue;
+    const float nm = fmaxf(M, ml[u].x);
+    const float sa = M == -INFINITY ? 0.f : expf(M - nm), sb = expf(ml[u].x - nm);
+    L = L * sa + ml[u].y * sb;
+    A = make_float4(A.x * sa + o[u].x * sb, A.y * sa + o[u].y * sb, A.z * sa + o[u].z * sb, A.w * sa + o[u].w * sb);
+    M = nm;
+  }
+  float4 *Acc = reinterpret_cast<float4 *>(scr);  // [groups][NQ]
+  float *Ms = scr + 4 * groups * NQ, *Ls = Ms + groups * NQ;
+  Acc[g * NQ + q] = A;
+  Ms[g * NQ + q] = M;
+  Ls[g * NQ + q] = L;
+  tm.sync();
+  if (g == 0) {
+    float Mx = -INFINITY;
+    for (int k = 0; k < groups; k++) Mx = fmaxf(Mx, Ms[k * NQ + q]);
+    float Lx = 0.f;
+    float4 Ax = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (Mx != -INFINITY)
+      for (int k = 0; k < groups; k++) {
+        const float mk = Ms[k * NQ + q];
+        if (mk == -INFINITY) continue;
+        const float e = expf(mk - Mx);
+        const float4 ak = Acc[k * NQ + q];
+        Lx += Ls[k * NQ + q] * e;
+        Ax = make_float4(Ax.x + ak.x * e, Ax.y + ak.y * e, Ax.z + ak.z * e, Ax.w + ak.w * e);
+      }
+    const float inv = Lx > 0.f ? 1.f / Lx : 0.f;
+    float4 z;
+    z.x = Ax.x * inv * sigmoidf_(gr.x * sg.x);
+    z.y = Ax.y * inv * sigmoidf_(gr.y * sg.y);
+    z.z = Ax.z * inv * sigmoidf_(gr.z * sg.z);
+    z.w = Ax.w * inv * sigmoidf_(gr.w * sg.w);
+    *reinterpret_cast<float4 *>(st.z + c) = z;
+  }
+  return true;
+}
+
 // Warp-wide: query head h of kv head kh against the item's 32 keys (lane = key): scores,
 // the item's softmax statistics and its value sum, written as the item's partial.
 template <int HD>
@@ -528,6 +615,9 @@ __device__ __noinline__ bool attn_stage(const WarpTeam &tm, const MegaArgs &a, c
   const int cw = tm.warp(), lane = threadIdx.x & 31;
   const int kw = rep % MW;  // the warp that prepares the new key and value
   const float *rc = rope_s[st.rope_kind], *rsn = rope_s[st.rope_kind] + HALF;
+  // With a block for every item and one more for every query head, no block waits for an
+  // arrival counter: each item publishes a flag, and block items + h merges head h.
+  const bool per_head = items + d.nh <= (int)gridDim.x && nblk <= MEGA_FLAGS;
   for (int it = blockIdx.x; it < items; it += gridDim.x) {
     const int kh = it / nblk, blk = it % nblk;
     const long P0 = (blk0 + blk) * AK;
@@ -535,23 +625,28 @@ __device__ __noinline__ bool attn_stage(const WarpTeam &tm, const MegaArgs &a, c
     const bool has_p = P0 + AK > p;  // the item that holds the row's own position
     tm.sync();                       // the previous item's tiles and scratch are no longer read
     if (tm.tid() == 0) {
-      fence_proxy_async_global();  // ring rows written earlier in this launch
-      fence_proxy_async_smem();    // the input row, tiles and merge scratch written before
+      // Ring rows are not fenced for the async proxy: rows of earlier launches are ordered by
+      // the launch boundary, and the one row this launch writes (position p) is replaced in the
+      // tile by the item that holds it before anything reads it.
+      fence_proxy_async_smem();  // the input row, tiles and merge scratch written before
       const uint32_t bar = smem_addr(abar), bytes = AK * HD * 4;
       mbar_expect_tx(bar, 2 * bytes);
       bulk_g2s(smem_addr(Ks), Kg + ((size_t)kh * cap + rr0) * HD, bytes, bar);
       bulk_g2s(smem_addr(Vs), Vg + ((size_t)kh * cap + rr0) * HD, bytes, bar);
     }
+    tr.mark(s, 2);
     aph++;
     const int tg = __ldcg(tags + rr0 + lane);
     // the group's query heads: RoPE on the pairs (j, j + hd/2), justnorm, times s_q^2
     for (int h = cw; h < rep; h += MW) {
       const size_t off = (size_t)(kh * rep + h) * HD;
-      float x[PP], y[PP], ss = 0.f;
+      float x[PP], y[PP], sx[PP], sy[PP], ss = 0.f;
 #pragma unroll
-      for (int u = 0; u < PP; u++) {
+      for (int u = 0; u < PP; u++) {  // the projection and the s_q^2 entries in one round trip
         const int j = lane + 32 * u;
         const float a0 = __ldcg(qkvg + off + j), b0 = __ldcg(qkvg + off + j + HALF);
+        sx[u] = __ldg(st.sq + off + j);
+        sy[u] = __ldg(st.sq + off + j + HALF);
         x[u] = a0 * rc[j] - b0 * rsn[j];
         y[u] = b0 * rc[j] + a0 * rsn[j];
         ss += x[u] * x[u] + y[u] * y[u];
@@ -561,8 +656,8 @@ __device__ __noinline__ bool attn_stage(const WarpTeam &tm, const MegaArgs &a, c
 #pragma unroll
       for (int u = 0; u < PP; u++) {
         const int j = lane + 32 * u;
-        qs[h][j] = x[u] * inv * __ldg(st.sq + off + j);
-        qs[h][j + HALF] = y[u] * inv * __ldg(st.sq + off + j + HALF);
+        qs[h][j] = x[u] * inv * sx[u];
+        qs[h][j + HALF] = y[u] * inv * sy[u];
       }
     }
     // the new key (rotated, normalised) and value of kv head kh
@@ -588,12 +683,14 @@ __device__ __noinline__ bool attn_stage(const WarpTeam &tm, const MegaArgs &a, c
         ky[u] *= inv;
       }
     }
+    tr.mark(s, 3);
     long long t0 = tr.clk();
     const bool landed = mbar_wait(smem_addr(abar), (aph - 1) & 1, &ctl.abort);
     if (!landed && lane == 0) flag_error(ctl, a.err);
     if (!team_ok(tm, ctl)) return false;
     long long t1 = tr.clk();
     tr.add(s, 8, t1 - t0);
+    tr.mark(s, 5);
     if (has_p && cw == kw) {
       // into the tile (it holds the ring's older row there), and into the ring
       const int jp = (int)(p - P0), rr = (int)(p % cap);
@@ -611,7 +708,6 @@ __device__ __noinline__ bool attn_stage(const WarpTeam &tm, const MegaArgs &a, c
         vg[j + HALF] = vy[u];
       }
       if (kh == 0 && lane == 0) tags[rr] = (int32_t)p;
-      fence_proxy_async_global();  // later passes read this row with bulk copies
     }
     tm.sync();
     for (int h = cw; h < rep; h += MW) attn_head<HD>(st, d.nk, Ks, Vs, qs[h], tg, P0, lo, p, kh, blk, rep, h);
@@ -619,6 +715,12 @@ __device__ __noinline__ bool attn_stage(const WarpTeam &tm, const MegaArgs &a, c
     tm.sync();
     t0 = tr.clk();
     tr.add(s, 9, t0 - t1);
+    tr.mark(s, 6);
+    if (per_head) {
+      // the item's partials are stored (the team sync above): publish them to the head merges
+      if (tm.tid() == 0) st_release_gpu(a.aflag + kh * MEGA_FLAGS + blk, s + 1);
+      continue;
+    }
     if (tm.tid() == 0) {
       const int old = atom_add_acq_rel_gpu(a.actr + kh, 1);
       ctl.last = old == nblk - 1;
@@ -627,10 +729,16 @@ __device__ __noinline__ bool attn_stage(const WarpTeam &tm, const MegaArgs &a, c
     tm.sync();
     t1 = tr.clk();
     tr.add(s, 10, t1 - t0);
+    tr.mark(s, 7);
     if (ctl.last) {
       merge_items<HD>(tm, st, d, kh, nblk, Ks, tr);
       tr.add(s, 11, tr.clk() - t1);
     }
+  }
+  if (per_head && (int)blockIdx.x >= items && (int)blockIdx.x < items + d.nh) {
+    const long long tm0 = tr.clk();
+    if (!merge_head<HD>(tm, a, st, d, (int)blockIdx.x - items, nblk, s, work, ctl)) return false;
+    tr.add(s, 11, tr.clk() - tm0);
   }
   tr.flush(s);
   return true;

@@ -250,6 +250,7 @@ struct MegaArgs {
   float *rope;              // [2][hd] cos | sin of the row's position
   int *sync;                // [0] blocks past each stage, [1] RoPE entries ready; zero at launch
   int *actr;                // [nk] attention item arrivals; zero at launch
+  int *aflag;               // [nk][MEGA_FLAGS] attention items done (stage + 1); zero at launch
   int *err;
   int32_t *seq_pos;         // advanced by `adv` at the last stage
   int adv_seq, adv_cnt;
@@ -266,8 +267,12 @@ struct MegaArgs {
 // stage's first chunk has landed (consumers); 8..11 SM cycles the first consumer thread
 // spent over the stage's chunks waiting for a slot, reducing, at the team barrier, and in
 // the epilogue (attention stages: copy wait, compute, arrival, merge); 12, 13 cycles of
-// the attention merge until its partials are folded, and until its team sync.
+// the attention merge until its partials are folded, and until its team sync. Attention
+// stages reuse 2, 3, 5, 6, 7 for the block's last item: K/V copies issued, queries
+// prepared, tiles landed, scores and values done, arrival counted.
 constexpr int MEGA_TRACE_EVENTS = 14;
+// Attention items of one kv head that the persistent kernel's per-head merge waits for at most.
+constexpr int MEGA_FLAGS = 32;
 
 // Bytes of dynamic shared memory and whether the device runs the kernel (one block per SM,
 // cooperative launch).

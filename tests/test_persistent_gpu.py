@@ -9,9 +9,9 @@ from parity import Pair
 pytestmark = pytest.mark.gpu
 
 
-def _run(P, cfg, seed, steps):
+def _run(P, cfg, seed, steps, context=150):
     """Context in every slot, a prompt chunk, then `steps` batch-1 decode tokens."""
-    P.write_context(0, 150, seed)
+    P.write_context(0, context, seed)
     ids = synth.token_ids(seed, 1, 40 + steps, cfg.vocab)
     P.prefill(0, ids[:40], cfg.loops, "last")
     launches = []
@@ -21,19 +21,23 @@ def _run(P, cfg, seed, steps):
     return launches
 
 
-@pytest.mark.parametrize("kv_mode,hd,rec_kinds", [
-    ("last_loop", 64, "S*"),
-    ("per_loop", 64, "*S"),
-    ("last_loop", 128, "SS"),
-    ("per_loop", 128, "S*"),
+@pytest.mark.parametrize("kv_mode,hd,rec_kinds,context", [
+    ("last_loop", 64, "S*", 150),
+    ("per_loop", 64, "*S", 150),
+    ("last_loop", 128, "SS", 150),
+    ("per_loop", 128, "S*", 150),
+    # a full-window layer over more than 32 items of 32 positions per kv head: its items are
+    # merged by the last one to arrive instead of one block per query head
+    ("last_loop", 128, "S*", 1100),
+    ("per_loop", 64, "*S", 1100),
 ])
-def test_one_launch_per_token_matches_the_oracle(kv_mode, hd, rec_kinds):
+def test_one_launch_per_token_matches_the_oracle(kv_mode, hd, rec_kinds, context):
     nh, nk = (8, 2) if hd == 64 else (4, 1)
     cfg = synth.small(kv_mode=kv_mode, hd=hd, nh=nh, nk=nk, rec_kinds=rec_kinds, full_window=0, loops=3,
-                      max_loops=3, max_context=1024)
+                      max_loops=3, max_context=2048)
     P = Pair(cfg, 3001)
     try:
-        launches = _run(P, cfg, 3001, 6)
+        launches = _run(P, cfg, 3001, 6, context)
         assert launches == [1] * 6, launches  # the whole token in one kernel
         assert P.max_hidden_err <= 1e-4, P.max_hidden_err
         assert all(P.top1)
