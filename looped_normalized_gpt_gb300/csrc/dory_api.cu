@@ -1493,7 +1493,8 @@ int dory_create(const dory_config *cfg, const dory_weights *w, void *stream, dor
     CK(cudaDeviceGetAttribute(&d->sms, cudaDevAttrMultiProcessorCount, dev));
     const size_t kmax = std::max(std::max(dm.hidden, dm.ffn), q_size);
     bool ok = d->wdtype == W_BF16 && !q8 && (dm.hd == 64 || dm.hd == 128) && dm.hidden % 8 == 0 &&
-              dm.ffn % 8 == 0 && q_size % 8 == 0 && kmax <= mega_work_floats() &&
+              dm.ffn % 8 == 0 && q_size % 8 == 0 && kmax + mega_park_floats(false) <= mega_work_floats() &&
+              (size_t)dm.hidden + mega_park_floats(true) <= mega_work_floats() &&
               (size_t)2 * MEGA_AK * dm.hd <= mega_work_floats() && mega_chunk_rows(dm.hidden, true) >= 1 &&
               mega_chunk_rows((int)kmax, false) >= 1;
     // the merge's per-warp partials of a kv head's query heads

@@ -14,9 +14,9 @@
 //   * copy the stage's descriptor into shared memory while their first thread waits until
 //     every block has finished the stage before (a counter in global memory);
 //   * GEMV: build the input row in shared memory (the embedding, a row norm, or the nGPT
-//     residual with the loop mix), then take the rows a warp each (bf16 weights, f32 sums;
-//     lanes split the row into 16-byte columns, a butterfly sums them) and apply the
-//     epilogue (SwiGLU, logit scale) as each sum comes out;
+//     residual with the loop mix), then take the rows two at a time (or a gate/up pair) per
+//     warp (bf16 weights, f32 sums; lanes split the row into 16-byte columns), park the lane
+//     sums and reduce them 8 rows at a time, and apply the epilogue (SwiGLU, logit scale);
 //   * attention (dory.rs fn attn_layer), in items of 32 positions of one kv head: the K and
 //     V rows of an item are contiguous in the ring and arrive with two bulk copies; meanwhile
 //     warp h rotates and normalises query head h of the group from the raw projection row
@@ -234,30 +234,72 @@ __device__ void produce(const MegaArgs &a, uint8_t *ring, uint64_t *full, uint64
 
 // ---- GEMV stage ---------------------------------------------------------------------------
 
-// A stage's rows, a warp per row: warp w of the team takes the block's rows w, w + MW, ...
-// (pairs of gate and up rows, DUAL). Its lanes split a row into 16-byte columns (lane l:
-// columns l, l + 32, ...) and multiply them with the input row, read from shared memory
-// (keeping a lane's part of the row in registers measured 2.5% slower: 64 registers held
-// across the stage), and a butterfly gives the row's sum, which lane 0 scales and stores
-// (summing 8 rows of a warp at once in one transpose reduction measured slower too). The
-// input row is held as two halves (inputs 8u..8u+3 at float4 u of the first, 8u+4..8u+7 of
-// the second), so a warp's loads of it are conflict-free. A chunk holds at most one row of
-// each warp (R <= MW).
+// A stage's rows in groups of NR (two rows, or one gate/up pair, share each load of the
+// input row): group i of the block's rows goes to warp i mod MW; a chunk holds whole groups
+// and at most one group of each warp. The lanes split a row into 16-byte columns (lane l:
+// columns l, l + 32, ...) against the input row in shared memory, held as two halves
+// (inputs 8u..8u+3 at float4 u of the first, 8u+4..8u+7 of the second) so that the loads
+// are conflict-free. A row's 32 lane sums are not reduced at once: the warp parks them in
+// shared memory and reduces 8 rows together (lane 4i + q adds 8 of row i's sums, two
+// shuffles finish), so that no shuffle chain stands between one row's loads and the next.
+// Lane 4i then applies the epilogue (SwiGLU, logit scale) and stores.
 // Every warp awaits every chunk of the stage and frees it with its own arrival (MW per
 // slot), so no team barrier runs inside the loop; since a warp frees a chunk only after it
 // has landed, its arrivals always fall in the slot's current phase.
+constexpr int PEND = 8;  // rows a warp parks before it reduces them
+
 template <bool DUAL>
+__device__ __forceinline__ void flush_rows(const MegaStage &st, int rb, int np, const float *pg, const float *pu,
+                                           const int *prow, const float (*epi)[EPI_ROWS]) {
+  const int lane = threadIdx.x & 31, i = lane >> 2, q = lane & 3;
+  __syncwarp();
+  const float4 *g4 = reinterpret_cast<const float4 *>(pg + i * 32 + q * 8);
+  const float4 ga = g4[0], gb = g4[1];
+  float g = ((ga.x + ga.y) + (ga.z + ga.w)) + ((gb.x + gb.y) + (gb.z + gb.w)), u = 0.f;
+  if (DUAL) {
+    const float4 *u4 = reinterpret_cast<const float4 *>(pu + i * 32 + q * 8);
+    const float4 ua = u4[0], ub = u4[1];
+    u = ((ua.x + ua.y) + (ua.z + ua.w)) + ((ub.x + ub.y) + (ub.z + ub.w));
+  }
+  g += __shfl_xor_sync(0xffffffffu, g, 1);
+  g += __shfl_xor_sync(0xffffffffu, g, 2);
+  if (DUAL) {
+    u += __shfl_xor_sync(0xffffffffu, u, 1);
+    u += __shfl_xor_sync(0xffffffffu, u, 2);
+  }
+  if (q == 0 && i < np) {
+    const int jr = prow[i];
+    const int mode = st.ep.mode;
+    float y;
+    if (mode == EPI_SCALE) {
+      y = g * epi[0][jr];
+    } else if (mode == EPI_SILU) {
+      const float gs = g * epi[0][jr];
+      y = gs * sigmoidf_(gs) * (u * epi[1][jr]);
+    } else {
+      y = g;
+    }
+    st.Y[rb + jr] = y;
+  }
+  __syncwarp();  // the parked sums may be overwritten
+}
+
+template <bool DUAL, int NR>
 __device__ void gemv_rows(const WarpTeam &tm, const MegaStage &st, int rb, int re, int c0, const uint8_t *ring,
-                          uint64_t *full, uint64_t *empty, const float *xs, const float (*epi)[EPI_ROWS], Ctl &ctl,
-                          int *err, const Tracer &tr, int s) {
+                          uint64_t *full, uint64_t *empty, const float *xs, float *park, const float (*epi)[EPI_ROWS],
+                          Ctl &ctl, int *err, const Tracer &tr, int s) {
+  static_assert(!DUAL || NR == 1, "a gate/up pair is a group of its own");
   const int lane = threadIdx.x & 31, cw = tm.warp();
-  const int K = st.K, R = st.R, mode = st.ep.mode, nu = K / 8;  // 16-byte columns per row
-  float *__restrict__ Y = st.Y;
+  const int K = st.K, R = st.R, nu = K / 8;  // 16-byte columns per row
+  // this warp's parked lane sums [PEND][32] (gate, then up), and their rows
+  float *pg = park + cw * (DUAL ? 2 : 1) * PEND * 32, *pu = pg + PEND * 32;
+  __shared__ int prow_all[MW][PEND];
+  int *prow = prow_all[cw];
+  int np = 0;
   // a 16-byte column of weights against the input row: two chains of paired FMAs
-  auto dot8 = [&](const uint4 &wq, int u, float2 &a0, float2 &a1) {
+  auto dot8 = [&](const uint4 &wq, const float4 &p, const float4 &q, float2 &a0, float2 &a1) {
     float wv[8];
     unpack8(wq, wv);
-    const float4 p = reinterpret_cast<const float4 *>(xs)[u], q = reinterpret_cast<const float4 *>(xs)[nu + u];
     a0 = ffma2(make_float2(wv[0], wv[1]), make_float2(p.x, p.y), a0);
     a1 = ffma2(make_float2(wv[2], wv[3]), make_float2(p.z, p.w), a1);
     a0 = ffma2(make_float2(wv[4], wv[5]), make_float2(q.x, q.y), a0);
@@ -275,39 +317,42 @@ __device__ void gemv_rows(const WarpTeam &tm, const MegaStage &st, int rb, int r
     if (!landed && lane == 0) flag_error(ctl, err);  // the block stops at the stage's end
     if (x == 0) tr.mark(s, 7);
     const int r0 = x * R, nr = min(R, n - r0);
-    const int jr = r0 + (((cw - r0) % MW) + MW) % MW;  // this warp's row in the chunk, if any
-    const bool mine = jr < r0 + nr;
-    if (mine) {
-      float2 a0 = make_float2(0.f, 0.f), a1 = a0, b0 = a0, b1 = a0;
+    const int g0 = r0 / NR;                            // the chunk's first group (R is a multiple of NR)
+    const int jg = g0 + (((cw - g0) % MW) + MW) % MW;  // this warp's group in the chunk, if any
+    const int jr = jg * NR;
+    if (jr < r0 + nr) {
+      // a group's second row past the block's last one reads stale slot bytes: not stored
+      float2 a0[NR], a1[NR], b0 = make_float2(0.f, 0.f), b1 = b0;
+#pragma unroll
+      for (int r = 0; r < NR; r++) a0[r] = a1[r] = make_float2(0.f, 0.f);
       if (landed) {
         const uint4 *wg = reinterpret_cast<const uint4 *>(ring + (size_t)sl * SLOT) + (size_t)(jr - r0) * nu;
         const uint4 *wu = wg + (size_t)nr * nu;
 #pragma unroll 8
         for (int u = lane; u < nu; u += 32) {
-          dot8(wg[u], u, a0, a1);
-          if (DUAL) dot8(wu[u], u, b0, b1);
+          const float4 p = reinterpret_cast<const float4 *>(xs)[u], q = reinterpret_cast<const float4 *>(xs)[nu + u];
+#pragma unroll
+          for (int r = 0; r < NR; r++) dot8(wg[u + r * nu], p, q, a0[r], a1[r]);
+          if (DUAL) dot8(wu[u], p, q, b0, b1);
         }
       }
-      const float vg = (a0.x + a0.y) + (a1.x + a1.y), vu = (b0.x + b0.y) + (b1.x + b1.y);
-      const float g = warp_sum(vg), u = DUAL ? warp_sum(vu) : 0.f;
-      if (lane == 0) {
-        const int row = rb + jr;
-        float y;
-        if (mode == EPI_SCALE) {
-          y = g * epi[0][jr];
-        } else if (mode == EPI_SILU) {
-          const float gs = g * epi[0][jr];
-          y = gs * sigmoidf_(gs) * (u * epi[1][jr]);
-        } else {
-          y = g;
+#pragma unroll
+      for (int r = 0; r < NR; r++) {
+        if (NR > 1 && jr + r >= n) break;
+        pg[np * 32 + lane] = (a0[r].x + a0[r].y) + (a1[r].x + a1[r].y);
+        if (DUAL) pu[np * 32 + lane] = (b0.x + b0.y) + (b1.x + b1.y);
+        if (lane == 0) prow[np] = jr + r;
+        if (++np == PEND) {
+          flush_rows<DUAL>(st, rb, np, pg, pu, prow, epi);
+          np = 0;
         }
-        Y[row] = y;
       }
     }
     __syncwarp();
     if (lane == 0 && !ctl.abort) mbar_arrive(smem_addr(&empty[sl]));  // this warp is out of the slot
     tr.add(s, 9, tr.clk() - t1);
   }
+  if (np > 0) flush_rows<DUAL>(st, rb, np, pg, pu, prow, epi);
   tr.flush(s);
 }
 
@@ -349,8 +394,10 @@ __device__ __noinline__ bool gemv_stage(const WarpTeam &tm, const MegaArgs &a, c
     tm.sync();
   }
   tr.mark(s, 2);
-  if (st.pair > 0) gemv_rows<true>(tm, st, rb, re, c, ring, full, empty, xs, epi, ctl, a.err, tr, s);
-  else gemv_rows<false>(tm, st, rb, re, c, ring, full, empty, xs, epi, ctl, a.err, tr, s);
+  float *park = xs + K;  // the rows' parked lane sums, after the input row
+  if (st.pair > 0) gemv_rows<true, 1>(tm, st, rb, re, c, ring, full, empty, xs, park, epi, ctl, a.err, tr, s);
+  else if (st.R % 2 == 0) gemv_rows<false, 2>(tm, st, rb, re, c, ring, full, empty, xs, park, epi, ctl, a.err, tr, s);
+  else gemv_rows<false, 1>(tm, st, rb, re, c, ring, full, empty, xs, park, epi, ctl, a.err, tr, s);
   c += re > rb ? (re - rb + st.R - 1) / st.R : 0;
   const bool ok = team_ok(tm, ctl);
   tr.mark(s, 3);
@@ -852,6 +899,8 @@ int mega_consumer_warps() { return MW; }
 int mega_max_rows_per_block() { return EPI_ROWS; }
 
 size_t mega_work_floats() { return WORK / 4; }
+
+size_t mega_park_floats(bool dual) { return (size_t)(dual ? 2 : 1) * MW * PEND * 32; }
 
 bool mega_supported(int hd, int sms) {
   if (hd != 64 && hd != 128) return false;

@@ -280,6 +280,7 @@ size_t mega_smem_bytes(int hd);
 bool mega_supported(int hd, int sms);
 int mega_chunk_rows(int K, bool dual);  // rows (or gate/up row pairs) per streamed chunk; 0: too long
 size_t mega_work_floats();              // shared scratch of a block: input row, tiles, merge
+size_t mega_park_floats(bool dual);     // ... of it after a GEMV's input row: parked row sums
 int mega_consumer_warps();
 int mega_max_rows_per_block();          // rows of one GEMV a block takes at most
 constexpr int MEGA_AK = 32;             // positions per attention item
