@@ -8,8 +8,8 @@
 // and copies chunks into a ring of shared-memory slots with cp.async.bulk, completion on one
 // mbarrier per slot. It never waits for activations, so HBM keeps streaming the next stages'
 // weights while the consumers wait at a grid barrier or run attention. Warps 1..8 are the
-// consumers; each of them awaits every chunk in order and frees it with its own arrival (so
-// a slot's barrier is always awaited for the phase right after the one last seen). Per
+// consumers; each awaits only the chunks that hold its rows, and a chunk's slot is free once
+// they have all arrived (the first of them arrives for the consumers without a row). Per
 // stage the consumers
 //   * copy the stage's descriptor into shared memory while their first thread waits until
 //     every block has finished the stage before (a counter in global memory);
@@ -46,7 +46,7 @@ constexpr int MTHREADS = 32 * (MW + 1);           // and the producer warp
 constexpr int NS = 7;                             // weight slots
 constexpr uint32_t SLOT = 26 * 1024;              // bytes per slot
 constexpr int RMAX = 8;                           // rows (or row pairs) per chunk at most
-static_assert(RMAX <= MW, "a chunk holds at most one row of each consumer warp");
+static_assert(RMAX <= 32, "a chunk's rows fit the parked sums of one warp in whole rounds");
 constexpr int EPI_ROWS = 256;                     // a block's rows of one GEMV at most
 constexpr uint32_t WORK = 32 * 1024;              // input row, or attention tiles and merge scratch
 constexpr int AK = MEGA_AK;                       // positions per attention item
@@ -64,6 +64,11 @@ struct Ctl {
 
 // Cycle counts of the current stage's phases (trace only; the team's first thread).
 __shared__ unsigned long long trace_acc[6];
+
+// The chunk each weight slot was last given (written by the producer before the copy). A
+// chunk's warp waits for its number before it waits on the slot's barrier: a slot may still
+// hold a chunk several phases older, which a parity wait could not tell apart.
+__shared__ volatile int slot_chunk[NS];
 
 // Optional per-stage timestamps (off when the pointer is null).
 struct Tracer {
@@ -216,6 +221,7 @@ __device__ void produce(const MegaArgs &a, uint8_t *ring, uint64_t *full, uint64
       tr.mark(cp.s, 5);
       marked = cp.s;
     }
+    slot_chunk[sl] = c;
     const uint32_t bytes = (uint32_t)cp.rows() * cp.K * 2, bar = smem_addr(&full[sl]);
     const uint32_t dst = smem_addr(ring + (size_t)sl * SLOT);
     mbar_expect_tx(bar, cp.pair > 0 ? 2 * bytes : bytes);
@@ -235,17 +241,14 @@ __device__ void produce(const MegaArgs &a, uint8_t *ring, uint64_t *full, uint64
 // ---- GEMV stage ---------------------------------------------------------------------------
 
 // A stage's rows in groups of NR (two rows, or one gate/up pair, share each load of the
-// input row): group i of the block's rows goes to warp i mod MW; a chunk holds whole groups
-// and at most one group of each warp. The lanes split a row into 16-byte columns (lane l:
-// columns l, l + 32, ...) against the input row in shared memory, held as two halves
-// (inputs 8u..8u+3 at float4 u of the first, 8u+4..8u+7 of the second) so that the loads
-// are conflict-free. A row's 32 lane sums are not reduced at once: the warp parks them in
-// shared memory and reduces 8 rows together (lane 4i + q adds 8 of row i's sums, two
-// shuffles finish), so that no shuffle chain stands between one row's loads and the next.
-// Lane 4i then applies the epilogue (SwiGLU, logit scale) and stores.
-// Every warp awaits every chunk of the stage and frees it with its own arrival (MW per
-// slot), so no team barrier runs inside the loop; since a warp frees a chunk only after it
-// has landed, its arrivals always fall in the slot's current phase.
+// input row): group g of the block's rows belongs to consumer warp g mod MW, which awaits only
+// the chunks that hold its groups (a chunk holds at most MW groups). The lanes split a row
+// into 16-byte columns (lane l: columns l, l + 32, ...) against the input row in shared
+// memory, held as two halves (inputs 8u..8u+3 at float4 u of the first, 8u+4..8u+7 of the
+// second) so that the loads are conflict-free. A row's 32 lane sums are not reduced at once:
+// the warp parks them in shared memory and reduces 8 rows together (lane 4i + q adds 8 of row
+// i's sums, two shuffles finish), so that no shuffle chain stands between one row's loads
+// and the next; lane 4i then applies the epilogue (SwiGLU, logit scale) and stores.
 constexpr int PEND = 8;  // rows a warp parks before it reduces them
 
 template <bool DUAL>
@@ -291,6 +294,8 @@ __device__ void gemv_rows(const WarpTeam &tm, const MegaStage &st, int rb, int r
   static_assert(!DUAL || NR == 1, "a gate/up pair is a group of its own");
   const int lane = threadIdx.x & 31, cw = tm.warp();
   const int K = st.K, R = st.R, nu = K / 8;  // 16-byte columns per row
+  const int n = re - rb;                     // rows (pairs) of this block
+  const int ngroups = (n + NR - 1) / NR;     // groups do not straddle chunks: R is a multiple of NR
   // this warp's parked lane sums [PEND][32] (gate, then up), and their rows
   float *pg = park + cw * (DUAL ? 2 : 1) * PEND * 32, *pu = pg + PEND * 32;
   __shared__ int prow_all[MW][PEND];
@@ -305,43 +310,40 @@ __device__ void gemv_rows(const WarpTeam &tm, const MegaStage &st, int rb, int r
     a0 = ffma2(make_float2(wv[4], wv[5]), make_float2(q.x, q.y), a0);
     a1 = ffma2(make_float2(wv[6], wv[7]), make_float2(q.z, q.w), a1);
   };
-  const int n = re - rb;  // rows (pairs) of this block
-  const int nch = n > 0 ? (n + R - 1) / R : 0;
   tr.zero(s);
-  for (int x = 0; x < nch; x++) {
-    const int c = c0 + x, sl = c % NS;
+  for (int gi = cw; gi < ngroups; gi += MW) {  // this warp's groups
+    const int x = gi * NR / R, c = c0 + x, sl = c % NS;
     long long t0 = tr.clk();
-    const bool landed = mbar_wait(smem_addr(&full[sl]), (c / NS) & 1, &ctl.abort);
+    bool landed = false;
+    for (uint32_t i = 0; i < MBAR_WAIT_LIMIT && !ctl.abort; i++)
+      if (slot_chunk[sl] == c) {
+        landed = mbar_wait(smem_addr(&full[sl]), (c / NS) & 1, &ctl.abort);
+        break;
+      }
     long long t1 = tr.clk();
     tr.add(s, 8, t1 - t0);
     if (!landed && lane == 0) flag_error(ctl, err);  // the block stops at the stage's end
-    if (x == 0) tr.mark(s, 7);
-    const int r0 = x * R, nr = min(R, n - r0);
-    const int g0 = r0 / NR;                            // the chunk's first group (R is a multiple of NR)
-    const int jg = g0 + (((cw - g0) % MW) + MW) % MW;  // this warp's group in the chunk, if any
-    const int jr = jg * NR;
-    if (jr < r0 + nr) {
-      // a group's second row past the block's last one reads stale slot bytes: not stored
+    const int r0 = x * R, nr = min(R, n - r0), j = gi * NR - r0;
+    if (landed) {
+      // a group's second row past the chunk's last one reads stale slot bytes: not stored
       float2 a0[NR], a1[NR], b0 = make_float2(0.f, 0.f), b1 = b0;
 #pragma unroll
       for (int r = 0; r < NR; r++) a0[r] = a1[r] = make_float2(0.f, 0.f);
-      if (landed) {
-        const uint4 *wg = reinterpret_cast<const uint4 *>(ring + (size_t)sl * SLOT) + (size_t)(jr - r0) * nu;
-        const uint4 *wu = wg + (size_t)nr * nu;
+      const uint4 *wc = reinterpret_cast<const uint4 *>(ring + (size_t)sl * SLOT);
+      const uint4 *wg = wc + (size_t)j * nu, *wu = wc + (size_t)(nr + j) * nu;
 #pragma unroll 8
-        for (int u = lane; u < nu; u += 32) {
-          const float4 p = reinterpret_cast<const float4 *>(xs)[u], q = reinterpret_cast<const float4 *>(xs)[nu + u];
+      for (int u = lane; u < nu; u += 32) {
+        const float4 p = reinterpret_cast<const float4 *>(xs)[u], q = reinterpret_cast<const float4 *>(xs)[nu + u];
 #pragma unroll
-          for (int r = 0; r < NR; r++) dot8(wg[u + r * nu], p, q, a0[r], a1[r]);
-          if (DUAL) dot8(wu[u], p, q, b0, b1);
-        }
+        for (int r = 0; r < NR; r++) dot8(wg[u + r * nu], p, q, a0[r], a1[r]);
+        if (DUAL) dot8(wu[u], p, q, b0, b1);
       }
 #pragma unroll
       for (int r = 0; r < NR; r++) {
-        if (NR > 1 && jr + r >= n) break;
+        if (NR > 1 && j + r >= nr) break;
         pg[np * 32 + lane] = (a0[r].x + a0[r].y) + (a1[r].x + a1[r].y);
         if (DUAL) pu[np * 32 + lane] = (b0.x + b0.y) + (b1.x + b1.y);
-        if (lane == 0) prow[np] = jr + r;
+        if (lane == 0) prow[np] = gi * NR + r;
         if (++np == PEND) {
           flush_rows<DUAL>(st, rb, np, pg, pu, prow, epi);
           np = 0;
@@ -349,7 +351,10 @@ __device__ void gemv_rows(const WarpTeam &tm, const MegaStage &st, int rb, int r
       }
     }
     __syncwarp();
-    if (lane == 0 && !ctl.abort) mbar_arrive(smem_addr(&empty[sl]));  // this warp is out of the slot
+    // the slot is free after MW arrivals: one per group of the chunk, the first group's warp
+    // also arriving for the warps that hold no group of it
+    const int ng = (nr + NR - 1) / NR;
+    if (lane == 0 && !ctl.abort) mbar_arrive_n(smem_addr(&empty[sl]), j == 0 ? MW - ng + 1 : 1);
     tr.add(s, 9, tr.clk() - t1);
   }
   if (np > 0) flush_rows<DUAL>(st, rb, np, pg, pu, prow, epi);
@@ -817,7 +822,8 @@ __global__ void __launch_bounds__(MTHREADS, 1) mega_decode_kernel(const __grid_c
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; s++) {
       mbar_init(smem_addr(&full[s]), 1);
-      mbar_init(smem_addr(&empty[s]), MW);  // every consumer warp frees every chunk
+      mbar_init(smem_addr(&empty[s]), MW);
+      slot_chunk[s] = -1;
     }
     mbar_init(smem_addr(&abar), 1);
     mbar_fence_init();
