@@ -165,12 +165,13 @@ int dory_prefill_chunk(dory_t *d, int32_t seq, const int32_t *ids, int32_t n, in
  * dory_prefill_chunk over consecutive chunks of 64 rows from pos0 with `want` on the last
  * chunk and DORY_WANT_NONE on the others (dory.rs fn forward_host; prompt_loops as there).
  * The input and output blocks run once per row, at loop 0, and attend causally to their own
- * rows, so they run over up to 512 rows of several chunks at once (dense contractions on the
- * tensor cores, activations rounded to bf16 from 256 rows up), while the recurrent block
- * runs chunk by chunk (under last_loop a chunk's rows see earlier chunks at their last
- * pass). The row count per block step is what the input/output rings hold beyond their
- * window (512 with the pages' sizes); without room for 128 rows, or with f32 weights, the
- * prompt goes chunk by chunk. `want`: DORY_WANT_NONE or DORY_WANT_LAST (one logits row).
+ * rows, so their projections and MLPs run over up to 4096 rows of many chunks at once (dense
+ * contractions on the tensor cores, activations rounded to bf16 from 256 rows up; 512 rows
+ * with q8_2f rings), while the recurrent block runs chunk by chunk (under last_loop a chunk's
+ * rows see earlier chunks at their last pass). Their attention takes pieces of as many rows
+ * as the input/output rings hold beyond their window (512 with the pages' sizes); without
+ * room for 128 rows, or with f32 weights, the prompt goes chunk by chunk. `want`:
+ * DORY_WANT_NONE or DORY_WANT_LAST (one logits row).
  * Errors: as dory_prefill_chunk (n >= 1, want none or last). */
 int dory_prefill(dory_t *d, int32_t seq, const int32_t *ids, int32_t n, int32_t pos0, int32_t loops, int32_t want);
 

@@ -64,6 +64,9 @@ constexpr int TC_TRACE_BLOCKS = 1024;
 // MMA's M side and bf16 activations (below it the weights stream once for a thin row block).
 constexpr int TC_BIG_ROWS = 256;
 constexpr int TC_BIG_CTRS = 4096;  // tile counters of launch_tc_gemm_big's split K
+// Rows of dory_prefill's input/output-block steps over f32 rings when the bf16-activation
+// tcgen05 kernel runs their projections (their attention goes in ring-sized pieces).
+constexpr int PREFILL_ROWS = 4096;
 
 int bn_index(int bn) { return bn <= 16 ? 0 : bn <= 32 ? 1 : bn <= 64 ? 2 : bn <= 128 ? 3 : 4; }
 
@@ -109,8 +112,10 @@ struct dory_handle {
   int wdtype = 0;
   size_t esz = 4;
   cudaStream_t stream = nullptr;
-  int Tmax = 64;
-  int prefill_rows = 0;  // rows of a whole prompt's input/output-block steps (dory_prefill); 0: chunk by chunk
+  int Tmax = 64;          // rows of a step at most (the row table's stride)
+  int Tstep = 64;         // ... of a decode or batched-prefill step, and of the logits buffers
+  int prefill_rows = 0;   // rows of a whole prompt's input/output-block steps (dory_prefill); 0: chunk by chunk
+  int piece_rows = 0;     // rows of such a step that join the rings and attend at once
 
   char *wmem = nullptr;
   size_t wbytes = 0;
@@ -515,8 +520,14 @@ int issue_step(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_splits, cud
       } else if ((rc = gemm(L.wqkvg, ldq, dm.hidden, H, dm.hidden, Tr, d->qkvg, ldq, ep))) {
         return rc;
       }
-      CK(launch_prep(d->qkvg, ldq, dm, rows_l, d->rope, L.sliding ? 0 : 1, L.sq, ring, d->kst, d->vst, s));
-      nl++;
+      // prefill chunks: a chunk's rows share every key block (the merge also row-normalises z);
+      // a step of more rows than a ring takes at once prepares and attends piece by piece
+      const bool chunked = chunk_rows && Tr == T && !q8 && (dm.hd == 64 || dm.hd == 128);
+      const bool pieces = chunked && T > d->piece_rows;
+      if (!pieces) {
+        CK(launch_prep(d->qkvg, ldq, dm, rows_l, d->rope, L.sliding ? 0 : 1, L.sq, ring, d->kst, d->vst, s));
+        nl++;
+      }
       if (q8) {
         CK(launch_q8_append(d->kst, d->vst, kv_size, dm, rows_l, ring, rewrite ? 1 : 0, s));
         nl++;
@@ -526,22 +537,27 @@ int issue_step(dory_t *d, const StepArgs &a, int32_t *rt, bool fixed_splits, cud
       const int splits = (int)((keys + KEYS_PER_SPLIT - 1) / KEYS_PER_SPLIT);
       if (splits > d->max_splits) return fail(DORY_ERANGE, "attention needs %d splits (max %d)", splits, d->max_splits);
       bool z_normed = false;
-      if (chunk_rows && Tr == T && !q8 && (dm.hd == 64 || dm.hd == 128)) {
-        // prefill chunks: a chunk's rows share every key block; the merge also row-normalises z
-        for (const auto &sg_ : segs) {
-          const int r0 = sg_.first, n = sg_.second;
-          const int nkb = attn_chunk_blocks(wmax, n);
-          if (nkb > d->max_splits) return fail(DORY_ERANGE, "chunk attention needs %d key blocks", nkb);
-          Rows rs = rows_l;
-          rs.seq = rows_l.seq + r0;
-          rs.off = rows_l.off + r0;
-          rs.n = n;
-          const size_t zo = (size_t)r0 * q_size;
-          const Emit ez = tc ? Emit{d->em_z.hi + zo, d->em_z.lo + zo} : Emit{nullptr, nullptr};
-          CK(launch_attention_chunk(d->qkvg + (size_t)r0 * ldq, ldq, dm, rs, ring, nkb, d->part, L.sg, d->z + zo, ez,
-                                    d->dev_err, s));
-          nl += 2;
-        }
+      if (chunked) {
+        for (const auto &sg_ : segs)
+          for (int r0 = sg_.first; r0 < sg_.first + sg_.second; r0 += d->piece_rows) {
+            const int n = std::min(d->piece_rows, sg_.first + sg_.second - r0);
+            const int nkb = attn_chunk_blocks(wmax, n);
+            if (nkb > d->max_splits) return fail(DORY_ERANGE, "chunk attention needs %d key blocks", nkb);
+            Rows rs = rows_l;
+            rs.seq = rows_l.seq + r0;
+            rs.off = rows_l.off + r0;
+            rs.n = n;
+            if (pieces) {
+              CK(launch_prep(d->qkvg + (size_t)r0 * ldq, ldq, dm, rs, d->rope + (size_t)r0 * 2 * dm.hd,
+                             L.sliding ? 0 : 1, L.sq, ring, d->kst, d->vst, s));
+              nl++;
+            }
+            const size_t zo = (size_t)r0 * q_size;
+            const Emit ez = tc ? Emit{d->em_z.hi + zo, d->em_z.lo + zo} : Emit{nullptr, nullptr};
+            CK(launch_attention_chunk(d->qkvg + (size_t)r0 * ldq, ldq, dm, rs, ring, nkb, d->part, L.sg, d->z + zo,
+                                      ez, d->dev_err, s));
+            nl += 2;
+          }
         z_normed = true;
       } else if ((q8 ? dm.hd == 128 && !getenv_off("DORY_STREAM_Q8") : (dm.hd == 64 || dm.hd == 128)) &&
                  !getenv_off("DORY_STREAM_ATTN")) {
@@ -1142,7 +1158,9 @@ int setup_tc(dory_t *d) {
   int dev = 0, sms = 148;
   CK(cudaGetDevice(&dev));
   CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-  const int bn_max = tc_tile_rows(d->Tmax);
+  // rows of the split-activation kernel's steps (larger steps take launch_tc_gemm_big)
+  const int small_rows = d->tc_big ? std::min(d->Tmax, TC_BIG_ROWS - 1) : d->Tmax;
+  const int bn_max = tc_tile_rows(small_rows);
   int max_split = 4;  // K splits per tile at most (measured best for 64-row steps); DORY_TC_SPLITS changes it
   if (const char *e = getenv("DORY_TC_SPLITS")) max_split = std::max(1, std::min(8, atoi(e)));
   int per_sm = 1;  // blocks per SM the splits aim at (one: the 64-row rings fill an SM); DORY_TC_PER_SM changes it
@@ -1162,7 +1180,7 @@ int setup_tc(dory_t *d) {
       }
     }
     w.splits = std::max(1, std::min(std::min(per_sm * sms / mt, max_split), nkb));
-    const int t_tiles = (d->Tmax + bn_max - 1) / bn_max;
+    const int t_tiles = (small_rows + bn_max - 1) / bn_max;
     ws_floats = std::max(ws_floats, (size_t)mt * t_tiles * w.splits * (pair ? 2 : 1) * bn_max * 128);
     max_tiles = std::max(max_tiles, mt * t_tiles);
     return DORY_OK;
@@ -1265,11 +1283,12 @@ int dory_create(const dory_config *cfg, const dory_weights *w, void *stream, dor
   d->wdtype = cfg->weight_dtype == DORY_W_BF16 ? W_BF16 : W_F32;
   d->esz = cfg->weight_dtype == DORY_W_BF16 ? 2 : 4;
   d->stream = static_cast<cudaStream_t>(stream);
-  d->Tmax = std::max(DORY_CHUNK_ROWS, cfg->max_batch);
+  d->Tmax = d->Tstep = std::max(DORY_CHUNK_ROWS, cfg->max_batch);
   {
-    // dory_prefill runs the input and output blocks over up to 512 rows at once: all of them
-    // join a ring before any attends, so a sliding (or capped full) ring must hold the rows
-    // plus the window behind the first: rows + window - 1 <= ring rows
+    // dory_prefill runs the input and output blocks over up to PREFILL_ROWS rows at once. Their
+    // attention takes pieces of at most 512 rows: a piece's rows join a ring before any of
+    // them attends, so a sliding (or capped full) ring must hold the piece plus the window
+    // behind its first row: rows + window - 1 <= ring rows
     long lim = 512;
     for (size_t li = 0; li < pat.size(); li++) {
       const bool io = (int)li < cfg->n_in || (int)li >= cfg->n_in + cfg->n_rec;
@@ -1281,9 +1300,19 @@ int dory_create(const dory_config *cfg, const dory_weights *w, void *stream, dor
       cap = (win + RING_EXTRA + 63) / 64 * 64;
       lim = std::min(lim, cap - win + 1);
     }
-    if (const char *e = getenv("DORY_PREFILL_ROWS")) lim = std::min<long>(lim, std::max(0, atoi(e)));
     lim = lim / 64 * 64;
-    d->prefill_rows = (lim >= 128 && cfg->weight_dtype == DORY_W_BF16) ? (int)lim : 0;
+    d->piece_rows = (int)lim;
+    // f32 rings: the projections and MLPs of the input and output blocks run over many more
+    // rows per step (tensor-bound contractions), the attention piece by piece; q8_2f rings
+    // attend the step's rows at once
+    const int q_sz = cfg->nh * cfg->hd;
+    const bool big = cfg->kv_quant != DORY_KV_Q8_2F && cfg->weight_dtype == DORY_W_BF16 && !getenv_off("DORY_TC") &&
+                     !getenv_off("DORY_TC_BIG") && cfg->ffn % 128 == 0 && cfg->hidden % 64 == 0 && q_sz % 64 == 0;
+    long rows = big ? std::max<long>(lim, PREFILL_ROWS) : lim;
+    if (const char *e = getenv("DORY_PREFILL_ROWS")) rows = std::min<long>(rows, std::max(0, atoi(e)));
+    rows = rows / 64 * 64;
+    d->piece_rows = (int)std::min<long>(d->piece_rows, rows);
+    d->prefill_rows = (d->piece_rows >= 128 && cfg->weight_dtype == DORY_W_BF16) ? (int)rows : 0;
     d->Tmax = std::max(d->Tmax, d->prefill_rows);
   }
   const Dims &dm = d->dims;
@@ -1415,7 +1444,7 @@ int dory_create(const dory_config *cfg, const dory_weights *w, void *stream, dor
     const long keys = o.window == INT_MAX ? (long)o.cap : std::min<long>(o.window, o.cap);
     d->max_splits = std::max<int>(d->max_splits, (int)((keys + KEYS_PER_SPLIT - 1) / KEYS_PER_SPLIT));
     d->max_splits = std::max<int>(d->max_splits, attn_tma_splits(keys));
-    d->max_splits = std::max<int>(d->max_splits, attn_chunk_blocks(keys, d->Tmax));
+    d->max_splits = std::max<int>(d->max_splits, attn_chunk_blocks(keys, std::max(d->Tstep, d->piece_rows)));
     if ((keys + KEYS_PER_SPLIT - 1) / KEYS_PER_SPLIT > 2 * dm.hd) {
       fail(DORY_EINVAL, "a window of %ld keys is more than the attention merge holds for hd %d", keys, dm.hd);
       return cleanup(DORY_EINVAL);
@@ -1452,12 +1481,13 @@ int dory_create(const dory_config *cfg, const dory_weights *w, void *stream, dor
                a_st = areserve((size_t)T * dm.hidden * 4),
                a_qkvg = areserve((size_t)T * (2 * q_size + 2 * kv_size) * 4),
                a_z = areserve((size_t)T * q_size * 4), a_out = areserve((size_t)T * dm.hidden * 4),
-               a_mlp = areserve((size_t)T * dm.ffn * 4), a_lg = areserve((size_t)T * dm.vocab * 4),
+               a_mlp = areserve((size_t)T * dm.ffn * 4), a_lg = areserve((size_t)d->Tstep * dm.vocab * 4),
                a_rope = areserve((size_t)T * 2 * dm.hd * 4),
-               a_part = areserve((size_t)T * dm.nk * d->max_splits * rep * (dm.hd + 2) * 4),
+               a_part = areserve((size_t)std::max(d->Tstep, d->piece_rows) * dm.nk * d->max_splits * rep *
+                                 (dm.hd + 2) * 4),
                a_kst = areserve((size_t)T * kv_size * 4), a_vst = areserve((size_t)T * kv_size * 4),
                a_ids = areserve((size_t)T * 4), a_ids2 = areserve((size_t)T * 4),
-               a_lg2 = areserve((size_t)T * dm.vocab * 4),
+               a_lg2 = areserve((size_t)d->Tstep * dm.vocab * 4),
                a_sp = areserve((size_t)cfg->max_seqs * 4), a_rows = areserve((size_t)ROW_TABLE * T * 4),
                a_zero = areserve((size_t)cfg->max_seqs * 4), a_err = areserve(256);
   const size_t ms_bytes = (size_t)(64 + dm.nk + dm.nk * MEGA_FLAGS) * 4, a_ms = areserve(ms_bytes);
@@ -1774,7 +1804,7 @@ int dory_prefill_batch(dory_t *d, int32_t nseq, const int32_t *seqs, const int32
                        int32_t loops, int32_t want) {
   if (!d) return fail(DORY_EINVAL, "handle is NULL");
   if (!seqs || !counts || !ids) return fail(DORY_EINVAL, "seqs, counts or ids is NULL");
-  if (nseq < 1 || nseq > d->Tmax) return fail(DORY_EINVAL, "nseq=%d: want 1..%d", nseq, d->Tmax);
+  if (nseq < 1 || nseq > d->Tstep) return fail(DORY_EINVAL, "nseq=%d: want 1..%d", nseq, d->Tstep);
   if (loops < 1 || loops > d->cfg.max_loops) return fail(DORY_EINVAL, "loops=%d: want 1..%d", loops, d->cfg.max_loops);
   if (want < DORY_WANT_NONE || want > DORY_WANT_ALL) return fail(DORY_EINVAL, "want=%d", want);
   std::vector<char> seen(d->cfg.max_seqs, 0);
@@ -1788,7 +1818,7 @@ int dory_prefill_batch(dory_t *d, int32_t nseq, const int32_t *seqs, const int32
     if ((rc = check_range(d, sq, (long)d->seq_pos[sq] + n - 1))) return rc;
     T += n;
   }
-  if (T > d->Tmax) return fail(DORY_EINVAL, "%d rows in one step: at most %d (max(64, max_batch))", T, d->Tmax);
+  if (T > d->Tstep) return fail(DORY_EINVAL, "%d rows in one step: at most %d (max(64, max_batch))", T, d->Tstep);
   // dory.rs fn chunk_loops
   int L = loops;
   if (want == DORY_WANT_NONE && d->cfg.prompt_loops > 0 && d->cfg.kv_mode == DORY_KV_LAST_LOOP)

@@ -292,14 +292,18 @@ def test_batch1_decode_at_prompt_4096_replays_exactly():
         g.close()
 
 
-def test_prefill_2048_in_block_steps_of_512_rows():
+@pytest.mark.parametrize("block", [2048, 512])
+def test_prefill_2048_in_block_steps(block, monkeypatch):
     """The prefill workload's shape through dory_prefill: 2048 tokens, the input and output
-    blocks over 512 rows at once (tensor-core kernel with the step rows as the MMA's M side),
-    the recurrent block in 64-row chunks, prompt_loops 2, the last row's logits read; against
-    the oracle's chunked forward."""
+    blocks over all 2048 rows at once (their attention in 512-row pieces) or over 512-row
+    steps (tensor-core kernel with the step rows as the MMA's M side), the recurrent block in
+    64-row chunks, prompt_loops 2, the last row's logits read; against the oracle's chunked
+    forward."""
     from looped_normalized_gpt_gb300 import Dory, build
 
     build()
+    if block == 512:
+        monkeypatch.setenv("DORY_PREFILL_ROWS", "512")
     cfg = synth.dory2b(prompt_loops=2, max_context=2048 + 64)
     w = synth.weights(cfg, SEED_4)
     g = Dory(cfg, w)
@@ -310,7 +314,7 @@ def test_prefill_2048_in_block_steps_of_512_rows():
         g.prefill(0, ids, 0, 4, "last")
         for a in range(0, 2048, 64):
             lo, ho = o.forward_chunk(st, ids[a:a + 64], a, 4, "last" if a + 64 >= 2048 else "none")
-        hg = g.read_hidden(512)
+        hg = g.read_hidden(block)
         herr = float(np.max(np.abs(hg[-64:] - ho)))
         assert herr <= 2e-2, herr
         e, t1 = _check_row(o, cfg, hg[-1], ho[-1], g.logits(0), lo[0])
