@@ -2034,7 +2034,8 @@ int dory_write_kv_rows(dory_t *d, int32_t seq, int32_t ordinal, int32_t loop_slo
   const bool q8 = d->cfg.kv_quant == DORY_KV_Q8_2F;
   cudaStream_t s = d->stream;
   for (int a = 0; a < n;) {
-    int m = std::min(n - a, d->Tmax);
+    // at most a ring's rows per launch: two rows of one launch never share a ring row
+    int m = std::min(std::min(n - a, d->Tmax), ring.cap);
     // q8: rows up to and including the freeze go one at a time in order
     const int c = cnt + a;
     int seq_rows = 0;
