@@ -399,13 +399,26 @@ cudaError_t stream_t(const float *qkvg, int ldq, Dims d, Rows rows, Ring ring, c
 
 int attn_stream_splits(long window_keys, int rows, int nk, int sms) {
   // only when the (row, kv head) blocks leave SMs idle (at batch 64 x 4 kv heads a split
-  // measured slower: 2.22 -> 2.46 ms a step); then blocks for two per SM (the kernel's stages
-  // take under half an SM's shared memory), at least 4 tiles (128 positions) a split
-  if ((long)rows * nk >= sms) return 1;
+  // measured slower: 2.22 -> 2.46 ms a step), at least 4 tiles (128 positions) a split. Two
+  // blocks fit an SM (the stages take under half its shared memory), so a split's time goes
+  // as the rounds of blocks times the tiles a block streams, plus the merge of the splits
+  // (half a tile a split): per_loop batch 16 at context 8192 measured 5 splits 2.59 ms a step,
+  // 8 2.31, 10 2.42, 12 2.35, 16 2.36 (cost 103, 64, 77, 64, 64 tiles)
+  const long units = (long)rows * nk;
+  if (units >= sms) return 1;
   const long tiles = (window_keys + AS_KEYS - 1) / AS_KEYS + 1;
-  const long want = (2L * sms + (long)rows * nk - 1) / ((long)rows * nk);
-  const long most = tiles / 4;
-  return (int)std::max(1L, std::min(want, std::min(most, 64L)));
+  const long most = std::max(1L, std::min(tiles / 4, 64L)), slots = 2L * sms;
+  long best = 1;
+  double best_cost = 1e30;
+  for (long sp = 1; sp <= most; sp++) {
+    const long rounds = (units * sp + slots - 1) / slots;
+    const double cost = (double)rounds * (double)((tiles + sp - 1) / sp) + 0.5 * (double)sp;
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = sp;
+    }
+  }
+  return (int)best;
 }
 
 cudaError_t launch_attention_stream(const float *qkvg, int ldq, Dims d, Rows rows, Ring ring, const float *sg,
