@@ -120,7 +120,7 @@ def profile_case(args):
     output pair at loops 1 (427 MB of weights per token, still larger than L2, about 1 GB on
     the device); prefill: 64-row chunks of a prompt of --prompt tokens on the 2B model;
     prefill-whole: the same prompt in one dory_prefill call;
-    batch64: the batch-64 decode line with 4 timed steps."""
+    batch64: the batch-64 decode line with 4 timed steps (in an NVTX range "decode")."""
     import torch
 
     from looped_normalized_gpt_gb300 import Dory, build
@@ -128,7 +128,7 @@ def profile_case(args):
     build()
     if args.profile_case == "batch64":
         w = synth.weights(synth.dory2b(), SEED)
-        out = bench_batch(Dory, torch, w, int(os.environ.get("LOCAL_RANK", "0")), steps=4)
+        out = bench_batch(Dory, torch, w, int(os.environ.get("LOCAL_RANK", "0")), steps=4, nvtx=True)
         return {"case": "batch64", **out, "note": "profiling case, not a bench line"}
     if args.profile_case == "context-small":
         # the long-context lines on fewer sequences (a few GB on the device), the timed decode
@@ -359,9 +359,11 @@ def bench_q8_batch64(g_cls, torch, w, dev, steps: int = 8, warmup: int = 3, nvtx
     return bench_context_decode(g_cls, torch, w, dev, cfg, 64, 8192, [16] * steps, warmup, SEED + 3, nvtx=nvtx)
 
 
-def bench_batch(g_cls, torch, w, dev, batch: int = 64, ctx: int = 1024, steps: int = 16, warmup: int = 3):
+def bench_batch(g_cls, torch, w, dev, batch: int = 64, ctx: int = 1024, steps: int = 16, warmup: int = 3,
+                nvtx: bool = False):
     """Batch decode on the same model: `batch` sequences, each with `ctx` positions of
-    synthetic unit-norm K/V rows in every slot, then `steps` decode steps at loops 4."""
+    synthetic unit-norm K/V rows in every slot, then `steps` decode steps at loops 4 (inside
+    an NVTX range "decode" with `nvtx`)."""
     cfg = synth.dory2b(max_batch=batch, max_seqs=batch, max_context=ctx + steps + warmup + 64)
     stream = torch.cuda.current_stream()
     g = g_cls(cfg, w, stream=stream.cuda_stream)
@@ -385,8 +387,12 @@ def bench_batch(g_cls, torch, w, dev, batch: int = 64, ctx: int = 1024, steps: i
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
+        if nvtx:
+            torch.cuda.nvtx.range_push("decode")
         for i in range(warmup, warmup + steps):
             g.decode_step(ids[i * batch:(i + 1) * batch], seqs, cfg.loops)
+        if nvtx:
+            torch.cuda.nvtx.range_pop()
         e1.record(stream)
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / steps
