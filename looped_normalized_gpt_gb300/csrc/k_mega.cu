@@ -506,13 +506,12 @@ __device__ __forceinline__ void merge_items(const WarpTeam &tm, const MegaStage 
   }
 }
 
-// Merge the items of query head h (of kv head kh = h / rep) once every item of kh has
-// published its flag for this stage, and gate: warp 0 polls the flags (relaxed loads, then an
-// acquire fence; the team sync passes the order on), then thread t takes the 4 outputs
-// q = t mod HD/4 and the items g, g + G, ... (g = t / (HD/4), G = team size / (HD/4)), loads
-// them at once and folds them in item order with a running max; the groups meet in shared
-// memory and warp 0 finishes in group order: y = sum o e^(m - M) / sum l e^(m - M),
-// z = y * sigmoid(g * s_g^2). Returns false (team-uniformly) when the block has stopped.
+// Merge the items of query head h (of kv head kh = h / rep) and gate: thread t takes the 4
+// outputs q = t mod HD/4 and the items g, g + G, ... (g = t / (HD/4), G = team size / (HD/4)),
+// loads each item's partials once the item has published its flag for this stage, and folds
+// them in item order with a running max; the groups meet in shared memory and warp 0
+// finishes in group order: y = sum o e^(m - M) / sum l e^(m - M), z = y * sigmoid(g * s_g^2).
+// Returns false (team-uniformly) when the block has stopped.
 template <int HD>
 __device__ __noinline__ bool merge_head(const WarpTeam &tm, const MegaArgs &a, const MegaStage &st, const Dims &d,
                                         int h, int nblk, int s, float *scr, Ctl &ctl) {
@@ -520,36 +519,37 @@ __device__ __noinline__ bool merge_head(const WarpTeam &tm, const MegaArgs &a, c
   constexpr int NQ = HD / 4, IB = MEGA_FLAGS / (32 * MW / NQ);  // items a thread holds at most
   const int rep = d.nh / d.nk, kh = h / rep, hh = h % rep;
   const int groups = tm.size() / NQ;
-  const int t = tm.tid(), q = t % NQ, g = t / NQ, lane = threadIdx.x & 31;
+  const int t = tm.tid(), q = t % NQ, g = t / NQ;
   const size_t c = (size_t)h * HD + (size_t)q * 4;
   float4 gr = make_float4(0.f, 0.f, 0.f, 0.f), sg = gr;
   if (g == 0) {  // the gate inputs, in flight while the items finish
     gr = __ldcg(reinterpret_cast<const float4 *>(st.qkvg + (size_t)(d.nh + 2 * d.nk) * HD + c));
     sg = __ldg(reinterpret_cast<const float4 *>(st.sg + c));
   }
-  if (tm.warp() == 0) {
-    const int *fl = a.aflag + kh * MEGA_FLAGS;
-    uint32_t polls = 0;
-    while (!__all_sync(0xffffffffu, lane >= nblk || ld_relaxed_gpu(fl + lane) == s + 1)) {
-      if (ctl.abort) break;
-      if (++polls > a.spin_limit) {
-        if (lane == 0) flag_error(ctl, a.err);
-        break;
-      }
-    }
-    fence_acq_rel_gpu();
-  }
-  if (!team_ok(tm, ctl)) return false;
+  // each item's partials as soon as it has published them: the flag is read with acquire
+  // loads, so the partial loads that follow it see the item's stores; only the last item's
+  // loads stay on the critical path
+  const int *fl = a.aflag + kh * MEGA_FLAGS;
   float4 o[IB];
   float2 ml[IB];
 #pragma unroll
   for (int u = 0; u < IB; u++) {
     const int it = g + u * groups;
-    const bool in = it < nblk;
-    o[u] = in ? __ldcg(reinterpret_cast<const float4 *>(part_o(st, rep, HD, kh, it, hh) + q * 4))
-              : make_float4(0.f, 0.f, 0.f, 0.f);
-    ml[u] = in ? __ldcg(reinterpret_cast<const float2 *>(part_ml(st, d.nk, rep, HD, kh, it, hh)))
-               : make_float2(-INFINITY, 0.f);
+    o[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    ml[u] = make_float2(-INFINITY, 0.f);
+    if (it >= nblk) continue;
+    bool seen = false;
+    for (uint32_t polls = 0; !ctl.abort && polls <= a.spin_limit; polls++)
+      if (ld_acquire_gpu(fl + it) == s + 1) {
+        seen = true;
+        break;
+      }
+    if (!seen) {
+      flag_error(ctl, a.err);
+      continue;
+    }
+    o[u] = __ldcg(reinterpret_cast<const float4 *>(part_o(st, rep, HD, kh, it, hh) + q * 4));
+    ml[u] = __ldcg(reinterpret_cast<const float2 *>(part_ml(st, d.nk, rep, HD, kh, it, hh)));
   }
   float M = -INFINITY, L = 0.f;
   float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -567,7 +567,7 @@ __device__ __noinline__ bool merge_head(const WarpTeam &tm, const MegaArgs &a, c
   Acc[g * NQ + q] = A;
   Ms[g * NQ + q] = M;
   Ls[g * NQ + q] = L;
-  tm.sync();
+  if (!team_ok(tm, ctl)) return false;  // (its first sync publishes the groups' states)
   if (g == 0) {
     float Mx = -INFINITY;
     for (int k = 0; k < groups; k++) Mx = fmaxf(Mx, Ms[k * NQ + q]);
