@@ -331,7 +331,7 @@ __device__ void gemv_rows(const WarpTeam &tm, const MegaStage &st, int rb, int r
       for (int r = 0; r < NR; r++) a0[r] = a1[r] = make_float2(0.f, 0.f);
       const uint4 *wc = reinterpret_cast<const uint4 *>(ring + (size_t)sl * SLOT);
       const uint4 *wg = wc + (size_t)j * nu, *wu = wc + (size_t)(nr + j) * nu;
-#pragma unroll 8
+#pragma unroll 4
       for (int u = lane; u < nu; u += 32) {
         const float4 p = reinterpret_cast<const float4 *>(xs)[u], q = reinterpret_cast<const float4 *>(xs)[nu + u];
 #pragma unroll
