@@ -33,6 +33,21 @@ __device__ __forceinline__ float block_sum(float v, float *red) {
   return t;
 }
 
+// Two block sums at once (the same order as two block_sum calls; `red` holds 64 floats).
+__device__ __forceinline__ void block_sum2(float &a, float &b, float *red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+  a = warp_sum(a);
+  b = warp_sum(b);
+  __syncthreads();
+  if (lane == 0) {
+    red[warp] = a;
+    red[32 + warp] = b;
+  }
+  __syncthreads();
+  a = warp_sum((lane < nw) ? red[lane] : 0.f);
+  b = warp_sum((lane < nw) ? red[32 + lane] : 0.f);
+}
+
 __device__ __forceinline__ float block_max(float v, float *red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
   v = warp_max(v);

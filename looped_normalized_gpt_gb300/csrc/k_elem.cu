@@ -191,38 +191,44 @@ template <int MAXV>
 __global__ void residual_kernel(float *__restrict__ h, const float *__restrict__ out,
                                 const float *__restrict__ alpha, int hidden, int mix, float *__restrict__ input,
                                 float *__restrict__ state, int do_residual, Emit em) {
-  __shared__ float red[32];
+  __shared__ float red[64];
   pdl_trigger_();
   const int r = blockIdx.x;
   float *hr = h + (size_t)r * hidden;
   const float *orow = out + (size_t)r * hidden;
-  float x[MAXV];
+  float x[MAXV], o[MAXV], al[MAXV], ip[MAXV];  // every row the kernel reads, loaded at once
   const int nper = (hidden + blockDim.x - 1) / blockDim.x;
+  float *in_r = input + (size_t)r * hidden, *st_r = state + (size_t)r * hidden;
+  const bool read_in = mix == MIX_LOOP || mix == MIX_RESUME;
   float sx = 0.f, so = 0.f;
 #pragma unroll
   for (int i = 0; i < MAXV; i++) {
     const int c = threadIdx.x + i * blockDim.x;
-    x[i] = 0.f;
+    x[i] = o[i] = al[i] = ip[i] = 0.f;
     if (i < nper && c < hidden) {
-      x[i] = mix == MIX_RESUME ? state[(size_t)r * hidden + c] : hr[c];
+      x[i] = mix == MIX_RESUME ? st_r[c] : hr[c];
       if (do_residual) {
-        const float o = orow[c];
-        sx += x[i] * x[i];
-        so += o * o;
+        o[i] = orow[c];
+        al[i] = alpha[c];
       }
+      if (read_in) ip[i] = in_r[c];
     }
   }
   if (do_residual) {
-    sx = block_sum(sx, red);
-    so = block_sum(so, red);
+#pragma unroll
+    for (int i = 0; i < MAXV; i++) {
+      sx += x[i] * x[i];
+      so += o[i] * o[i];
+    }
+    block_sum2(sx, so, red);
     const float ix = 1.f / sqrtf(sx + DORY_EPS), io = 1.f / sqrtf(so + DORY_EPS);
     float s = 0.f;
 #pragma unroll
     for (int i = 0; i < MAXV; i++) {
       const int c = threadIdx.x + i * blockDim.x;
       if (i < nper && c < hidden) {
-        const float xh = x[i] * ix, oh = orow[c] * io;
-        x[i] = xh + alpha[c] * (oh - xh);
+        const float xh = x[i] * ix, oh = o[i] * io;
+        x[i] = xh + al[i] * (oh - xh);
         s += x[i] * x[i];
       }
     }
@@ -240,7 +246,6 @@ __global__ void residual_kernel(float *__restrict__ h, const float *__restrict__
 #pragma unroll
     for (int i = 0; i < MAXV; i++) x[i] *= inv;
   }
-  float *in_r = input + (size_t)r * hidden, *st_r = state + (size_t)r * hidden;
   if (mix == MIX_BEGIN || mix == MIX_LOOP || mix == MIX_RESUME) {
     float s = 0.f;
 #pragma unroll
@@ -252,7 +257,7 @@ __global__ void residual_kernel(float *__restrict__ h, const float *__restrict__
           inp = x[i];
           in_r[c] = inp;
         } else {
-          inp = in_r[c];
+          inp = ip[i];
         }
         if (mix != MIX_RESUME) st_r[c] = x[i];
         x[i] = x[i] + inp;
