@@ -120,5 +120,46 @@ __device__ __forceinline__ void st_release_gpu(int *p, int v) {
   asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// Tagged words: a float and the tag of the stage that wrote it in one 64-bit word (value in
+// the low half), stored and loaded as single 64-bit accesses, so a reader sees either the old
+// word or the new one whole. A reader polls until the tag is the one it expects: the word is
+// its own completion flag, with no fence and no separate counter.
+__device__ __forceinline__ unsigned long long tag_word(float v, uint32_t tag) {
+  return ((unsigned long long)tag << 32) | __float_as_uint(v);
+}
+
+__device__ __forceinline__ void st_tagged(unsigned long long *p, float v, uint32_t tag) {
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(tag_word(v, tag)) : "memory");
+}
+
+// 4 consecutive values (16-byte aligned words p[0..3])
+__device__ __forceinline__ void st_tagged4(unsigned long long *p, const float4 &v, uint32_t tag) {
+  asm volatile("st.relaxed.gpu.global.v2.b64 [%0], {%1, %2};" ::"l"(p), "l"(tag_word(v.x, tag)),
+               "l"(tag_word(v.y, tag))
+               : "memory");
+  asm volatile("st.relaxed.gpu.global.v2.b64 [%0], {%1, %2};" ::"l"(p + 2), "l"(tag_word(v.z, tag)),
+               "l"(tag_word(v.w, tag))
+               : "memory");
+}
+
+// true when the word carries `tag` (v is then its value)
+__device__ __forceinline__ bool ld_tagged(const unsigned long long *p, uint32_t tag, float &v) {
+  unsigned long long w;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(p));
+  v = __uint_as_float((uint32_t)w);
+  return (uint32_t)(w >> 32) == tag;
+}
+
+// true when all 4 words p[0..3] (16-byte aligned) carry `tag`
+__device__ __forceinline__ bool ld_tagged4(const unsigned long long *p, uint32_t tag, float4 &v) {
+  unsigned long long a, b, c, d;
+  asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p));
+  asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(c), "=l"(d) : "l"(p + 2));
+  v = make_float4(__uint_as_float((uint32_t)a), __uint_as_float((uint32_t)b), __uint_as_float((uint32_t)c),
+                  __uint_as_float((uint32_t)d));
+  return (uint32_t)(a >> 32) == tag && (uint32_t)(b >> 32) == tag && (uint32_t)(c >> 32) == tag &&
+         (uint32_t)(d >> 32) == tag;
+}
+
 
 }  // namespace dory

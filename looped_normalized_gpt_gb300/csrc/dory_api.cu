@@ -131,12 +131,15 @@ struct dory_handle {
   float *h2 = nullptr, *h_last = nullptr;  // second hidden buffer (fused path), final rows
   int32_t *hctr = nullptr, *actr = nullptr;  // arrival counters of the fused kernels
   bool fused_ok = false;
-  // persistent batch-1 decode: one block per SM; counters zeroed before each launch:
-  // [0] grid barrier, [1] RoPE entries, [64..) per-kv-head attention item arrivals
+  // persistent batch-1 decode: one block per SM; zeroed before each launch: counters
+  // ([1] RoPE entries, [2] blocks done, [64..) per-kv-head attention item arrivals and
+  // flags), then the tagged words that stages hand on (q/k/v/g row, z, out, mlp)
   bool mega_ok = false;
   int sms = 0;
   int32_t *mega_sync = nullptr;
   size_t mega_sync_bytes = 0;
+  unsigned long long *mega_tq = nullptr, *mega_tz = nullptr, *mega_to = nullptr, *mega_tm = nullptr;
+  float *mega_priv = nullptr;  // per block: its hidden rows (2) and the loop's input row
   MegaStage *mega_stages = nullptr;  // stage list of the launches issued without graphs
   size_t mega_cap = 0;
   // optional trace of the persistent kernel (DORY_MEGA_TRACE=<file>, written at destroy)
@@ -265,6 +268,7 @@ void free_all(dory_t *d) {
   if (d->mega_stages) cudaFree(d->mega_stages);
   d->mega_stages = nullptr;
   if (d->mega_trace) cudaFree(d->mega_trace);
+  if (d->mega_priv) cudaFree(d->mega_priv);
   d->mega_trace = nullptr;
   for (auto &pr : d->tcw)
     for (TcW &w : pr)
@@ -872,6 +876,12 @@ int mega_build(dory_t *d, const StepArgs &a, int32_t *rt, std::vector<MegaStage>
     const float *alpha = nullptr;
     int mix = MIX_NONE;
   } pend;
+  // Stages hand on their outputs as tagged words (tag = the producing stage's index + 1).
+  // The hidden rows and the loop's input row, which every block computes alike, go to each
+  // block's private rows too (1: h, 2: h2, 3: input) and are read back from there.
+  uint32_t tag_q = 0, tag_z = 0, tag_o = 0, tag_m = 0;
+  bool input_here = false;  // the input row was written earlier in this launch
+  auto pv = [&](const float *p) { return p == d->h ? 1 : p == d->h2 ? 2 : 0; };
   auto first_in = [&]() {
     GemvIn g{};
     g.ld = dm.hidden;
@@ -881,6 +891,7 @@ int mega_build(dory_t *d, const StepArgs &a, int32_t *rt, std::vector<MegaStage>
       g.src = d->state;
       g.mix = MIX_RESUME;
       g.h_dst = other;
+      g.hdst_pv = pv(other);
       g.input = d->input;
       g.state = d->state;
       std::swap(cur, other);
@@ -893,20 +904,32 @@ int mega_build(dory_t *d, const StepArgs &a, int32_t *rt, std::vector<MegaStage>
       g.embed = static_cast<const __nv_bfloat16 *>(d->embed);
       g.vocab = dm.vocab;
       g.h_dst = cur;
+      g.hdst_pv = pv(cur);
       return g;
     }
     if (!pend.on) {
       g.mode = IN_PLAIN;
       g.src = cur;
+      g.src_pv = pv(cur);
       return g;
     }
     g.mode = IN_RESID;
     g.src = cur;
+    g.src_pv = pv(cur);
     g.out = d->out;
+    g.out_t = d->mega_to;
+    g.out_tag = tag_o;
     g.alpha = pend.alpha;
     g.mix = pend.mix;
     g.h_dst = other;
+    g.hdst_pv = pv(other);
     g.input = d->input;
+    if (pend.mix == MIX_BEGIN) {
+      g.input_pv = 3;
+      input_here = true;
+    } else if (pend.mix == MIX_LOOP && input_here) {
+      g.input_pv = 3;
+    }
     g.state = d->state;
     std::swap(cur, other);
     pend.on = false;
@@ -922,6 +945,17 @@ int mega_build(dory_t *d, const StepArgs &a, int32_t *rt, std::vector<MegaStage>
     st.R = mega_chunk_rows(K, pair > 0);
     st.in = in;
     st.Y = Y;
+    const uint32_t tag = (uint32_t)out.size() + 1;
+    if (Y == d->qkvg) {
+      st.Yt = d->mega_tq;
+      tag_q = tag;
+    } else if (Y == d->out) {
+      st.Yt = d->mega_to;
+      tag_o = tag;
+    } else if (Y == d->mlp) {
+      st.Yt = d->mega_tm;
+      tag_m = tag;
+    }
     st.ep = ep;
     out.push_back(st);
   };
@@ -934,18 +968,22 @@ int mega_build(dory_t *d, const StepArgs &a, int32_t *rt, std::vector<MegaStage>
       MegaStage at{};
       at.kind = MK_ATTN;
       at.ring = ring;
-      at.qkvg = d->qkvg;
+      at.qkvg_t = d->mega_tq;
+      at.qtag = tag_q;
       at.sq = L.sq;
       at.rope_kind = L.sliding ? 0 : 1;
       at.sg = L.sg;
-      at.z = d->z;
+      at.zt = d->mega_tz;
       at.part = d->part;
       const long keys = ring.window == INT_MAX ? (long)ring.cap : std::min<long>(ring.window, ring.cap);
       at.maxblk = (int)(keys / MEGA_AK + 2);
+      tag_z = (uint32_t)out.size() + 1;
       out.push_back(at);
       GemvIn in{};
       in.mode = IN_NORM;
       in.src = d->z;
+      in.src_t = d->mega_tz;
+      in.src_tag = tag_z;
       in.ld = q_size;
       gemv(L.wo, dm.hidden, q_size, 0, in, d->out, EpiArgs{EPI_STORE, nullptr, nullptr, 0});
     } else {
@@ -953,6 +991,8 @@ int mega_build(dory_t *d, const StepArgs &a, int32_t *rt, std::vector<MegaStage>
       GemvIn in{};
       in.mode = IN_NORM;
       in.src = d->mlp;
+      in.src_t = d->mega_tm;
+      in.src_tag = tag_m;
       in.ld = dm.ffn;
       gemv(L.wdown, dm.hidden, dm.ffn, 0, in, d->out, EpiArgs{EPI_STORE, nullptr, nullptr, 0});
     }
@@ -970,6 +1010,14 @@ int mega_build(dory_t *d, const StepArgs &a, int32_t *rt, std::vector<MegaStage>
   for (int li = n_in + n_rec; li < n_all; li++) layer(li, 0, MIX_NONE);  // f32 rings: the same row is rewritten
   gemv(d->head, dm.vocab, dm.hidden, 0, first_in(), d->logits, EpiArgs{EPI_SCALE, d->logit_scale, nullptr, 0});
   *h_last = cur;
+  // DORY_MEGA_STALL=1 (tests): the first row-norm input awaits a tag that no stage writes,
+  // so that its wait runs out (bounded by DORY_MEGA_SPIN) and the failure path runs
+  if (const char *e = getenv("DORY_MEGA_STALL"); e && e[0] == '1')
+    for (MegaStage &x : out)
+      if (x.kind == MK_GEMV && x.in.mode == IN_NORM) {
+        x.in.src_tag = 0xffffffffu;
+        break;
+      }
   if (d->mega_trace) {
     d->mega_trace_desc.clear();
     for (const MegaStage &x : out) {
@@ -1001,6 +1049,8 @@ int issue_mega(dory_t *d, const StepArgs &a, int32_t *rt, const MegaStage *stage
   m.aflag = d->mega_sync + 64 + d->dims.nk;
   m.err = d->dev_err;
   m.seq_pos = d->d_seq_pos;
+  m.priv = d->mega_priv;
+  m.priv_stride = 3 * d->dims.hidden;
   m.adv_seq = a.aseq[0];
   m.adv_cnt = a.acnt[0];
   m.trace = (size_t)nstages <= d->mega_trace_stages ? d->mega_trace : nullptr;
@@ -1496,7 +1546,9 @@ int dory_create(const dory_config *cfg, const dory_weights *w, void *stream, dor
                a_lg2 = areserve((size_t)d->Tstep * dm.vocab * 4),
                a_sp = areserve((size_t)cfg->max_seqs * 4), a_rows = areserve((size_t)ROW_TABLE * T * 4),
                a_zero = areserve((size_t)cfg->max_seqs * 4), a_err = areserve(256);
-  const size_t ms_bytes = (size_t)(64 + dm.nk + dm.nk * MEGA_FLAGS) * 4, a_ms = areserve(ms_bytes);
+  const size_t ms_ints = ((size_t)(64 + dm.nk + dm.nk * MEGA_FLAGS) * 4 + 15) & ~(size_t)15;
+  const size_t ms_words = (size_t)(2 * q_size + 2 * kv_size) + q_size + dm.hidden + dm.ffn;
+  const size_t ms_bytes = ms_ints + ms_words * 8, a_ms = areserve(ms_bytes);
   const size_t a_stab = areserve((size_t)d->n_flat_slots * 3 * 8), a_drop = areserve((size_t)d->n_flat_slots * 4),
                a_top = areserve(4);
   if (cudaMalloc(&d->act, ab) != cudaSuccess) {
@@ -1520,6 +1572,10 @@ int dory_create(const dory_config *cfg, const dory_weights *w, void *stream, dor
   }
   d->mega_sync = reinterpret_cast<int32_t *>(A + a_ms);
   d->mega_sync_bytes = ms_bytes;
+  d->mega_tq = reinterpret_cast<unsigned long long *>(A + a_ms + ms_ints);
+  d->mega_tz = d->mega_tq + 2 * q_size + 2 * kv_size;
+  d->mega_to = d->mega_tz + q_size;
+  d->mega_tm = d->mega_to + dm.hidden;
   {
     // the persistent decode kernel: bf16 weights, f32 rings, rows that stream as whole
     // 16-byte runs and fit a ring slot, a block's input row and attention scratch within
@@ -1535,7 +1591,8 @@ int dory_create(const dory_config *cfg, const dory_weights *w, void *stream, dor
               mega_chunk_rows((int)kmax, false) >= 1;
     // the merge's per-warp partials of a kv head's query heads
     if ((size_t)mega_consumer_warps() * rep * (dm.hd + 2) > mega_work_floats()) ok = false;
-    if (dm.hidden > 6144 || dm.ffn > 6144 || q_size > 6144) ok = false;  // three 16-byte columns per thread
+    // input rows of at most six float4 chunks a thread, a residual (hidden row) of at most two
+    if (dm.hidden > 2048 || dm.ffn > 6144 || q_size > 6144) ok = false;
     const int nmax = std::max(std::max(dm.vocab, dm.ffn), 2 * q_size + 2 * kv_size);
     if (d->sms > 0 && (nmax + d->sms - 1) / d->sms > mega_max_rows_per_block()) ok = false;
     for (const OrdInfo &o : d->ords) {
@@ -1546,6 +1603,11 @@ int dory_create(const dory_config *cfg, const dory_weights *w, void *stream, dor
     const char *e = getenv("DORY_MEGA");
     if (e && e[0] == '0') ok = false;
     d->mega_ok = ok && mega_supported(dm.hd, d->sms);
+    if (d->mega_ok && cudaMalloc(&d->mega_priv, (size_t)d->sms * 3 * dm.hidden * 4) != cudaSuccess) {
+      cudaGetLastError();
+      d->mega_priv = nullptr;
+      d->mega_ok = false;
+    }
     if (const char *pe = getenv("DORY_MEGA_PREFETCH")) d->mega_prefetch = std::max(0, atoi(pe));
     if (const char *pe = getenv("DORY_MEGA_LEAD")) d->mega_lead = std::max(0, atoi(pe));
     if (const char *pe = getenv("DORY_MEGA_INFLIGHT")) d->mega_inflight = std::max(0, atoi(pe));

@@ -7,12 +7,20 @@
 // in stage order, asks L2 for the bytes about two chunks ahead (cp.async.bulk.prefetch),
 // and copies chunks into a ring of shared-memory slots with cp.async.bulk, completion on one
 // mbarrier per slot. It never waits for activations, so HBM keeps streaming the next stages'
-// weights while the consumers wait at a grid barrier or run attention. Warps 1..8 are the
+// weights while the consumers wait for their inputs or run attention. Warps 1..8 are the
 // consumers; each awaits only the chunks that hold its rows, and a chunk's slot is free once
-// they have all arrived (the first of them arrives for the consumers without a row). Per
-// stage the consumers
-//   * copy the stage's descriptor into shared memory while their first thread waits until
-//     every block has finished the stage before (a counter in global memory);
+// they have all arrived (the first of them arrives for the consumers without a row).
+//
+// There is no grid barrier. A stage's outputs (GEMV rows, the attention output z) are
+// tagged words: value and the stage's index + 1 in one 64-bit store. A consumer thread loads
+// the words it needs and polls again until each carries the tag it expects, so a stage
+// starts as soon as its own inputs exist, one L2 round trip after the last of them was
+// stored, with no fence and no counter. The words are zeroed before each launch, and a
+// buffer is reused only by a stage that depends on every reader of its previous contents.
+// Rows that every block computes alike (the hidden row, the loop's input row) are kept in a
+// private area per block and read back by the thread that wrote them. Per stage the
+// consumers
+//   * copy the stage's descriptor into shared memory;
 //   * GEMV: build the input row in shared memory (the embedding, a row norm, or the nGPT
 //     residual with the loop mix), then take the rows two at a time (or a gate/up pair) per
 //     warp (bf16 weights, f32 sums; lanes split the row into 16-byte columns), park the lane
@@ -23,11 +31,11 @@
 //     (q = s_q^2 q^), and in the item that holds the row's own position one warp rotates and
 //     normalises the new key, puts key and value into the tile and writes them (and the
 //     position tag) to the ring; warp h then scores (lane = key), takes the item's softmax and
-//     value sum; the last item of a kv head merges the items (all partials loaded at once)
+//     value sum; one block per query head (or the last item of a kv head) merges the items
 //     and applies the output gate.
 // Every wait is bounded. When one runs out the block records error 6, stops at the next
-// team-wide check, lets its copies in flight land and returns; the other blocks then stop
-// at their next grid barrier.
+// team-wide check, lets its copies in flight land and returns; the other blocks then give up
+// waiting for its words. The last block to finish advances the row's position.
 #include <algorithm>
 #include <climits>
 
@@ -52,7 +60,7 @@ constexpr uint32_t WORK = 32 * 1024;              // input row, or attention til
 constexpr int AK = MEGA_AK;                       // positions per attention item
 constexpr int ERR_MEGA = 6;                       // dev_err: a wait of the persistent kernel ran out
 static_assert(EPI_ROWS == 32 * MW, "a consumer thread holds one row's epilogue scales");
-static_assert(sizeof(MegaStage) % 4 == 0 && sizeof(MegaStage) / 4 < 32 * MW, "stage copy by the team");
+static_assert(sizeof(MegaStage) % 4 == 0 && sizeof(MegaStage) / 4 <= 32 * MW, "stage copy by the team");
 
 struct Ctl {
   volatile int abort;  // a wait ran out somewhere in the block
@@ -108,7 +116,7 @@ __device__ __forceinline__ bool team_ok(const WarpTeam &tm, Ctl &ctl) {
   return ctl.decision == 0;
 }
 
-// Wait until `*ctr >= target` (blocks past a stage, or RoPE entries written).
+// Wait until `*ctr >= target` (the RoPE entries written).
 __device__ bool team_wait_counter(const WarpTeam &tm, const int *ctr, int target, Ctl &ctl, int *err,
                                   uint32_t limit) {
   if (tm.tid() == 0) {
@@ -126,11 +134,30 @@ __device__ bool team_wait_counter(const WarpTeam &tm, const int *ctr, int target
   return ctl.decision == 0;
 }
 
-// The block's writes of this stage, then one arrival (release orders them all: the
-// barrier before it makes every thread's writes precede the first thread's release).
-__device__ __forceinline__ void grid_arrive(const WarpTeam &tm, int *ctr) {
-  tm.sync();
-  if (tm.tid() == 0) red_release_gpu_add(ctr, 1);
+
+// Words p[off[i]] of a tagged row into v[i], re-polling those that do not carry `tag` yet.
+// False when the polls ran out or the block stopped.
+template <int N>
+__device__ __forceinline__ bool await_words(const unsigned long long *p, const int (&off)[N], uint32_t tag,
+                                            float (&v)[N], const Ctl &ctl, uint32_t limit) {
+  uint32_t pend = 0;
+#pragma unroll
+  for (int i = 0; i < N; i++)
+    if (!ld_tagged(p + off[i], tag, v[i])) pend |= 1u << i;
+  for (uint32_t k = 0; pend && k < limit && !ctl.abort; k++) {
+#pragma unroll
+    for (int i = 0; i < N; i++)
+      if (((pend >> i) & 1u) && ld_tagged(p + off[i], tag, v[i])) pend &= ~(1u << i);
+  }
+  return pend == 0;
+}
+
+// 4 consecutive tagged words p[0..3] (16-byte aligned) into v
+__device__ __forceinline__ bool await4(const unsigned long long *p, uint32_t tag, float4 &v, const Ctl &ctl,
+                                       uint32_t limit) {
+  for (uint32_t k = 0; k <= limit && !ctl.abort; k++)
+    if (ld_tagged4(p, tag, v)) return true;
+  return false;
 }
 
 // ---- producer -----------------------------------------------------------------------------
@@ -253,7 +280,7 @@ constexpr int PEND = 8;  // rows a warp parks before it reduces them
 
 template <bool DUAL>
 __device__ __forceinline__ void flush_rows(const MegaStage &st, int rb, int np, const float *pg, const float *pu,
-                                           const int *prow, const float (*epi)[EPI_ROWS]) {
+                                           const int *prow, const float (*epi)[EPI_ROWS], uint32_t tag) {
   const int lane = threadIdx.x & 31, i = lane >> 2, q = lane & 3;
   __syncwarp();
   const float4 *g4 = reinterpret_cast<const float4 *>(pg + i * 32 + q * 8);
@@ -282,7 +309,8 @@ __device__ __forceinline__ void flush_rows(const MegaStage &st, int rb, int np, 
     } else {
       y = g;
     }
-    st.Y[rb + jr] = y;
+    if (st.Yt) st_tagged(st.Yt + rb + jr, y, tag);
+    else st.Y[rb + jr] = y;
   }
   __syncwarp();  // the parked sums may be overwritten
 }
@@ -345,7 +373,7 @@ __device__ void gemv_rows(const WarpTeam &tm, const MegaStage &st, int rb, int r
         if (DUAL) pu[np * 32 + lane] = (b0.x + b0.y) + (b1.x + b1.y);
         if (lane == 0) prow[np] = gi * NR + r;
         if (++np == PEND) {
-          flush_rows<DUAL>(st, rb, np, pg, pu, prow, epi);
+          flush_rows<DUAL>(st, rb, np, pg, pu, prow, epi, s + 1);
           np = 0;
         }
       }
@@ -357,13 +385,13 @@ __device__ void gemv_rows(const WarpTeam &tm, const MegaStage &st, int rb, int r
     if (lane == 0 && !ctl.abort) mbar_arrive_n(smem_addr(&empty[sl]), j == 0 ? MW - ng + 1 : 1);
     tr.add(s, 9, tr.clk() - t1);
   }
-  if (np > 0) flush_rows<DUAL>(st, rb, np, pg, pu, prow, epi);
+  if (np > 0) flush_rows<DUAL>(st, rb, np, pg, pu, prow, epi, s + 1);
   tr.flush(s);
 }
 
-template <int KC>
-__device__ __forceinline__ void input_row(const WarpTeam &tm, const GemvIn &in, int K, float *xs) {
-  build_input<1, KC, WarpTeam, true>(tm, in, 1, K, xs, blockIdx.x == 0);
+template <int KC, bool RESID>
+__device__ __forceinline__ bool input_row(const WarpTeam &tm, const GemvIn &in, int K, float *xs, const TagWait &tw) {
+  return build_input<1, KC, WarpTeam, true, true, RESID>(tm, in, 1, K, xs, blockIdx.x == 0, &tw);
 }
 
 // Returns false (team-uniformly) when the block has stopped.
@@ -388,9 +416,13 @@ __device__ __noinline__ bool gemv_stage(const WarpTeam &tm, const MegaArgs &a, c
   }
   const int kc = (K / 4 + tm.size() - 1) / tm.size();  // float4 chunks per thread
   // K is at most 6144 (the host's limit): 2 or 6 float4 chunks a thread. Two forms only: with
-  // four (2, 4, 6, 8) the stage's register allocation spilled and a token took 4.4% longer.
-  if (kc <= 2) input_row<2>(tm, st.in, K, xs);
-  else input_row<6>(tm, st.in, K, xs);
+  // four (2, 4, 6, 8) the stage's register allocation spilled and a token took 4.4% longer;
+  // a residual of 6 chunks (two rows of tagged words awaited at once) spilled too, inline or
+  // called, so hidden rows are at most 2048 wide here.
+  const TagWait tw{&ctl.abort, a.spin_limit, a.priv + (size_t)b * a.priv_stride};
+  // (a residual row is a hidden row: at most 2048, the host's limit)
+  const bool in_ok = kc <= 2 ? input_row<2, true>(tm, st.in, K, xs, tw) : input_row<6, false>(tm, st.in, K, xs, tw);
+  if (!in_ok) flag_error(ctl, a.err);  // the rows below see the stop and skip their work
   if (st.ep.mode != EPI_STORE) {
     if (has_e) {
       epi[0][ei] = e0;
@@ -426,8 +458,8 @@ __device__ __forceinline__ float *part_ml(const MegaStage &st, int nk, int rep, 
 // meet in shared memory `scr` and the first nq threads finish: y = sum o e^(m - M) / sum l
 // e^(m - M), z = y * sigmoid(g * s_g^2).
 template <int HD>
-__device__ __forceinline__ void merge_items(const WarpTeam &tm, const MegaStage &st, const Dims &d, int kh, int nblk,
-                                         float *scr, const Tracer &tr) {
+__device__ __forceinline__ void merge_items(const WarpTeam &tm, const MegaArgs &a, const MegaStage &st, const Dims &d,
+                                            int kh, int nblk, int s, float *scr, Ctl &ctl, const Tracer &tr) {
   const long long t_in = tr.clk();
   constexpr int IB = 9;  // items a thread loads per round
   const int rep = d.nh / d.nk, nq = rep * HD / 4;
@@ -446,8 +478,9 @@ __device__ __forceinline__ void merge_items(const WarpTeam &tm, const MegaStage 
     const size_t c = col0 + (size_t)q * 4;
     float4 gr = make_float4(0.f, 0.f, 0.f, 0.f), sg = gr;
     if (g == 0 && act) {
-      gr = __ldcg(reinterpret_cast<const float4 *>(st.qkvg + (size_t)(d.nh + 2 * d.nk) * HD + c));
       sg = __ldg(reinterpret_cast<const float4 *>(st.sg + c));
+      if (!await4(st.qkvg_t + (size_t)(d.nh + 2 * d.nk) * HD + c, st.qtag, gr, ctl, a.spin_limit))
+        flag_error(ctl, a.err);
     }
     for (int i0 = g; act && i0 < nblk; i0 += IB * groups) {
       float4 o[IB];
@@ -500,7 +533,7 @@ __device__ __forceinline__ void merge_items(const WarpTeam &tm, const MegaStage 
       z.y = Ax.y * inv * sigmoidf_(gr.y * sg.y);
       z.z = Ax.z * inv * sigmoidf_(gr.z * sg.z);
       z.w = Ax.w * inv * sigmoidf_(gr.w * sg.w);
-      *reinterpret_cast<float4 *>(st.z + c) = z;
+      st_tagged4(st.zt + c, z, s + 1);
     }
     tm.sync();
   }
@@ -522,9 +555,10 @@ __device__ __noinline__ bool merge_head(const WarpTeam &tm, const MegaArgs &a, c
   const int t = tm.tid(), q = t % NQ, g = t / NQ;
   const size_t c = (size_t)h * HD + (size_t)q * 4;
   float4 gr = make_float4(0.f, 0.f, 0.f, 0.f), sg = gr;
-  if (g == 0) {  // the gate inputs, in flight while the items finish
-    gr = __ldcg(reinterpret_cast<const float4 *>(st.qkvg + (size_t)(d.nh + 2 * d.nk) * HD + c));
+  if (g == 0) {  // the gate inputs, while the items finish
     sg = __ldg(reinterpret_cast<const float4 *>(st.sg + c));
+    if (!await4(st.qkvg_t + (size_t)(d.nh + 2 * d.nk) * HD + c, st.qtag, gr, ctl, a.spin_limit))
+      flag_error(ctl, a.err);
   }
   // each item's partials as soon as it has published them: the flag is read with acquire
   // loads, so the partial loads that follow it see the item's stores; only the last item's
@@ -588,7 +622,7 @@ __device__ __noinline__ bool merge_head(const WarpTeam &tm, const MegaArgs &a, c
     z.y = Ax.y * inv * sigmoidf_(gr.y * sg.y);
     z.z = Ax.z * inv * sigmoidf_(gr.z * sg.z);
     z.w = Ax.w * inv * sigmoidf_(gr.w * sg.w);
-    *reinterpret_cast<float4 *>(st.z + c) = z;
+    st_tagged4(st.zt + c, z, s + 1);
   }
   return true;
 }
@@ -662,7 +696,7 @@ __device__ __noinline__ bool attn_stage(const WarpTeam &tm, const MegaArgs &a, c
   char *slot = st.ring.base + (size_t)seq * st.ring.seq_stride + st.ring.off;
   int32_t *tags = reinterpret_cast<int32_t *>(slot + st.ring.L.tags);
   float *Kg = reinterpret_cast<float *>(slot + st.ring.L.k), *Vg = reinterpret_cast<float *>(slot + st.ring.L.v);
-  const float *qkvg = st.qkvg;
+  const unsigned long long *qkvg = st.qkvg_t;
   float *Ks = work, *Vs = work + AK * HD;
   const int cw = tm.warp(), lane = threadIdx.x & 31;
   const int kw = rep % MW;  // the warp that prepares the new key and value
@@ -693,12 +727,21 @@ __device__ __noinline__ bool attn_stage(const WarpTeam &tm, const MegaArgs &a, c
     for (int h = cw; h < rep; h += MW) {
       const size_t off = (size_t)(kh * rep + h) * HD;
       float x[PP], y[PP], sx[PP], sy[PP], ss = 0.f;
+      int wo[2 * PP];
+      float wv[2 * PP];
 #pragma unroll
       for (int u = 0; u < PP; u++) {  // the projection and the s_q^2 entries in one round trip
         const int j = lane + 32 * u;
-        const float a0 = __ldcg(qkvg + off + j), b0 = __ldcg(qkvg + off + j + HALF);
         sx[u] = __ldg(st.sq + off + j);
         sy[u] = __ldg(st.sq + off + j + HALF);
+        wo[2 * u] = (int)off + j;
+        wo[2 * u + 1] = (int)off + j + HALF;
+      }
+      if (!await_words(qkvg, wo, st.qtag, wv, ctl, a.spin_limit)) flag_error(ctl, a.err);
+#pragma unroll
+      for (int u = 0; u < PP; u++) {
+        const int j = lane + 32 * u;
+        const float a0 = wv[2 * u], b0 = wv[2 * u + 1];
         x[u] = a0 * rc[j] - b0 * rsn[j];
         y[u] = b0 * rc[j] + a0 * rsn[j];
         ss += x[u] * x[u] + y[u] * y[u];
@@ -715,17 +758,28 @@ __device__ __noinline__ bool attn_stage(const WarpTeam &tm, const MegaArgs &a, c
     // the new key (rotated, normalised) and value of kv head kh
     float kx[PP], ky[PP], vx[PP], vy[PP];
     if (has_p && cw == kw) {
-      const size_t ko = (size_t)(d.nh + kh) * HD, vo = (size_t)(d.nh + d.nk + kh) * HD;
+      const int ko = (d.nh + kh) * HD, vo = (d.nh + d.nk + kh) * HD;
       float ss = 0.f;
+      int wo[4 * PP];
+      float wv[4 * PP];
 #pragma unroll
       for (int u = 0; u < PP; u++) {
         const int j = lane + 32 * u;
-        const float a0 = __ldcg(qkvg + ko + j), b0 = __ldcg(qkvg + ko + j + HALF);
+        wo[4 * u] = ko + j;
+        wo[4 * u + 1] = ko + j + HALF;
+        wo[4 * u + 2] = vo + j;
+        wo[4 * u + 3] = vo + j + HALF;
+      }
+      if (!await_words(qkvg, wo, st.qtag, wv, ctl, a.spin_limit)) flag_error(ctl, a.err);
+#pragma unroll
+      for (int u = 0; u < PP; u++) {
+        const int j = lane + 32 * u;
+        const float a0 = wv[4 * u], b0 = wv[4 * u + 1];
         kx[u] = a0 * rc[j] - b0 * rsn[j];
         ky[u] = b0 * rc[j] + a0 * rsn[j];
         ss += kx[u] * kx[u] + ky[u] * ky[u];
-        vx[u] = __ldcg(qkvg + vo + j);
-        vy[u] = __ldcg(qkvg + vo + j + HALF);
+        vx[u] = wv[4 * u + 2];
+        vy[u] = wv[4 * u + 3];
       }
       ss = warp_sum(ss);
       const float inv = 1.f / sqrtf(ss + DORY_EPS);
@@ -783,7 +837,7 @@ __device__ __noinline__ bool attn_stage(const WarpTeam &tm, const MegaArgs &a, c
     tr.add(s, 10, t1 - t0);
     tr.mark(s, 7);
     if (ctl.last) {
-      merge_items<HD>(tm, st, d, kh, nblk, Ks, tr);
+      merge_items<HD>(tm, a, st, d, kh, nblk, s, Ks, ctl, tr);
       tr.add(s, 11, tr.clk() - t1);
     }
   }
@@ -793,15 +847,17 @@ __device__ __noinline__ bool attn_stage(const WarpTeam &tm, const MegaArgs &a, c
     tr.add(s, 11, tr.clk() - tm0);
   }
   tr.flush(s);
+  // the merge's last warp may still read the descriptor and the scratch: the next stage
+  // copies its descriptor over this one
+  tm.sync();
   return true;
 }
 
-// Threads 1.. of the team copy a stage's descriptor into shared memory (thread 0 is waiting
-// at the grid barrier meanwhile; the barrier's team sync publishes the copy).
+// The team copies a stage's descriptor into shared memory.
 __device__ __forceinline__ void copy_stage(const WarpTeam &tm, const MegaStage *src, MegaStage *dst) {
   constexpr int n = sizeof(MegaStage) / 4;
-  const int i = tm.tid() - 1;
-  if (i >= 0 && i < n) reinterpret_cast<int *>(dst)[i] = __ldg(reinterpret_cast<const int *>(src) + i);
+  const int i = tm.tid();
+  if (i < n) reinterpret_cast<int *>(dst)[i] = __ldg(reinterpret_cast<const int *>(src) + i);
 }
 
 // ---- the kernel ---------------------------------------------------------------------------
@@ -862,14 +918,9 @@ __global__ void __launch_bounds__(MTHREADS, 1) mega_decode_kernel(const __grid_c
   bool ok = true, rope_ready = false;
   for (int s = 0; s < a.nstages && ok; s++) {
     tr.mark(s, 0);
-    copy_stage(tm, a.stages + s, &sst);
-    if (!team_wait_counter(tm, a.sync, s * G, ctl, a.err, a.spin_limit)) {
-      ok = false;
-      break;
-    }
+    copy_stage(tm, a.stages + s, &sst);  // (every stage ends with a team sync)
+    tm.sync();
     tr.mark(s, 1);
-    // every reader of the position has passed: the last stage advances it
-    if (s == a.nstages - 1 && b == 0 && tm.tid() == 0) a.seq_pos[a.adv_seq] += a.adv_cnt;
     if (sst.kind == MK_GEMV) {
       ok = gemv_stage(tm, a, sst, s, c, ring, full, empty, work, epi, ctl);
     } else {
@@ -885,10 +936,11 @@ __global__ void __launch_bounds__(MTHREADS, 1) mega_decode_kernel(const __grid_c
       ok = attn_stage<HD>(tm, a, sst, s, work, &abar, aph, qs, rope_s, ctl);
     }
     tr.mark(s, 4);
-    if (ok && s + 1 < a.nstages) grid_arrive(tm, a.sync);
   }
   // an attention copy may still be in flight after a stop
   if (!ok && tm.tid() == 0 && aph > 0) mbar_wait(smem_addr(&abar), (aph - 1) & 1);
+  // every block read the position at its start: the last block done advances it
+  if (ok && tm.tid() == 0 && atom_add_acq_rel_gpu(a.sync + 2, 1) == G - 1) a.seq_pos[a.adv_seq] += a.adv_cnt;
 }
 
 }  // namespace

@@ -144,6 +144,15 @@ struct GemvIn {
   const int32_t *ids;            // IN_EMBED: token ids [T]; an id outside [0, vocab) gives a zero row
   const __nv_bfloat16 *embed;    // IN_EMBED: table [vocab][K]
   int vocab;
+  // Persistent kernel only (zero elsewhere). Rows that earlier stages of the same launch
+  // wrote as tagged words (value, tag) are awaited word by word until each carries the
+  // producing stage's tag: src_t replaces src, out_t replaces out.
+  const unsigned long long *src_t, *out_t;
+  uint32_t src_tag, out_tag;
+  // 1 + the row of the block's private area that holds src / input (the block wrote it
+  // itself earlier in the launch), or 0: read the shared row; hdst_pv / input_pv: also store
+  // the new hidden row / the mix's input row there (every block, not only the leading one)
+  int src_pv, hdst_pv, input_pv;
 };
 
 // Per-head epilogue of the q/k/v/g projection (RoPE, justnorm, s_q^2, ring write).
@@ -217,8 +226,9 @@ cudaError_t launch_attention_tma_q8(const KvMaps &m, const float *qkvg, int ldq,
 
 enum MegaKind { MK_GEMV = 0, MK_ATTN = 1 };
 
-// One stage of the persistent decode kernel. Stages run in order; every block finishes a
-// stage before any block starts the next.
+// One stage of the persistent decode kernel. Stages run in order in every block. A stage
+// waits for the words it reads from earlier stages (tagged with the producing stage), not
+// for the other blocks as a whole.
 struct MegaStage {
   int kind;
   // MK_GEMV: Y[n] = epilogue(W[n] . x) for n < N, x built from `in`; bf16 W [N(+pair)][K]
@@ -228,15 +238,17 @@ struct MegaStage {
   long pair;      // > 0: SwiGLU, up rows at n + pair
   GemvIn in;
   float *Y;
+  unsigned long long *Yt;  // non-null: Y goes here instead, each value tagged with the stage (index + 1)
   EpiArgs ep;
   // MK_ATTN: from the raw q/k/v/g row, RoPE + justnorm of q and k, q * s_q^2, the ring
   // write of the new k and v, windowed attention over `ring`, the gate, into z
   Ring ring;
-  const float *qkvg;
+  const unsigned long long *qkvg_t;  // the q/k/v/g row as tagged words of stage qtag - 1
+  uint32_t qtag;
   const float *sq;
   int rope_kind;  // 0 sliding, 1 full (which RoPE base)
   const float *sg;
-  float *z;
+  unsigned long long *zt;  // z as tagged words (the stage's index + 1)
   float *part;    // [nk][maxblk][REP][hd + 2] item partials
   int maxblk;     // items per kv head at most
 };
@@ -248,11 +260,13 @@ struct MegaArgs {
   Rows rows;                // one row
   double theta_s, theta_f;  // RoPE bases of sliding and full layers
   float *rope;              // [2][hd] cos | sin of the row's position
-  int *sync;                // [0] blocks past each stage, [1] RoPE entries ready; zero at launch
+  int *sync;                // [1] RoPE entries ready, [2] blocks done; zero at launch
   int *actr;                // [nk] attention item arrivals; zero at launch
   int *aflag;               // [nk][MEGA_FLAGS] attention items done (stage + 1); zero at launch
   int *err;
-  int32_t *seq_pos;         // advanced by `adv` at the last stage
+  int32_t *seq_pos;         // advanced by `adv` once every block is done
+  float *priv;              // per block: priv_stride floats of rows only that block reads
+  int priv_stride;
   int adv_seq, adv_cnt;
   unsigned long long *trace;  // null, or [nstages][grid][MEGA_TRACE_EVENTS] %globaltimer stamps
   int prefetch_ahead;         // bytes per block the producer asks L2 for ahead of its copies
@@ -262,7 +276,7 @@ struct MegaArgs {
 };
 
 // Stamps per (stage, block) of the persistent kernel's optional trace: 0 stage entered,
-// 1 grid barrier passed, 2 input row built, 3 chunks or attention items done, 4 stage done;
+// 1 stage descriptor copied, 2 input row built, 3 chunks or attention items done, 4 stage done;
 // from the producer warp: 5 first chunk of the stage issued, 6 last chunk issued; 7 the
 // stage's first chunk has landed (consumers); 8..11 SM cycles the first consumer thread
 // spent over the stage's chunks waiting for a slot, reducing, at the team barrier, and in

@@ -115,11 +115,11 @@ def test_group_sizes_prefill_chunks_and_decode(nh, nk, hd):
 
 
 def test_a_wait_that_runs_out_is_reported_and_the_handle_recovers(monkeypatch):
-    """The persistent kernel's grid-barrier wait bounded to one poll (DORY_MEGA_SPIN, read at
-    each launch when steps are not graph replays): a block gives up at its first barrier, the
-    kernel stops and returns, and the next synchronising call reports DORY_EWAIT with code 6
-    once. With the limit back, the sequence reset and its prompt run again, the same handle
-    matches the oracle."""
+    """A stage of the persistent kernel awaits words that nothing writes (DORY_MEGA_STALL) with
+    its polls bounded (DORY_MEGA_SPIN; both read when a step is built, every step without
+    graphs): its blocks give up, the others give up waiting for them, the kernel returns, and
+    the next synchronising call reports DORY_EWAIT with code 6 once. With both unset, the
+    sequence reset and its prompt run again, the same handle matches the oracle."""
     from looped_normalized_gpt_gb300 import DoryError
     from oracle import dory_oracle as O
 
@@ -130,13 +130,15 @@ def test_a_wait_that_runs_out_is_reported_and_the_handle_recovers(monkeypatch):
         ids = synth.token_ids(3006, 0, 48, cfg.vocab)
         P.prefill(0, ids[:40], 2, "last")
         P.decode([0], [int(ids[40])], 2)
-        monkeypatch.setenv("DORY_MEGA_SPIN", "1")
+        monkeypatch.setenv("DORY_MEGA_SPIN", "4096")
+        monkeypatch.setenv("DORY_MEGA_STALL", "1")
         P.gpu.decode_step([int(ids[41])], [0], 2)
         assert P.gpu.stats()["launches"] == 1
         with pytest.raises(DoryError) as e:
             P.gpu.logits(0)
         assert e.value.code == -6 and "code 6" in str(e.value)
         monkeypatch.delenv("DORY_MEGA_SPIN")
+        monkeypatch.delenv("DORY_MEGA_STALL")
         P.gpu.reset(0)
         P.states[0] = O.SeqState()
         P.max_hidden_err = 0.0
