@@ -4,36 +4,10 @@
 // a block) given as a template parameter.
 #pragma once
 
-#include "async.cuh"
 #include "kernels.h"
 #include "team.cuh"
 
 namespace dory {
-
-// How a stage of the persistent kernel awaits tagged rows: the block's stop flag, the polls
-// of a word before it gives up, and the block's private rows.
-struct TagWait {
-  const volatile int *abort;
-  uint32_t limit;
-  float *priv;
-};
-
-// Chunks tid + j * nt (< nch) of a row of tagged words into v, re-polling the chunks whose
-// words do not all carry `tag` yet. False when the polls ran out or the block stopped.
-template <int KC>
-__device__ __forceinline__ bool await_row(const unsigned long long *src, uint32_t tag, int tid, int nt, int nch,
-                                          float4 (&v)[KC], const TagWait &tw) {
-  for (uint32_t i = 0; i <= tw.limit && !*tw.abort; i++) {
-    bool all = true;
-#pragma unroll
-    for (int j = 0; j < KC; j++) {
-      const int c = tid + j * nt;
-      if (c < nch) all &= ld_tagged4(src + 4 * (size_t)c, tag, v[j]);
-    }
-    if (all) return true;
-  }
-  return false;
-}
 
 // Prologue: the team's input rows xs[t][K] from the previous kernels' outputs. Each
 // thread owns the float4 chunks tid + j * (team size) of a row (KC of them at most) and loads
@@ -43,19 +17,11 @@ __device__ __forceinline__ bool await_row(const unsigned long long *src, uint32_
 // chunk c at (c & 1) * K / 8 + c / 2, so that a lane reading the 8 inputs of a 16-byte
 // weight column reads float4 u of each half: consecutive lanes, consecutive addresses
 // (the plain layout puts a lane's two float4 loads 32 bytes apart, two-way bank conflicts).
-//
-// TAGGED (persistent kernel, one row): rows of earlier stages of the launch are tagged words
-// (in.src_t, in.out_t), awaited word by word; rows the block wrote itself come from its
-// private area (tw->priv), where every block also stores the new hidden and input rows.
-// Returns false when a tagged wait ran out or the block stopped.
-// RESID = false leaves out the residual and the mix (the caller passes no IN_RESID row).
-template <int TT, int KC, typename Team, bool HALVES = false, bool TAGGED = false, bool RESID = true>
-__device__ bool build_input(const Team &tm, const GemvIn &in, int T, int K, float *xs, bool lead,
-                            const TagWait *tw = nullptr) {
+template <int TT, int KC, typename Team, bool HALVES = false>
+__device__ void build_input(const Team &tm, const GemvIn &in, int T, int K, float *xs, bool lead) {
   __shared__ float red[2][TEAM_MAX_WARPS];
   const int tid = tm.tid(), nt = tm.size();
   const int nch = K / 4;
-  bool ok = true;
   for (int t = 0; t < T; t++) {
     // rows written earlier in the same launch (persistent kernel) are read from L2
     const float4 *src = reinterpret_cast<const float4 *>(in.src + (size_t)t * in.ld);
@@ -73,27 +39,16 @@ __device__ bool build_input(const Team &tm, const GemvIn &in, int T, int K, floa
             const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
             x[j] = make_float4(a.x, a.y, b.x, b.y);
           }
-        } else if (TAGGED && in.src_pv) {
-          x[j] = reinterpret_cast<const float4 *>(tw->priv + (size_t)(in.src_pv - 1) * K)[c];
-        } else if (!TAGGED || !in.src_t) {
+        } else {
           x[j] = __ldcg(src + c);
         }
-        if (RESID && in.mode == IN_RESID && in.alpha) {
-          if (!TAGGED) o[j] = __ldcg(reinterpret_cast<const float4 *>(in.out + (size_t)t * K) + c);
+        if (in.mode == IN_RESID && in.alpha) {
+          o[j] = __ldcg(reinterpret_cast<const float4 *>(in.out + (size_t)t * K) + c);
           al[j] = __ldg(reinterpret_cast<const float4 *>(in.alpha) + c);
         }
-        if (RESID && in.mode == IN_RESID && (in.mix == MIX_LOOP || in.mix == MIX_RESUME)) {
-          if (TAGGED && in.input_pv)
-            inp[j] = reinterpret_cast<const float4 *>(tw->priv + (size_t)(in.input_pv - 1) * K)[c];
-          else
-            inp[j] = __ldcg(reinterpret_cast<const float4 *>(in.input + (size_t)t * K) + c);
-        }
+        if (in.mode == IN_RESID && (in.mix == MIX_LOOP || in.mix == MIX_RESUME))
+          inp[j] = __ldcg(reinterpret_cast<const float4 *>(in.input + (size_t)t * K) + c);
       }
-    }
-    if (TAGGED) {
-      if (in.mode != IN_EMBED && in.src_t && !await_row<KC>(in.src_t, in.src_tag, tid, nt, nch, x, *tw)) ok = false;
-      if (RESID && in.mode == IN_RESID && in.alpha && !await_row<KC>(in.out_t, in.out_tag, tid, nt, nch, o, *tw))
-        ok = false;
     }
     auto sq4 = [](const float4 &v) { return v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w; };
     auto scale4 = [](float4 &v, float f) {
@@ -110,7 +65,7 @@ __device__ bool build_input(const Team &tm, const GemvIn &in, int T, int K, floa
       const float inv = 1.f / sqrtf(ss + DORY_EPS);
 #pragma unroll
       for (int j = 0; j < KC; j++) scale4(x[j], inv);
-    } else if (RESID && in.mode == IN_RESID) {
+    } else if (in.mode == IN_RESID) {
       if (in.alpha) {
         float sx = 0.f, so = 0.f;
 #pragma unroll
@@ -160,8 +115,6 @@ __device__ bool build_input(const Team &tm, const GemvIn &in, int T, int K, floa
               reinterpret_cast<float4 *>(in.input + (size_t)t * K)[c] = x[j];
               reinterpret_cast<float4 *>(in.state + (size_t)t * K)[c] = x[j];
             }
-            if (TAGGED && in.input_pv && c < nch)
-              reinterpret_cast<float4 *>(tw->priv + (size_t)(in.input_pv - 1) * K)[c] = x[j];
           }
           x[j] = make_float4(x[j].x + inp[j].x, x[j].y + inp[j].y, x[j].z + inp[j].z, x[j].w + inp[j].w);
           ss += sq4(x[j]);
@@ -179,12 +132,10 @@ __device__ bool build_input(const Team &tm, const GemvIn &in, int T, int K, floa
         reinterpret_cast<float4 *>(xs + (size_t)t * K)[HALVES ? (c & 1) * (nch / 2) + (c >> 1) : c] = x[j];
         if ((in.mode == IN_RESID || in.mode == IN_EMBED) && lead && in.h_dst)
           reinterpret_cast<float4 *>(in.h_dst + (size_t)t * K)[c] = x[j];
-        if (TAGGED && in.hdst_pv) reinterpret_cast<float4 *>(tw->priv + (size_t)(in.hdst_pv - 1) * K)[c] = x[j];
       }
     }
   }
   tm.sync();
-  return ok;
 }
 
 // The last team of a q/k/v/g head: RoPE + justnorm (+ s_q^2) and the ring write

@@ -41,7 +41,6 @@
 
 #include "async.cuh"
 #include "common.cuh"
-#include "fused_body.cuh"
 #include "kernels.h"
 #include "team.cuh"
 
@@ -94,9 +93,9 @@ struct Tracer {
     if (p)
       for (int e = 0; e < 6; e++) trace_acc[e] = 0;
   }
-  __device__ __forceinline__ void flush(int stage) const {
+  __device__ __forceinline__ void flush(int stage, int n = 6) const {
     if (p)
-      for (int e = 0; e < 6; e++) p[((size_t)stage * gridDim.x + blockIdx.x) * MEGA_TRACE_EVENTS + 8 + e] = trace_acc[e];
+      for (int e = 0; e < n; e++) p[((size_t)stage * gridDim.x + blockIdx.x) * MEGA_TRACE_EVENTS + 8 + e] = trace_acc[e];
   }
   __device__ __forceinline__ long long clk() const { return p ? clock64() : 0; }
 };
@@ -386,12 +385,230 @@ __device__ void gemv_rows(const WarpTeam &tm, const MegaStage &st, int rb, int r
     tr.add(s, 9, tr.clk() - t1);
   }
   if (np > 0) flush_rows<DUAL>(st, rb, np, pg, pu, prow, epi, s + 1);
-  tr.flush(s);
+  tr.flush(s, 4);  // (12 and 13 hold the input row's wait)
 }
 
-template <int KC, bool RESID>
-__device__ __forceinline__ bool input_row(const WarpTeam &tm, const GemvIn &in, int K, float *xs, const TagWait &tw) {
-  return build_input<1, KC, WarpTeam, true, true, RESID>(tm, in, 1, K, xs, blockIdx.x == 0, &tw);
+// ---- input rows ---------------------------------------------------------------------------
+//
+// One row. Thread t owns the float4 chunks t + 256 j (j < KC) and stores them to the shared
+// input row as two halves (chunk c at (c & 1) * K/8 + c/2), so that a lane reading the 8
+// inputs of a 16-byte weight column reads float4 u of each half: consecutive lanes,
+// consecutive addresses. Each kind of input row has its own function, so that a stage runs
+// (and fetches) only its own code. All end with a team sync and return false when a tagged
+// wait ran out or the block stopped.
+
+// How an input row awaits tagged words: the block's stop flag, the polls of a word before
+// it gives up, the block's private rows, and (trace only, or null) where to stamp the time
+// the words were all in ([0]), count the poll rounds ([1]) and stamp the first poll ([2]).
+struct TagWait {
+  const volatile int *abort;
+  uint32_t limit;
+  float *priv;
+  unsigned long long *trace;
+};
+
+// Chunks tid + 256 j (< nch) of a row of tagged words into v, polled again (the whole set)
+// until every word carries `tag`.
+template <int KC>
+__device__ __forceinline__ bool await_row(const unsigned long long *src, uint32_t tag, int tid, int nch,
+                                          float4 (&v)[KC], const TagWait &tw) {
+  if (tw.trace && tid == 0) {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    tw.trace[2] = t;
+  }
+  for (uint32_t i = 0; i <= tw.limit && !*tw.abort; i++) {
+    bool all = true;
+#pragma unroll
+    for (int j = 0; j < KC; j++) {
+      const int c = tid + j * 32 * MW;
+      if (c < nch) all &= ld_tagged4(src + 4 * (size_t)c, tag, v[j]);
+    }
+    if (all) {
+      if (tw.trace && tid == 0) tw.trace[1] += i + 1;
+      return true;
+    }
+  }
+  return false;
+}
+
+__device__ __forceinline__ void stamp_in(const TagWait &tw, int tid) {
+  if (tw.trace && tid == 0) {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    tw.trace[0] = t;
+  }
+}
+
+__device__ __forceinline__ float sq4(const float4 &v) { return v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w; }
+__device__ __forceinline__ float4 mul4(const float4 &v, float f) {
+  return make_float4(v.x * f, v.y * f, v.z * f, v.w * f);
+}
+
+__shared__ float red_in[2][TEAM_MAX_WARPS];
+
+__device__ __forceinline__ float row_sum(const WarpTeam &tm, float a) {
+  float b = 0.f;
+  team_sum2(tm, a, b, red_in);
+  return a;
+}
+
+__device__ __forceinline__ float4 *xs_chunk(float *xs, int nch, int c) {
+  return reinterpret_cast<float4 *>(xs) + (c & 1) * (nch / 2) + (c >> 1);
+}
+
+// IN_NORM: x / sqrt(sum x^2 + eps) (dory.rs fn justnorm); IN_PLAIN: x. The row is tagged
+// words of an earlier stage, or a row of the block's private area.
+template <int KC>
+__device__ __forceinline__ bool in_norm(const WarpTeam &tm, const GemvIn &in, int K, float *xs, const TagWait &tw) {
+  const int tid = tm.tid(), nch = K / 4;
+  float4 x[KC];
+#pragma unroll
+  for (int j = 0; j < KC; j++) x[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+  bool ok = true;
+  if (in.src_t) {
+    ok = await_row<KC>(in.src_t, in.src_tag, tid, nch, x, tw);
+  } else {
+    const float4 *src = reinterpret_cast<const float4 *>(in.src_pv ? tw.priv + (size_t)(in.src_pv - 1) * K : in.src);
+#pragma unroll
+    for (int j = 0; j < KC; j++)
+      if (tid + j * 32 * MW < nch) x[j] = src[tid + j * 32 * MW];
+  }
+  stamp_in(tw, tid);
+  if (in.mode == IN_NORM) {
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < KC; j++) ss += sq4(x[j]);
+    const float inv = 1.f / sqrtf(row_sum(tm, ss) + DORY_EPS);
+#pragma unroll
+    for (int j = 0; j < KC; j++) x[j] = mul4(x[j], inv);
+  }
+#pragma unroll
+  for (int j = 0; j < KC; j++)
+    if (tid + j * 32 * MW < nch) *xs_chunk(xs, nch, tid + j * 32 * MW) = x[j];
+  tm.sync();
+  return ok;
+}
+
+// The token's embedding row (bf16 table; an id outside the vocabulary gives zeros), stored
+// as the hidden row (K <= 2048: two chunks a thread).
+__device__ __forceinline__ bool in_embed(const WarpTeam &tm, const GemvIn &in, int K, float *xs, const TagWait &tw) {
+  const int tid = tm.tid(), nch = K / 4;
+  const int id = in.ids[0];
+  const bool lead = blockIdx.x == 0;
+#pragma unroll
+  for (int j = 0; j < 2; j++) {
+    const int c = tid + j * 32 * MW;
+    if (c >= nch) continue;
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (id >= 0 && id < in.vocab) {
+      const uint2 u = __ldg(reinterpret_cast<const uint2 *>(in.embed + (size_t)id * K) + c);
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
+      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
+      x = make_float4(a.x, a.y, b.x, b.y);
+    }
+    *xs_chunk(xs, nch, c) = x;
+    if (lead) reinterpret_cast<float4 *>(in.h_dst)[c] = x;
+    if (in.hdst_pv) reinterpret_cast<float4 *>(tw.priv + (size_t)(in.hdst_pv - 1) * K)[c] = x;
+  }
+  tm.sync();
+  return true;
+}
+
+// IN_RESID (K <= 2048: two chunks a thread): the nGPT residual x = (x^ + alpha (out^ -
+// x^))^ (dory.rs fn slerp), then the loop mix (dory.rs fn stack): MIX_LOOP / MIX_END state =
+// x^; MIX_BEGIN input = state = x; MIX_BEGIN / MIX_LOOP / MIX_RESUME x = (x + input)^. The
+// new hidden row goes to the block's private area, and from the leading block to h_dst; the
+// leading block also stores the state and input rows.
+__device__ __forceinline__ bool in_resid(const WarpTeam &tm, const GemvIn &in, int K, float *xs, const TagWait &tw) {
+  constexpr int KC = 2;
+  const int tid = tm.tid(), nch = K / 4;
+  const bool lead = blockIdx.x == 0;
+  const bool has_in = in.mix == MIX_LOOP || in.mix == MIX_RESUME;
+  const float4 *src = reinterpret_cast<const float4 *>(in.src_pv ? tw.priv + (size_t)(in.src_pv - 1) * K : in.src);
+  const float4 *inr =
+      reinterpret_cast<const float4 *>(in.input_pv ? tw.priv + (size_t)(in.input_pv - 1) * K : in.input);
+  float4 x[KC], o[KC], al[KC], inp[KC];
+#pragma unroll
+  for (int j = 0; j < KC; j++) {
+    const int c = tid + j * 32 * MW;
+    x[j] = o[j] = al[j] = inp[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (c < nch) {
+      x[j] = in.src_pv ? src[c] : __ldcg(src + c);
+      if (in.alpha) al[j] = __ldg(reinterpret_cast<const float4 *>(in.alpha) + c);
+      if (has_in) inp[j] = in.input_pv ? inr[c] : __ldcg(inr + c);
+    }
+  }
+  bool ok = true;
+  if (in.alpha) ok = await_row<KC>(in.out_t, in.out_tag, tid, nch, o, tw);
+  stamp_in(tw, tid);
+  if (in.alpha) {
+    float sx = 0.f, so = 0.f;
+#pragma unroll
+    for (int j = 0; j < KC; j++) {
+      sx += sq4(x[j]);
+      so += sq4(o[j]);
+    }
+    team_sum2(tm, sx, so, red_in);
+    const float ix = 1.f / sqrtf(sx + DORY_EPS), io = 1.f / sqrtf(so + DORY_EPS);
+    float sr = 0.f;
+#pragma unroll
+    for (int j = 0; j < KC; j++) {
+      const float4 xh = mul4(x[j], ix), oh = mul4(o[j], io);
+      x[j] = make_float4(xh.x + al[j].x * (oh.x - xh.x), xh.y + al[j].y * (oh.y - xh.y),
+                         xh.z + al[j].z * (oh.z - xh.z), xh.w + al[j].w * (oh.w - xh.w));
+      sr += sq4(x[j]);
+    }
+    const float inv = 1.f / sqrtf(row_sum(tm, sr) + DORY_EPS);
+#pragma unroll
+    for (int j = 0; j < KC; j++) x[j] = mul4(x[j], inv);
+  }
+  if (in.mix == MIX_LOOP || in.mix == MIX_END) {  // state = h^
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < KC; j++) ss += sq4(x[j]);
+    const float inv = 1.f / sqrtf(row_sum(tm, ss) + DORY_EPS);
+#pragma unroll
+    for (int j = 0; j < KC; j++) {
+      x[j] = mul4(x[j], inv);
+      const int c = tid + j * 32 * MW;
+      if (lead && c < nch) reinterpret_cast<float4 *>(in.state)[c] = x[j];
+    }
+  }
+  if (in.mix == MIX_BEGIN || in.mix == MIX_LOOP || in.mix == MIX_RESUME) {  // h = (state + input)^
+    // (MIX_RESUME: src is the saved state row, taken as it is)
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < KC; j++) {
+      const int c = tid + j * 32 * MW;
+      if (in.mix == MIX_BEGIN) {
+        inp[j] = x[j];
+        if (c < nch) {
+          if (lead) {
+            reinterpret_cast<float4 *>(in.input)[c] = x[j];
+            reinterpret_cast<float4 *>(in.state)[c] = x[j];
+          }
+          if (in.input_pv) reinterpret_cast<float4 *>(tw.priv + (size_t)(in.input_pv - 1) * K)[c] = x[j];
+        }
+      }
+      x[j] = make_float4(x[j].x + inp[j].x, x[j].y + inp[j].y, x[j].z + inp[j].z, x[j].w + inp[j].w);
+      ss += sq4(x[j]);
+    }
+    const float inv = 1.f / sqrtf(row_sum(tm, ss) + DORY_EPS);
+#pragma unroll
+    for (int j = 0; j < KC; j++) x[j] = mul4(x[j], inv);
+  }
+#pragma unroll
+  for (int j = 0; j < KC; j++) {
+    const int c = tid + j * 32 * MW;
+    if (c < nch) {
+      *xs_chunk(xs, nch, c) = x[j];
+      if (lead && in.h_dst) reinterpret_cast<float4 *>(in.h_dst)[c] = x[j];
+      if (in.hdst_pv) reinterpret_cast<float4 *>(tw.priv + (size_t)(in.hdst_pv - 1) * K)[c] = x[j];
+    }
+  }
+  tm.sync();
+  return ok;
 }
 
 // Returns false (team-uniformly) when the block has stopped.
@@ -415,13 +632,20 @@ __device__ __noinline__ bool gemv_stage(const WarpTeam &tm, const MegaArgs &a, c
     if (st.ep.mode == EPI_SILU) e1 = __ldg(st.ep.vec2 + rb + ei);
   }
   const int kc = (K / 4 + tm.size() - 1) / tm.size();  // float4 chunks per thread
-  // K is at most 6144 (the host's limit): 2 or 6 float4 chunks a thread. Two forms only: with
+  // K is at most 6144 (the host's limit): 2 or 6 float4 chunks a thread. Two sizes only: with
   // four (2, 4, 6, 8) the stage's register allocation spilled and a token took 4.4% longer;
   // a residual of 6 chunks (two rows of tagged words awaited at once) spilled too, inline or
-  // called, so hidden rows are at most 2048 wide here.
-  const TagWait tw{&ctl.abort, a.spin_limit, a.priv + (size_t)b * a.priv_stride};
-  // (a residual row is a hidden row: at most 2048, the host's limit)
-  const bool in_ok = kc <= 2 ? input_row<2, true>(tm, st.in, K, xs, tw) : input_row<6, false>(tm, st.in, K, xs, tw);
+  // called, so hidden rows (residuals, embeddings) are at most 2048 wide here.
+  // trace: events 12 and 13 of a GEMV stage are the time its input words were all in and the poll rounds
+  unsigned long long *tw_trace =
+      tr.p ? tr.p + ((size_t)s * gridDim.x + blockIdx.x) * MEGA_TRACE_EVENTS + 12 : nullptr;
+  if (tw_trace) tw_trace[1] = 0;
+  const TagWait tw{&ctl.abort, a.spin_limit, a.priv + (size_t)b * a.priv_stride, tw_trace};
+  bool in_ok;
+  if (st.in.mode == IN_RESID) in_ok = in_resid(tm, st.in, K, xs, tw);
+  else if (st.in.mode == IN_EMBED) in_ok = in_embed(tm, st.in, K, xs, tw);
+  else if (kc <= 2) in_ok = in_norm<2>(tm, st.in, K, xs, tw);
+  else in_ok = in_norm<6>(tm, st.in, K, xs, tw);
   if (!in_ok) flag_error(ctl, a.err);  // the rows below see the stop and skip their work
   if (st.ep.mode != EPI_STORE) {
     if (has_e) {

@@ -281,10 +281,12 @@ struct MegaArgs {
 // stage's first chunk has landed (consumers); 8..11 SM cycles the first consumer thread
 // spent over the stage's chunks waiting for a slot, reducing, at the team barrier, and in
 // the epilogue (attention stages: copy wait, compute, arrival, merge); 12, 13 cycles of
-// the attention merge until its partials are folded, and until its team sync. Attention
+// the attention merge until its partials are folded, and until its team sync (GEMV
+// stages: the %globaltimer stamp once the input row's words were all in, and the poll
+// rounds that took); 14 the stamp when the input row's first poll was issued. Attention
 // stages reuse 2, 3, 5, 6, 7 for the block's last item: K/V copies issued, queries
 // prepared, tiles landed, scores and values done, arrival counted.
-constexpr int MEGA_TRACE_EVENTS = 14;
+constexpr int MEGA_TRACE_EVENTS = 16;
 // Attention items of one kv head that the persistent kernel's per-head merge waits for at most.
 constexpr int MEGA_FLAGS = 32;
 
