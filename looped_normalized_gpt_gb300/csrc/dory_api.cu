@@ -1588,7 +1588,7 @@ int dory_create(const dory_config *cfg, const dory_weights *w, void *stream, dor
               dm.ffn % 8 == 0 && q_size % 8 == 0 && kmax + mega_park_floats(false) <= mega_work_floats() &&
               (size_t)dm.hidden + mega_park_floats(true) <= mega_work_floats() &&
               (size_t)2 * MEGA_AK * dm.hd <= mega_work_floats() && mega_chunk_rows(dm.hidden, true) >= 1 &&
-              mega_chunk_rows((int)kmax, false) >= 1;
+              mega_chunk_rows((int)kmax, false) >= 2;
     // the merge's per-warp partials of a kv head's query heads
     if ((size_t)mega_consumer_warps() * rep * (dm.hd + 2) > mega_work_floats()) ok = false;
     // input rows of at most six float4 chunks a thread, a residual (hidden row) of at most two

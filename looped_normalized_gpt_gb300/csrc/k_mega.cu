@@ -266,7 +266,7 @@ __device__ void produce(const MegaArgs &a, uint8_t *ring, uint64_t *full, uint64
 
 // ---- GEMV stage ---------------------------------------------------------------------------
 
-// A stage's rows in groups of NR (two rows, or one gate/up pair, share each load of the
+// A stage's rows in groups of two (two rows, or one gate/up pair, share each load of the
 // input row): group g of the block's rows belongs to consumer warp g mod MW, which awaits only
 // the chunks that hold its groups (a chunk holds at most MW groups). The lanes split a row
 // into 16-byte columns (lane l: columns l, l + 32, ...) against the input row in shared
@@ -277,25 +277,25 @@ __device__ void produce(const MegaArgs &a, uint8_t *ring, uint64_t *full, uint64
 // and the next; lane 4i then applies the epilogue (SwiGLU, logit scale) and stores.
 constexpr int PEND = 8;  // rows a warp parks before it reduces them
 
-template <bool DUAL>
-__device__ __forceinline__ void flush_rows(const MegaStage &st, int rb, int np, const float *pg, const float *pu,
-                                           const int *prow, const float (*epi)[EPI_ROWS], uint32_t tag) {
+// The parked sums of np (<= PEND) rows: reduce, apply the epilogue, store (tagged words, or
+// plain floats for the logits). Dual: the gate sums at pg, the up sums at pu, one row each.
+__device__ __forceinline__ void flush_rows(const MegaStage &st, bool dual, int rb, int np, const float *pg,
+                                           const float *pu, const int *prow, const float (*epi)[EPI_ROWS],
+                                           uint32_t tag) {
   const int lane = threadIdx.x & 31, i = lane >> 2, q = lane & 3;
   __syncwarp();
   const float4 *g4 = reinterpret_cast<const float4 *>(pg + i * 32 + q * 8);
   const float4 ga = g4[0], gb = g4[1];
   float g = ((ga.x + ga.y) + (ga.z + ga.w)) + ((gb.x + gb.y) + (gb.z + gb.w)), u = 0.f;
-  if (DUAL) {
+  if (dual) {
     const float4 *u4 = reinterpret_cast<const float4 *>(pu + i * 32 + q * 8);
     const float4 ua = u4[0], ub = u4[1];
     u = ((ua.x + ua.y) + (ua.z + ua.w)) + ((ub.x + ub.y) + (ub.z + ub.w));
   }
   g += __shfl_xor_sync(0xffffffffu, g, 1);
   g += __shfl_xor_sync(0xffffffffu, g, 2);
-  if (DUAL) {
-    u += __shfl_xor_sync(0xffffffffu, u, 1);
-    u += __shfl_xor_sync(0xffffffffu, u, 2);
-  }
+  u += __shfl_xor_sync(0xffffffffu, u, 1);
+  u += __shfl_xor_sync(0xffffffffu, u, 2);
   if (q == 0 && i < np) {
     const int jr = prow[i];
     const int mode = st.ep.mode;
@@ -314,17 +314,20 @@ __device__ __forceinline__ void flush_rows(const MegaStage &st, int rb, int np, 
   __syncwarp();  // the parked sums may be overwritten
 }
 
-template <bool DUAL, int NR>
+// One body for every GEMV stage: a group is two weight rows against the shared input row,
+// either two consecutive rows of a chunk or (dual) the gate and up rows of one SwiGLU pair,
+// so that each load of the input row serves two rows.
 __device__ void gemv_rows(const WarpTeam &tm, const MegaStage &st, int rb, int re, int c0, const uint8_t *ring,
                           uint64_t *full, uint64_t *empty, const float *xs, float *park, const float (*epi)[EPI_ROWS],
                           Ctl &ctl, int *err, const Tracer &tr, int s) {
-  static_assert(!DUAL || NR == 1, "a gate/up pair is a group of its own");
+  const bool dual = st.pair > 0;
   const int lane = threadIdx.x & 31, cw = tm.warp();
   const int K = st.K, R = st.R, nu = K / 8;  // 16-byte columns per row
   const int n = re - rb;                     // rows (pairs) of this block
-  const int ngroups = (n + NR - 1) / NR;     // groups do not straddle chunks: R is a multiple of NR
+  const int per = dual ? 1 : 2;              // rows (pairs) a group covers; R is a multiple of it
+  const int ngroups = (n + per - 1) / per;
   // this warp's parked lane sums [PEND][32] (gate, then up), and their rows
-  float *pg = park + cw * (DUAL ? 2 : 1) * PEND * 32, *pu = pg + PEND * 32;
+  float *pg = park + cw * (dual ? 2 : 1) * PEND * 32, *pu = pg + PEND * 32;
   __shared__ int prow_all[MW][PEND];
   int *prow = prow_all[cw];
   int np = 0;
@@ -339,7 +342,7 @@ __device__ void gemv_rows(const WarpTeam &tm, const MegaStage &st, int rb, int r
   };
   tr.zero(s);
   for (int gi = cw; gi < ngroups; gi += MW) {  // this warp's groups
-    const int x = gi * NR / R, c = c0 + x, sl = c % NS;
+    const int x = gi * per / R, c = c0 + x, sl = c % NS;
     long long t0 = tr.clk();
     bool landed = false;
     for (uint32_t i = 0; i < MBAR_WAIT_LIMIT && !ctl.abort; i++)
@@ -350,42 +353,45 @@ __device__ void gemv_rows(const WarpTeam &tm, const MegaStage &st, int rb, int r
     long long t1 = tr.clk();
     tr.add(s, 8, t1 - t0);
     if (!landed && lane == 0) flag_error(ctl, err);  // the block stops at the stage's end
-    const int r0 = x * R, nr = min(R, n - r0), j = gi * NR - r0;
+    const int r0 = x * R, nr = min(R, n - r0), j = gi * per - r0;
     if (landed) {
       // a group's second row past the chunk's last one reads stale slot bytes: not stored
-      float2 a0[NR], a1[NR], b0 = make_float2(0.f, 0.f), b1 = b0;
-#pragma unroll
-      for (int r = 0; r < NR; r++) a0[r] = a1[r] = make_float2(0.f, 0.f);
+      float2 a0 = make_float2(0.f, 0.f), a1 = a0, b0 = a0, b1 = a0;
       const uint4 *wc = reinterpret_cast<const uint4 *>(ring + (size_t)sl * SLOT);
-      const uint4 *wg = wc + (size_t)j * nu, *wu = wc + (size_t)(nr + j) * nu;
+      const uint4 *w0 = wc + (size_t)j * nu, *w1 = wc + (size_t)(dual ? nr + j : j + 1) * nu;
 #pragma unroll 4
       for (int u = lane; u < nu; u += 32) {
         const float4 p = reinterpret_cast<const float4 *>(xs)[u], q = reinterpret_cast<const float4 *>(xs)[nu + u];
-#pragma unroll
-        for (int r = 0; r < NR; r++) dot8(wg[u + r * nu], p, q, a0[r], a1[r]);
-        if (DUAL) dot8(wu[u], p, q, b0, b1);
+        dot8(w0[u], p, q, a0, a1);
+        dot8(w1[u], p, q, b0, b1);
       }
-#pragma unroll
-      for (int r = 0; r < NR; r++) {
-        if (NR > 1 && j + r >= nr) break;
-        pg[np * 32 + lane] = (a0[r].x + a0[r].y) + (a1[r].x + a1[r].y);
-        if (DUAL) pu[np * 32 + lane] = (b0.x + b0.y) + (b1.x + b1.y);
-        if (lane == 0) prow[np] = gi * NR + r;
-        if (++np == PEND) {
-          flush_rows<DUAL>(st, rb, np, pg, pu, prow, epi, s + 1);
-          np = 0;
-        }
+      const float sa = (a0.x + a0.y) + (a1.x + a1.y), sb = (b0.x + b0.y) + (b1.x + b1.y);
+      pg[np * 32 + lane] = sa;
+      if (lane == 0) prow[np] = gi * per;
+      if (dual) {
+        pu[np * 32 + lane] = sb;
+        np++;
+      } else if (j + 1 < nr) {
+        pg[(np + 1) * 32 + lane] = sb;
+        if (lane == 0) prow[np + 1] = gi * per + 1;
+        np += 2;
+      } else {
+        np++;
       }
+    }
+    // one place reduces and stores: when two more rows might not fit, and after the last group
+    if (np > PEND - 2 || (gi + MW >= ngroups && np > 0)) {
+      flush_rows(st, dual, rb, np, pg, pu, prow, epi, s + 1);
+      np = 0;
     }
     __syncwarp();
     // the slot is free after MW arrivals: one per group of the chunk, the first group's warp
     // also arriving for the warps that hold no group of it
-    const int ng = (nr + NR - 1) / NR;
+    const int ng = (nr + per - 1) / per;
     if (lane == 0 && !ctl.abort) mbar_arrive_n(smem_addr(&empty[sl]), j == 0 ? MW - ng + 1 : 1);
     tr.add(s, 9, tr.clk() - t1);
   }
-  if (np > 0) flush_rows<DUAL>(st, rb, np, pg, pu, prow, epi, s + 1);
-  tr.flush(s, 4);  // (12 and 13 hold the input row's wait)
+  tr.flush(s, 4);  // (12 .. 14 hold the input row's wait)
 }
 
 // ---- input rows ---------------------------------------------------------------------------
@@ -447,11 +453,14 @@ __device__ __forceinline__ float4 mul4(const float4 &v, float f) {
 
 __shared__ float red_in[2][TEAM_MAX_WARPS];
 
-__device__ __forceinline__ float row_sum(const WarpTeam &tm, float a) {
-  float b = 0.f;
+// Sums of two values over the consumer warps, out of line: inline, each of the reductions
+// of the input rows added about 3.7 KB of code to the stage.
+__device__ __noinline__ float2 row_sum2(float a, float b) {
+  const WarpTeam tm{1, MW, 1};
   team_sum2(tm, a, b, red_in);
-  return a;
+  return make_float2(a, b);
 }
+__device__ __forceinline__ float row_sum(float a) { return row_sum2(a, 0.f).x; }
 
 __device__ __forceinline__ float4 *xs_chunk(float *xs, int nch, int c) {
   return reinterpret_cast<float4 *>(xs) + (c & 1) * (nch / 2) + (c >> 1);
@@ -479,7 +488,7 @@ __device__ __forceinline__ bool in_norm(const WarpTeam &tm, const GemvIn &in, in
     float ss = 0.f;
 #pragma unroll
     for (int j = 0; j < KC; j++) ss += sq4(x[j]);
-    const float inv = 1.f / sqrtf(row_sum(tm, ss) + DORY_EPS);
+    const float inv = 1.f / sqrtf(row_sum(ss) + DORY_EPS);
 #pragma unroll
     for (int j = 0; j < KC; j++) x[j] = mul4(x[j], inv);
   }
@@ -549,7 +558,9 @@ __device__ __forceinline__ bool in_resid(const WarpTeam &tm, const GemvIn &in, i
       sx += sq4(x[j]);
       so += sq4(o[j]);
     }
-    team_sum2(tm, sx, so, red_in);
+    const float2 sxo = row_sum2(sx, so);
+    sx = sxo.x;
+    so = sxo.y;
     const float ix = 1.f / sqrtf(sx + DORY_EPS), io = 1.f / sqrtf(so + DORY_EPS);
     float sr = 0.f;
 #pragma unroll
@@ -559,7 +570,7 @@ __device__ __forceinline__ bool in_resid(const WarpTeam &tm, const GemvIn &in, i
                          xh.z + al[j].z * (oh.z - xh.z), xh.w + al[j].w * (oh.w - xh.w));
       sr += sq4(x[j]);
     }
-    const float inv = 1.f / sqrtf(row_sum(tm, sr) + DORY_EPS);
+    const float inv = 1.f / sqrtf(row_sum(sr) + DORY_EPS);
 #pragma unroll
     for (int j = 0; j < KC; j++) x[j] = mul4(x[j], inv);
   }
@@ -567,7 +578,7 @@ __device__ __forceinline__ bool in_resid(const WarpTeam &tm, const GemvIn &in, i
     float ss = 0.f;
 #pragma unroll
     for (int j = 0; j < KC; j++) ss += sq4(x[j]);
-    const float inv = 1.f / sqrtf(row_sum(tm, ss) + DORY_EPS);
+    const float inv = 1.f / sqrtf(row_sum(ss) + DORY_EPS);
 #pragma unroll
     for (int j = 0; j < KC; j++) {
       x[j] = mul4(x[j], inv);
@@ -594,7 +605,7 @@ __device__ __forceinline__ bool in_resid(const WarpTeam &tm, const GemvIn &in, i
       x[j] = make_float4(x[j].x + inp[j].x, x[j].y + inp[j].y, x[j].z + inp[j].z, x[j].w + inp[j].w);
       ss += sq4(x[j]);
     }
-    const float inv = 1.f / sqrtf(row_sum(tm, ss) + DORY_EPS);
+    const float inv = 1.f / sqrtf(row_sum(ss) + DORY_EPS);
 #pragma unroll
     for (int j = 0; j < KC; j++) x[j] = mul4(x[j], inv);
   }
@@ -656,9 +667,7 @@ __device__ __noinline__ bool gemv_stage(const WarpTeam &tm, const MegaArgs &a, c
   }
   tr.mark(s, 2);
   float *park = xs + K;  // the rows' parked lane sums, after the input row
-  if (st.pair > 0) gemv_rows<true, 1>(tm, st, rb, re, c, ring, full, empty, xs, park, epi, ctl, a.err, tr, s);
-  else if (st.R % 2 == 0) gemv_rows<false, 2>(tm, st, rb, re, c, ring, full, empty, xs, park, epi, ctl, a.err, tr, s);
-  else gemv_rows<false, 1>(tm, st, rb, re, c, ring, full, empty, xs, park, epi, ctl, a.err, tr, s);
+  gemv_rows(tm, st, rb, re, c, ring, full, empty, xs, park, epi, ctl, a.err, tr, s);
   c += re > rb ? (re - rb + st.R - 1) / st.R : 0;
   const bool ok = team_ok(tm, ctl);
   tr.mark(s, 3);
@@ -1173,7 +1182,8 @@ size_t mega_smem_bytes(int) { return 1024 + (size_t)NS * SLOT + WORK; }
 
 int mega_chunk_rows(int K, bool dual) {  // 0: a row does not fit a slot
   const size_t rb = (size_t)K * 2 * (dual ? 2 : 1);
-  return (int)std::min<size_t>(SLOT / rb, RMAX);
+  const int r = (int)std::min<size_t>(SLOT / rb, RMAX);
+  return dual || r < 2 ? r : r & ~1;  // rows go in pairs: an even count per chunk
 }
 
 int mega_consumer_warps() { return MW; }
