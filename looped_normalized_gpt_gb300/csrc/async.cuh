@@ -150,6 +150,20 @@ __device__ __forceinline__ bool ld_tagged(const unsigned long long *p, uint32_t 
   return (uint32_t)(w >> 32) == tag;
 }
 
+// 2 consecutive values (16-byte aligned words p[0..1])
+__device__ __forceinline__ void st_tagged2(unsigned long long *p, float a, float b, uint32_t tag) {
+  asm volatile("st.relaxed.gpu.global.v2.b64 [%0], {%1, %2};" ::"l"(p), "l"(tag_word(a, tag)), "l"(tag_word(b, tag))
+               : "memory");
+}
+
+// true when both words p[0..1] (16-byte aligned) carry `tag`
+__device__ __forceinline__ bool ld_tagged2(const unsigned long long *p, uint32_t tag, float2 &v) {
+  unsigned long long a, b;
+  asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p));
+  v = make_float2(__uint_as_float((uint32_t)a), __uint_as_float((uint32_t)b));
+  return (uint32_t)(a >> 32) == tag && (uint32_t)(b >> 32) == tag;
+}
+
 // true when all 4 words p[0..3] (16-byte aligned) carry `tag`
 __device__ __forceinline__ bool ld_tagged4(const unsigned long long *p, uint32_t tag, float4 &v) {
   unsigned long long a, b, c, d;

@@ -132,13 +132,14 @@ struct dory_handle {
   int32_t *hctr = nullptr, *actr = nullptr;  // arrival counters of the fused kernels
   bool fused_ok = false;
   // persistent batch-1 decode: one block per SM; zeroed before each launch: counters
-  // ([1] RoPE entries, [2] blocks done, [64..) per-kv-head attention item arrivals and
-  // flags), then the tagged words that stages hand on (q/k/v/g row, z, out, mlp)
+  // ([1] RoPE entries, [2] blocks done, [64..) per-kv-head attention item arrivals), then the
+  // tagged words that stages hand on (q/k/v/g row, z, out, mlp, attention item partials)
   bool mega_ok = false;
   int sms = 0;
   int32_t *mega_sync = nullptr;
   size_t mega_sync_bytes = 0;
   unsigned long long *mega_tq = nullptr, *mega_tz = nullptr, *mega_to = nullptr, *mega_tm = nullptr;
+  unsigned long long *mega_tp = nullptr;  // attention item partials of the per-head merges
   float *mega_priv = nullptr;  // per block: its hidden rows (2) and the loop's input row
   MegaStage *mega_stages = nullptr;  // stage list of the launches issued without graphs
   size_t mega_cap = 0;
@@ -1046,7 +1047,7 @@ int issue_mega(dory_t *d, const StepArgs &a, int32_t *rt, const MegaStage *stage
   m.rope = d->rope;
   m.sync = d->mega_sync;
   m.actr = d->mega_sync + 64;
-  m.aflag = d->mega_sync + 64 + d->dims.nk;
+  m.tpart = d->mega_tp;
   m.err = d->dev_err;
   m.seq_pos = d->d_seq_pos;
   m.priv = d->mega_priv;
@@ -1546,8 +1547,9 @@ int dory_create(const dory_config *cfg, const dory_weights *w, void *stream, dor
                a_lg2 = areserve((size_t)d->Tstep * dm.vocab * 4),
                a_sp = areserve((size_t)cfg->max_seqs * 4), a_rows = areserve((size_t)ROW_TABLE * T * 4),
                a_zero = areserve((size_t)cfg->max_seqs * 4), a_err = areserve(256);
-  const size_t ms_ints = ((size_t)(64 + dm.nk + dm.nk * MEGA_FLAGS) * 4 + 15) & ~(size_t)15;
-  const size_t ms_words = (size_t)(2 * q_size + 2 * kv_size) + q_size + dm.hidden + dm.ffn;
+  const size_t ms_ints = ((size_t)(64 + dm.nk) * 4 + 15) & ~(size_t)15;
+  const size_t ms_words = (size_t)(2 * q_size + 2 * kv_size) + q_size + dm.hidden + dm.ffn +
+                          (size_t)dm.nh * MEGA_FLAGS * (dm.hd + 2);
   const size_t ms_bytes = ms_ints + ms_words * 8, a_ms = areserve(ms_bytes);
   const size_t a_stab = areserve((size_t)d->n_flat_slots * 3 * 8), a_drop = areserve((size_t)d->n_flat_slots * 4),
                a_top = areserve(4);
@@ -1576,6 +1578,7 @@ int dory_create(const dory_config *cfg, const dory_weights *w, void *stream, dor
   d->mega_tz = d->mega_tq + 2 * q_size + 2 * kv_size;
   d->mega_to = d->mega_tz + q_size;
   d->mega_tm = d->mega_to + dm.hidden;
+  d->mega_tp = d->mega_tm + dm.ffn;
   {
     // the persistent decode kernel: bf16 weights, f32 rings, rows that stream as whole
     // 16-byte runs and fit a ring slot, a block's input row and attention scratch within

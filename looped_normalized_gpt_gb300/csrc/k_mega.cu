@@ -774,8 +774,8 @@ __device__ __forceinline__ void merge_items(const WarpTeam &tm, const MegaArgs &
 
 // Merge the items of query head h (of kv head kh = h / rep) and gate: thread t takes the 4
 // outputs q = t mod HD/4 and the items g, g + G, ... (g = t / (HD/4), G = team size / (HD/4)),
-// loads each item's partials once the item has published its flag for this stage, and folds
-// them in item order with a running max; the groups meet in shared memory and warp 0
+// polls each item's partials (tagged words of this stage) and folds them in item order with
+// a running max; the groups meet in shared memory and warp 0
 // finishes in group order: y = sum o e^(m - M) / sum l e^(m - M), z = y * sigmoid(g * s_g^2).
 // Returns false (team-uniformly) when the block has stopped.
 template <int HD>
@@ -793,31 +793,37 @@ __device__ __noinline__ bool merge_head(const WarpTeam &tm, const MegaArgs &a, c
     if (!await4(st.qkvg_t + (size_t)(d.nh + 2 * d.nk) * HD + c, st.qtag, gr, ctl, a.spin_limit))
       flag_error(ctl, a.err);
   }
-  // each item's partials as soon as it has published them: the flag is read with acquire
-  // loads, so the partial loads that follow it see the item's stores; only the last item's
-  // loads stay on the critical path
-  const int *fl = a.aflag + kh * MEGA_FLAGS;
+  // each item's partials are tagged words of this stage: the thread's items are polled
+  // together, again only those whose words are not all in yet
+  const unsigned long long *po = a.tpart + (size_t)h * MEGA_FLAGS * HD + q * 4;
+  const unsigned long long *pml = a.tpart + (size_t)d.nh * MEGA_FLAGS * HD + (size_t)h * MEGA_FLAGS * 2;
+  const uint32_t tag = s + 1;
   float4 o[IB];
   float2 ml[IB];
+  uint32_t pend = 0;
 #pragma unroll
   for (int u = 0; u < IB; u++) {
-    const int it = g + u * groups;
     o[u] = make_float4(0.f, 0.f, 0.f, 0.f);
     ml[u] = make_float2(-INFINITY, 0.f);
-    if (it >= nblk) continue;
-    bool seen = false;
-    for (uint32_t polls = 0; !ctl.abort && polls <= a.spin_limit; polls++)
-      if (ld_acquire_gpu(fl + it) == s + 1) {
-        seen = true;
-        break;
-      }
-    if (!seen) {
-      flag_error(ctl, a.err);
-      continue;
-    }
-    o[u] = __ldcg(reinterpret_cast<const float4 *>(part_o(st, rep, HD, kh, it, hh) + q * 4));
-    ml[u] = __ldcg(reinterpret_cast<const float2 *>(part_ml(st, d.nk, rep, HD, kh, it, hh)));
+    if (g + u * groups < nblk) pend |= 1u << u;
   }
+  for (uint32_t polls = 0; pend && !ctl.abort && polls <= a.spin_limit; polls++) {
+#pragma unroll
+    for (int u = 0; u < IB; u++) {
+      if (!((pend >> u) & 1u)) continue;
+      const int it = g + u * groups;
+      float4 ov;
+      float2 mv;
+      const bool o_in = ld_tagged4(po + (size_t)it * HD, tag, ov);
+      const bool ml_in = ld_tagged2(pml + (size_t)it * 2, tag, mv);
+      if (o_in && ml_in) {
+        o[u] = ov;
+        ml[u] = mv;
+        pend &= ~(1u << u);
+      }
+    }
+  }
+  if (pend) flag_error(ctl, a.err);
   float M = -INFINITY, L = 0.f;
   float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -864,7 +870,8 @@ __device__ __noinline__ bool merge_head(const WarpTeam &tm, const MegaArgs &a, c
 // the item's softmax statistics and its value sum, written as the item's partial.
 template <int HD>
 __device__ __forceinline__ void attn_head(const MegaStage &st, int nk, const float *Ks, const float *Vs, const float *q,
-                                          int tg, long P0, long lo, long p, int kh, int blk, int rep, int h) {
+                                          int tg, long P0, long lo, long p, int kh, int blk, int rep, int h,
+                                          unsigned long long *tp, int nh, uint32_t tag) {
   constexpr int NV = HD / 32, NC = HD / 4;
   const int lane = threadIdx.x & 31;
   const float scale = 1.f / sqrtf((float)HD);
@@ -899,6 +906,16 @@ __device__ __forceinline__ void attn_head(const MegaStage &st, int nk, const flo
       acc[i] = fmaf(w0, v0[i], acc[i]);
       acc_b[i] = fmaf(w1, v1[i], acc_b[i]);
     }
+  }
+  if (tp) {  // the per-head merges poll these words
+    const size_t qh = (size_t)kh * rep + h;
+    unsigned long long *to = tp + (qh * MEGA_FLAGS + blk) * HD + lane * NV;
+    if constexpr (NV == 4)
+      st_tagged4(to, make_float4(acc[0] + acc_b[0], acc[1] + acc_b[1], acc[2] + acc_b[2], acc[3] + acc_b[3]), tag);
+    else
+      st_tagged2(to, acc[0] + acc_b[0], acc[1] + acc_b[1], tag);
+    if (lane == 0) st_tagged2(tp + (size_t)nh * MEGA_FLAGS * HD + (qh * MEGA_FLAGS + blk) * 2, m, l, tag);
+    return;
   }
   float *out = part_o(st, rep, HD, kh, blk, h);
 #pragma unroll
@@ -935,7 +952,8 @@ __device__ __noinline__ bool attn_stage(const WarpTeam &tm, const MegaArgs &a, c
   const int kw = rep % MW;  // the warp that prepares the new key and value
   const float *rc = rope_s[st.rope_kind], *rsn = rope_s[st.rope_kind] + HALF;
   // With a block for every item and one more for every query head, no block waits for an
-  // arrival counter: each item publishes a flag, and block items + h merges head h.
+  // arrival counter: each item stores its partials as tagged words, and block items + h
+  // merges head h.
   const bool per_head = items + d.nh <= (int)gridDim.x && nblk <= MEGA_FLAGS;
   for (int it = blockIdx.x; it < items; it += gridDim.x) {
     const int kh = it / nblk, blk = it % nblk;
@@ -1049,17 +1067,14 @@ __device__ __noinline__ bool attn_stage(const WarpTeam &tm, const MegaArgs &a, c
       if (kh == 0 && lane == 0) tags[rr] = (int32_t)p;
     }
     tm.sync();
-    for (int h = cw; h < rep; h += MW) attn_head<HD>(st, d.nk, Ks, Vs, qs[h], tg, P0, lo, p, kh, blk, rep, h);
+    for (int h = cw; h < rep; h += MW)
+      attn_head<HD>(st, d.nk, Ks, Vs, qs[h], tg, P0, lo, p, kh, blk, rep, h, per_head ? a.tpart : nullptr, d.nh, s + 1);
     // the last item of this kv head merges the items and gates
     tm.sync();
     t0 = tr.clk();
     tr.add(s, 9, t0 - t1);
     tr.mark(s, 6);
-    if (per_head) {
-      // the item's partials are stored (the team sync above): publish them to the head merges
-      if (tm.tid() == 0) st_release_gpu(a.aflag + kh * MEGA_FLAGS + blk, s + 1);
-      continue;
-    }
+    if (per_head) continue;  // the head merges poll the item's tagged partials
     if (tm.tid() == 0) {
       const int old = atom_add_acq_rel_gpu(a.actr + kh, 1);
       ctl.last = old == nblk - 1;

@@ -262,7 +262,9 @@ struct MegaArgs {
   float *rope;              // [2][hd] cos | sin of the row's position
   int *sync;                // [1] RoPE entries ready, [2] blocks done; zero at launch
   int *actr;                // [nk] attention item arrivals; zero at launch
-  int *aflag;               // [nk][MEGA_FLAGS] attention items done (stage + 1); zero at launch
+  // item partials of the per-head merges as tagged words (stage + 1): o [nh][MEGA_FLAGS][hd]
+  // (query head h, item i), then (m, l) [nh][MEGA_FLAGS][2]; zero at launch
+  unsigned long long *tpart;
   int *err;
   int32_t *seq_pos;         // advanced by `adv` once every block is done
   float *priv;              // per block: priv_stride floats of rows only that block reads
