@@ -92,14 +92,15 @@ class Clocks:
 
 
 # DRAM bytes (read + write) per algorithmic byte of the persistent decode kernel, from the
-# ncu capture of the reduced 3-pass case (429.7 + 4.1 MB for 427.3 MB of weights and KV);
+# ncu capture of the reduced 3-pass case (429.3 + 5.1 MB for 427.3 MB of weights and KV);
 # the kernel streams every weight once per token, so the ratio carries to the full model.
-MEGA_TRAFFIC_PER_BYTE = (429.7 + 4.1) / 427.3
+MEGA_TRAFFIC_PER_BYTE = (429.3 + 5.1) / 427.3
 
 
 def roofline_decode(st, bytes_step, achieved, hbm, src):
-    """The batch-1 decode step is one launch of the persistent kernel (plus a 784-byte
-    counter reset), so the step's CUDA-event time is that kernel's launch duration."""
+    """The batch-1 decode step is one launch of the persistent kernel, after one memset of
+    its counters and tagged words (652 KB for the 2B shape, about a microsecond), so the
+    step's CUDA-event time is that kernel's launch duration (and a little more)."""
     one = int(st["launches"]) == 1
     return {"bound": "hbm", "kernel": "mega_decode_kernel" if one else "fused decode kernels",
             "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
