@@ -95,7 +95,8 @@ struct Tracer {
   }
   __device__ __forceinline__ void flush(int stage, int n = 6) const {
     if (p)
-      for (int e = 0; e < n; e++) p[((size_t)stage * gridDim.x + blockIdx.x) * MEGA_TRACE_EVENTS + 8 + e] = trace_acc[e];
+      for (int e = 0; e < n; e++)
+        p[((size_t)stage * gridDim.x + blockIdx.x) * MEGA_TRACE_EVENTS + 8 + e] = trace_acc[e];
   }
   __device__ __forceinline__ long long clk() const { return p ? clock64() : 0; }
 };
@@ -172,8 +173,8 @@ struct ChunkWalk {
     for (s = from; s < a.nstages; s++) {
       const MegaStage &st = a.stages[s];
       if (st.kind != MK_GEMV) continue;
-      const int rb = (int)((long)st.N * b / G);
-      re = (int)((long)st.N * (b + 1) / G);
+      const int rb = (int)((unsigned)st.N * (unsigned)b / (unsigned)G);  // N * G < 2^32 (host limit)
+      re = (int)((unsigned)st.N * (unsigned)(b + 1) / (unsigned)G);
       if (rb < re) {
         r0 = rb;
         K = st.K;
@@ -632,7 +633,9 @@ __device__ __noinline__ bool gemv_stage(const WarpTeam &tm, const MegaArgs &a, c
   const Tracer tr{tm.tid() == 0 ? a.trace : nullptr};
   const int G = gridDim.x, b = blockIdx.x;
   const int N = st.N, K = st.K;
-  const int rb = (int)((long)N * b / G), re = (int)((long)N * (b + 1) / G);
+  // 32-bit: N * G < 2^32 (the host's limit on rows per block); a 64-bit division is a subroutine
+  const int rb = (int)((unsigned)N * (unsigned)b / (unsigned)G);
+  const int re = (int)((unsigned)N * (unsigned)(b + 1) / (unsigned)G);
   // the epilogue's per-row scales of this block's rows (re - rb <= EPI_ROWS = team size),
   // held in registers while the input row's loads are in flight, stored to shared memory after
   const int ei = tm.tid();
@@ -866,22 +869,30 @@ __device__ __noinline__ bool merge_head(const WarpTeam &tm, const MegaArgs &a, c
   return true;
 }
 
+// Scores of the two halves of a query head's dimensions (split heads), one row per warp.
+__shared__ float sc_part[MW][32];
+
 // Warp-wide: query head h of kv head kh against the item's 32 keys (lane = key): scores,
-// the item's softmax statistics and its value sum, written as the item's partial.
-template <int HD>
-__device__ __forceinline__ void attn_head(const MegaStage &st, int nk, const float *Ks, const float *Vs, const float *q,
-                                          int tg, long P0, long lo, long p, int kh, int blk, int rep, int h,
-                                          unsigned long long *tp, int nh, uint32_t tag) {
-  constexpr int NV = HD / 32, NC = HD / 4;
+// the item's softmax statistics and its value sum, written as the item's partial. SPLIT = 2:
+// two warps share the head, each takes half of its dimensions (half = 0, 1: warps h and
+// h + rep); they add their partial scores through shared memory (a team sync: every warp of
+// the team is one of the pairs), take the same softmax, and each sums the values of its half.
+template <int HD, int SPLIT>
+__device__ __forceinline__ void attn_head(const WarpTeam &tm, const MegaStage &st, int nk, const float *Ks,
+                                          const float *Vs, const float *q, int tg, long P0, long lo, long p, int kh,
+                                          int blk, int rep, int h, int half, unsigned long long *tp, int nh,
+                                          uint32_t tag) {
+  constexpr int NV = HD / 32 / SPLIT, NC = HD / 4 / SPLIT;  // values a lane sums, float4 chunks scored
   const int lane = threadIdx.x & 31;
+  const int d0 = half * (HD / SPLIT);  // this warp's first dimension
   const float scale = 1.f / sqrtf((float)HD);
   const int j = lane;
   const long pe = P0 + j;
   const bool valid = pe >= lo && pe <= p && (tg == (int32_t)pe || pe == p);
   float s0 = 0.f, s1 = 0.f;
   if (valid) {
-    const float4 *kr = reinterpret_cast<const float4 *>(Ks + j * HD);
-    const float4 *q4 = reinterpret_cast<const float4 *>(q);
+    const float4 *kr = reinterpret_cast<const float4 *>(Ks + j * HD + d0);
+    const float4 *q4 = reinterpret_cast<const float4 *>(q + d0);
 #pragma unroll 8
     for (int c = 0; c < NC; c++) {
       const int cc = (c + j) & (NC - 1);  // rotated: the 32 lanes spread over all banks
@@ -890,7 +901,13 @@ __device__ __forceinline__ void attn_head(const MegaStage &st, int nk, const flo
       s1 = fmaf(qq.z, k.z, fmaf(qq.w, k.w, s1));
     }
   }
-  const float s = valid ? (s0 + s1) * scale : -INFINITY;
+  float sp = s0 + s1;
+  if constexpr (SPLIT == 2) {
+    sc_part[tm.warp()][lane] = sp;
+    tm.sync();
+    sp = sc_part[h][lane] + sc_part[h + rep][lane];  // the same order in both warps
+  }
+  const float s = valid ? sp * scale : -INFINITY;
   const float m = warp_max(s);
   const float e = m == -INFINITY ? 0.f : expf(s - m);
   const float l = warp_sum(e);
@@ -900,7 +917,7 @@ __device__ __forceinline__ void attn_head(const MegaStage &st, int nk, const flo
 #pragma unroll 4
   for (int jj = 0; jj < AK; jj += 2) {
     const float w0 = __shfl_sync(0xffffffffu, e, jj), w1 = __shfl_sync(0xffffffffu, e, jj + 1);
-    const float *v0 = Vs + jj * HD + lane * NV, *v1 = v0 + HD;
+    const float *v0 = Vs + jj * HD + d0 + lane * NV, *v1 = v0 + HD;
 #pragma unroll
     for (int i = 0; i < NV; i++) {
       acc[i] = fmaf(w0, v0[i], acc[i]);
@@ -909,18 +926,21 @@ __device__ __forceinline__ void attn_head(const MegaStage &st, int nk, const flo
   }
   if (tp) {  // the per-head merges poll these words
     const size_t qh = (size_t)kh * rep + h;
-    unsigned long long *to = tp + (qh * MEGA_FLAGS + blk) * HD + lane * NV;
+    unsigned long long *to = tp + (qh * MEGA_FLAGS + blk) * HD + d0 + lane * NV;
     if constexpr (NV == 4)
       st_tagged4(to, make_float4(acc[0] + acc_b[0], acc[1] + acc_b[1], acc[2] + acc_b[2], acc[3] + acc_b[3]), tag);
-    else
+    else if constexpr (NV == 2)
       st_tagged2(to, acc[0] + acc_b[0], acc[1] + acc_b[1], tag);
-    if (lane == 0) st_tagged2(tp + (size_t)nh * MEGA_FLAGS * HD + (qh * MEGA_FLAGS + blk) * 2, m, l, tag);
+    else
+      st_tagged(to, acc[0] + acc_b[0], tag);
+    if (lane == 0 && half == 0)
+      st_tagged2(tp + (size_t)nh * MEGA_FLAGS * HD + (qh * MEGA_FLAGS + blk) * 2, m, l, tag);
     return;
   }
-  float *out = part_o(st, rep, HD, kh, blk, h);
+  float *out = part_o(st, rep, HD, kh, blk, h) + d0;
 #pragma unroll
   for (int i = 0; i < NV; i++) out[lane * NV + i] = acc[i] + acc_b[i];
-  if (lane == 0) *reinterpret_cast<float2 *>(part_ml(st, nk, rep, HD, kh, blk, h)) = make_float2(m, l);
+  if (lane == 0 && half == 0) *reinterpret_cast<float2 *>(part_ml(st, nk, rep, HD, kh, blk, h)) = make_float2(m, l);
 }
 
 // (stages are not inlined: each gets its own register allocation, so the chunk loop does
@@ -958,7 +978,7 @@ __device__ __noinline__ bool attn_stage(const WarpTeam &tm, const MegaArgs &a, c
   for (int it = blockIdx.x; it < items; it += gridDim.x) {
     const int kh = it / nblk, blk = it % nblk;
     const long P0 = (blk0 + blk) * AK;
-    const int rr0 = (int)(P0 % cap);
+    const int rr0 = (int)P0 % cap;  // positions are below 2^31: a 32-bit remainder
     const bool has_p = P0 + AK > p;  // the item that holds the row's own position
     tm.sync();                       // the previous item's tiles and scratch are no longer read
     if (tm.tid() == 0) {
@@ -1050,7 +1070,7 @@ __device__ __noinline__ bool attn_stage(const WarpTeam &tm, const MegaArgs &a, c
     tr.mark(s, 5);
     if (has_p && cw == kw) {
       // into the tile (it holds the ring's older row there), and into the ring
-      const int jp = (int)(p - P0), rr = (int)(p % cap);
+      const int jp = (int)(p - P0), rr = (int)p % cap;
       float *kg = Kg + ((size_t)kh * cap + rr) * HD, *vg = Vg + ((size_t)kh * cap + rr) * HD;
 #pragma unroll
       for (int u = 0; u < PP; u++) {
@@ -1067,8 +1087,13 @@ __device__ __noinline__ bool attn_stage(const WarpTeam &tm, const MegaArgs &a, c
       if (kh == 0 && lane == 0) tags[rr] = (int32_t)p;
     }
     tm.sync();
-    for (int h = cw; h < rep; h += MW)
-      attn_head<HD>(st, d.nk, Ks, Vs, qs[h], tg, P0, lo, p, kh, blk, rep, h, per_head ? a.tpart : nullptr, d.nh, s + 1);
+    unsigned long long *tp = per_head ? a.tpart : nullptr;
+    if (2 * rep == MW)  // two warps a query head, half of its dimensions each
+      attn_head<HD, 2>(tm, st, d.nk, Ks, Vs, qs[cw % rep], tg, P0, lo, p, kh, blk, rep, cw % rep, cw / rep, tp, d.nh,
+                       s + 1);
+    else
+      for (int h = cw; h < rep; h += MW)
+        attn_head<HD, 1>(tm, st, d.nk, Ks, Vs, qs[h], tg, P0, lo, p, kh, blk, rep, h, 0, tp, d.nh, s + 1);
     // the last item of this kv head merges the items and gates
     tm.sync();
     t0 = tr.clk();
