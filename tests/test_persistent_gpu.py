@@ -46,6 +46,22 @@ def test_one_launch_per_token_matches_the_oracle(kv_mode, hd, rec_kinds, context
         P.close()
 
 
+def test_blocks_with_more_row_groups_than_consumer_warps():
+    """More row groups per block than consumer warps, in uneven rounds: ffn 4096 gives 26-27
+    gate/up pairs per block (3 whole rounds and 2-3 pairs more); vocab 5000 gives 32-33 head
+    rows (row pairs, the last one a single row where a block's row count is odd)."""
+    cfg = synth.small(ffn=4096, vocab=5000, kv_mode="last_loop", rec_kinds="S*", full_window=0, loops=2,
+                      max_loops=2, max_context=1024)
+    P = Pair(cfg, 3010)
+    try:
+        launches = _run(P, cfg, 3010, 4)
+        assert launches == [1] * 4, launches
+        assert P.max_hidden_err <= 1e-4, P.max_hidden_err
+        assert all(P.top1)
+    finally:
+        P.close()
+
+
 def test_same_logits_as_the_multi_kernel_path(monkeypatch):
     cfg = synth.small(kv_mode="last_loop", rec_kinds="S*", full_window=0, loops=3, max_context=1024)
     w = synth.weights(cfg, 3002)
