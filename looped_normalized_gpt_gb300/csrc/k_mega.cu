@@ -416,6 +416,10 @@ struct TagWait {
 
 // Chunks tid + 256 j (< nch) of a row of tagged words into v, polled again (the whole set)
 // until every word carries `tag`.
+// A failed poll of a row sleeps this long before the next: while a stage waits (the O
+// projection during an attention stage), up to 150 blocks poll the same few lines of L2.
+constexpr unsigned POLL_SLEEP_NS = 200;
+
 template <int KC>
 __device__ __forceinline__ bool await_row(const unsigned long long *src, uint32_t tag, int tid, int nch,
                                           float4 (&v)[KC], const TagWait &tw) {
@@ -435,6 +439,7 @@ __device__ __forceinline__ bool await_row(const unsigned long long *src, uint32_
       if (tw.trace && tid == 0) tw.trace[1] += i + 1;
       return true;
     }
+    __nanosleep(POLL_SLEEP_NS);
   }
   return false;
 }
