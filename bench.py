@@ -92,9 +92,9 @@ class Clocks:
 
 
 # DRAM bytes (read + write) per algorithmic byte of the persistent decode kernel, from the
-# ncu capture of the reduced 3-pass case (429.3 + 5.1 MB for 427.3 MB of weights and KV);
+# ncu capture of the reduced 3-pass case (429.4 + 4.8 MB for 427.3 MB of weights and KV);
 # the kernel streams every weight once per token, so the ratio carries to the full model.
-MEGA_TRAFFIC_PER_BYTE = (429.3 + 5.1) / 427.3
+MEGA_TRAFFIC_PER_BYTE = (429.4 + 4.8) / 427.3
 
 
 def roofline_decode(st, bytes_step, achieved, hbm, src):
