@@ -46,6 +46,23 @@ def test_one_launch_per_token_matches_the_oracle(kv_mode, hd, rec_kinds, context
         P.close()
 
 
+@pytest.mark.parametrize("nh,nk", [(4, 2), (16, 2)])
+def test_query_groups_other_than_four(nh, nk):
+    """Groups of 2 and of 8 query heads per kv head: the attention stage takes one warp per
+    query head (groups of four take two warps each, half of the head's dimensions apiece)."""
+    cfg = synth.small(nh=nh, nk=nk, hd=64, kv_mode="last_loop", rec_kinds="S*", full_window=0, loops=2,
+                      max_loops=2, max_context=1024)
+    P = Pair(cfg, 3020 + nh)
+    try:
+        launches = _run(P, cfg, 3020 + nh, 4)
+        assert launches == [1] * 4, launches
+        assert P.max_hidden_err <= 1e-4, P.max_hidden_err
+        assert all(P.top1)
+        P.check_rings(0, 1e-5)
+    finally:
+        P.close()
+
+
 def test_blocks_with_more_row_groups_than_consumer_warps():
     """More row groups per block than consumer warps, in uneven rounds: ffn 4096 gives 26-27
     gate/up pairs per block (3 whole rounds and 2-3 pairs more); vocab 5000 gives 32-33 head
