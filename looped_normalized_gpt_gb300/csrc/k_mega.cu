@@ -31,8 +31,9 @@
 //     (q = s_q^2 q^), and in the item that holds the row's own position one warp rotates and
 //     normalises the new key, puts key and value into the tile and writes them (and the
 //     position tag) to the ring; warp h then scores (lane = key), takes the item's softmax and
-//     value sum; one block per query head (or the last item of a kv head) merges the items
-//     and applies the output gate.
+//     value sum (with four query heads a group, warps h and h + 4 share head h, half of its
+//     dimensions each); one block per query head (or the last item of a kv head) merges the
+//     items and applies the output gate.
 // Every wait is bounded. When one runs out the block records error 6, stops at the next
 // team-wide check, lets its copies in flight land and returns; the other blocks then give up
 // waiting for its words. The last block to finish advances the row's position.
